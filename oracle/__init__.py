@@ -1,0 +1,270 @@
+"""fp64 CPU oracle for shared-prefix (cascade) decode attention.
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+CUDA library never imports, links or calls it, and it never imports the CUDA
+library: the two share only the seeded input generator.
+
+The arithmetic lives in ``hp_oracle.c`` (plain loops, double precision,
+OpenMP over output rows); this module marshals numpy / torch CPU arrays into
+it.  Each wrapper names the passage it follows:
+
+* ``sdp``            - SDP(Q,K,V) and LSE(Q,K), Hydragen "Attention
+                       Decomposition Across Subsequences" (the LSE definition).
+* ``merge``          - two-part exact merge, Hydragen Eq. 5 with the
+                       max-subtracted combine_lse step.
+* ``partial_attn`` / ``attn_reduce`` - ChunkAttention Eq. 1 and Eq. 2.
+* ``cascade``        - attention of each sequence over the concatenation of
+                       its tree nodes' keys (Hydragen "Hierarchical Sharing";
+                       ChunkAttention prefix tree), i.e. the unsplit definition.
+* ``paged_decode``   - per-sequence attention through a page table.
+* ``prefix``         - attention of a batch of queries against one contiguous
+                       prefix laid out [len][Hkv][d].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hp_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "libhp_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C, -O2, OpenMP)."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.hpo_sdp_f64.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp, _dp, _dp,
+                                        ctypes.c_double, _dp, _dp]
+            lib.hpo_merge.argtypes = [ctypes.c_long, ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _dp]
+            lib.hpo_partial_attn.argtypes = [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp,
+                                             ctypes.c_double, _dp, _dp, _dp]
+            lib.hpo_attn_reduce.argtypes = [ctypes.c_int, _dp, ctypes.c_double, ctypes.c_double,
+                                            _dp, _dp, _dp]
+            lib.hpo_cascade.argtypes = [ctypes.c_int] * 4 + [ctypes.c_double, _u16p, ctypes.c_int,
+                                        ctypes.POINTER(_u16p), ctypes.POINTER(_u16p), _i32p, _i32p,
+                                        ctypes.POINTER(_i32p), ctypes.POINTER(_i32p),
+                                        ctypes.c_long, _i32p, _dp, _dp]
+            lib.hpo_cascade.restype = ctypes.c_int
+            lib.hpo_paged_decode.argtypes = [ctypes.c_int] * 4 + [
+                ctypes.c_double, _u16p, ctypes.c_long, ctypes.c_long, _u16p, _u16p, ctypes.c_int,
+                _i32p, ctypes.c_int, _i32p, _dp, _dp]
+            lib.hpo_paged_decode.restype = ctypes.c_int
+            lib.hpo_prefix.argtypes = [ctypes.c_int] * 4 + [
+                ctypes.c_double, _u16p, ctypes.c_long, ctypes.c_long, _u16p, _u16p, ctypes.c_long,
+                ctypes.c_long, ctypes.c_int, _dp, _dp]
+            lib.hpo_prefix.restype = ctypes.c_int
+            lib.hpo_num_threads.restype = ctypes.c_int
+            lib.hpo_set_num_threads.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return int(_load().hpo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().hpo_set_num_threads(int(n))
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray, typ):
+    return a.ctypes.data_as(typ)
+
+
+def _bf16_bits(t) -> np.ndarray:
+    """Raw bf16 bits of a CPU torch bf16 tensor as a contiguous uint16 array."""
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16:
+        raise TypeError("expected a torch.bfloat16 tensor")
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def sdp(Q, K, V, scale: float):
+    """Q [nq,d], K/V [nk,d] (fp64) -> (O [nq,d], lse [nq])."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    nq, d = Q.shape
+    nk = K.shape[0]
+    O = np.zeros((nq, d))
+    L = np.zeros(nq)
+    _load().hpo_sdp_f64(nq, nk, d, _ptr(Q, _dp), _ptr(K, _dp), _ptr(V, _dp), float(scale),
+                        _ptr(O, _dp), _ptr(L, _dp))
+    return O, L
+
+
+def merge(O1, L1, O2, L2):
+    """Exact two-part merge of (O, LSE) states; rows x d."""
+    O1, L1, O2, L2 = _f64(O1), _f64(L1), _f64(O2), _f64(L2)
+    n, d = O1.shape
+    O = np.zeros((n, d))
+    L = np.zeros(n)
+    _load().hpo_merge(n, d, _ptr(O1, _dp), _ptr(L1, _dp), _ptr(O2, _dp), _ptr(L2, _dp),
+                      _ptr(O, _dp), _ptr(L, _dp))
+    return O, L
+
+
+def partial_attn(q, Kc, Vc, scale: float):
+    """ChunkAttention Eq. 1 for one query row: returns (o, m, n)."""
+    q, Kc, Vc = _f64(q), _f64(Kc), _f64(Vc)
+    d = q.shape[0]
+    c = Kc.shape[0]
+    o = np.zeros(d)
+    m = ctypes.c_double()
+    n = ctypes.c_double()
+    _load().hpo_partial_attn(d, c, _ptr(q, _dp), _ptr(Kc, _dp), _ptr(Vc, _dp), float(scale),
+                             _ptr(o, _dp), ctypes.byref(m), ctypes.byref(n))
+    return o, m.value, n.value
+
+
+def attn_reduce(o_c, m_c: float, n_c: float, state):
+    """ChunkAttention Eq. 2: fold chunk state into ``state = [O, m, n]`` (in place)."""
+    O, m, n = state
+    O = _f64(O).copy()
+    o_c = _f64(o_c)
+    mm = ctypes.c_double(m)
+    nn = ctypes.c_double(n)
+    _load().hpo_attn_reduce(O.shape[0], _ptr(o_c, _dp), float(m_c), float(n_c), _ptr(O, _dp),
+                            ctypes.byref(mm), ctypes.byref(nn))
+    state[0], state[1], state[2] = O, mm.value, nn.value
+    return state
+
+
+def cascade(wl, rows: Optional[Sequence[Sequence[int]]] = None):
+    """Attention of rows (b, h) of a ``CascadeWorkload`` over each sequence's
+    concatenated tree keys.  Default: every row.  Returns (O [n,d], lse [n])."""
+    lib = _load()
+    if rows is None:
+        rows = [(b, h) for b in range(wl.B) for h in range(wl.Hq)]
+    rows_np = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+    n = rows_np.shape[0]
+    q = _bf16_bits(wl.q)
+    kp = _bf16_bits(wl.k_pool)
+    vp = _bf16_bits(wl.v_pool)
+    nl = len(wl.levels)
+    keep = []
+    k_arr = (_u16p * max(nl, 1))()
+    v_arr = (_u16p * max(nl, 1))()
+    nodes_arr = (_i32p * max(nl, 1))()
+    ids_arr = (_i32p * max(nl, 1))()
+    ps_arr = np.full(max(nl, 1), wl.page_size, dtype=np.int32)
+    nn_arr = np.zeros(max(nl, 1), dtype=np.int32)
+    for i, lv in enumerate(wl.levels):
+        nodes = np.ascontiguousarray(lv.nodes.cpu().numpy().astype(np.int32))
+        ids = np.ascontiguousarray(lv.page_ids.cpu().numpy().astype(np.int32))
+        if ids.size == 0:
+            ids = np.zeros(1, dtype=np.int32)
+        keep += [nodes, ids]
+        k_arr[i] = _ptr(kp, _u16p)
+        v_arr[i] = _ptr(vp, _u16p)
+        nodes_arr[i] = _ptr(nodes, _i32p)
+        ids_arr[i] = _ptr(ids, _i32p)
+        nn_arr[i] = nodes.shape[0]
+    O = np.zeros((n, wl.d))
+    L = np.zeros(n)
+    rc = lib.hpo_cascade(wl.B, wl.Hq, wl.Hkv, wl.d, float(wl.scale), _ptr(q, _u16p), nl, k_arr,
+                         v_arr, _ptr(ps_arr, _i32p), _ptr(nn_arr, _i32p), nodes_arr, ids_arr, n,
+                         _ptr(rows_np, _i32p), _ptr(O, _dp), _ptr(L, _dp))
+    if rc != 0:
+        raise ValueError(f"hpo_cascade rejected its arguments ({rc})")
+    return O, L
+
+
+def paged_decode(q, k_pool, v_pool, page_table, seq_lens, scale: float):
+    """q [B,Hq,d] bf16; pools [P,Hkv,ps,d] bf16; page_table [B,W] int32;
+    seq_lens [B] int32 -> (O [B,Hq,d], lse [B,Hq])."""
+    lib = _load()
+    B, Hq, d = q.shape
+    _, Hkv, ps, _ = k_pool.shape
+    qb = _bf16_bits(q)
+    kp, vp = _bf16_bits(k_pool), _bf16_bits(v_pool)
+    pt = np.ascontiguousarray(np.asarray(page_table, dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    O = np.zeros((B, Hq, d))
+    L = np.zeros((B, Hq))
+    rc = lib.hpo_paged_decode(B, Hq, Hkv, d, float(scale), _ptr(qb, _u16p), Hq * d, d,
+                              _ptr(kp, _u16p), _ptr(vp, _u16p), ps, _ptr(pt, _i32p),
+                              pt.shape[1], _ptr(sl, _i32p), _ptr(O, _dp), _ptr(L, _dp))
+    if rc != 0:
+        raise ValueError("hpo_paged_decode rejected its arguments")
+    return O, L
+
+
+def prefix(q, k, v, scale: float):
+    """q [nb,Hq,d] bf16; k/v [len,Hkv,d] bf16 -> (O [nb,Hq,d], lse [nb,Hq])."""
+    lib = _load()
+    nb, Hq, d = q.shape
+    ln, Hkv, _ = k.shape
+    qb = _bf16_bits(q)
+    kb, vb = _bf16_bits(k), _bf16_bits(v)
+    O = np.zeros((nb, Hq, d))
+    L = np.zeros((nb, Hq))
+    rc = lib.hpo_prefix(nb, Hq, Hkv, d, float(scale), _ptr(qb, _u16p), Hq * d, d,
+                        _ptr(kb, _u16p), _ptr(vb, _u16p), Hkv * d, d, ln, _ptr(O, _dp),
+                        _ptr(L, _dp))
+    if rc != 0:
+        raise ValueError("hpo_prefix rejected its arguments")
+    return O, L
+
+
+class use_library:
+    """Context manager that routes the wrappers through another compiled copy of
+    the oracle (used by the tests that plant a mistake in the oracle source and
+    check that the pins catch it)."""
+
+    def __init__(self, so_path: str):
+        self.so_path = so_path
+        self._saved = None
+
+    def __enter__(self):
+        global _lib
+        base = _load()
+        lib = ctypes.CDLL(self.so_path)
+        for name in ("hpo_sdp_f64", "hpo_merge", "hpo_partial_attn", "hpo_attn_reduce",
+                     "hpo_cascade", "hpo_paged_decode", "hpo_prefix", "hpo_num_threads",
+                     "hpo_set_num_threads"):
+            f, g = getattr(lib, name), getattr(base, name)
+            f.argtypes = g.argtypes
+            f.restype = g.restype
+        with _lock:
+            self._saved = _lib
+            _lib = lib
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self._saved
+        return False
+
+
+def source_path() -> str:
+    return _SRC

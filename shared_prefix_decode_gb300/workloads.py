@@ -1,0 +1,325 @@
+"""Seeded synthetic inputs for shared-prefix (cascade) decode attention.
+
+This module only builds inputs: query tensors, paged KV pools, page tables and
+the per-level prefix-tree descriptor.  It holds none of the attention
+arithmetic, so both the CUDA path and the fp64 oracle consume exactly the same
+tensors.
+
+Storage model (Hydragen, "Hierarchical Sharing"; ChunkAttention, "Prefix-Aware
+KV Cache (PAKV): The Prefix Tree Structure"):
+
+* all KV lives in one page pool per workload, laid out ``[page][Hkv][ps][d]``
+  (bf16).  A shared prefix is the same physical pages for every sequence that
+  shares it.
+* the tree is given level by level.  A level is a list of nodes
+  ``(seq_begin, seq_end, kv_len, page_off)``: the node's ``kv_len`` tokens are
+  visible to the contiguous sequence range ``[seq_begin, seq_end)`` and sit in
+  pages ``page_ids[page_off : page_off + ceil(kv_len / ps)]``.
+* a private suffix is a level whose nodes cover one sequence each.
+* sequence ``b`` sees, in order, the tokens of the node that covers it at each
+  level.  A level may leave a sequence uncovered (it then contributes nothing).
+
+Random draws (seeded ``torch.Generator``): lengths with ``torch.randint``
+(inclusive ranges), the physical page permutation with ``torch.randperm``, then
+q, K, V as N(0,1) fp32 rounded to bf16.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+__all__ = [
+    "TreeLevel",
+    "CascadeWorkload",
+    "build_cascade",
+    "make_config",
+    "CONFIG_NAMES",
+    "full_page_tables",
+    "apply_probe",
+]
+
+
+@dataclass
+class TreeLevel:
+    """One level of the prefix tree.
+
+    ``nodes`` is an int32 tensor ``[n, 4]`` of ``(seq_begin, seq_end, kv_len,
+    page_off)``; ``page_ids`` an int32 tensor of physical page ids.
+    """
+
+    nodes: torch.Tensor
+    page_ids: torch.Tensor
+
+    @property
+    def num_nodes(self) -> int:
+        return int(self.nodes.shape[0])
+
+
+@dataclass
+class CascadeWorkload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    page_size: int
+    scale: float
+    q: torch.Tensor  # [B, Hq, d] bf16
+    k_pool: torch.Tensor  # [num_pages, Hkv, ps, d] bf16
+    v_pool: torch.Tensor
+    levels: List[TreeLevel] = field(default_factory=list)
+    seed: int = 0
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_pool.shape[0])
+
+    def seq_kv_len(self) -> List[int]:
+        """Total number of keys each sequence attends over."""
+        out = [0] * self.B
+        for lv in self.levels:
+            for sb, se, kl, _ in lv.nodes.tolist():
+                for b in range(sb, se):
+                    out[b] += kl
+        return out
+
+    def unique_kv_tokens(self) -> int:
+        """Stored tokens: each node's tokens once, however many sequences share them."""
+        return sum(int(lv.nodes[:, 2].sum()) for lv in self.levels)
+
+    def unique_kv_bytes(self) -> int:
+        return self.unique_kv_tokens() * self.Hkv * self.d * 2 * 2
+
+    def shared_flops(self) -> int:
+        """4 * rows * keys * d over nodes that cover more than one sequence
+        (the batched matrix-matrix part)."""
+        tot = 0
+        for lv in self.levels:
+            for sb, se, kl, _ in lv.nodes.tolist():
+                if se - sb > 1:
+                    tot += 4 * (se - sb) * self.Hq * kl * self.d
+        return tot
+
+    def to(self, device) -> "CascadeWorkload":
+        lv = [TreeLevel(l.nodes.clone(), l.page_ids.to(device)) for l in self.levels]
+        return CascadeWorkload(self.name, self.B, self.Hq, self.Hkv, self.d, self.page_size,
+                               self.scale, self.q.to(device), self.k_pool.to(device),
+                               self.v_pool.to(device), lv, self.seed)
+
+
+def build_cascade(
+    name: str,
+    *,
+    B: int,
+    Hq: int,
+    Hkv: int,
+    d: int,
+    page_size: int,
+    shared: Sequence[Sequence[Tuple[int, int, int]]],
+    suffix_lens: Optional[Sequence[int]] = None,
+    suffix_range: Optional[Tuple[int, int]] = None,
+    seed: int = 0,
+    scale: Optional[float] = None,
+    shuffle: bool = True,
+    extra_suffix_range: Optional[Tuple[int, int]] = None,
+) -> CascadeWorkload:
+    """Build a workload.
+
+    ``shared`` lists the shared levels, each a list of ``(seq_begin, seq_end,
+    kv_len)`` nodes.  Private suffix lengths are either given or drawn from
+    ``suffix_range`` (inclusive); ``extra_suffix_range`` adds a second drawn
+    length to each suffix (question + answer-so-far).
+    """
+    g = torch.Generator().manual_seed(seed)
+    if suffix_lens is None:
+        lo, hi = suffix_range if suffix_range is not None else (0, 0)
+        suffix_lens = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+        if extra_suffix_range is not None:
+            lo2, hi2 = extra_suffix_range
+            extra = torch.randint(lo2, hi2 + 1, (B,), generator=g).tolist()
+            suffix_lens = [a + b for a, b in zip(suffix_lens, extra)]
+    suffix_lens = [int(x) for x in suffix_lens]
+    assert len(suffix_lens) == B
+
+    ps = page_size
+    # logical page allocation, in tree order: shared levels, then suffixes
+    level_specs = [list(lv) for lv in shared] + [[(b, b + 1, suffix_lens[b]) for b in range(B)]]
+    n_logical = 0
+    level_nodes = []
+    for spec in level_specs:
+        rows = []
+        for sb, se, kl in spec:
+            npg = (kl + ps - 1) // ps
+            rows.append((sb, se, kl, n_logical, npg))
+            n_logical += npg
+        level_nodes.append(rows)
+    n_pages = max(n_logical, 1)
+    perm = torch.randperm(n_pages, generator=g) if shuffle else torch.arange(n_pages)
+
+    q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16)
+    k_pool = torch.randn(n_pages, Hkv, ps, d, generator=g).to(torch.bfloat16)
+    v_pool = torch.randn(n_pages, Hkv, ps, d, generator=g).to(torch.bfloat16)
+
+    levels = []
+    for rows in level_nodes:
+        ids = []
+        nodes = []
+        for sb, se, kl, first, npg in rows:
+            nodes.append((sb, se, kl, len(ids)))
+            ids.extend(perm[first:first + npg].tolist())
+        levels.append(TreeLevel(torch.tensor(nodes, dtype=torch.int32).reshape(-1, 4),
+                                torch.tensor(ids, dtype=torch.int32)))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return CascadeWorkload(name, B, Hq, Hkv, d, ps, float(scale), q, k_pool, v_pool, levels, seed)
+
+
+# Named workloads.  Shapes follow the attention shapes of the models the pages
+# use (Llama-3-8B, CodeLlama-13b, Llama-2-7B, CodeLlama-7B); weights are never
+# needed because attention cost depends only on shapes and lengths.
+CONFIG_NAMES = ("tiny", "llama3_8b", "codellama13b", "tree2", "doc_streams", "no_sharing")
+
+
+def make_config(name: str, seed: int = 0, B: Optional[int] = None, prefix: Optional[int] = None,
+                shuffle: bool = True) -> CascadeWorkload:
+    """Named workloads; ``B``/``prefix`` override the batch and the first-level
+    prefix length to make smaller variants of the same structure."""
+    if name == "tiny":
+        B_ = B or 4
+        P = 256 if prefix is None else prefix
+        return build_cascade(name, B=B_, Hq=4, Hkv=1, d=64, page_size=16,
+                             shared=[[(0, B_, P)]] if P > 0 else [],
+                             suffix_range=(0, 32), seed=seed, scale=1.0 / math.sqrt(64),
+                             shuffle=shuffle)
+    if name == "llama3_8b":
+        B_ = B or 64
+        P = 4096 if prefix is None else prefix
+        return build_cascade(name, B=B_, Hq=32, Hkv=8, d=128, page_size=16,
+                             shared=[[(0, B_, P)]] if P > 0 else [],
+                             suffix_range=(1, 256), seed=seed, shuffle=shuffle)
+    if name == "codellama13b":
+        B_ = B or 256
+        P = 16384 if prefix is None else prefix
+        return build_cascade(name, B=B_, Hq=40, Hkv=40, d=128, page_size=16,
+                             shared=[[(0, B_, P)]] if P > 0 else [],
+                             suffix_range=(1, 512), seed=seed, shuffle=shuffle)
+    if name == "tree2":
+        # global prefix shared by all sequences, then 8 contiguous subgroups
+        # sharing a second-level prefix, then private suffixes; 64-token chunks
+        B_ = B or 128
+        P = 2048 if prefix is None else prefix
+        groups = 8
+        per = B_ // groups
+        P2 = 1024 if prefix is None else max(prefix // 2, 64)
+        lvl2 = [(gi * per, (gi + 1) * per, P2) for gi in range(groups)]
+        return build_cascade(name, B=B_, Hq=32, Hkv=32, d=128, page_size=64,
+                             shared=[[(0, B_, P)], lvl2], suffix_range=(64, 256),
+                             seed=seed, shuffle=shuffle)
+    if name == "doc_streams":
+        # one document shared by all streams; each stream's private segment is
+        # its question (32..64 tokens) plus its answer so far (0..256 tokens)
+        B_ = B or 256
+        P = 16384 if prefix is None else prefix
+        return build_cascade(name, B=B_, Hq=32, Hkv=32, d=128, page_size=16,
+                             shared=[[(0, B_, P)]] if P > 0 else [],
+                             suffix_range=(32, 64), extra_suffix_range=(0, 256),
+                             seed=seed, shuffle=shuffle)
+    if name == "no_sharing":
+        B_ = B or 64
+        L = 2048 if prefix is None else prefix
+        return build_cascade(name, B=B_, Hq=32, Hkv=32, d=128, page_size=16, shared=[],
+                             suffix_lens=[L] * B_, seed=seed, shuffle=shuffle)
+    raise ValueError(f"unknown config {name!r}; known: {CONFIG_NAMES}")
+
+
+def full_page_tables(wl: CascadeWorkload) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-sequence page table over the whole concatenated context (shared
+    pages aliased into every sequence that sees them), for per-sequence paged
+    decode.  Requires every level but the last to hold whole pages.
+
+    Returns ``(page_table [B, max_pages] int32, seq_lens [B] int32)``.
+    """
+    ps = wl.page_size
+    per_seq: List[List[int]] = [[] for _ in range(wl.B)]
+    lens = [0] * wl.B
+    for li, lv in enumerate(wl.levels):
+        ids = lv.page_ids.tolist()
+        for sb, se, kl, off in lv.nodes.tolist():
+            npg = (kl + ps - 1) // ps
+            for b in range(sb, se):
+                if lens[b] % ps != 0:
+                    raise ValueError("a non-final level holds a partial page")
+                per_seq[b].extend(ids[off:off + npg])
+                lens[b] += kl
+    width = max(1, max(len(p) for p in per_seq))
+    pt = torch.zeros(wl.B, width, dtype=torch.int32)
+    for b, p in enumerate(per_seq):
+        if p:
+            pt[b, :len(p)] = torch.tensor(p, dtype=torch.int32)
+    return pt, torch.tensor(lens, dtype=torch.int32)
+
+
+def _probe_code(b: int, d: int) -> torch.Tensor:
+    """A bf16-exact value row unique to sequence ``b`` (and to each column)."""
+    i = torch.arange(d)
+    return (((b * 131 + i * 7) % 256) - 128).to(torch.float32) / 16.0
+
+
+def apply_probe(wl: CascadeWorkload, targets: Sequence[int], alpha: float = 64.0,
+                beta: float = 64.0) -> CascadeWorkload:
+    """Turn a workload into an indexing probe (in place; returns it).
+
+    Sequence ``b`` gets the query ``alpha * s_b * e_{j_b}`` for every head (a
+    signed basis direction distinct per sequence, so one sequence's target key
+    scores ~0 or very negative for every other sequence), and the key at
+    logical position ``targets[b]`` of its concatenated context becomes
+    ``beta * s_b * e_{j_b}`` for every KV head, with the value row set to a code
+    unique to ``b``.  All other scores sit far below the target's, so the exact
+    softmax output of row ``(b, h)`` is the code row itself.
+    """
+    d = wl.d
+    if wl.B > 2 * d:
+        raise ValueError("probe needs B <= 2*d distinct signed directions")
+    ps = wl.page_size
+    q = torch.zeros(wl.B, wl.Hq, d, dtype=torch.float32)
+    locs = []
+    for b in range(wl.B):
+        j, sgn = b % d, (1.0 if b < d else -1.0)
+        q[b, :, j] = alpha * sgn
+        # walk b's levels to find the physical slot of logical token targets[b]
+        t = int(targets[b])
+        loc = None
+        for lv in wl.levels:
+            ids = lv.page_ids.tolist()
+            for sb, se, kl, off in lv.nodes.tolist():
+                if sb <= b < se:
+                    if t < kl:
+                        loc = (ids[off + t // ps], t % ps)
+                    t -= kl
+                    break
+            if loc is not None:
+                break
+        if loc is None:
+            raise ValueError(f"target {targets[b]} beyond sequence {b}'s context")
+        locs.append((b, j, sgn, loc))
+    slots = [loc for _, _, _, loc in locs]
+    if len(set(slots)) != len(slots):
+        raise ValueError("two probe targets share one physical slot")
+    wl.q = q.to(torch.bfloat16)
+    for b, j, sgn, (page, slot) in locs:
+        krow = torch.zeros(d)
+        krow[j] = beta * sgn
+        wl.k_pool[page, :, slot, :] = krow.to(torch.bfloat16)
+        wl.v_pool[page, :, slot, :] = _probe_code(b, d).to(torch.bfloat16)
+    return wl
+
+
+def probe_expected(b: int, d: int) -> torch.Tensor:
+    return _probe_code(b, d).to(torch.bfloat16)

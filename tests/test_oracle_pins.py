@@ -1,0 +1,387 @@
+"""Pins for the fp64 oracle: each test checks the oracle against something
+other than itself (a closed form, a printed worked example, an invariant, or
+an independently written brute force)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from shared_prefix_decode_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16(x):
+    return torch.tensor(np.asarray(x), dtype=torch.float32).to(torch.bfloat16).double().numpy()
+
+
+# ---------------------------------------------------------------- closed forms
+def test_single_key_returns_its_value():
+    """One key: softmax weight 1, so O = v exactly and LSE = the scaled score."""
+    rng = np.random.default_rng(1)
+    d = 64
+    q, k, v = rng.standard_normal((1, d)), rng.standard_normal((1, d)), rng.standard_normal((1, d))
+    scale = 0.37
+    O, L = oracle.sdp(q, k, v, scale)
+    assert np.array_equal(O[0], v[0])
+    assert L[0] == pytest.approx(scale * float(q[0] @ k[0]), abs=1e-13)
+
+
+def test_identical_keys_give_mean_value():
+    """n identical keys: equal weights, O = mean(V), LSE = s + ln n."""
+    rng = np.random.default_rng(2)
+    d, n = 32, 37
+    q = rng.standard_normal((3, d))
+    k = np.repeat(rng.standard_normal((1, d)), n, axis=0)
+    v = rng.standard_normal((n, d))
+    O, L = oracle.sdp(q, k, v, 0.25)
+    for r in range(3):
+        np.testing.assert_allclose(O[r], v.mean(axis=0), atol=1e-13)
+        assert L[r] == pytest.approx(0.25 * float(q[r] @ k[0]) + math.log(n), abs=1e-12)
+
+
+def test_scores_use_scale_and_natural_log():
+    """Two keys with scores a, b: LSE = ln(e^a + e^b), weights e^a/(e^a+e^b)."""
+    d = 4
+    q = np.array([[1.0, 0, 0, 0]])
+    k = np.array([[2.0, 0, 0, 0], [-1.0, 0, 0, 0]])
+    v = np.array([[1.0, 0, 0, 0], [0, 1.0, 0, 0]])
+    scale = 0.5
+    O, L = oracle.sdp(q, k, v, scale)
+    a, b = 1.0, -0.5
+    assert L[0] == pytest.approx(math.log(math.exp(a) + math.exp(b)), abs=1e-14)
+    wa = math.exp(a) / (math.exp(a) + math.exp(b))
+    np.testing.assert_allclose(O[0], [wa, 1 - wa, 0, 0], atol=1e-15)
+
+
+def test_empty_key_set_is_zero_and_minus_inf():
+    O, L = oracle.sdp(np.ones((2, 8)), np.zeros((0, 8)), np.zeros((0, 8)), 1.0)
+    assert np.all(O == 0) and np.all(L == -np.inf)
+
+
+def test_merge_with_empty_part_is_identity_and_both_empty_is_empty():
+    rng = np.random.default_rng(3)
+    O1 = rng.standard_normal((4, 16))
+    L1 = rng.standard_normal(4)
+    O, L = oracle.merge(O1, L1, np.zeros((4, 16)), np.full(4, -np.inf))
+    np.testing.assert_array_equal(O, O1)
+    np.testing.assert_array_equal(L, L1)
+    O, L = oracle.merge(np.zeros((2, 16)), np.full(2, -np.inf), np.zeros((2, 16)),
+                        np.full(2, -np.inf))
+    assert np.all(O == 0) and np.all(L == -np.inf) and not np.any(np.isnan(O))
+
+
+# ------------------------------------------------------------- invariants
+def test_key_permutation_invariance():
+    rng = np.random.default_rng(4)
+    d, n = 48, 300
+    q, K, V = rng.standard_normal((5, d)), rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    O, L = oracle.sdp(q, K, V, 0.2)
+    p = rng.permutation(n)
+    O2, L2 = oracle.sdp(q, K[p], V[p], 0.2)
+    np.testing.assert_allclose(O2, O, atol=1e-12)
+    np.testing.assert_allclose(L2, L, atol=1e-12)
+
+
+def test_merge_identity_on_random_splits():
+    """Hydragen Eq. 5: merging the (O, LSE) of two disjoint key parts equals
+    attention over their concatenation."""
+    rng = np.random.default_rng(5)
+    d, n = 64, 500
+    q, K, V = rng.standard_normal((7, d)), rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    q *= 3.0  # peaked softmax
+    O, L = oracle.sdp(q, K, V, 1 / 8)
+    for cut in (1, 17, 250, 499):
+        mask = np.zeros(n, bool)
+        mask[rng.permutation(n)[:cut]] = True
+        Oa, La = oracle.sdp(q, K[mask], V[mask], 1 / 8)
+        Ob, Lb = oracle.sdp(q, K[~mask], V[~mask], 1 / 8)
+        Om, Lm = oracle.merge(Oa, La, Ob, Lb)
+        np.testing.assert_allclose(Om, O, atol=1e-12)
+        np.testing.assert_allclose(Lm, L, atol=1e-12)
+
+
+def test_chunk_partial_states_reduce_to_full_attention():
+    """ChunkAttention Eq. 1 + Eq. 2: partial (o, m, n) per chunk, reduced in an
+    arbitrary order, then O / n equals softmax attention; m + ln n equals LSE."""
+    rng = np.random.default_rng(6)
+    d, n, c = 32, 333, 64
+    q, K, V = rng.standard_normal(d), rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    O, L = oracle.sdp(q[None], K, V, 0.3)
+    chunks = [(s, min(s + c, n)) for s in range(0, n, c)]
+    order = rng.permutation(len(chunks))
+    state = [np.zeros(d), -math.inf, 0.0]
+    for i in order:
+        s, e = chunks[i]
+        o_c, m_c, n_c = oracle.partial_attn(q, K[s:e], V[s:e], 0.3)
+        oracle.attn_reduce(o_c, m_c, n_c, state)
+    np.testing.assert_allclose(state[0] / state[2], O[0], atol=1e-12)
+    assert state[1] + math.log(state[2]) == pytest.approx(L[0], abs=1e-12)
+
+
+# -------------------------------------------- printed worked example (blog)
+def test_blog_split_merge_example():
+    """The shared-prefix KV caching blog's float64 check: prefix pass + per
+    sequence suffix pass, merged, vs single pass; printed max error 3.05e-16."""
+    g = json.load(open(os.path.join(GOLDEN, "blog_split_merge_check.json")))
+    d, P, B, S = g["d"], g["P"], g["B"], g["S"]
+    rng = np.random.default_rng(0)
+    Kp, Vp = rng.standard_normal((P, d)), rng.standard_normal((P, d))
+    Ks, Vs = rng.standard_normal((B, S, d)), rng.standard_normal((B, S, d))
+    Q = rng.standard_normal((B, d))
+    scale = 1 / math.sqrt(d)
+    O1, L1 = oracle.sdp(Q, Kp, Vp, scale)
+    O2, L2 = np.zeros((B, d)), np.zeros(B)
+    for b in range(B):
+        o, l = oracle.sdp(Q[b:b + 1], Ks[b], Vs[b], scale)
+        O2[b], L2[b] = o[0], l[0]
+    Om, _ = oracle.merge(O1, L1, O2, L2)
+    ref = np.stack([oracle.sdp(Q[b:b + 1], np.vstack([Kp, Ks[b]]), np.vstack([Vp, Vs[b]]),
+                               scale)[0][0] for b in range(B)])
+    err = np.abs(Om - ref).max()
+    assert err <= g["bound_used"], err
+    assert err < 100 * g["printed_max_abs_error"]
+
+
+# ------------------------------------------ brute force (independent numpy)
+def _np_attention(q, K, V, scale):
+    """Second, independent fp64 softmax attention (numpy / scipy)."""
+    from scipy.special import logsumexp, softmax
+    s = scale * (K @ q)
+    return softmax(s) @ V, logsumexp(s)
+
+
+def _np_cascade(wl):
+    """Brute-force cascade: gather each sequence's keys with numpy fancy
+    indexing from the page lists, then the numpy softmax above."""
+    kp = wl.k_pool.double().numpy()
+    vp = wl.v_pool.double().numpy()
+    q = wl.q.double().numpy()
+    ps = wl.page_size
+    G = wl.Hq // wl.Hkv
+    O = np.zeros((wl.B, wl.Hq, wl.d))
+    L = np.zeros((wl.B, wl.Hq))
+    for b in range(wl.B):
+        pages, slots = [], []
+        for lv in wl.levels:
+            nodes = lv.nodes.numpy()
+            ids = lv.page_ids.numpy()
+            hit = np.nonzero((nodes[:, 0] <= b) & (b < nodes[:, 1]))[0]
+            assert len(hit) <= 1
+            if len(hit) == 0:
+                continue
+            _, _, kl, off = nodes[hit[0]]
+            t = np.arange(kl)
+            pages.append(ids[off + t // ps])
+            slots.append(t % ps)
+        pages = np.concatenate(pages) if pages else np.zeros(0, int)
+        slots = np.concatenate(slots) if slots else np.zeros(0, int)
+        for h in range(wl.Hq):
+            K = kp[pages, h // G, slots, :]
+            V = vp[pages, h // G, slots, :]
+            if len(pages) == 0:
+                O[b, h], L[b, h] = 0.0, -np.inf
+            else:
+                O[b, h], L[b, h] = _np_attention(q[b, h], K, V, wl.scale)
+    return O, L
+
+
+def test_sdp_matches_brute_force_tiny():
+    rng = np.random.default_rng(7)
+    for nk in (1, 2, 5, 64):
+        q, K, V = rng.standard_normal((3, 16)), rng.standard_normal((nk, 16)), rng.standard_normal((nk, 16))
+        O, L = oracle.sdp(q, K, V, 0.7)
+        for r in range(3):
+            o, l = _np_attention(q[r], K, V, 0.7)
+            np.testing.assert_allclose(O[r], o, atol=1e-12)
+            assert L[r] == pytest.approx(l, abs=1e-12)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_cascade_matches_brute_force_tiny_trees(seed):
+    """Tiny trees (B<=4, <=64 keys per sequence) with GQA, shuffled pages,
+    two shared levels and ragged suffixes including empty ones."""
+    wl = W.build_cascade("t", B=4, Hq=4, Hkv=2, d=16, page_size=4,
+                         shared=[[(0, 4, 12)], [(0, 2, 8), (2, 4, 5)]],
+                         suffix_range=(0, 9), seed=seed)
+    O, L = oracle.cascade(wl)
+    Ob, Lb = _np_cascade(wl)
+    np.testing.assert_allclose(O.reshape(Ob.shape), Ob, atol=1e-12)
+    np.testing.assert_allclose(L.reshape(Lb.shape), Lb, atol=1e-12)
+
+
+def test_cascade_config_tiny_matches_brute_force():
+    wl = W.make_config("tiny", seed=3)
+    O, L = oracle.cascade(wl)
+    Ob, Lb = _np_cascade(wl)
+    np.testing.assert_allclose(O.reshape(Ob.shape), Ob, atol=1e-12)
+    np.testing.assert_allclose(L.reshape(Lb.shape), Lb, atol=1e-12)
+
+
+def test_zero_query_counts_visible_keys():
+    """q = 0: every key has score 0, so LSE = ln(#visible keys) and O = their
+    mean -- pins the number of keys each sequence sees (catches length
+    off-by-ones in the tree walk)."""
+    wl = W.build_cascade("z", B=5, Hq=2, Hkv=1, d=8, page_size=4,
+                         shared=[[(0, 5, 7)], [(1, 3, 6)]], suffix_lens=[0, 3, 4, 1, 9], seed=1)
+    wl.q.zero_()
+    O, L = oracle.cascade(wl)
+    n_vis = wl.seq_kv_len()
+    assert n_vis == [7, 16, 17, 8, 16]
+    for r, (b, h) in enumerate([(b, h) for b in range(5) for h in range(2)]):
+        assert L[r] == pytest.approx(math.log(n_vis[b]), abs=1e-13)
+    Ob, _ = _np_cascade(wl)
+    np.testing.assert_allclose(O.reshape(Ob.shape), Ob, atol=1e-13)
+
+
+def test_page_shuffle_invariance():
+    """Physical page order is immaterial: same logical KV under two different
+    page permutations gives the same output."""
+    wl = W.build_cascade("s", B=3, Hq=4, Hkv=4, d=16, page_size=4,
+                         shared=[[(0, 3, 16)]], suffix_lens=[5, 0, 11], seed=9, shuffle=False)
+    O, L = oracle.cascade(wl)
+    perm = torch.randperm(wl.num_pages, generator=torch.Generator().manual_seed(11))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(len(perm))
+    wl.k_pool = wl.k_pool[inv].contiguous()  # logical page p now at physical perm[p]
+    wl.v_pool = wl.v_pool[inv].contiguous()
+    for lv in wl.levels:
+        lv.page_ids = perm[lv.page_ids.long()].to(torch.int32)
+    O2, L2 = oracle.cascade(wl)
+    np.testing.assert_allclose(O2, O, atol=1e-12)
+    np.testing.assert_allclose(L2, L, atol=1e-12)
+
+
+def test_boundaries_zero_suffix_and_zero_prefix():
+    """Zero-length suffix = prefix-only attention; P = 0 = pure suffix decode."""
+    wl = W.build_cascade("b", B=2, Hq=2, Hkv=1, d=16, page_size=4,
+                         shared=[[(0, 2, 10)]], suffix_lens=[0, 0], seed=4)
+    O, L = oracle.cascade(wl)
+    ids = wl.levels[0].page_ids.long()
+    K = wl.k_pool[ids].permute(1, 0, 2, 3).reshape(1, -1, 16)[0, :10].double().numpy()
+    V = wl.v_pool[ids].permute(1, 0, 2, 3).reshape(1, -1, 16)[0, :10].double().numpy()
+    Op, Lp = oracle.sdp(wl.q.double().numpy().reshape(4, 16), K, V, wl.scale)
+    np.testing.assert_allclose(O, Op, atol=1e-13)
+    np.testing.assert_allclose(L, Lp, atol=1e-13)
+    # no shared level, one empty sequence
+    wl2 = W.build_cascade("c", B=2, Hq=2, Hkv=1, d=16, page_size=4, shared=[],
+                          suffix_lens=[6, 0], seed=5)
+    O2, L2 = oracle.cascade(wl2)
+    assert np.all(O2[2:] == 0) and np.all(L2[2:] == -np.inf)
+    Ob, Lb = _np_cascade(wl2)
+    np.testing.assert_allclose(O2[:2], Ob.reshape(-1, 16)[:2], atol=1e-12)
+
+
+def test_paged_decode_and_prefix_agree_with_cascade():
+    """The per-sequence page-table form and the contiguous-prefix form are
+    independently written gathers; both must agree with the tree form."""
+    wl = W.make_config("tiny", seed=5)
+    O, L = oracle.cascade(wl)
+    pt, sl = W.full_page_tables(wl)
+    Op, Lp = oracle.paged_decode(wl.q, wl.k_pool, wl.v_pool, pt, sl, wl.scale)
+    np.testing.assert_allclose(Op.reshape(O.shape), O, atol=1e-12)
+    np.testing.assert_allclose(Lp.reshape(L.shape), L, atol=1e-12)
+    # contiguous [len][Hkv][d] prefix built from the shared level's pages
+    wl0 = W.make_config("tiny", seed=5)
+    wl0.levels = wl0.levels[:1]
+    O0, L0 = oracle.cascade(wl0)
+    ids = wl0.levels[0].page_ids.long()
+    k = wl0.k_pool[ids].permute(0, 2, 1, 3).reshape(-1, wl0.Hkv, wl0.d)
+    v = wl0.v_pool[ids].permute(0, 2, 1, 3).reshape(-1, wl0.Hkv, wl0.d)
+    Oc, Lc = oracle.prefix(wl0.q, k, v, wl0.scale)
+    np.testing.assert_allclose(Oc.reshape(O0.shape), O0, atol=1e-12)
+    np.testing.assert_allclose(Lc.reshape(L0.shape), L0, atol=1e-12)
+
+
+def test_probe_output_is_the_code_row():
+    wl = W.make_config("tiny", seed=0)
+    n = wl.seq_kv_len()
+    targets = [0, n[1] - 1, 255, 256 if n[3] > 256 else 3]
+    W.apply_probe(wl, targets)
+    O, L = oracle.cascade(wl)
+    for r, (b, h) in enumerate([(b, h) for b in range(wl.B) for h in range(wl.Hq)]):
+        # every other weight is below e^-300: zero to fp32, ~1e-200 in fp64
+        np.testing.assert_allclose(O[r], W.probe_expected(b, wl.d).double().numpy(), rtol=0,
+                                   atol=1e-30)
+
+
+def test_gqa_mapping_consecutive_heads():
+    """Query heads h and h' read the same KV head iff h // G == h' // G: with
+    identical q rows, heads of one group agree and heads of different groups
+    differ."""
+    wl = W.build_cascade("g", B=1, Hq=4, Hkv=2, d=16, page_size=4, shared=[],
+                         suffix_lens=[9], seed=2)
+    wl.q[0, :, :] = wl.q[0, 0, :]
+    O, _ = oracle.cascade(wl)
+    np.testing.assert_array_equal(O[0], O[1])
+    np.testing.assert_array_equal(O[2], O[3])
+    assert np.abs(O[0] - O[2]).max() > 1e-3
+
+
+# ------------------------------------------- planted mistakes must be caught
+_PINS = [
+    test_single_key_returns_its_value,
+    test_identical_keys_give_mean_value,
+    test_scores_use_scale_and_natural_log,
+    test_merge_identity_on_random_splits,
+    test_chunk_partial_states_reduce_to_full_attention,
+    test_blog_split_merge_example,
+    test_sdp_matches_brute_force_tiny,
+    lambda: test_cascade_matches_brute_force_tiny_trees(0),
+    test_zero_query_counts_visible_keys,
+    test_paged_decode_and_prefix_agree_with_cascade,
+    test_probe_output_is_the_code_row,
+    test_gqa_mapping_consecutive_heads,
+]
+
+_MUTANTS = {
+    "dropped_scale": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "gqa_modulo": ("int kvh = h / G;\n        int nk", "int kvh = h % G;\n        int nk"),
+    "short_node": ("for (t = 0; t < nd[2]; ++t)", "for (t = 0; t < nd[2] - 1; ++t)"),
+    "merge_sign": ("(w1 * O1[r * d + i] + w2 * O2[r * d + i])", "(w1 * O1[r * d + i] - w2 * O2[r * d + i])"),
+    "lse_without_max": ("double L = m + log(sum);", "double L = log(sum);"),
+    "slot_reversed": ("long slot = t % L->page_size;",
+                      "long slot = L->page_size - 1 - t % L->page_size;"),
+    "reduce_wrong_factor": ("O[i] = x * o_c[i] + y * O[i];", "O[i] = y * o_c[i] + x * O[i];"),
+}
+
+
+def _run_pins_with(so_path):
+    """Child-process entry: run every pin against a compiled oracle variant and
+    print how many failed."""
+    failed = []
+    with oracle.use_library(so_path):
+        for pin in _PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError):
+                failed.append(getattr(pin, "__name__", "lambda"))
+    print("FAILED_PINS", len(failed), ",".join(failed))
+
+
+@pytest.mark.parametrize("name", sorted(_MUTANTS))
+def test_pins_catch_planted_oracle_mistake(name, tmp_path):
+    """Plant one mistake in a copy of the oracle source; at least one pin must
+    fail (a crash of the mutant, e.g. an out-of-range read, also counts)."""
+    import subprocess
+    import sys
+    src = open(oracle.source_path()).read()
+    old, new = _MUTANTS[name]
+    assert old in src, f"mutation anchor for {name} not found"
+    c = tmp_path / "mut.c"
+    so = tmp_path / "mut.so"
+    c.write_text(src.replace(old, new))
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99", "-o", str(so),
+                           str(c), "-lm"])
+    code = ("import sys; sys.path[:0] = [%r, %r]; import test_oracle_pins as t; "
+            "t._run_pins_with(%r)" % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                                     os.path.dirname(os.path.abspath(__file__)), str(so)))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    if r.returncode != 0:
+        return  # the mutant crashed: caught
+    line = [l for l in r.stdout.splitlines() if l.startswith("FAILED_PINS")][-1]
+    assert int(line.split()[1]) > 0, f"planted mistake {name!r} passed every pin"
