@@ -1,0 +1,223 @@
+/*
+ * hp.h -- C ABI of the shared-prefix (cascade) decode attention library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The problem.  B decoding sequences each hold one new query token per query
+ * head.  Their keys and values form a prefix tree: a prefix shared by all or
+ * some of the sequences, possibly further shared levels, and a private suffix
+ * per sequence.  Attention over the concatenated keys is split at every tree
+ * vertex; the parts are computed separately and merged exactly by their
+ * log-sum-exp (Hydragen, "Attention Decomposition Across Subsequences", Eq. 5;
+ * "Hierarchical Sharing").  The queries of all sequences below a shared node
+ * are stacked into one matrix and attend to the node's keys in one
+ * matrix-matrix pass, so the node's KV is read once per step (Hydragen,
+ * "Inter-Sequence Batched Prefix Attention"; ChunkAttention, "The Chunk-First
+ * Phase Kernel in Detail").  Private suffixes are a paged per-sequence decode
+ * (ChunkAttention, "The Sequence-First Phase Kernel in Detail").
+ *
+ * Conventions shared by every call:
+ *   - q: bf16, row (b, h) at q + b*q_sb + h*q_sh (element strides; the head
+ *     dimension is contiguous).  Query head h reads KV head h / (Hq/Hkv).
+ *   - paged KV pools: bf16 [num_pages][Hkv][page_size][d], contiguous.  Token t
+ *     of a page list sits at page list[t / page_size], slot t % page_size.
+ *   - scale: the softmax scale applied to q.k (1/sqrt(d) in the pages).
+ *   - out: bf16 or f32, row (b, h) at out + b*o_sb + h*o_sh (elements).
+ *   - lse: f32, natural log of the softmax denominator of the scaled scores
+ *     (Hydragen's LSE(Q,K)), element (b, h) at lse + b*lse_sb + h.  A row with
+ *     no visible key gets out = 0 and lse = -inf.
+ *   - All device pointers are owned by the caller.  The library never
+ *     allocates, frees or synchronises inside the compute calls; every launch
+ *     is ordered on the given stream and can be captured in a CUDA graph.
+ *   - ws: caller-owned device workspace of at least the size the matching
+ *     *_workspace_bytes / plan call reports, 256-byte aligned.  Its first
+ *     bytes hold a device status word that kernels set on a bounds violation
+ *     or a wait that ran out; read it with hp_read_device_status.
+ *   - Supported: d in {64, 128}; Hq % Hkv == 0; page_size a multiple of 16 up
+ *     to 256; bf16 q/K/V.  Anything else returns HP_ERR_UNSUPPORTED.
+ *   - Errors are return codes; argument errors return before any launch.
+ */
+#ifndef HP_H
+#define HP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime's stream handle); NULL is the legacy stream. */
+typedef struct CUstream_st *hp_stream_t;
+
+typedef enum {
+    HP_OK = 0,
+    HP_ERR_ARG = 1,             /* invalid argument (null pointer, bad size, bad tree) */
+    HP_ERR_UNSUPPORTED = 2,     /* valid but outside the supported shapes */
+    HP_ERR_WORKSPACE = 3,       /* workspace or plan buffer too small or misaligned */
+    HP_ERR_CUDA = 4,            /* a CUDA runtime call failed */
+    HP_ERR_BOUNDS = 5,          /* device: a page id or length was out of range */
+    HP_ERR_DEVICE_TIMEOUT = 6   /* device: a bounded wait ran out */
+} hp_status;
+
+typedef enum { HP_BF16 = 0, HP_F32 = 1 } hp_dtype;
+
+const char *hp_status_str(hp_status s);
+
+/* ---------------------------------------------------------------------------
+ * hp_merge_states -- exact merge of two attention states over disjoint key
+ * sets (Hydragen Eq. 5 in its max-subtracted combine_lse form):
+ *   M = max(lse_a, lse_b); wa = e^(lse_a - M); wb = e^(lse_b - M)
+ *   o = (wa o_a + wb o_b) / (wa + wb);  lse = M + ln(wa + wb)
+ * o_a, o_b: f32 [rows][d] (contiguous); lse_a, lse_b: f32 [rows].
+ * o_out: [rows][d] of out_dt; lse_out: f32 [rows] (may be NULL).  Outputs may
+ * alias the inputs element for element (o_out == o_a with out_dt = HP_F32).
+ * Both states empty (-inf) gives o = 0, lse = -inf.  Any d >= 1.
+ * ------------------------------------------------------------------------- */
+hp_status hp_merge_states(const float *o_a, const float *lse_a, const float *o_b,
+                          const float *lse_b, void *o_out, hp_dtype out_dt, float *lse_out,
+                          int64_t rows, int32_t d, hp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hp_suffix_decode_paged -- per-sequence paged decode (ChunkAttention's
+ * sequence-first phase over private chunks; Hydragen's suffix attention).
+ * Sequence b attends over its first seq_lens[b] tokens, token t at page
+ * page_table[b*pt_stride + t/page_size], slot t % page_size, of the pools.
+ * The G = Hq/Hkv query heads of a KV head are processed together; the keys of
+ * a sequence are split into chunks whose partial states are merged in the
+ * same call.  page_table and seq_lens are device int32 arrays read on the
+ * device (so lengths may change between replays of a captured graph); a page
+ * id outside [0, num_pages) or a length above pt_stride*page_size sets
+ * HP_ERR_BOUNDS in the workspace status word and the offending keys are
+ * skipped.
+ * ------------------------------------------------------------------------- */
+size_t hp_suffix_workspace_bytes(int32_t B, int32_t Hq, int32_t d, int32_t pt_stride,
+                                 int32_t page_size);
+hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int32_t B,
+                                 const void *k_pool, const void *v_pool, int32_t num_pages,
+                                 int32_t page_size, const int32_t *page_table, int32_t pt_stride,
+                                 const int32_t *seq_lens, int32_t Hq, int32_t Hkv, int32_t d,
+                                 float scale, void *out, hp_dtype out_dt, int64_t o_sb,
+                                 int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
+                                 size_t ws_bytes, hp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * hp_prefix_attn -- inter-sequence batched attention against one contiguous
+ * shared prefix (Hydragen, "Inter-Sequence Batched Prefix Attention": the
+ * queries of sequences [row_begin, row_begin + rows) are stacked and attend
+ * to the prefix in one matrix-matrix pass; the prefix is read once).
+ * k, v: bf16, token t of KV head g at k + t*kv_st + g*kv_sh (elements; the
+ * head dimension contiguous; kv_st and kv_sh multiples of 8; 16-byte aligned
+ * base).  Outputs rows b in [row_begin, row_begin + rows) of out / lse.
+ * prefix_len = 0 gives out = 0, lse = -inf.
+ * ------------------------------------------------------------------------- */
+size_t hp_prefix_workspace_bytes(int32_t rows, int32_t Hq, int32_t Hkv, int32_t d,
+                                 int32_t prefix_len);
+hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_begin,
+                         int32_t rows, const void *k, const void *v, int64_t kv_st, int64_t kv_sh,
+                         int32_t prefix_len, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                         void *out, hp_dtype out_dt, int64_t o_sb, int64_t o_sh, float *lse,
+                         int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Cascade decode over a level-by-level prefix tree (Hydragen "Hierarchical
+ * Sharing"; ChunkAttention prefix tree and its (C, i, j) kernel context).
+ *
+ * A level is a set of nodes with disjoint sequence ranges.  Node
+ * (seq_begin, seq_end, kv_len, page_off) holds kv_len tokens, visible to the
+ * contiguous sequences [seq_begin, seq_end), in pages
+ * page_ids[page_off .. page_off + ceil(kv_len/page_size)) of the level's pools.
+ * Sequence b attends over the tokens of the node covering it at each level
+ * (a level may leave b uncovered).  A private suffix is a level whose nodes
+ * cover one sequence each; kv_len = 0 is legal.
+ *
+ * The nodes and page ids are HOST arrays, read only during hp_cascade_plan.
+ * The pools are device pointers; they must stay valid while the plan is used.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int32_t seq_begin, seq_end, kv_len, page_off;
+} hp_tree_node;
+
+typedef struct {
+    const void *k_pool; /* device, bf16 [num_pages][Hkv][page_size][d], 16-byte aligned */
+    const void *v_pool;
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t num_nodes;
+    const hp_tree_node *nodes; /* host */
+    const int32_t *page_ids;   /* host */
+    int32_t num_page_ids;
+} hp_tree_level;
+
+typedef struct {
+    int32_t num_levels; /* 1 .. 8 */
+    int32_t B, Hq, Hkv, d;
+    const hp_tree_level *levels; /* host */
+    int32_t num_sms;             /* SMs to plan for; 0 = the current device's count */
+} hp_tree_desc;
+
+/* Host summary of a plan, filled by hp_cascade_plan and passed back to
+ * hp_cascade_decode (plain data, caller-owned, copyable).  `tag` ties it to
+ * the device plan it describes; the kernels check it and report HP_ERR_ARG
+ * through the status word on a mismatch. */
+typedef struct {
+    int32_t B, Hq, Hkv, d;
+    int32_t n_tc_items;    /* shared-node items on the tensor-core kernel */
+    int32_t n_small_items; /* small-row items (private suffixes, narrow nodes) */
+    int32_t grid_tc, grid_small;
+    int64_t n_part_rows;   /* partial (O, LSE) rows in the workspace */
+    int64_t plan_bytes;
+    int64_t ws_bytes;      /* workspace hp_cascade_decode needs */
+    uint64_t tag;
+} hp_plan_info;
+
+/* Bytes of the device plan buffer for this tree (host only, no CUDA calls
+ * when desc->num_sms > 0).  0 on an invalid descriptor. */
+size_t hp_cascade_plan_bytes(const hp_tree_desc *desc);
+
+/* Validate the tree, flatten it into work items (the pages' context
+ * generation: shared nodes become batched items split along the key axis,
+ * private nodes become per-sequence items), encode the TMA descriptors of
+ * the pools, and copy the plan into plan_dev (device, >= plan_bytes,
+ * 256-byte aligned) on `stream`.  The call waits for that copy, so it is not
+ * for use inside stream capture.  Re-run only when the tree changes; a plan
+ * is reused across steps while the tree and the pools are unchanged. */
+hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_bytes,
+                          hp_plan_info *info, hp_stream_t stream);
+
+/* One cascade decode step: every sequence, every head, all levels, merged.
+ * q, out, lse as in the conventions above, for all B sequences; q strides
+ * multiples of 8 elements and q 16-byte aligned.  ws: >= info->ws_bytes.
+ * No host synchronisation, no allocation; graph-capturable. */
+hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, const void *q,
+                            int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,
+                            int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
+                            size_t ws_bytes, hp_stream_t stream);
+
+/* Host-side description of a plan for inspection and tests: the (level, node,
+ * seq_begin, seq_end, pass) context list in the order the pages list it --
+ * shared nodes (more than one sequence; batched pass = 1) level by level,
+ * then each sequence's private nodes in level order (pass = 0).  Writes at
+ * most cap entries of 5 int32 each into out; returns the entry count, or -1
+ * on an invalid descriptor. */
+int32_t hp_cascade_contexts(const hp_tree_desc *desc, int32_t *out, int32_t cap);
+
+/* Work-item counts of a plan for a descriptor: [0] tensor-core items,
+ * [1] small-row items, [2] partial rows, [3] merge entries.  -1 on error. */
+int32_t hp_cascade_plan_stats(const hp_tree_desc *desc, int64_t *stats4);
+
+/* ---------------------------------------------------------------------------
+ * Device status: reads and clears the status word of a workspace.  This call
+ * synchronises `stream`.  Returns HP_OK, HP_ERR_BOUNDS, HP_ERR_DEVICE_TIMEOUT
+ * or HP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+hp_status hp_read_device_status(void *ws, hp_stream_t stream);
+
+/* Library build information: the SM architecture compiled for (103 for
+ * sm_103a) and the library ABI version. */
+int32_t hp_build_arch(void);
+int32_t hp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HP_H */

@@ -1,0 +1,325 @@
+"""ctypes binding of the C ABI in include/hp.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libhp.so.  There is no fallback -- if the library is missing or
+fails to load, every call raises.  PyTorch supplies device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libhp.so")
+
+HP_OK, HP_ERR_ARG, HP_ERR_UNSUPPORTED, HP_ERR_WORKSPACE, HP_ERR_CUDA, HP_ERR_BOUNDS, HP_ERR_DEVICE_TIMEOUT = range(7)
+HP_BF16, HP_F32 = 0, 1
+
+c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+
+class HpTreeNode(ctypes.Structure):
+    _fields_ = [("seq_begin", c_i32), ("seq_end", c_i32), ("kv_len", c_i32), ("page_off", c_i32)]
+
+
+class HpTreeLevel(ctypes.Structure):
+    _fields_ = [("k_pool", c_vp), ("v_pool", c_vp), ("num_pages", c_i32), ("page_size", c_i32),
+                ("num_nodes", c_i32), ("nodes", ctypes.POINTER(HpTreeNode)),
+                ("page_ids", ctypes.POINTER(c_i32)), ("num_page_ids", c_i32)]
+
+
+class HpTreeDesc(ctypes.Structure):
+    _fields_ = [("num_levels", c_i32), ("B", c_i32), ("Hq", c_i32), ("Hkv", c_i32), ("d", c_i32),
+                ("levels", ctypes.POINTER(HpTreeLevel)), ("num_sms", c_i32)]
+
+
+class HpPlanInfo(ctypes.Structure):
+    _fields_ = [("B", c_i32), ("Hq", c_i32), ("Hkv", c_i32), ("d", c_i32), ("n_tc_items", c_i32),
+                ("n_small_items", c_i32), ("grid_tc", c_i32), ("grid_small", c_i32),
+                ("n_part_rows", c_i64), ("plan_bytes", c_i64), ("ws_bytes", c_i64),
+                ("tag", ctypes.c_uint64)]
+
+
+# name -> (restype, argtypes); the exported surface of hp.h
+_SIGNATURES = {
+    "hp_status_str": (ctypes.c_char_p, [c_i32]),
+    "hp_build_arch": (c_i32, []),
+    "hp_abi_version": (c_i32, []),
+    "hp_merge_states": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_i64, c_i32, c_vp]),
+    "hp_suffix_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "hp_suffix_decode_paged": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_i32, c_i32, c_vp, c_i32,
+                                       c_vp, c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64, c_i64,
+                                       c_vp, c_i64, c_vp, c_sz, c_vp]),
+    "hp_prefix_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "hp_prefix_attn": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_i64, c_i64, c_i32,
+                               c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64, c_i64, c_vp, c_i64,
+                               c_vp, c_sz, c_vp]),
+    "hp_cascade_plan_bytes": (c_sz, [ctypes.POINTER(HpTreeDesc)]),
+    "hp_cascade_plan": (c_i32, [ctypes.POINTER(HpTreeDesc), c_vp, c_sz, ctypes.POINTER(HpPlanInfo), c_vp]),
+    "hp_cascade_decode": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_i64, c_i64, c_f32, c_vp,
+                                  c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz, c_vp]),
+    "hp_cascade_contexts": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i32), c_i32]),
+    "hp_cascade_plan_stats": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i64)]),
+    "hp_read_device_status": (c_i32, [c_vp, c_vp]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class HpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)} (status {status})")
+
+
+def library() -> ctypes.CDLL:
+    """Load libhp.so (built by ``shared_prefix_decode_gb300.build``).  Raises
+    if it is missing: there is no other implementation to fall back to."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing; run "
+                                   "`python -m shared_prefix_decode_gb300.build` (nvcc, sm_103a)")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def exported_symbols() -> List[str]:
+    return list(_SIGNATURES)
+
+
+def status_str(status: int) -> str:
+    return library().hp_status_str(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != HP_OK:
+        raise HpError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dt(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return HP_BF16
+    if dtype == torch.float32:
+        return HP_F32
+    raise ValueError(f"output dtype must be bfloat16 or float32, not {dtype}")
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zeroed workspace (the first word is the device status word)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------- merge
+def hp_merge_states(o_a: torch.Tensor, lse_a: torch.Tensor, o_b: torch.Tensor, lse_b: torch.Tensor,
+                    out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None,
+                    out_dtype=torch.float32, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Exact two-state merge; o_* f32 [rows, d], lse_* f32 [rows]."""
+    _need(o_a.dtype == torch.float32 and o_b.dtype == torch.float32, "states must be float32")
+    _need(o_a.is_contiguous() and o_b.is_contiguous(), "states must be contiguous")
+    rows, d = o_a.shape
+    if out is None:
+        out = torch.empty(rows, d, dtype=out_dtype, device=o_a.device)
+    if lse_out is None:
+        lse_out = torch.empty(rows, dtype=torch.float32, device=o_a.device)
+    _check(library().hp_merge_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(out),
+                                     _dt(out.dtype), _ptr(lse_out), rows, d, _stream(stream)),
+           "hp_merge_states")
+    return out, lse_out
+
+
+# ----------------------------------------------------- paged suffix decode
+def suffix_workspace_bytes(B: int, Hq: int, d: int, pt_stride: int, page_size: int) -> int:
+    return int(library().hp_suffix_workspace_bytes(B, Hq, d, pt_stride, page_size))
+
+
+def hp_suffix_decode_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           page_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           ws: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                           stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """q [B,Hq,d] bf16; pools [P,Hkv,ps,d] bf16; page_table [B,W] int32;
+    seq_lens [B] int32 (device)."""
+    B, Hq, d = q.shape
+    P, Hkv, ps, d2 = k_pool.shape
+    _need(d2 == d and v_pool.shape == k_pool.shape, "pool shape mismatch")
+    _need(page_table.dtype == torch.int32 and seq_lens.dtype == torch.int32, "int32 tables")
+    _need(page_table.is_contiguous() and k_pool.is_contiguous() and v_pool.is_contiguous(), "contiguous")
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = alloc_workspace(suffix_workspace_bytes(B, Hq, d, page_table.shape[1], ps), q.device)
+    _check(library().hp_suffix_decode_paged(
+        _ptr(q), q.stride(0), q.stride(1), B, _ptr(k_pool), _ptr(v_pool), P, ps, _ptr(page_table),
+        page_table.stride(0), _ptr(seq_lens), Hq, Hkv, d, float(scale), _ptr(out), _dt(out.dtype),
+        out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(), _stream(stream)),
+        "hp_suffix_decode_paged")
+    return out, lse
+
+
+# --------------------------------------------------- contiguous prefix
+def prefix_workspace_bytes(rows: int, Hq: int, Hkv: int, d: int, prefix_len: int) -> int:
+    return int(library().hp_prefix_workspace_bytes(rows, Hq, Hkv, d, prefix_len))
+
+
+def hp_prefix_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float, row_begin: int = 0,
+                   rows: Optional[int] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                   out_dtype=torch.bfloat16, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """q [B,Hq,d] bf16; k/v [len,Hkv,d] bf16 (strided rows allowed)."""
+    B, Hq, d = q.shape
+    ln, Hkv, d2 = k.shape
+    _need(d2 == d and v.shape == k.shape and v.stride() == k.stride(), "prefix shape mismatch")
+    _need(k.stride(2) == 1, "head dimension must be contiguous")
+    if rows is None:
+        rows = B - row_begin
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = alloc_workspace(prefix_workspace_bytes(rows, Hq, Hkv, d, ln), q.device)
+    _check(library().hp_prefix_attn(
+        _ptr(q), q.stride(0), q.stride(1), row_begin, rows, _ptr(k), _ptr(v), k.stride(0), k.stride(1),
+        ln, Hq, Hkv, d, float(scale), _ptr(out), _dt(out.dtype), out.stride(0), out.stride(1), _ptr(lse),
+        lse.stride(0), _ptr(ws), ws.numel(), _stream(stream)), "hp_prefix_attn")
+    return out, lse
+
+
+# ------------------------------------------------------------- cascade
+class _Desc:
+    """Keeps the ctypes arrays of a tree descriptor alive."""
+
+    def __init__(self, levels, B: int, Hq: int, Hkv: int, d: int, num_sms: int = 0):
+        self.keep = []
+        arr = (HpTreeLevel * max(len(levels), 1))()
+        for i, (k_pool, v_pool, num_pages, page_size, nodes, page_ids) in enumerate(levels):
+            nodes = [tuple(int(x) for x in n) for n in nodes]
+            n_arr = (HpTreeNode * max(len(nodes), 1))(*[HpTreeNode(*n) for n in nodes])
+            ids = [int(x) for x in page_ids]
+            i_arr = (c_i32 * max(len(ids), 1))(*ids)
+            self.keep += [n_arr, i_arr]
+            arr[i] = HpTreeLevel(k_pool, v_pool, num_pages, page_size, len(nodes),
+                                 ctypes.cast(n_arr, ctypes.POINTER(HpTreeNode)),
+                                 ctypes.cast(i_arr, ctypes.POINTER(c_i32)), len(ids))
+        self.keep.append(arr)
+        self.desc = HpTreeDesc(len(levels), B, Hq, Hkv, d, ctypes.cast(arr, ctypes.POINTER(HpTreeLevel)),
+                               num_sms)
+
+
+def _levels_of(wl) -> list:
+    """Tree levels of a ``workloads.CascadeWorkload`` (pools must be on the GPU
+    for planning; host-only inspection accepts CPU pools)."""
+    out = []
+    for lv in wl.levels:
+        out.append((wl.k_pool.data_ptr(), wl.v_pool.data_ptr(), wl.num_pages, wl.page_size,
+                    lv.nodes.tolist(), lv.page_ids.cpu().tolist()))
+    return out
+
+
+def hp_cascade_contexts(levels, B, Hq, Hkv, d) -> List[Tuple[int, int, int, int, int]]:
+    """(level, node, seq_begin, seq_end, batched) context list (host only)."""
+    D = _Desc(levels, B, Hq, Hkv, d, num_sms=1)
+    n = library().hp_cascade_contexts(ctypes.byref(D.desc), None, 0)
+    if n < 0:
+        raise HpError(HP_ERR_ARG, "hp_cascade_contexts")
+    buf = (c_i32 * (5 * max(n, 1)))()
+    library().hp_cascade_contexts(ctypes.byref(D.desc), buf, n)
+    return [tuple(buf[5 * i:5 * i + 5]) for i in range(n)]
+
+
+def hp_cascade_plan_stats(levels, B, Hq, Hkv, d, num_sms: int = 152) -> Tuple[int, int, int, int]:
+    D = _Desc(levels, B, Hq, Hkv, d, num_sms=num_sms)
+    st = (c_i64 * 4)()
+    if library().hp_cascade_plan_stats(ctypes.byref(D.desc), st) != 0:
+        raise HpError(HP_ERR_ARG, "hp_cascade_plan_stats")
+    return tuple(int(x) for x in st)
+
+
+def hp_cascade_plan_bytes(levels, B, Hq, Hkv, d, num_sms: int = 0) -> int:
+    D = _Desc(levels, B, Hq, Hkv, d, num_sms=num_sms)
+    return int(library().hp_cascade_plan_bytes(ctypes.byref(D.desc)))
+
+
+class CascadePlan:
+    """A device-resident plan for one prefix tree (re-plan when the tree
+    changes).  Owns the plan buffer and a workspace sized for it."""
+
+    def __init__(self, levels, B: int, Hq: int, Hkv: int, d: int, device="cuda", stream=None,
+                 num_sms: int = 0, workspace: bool = True):
+        D = _Desc(levels, B, Hq, Hkv, d, num_sms=num_sms)
+        nbytes = int(library().hp_cascade_plan_bytes(ctypes.byref(D.desc)))
+        if nbytes == 0:
+            raise HpError(HP_ERR_ARG, "hp_cascade_plan_bytes")
+        self.plan = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.info = HpPlanInfo()
+        _check(library().hp_cascade_plan(ctypes.byref(D.desc), _ptr(self.plan), nbytes,
+                                         ctypes.byref(self.info), _stream(stream)), "hp_cascade_plan")
+        self.B, self.Hq, self.Hkv, self.d = B, Hq, Hkv, d
+        self.ws = alloc_workspace(self.info.ws_bytes, device) if workspace else None
+
+    @classmethod
+    def from_workload(cls, wl, **kw) -> "CascadePlan":
+        return cls(_levels_of(wl), wl.B, wl.Hq, wl.Hkv, wl.d, device=wl.q.device, **kw)
+
+    def decode(self, q: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+               lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+               out_dtype=torch.bfloat16, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        return hp_cascade_decode(self, q, scale, out=out, lse=lse, ws=ws, out_dtype=out_dtype, stream=stream)
+
+
+def hp_cascade_plan(levels, B, Hq, Hkv, d, device="cuda", stream=None, num_sms: int = 0) -> CascadePlan:
+    return CascadePlan(levels, B, Hq, Hkv, d, device=device, stream=stream, num_sms=num_sms)
+
+
+def hp_cascade_decode(plan: CascadePlan, q: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                      out_dtype=torch.bfloat16, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    B, Hq, d = q.shape
+    _need((B, Hq, d) == (plan.B, plan.Hq, plan.d), "q shape does not match the plan")
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = plan.ws
+    _check(library().hp_cascade_decode(
+        _ptr(plan.plan), ctypes.byref(plan.info), _ptr(q), q.stride(0), q.stride(1), float(scale), _ptr(out),
+        _dt(out.dtype), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(),
+        _stream(stream)), "hp_cascade_decode")
+    return out, lse
+
+
+def hp_read_device_status(ws: torch.Tensor, stream=None) -> int:
+    """Reads and clears the workspace status word (synchronises the stream)."""
+    return int(library().hp_read_device_status(_ptr(ws), _stream(stream)))

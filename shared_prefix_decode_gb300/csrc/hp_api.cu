@@ -1,0 +1,769 @@
+// hp_api.cu -- host side of the C ABI declared in include/hp.h: argument
+// validation, TMA descriptor encoding, the prefix-tree planner, and the
+// launches.  No entry point here allocates device memory or synchronises,
+// except hp_cascade_plan (waits for its upload) and hp_read_device_status.
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "hp_internal.h"
+
+using namespace hp;
+
+namespace {
+
+constexpr int32_t kAbiVersion = 1;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------- utilities
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int device_sms()
+{
+    static std::atomic<int> cached{0};
+    int v = cached.load();
+    if (v > 0)
+        return v;
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
+        cached.store(n);
+        return n;
+    }
+    cudaGetLastError();  // clear a sticky "no device" error
+    return 152;          // GB300
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Paged pool [num_pages][Hkv][ps][d] bf16, box = 64 columns x box_tok tokens,
+// 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *m, const void *pool, int num_pages, int Hkv, int ps, int d, int box_tok)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)ps * d * 2, (cuuint64_t)Hkv * ps * d * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_tok, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Contiguous prefix: token t, head g at base + t*st + g*sh (elements);
+// box = 64 columns x 1 head x 128 tokens.
+bool encode_prefix_map(CUtensorMap *m, const void *base, int len, int Hkv, int d, int64_t st, int64_t sh)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)len};
+    cuuint64_t strides[2] = {(cuuint64_t)sh * 2, (cuuint64_t)st * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kTcTile};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool supported_d(int d) { return d == 64 || d == 128; }
+
+// q (and out) rows are read as 16-byte vectors by the tensor-core kernel and
+// 4-byte words by the small kernel.
+bool q_layout_ok(const void *q, int64_t q_sb, int64_t q_sh)
+{
+    return aligned(q, 16) && q_sb % 8 == 0 && q_sh % 8 == 0 && q_sb >= 0 && q_sh >= 0;
+}
+
+bool out_layout_ok(const void *out, hp_dtype dt, int64_t o_sb, int64_t o_sh, int d)
+{
+    if (dt != HP_BF16 && dt != HP_F32)
+        return false;
+    // each lane of the merge writes d/32 consecutive values
+    const size_t esz = dt == HP_F32 ? 4 : 2;
+    const size_t lane_bytes = esz * (size_t)(d / 32);
+    return aligned(out, lane_bytes) && (o_sb * (int64_t)esz) % (int64_t)lane_bytes == 0 &&
+           (o_sh * (int64_t)esz) % (int64_t)lane_bytes == 0;
+}
+
+struct WsLayout {
+    size_t off_lse, off_o, total;
+};
+
+WsLayout ws_layout(int64_t part_rows, int d)
+{
+    WsLayout w;
+    w.off_lse = kWsHeader;
+    w.off_o = round_up(w.off_lse + (size_t)std::max<int64_t>(part_rows, 1) * 4, 256);
+    w.total = round_up(w.off_o + (size_t)std::max<int64_t>(part_rows, 1) * d * 4, 256);
+    return w;
+}
+
+// ------------------------------------------------------ standalone splits
+int suffix_split_len(int B, int Hq, int max_len, int sms)
+{
+    const int64_t chunks = (int64_t)B * Hq * ceil_div(std::max(max_len, 1), kChunk);
+    const int64_t target = (int64_t)sms * 32;  // ~4 items per warp slot, per head
+    const int64_t per = std::max<int64_t>(4, ceil_div(chunks, target));
+    return (int)(per * kChunk);
+}
+
+struct PrefixGeo {
+    int spi, n_rc, n_split, split_len, n_items;
+    int64_t part_rows;
+};
+
+PrefixGeo prefix_geo(int rows, int G, int Hkv, int len, int sms)
+{
+    PrefixGeo g{};
+    g.spi = std::max(1, kTcMaxRows / G);
+    g.spi = std::min(g.spi, std::max(rows, 1));
+    g.n_rc = (int)ceil_div(rows, g.spi);
+    const int64_t tiles = ceil_div(std::max(len, 1), kTcTile);
+    const int64_t per = std::max<int64_t>(1, ceil_div((int64_t)g.n_rc * Hkv * tiles, sms));
+    g.split_len = (int)(per * kTcTile);
+    g.n_split = len > 0 ? (int)ceil_div(len, g.split_len) : 0;
+    g.n_items = g.n_rc * Hkv * g.n_split;
+    g.part_rows = (int64_t)g.n_items * g.spi * G;
+    return g;
+}
+
+// --------------------------------------------------------------- planner
+struct HostPlan {
+    PlanHeader hdr;
+    std::vector<CUtensorMap> maps;
+    std::vector<WorkItem> tc, small;
+    std::vector<int32_t> page_ids;
+    std::vector<int32_t> merge_ptr, merge_idx;
+    std::vector<int32_t> contexts;  // (level, node, seq_begin, seq_end, pass) x n
+};
+
+hp_status validate_desc(const hp_tree_desc *d)
+{
+    if (!d || !d->levels || d->num_levels < 1 || d->B < 1 || d->Hq < 1 || d->Hkv < 1 || d->Hq % d->Hkv)
+        return HP_ERR_ARG;
+    if (d->num_levels > kMaxLevels || !supported_d(d->d) || d->Hq / d->Hkv > kTcMaxRows)
+        return HP_ERR_UNSUPPORTED;
+    for (int l = 0; l < d->num_levels; ++l) {
+        const hp_tree_level &L = d->levels[l];
+        if (L.num_nodes < 0 || L.num_page_ids < 0 || L.num_pages < 1)
+            return HP_ERR_ARG;
+        if (L.page_size < 16 || L.page_size > 256 || L.page_size % 16)
+            return HP_ERR_UNSUPPORTED;
+        if (!L.k_pool || !L.v_pool || !aligned(L.k_pool, 16) || !aligned(L.v_pool, 16))
+            return HP_ERR_ARG;
+        if ((L.num_nodes > 0 && !L.nodes) || (L.num_page_ids > 0 && !L.page_ids))
+            return HP_ERR_ARG;
+        std::vector<std::pair<int, int>> ranges;
+        for (int n = 0; n < L.num_nodes; ++n) {
+            const hp_tree_node &N = L.nodes[n];
+            if (N.seq_begin < 0 || N.seq_end > d->B || N.seq_begin >= N.seq_end || N.kv_len < 0 || N.page_off < 0)
+                return HP_ERR_ARG;
+            const int64_t npg = ceil_div(N.kv_len, L.page_size);
+            if ((int64_t)N.page_off + npg > L.num_page_ids)
+                return HP_ERR_ARG;
+            for (int64_t i = 0; i < npg; ++i) {
+                const int32_t pid = L.page_ids[N.page_off + i];
+                if (pid < 0 || pid >= L.num_pages)
+                    return HP_ERR_ARG;
+            }
+            ranges.emplace_back(N.seq_begin, N.seq_end);
+        }
+        std::sort(ranges.begin(), ranges.end());
+        for (size_t i = 1; i < ranges.size(); ++i)
+            if (ranges[i].first < ranges[i - 1].second)
+                return HP_ERR_ARG;  // nodes of one level must cover disjoint sequences
+    }
+    return HP_OK;
+}
+
+// Context list in the pages' order: shared nodes level by level, then each
+// sequence's private nodes in level order.
+void build_contexts(const hp_tree_desc *d, std::vector<int32_t> &out)
+{
+    out.clear();
+    for (int l = 0; l < d->num_levels; ++l)
+        for (int n = 0; n < d->levels[l].num_nodes; ++n) {
+            const hp_tree_node &N = d->levels[l].nodes[n];
+            if (N.seq_end - N.seq_begin > 1)
+                out.insert(out.end(), {l, n, N.seq_begin, N.seq_end, 1});
+        }
+    for (int b = 0; b < d->B; ++b)
+        for (int l = 0; l < d->num_levels; ++l)
+            for (int n = 0; n < d->levels[l].num_nodes; ++n) {
+                const hp_tree_node &N = d->levels[l].nodes[n];
+                if (N.seq_begin == b && N.seq_end == b + 1)
+                    out.insert(out.end(), {l, n, N.seq_begin, N.seq_end, 0});
+            }
+}
+
+hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
+{
+    hp_status st = validate_desc(d);
+    if (st != HP_OK)
+        return st;
+    const int G = d->Hq / d->Hkv;
+    const int sms = d->num_sms > 0 ? d->num_sms : device_sms();
+    PlanHeader &H = P.hdr;
+    std::memset(&H, 0, sizeof(H));
+    H.magic = kPlanMagic;
+    H.version = 1;
+    H.B = d->B;
+    H.Hq = d->Hq;
+    H.Hkv = d->Hkv;
+    H.d = d->d;
+    H.G = G;
+    H.num_levels = d->num_levels;
+
+    // page ids of all levels, concatenated
+    std::vector<int32_t> level_page_off(d->num_levels);
+    for (int l = 0; l < d->num_levels; ++l) {
+        const hp_tree_level &L = d->levels[l];
+        level_page_off[l] = (int32_t)P.page_ids.size();
+        P.page_ids.insert(P.page_ids.end(), L.page_ids, L.page_ids + L.num_page_ids);
+        LevelDev &LD = H.levels[l];
+        LD.k_pool = L.k_pool;
+        LD.v_pool = L.v_pool;
+        LD.num_pages = L.num_pages;
+        LD.page_size = L.page_size;
+        LD.tc_box = std::gcd(L.page_size, kTcTile);
+    }
+
+    // Split sizes.  Shared (tensor-core) work: total 128-key tiles spread over
+    // one wave of CTAs (one per SM).  Small-row work: 16-key chunks spread
+    // over ~8 warps per SM.
+    int64_t tc_tiles = 0, small_chunks = 0;
+    for (int l = 0; l < d->num_levels; ++l)
+        for (int n = 0; n < d->levels[l].num_nodes; ++n) {
+            const hp_tree_node &N = d->levels[l].nodes[n];
+            const int64_t rows = (int64_t)(N.seq_end - N.seq_begin) * G;
+            if (N.kv_len == 0)
+                continue;
+            if (rows > kSmallRows) {
+                const int spc = std::max(1, kTcMaxRows / G);
+                tc_tiles += ceil_div(N.seq_end - N.seq_begin, spc) * d->Hkv * ceil_div(N.kv_len, kTcTile);
+            } else {
+                small_chunks += (int64_t)d->Hkv * ceil_div(N.kv_len, kChunk);
+            }
+        }
+    const int64_t tc_split = kTcTile * std::max<int64_t>(1, ceil_div(tc_tiles, sms));
+    const int64_t small_split = kChunk * std::max<int64_t>(4, ceil_div(small_chunks, (int64_t)sms * 8));
+
+    // Items and partial rows, level by level; merge lists per (b, kvh).
+    std::vector<std::vector<int32_t>> lists((size_t)d->B * d->Hkv);
+    int64_t part = 0;
+    for (int l = 0; l < d->num_levels; ++l) {
+        const hp_tree_level &L = d->levels[l];
+        for (int n = 0; n < L.num_nodes; ++n) {
+            const hp_tree_node &N = L.nodes[n];
+            if (N.kv_len == 0)
+                continue;
+            const int nseq = N.seq_end - N.seq_begin;
+            const bool tc = (int64_t)nseq * G > kSmallRows;
+            const int spc = tc ? std::max(1, kTcMaxRows / G) : nseq;
+            const int64_t split = tc ? tc_split : small_split;
+            for (int s0 = N.seq_begin; s0 < N.seq_end; s0 += spc) {
+                const int ns = std::min(spc, N.seq_end - s0);
+                for (int kvh = 0; kvh < d->Hkv; ++kvh)
+                    for (int64_t k0 = 0; k0 < N.kv_len; k0 += split) {
+                        WorkItem w;
+                        w.level = l;
+                        w.seq_begin = s0;
+                        w.n_seq = ns;
+                        w.kvh = kvh;
+                        w.k0 = (int32_t)k0;
+                        w.k1 = (int32_t)std::min<int64_t>(k0 + split, N.kv_len);
+                        w.page_base = level_page_off[l] + N.page_off;
+                        w.part_row = (int32_t)part;
+                        for (int b = s0; b < s0 + ns; ++b)
+                            lists[(size_t)b * d->Hkv + kvh].push_back((int32_t)(part + (int64_t)(b - s0) * G));
+                        part += (int64_t)ns * G;
+                        (tc ? P.tc : P.small).push_back(w);
+                    }
+            }
+        }
+    }
+    if (part > INT32_MAX)
+        return HP_ERR_UNSUPPORTED;
+    // longest items first: the static round-robin over warps then balances
+    std::stable_sort(P.small.begin(), P.small.end(),
+                     [](const WorkItem &a, const WorkItem &b) { return (a.k1 - a.k0) > (b.k1 - b.k0); });
+    P.merge_ptr.assign((size_t)d->B * d->Hkv + 1, 0);
+    for (size_t i = 0; i < lists.size(); ++i) {
+        P.merge_ptr[i + 1] = P.merge_ptr[i] + (int32_t)lists[i].size();
+        P.merge_idx.insert(P.merge_idx.end(), lists[i].begin(), lists[i].end());
+    }
+    H.n_tc = (int32_t)P.tc.size();
+    H.n_small = (int32_t)P.small.size();
+    H.n_part_rows = (int32_t)part;
+    H.n_merge = (int32_t)P.merge_idx.size();
+
+    // device layout
+    size_t off = round_up(sizeof(PlanHeader), 128);
+    H.off_maps = (int64_t)off;
+    off += sizeof(CUtensorMap) * kMapsPerLevel * d->num_levels;
+    off = round_up(off, 64);
+    H.off_tc = (int64_t)off;
+    off += sizeof(WorkItem) * P.tc.size();
+    off = round_up(off, 64);
+    H.off_small = (int64_t)off;
+    off += sizeof(WorkItem) * P.small.size();
+    off = round_up(off, 64);
+    H.off_page_ids = (int64_t)off;
+    off += 4 * std::max<size_t>(P.page_ids.size(), 1);
+    off = round_up(off, 64);
+    H.off_merge_ptr = (int64_t)off;
+    off += 4 * P.merge_ptr.size();
+    off = round_up(off, 64);
+    H.off_merge_idx = (int64_t)off;
+    off += 4 * std::max<size_t>(P.merge_idx.size(), 1);
+    H.total_bytes = (int64_t)round_up(off, 256);
+    const WsLayout ws = ws_layout(part, d->d);
+    H.ws_off_lse = (int64_t)ws.off_lse;
+    H.ws_off_o = (int64_t)ws.off_o;
+    H.ws_bytes = (int64_t)ws.total;
+
+    build_contexts(d, P.contexts);
+
+    if (encode) {
+        P.maps.resize((size_t)kMapsPerLevel * d->num_levels);
+        for (int l = 0; l < d->num_levels; ++l) {
+            const hp_tree_level &L = d->levels[l];
+            const int tcb = H.levels[l].tc_box;
+            CUtensorMap *m = &P.maps[(size_t)l * kMapsPerLevel];
+            if (!encode_pool_map(m + 0, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, tcb) ||
+                !encode_pool_map(m + 1, L.v_pool, L.num_pages, d->Hkv, L.page_size, d->d, tcb) ||
+                !encode_pool_map(m + 2, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk) ||
+                !encode_pool_map(m + 3, L.v_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk))
+                return HP_ERR_CUDA;
+        }
+    }
+    return HP_OK;
+}
+
+uint64_t new_tag()
+{
+    static std::atomic<uint64_t> ctr{0};
+    const uint64_t t = (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count();
+    return (t * 0x9E3779B97F4A7C15ull) ^ (++ctr * 0xBF58476D1CE4E5B9ull) ^ 0x68706c616e000000ull;
+}
+
+uint32_t *status_ptr(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+const char *hp_status_str(hp_status s)
+{
+    switch (s) {
+    case HP_OK: return "ok";
+    case HP_ERR_ARG: return "invalid argument";
+    case HP_ERR_UNSUPPORTED: return "unsupported shape or layout";
+    case HP_ERR_WORKSPACE: return "workspace or plan buffer too small or misaligned";
+    case HP_ERR_CUDA: return "CUDA runtime error";
+    case HP_ERR_BOUNDS: return "device: page id or length out of range";
+    case HP_ERR_DEVICE_TIMEOUT: return "device: bounded wait ran out";
+    }
+    return "unknown status";
+}
+
+int32_t hp_build_arch(void) { return 103; }
+int32_t hp_abi_version(void) { return kAbiVersion; }
+
+hp_status hp_merge_states(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
+                          void *o_out, hp_dtype out_dt, float *lse_out, int64_t rows, int32_t d,
+                          hp_stream_t stream)
+{
+    if (rows < 0 || d < 1 || (out_dt != HP_BF16 && out_dt != HP_F32))
+        return HP_ERR_ARG;
+    if (rows == 0)
+        return HP_OK;
+    if (!o_a || !lse_a || !o_b || !lse_b || !o_out)
+        return HP_ERR_ARG;
+    cudaError_t e = launch_merge2(o_a, lse_a, o_b, lse_b, o_out, out_dt == HP_F32, lse_out, rows, d,
+                                  reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
+
+size_t hp_suffix_workspace_bytes(int32_t B, int32_t Hq, int32_t d, int32_t pt_stride, int32_t page_size)
+{
+    if (B < 1 || Hq < 1 || !supported_d(d) || pt_stride < 1 || page_size < 16)
+        return 0;
+    const int max_len = pt_stride * page_size;
+    const int split = suffix_split_len(B, Hq, max_len, device_sms());
+    const int64_t n_split = ceil_div(max_len, split);
+    return ws_layout((int64_t)B * Hq * n_split, d).total;
+}
+
+hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int32_t B, const void *k_pool,
+                                 const void *v_pool, int32_t num_pages, int32_t page_size,
+                                 const int32_t *page_table, int32_t pt_stride, const int32_t *seq_lens,
+                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void *out, hp_dtype out_dt,
+                                 int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
+                                 size_t ws_bytes, hp_stream_t stream)
+{
+    if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out || !ws)
+        return HP_ERR_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || num_pages < 1 || pt_stride < 1 || !std::isfinite(scale))
+        return HP_ERR_ARG;
+    if (!supported_d(d) || page_size < 16 || page_size > 256 || page_size % 16 || Hq / Hkv > kSmallRows)
+        return HP_ERR_UNSUPPORTED;
+    if (!q_layout_ok(q, q_sb, q_sh) || !out_layout_ok(out, out_dt, o_sb, o_sh, d) || !aligned(k_pool, 16) ||
+        !aligned(v_pool, 16))
+        return HP_ERR_UNSUPPORTED;
+    if ((int64_t)pt_stride * page_size > INT32_MAX)
+        return HP_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    const int max_len = pt_stride * page_size;
+    const int sms = device_sms();
+    const int split = suffix_split_len(B, Hq, max_len, sms);
+    const int n_split = (int)ceil_div(max_len, split);
+    const WsLayout wl = ws_layout((int64_t)B * Hq * n_split, d);
+    if (ws_bytes < wl.total || !aligned(ws, 256))
+        return HP_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+
+    SmallParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    if (!encode_pool_map(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, kChunk) ||
+        !encode_pool_map(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, kChunk))
+        return HP_ERR_CUDA;
+    sp.q = static_cast<const uint16_t *>(q);
+    sp.q_sb = q_sb;
+    sp.q_sh = q_sh;
+    sp.G = G;
+    sp.Hkv = Hkv;
+    sp.scale_log2 = scale * kLog2e;
+    sp.plan = nullptr;
+    sp.n_items = B * Hkv * n_split;
+    sp.page_table = page_table;
+    sp.pt_stride = pt_stride;
+    sp.seq_lens = seq_lens;
+    sp.B = B;
+    sp.num_pages = num_pages;
+    sp.page_size = page_size;
+    sp.split_len = split;
+    sp.n_split = n_split;
+    sp.seqs_per_item = 1;
+    sp.part_o = reinterpret_cast<float *>(wsb + wl.off_o);
+    sp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
+    sp.status = status_ptr(ws);
+    const int warps = small_warps_per_cta();
+    const int grid = (int)std::min<int64_t>(ceil_div(sp.n_items, warps), (int64_t)sms * 8);
+    if (launch_small(sp, grid, d, s) != cudaSuccess)
+        return HP_ERR_CUDA;
+
+    MergeParams mp;
+    std::memset(&mp, 0, sizeof(mp));
+    mp.part_o = sp.part_o;
+    mp.part_lse = sp.part_lse;
+    mp.d = d;
+    mp.G = G;
+    mp.Hq = Hq;
+    mp.Hkv = Hkv;
+    mp.B = B;
+    mp.mode = 1;
+    mp.seq_lens = seq_lens;
+    mp.split_len = split;
+    mp.n_split = n_split;
+    mp.out = out;
+    mp.out_f32 = out_dt == HP_F32;
+    mp.o_sb = o_sb;
+    mp.o_sh = o_sh;
+    mp.lse = lse;
+    mp.lse_sb = lse_sb;
+    mp.status = status_ptr(ws);
+    return launch_merge(mp, (int64_t)B * Hq, s) == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
+
+size_t hp_prefix_workspace_bytes(int32_t rows, int32_t Hq, int32_t Hkv, int32_t d, int32_t prefix_len)
+{
+    if (rows < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || !supported_d(d) || prefix_len < 0)
+        return 0;
+    const PrefixGeo g = prefix_geo(rows, Hq / Hkv, Hkv, prefix_len, device_sms());
+    return ws_layout(g.part_rows, d).total;
+}
+
+hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_begin, int32_t rows, const void *k,
+                         const void *v, int64_t kv_st, int64_t kv_sh, int32_t prefix_len, int32_t Hq, int32_t Hkv,
+                         int32_t d, float scale, void *out, hp_dtype out_dt, int64_t o_sb, int64_t o_sh,
+                         float *lse, int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream)
+{
+    if (!q || !out || !ws || rows < 1 || row_begin < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || prefix_len < 0 ||
+        !std::isfinite(scale))
+        return HP_ERR_ARG;
+    if (prefix_len > 0 && (!k || !v))
+        return HP_ERR_ARG;
+    if (!supported_d(d) || Hq / Hkv > kTcMaxRows)
+        return HP_ERR_UNSUPPORTED;
+    if (!q_layout_ok(q, q_sb, q_sh) || !out_layout_ok(out, out_dt, o_sb, o_sh, d))
+        return HP_ERR_UNSUPPORTED;
+    if (prefix_len > 0 &&
+        (!aligned(k, 16) || !aligned(v, 16) || kv_st % 8 || kv_sh % 8 || kv_st <= 0 || kv_sh < 0))
+        return HP_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    const int sms = device_sms();
+    const PrefixGeo g = prefix_geo(rows, G, Hkv, prefix_len, sms);
+    const WsLayout wl = ws_layout(g.part_rows, d);
+    if (ws_bytes < wl.total || !aligned(ws, 256))
+        return HP_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+
+    TcParams tp;
+    std::memset(&tp, 0, sizeof(tp));
+    if (g.n_items > 0) {
+        if (!encode_prefix_map(&tp.map_k, k, prefix_len, Hkv, d, kv_st, kv_sh) ||
+            !encode_prefix_map(&tp.map_v, v, prefix_len, Hkv, d, kv_st, kv_sh))
+            return HP_ERR_CUDA;
+        tp.q = static_cast<const uint16_t *>(q);
+        tp.q_sb = q_sb;
+        tp.q_sh = q_sh;
+        tp.G = G;
+        tp.Hkv = Hkv;
+        tp.scale_log2 = scale * kLog2e;
+        tp.plan = nullptr;
+        tp.n_items = g.n_items;
+        tp.imp_row_begin = row_begin;
+        tp.imp_rows = rows;
+        tp.imp_seqs_per_item = g.spi;
+        tp.imp_split_len = g.split_len;
+        tp.imp_n_split = g.n_split;
+        tp.imp_len = prefix_len;
+        tp.part_o = reinterpret_cast<float *>(wsb + wl.off_o);
+        tp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
+        tp.status = status_ptr(ws);
+        if (launch_tc(tp, g.n_items, d, s) != cudaSuccess)
+            return HP_ERR_CUDA;
+    }
+    MergeParams mp;
+    std::memset(&mp, 0, sizeof(mp));
+    mp.part_o = reinterpret_cast<float *>(wsb + wl.off_o);
+    mp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
+    mp.d = d;
+    mp.G = G;
+    mp.Hq = Hq;
+    mp.Hkv = Hkv;
+    mp.B = rows;  // output rows b - row_begin
+    mp.mode = 2;
+    mp.n_split = g.n_split;
+    mp.seqs_per_item = g.spi;
+    mp.row_begin = 0;
+    mp.rows = rows;
+    mp.n_rc = g.n_rc;
+    // rows are addressed relative to row_begin
+    const size_t esz = out_dt == HP_F32 ? 4 : 2;
+    mp.out = static_cast<uint8_t *>(out) + (size_t)row_begin * o_sb * esz;
+    mp.out_f32 = out_dt == HP_F32;
+    mp.o_sb = o_sb;
+    mp.o_sh = o_sh;
+    mp.lse = lse ? lse + (size_t)row_begin * lse_sb : nullptr;
+    mp.lse_sb = lse_sb;
+    mp.status = status_ptr(ws);
+    return launch_merge(mp, (int64_t)rows * Hq, s) == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
+
+size_t hp_cascade_plan_bytes(const hp_tree_desc *desc)
+{
+    HostPlan P;
+    if (build_plan(desc, P, false) != HP_OK)
+        return 0;
+    return (size_t)P.hdr.total_bytes;
+}
+
+hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_bytes, hp_plan_info *info,
+                          hp_stream_t stream)
+{
+    if (!plan_dev || !info)
+        return HP_ERR_ARG;
+    HostPlan P;
+    hp_status st = build_plan(desc, P, true);
+    if (st != HP_OK)
+        return st;
+    PlanHeader &H = P.hdr;
+    if (plan_bytes < (size_t)H.total_bytes || !aligned(plan_dev, 256))
+        return HP_ERR_WORKSPACE;
+    H.tag = new_tag();
+    std::vector<uint8_t> img((size_t)H.total_bytes, 0);
+    std::memcpy(img.data(), &H, sizeof(H));
+    if (!P.maps.empty())
+        std::memcpy(img.data() + H.off_maps, P.maps.data(), sizeof(CUtensorMap) * P.maps.size());
+    if (!P.tc.empty())
+        std::memcpy(img.data() + H.off_tc, P.tc.data(), sizeof(WorkItem) * P.tc.size());
+    if (!P.small.empty())
+        std::memcpy(img.data() + H.off_small, P.small.data(), sizeof(WorkItem) * P.small.size());
+    if (!P.page_ids.empty())
+        std::memcpy(img.data() + H.off_page_ids, P.page_ids.data(), 4 * P.page_ids.size());
+    std::memcpy(img.data() + H.off_merge_ptr, P.merge_ptr.data(), 4 * P.merge_ptr.size());
+    if (!P.merge_idx.empty())
+        std::memcpy(img.data() + H.off_merge_idx, P.merge_idx.data(), 4 * P.merge_idx.size());
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(plan_dev, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return HP_ERR_CUDA;
+    const int sms = desc->num_sms > 0 ? desc->num_sms : device_sms();
+    std::memset(info, 0, sizeof(*info));
+    info->B = H.B;
+    info->Hq = H.Hq;
+    info->Hkv = H.Hkv;
+    info->d = H.d;
+    info->n_tc_items = H.n_tc;
+    info->n_small_items = H.n_small;
+    info->grid_tc = H.n_tc;
+    info->grid_small = (int32_t)std::min<int64_t>(ceil_div(H.n_small, small_warps_per_cta()), (int64_t)sms * 8);
+    info->n_part_rows = H.n_part_rows;
+    info->plan_bytes = H.total_bytes;
+    info->ws_bytes = H.ws_bytes;
+    info->tag = H.tag;
+    return HP_OK;
+}
+
+hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, const void *q, int64_t q_sb,
+                            int64_t q_sh, float scale, void *out, hp_dtype out_dt, int64_t o_sb, int64_t o_sh,
+                            float *lse, int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream)
+{
+    if (!plan_dev || !info || !q || !out || !ws || !std::isfinite(scale))
+        return HP_ERR_ARG;
+    if (info->B < 1 || info->Hq < 1 || info->Hkv < 1 || info->Hq % info->Hkv || !supported_d(info->d))
+        return HP_ERR_ARG;
+    if (!q_layout_ok(q, q_sb, q_sh) || !out_layout_ok(out, out_dt, o_sb, o_sh, info->d))
+        return HP_ERR_UNSUPPORTED;
+    if (ws_bytes < (size_t)info->ws_bytes || !aligned(ws, 256))
+        return HP_ERR_WORKSPACE;
+    const WsLayout wl = ws_layout(info->n_part_rows, info->d);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    const PlanHeader *plan = static_cast<const PlanHeader *>(plan_dev);
+    const int G = info->Hq / info->Hkv;
+    float *part_o = reinterpret_cast<float *>(wsb + wl.off_o);
+    float *part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
+
+    if (info->n_tc_items > 0) {
+        TcParams tp;
+        std::memset(&tp, 0, sizeof(tp));
+        tp.q = static_cast<const uint16_t *>(q);
+        tp.q_sb = q_sb;
+        tp.q_sh = q_sh;
+        tp.G = G;
+        tp.Hkv = info->Hkv;
+        tp.scale_log2 = scale * kLog2e;
+        tp.plan = plan;
+        tp.tag = info->tag;
+        tp.n_items = info->n_tc_items;
+        tp.part_o = part_o;
+        tp.part_lse = part_lse;
+        tp.status = status_ptr(ws);
+        if (launch_tc(tp, info->grid_tc, info->d, s) != cudaSuccess)
+            return HP_ERR_CUDA;
+    }
+    if (info->n_small_items > 0) {
+        SmallParams sp;
+        std::memset(&sp, 0, sizeof(sp));
+        sp.q = static_cast<const uint16_t *>(q);
+        sp.q_sb = q_sb;
+        sp.q_sh = q_sh;
+        sp.G = G;
+        sp.Hkv = info->Hkv;
+        sp.scale_log2 = scale * kLog2e;
+        sp.plan = plan;
+        sp.tag = info->tag;
+        sp.n_items = info->n_small_items;
+        sp.part_o = part_o;
+        sp.part_lse = part_lse;
+        sp.status = status_ptr(ws);
+        if (launch_small(sp, info->grid_small, info->d, s) != cudaSuccess)
+            return HP_ERR_CUDA;
+    }
+    MergeParams mp;
+    std::memset(&mp, 0, sizeof(mp));
+    mp.part_o = part_o;
+    mp.part_lse = part_lse;
+    mp.d = info->d;
+    mp.G = G;
+    mp.Hq = info->Hq;
+    mp.Hkv = info->Hkv;
+    mp.B = info->B;
+    mp.plan = plan;
+    mp.tag = info->tag;
+    mp.out = out;
+    mp.out_f32 = out_dt == HP_F32;
+    mp.o_sb = o_sb;
+    mp.o_sh = o_sh;
+    mp.lse = lse;
+    mp.lse_sb = lse_sb;
+    mp.status = status_ptr(ws);
+    return launch_merge(mp, (int64_t)info->B * info->Hq, s) == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
+
+int32_t hp_cascade_contexts(const hp_tree_desc *desc, int32_t *out, int32_t cap)
+{
+    if (validate_desc(desc) != HP_OK)
+        return -1;
+    std::vector<int32_t> ctx;
+    build_contexts(desc, ctx);
+    const int32_t n = (int32_t)(ctx.size() / 5);
+    if (out)
+        std::memcpy(out, ctx.data(), sizeof(int32_t) * 5 * (size_t)std::min(n, std::max(cap, 0)));
+    return n;
+}
+
+int32_t hp_cascade_plan_stats(const hp_tree_desc *desc, int64_t *stats4)
+{
+    HostPlan P;
+    if (!stats4 || build_plan(desc, P, false) != HP_OK)
+        return -1;
+    stats4[0] = P.hdr.n_tc;
+    stats4[1] = P.hdr.n_small;
+    stats4[2] = P.hdr.n_part_rows;
+    stats4[3] = P.hdr.n_merge;
+    return 0;
+}
+
+hp_status hp_read_device_status(void *ws, hp_stream_t stream)
+{
+    if (!ws)
+        return HP_ERR_ARG;
+    uint32_t word = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(ws, 0, sizeof(word), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return HP_ERR_CUDA;
+    if (word & kStTimeout)
+        return HP_ERR_DEVICE_TIMEOUT;
+    if (word & kStBounds)
+        return HP_ERR_BOUNDS;
+    if (word & kStPlan)
+        return HP_ERR_ARG;
+    return HP_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,178 @@
+// hp_merge_kernel.cu -- exact log-sum-exp merge of partial attention states.
+//
+// Each output row (b, h) has a fixed, ordered list of partial states
+// (O_i normalised over its own keys, LSE_i); the merge is Hydragen Eq. 5
+// applied to all of them at once in its max-subtracted form (combine_lse):
+//   M = max_i LSE_i;  w_i = e^(LSE_i - M);  O = sum_i w_i O_i / sum_i w_i;
+//   LSE = M + ln sum_i w_i.
+// An empty part has LSE = -inf and weight exactly 0; a row with no parts, or
+// only empty ones, gets O = 0 and LSE = -inf.  The order of the parts is
+// fixed by the plan, so results are deterministic.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "hp_internal.h"
+#include "hp_ptx.cuh"
+
+namespace hp {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMergeWarps = 4;
+
+// Partial row of entry e of output row (b, h); returns -1 past the end.
+struct PartList {
+    int n;
+    int base;    // plan mode: CSR begin
+    int b, kvh, g;
+};
+
+__device__ __forceinline__ int part_row(const MergeParams &p, const PartList &L, int e)
+{
+    if (p.plan != nullptr)
+        return __ldg(plan_array<int32_t>(p.plan, p.plan->off_merge_idx) + L.base + e) + L.g;
+    if (p.mode == 1)
+        return ((L.b * p.Hkv + L.kvh) * p.n_split + e) * p.G + L.g;
+    // mode 2: contiguous prefix items (rc, kvh, split), rows (s, g)
+    const int rel = L.b - p.row_begin;
+    const int rc = rel / p.seqs_per_item, sl = rel % p.seqs_per_item;
+    return (((rc * p.Hkv + L.kvh) * p.n_split + e) * p.seqs_per_item + sl) * p.G + L.g;
+}
+
+template <int VPT>  // values per lane: d / 32
+__global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeParams p)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * kMergeWarps + warp;
+    const int64_t n_rows = (int64_t)p.B * p.Hq;
+    if (row >= n_rows)
+        return;
+    PartList L;
+    L.b = (int)(row / p.Hq);
+    const int h = (int)(row % p.Hq);
+    L.kvh = h / p.G;
+    L.g = h % p.G;
+    if (p.plan != nullptr) {
+        if (p.plan->magic != kPlanMagic || p.plan->tag != p.tag) {
+            if (lane == 0)
+                atomicOr(p.status, kStPlan);
+            return;
+        }
+        const int32_t *mptr = plan_array<int32_t>(p.plan, p.plan->off_merge_ptr);
+        L.base = __ldg(mptr + L.b * p.Hkv + L.kvh);
+        L.n = __ldg(mptr + L.b * p.Hkv + L.kvh + 1) - L.base;
+    } else if (p.mode == 1) {
+        int len = __ldg(p.seq_lens + L.b);
+        len = max(0, len);
+        L.n = min(p.n_split, (len + p.split_len - 1) / p.split_len);
+        L.base = 0;
+    } else {
+        L.n = p.n_split;
+        L.base = 0;
+    }
+    // pass 1: the largest LSE
+    float M = -INFINITY;
+    for (int e = lane; e < L.n; e += 32)
+        M = fmaxf(M, __ldg(p.part_lse + part_row(p, L, e)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // pass 2: weighted sum in the fixed part order
+    float acc[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+        acc[i] = 0.f;
+    float den = 0.f;
+    if (M != -INFINITY) {
+        for (int e = 0; e < L.n; ++e) {
+            const int pr = part_row(p, L, e);
+            const float w = fast_exp2((__ldg(p.part_lse + pr) - M) * kLog2e);
+            den += w;
+            const float *src = p.part_o + (size_t)pr * p.d + lane * VPT;
+            if (VPT == 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+                acc[0] += w * v.x;
+                acc[1] += w * v.y;
+                acc[2] += w * v.z;
+                acc[3] += w * v.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < VPT; ++i)
+                    acc[i] += w * __ldg(src + i);
+            }
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int64_t off = (int64_t)L.b * p.o_sb + (int64_t)h * p.o_sh + lane * VPT;
+    if (p.out_f32) {
+        float *dst = reinterpret_cast<float *>(p.out) + off;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+            dst[i] = acc[i] * inv;
+    } else {
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + off;
+#pragma unroll
+        for (int i = 0; i < VPT; i += 2)
+            *reinterpret_cast<__nv_bfloat162 *>(dst + i) = __floats2bfloat162_rn(acc[i] * inv, acc[i + 1] * inv);
+    }
+    if (lane == 0 && p.lse != nullptr)
+        p.lse[(int64_t)L.b * p.lse_sb + h] = den > 0.f ? M + __logf(den) : -INFINITY;
+}
+
+// Two-state merge of arbitrary d: one warp per row.
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    hp_merge2_kernel(const float *oa, const float *la, const float *ob, const float *lb, void *o, int out_f32,
+                     float *lse, int64_t rows, int d)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * kMergeWarps + warp;
+    if (r >= rows)
+        return;
+    const float A = la[r], Bv = lb[r];
+    const float M = fmaxf(A, Bv);
+    float wa = 0.f, wb = 0.f;
+    if (M != -INFINITY) {
+        wa = fast_exp2((A - M) * kLog2e);
+        wb = fast_exp2((Bv - M) * kLog2e);
+    }
+    const float den = wa + wb;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    // every lane reads its inputs before any lane writes (in-place merges)
+    for (int i = lane; i < d; i += 32) {
+        const float x = oa[r * d + i], y = ob[r * d + i];
+        const float v = (wa * x + wb * y) * inv;
+        if (out_f32)
+            reinterpret_cast<float *>(o)[r * d + i] = v;
+        else
+            reinterpret_cast<__nv_bfloat16 *>(o)[r * d + i] = __float2bfloat16_rn(v);
+    }
+    if (lane == 0 && lse != nullptr)
+        lse[r] = den > 0.f ? M + __logf(den) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams &p, int64_t out_rows, cudaStream_t s)
+{
+    if (out_rows <= 0)
+        return cudaSuccess;
+    const int64_t grid = (out_rows + kMergeWarps - 1) / kMergeWarps;
+    if (p.d == 128)
+        hp_merge_kernel<4><<<(unsigned)grid, kMergeWarps * 32, 0, s>>>(p);
+    else
+        hp_merge_kernel<2><<<(unsigned)grid, kMergeWarps * 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge2(const float *oa, const float *la, const float *ob, const float *lb, void *o,
+                          int out_f32, float *lse, int64_t rows, int d, cudaStream_t s)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    const int64_t grid = (rows + kMergeWarps - 1) / kMergeWarps;
+    hp_merge2_kernel<<<(unsigned)grid, kMergeWarps * 32, 0, s>>>(oa, la, ob, lb, o, out_f32, lse, rows, d);
+    return cudaGetLastError();
+}
+
+}  // namespace hp

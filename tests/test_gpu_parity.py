@@ -1,0 +1,390 @@
+"""GPU parity: every entry point of the C ABI against the fp64 oracle on the
+same seeded inputs.
+
+Tolerances: O max-abs <= 2e-2 and mean-abs <= 2e-3, LSE abs <= 1e-3 for bf16
+inputs (the stated accuracy bar); merge of f32 states within f32 rounding;
+index probes bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from shared_prefix_decode_gb300 import binding as hb
+from shared_prefix_decode_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_ABS = 2e-2, 2e-3, 1e-3
+DEV = "cuda"
+
+
+def _check(out, lse, O, L, what=""):
+    o = out.double().cpu().numpy().reshape(O.shape)
+    l = lse.double().cpu().numpy().reshape(L.shape)
+    fin = np.isfinite(L)
+    assert np.array_equal(np.isfinite(l), fin), f"{what}: empty rows differ"
+    assert np.all(l[~fin] == -np.inf) and np.all(o[~fin] == 0), f"{what}: empty rows must be (0, -inf)"
+    d_o = np.abs(o - O)
+    d_l = np.abs(l[fin] - L[fin]) if fin.any() else np.zeros(1)
+    assert d_o.max() <= O_MAX, f"{what}: max|dO| {d_o.max():.3g}"
+    assert d_o.mean() <= O_MEAN, f"{what}: mean|dO| {d_o.mean():.3g}"
+    assert d_l.max() <= LSE_ABS, f"{what}: max|dLSE| {d_l.max():.3g}"
+    return float(d_o.max()), float(d_l.max())
+
+
+def _status_ok(ws):
+    torch.cuda.synchronize()
+    assert hb.hp_read_device_status(ws) == hb.HP_OK
+
+
+# ------------------------------------------------------------------ merge
+@pytest.mark.parametrize("d", [64, 128, 100])
+def test_merge_states(d):
+    g = torch.Generator().manual_seed(d)
+    rows = 1000
+    oa, ob = torch.randn(rows, d, generator=g), torch.randn(rows, d, generator=g)
+    la, lb = torch.randn(rows, generator=g) * 5, torch.randn(rows, generator=g) * 5
+    la[:10] = -math.inf          # first part empty
+    lb[10:20] = -math.inf        # second part empty
+    la[20:25] = lb[20:25] = -math.inf  # both empty
+    lb[25:30] = la[25:30] + 80   # far apart
+    O, L = oracle.merge(oa.numpy(), la.numpy(), ob.numpy(), lb.numpy())
+    out, lse = hb.hp_merge_states(oa.to(DEV), la.to(DEV), ob.to(DEV), lb.to(DEV))
+    o, l = out.cpu().double().numpy(), lse.cpu().double().numpy()
+    np.testing.assert_allclose(o, O, atol=2e-6, rtol=1e-5)
+    fin = np.isfinite(L)
+    np.testing.assert_allclose(l[fin], L[fin], atol=2e-5)
+    assert np.all(l[~fin] == -np.inf) and np.all(o[~fin] == 0)
+    # in place, and bf16 output
+    oa_d = oa.to(DEV)
+    hb.hp_merge_states(oa_d, la.to(DEV), ob.to(DEV), lb.to(DEV), out=oa_d)
+    np.testing.assert_allclose(oa_d.cpu().double().numpy(), O, atol=2e-6, rtol=1e-5)
+    ob16, _ = hb.hp_merge_states(oa.to(DEV), la.to(DEV), ob.to(DEV), lb.to(DEV), out_dtype=torch.bfloat16)
+    np.testing.assert_allclose(ob16.cpu().double().numpy(), O, atol=2e-2)
+
+
+# ---------------------------------------------------- paged decode (suffix)
+def _paged_case(name, seed, **kw):
+    wl = W.make_config(name, seed=seed, **kw)
+    pt, sl = W.full_page_tables(wl)
+    return wl, pt, sl
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", {}),
+    ("llama3_8b", dict(B=6, prefix=256)),
+    ("codellama13b", dict(B=3, prefix=128)),
+    ("tree2", dict(B=16, prefix=256)),
+    ("no_sharing", dict(B=4, prefix=300)),
+])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_suffix_decode_paged(name, kw, seed):
+    wl, pt, sl = _paged_case(name, seed, **kw)
+    O, L = oracle.paged_decode(wl.q, wl.k_pool, wl.v_pool, pt, sl, wl.scale)
+    wg = wl.to(DEV)
+    ws = hb.alloc_workspace(hb.suffix_workspace_bytes(wl.B, wl.Hq, wl.d, pt.shape[1], wl.page_size), DEV)
+    out, lse = hb.hp_suffix_decode_paged(wg.q, wg.k_pool, wg.v_pool, pt.to(DEV), sl.to(DEV), wl.scale,
+                                         ws=ws, out_dtype=torch.float32)
+    _status_ok(ws)
+    _check(out, lse, O, L, f"paged {name}")
+
+
+def test_suffix_decode_edge_lengths():
+    """Lengths 0, 1, 15, 16, 17, a full table, and a page table wider than
+    needed; G = 4 and d = 128."""
+    lens = [0, 1, 15, 16, 17, 33, 64, 127]
+    wl = W.build_cascade("e", B=len(lens), Hq=8, Hkv=2, d=128, page_size=16, shared=[],
+                         suffix_lens=lens, seed=3)
+    pt, sl = W.full_page_tables(wl)
+    pt = torch.cat([pt, torch.zeros(pt.shape[0], 3, dtype=torch.int32)], 1)
+    O, L = oracle.paged_decode(wl.q, wl.k_pool, wl.v_pool, pt, sl, wl.scale)
+    wg = wl.to(DEV)
+    out, lse = hb.hp_suffix_decode_paged(wg.q, wg.k_pool, wg.v_pool, pt.to(DEV), sl.to(DEV), wl.scale,
+                                         out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _check(out, lse, O, L, "edge lengths")
+
+
+def test_suffix_decode_bad_page_sets_bounds_status():
+    wl = W.build_cascade("x", B=2, Hq=4, Hkv=1, d=64, page_size=16, shared=[], suffix_lens=[40, 20], seed=1)
+    pt, sl = W.full_page_tables(wl)
+    pt[0, 1] = wl.num_pages + 5  # out of range
+    wg = wl.to(DEV)
+    ws = hb.alloc_workspace(hb.suffix_workspace_bytes(2, 4, 64, pt.shape[1], 16), DEV)
+    out, lse = hb.hp_suffix_decode_paged(wg.q, wg.k_pool, wg.v_pool, pt.to(DEV), sl.to(DEV), wl.scale, ws=ws)
+    torch.cuda.synchronize()
+    assert hb.hp_read_device_status(ws) == hb.HP_ERR_BOUNDS
+    assert torch.isfinite(out.float()).all()
+    # sequence 1 is untouched by the bad page
+    O, L = oracle.paged_decode(wl.q[1:], wl.k_pool, wl.v_pool, pt[1:], sl[1:], wl.scale)
+    _check(out[1:], lse[1:], O, L, "bounds: clean row")
+    # the status word was cleared by the read
+    assert hb.hp_read_device_status(ws) == hb.HP_OK
+
+
+# ---------------------------------------------------- contiguous prefix
+def _contig_prefix(wl):
+    ids = wl.levels[0].page_ids.long()
+    kv_len = int(wl.levels[0].nodes[0, 2])
+    k = wl.k_pool[ids].permute(0, 2, 1, 3).reshape(-1, wl.Hkv, wl.d)[:kv_len].contiguous()
+    v = wl.v_pool[ids].permute(0, 2, 1, 3).reshape(-1, wl.Hkv, wl.d)[:kv_len].contiguous()
+    return k, v
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,B,P", [
+    (4, 1, 64, 4, 256),      # GQA 4, 16 rows
+    (32, 8, 128, 64, 4096),  # Llama-3-8B shape, 256 rows per KV head
+    (32, 8, 128, 10, 1000),  # ragged tail tile, 40 rows
+    (8, 8, 128, 300, 384),   # MHA, 300 rows -> two row chunks
+    (16, 2, 64, 33, 130),    # G = 8, d = 64, tail of 2 keys
+])
+def test_prefix_attn(Hq, Hkv, d, B, P):
+    g = torch.Generator().manual_seed(B + P)
+    q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(P, Hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(P, Hkv, d, generator=g).to(torch.bfloat16)
+    scale = 1 / math.sqrt(d)
+    O, L = oracle.prefix(q, k, v, scale)
+    out, lse = hb.hp_prefix_attn(q.to(DEV), k.to(DEV), v.to(DEV), scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _check(out, lse, O, L, f"prefix {Hq}/{Hkv}/{d} B={B} P={P}")
+
+
+def test_prefix_attn_row_window_and_strides():
+    """rows [3, 3+20) only; K/V as a strided view of a wider [len][2*Hkv][d]."""
+    g = torch.Generator().manual_seed(5)
+    B, Hq, Hkv, d, P = 30, 8, 2, 128, 640
+    q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16)
+    kw = torch.randn(P, 2 * Hkv, d, generator=g).to(torch.bfloat16)
+    vw = torch.randn(P, 2 * Hkv, d, generator=g).to(torch.bfloat16)
+    k, v = kw[:, ::2], vw[:, ::2]
+    O, L = oracle.prefix(q[3:23], k.contiguous(), v.contiguous(), 0.1)
+    out = torch.full((B, Hq, d), 7.0, device=DEV)
+    lse = torch.full((B, Hq), 7.0, device=DEV)
+    kd, vd = kw.to(DEV)[:, ::2], vw.to(DEV)[:, ::2]
+    hb.hp_prefix_attn(q.to(DEV), kd, vd, 0.1, row_begin=3, rows=20, out=out, lse=lse)
+    torch.cuda.synchronize()
+    _check(out[3:23], lse[3:23], O, L, "row window")
+    assert torch.all(out[:3] == 7.0) and torch.all(out[23:] == 7.0)
+
+
+def test_prefix_attn_empty_prefix():
+    q = torch.randn(4, 4, 64).to(torch.bfloat16).to(DEV)
+    k = torch.zeros(0, 1, 64, dtype=torch.bfloat16, device=DEV)
+    out, lse = hb.hp_prefix_attn(q, k, k, 0.125, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(lse == -math.inf)
+
+
+# ------------------------------------------------------------- cascade
+SMALL_CASES = [
+    ("tiny", {}),
+    ("llama3_8b", dict(B=8, prefix=512)),
+    ("codellama13b", dict(B=12, prefix=384)),
+    ("tree2", dict(B=32, prefix=256)),
+    ("doc_streams", dict(B=20, prefix=640)),
+    ("no_sharing", dict(B=6, prefix=200)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL_CASES)
+@pytest.mark.parametrize("seed", [0, 1, 2, 3, 4])
+def test_cascade_small(name, kw, seed):
+    wl = W.make_config(name, seed=seed, **kw)
+    O, L = oracle.cascade(wl)
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    out, lse = plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
+    _status_ok(plan.ws)
+    _check(out, lse, O, L, f"cascade {name} seed {seed}")
+
+
+def test_cascade_llama3_full_all_rows():
+    """The benchmarked workload at full size: B=64, 32/8 heads, d=128, 4K
+    prefix, suffixes U[1,256], shuffled 16-token pages; every output row."""
+    for seed in (0, 1):
+        wl = W.make_config("llama3_8b", seed=seed)
+        O, L = oracle.cascade(wl)
+        wg = wl.to(DEV)
+        plan = hb.CascadePlan.from_workload(wg)
+        out, lse = plan.decode(wg.q, wl.scale)  # bf16 output, as benchmarked
+        _status_ok(plan.ws)
+        _check(out, lse, O, L, f"llama3 full seed {seed}")
+
+
+def _sample_rows(wl, n, seed):
+    g = torch.Generator().manual_seed(seed)
+    bs = torch.randint(0, wl.B, (n,), generator=g).tolist()
+    hs = torch.randint(0, wl.Hq, (n,), generator=g).tolist()
+    rows = sorted(set(zip(bs, hs)) | {(0, 0), (wl.B - 1, wl.Hq - 1)})
+    return rows
+
+
+@pytest.mark.parametrize("name", ["codellama13b", "tree2", "doc_streams", "no_sharing"])
+def test_cascade_full_size_sampled(name):
+    wl = W.make_config(name, seed=0)
+    rows = _sample_rows(wl, 96, 7)
+    O, L = oracle.cascade(wl, rows)
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    out, lse = plan.decode(wg.q, wl.scale)
+    _status_ok(plan.ws)
+    idx_b = torch.tensor([r[0] for r in rows])
+    idx_h = torch.tensor([r[1] for r in rows])
+    _check(out.cpu()[idx_b, idx_h], lse.cpu()[idx_b, idx_h], O, L, f"{name} full sampled")
+    # property at any size: every row is finite and its LSE at least the
+    # largest single score bound log(1) for a non-empty key set is finite
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+# ------------------------------------------------- bit-exact index probes
+def _probe_targets(wl, where):
+    n = wl.seq_kv_len()
+    ps = wl.page_size
+    tg = []
+    for b in range(wl.B):
+        if where == "first":
+            t = 0 if b == 0 else None
+        elif where == "last":
+            t = n[b] - 1
+        elif where == "page_edge":
+            t = min(n[b] - 1, (b % max(1, n[b] // ps)) * ps + (ps - 1 if b % 2 else 0))
+        else:
+            raise ValueError(where)
+        tg.append(t)
+    return tg
+
+
+def _distinct_targets(wl, seed):
+    """One target per sequence, spread over every level; targets inside a
+    shared node are distinct tokens so no two sequences' probes collide."""
+    g = torch.Generator().manual_seed(seed)
+    n = wl.seq_kv_len()
+    used = set()
+    tg = []
+    for b in range(wl.B):
+        for _ in range(1000):
+            t = int(torch.randint(0, n[b], (1,), generator=g))
+            # locate (level, node) to test collision on shared tokens
+            off, key = t, None
+            for li, lv in enumerate(wl.levels):
+                hit = [(i, nd) for i, nd in enumerate(lv.nodes.tolist()) if nd[0] <= b < nd[1]]
+                if not hit:
+                    continue
+                i, nd = hit[0]
+                if off < nd[2]:
+                    key = (li, i, off)
+                    break
+                off -= nd[2]
+            if key not in used:
+                used.add(key)
+                tg.append(t)
+                break
+    return tg
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", {}),
+    ("llama3_8b", dict(B=16, prefix=512)),
+    ("tree2", dict(B=32, prefix=256)),
+    ("codellama13b", dict(B=8, prefix=256)),
+])
+@pytest.mark.parametrize("mode", ["random", "last", "page_edge"])
+def test_probe_bit_exact(name, kw, mode):
+    wl = W.make_config(name, seed=11, **kw)
+    if mode == "random":
+        tg = _distinct_targets(wl, 3)
+    else:
+        tg = _probe_targets(wl, mode)
+        if mode == "last" or mode == "page_edge":
+            # make shared-node collisions impossible: fall back to distinct
+            # random targets for sequences whose pick lands in a shared node
+            # already used
+            try:
+                W.apply_probe(W.make_config(name, seed=11, **kw), tg)
+            except ValueError:
+                tg = _distinct_targets(wl, 5)
+    W.apply_probe(wl, tg)
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    out, lse = plan.decode(wg.q, wl.scale)  # bf16 output
+    _status_ok(plan.ws)
+    out = out.cpu()
+    for b in range(wl.B):
+        want = W.probe_expected(b, wl.d)
+        got = out[b]
+        bad = (got.view(torch.int16) != want.view(torch.int16)[None, :]).any(dim=1)
+        assert not bad.any(), f"{name} {mode}: sequence {b} (target {tg[b]}) heads {bad.nonzero().flatten().tolist()}"
+
+
+def test_probe_bit_exact_paged_decode():
+    wl = W.make_config("llama3_8b", seed=2, B=8, prefix=256)
+    W.apply_probe(wl, _distinct_targets(wl, 9))
+    pt, sl = W.full_page_tables(wl)
+    wg = wl.to(DEV)
+    out, _ = hb.hp_suffix_decode_paged(wg.q, wg.k_pool, wg.v_pool, pt.to(DEV), sl.to(DEV), wl.scale)
+    torch.cuda.synchronize()
+    out = out.cpu()
+    for b in range(wl.B):
+        assert torch.equal(out[b].view(torch.int16), W.probe_expected(b, wl.d).view(torch.int16)[None].expand(wl.Hq, -1))
+
+
+# -------------------------------------------- determinism, graphs, plans
+def test_cascade_deterministic_and_graph_replay():
+    wl = W.make_config("llama3_8b", seed=4, B=16, prefix=1024)
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    o1, l1 = plan.decode(wg.q, wl.scale)
+    o2, l2 = plan.decode(wg.q, wl.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    out = torch.empty_like(o1)
+    lse = torch.empty_like(l1)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.decode(wg.q, wl.scale, out=out, lse=lse)  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        plan.decode(wg.q, wl.scale, out=out, lse=lse)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, o1) and torch.equal(lse, l1)
+    # new queries in the same buffer, replay again
+    wg.q.copy_(torch.randn_like(wg.q, dtype=torch.float32).to(torch.bfloat16))
+    g.replay()
+    o3, l3 = plan.decode(wg.q, wl.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o3) and torch.equal(lse, l3)
+
+
+def test_cascade_stale_plan_info_is_reported():
+    wl = W.make_config("tiny", seed=0)
+    wg = wl.to(DEV)
+    p1 = hb.CascadePlan.from_workload(wg)
+    p2 = hb.CascadePlan.from_workload(wg)
+    p1.info.tag = p2.info.tag  # info of another plan
+    p1.decode(wg.q, wl.scale)
+    torch.cuda.synchronize()
+    assert hb.hp_read_device_status(p1.ws) == hb.HP_ERR_ARG
+
+
+def test_cascade_matches_naive_per_sequence_decode():
+    """The cascade result equals per-sequence paged decode over the whole
+    context (the prefix re-read per sequence), within the same tolerance."""
+    wl = W.make_config("llama3_8b", seed=3, B=16, prefix=1024)
+    pt, sl = W.full_page_tables(wl)
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    oc, lc = plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
+    on, ln = hb.hp_suffix_decode_paged(wg.q, wg.k_pool, wg.v_pool, pt.to(DEV), sl.to(DEV), wl.scale,
+                                       out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert (oc - on).abs().max().item() <= O_MAX
+    assert (lc - ln).abs().max().item() <= LSE_ABS

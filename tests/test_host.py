@@ -1,0 +1,150 @@
+"""Host-side tests (no GPU): the C-ABI library loads and exports every symbol
+include/hp.h declares; the tree planner reproduces the pages' context list and
+rejects invalid trees before any launch."""
+import json
+import os
+import re
+
+import pytest
+import torch
+
+from shared_prefix_decode_gb300 import binding as hb
+from shared_prefix_decode_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "hp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(hp_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = hb.library()
+    declared = _header_functions()
+    assert len(declared) >= 14
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in hp.h but not exported"
+    assert set(declared) == set(hb.exported_symbols())
+    assert lib.hp_build_arch() == 103
+    assert lib.hp_abi_version() == 1
+
+
+def test_status_strings():
+    assert hb.status_str(0) == "ok"
+    for s in range(1, 7):
+        assert hb.status_str(s) and hb.status_str(s) != "unknown status"
+
+
+def _pool():
+    # a host buffer stands in for the pools: planning reads no pool memory
+    return torch.zeros(64, dtype=torch.uint8)
+
+
+def _fig2_levels(pool, ps=16):
+    """ChunkAttention's Figure 2 tree as levels of chunk nodes, one page each."""
+    g = json.load(open(os.path.join(GOLDEN, "chunkattention_fig2_contexts.json")))
+    chunks = g["tree"]["chunks"]
+
+    def depth(c):
+        d = 0
+        while chunks[c]["parent"] is not None:
+            c = chunks[c]["parent"]
+            d += 1
+        return d
+
+    by_level = {}
+    for name, c in chunks.items():
+        by_level.setdefault(depth(name), []).append((name, c["covers"]))
+    levels, names, page = [], {}, 0
+    for lvl in sorted(by_level):
+        nodes, ids = [], []
+        for n, (name, (i, j)) in enumerate(sorted(by_level[lvl], key=lambda x: x[1][0])):
+            nodes.append((i, j, ps, len(ids)))
+            ids.append(page)
+            page += 1
+            names[(lvl, n)] = name
+        levels.append((pool.data_ptr(), pool.data_ptr(), 64, ps, nodes, ids))
+    return g, levels, names
+
+
+def test_chunkattention_fig2_context_list():
+    pool = _pool()
+    g, levels, names = _fig2_levels(pool)
+    ctx = hb.hp_cascade_contexts(levels, B=3, Hq=4, Hkv=4, d=128)
+    got = [[names[(l, n)], i, j] for (l, n, i, j, _) in ctx]
+    assert got == g["contexts"]
+    shared = [names[(l, n)] for (l, n, i, j, batched) in ctx if batched]
+    assert shared == g["shared"]
+    assert all((j - i > 1) == bool(batched) for (_, _, i, j, batched) in ctx)
+
+
+def test_plan_stats_llama3_shape():
+    """B=64 x G=4 rows share the prefix: 256 rows per KV head go to the
+    tensor-core kernel; each sequence's suffix is a small-row item."""
+    wl = W.make_config("llama3_8b", seed=0)
+    levels = hb._levels_of(wl)
+    n_tc, n_small, part_rows, n_merge = hb.hp_cascade_plan_stats(levels, wl.B, wl.Hq, wl.Hkv, wl.d,
+                                                                 num_sms=152)
+    tiles = 8 * (4096 // 128)
+    assert n_tc == tiles // ((tiles + 151) // 152)
+    assert n_small >= wl.B * wl.Hkv
+    # every (b, kvh) merges the prefix splits that cover it plus its suffix splits
+    assert n_merge >= wl.B * wl.Hkv * 2
+    assert part_rows > 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "tree2", "doc_streams", "no_sharing"])
+def test_plan_stats_configs(name):
+    wl = W.make_config(name, seed=1, B=16 if name != "tiny" else None, prefix=512 if name != "tiny" else None)
+    st = hb.hp_cascade_plan_stats(hb._levels_of(wl), wl.B, wl.Hq, wl.Hkv, wl.d, num_sms=152)
+    assert all(x >= 0 for x in st)
+    if name == "no_sharing":
+        assert st[0] == 0
+
+
+def _desc_levels(nodes, ids, num_pages=8, ps=16, pool=None):
+    pool = pool if pool is not None else _pool()
+    return [(pool.data_ptr(), pool.data_ptr(), num_pages, ps, nodes, ids)]
+
+
+@pytest.mark.parametrize("nodes,ids,why", [
+    ([(0, 5, 16, 0)], [0], "seq_end beyond B"),
+    ([(2, 2, 16, 0)], [0], "empty sequence range"),
+    ([(0, 2, 16, 0), (1, 3, 16, 1)], [0, 1], "overlapping nodes in one level"),
+    ([(0, 2, 33, 0)], [0, 1], "page list too short"),
+    ([(0, 2, 16, 0)], [8], "page id beyond the pool"),
+    ([(0, 2, 16, 0)], [-1], "negative page id"),
+    ([(0, 2, -1, 0)], [0], "negative length"),
+])
+def test_invalid_trees_are_rejected_on_the_host(nodes, ids, why):
+    levels = _desc_levels(nodes, ids)
+    assert hb.hp_cascade_plan_bytes(levels, 4, 4, 4, 128, num_sms=152) == 0, why
+    with pytest.raises(hb.HpError):
+        hb.hp_cascade_plan_stats(levels, 4, 4, 4, 128)
+
+
+def test_unsupported_shapes_are_rejected():
+    ok = _desc_levels([(0, 2, 16, 0)], [0])
+    assert hb.hp_cascade_plan_bytes(ok, 4, 4, 4, 128, num_sms=152) > 0
+    assert hb.hp_cascade_plan_bytes(ok, 4, 4, 4, 96, num_sms=152) == 0      # d
+    assert hb.hp_cascade_plan_bytes(ok, 4, 6, 4, 128, num_sms=152) == 0     # Hq % Hkv
+    assert hb.hp_cascade_plan_bytes(_desc_levels([(0, 2, 16, 0)], [0], ps=24), 4, 4, 4, 128,
+                                    num_sms=152) == 0                        # page size
+    assert hb.hp_cascade_plan_bytes(_desc_levels([(0, 2, 0, 0)], []), 4, 4, 4, 128, num_sms=152) > 0
+
+
+def test_zero_length_nodes_make_no_items():
+    levels = _desc_levels([(0, 4, 0, 0)], [])
+    st = hb.hp_cascade_plan_stats(levels, 4, 4, 4, 128)
+    assert st == (0, 0, 0, 0)
+
+
+def test_workspace_sizes_are_positive_and_rejections_are_zero():
+    assert hb.suffix_workspace_bytes(4, 32, 128, 16, 16) >= 256
+    assert hb.suffix_workspace_bytes(4, 32, 96, 16, 16) == 0
+    assert hb.prefix_workspace_bytes(64, 32, 8, 128, 4096) >= 256
+    assert hb.prefix_workspace_bytes(64, 30, 8, 128, 4096) == 0
