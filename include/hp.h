@@ -193,6 +193,17 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
                             int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
                             size_t ws_bytes, hp_stream_t stream);
 
+/* The same step, recording caller-created CUDA events (cudaEvent_t handles;
+ * any may be NULL) on `stream` -- as external event nodes when the stream is
+ * being captured, so they time each replay: events[0] before the shared-node kernel,
+ * events[1] after it, events[2] after the small-row kernel, events[3] after
+ * the merge -- for timing each kernel of the step on its own stream. */
+hp_status hp_cascade_decode_profiled(const void *plan_dev, const hp_plan_info *info, const void *q,
+                                     int64_t q_sb, int64_t q_sh, float scale, void *out,
+                                     hp_dtype out_dt, int64_t o_sb, int64_t o_sh, float *lse,
+                                     int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream,
+                                     void *const *events);
+
 /* Host-side description of a plan for inspection and tests: the (level, node,
  * seq_begin, seq_end, pass) context list in the order the pages list it --
  * shared nodes (more than one sequence; batched pass = 1) level by level,

@@ -62,6 +62,9 @@ _SIGNATURES = {
     "hp_cascade_plan": (c_i32, [ctypes.POINTER(HpTreeDesc), c_vp, c_sz, ctypes.POINTER(HpPlanInfo), c_vp]),
     "hp_cascade_decode": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_i64, c_i64, c_f32, c_vp,
                                   c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz, c_vp]),
+    "hp_cascade_decode_profiled": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_i64, c_i64, c_f32, c_vp,
+                                           c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz, c_vp,
+                                           ctypes.POINTER(c_vp)]),
     "hp_cascade_contexts": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i32), c_i32]),
     "hp_cascade_plan_stats": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i64)]),
     "hp_read_device_status": (c_i32, [c_vp, c_vp]),
@@ -318,6 +321,17 @@ def hp_cascade_decode(plan: CascadePlan, q: torch.Tensor, scale: float, out: Opt
         _dt(out.dtype), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(),
         _stream(stream)), "hp_cascade_decode")
     return out, lse
+
+
+def hp_cascade_decode_profiled(plan: CascadePlan, q: torch.Tensor, scale: float, out: torch.Tensor,
+                               lse: torch.Tensor, events: Sequence[Optional[torch.cuda.Event]],
+                               ws: Optional[torch.Tensor] = None, stream=None) -> None:
+    """hp_cascade_decode that records events[0..3] around its three kernels."""
+    ev = (c_vp * 4)(*[None if e is None else e.cuda_event for e in events])
+    _check(library().hp_cascade_decode_profiled(
+        _ptr(plan.plan), ctypes.byref(plan.info), _ptr(q), q.stride(0), q.stride(1), float(scale), _ptr(out),
+        _dt(out.dtype), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(plan.ws if ws is None else ws),
+        (plan.ws if ws is None else ws).numel(), _stream(stream), ev), "hp_cascade_decode_profiled")
 
 
 def hp_read_device_status(ws: torch.Tensor, stream=None) -> int:

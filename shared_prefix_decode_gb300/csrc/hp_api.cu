@@ -647,10 +647,16 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
     return HP_OK;
 }
 
-hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, const void *q, int64_t q_sb,
-                            int64_t q_sh, float scale, void *out, hp_dtype out_dt, int64_t o_sb, int64_t o_sh,
-                            float *lse, int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream)
+static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *info, const void *q,
+                                     int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,
+                                     int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
+                                     size_t ws_bytes, hp_stream_t stream, void *const *events)
 {
+    auto mark = [&](int i) {
+        if (events && events[i])
+            cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), reinterpret_cast<cudaStream_t>(stream),
+                                     cudaEventRecordExternal);
+    };
     if (!plan_dev || !info || !q || !out || !ws || !std::isfinite(scale))
         return HP_ERR_ARG;
     if (info->B < 1 || info->Hq < 1 || info->Hkv < 1 || info->Hq % info->Hkv || !supported_d(info->d))
@@ -667,6 +673,7 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
     float *part_o = reinterpret_cast<float *>(wsb + wl.off_o);
     float *part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
 
+    mark(0);
     if (info->n_tc_items > 0) {
         TcParams tp;
         std::memset(&tp, 0, sizeof(tp));
@@ -685,6 +692,7 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
         if (launch_tc(tp, info->grid_tc, info->d, s) != cudaSuccess)
             return HP_ERR_CUDA;
     }
+    mark(1);
     if (info->n_small_items > 0) {
         SmallParams sp;
         std::memset(&sp, 0, sizeof(sp));
@@ -703,6 +711,7 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
         if (launch_small(sp, info->grid_small, info->d, s) != cudaSuccess)
             return HP_ERR_CUDA;
     }
+    mark(2);
     MergeParams mp;
     std::memset(&mp, 0, sizeof(mp));
     mp.part_o = part_o;
@@ -721,7 +730,27 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
     mp.lse = lse;
     mp.lse_sb = lse_sb;
     mp.status = status_ptr(ws);
-    return launch_merge(mp, (int64_t)info->B * info->Hq, s) == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+    if (launch_merge(mp, (int64_t)info->B * info->Hq, s) != cudaSuccess)
+        return HP_ERR_CUDA;
+    mark(3);
+    return HP_OK;
+}
+
+hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, const void *q, int64_t q_sb,
+                            int64_t q_sh, float scale, void *out, hp_dtype out_dt, int64_t o_sb, int64_t o_sh,
+                            float *lse, int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream)
+{
+    return cascade_decode_impl(plan_dev, info, q, q_sb, q_sh, scale, out, out_dt, o_sb, o_sh, lse, lse_sb, ws,
+                               ws_bytes, stream, nullptr);
+}
+
+hp_status hp_cascade_decode_profiled(const void *plan_dev, const hp_plan_info *info, const void *q,
+                                     int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,
+                                     int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
+                                     size_t ws_bytes, hp_stream_t stream, void *const *events)
+{
+    return cascade_decode_impl(plan_dev, info, q, q_sb, q_sh, scale, out, out_dt, o_sb, o_sh, lse, lse_sb, ws,
+                               ws_bytes, stream, events);
 }
 
 int32_t hp_cascade_contexts(const hp_tree_desc *desc, int32_t *out, int32_t cap)
