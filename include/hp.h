@@ -101,6 +101,37 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
                                  size_t ws_bytes, hp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * hp_suffix_decode_paged_noalloc -- the same paged decode for callers that
+ * cannot hand the library any device memory of their own: a host program or
+ * plugin that reaches this library only through the C ABI and has no device
+ * allocator, code running where a caching allocator already holds all device
+ * memory so that cudaMalloc would fail, or a latency-critical path that must
+ * not pay for cudaMalloc's implicit synchronisation.  (This entry point has
+ * no counterpart in the papers; it is a deployment convenience.)
+ *
+ * Arguments and results are those of hp_suffix_decode_paged without the
+ * workspace.  Scratch lives in one fixed 16 MiB device array inside the
+ * library, resident on every GPU that loads the library until the process
+ * exits; the call itself allocates and frees nothing.  Each call needs
+ * B*Hq*(d+1)*4 bytes per key split; the call picks splits that fit and
+ * returns HP_ERR_WORKSPACE when even one split per sequence does not
+ * (B*Hq above about 32,000 rows at d = 128).  The first call on each device
+ * looks up the array's device address (a host call made with that device
+ * current); make that first call before any stream capture.  All calls share
+ * the array and it keeps the last call's contents: calls that run at the same
+ * time on the GPU race with each other, so serialise them.  Device bounds
+ * errors are not reported (there is no status word to read back).
+ * ------------------------------------------------------------------------- */
+hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb, int64_t q_sh, int32_t B,
+                                         const void *k_pool, const void *v_pool,
+                                         int32_t num_pages, int32_t page_size,
+                                         const int32_t *page_table, int32_t pt_stride,
+                                         const int32_t *seq_lens, int32_t Hq, int32_t Hkv,
+                                         int32_t d, float scale, void *out, hp_dtype out_dt,
+                                         int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb,
+                                         hp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * hp_prefix_attn -- inter-sequence batched attention against one contiguous
  * shared prefix (Hydragen, "Inter-Sequence Batched Prefix Attention": the
  * queries of sequences [row_begin, row_begin + rows) are stacked and attend

@@ -54,6 +54,9 @@ _SIGNATURES = {
     "hp_suffix_decode_paged": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_i32, c_i32, c_vp, c_i32,
                                        c_vp, c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64, c_i64,
                                        c_vp, c_i64, c_vp, c_sz, c_vp]),
+    "hp_suffix_decode_paged_noalloc": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_i32, c_i32, c_vp,
+                                               c_i32, c_vp, c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64,
+                                               c_i64, c_vp, c_i64, c_vp]),
     "hp_prefix_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "hp_prefix_attn": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_i64, c_i64, c_i32,
                                c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64, c_i64, c_vp, c_i64,

@@ -1,0 +1,206 @@
+// hp_noalloc.cu -- paged decode for callers that cannot allocate device
+// memory.
+//
+// hp_suffix_decode_paged needs a caller-provided workspace for its partial
+// (O, LSE) states.  Some callers have no way to provide one: a host program or
+// plugin that reaches this library only through its C ABI and has no device
+// allocator of its own, code running where a caching allocator already owns
+// all device memory so that cudaMalloc would fail, or a latency-critical path
+// that must not pay for cudaMalloc's implicit device synchronisation.  This
+// file gives them hp_suffix_decode_paged_noalloc, which keeps its scratch in a
+// fixed device array that is part of the library itself.
+//
+// The array below is created when the library's device code is loaded and
+// stays resident on every GPU that loads it until the process exits.  Its
+// device address is looked up once per device (cudaGetSymbolAddress, with
+// that device current) during the first call on that device.  Every call
+// shares the one array, so calls that run at the same time on the GPU (on
+// different streams, or from different host threads) overwrite each other's
+// partial states: serialise them.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "hp_internal.h"
+
+namespace {
+
+// Largest scratch this entry point uses: the device status word plus the
+// partial rows of one call.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+
+static __device__ __align__(256) unsigned char g_hp_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_lock;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set up on the
+// first call per device).  Returns nullptr if the lookup failed.
+void *scratch_on_current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> g(g_setup_lock);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_hp_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_noalloc()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+bool encode_pool(CUtensorMap *m, const void *pool, int num_pages, int Hkv, int ps, int d)
+{
+    auto fn = encode_fn_noalloc();
+    if (!fn)
+        return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)ps * d * 2, (cuuint64_t)Hkv * ps * d * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)hp::kChunk, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool is_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb, int64_t q_sh, int32_t B,
+                                                    const void *k_pool, const void *v_pool, int32_t num_pages,
+                                                    int32_t page_size, const int32_t *page_table,
+                                                    int32_t pt_stride, const int32_t *seq_lens, int32_t Hq,
+                                                    int32_t Hkv, int32_t d, float scale, void *out,
+                                                    hp_dtype out_dt, int64_t o_sb, int64_t o_sh, float *lse,
+                                                    int64_t lse_sb, hp_stream_t stream)
+{
+    using namespace hp;
+    if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out)
+        return HP_ERR_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || num_pages < 1 || pt_stride < 1 || !std::isfinite(scale))
+        return HP_ERR_ARG;
+    if ((d != 64 && d != 128) || page_size < 16 || page_size > 256 || page_size % 16 || Hq / Hkv > kSmallRows)
+        return HP_ERR_UNSUPPORTED;
+    if (out_dt != HP_BF16 && out_dt != HP_F32)
+        return HP_ERR_ARG;
+    const size_t esz = out_dt == HP_F32 ? 4 : 2;
+    const size_t lane_bytes = esz * (size_t)(d / 32);
+    if (!is_aligned(q, 16) || q_sb % 8 || q_sh % 8 || q_sb < 0 || q_sh < 0 || !is_aligned(out, lane_bytes) ||
+        (o_sb * (int64_t)esz) % (int64_t)lane_bytes || (o_sh * (int64_t)esz) % (int64_t)lane_bytes ||
+        !is_aligned(k_pool, 16) || !is_aligned(v_pool, 16))
+        return HP_ERR_UNSUPPORTED;
+    if ((int64_t)pt_stride * page_size > INT32_MAX)
+        return HP_ERR_UNSUPPORTED;
+
+    // Split each sequence into as few key ranges as fit the scratch: at
+    // least 64 keys per range, and no more ranges than the scratch holds.
+    const int max_len = pt_stride * page_size;
+    const size_t per_row = (size_t)(d + 1) * 4;  // partial O row + its LSE
+    const size_t avail = kNoAllocScratchBytes - 2 * kWsHeader;
+    const int64_t rows_per_split = (int64_t)B * Hq;
+    const int64_t max_splits = (int64_t)(avail / per_row) / rows_per_split;
+    if (max_splits < 1)
+        return HP_ERR_WORKSPACE;  // B * Hq partial rows exceed the fixed scratch
+    int64_t split = 64;
+    while (cdiv(max_len, split) > max_splits)
+        split *= 2;
+    const int n_split = (int)cdiv(max_len, split);
+    const int64_t part_rows = rows_per_split * n_split;
+
+    void *scratch = scratch_on_current_device();
+    if (!scratch)
+        return HP_ERR_CUDA;
+    uint8_t *base = static_cast<uint8_t *>(scratch);
+    const size_t off_lse = kWsHeader;
+    const size_t off_o = up(off_lse + (size_t)part_rows * 4, 256);
+    if (off_o + (size_t)part_rows * d * 4 > kNoAllocScratchBytes)
+        return HP_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the status word is the only scratch that must start at zero
+    if (cudaMemsetAsync(base, 0, sizeof(uint32_t), s) != cudaSuccess)
+        return HP_ERR_CUDA;
+
+    SmallParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    if (!encode_pool(&sp.map_k, k_pool, num_pages, Hkv, page_size, d) ||
+        !encode_pool(&sp.map_v, v_pool, num_pages, Hkv, page_size, d))
+        return HP_ERR_CUDA;
+    const int G = Hq / Hkv;
+    sp.q = static_cast<const uint16_t *>(q);
+    sp.q_sb = q_sb;
+    sp.q_sh = q_sh;
+    sp.G = G;
+    sp.Hkv = Hkv;
+    sp.scale_log2 = scale * 1.4426950408889634f;
+    sp.plan = nullptr;
+    sp.n_items = B * Hkv * n_split;
+    sp.page_table = page_table;
+    sp.pt_stride = pt_stride;
+    sp.seq_lens = seq_lens;
+    sp.B = B;
+    sp.num_pages = num_pages;
+    sp.page_size = page_size;
+    sp.split_len = (int)split;
+    sp.n_split = n_split;
+    sp.seqs_per_item = 1;
+    sp.part_o = reinterpret_cast<float *>(base + off_o);
+    sp.part_lse = reinterpret_cast<float *>(base + off_lse);
+    sp.status = reinterpret_cast<uint32_t *>(base);
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = (int)std::min<int64_t>(cdiv(sp.n_items, small_warps_per_cta()), (int64_t)sms * 8);
+    if (launch_small(sp, grid, d, s) != cudaSuccess)
+        return HP_ERR_CUDA;
+
+    MergeParams mp;
+    std::memset(&mp, 0, sizeof(mp));
+    mp.part_o = sp.part_o;
+    mp.part_lse = sp.part_lse;
+    mp.d = d;
+    mp.G = G;
+    mp.Hq = Hq;
+    mp.Hkv = Hkv;
+    mp.B = B;
+    mp.plan = nullptr;
+    mp.mode = 1;
+    mp.seq_lens = seq_lens;
+    mp.split_len = (int)split;
+    mp.n_split = n_split;
+    mp.out = out;
+    mp.out_f32 = out_dt == HP_F32;
+    mp.o_sb = o_sb;
+    mp.o_sh = o_sh;
+    mp.lse = lse;
+    mp.lse_sb = lse_sb;
+    mp.status = sp.status;
+    return launch_merge(mp, (int64_t)B * Hq, s) == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
