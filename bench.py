@@ -15,7 +15,7 @@ max(prefix FLOPs / bf16 peak, unique KV bytes / HBM peak).
 Timing: inputs resident in HBM; the step is a CUDA graph; R distinct input
 sets (own pools, tables, q and plan each) are rotated so that R x working set
 exceeds 3x the L2 size read at run time, which keeps every step's KV cold in
-L2.  CUDA events on the launching stream, W warm-up steps, exactly K timed
+L2; the sets share one workspace (partial states), as a decode loop reuses one.  CUDA events on the launching stream, W warm-up steps, exactly K timed
 steps, barrier + synchronize on both sides, max over ranks.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hp|reference]
@@ -250,6 +250,10 @@ def main():
         sets.append({"wl": wl, "wg": wg, "plan": plan, "out": out, "lse": lse})
     l2_note = (f"rotating {R} input sets, {R * set_bytes / 1e6:.0f} MB >= 3x L2 ({l2 / 2**20:.0f} MiB); "
                f"no flush")
+    # one workspace for every input set, as a decode loop reuses one buffer
+    ws_shared = hb.alloc_workspace(max(s["plan"].info.ws_bytes for s in sets), dev)
+    for s in sets:
+        s["plan"].ws = ws_shared
     info = sets[0]["plan"].info
     kernels_per_step = int(info.n_tc_items > 0) + int(info.n_small_items > 0) + 1
     stream = torch.cuda.Stream(device=dev)

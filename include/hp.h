@@ -20,7 +20,8 @@
  *     dimension is contiguous).  Query head h reads KV head h / (Hq/Hkv).
  *   - paged KV pools: bf16 [num_pages][Hkv][page_size][d], contiguous.  Token t
  *     of a page list sits at page list[t / page_size], slot t % page_size.
- *   - scale: the softmax scale applied to q.k (1/sqrt(d) in the pages).
+ *   - scale: the softmax scale applied to q.k (1/sqrt(d) in the pages); must be
+ *     positive for hp_prefix_attn and hp_cascade_decode (HP_ERR_ARG otherwise).
  *   - out: bf16 or f32, row (b, h) at out + b*o_sb + h*o_sh (elements).
  *   - lse: f32, natural log of the softmax denominator of the scaled scores
  *     (Hydragen's LSE(Q,K)), element (b, h) at lse + b*lse_sb + h.  A row with

@@ -20,6 +20,11 @@ using namespace hp;
 namespace {
 
 constexpr int32_t kAbiVersion = 1;
+// A tensor-core item processes at least this many 128-key tiles (its fixed
+// set-up -- TMEM allocation, Q staging, pipeline fill -- is amortised over
+// them) and at most kMaxTcTiles (its page ids must fit the staging area).
+constexpr int64_t kMinTcTiles = 4;
+constexpr int64_t kMaxTcTiles = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------- utilities
@@ -62,14 +67,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 // Paged pool [num_pages][Hkv][ps][d] bf16, box = 64 columns x box_tok tokens,
 // 128-byte swizzle.
-bool encode_pool_map(CUtensorMap *m, const void *pool, int num_pages, int Hkv, int ps, int d, int box_tok)
+bool encode_pool_map(CUtensorMap *m, const void *pool, int num_pages, int Hkv, int ps, int d, int box_tok,
+                     int box_heads = 1)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
     cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)ps * d * 2, (cuuint64_t)Hkv * ps * d * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)box_tok, 1, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_tok, (cuuint32_t)box_heads, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -112,6 +118,13 @@ bool out_layout_ok(const void *out, hp_dtype dt, int64_t o_sb, int64_t o_sh, int
            (o_sh * (int64_t)esz) % (int64_t)lane_bytes == 0;
 }
 
+// CTAs of the small-row kernel resident per SM (shared memory bound); its
+// grid is one such wave, each warp walking several items.
+int small_ctas_per_sm(int d)
+{
+    return (int)std::max<size_t>(1, std::min<size_t>(4, (size_t)(227 * 1024) / small_smem_bytes(d)));
+}
+
 struct WsLayout {
     size_t off_lse, off_o, total;
 };
@@ -126,10 +139,14 @@ WsLayout ws_layout(int64_t part_rows, int d)
 }
 
 // ------------------------------------------------------ standalone splits
-int suffix_split_len(int B, int Hq, int max_len, int sms)
+// Key split of the standalone paged decode: items are (sequence, KV-head
+// group, split); aim for about three items per resident CTA, at least 64 keys
+// each.
+int suffix_split_len(int B, int Hkv, int max_len, int sms, int d)
 {
-    const int64_t chunks = (int64_t)B * Hq * ceil_div(std::max(max_len, 1), kChunk);
-    const int64_t target = (int64_t)sms * 32;  // ~4 items per warp slot, per head
+    const int nh = small_heads_per_item(Hkv);
+    const int64_t chunks = (int64_t)B * (Hkv / nh) * ceil_div(std::max(max_len, 1), kChunk);
+    const int64_t target = (int64_t)sms * small_ctas_per_sm(d) * 3;
     const int64_t per = std::max<int64_t>(4, ceil_div(chunks, target));
     return (int)(per * kChunk);
 }
@@ -146,7 +163,7 @@ PrefixGeo prefix_geo(int rows, int G, int Hkv, int len, int sms)
     g.spi = std::min(g.spi, std::max(rows, 1));
     g.n_rc = (int)ceil_div(rows, g.spi);
     const int64_t tiles = ceil_div(std::max(len, 1), kTcTile);
-    const int64_t per = std::max<int64_t>(1, ceil_div((int64_t)g.n_rc * Hkv * tiles, sms));
+    const int64_t per = std::max<int64_t>(kMinTcTiles, ceil_div((int64_t)g.n_rc * Hkv * tiles, sms));
     g.split_len = (int)(per * kTcTile);
     g.n_split = len > 0 ? (int)ceil_div(len, g.split_len) : 0;
     g.n_items = g.n_rc * Hkv * g.n_split;
@@ -258,6 +275,8 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     // Split sizes.  Shared (tensor-core) work: total 128-key tiles spread over
     // one wave of CTAs (one per SM).  Small-row work: 16-key chunks spread
     // over ~8 warps per SM.
+    const int nh = small_heads_per_item(d->Hkv);
+    H.small_nh = nh;
     int64_t tc_tiles = 0, small_chunks = 0;
     for (int l = 0; l < d->num_levels; ++l)
         for (int n = 0; n < d->levels[l].num_nodes; ++n) {
@@ -269,11 +288,13 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
                 const int spc = std::max(1, kTcMaxRows / G);
                 tc_tiles += ceil_div(N.seq_end - N.seq_begin, spc) * d->Hkv * ceil_div(N.kv_len, kTcTile);
             } else {
-                small_chunks += (int64_t)d->Hkv * ceil_div(N.kv_len, kChunk);
+                small_chunks += (int64_t)(d->Hkv / nh) * ceil_div(N.kv_len, kChunk);
             }
         }
-    const int64_t tc_split = kTcTile * std::max<int64_t>(1, ceil_div(tc_tiles, sms));
-    const int64_t small_split = kChunk * std::max<int64_t>(4, ceil_div(small_chunks, (int64_t)sms * 8));
+    const int64_t tc_split =
+        kTcTile * std::min(kMaxTcTiles, std::max<int64_t>(kMinTcTiles, ceil_div(tc_tiles, sms)));
+    const int64_t small_split =
+        kChunk * std::max<int64_t>(4, ceil_div(small_chunks, (int64_t)sms * small_ctas_per_sm(d->d) * 3));
 
     // Items and partial rows, level by level; merge lists per (b, kvh).
     std::vector<std::vector<int32_t>> lists((size_t)d->B * d->Hkv);
@@ -288,9 +309,12 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
             const bool tc = (int64_t)nseq * G > kSmallRows;
             const int spc = tc ? std::max(1, kTcMaxRows / G) : nseq;
             const int64_t split = tc ? tc_split : small_split;
+            // tensor-core items take one KV head; small-row items a group of
+            // nh heads whose rows are laid out [head in group][sequence][g]
+            const int hstep = tc ? 1 : nh;
             for (int s0 = N.seq_begin; s0 < N.seq_end; s0 += spc) {
                 const int ns = std::min(spc, N.seq_end - s0);
-                for (int kvh = 0; kvh < d->Hkv; ++kvh)
+                for (int kvh = 0; kvh < d->Hkv; kvh += hstep)
                     for (int64_t k0 = 0; k0 < N.kv_len; k0 += split) {
                         WorkItem w;
                         w.level = l;
@@ -301,9 +325,11 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
                         w.k1 = (int32_t)std::min<int64_t>(k0 + split, N.kv_len);
                         w.page_base = level_page_off[l] + N.page_off;
                         w.part_row = (int32_t)part;
-                        for (int b = s0; b < s0 + ns; ++b)
-                            lists[(size_t)b * d->Hkv + kvh].push_back((int32_t)(part + (int64_t)(b - s0) * G));
-                        part += (int64_t)ns * G;
+                        for (int hw = 0; hw < hstep; ++hw)
+                            for (int b = s0; b < s0 + ns; ++b)
+                                lists[(size_t)b * d->Hkv + kvh + hw].push_back(
+                                    (int32_t)(part + ((int64_t)hw * ns + (b - s0)) * G));
+                        part += (int64_t)ns * G * hstep;
                         (tc ? P.tc : P.small).push_back(w);
                     }
             }
@@ -359,8 +385,8 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
             CUtensorMap *m = &P.maps[(size_t)l * kMapsPerLevel];
             if (!encode_pool_map(m + 0, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, tcb) ||
                 !encode_pool_map(m + 1, L.v_pool, L.num_pages, d->Hkv, L.page_size, d->d, tcb) ||
-                !encode_pool_map(m + 2, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk) ||
-                !encode_pool_map(m + 3, L.v_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk))
+                !encode_pool_map(m + 2, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk, nh) ||
+                !encode_pool_map(m + 3, L.v_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk, nh))
                 return HP_ERR_CUDA;
         }
     }
@@ -418,9 +444,10 @@ size_t hp_suffix_workspace_bytes(int32_t B, int32_t Hq, int32_t d, int32_t pt_st
     if (B < 1 || Hq < 1 || !supported_d(d) || pt_stride < 1 || page_size < 16)
         return 0;
     const int max_len = pt_stride * page_size;
-    const int split = suffix_split_len(B, Hq, max_len, device_sms());
-    const int64_t n_split = ceil_div(max_len, split);
-    return ws_layout((int64_t)B * Hq * n_split, d).total;
+    // the workspace bound assumes the most KV heads per group (Hkv = Hq)
+    const int split = suffix_split_len(B, Hq, max_len, device_sms(), d);
+    const int64_t n_split_max = ceil_div(max_len, std::min(split, 4 * kChunk));
+    return ws_layout((int64_t)B * Hq * n_split_max, d).total;
 }
 
 hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int32_t B, const void *k_pool,
@@ -444,8 +471,9 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
     const int G = Hq / Hkv;
     const int max_len = pt_stride * page_size;
     const int sms = device_sms();
-    const int split = suffix_split_len(B, Hq, max_len, sms);
+    const int split = suffix_split_len(B, Hkv, max_len, sms, d);
     const int n_split = (int)ceil_div(max_len, split);
+    const int nh = small_heads_per_item(Hkv);
     const WsLayout wl = ws_layout((int64_t)B * Hq * n_split, d);
     if (ws_bytes < wl.total || !aligned(ws, 256))
         return HP_ERR_WORKSPACE;
@@ -454,8 +482,8 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
 
     SmallParams sp;
     std::memset(&sp, 0, sizeof(sp));
-    if (!encode_pool_map(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, kChunk) ||
-        !encode_pool_map(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, kChunk))
+    if (!encode_pool_map(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, kChunk, nh) ||
+        !encode_pool_map(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, kChunk, nh))
         return HP_ERR_CUDA;
     sp.q = static_cast<const uint16_t *>(q);
     sp.q_sb = q_sb;
@@ -464,7 +492,8 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
     sp.Hkv = Hkv;
     sp.scale_log2 = scale * kLog2e;
     sp.plan = nullptr;
-    sp.n_items = B * Hkv * n_split;
+    sp.n_items = B * (Hkv / nh) * n_split;
+    sp.nh = nh;
     sp.page_table = page_table;
     sp.pt_stride = pt_stride;
     sp.seq_lens = seq_lens;
@@ -477,8 +506,7 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
     sp.part_o = reinterpret_cast<float *>(wsb + wl.off_o);
     sp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
     sp.status = status_ptr(ws);
-    const int warps = small_warps_per_cta();
-    const int grid = (int)std::min<int64_t>(ceil_div(sp.n_items, warps), (int64_t)sms * 8);
+    const int grid = (int)std::min<int64_t>(sp.n_items, (int64_t)sms * small_ctas_per_sm(d));
     if (launch_small(sp, grid, d, s) != cudaSuccess)
         return HP_ERR_CUDA;
 
@@ -495,6 +523,7 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
     mp.seq_lens = seq_lens;
     mp.split_len = split;
     mp.n_split = n_split;
+    mp.nh = nh;
     mp.out = out;
     mp.out_f32 = out_dt == HP_F32;
     mp.o_sb = o_sb;
@@ -519,7 +548,7 @@ hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_
                          float *lse, int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream)
 {
     if (!q || !out || !ws || rows < 1 || row_begin < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || prefix_len < 0 ||
-        !std::isfinite(scale))
+        !std::isfinite(scale) || !(scale > 0.f))
         return HP_ERR_ARG;
     if (prefix_len > 0 && (!k || !v))
         return HP_ERR_ARG;
@@ -639,7 +668,7 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
     info->n_tc_items = H.n_tc;
     info->n_small_items = H.n_small;
     info->grid_tc = H.n_tc;
-    info->grid_small = (int32_t)std::min<int64_t>(ceil_div(H.n_small, small_warps_per_cta()), (int64_t)sms * 8);
+    info->grid_small = (int32_t)std::min<int64_t>(H.n_small, (int64_t)sms * small_ctas_per_sm(H.d));
     info->n_part_rows = H.n_part_rows;
     info->plan_bytes = H.total_bytes;
     info->ws_bytes = H.ws_bytes;
@@ -657,7 +686,7 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
             cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), reinterpret_cast<cudaStream_t>(stream),
                                      cudaEventRecordExternal);
     };
-    if (!plan_dev || !info || !q || !out || !ws || !std::isfinite(scale))
+    if (!plan_dev || !info || !q || !out || !ws || !std::isfinite(scale) || !(scale > 0.f))
         return HP_ERR_ARG;
     if (info->B < 1 || info->Hq < 1 || info->Hkv < 1 || info->Hq % info->Hkv || !supported_d(info->d))
         return HP_ERR_ARG;
@@ -705,6 +734,7 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         sp.plan = plan;
         sp.tag = info->tag;
         sp.n_items = info->n_small_items;
+        sp.nh = small_heads_per_item(info->Hkv);
         sp.part_o = part_o;
         sp.part_lse = part_lse;
         sp.status = status_ptr(ws);

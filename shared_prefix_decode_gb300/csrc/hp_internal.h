@@ -56,6 +56,8 @@ struct alignas(64) PlanHeader {
     uint64_t tag;
     int32_t B, Hq, Hkv, d, G, num_levels;
     int32_t n_tc, n_small, n_part_rows, n_merge;
+    int32_t small_nh;       // KV heads per small-row item
+    int32_t pad0;
     int64_t off_maps;       // byte offsets from the plan base
     int64_t off_tc;
     int64_t off_small;
@@ -107,6 +109,7 @@ struct SmallParams {
     int32_t pt_stride;
     const int32_t *seq_lens;
     int32_t B, num_pages, page_size, split_len, n_split, seqs_per_item;
+    int32_t nh;  // KV heads per item (a group of consecutive heads; 1, 2 or 4)
     float *part_o;
     float *part_lse;
     uint32_t *status;
@@ -124,6 +127,7 @@ struct MergeParams {
     int32_t mode;            // 1: paged decode splits; 2: contiguous prefix splits
     const int32_t *seq_lens; // mode 1
     int32_t split_len, n_split, seqs_per_item, row_begin, rows, n_rc;
+    int32_t nh;  // mode 1: KV heads per small-kernel item
     void *out;
     int32_t out_f32;
     int64_t o_sb, o_sh;
@@ -146,6 +150,6 @@ cudaError_t launch_merge2(const float *oa, const float *la, const float *ob, con
                           void *o, int out_f32, float *lse, int64_t rows, int d, cudaStream_t s);
 size_t tc_smem_bytes(int d);
 size_t small_smem_bytes(int d);
-int small_warps_per_cta();
+int small_heads_per_item(int Hkv);
 
 }  // namespace hp

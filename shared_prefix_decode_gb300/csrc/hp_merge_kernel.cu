@@ -32,8 +32,12 @@ __device__ __forceinline__ int part_row(const MergeParams &p, const PartList &L,
 {
     if (p.plan != nullptr)
         return __ldg(plan_array<int32_t>(p.plan, p.plan->off_merge_idx) + L.base + e) + L.g;
-    if (p.mode == 1)
-        return ((L.b * p.Hkv + L.kvh) * p.n_split + e) * p.G + L.g;
+    if (p.mode == 1) {
+        // small-kernel items (b, head group, split), rows (head in group, g)
+        const int groups = p.Hkv / p.nh;
+        const int item = ((L.b * groups + L.kvh / p.nh) * p.n_split + e);
+        return (item * p.nh + L.kvh % p.nh) * p.G + L.g;
+    }
     // mode 2: contiguous prefix items (rc, kvh, split), rows (s, g)
     const int rel = L.b - p.row_begin;
     const int rc = rel / p.seqs_per_item, sl = rel % p.seqs_per_item;
@@ -71,37 +75,69 @@ __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeP
         L.n = p.n_split;
         L.base = 0;
     }
-    // pass 1: the largest LSE
+    // Lanes own parts e = lane, lane + 32, ...: gather their rows and LSEs in
+    // parallel, then the weighted sum walks the parts in their fixed order
+    // with the row loads of 8 parts in flight at a time.
     float M = -INFINITY;
     for (int e = lane; e < L.n; e += 32)
         M = fmaxf(M, __ldg(p.part_lse + part_row(p, L, e)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    // pass 2: weighted sum in the fixed part order
     float acc[VPT];
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
         acc[i] = 0.f;
     float den = 0.f;
     if (M != -INFINITY) {
-        for (int e = 0; e < L.n; ++e) {
-            const int pr = part_row(p, L, e);
-            const float w = fast_exp2((__ldg(p.part_lse + pr) - M) * kLog2e);
+        for (int e0 = 0; e0 < L.n; e0 += 32) {
+            const int e = e0 + lane;
+            int pr = 0;
+            float w = 0.f;
+            if (e < L.n) {
+                pr = part_row(p, L, e);
+                w = fast_exp2((__ldg(p.part_lse + pr) - M) * kLog2e);
+            }
             den += w;
-            const float *src = p.part_o + (size_t)pr * p.d + lane * VPT;
-            if (VPT == 4) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
-                acc[0] += w * v.x;
-                acc[1] += w * v.y;
-                acc[2] += w * v.z;
-                acc[3] += w * v.w;
-            } else {
+            const int cnt = min(32, L.n - e0);
+            for (int k0 = 0; k0 < cnt; k0 += 8) {
+                float wk[8];
+                float v[8][VPT];
 #pragma unroll
-                for (int i = 0; i < VPT; ++i)
-                    acc[i] += w * __ldg(src + i);
+                for (int k = 0; k < 8; ++k) {
+                    const int kk = min(k0 + k, 31);
+                    wk[k] = __shfl_sync(0xffffffffu, w, kk);
+                    const int prk = __shfl_sync(0xffffffffu, pr, kk);
+                    if (k0 + k < cnt) {
+                        const float *src = p.part_o + (size_t)prk * p.d + lane * VPT;
+                        if (VPT == 4) {
+                            const float4 x = __ldg(reinterpret_cast<const float4 *>(src));
+                            v[k][0] = x.x;
+                            v[k][1] = x.y;
+                            v[k][2] = x.z;
+                            v[k][3] = x.w;
+                        } else {
+                            const float2 x = __ldg(reinterpret_cast<const float2 *>(src));
+                            v[k][0] = x.x;
+                            v[k][1] = x.y;
+                        }
+                    } else {
+                        wk[k] = 0.f;
+#pragma unroll
+                        for (int i = 0; i < VPT; ++i)
+                            v[k][i] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int i = 0; i < VPT; ++i)
+                        acc[i] += wk[k] * v[k][i];
             }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            den += __shfl_xor_sync(0xffffffffu, den, o);
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     const int64_t off = (int64_t)L.b * p.o_sb + (int64_t)h * p.o_sh + lane * VPT;

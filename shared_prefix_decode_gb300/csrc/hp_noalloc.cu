@@ -74,14 +74,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_noalloc()
     return fn;
 }
 
-bool encode_pool(CUtensorMap *m, const void *pool, int num_pages, int Hkv, int ps, int d)
+bool encode_pool(CUtensorMap *m, const void *pool, int num_pages, int Hkv, int ps, int d, int heads)
 {
     auto fn = encode_fn_noalloc();
     if (!fn)
         return false;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
     cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)ps * d * 2, (cuuint64_t)Hkv * ps * d * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)hp::kChunk, 1, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)hp::kChunk, (cuuint32_t)heads, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -150,8 +150,9 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
 
     SmallParams sp;
     std::memset(&sp, 0, sizeof(sp));
-    if (!encode_pool(&sp.map_k, k_pool, num_pages, Hkv, page_size, d) ||
-        !encode_pool(&sp.map_v, v_pool, num_pages, Hkv, page_size, d))
+    const int nh = small_heads_per_item(Hkv);
+    if (!encode_pool(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, nh) ||
+        !encode_pool(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, nh))
         return HP_ERR_CUDA;
     const int G = Hq / Hkv;
     sp.q = static_cast<const uint16_t *>(q);
@@ -161,7 +162,8 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
     sp.Hkv = Hkv;
     sp.scale_log2 = scale * 1.4426950408889634f;
     sp.plan = nullptr;
-    sp.n_items = B * Hkv * n_split;
+    sp.n_items = B * (Hkv / nh) * n_split;
+    sp.nh = nh;
     sp.page_table = page_table;
     sp.pt_stride = pt_stride;
     sp.seq_lens = seq_lens;
@@ -177,7 +179,8 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = (int)std::min<int64_t>(cdiv(sp.n_items, small_warps_per_cta()), (int64_t)sms * 8);
+    const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(4, (size_t)(227 * 1024) / small_smem_bytes(d)));
+    const int grid = (int)std::min<int64_t>(sp.n_items, (int64_t)sms * per_sm);
     if (launch_small(sp, grid, d, s) != cudaSuccess)
         return HP_ERR_CUDA;
 
@@ -195,6 +198,7 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
     mp.seq_lens = seq_lens;
     mp.split_len = (int)split;
     mp.n_split = n_split;
+    mp.nh = nh;
     mp.out = out;
     mp.out_f32 = out_dt == HP_F32;
     mp.o_sb = o_sb;

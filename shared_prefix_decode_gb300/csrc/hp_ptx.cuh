@@ -232,6 +232,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
                  : "memory");
 }
 
+// Register re-balancing between warpgroups (all four warps of a warpgroup
+// execute it).  The launch gives every thread the same count; a warpgroup
+// that lowers its count returns registers to the pool that a raising
+// warpgroup draws from, so the sum must stay within the launch allocation.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose
 // 8-row swizzle atoms are 1024-byte aligned.  lbo/sbo in bytes.
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo)

@@ -37,6 +37,8 @@ namespace hp {
 
 namespace {
 
+constexpr int kMaxBoxes = 1024;
+
 template <int D>
 struct TcLayout {
     static constexpr int kHalves = D / 64;
@@ -46,7 +48,8 @@ struct TcLayout {
     static constexpr int kK = kQ + 2 * kTile;
     static constexpr int kV = kK + 2 * kTile;
     static constexpr int kBar = kV + 2 * kTile;
-    static constexpr int kBytes = kBar + 256;
+    static constexpr int kPages = kBar + 256;  // staged page ids of the item's boxes
+    static constexpr int kBytes = kPages + 4 * kMaxBoxes;
 };
 
 // barrier slots
@@ -54,6 +57,12 @@ enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_S = 8, B_P = 10, 
        B_COUNT = 15 };
 
 constexpr int kThreads = 384;
+// Register split: warpgroup 0 (producer, MMA, two helper warps) lowers its
+// count, the two softmax warpgroups raise theirs; the sum equals the launch
+// allocation (384 threads x kRegsLaunch), which the host checks before the
+// first launch.
+constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 136, kRegsSoftmax = 184;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax == kThreads * kRegsLaunch, "register split");
 constexpr float kTau = 8.0f;  // lazy rescale threshold, log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -107,35 +116,32 @@ __device__ __forceinline__ ItemGeo resolve_item(const TcParams &p, int idx)
     return g;
 }
 
+// Issue the TMA copies of one 128-key tile (K or V) into `dst`.  Paged items
+// take the page of each box from the ids staged in shared memory.
+// Issue the TMA copies of one 128-key tile (K or V) into `dst`, one box per
+// lane (box, column half) so that all boxes leave in one warp instruction: a
+// single thread issuing small boxes one after another is limited to a
+// fraction of HBM bandwidth, several lanes issuing together are not.  Paged
+// items take the page of each box from the ids staged in shared memory.
 template <int D>
-__device__ __forceinline__ void issue_tile_loads(const TcParams &p, const ItemGeo &g,
-                                                 const void *map, uint32_t dst, uint32_t bar,
-                                                 int tile)
+__device__ __forceinline__ void issue_tile(const ItemGeo &g, const int32_t *s_pages, const void *map,
+                                           uint32_t dst, uint32_t bar, int tile, int lane)
 {
     constexpr int kHalves = D / 64;
+    if (lane == 0)
+        mbar_arrive_expect_tx(bar, TcLayout<D>::kTile);
+    __syncwarp();
     const int kt0 = g.k0 + tile * kTcTile;
-    mbar_arrive_expect_tx(bar, TcLayout<D>::kTile);
     if (g.paged) {
         const int nbox = kTcTile / g.box;
-        for (int bx = 0; bx < nbox; ++bx) {
+        for (int l = lane; l < nbox * kHalves; l += 32) {
+            const int bx = l / kHalves, h = l - bx * kHalves;
             const int t = kt0 + bx * g.box;
-            int page = g.num_pages;  // out of range: the box is zero-filled
-            int slot = 0;
-            if (t < g.k1) {
-                page = __ldg(g.pages + t / g.ps);
-                slot = t % g.ps;
-                if ((unsigned)page >= (unsigned)g.num_pages) {
-                    atomicOr(p.status, kStBounds);
-                    page = g.num_pages;
-                }
-            }
-            for (int h = 0; h < kHalves; ++h)
-                tma_load_4d(dst + h * TcLayout<D>::kRegion + bx * g.box * 128, map, bar, h * 64, slot,
-                            g.kvh, page);
+            tma_load_4d(dst + h * TcLayout<D>::kRegion + bx * g.box * 128, map, bar, h * 64, t % g.ps, g.kvh,
+                        s_pages[tile * nbox + bx]);
         }
-    } else {
-        for (int h = 0; h < kHalves; ++h)
-            tma_load_3d(dst + h * TcLayout<D>::kRegion, map, bar, h * 64, g.kvh, kt0);
+    } else if (lane < kHalves) {
+        tma_load_3d(dst + lane * TcLayout<D>::kRegion, map, bar, lane * 64, g.kvh, kt0);
     }
 }
 
@@ -155,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_tc_kernel(const __grid_constan
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBar + 128);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + L::kBar + 132);
+    int32_t *s_pages = reinterpret_cast<int32_t *>(smem + L::kPages);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -169,74 +176,122 @@ __global__ void __launch_bounds__(kThreads, 1) hp_tc_kernel(const __grid_constan
     const int rows_total = g.n_seq * p.G;
     const int nmb = (rows_total + 127) >> 7;
     const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
-    if (nmb > 2 || n_tiles <= 0) {
+    const int n_boxes = g.paged ? n_tiles * (kTcTile / g.box) : 0;
+    if (nmb > 2 || n_tiles <= 0 || n_boxes > kMaxBoxes) {
         if (threadIdx.x == 0)
             atomicOr(p.status, kStPlan);
         return;  // uniform across the CTA: nothing allocated yet
     }
+    const int pre = n_tiles < 2 ? n_tiles : 2;  // tiles issued before the CTA barrier
 
-    if (tid == 0) {
-        for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(bar(i), (i == B_P || i == B_P + 1) ? 128u : 1u);
-        *abort = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
-        tmem_relinquish();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tensormap(g.map_k);
-        prefetch_tensormap(g.map_v);
-    }
+    // warp-uniform bounded wait
+    auto wait_warp = [&](int b, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar(b), parity, p.status, abort)) != 0;
+    };
 
-    // Stage Q (rows r = s*G + g of the item; rows past the item are zero) in
-    // the 128-byte-swizzled K-major layout the MMA descriptors describe.
-    {
+    if (warp == 0) {
+        // Barriers, then the page id of every box of the item (ids out of
+        // range become the zero-filled page num_pages and set the bounds
+        // flag), then the first tiles' copies -- these overlap Q staging.
+        if (lane == 0) {
+            for (int i = 0; i < B_COUNT; ++i)
+                mbar_init(bar(i), (i == B_P || i == B_P + 1) ? 128u : 1u);
+            *abort = 0;
+            fence_mbar_init();
+            prefetch_tensormap(g.map_k);
+            prefetch_tensormap(g.map_v);
+        }
+        if (g.paged) {
+            const int nbox = kTcTile / g.box;
+            for (int i = lane; i < n_boxes; i += 32) {
+                const int t = g.k0 + (i / nbox) * kTcTile + (i % nbox) * g.box;
+                int page = g.num_pages;
+                if (t < g.k1) {
+                    page = __ldg(g.pages + t / g.ps);
+                    if ((unsigned)page >= (unsigned)g.num_pages) {
+                        atomicOr(p.status, kStBounds);
+                        page = g.num_pages;
+                    }
+                }
+                s_pages[i] = page;
+            }
+        }
+        __syncwarp();
+        for (int j = 0; j < pre; ++j) {
+            issue_tile<D>(g, s_pages, g.map_k, sbase + L::kK + j * L::kTile, bar(B_KFULL + j), j, lane);
+            issue_tile<D>(g, s_pages, g.map_v, sbase + L::kV + j * L::kTile, bar(B_VFULL + j), j, lane);
+        }
+    } else {
+        if (warp == 1) {
+            tmem_alloc(smem_u32(tmem_slot), 512);
+            tmem_relinquish();
+        }
+        // Stage Q (rows r = s*G + g of the item; rows past the item are zero)
+        // in the 128-byte-swizzled K-major layout the MMA descriptors
+        // describe.  Warps 1-11; all loads of a thread before its stores.
+        constexpr int kQThreads = kThreads - 32;
         constexpr int kCpr = D / 8;  // 16-byte chunks per row
+        constexpr int kPer = (2 * 128 * kCpr + kQThreads - 1) / kQThreads;
+        const int qt = tid - 32;
         const int total = nmb * 128 * kCpr;
-        for (int i = tid; i < total; i += kThreads) {
+        uint4 buf[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = qt + k * kQThreads;
             const int r = i / kCpr;
-            const int c = i % kCpr;
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            if (r < rows_total) {
+            buf[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < total && r < rows_total) {
+                const int c = i % kCpr;
                 const int s = r / p.G;
                 const int gg = r - s * p.G;
-                const uint16_t *src = p.q + (int64_t)(g.seq_begin + s) * p.q_sb +
-                                      (int64_t)(g.kvh * p.G + gg) * p.q_sh + c * 8;
-                val = __ldg(reinterpret_cast<const uint4 *>(src));
+                const uint16_t *src =
+                    p.q + (int64_t)(g.seq_begin + s) * p.q_sb + (int64_t)(g.kvh * p.G + gg) * p.q_sh + c * 8;
+                buf[k] = __ldg(reinterpret_cast<const uint4 *>(src));
             }
-            const int mb = r >> 7, rr = r & 127, h = c >> 3, cc = c & 7;
-            uint8_t *dst = smem + L::kQ + ((mb * kHalves + h) * 128 + rr) * 128 + ((cc ^ (rr & 7)) << 4);
-            *reinterpret_cast<uint4 *>(dst) = val;
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = qt + k * kQThreads;
+            if (i < total) {
+                const int r = i / kCpr, c = i % kCpr;
+                const int mb = r >> 7, rr = r & 127, h = c >> 3, cc = c & 7;
+                uint8_t *dst = smem + L::kQ + ((mb * kHalves + h) * 128 + rr) * 128 + ((cc ^ (rr & 7)) << 4);
+                *reinterpret_cast<uint4 *>(dst) = buf[k];
+            }
         }
     }
     fence_proxy_async_smem();
     tc_fence_before();
+    __syncwarp();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Registers: the softmax warpgroups hold a whole 128-column score row
+    if (warp < 4)
+        setmaxnreg_dec<kRegsCtl>();
+    else
+        setmaxnreg_inc<kRegsSoftmax>();
+
     if (warp == 0) {
         // ------------------------------------------------------ producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-                if (!mbar_wait(bar(B_KEMPTY + st), ph ^ 1u, p.status, abort))
-                    break;
-                issue_tile_loads<D>(p, g, g.map_k, sbase + L::kK + st * L::kTile, bar(B_KFULL + st), j);
-                if (!mbar_wait(bar(B_VEMPTY + st), ph ^ 1u, p.status, abort)) {
-                    issued = j + 1;  // K of tile j is in flight
-                    mbar_wait_drain(bar(B_KFULL + st), ph);
-                    issued = j;
-                    break;
-                }
-                issue_tile_loads<D>(p, g, g.map_v, sbase + L::kV + st * L::kTile, bar(B_VFULL + st), j);
-                issued = j + 1;
+        int issued = pre;
+        for (int j = pre; j < n_tiles; ++j) {
+            const int st = j & 1;
+            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+            if (!wait_warp(B_KEMPTY + st, ph ^ 1u))
+                break;
+            issue_tile<D>(g, s_pages, g.map_k, sbase + L::kK + st * L::kTile, bar(B_KFULL + st), j, lane);
+            if (!wait_warp(B_VEMPTY + st, ph ^ 1u)) {
+                if (lane == 0)
+                    mbar_wait_drain(bar(B_KFULL + st), ph);  // K of tile j is in flight
+                break;
             }
-            // drain: every load issued has landed before the CTA exits
+            issue_tile<D>(g, s_pages, g.map_v, sbase + L::kV + st * L::kTile, bar(B_VFULL + st), j, lane);
+            issued = j + 1;
+        }
+        // drain: every load issued has landed before the CTA exits
+        if (lane == 0) {
             for (int j = max(0, issued - 2); j < issued; ++j) {
                 const uint32_t ph = (uint32_t)(j >> 1) & 1u;
                 mbar_wait_drain(bar(B_KFULL + (j & 1)), ph);
@@ -314,82 +369,95 @@ __global__ void __launch_bounds__(kThreads, 1) hp_tc_kernel(const __grid_constan
         const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t s_col = tl + mb * 128;
         const uint32_t o_col = tl + 256 + mb * 128;
-        // waits whose outcome is made warp-uniform (TMEM ld/st are warp-wide)
-        auto wait_all = [&](int b, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait(bar(b), parity, p.status, abort)) != 0;
-        };
-        float m_run = -INFINITY;
+        const float c = p.scale_log2;  // > 0 (checked on the host)
+        float m_run = -INFINITY;       // reference max, log2 units
         float l_run = 0.f;
         bool ok = mb < nmb;
+        uint32_t sv[128];
         uint32_t r[32];
-        int j = 0;
-        for (; ok && j < n_tiles; ++j) {
-            if (!(ok = wait_all(B_S + mb, (uint32_t)j & 1u)))
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            if (!(ok = wait_warp(B_S + mb, (uint32_t)j & 1u)))
                 break;
             tc_fence_after();
             const int nvalid = min(kTcTile, g.k1 - (g.k0 + j * kTcTile));
-            float tmax = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(s_col + c * 32, r);
-                tmem_ld_wait();
+            for (int cc = 0; cc < 4; ++cc)
+                tmem_ld32(s_col + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[cc * 32]));
+            tmem_ld_wait();
+            // the scale is positive, so the largest scaled score is the
+            // largest raw score times the scale
+            float mx = -INFINITY;
+            if (nvalid >= kTcTile) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (c * 32 + i < nvalid)
-                        tmax = fmaxf(tmax, __uint_as_float(r[i]) * p.scale_log2);
+                for (int i = 0; i < 128; ++i)
+                    mx = fmaxf(mx, __uint_as_float(sv[i]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 128; ++i)
+                    if (i < nvalid)
+                        mx = fmaxf(mx, __uint_as_float(sv[i]));
             }
+            const float tmax = mx * c;
             const bool need = tmax > m_run + kTau;
             const float alpha = need ? fast_exp2(m_run - tmax) : 1.f;
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-                if (!(ok = wait_all(B_O + mb, (uint32_t)(j - 1) & 1u)))
-                    break;
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    tmem_ld32(o_col + c * 32, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tmem_st32(o_col + c * 32, r);
-                }
-                tmem_st_wait();
-            }
             if (need) {
                 l_run *= alpha;
                 m_run = tmax;
             }
+            // P = exp2(s * c - m) as bf16 pairs over the S columns (the score
+            // row is dead afterwards, which keeps the rescale below cheap in
+            // registers)
+            const float nm = -m_run;
             float lsum = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(s_col + c * 32, r);
-                tmem_ld_wait();
+            for (int cc = 0; cc < 4; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int c0 = c * 32 + 2 * i;
-                    const float p0 = c0 < nvalid ? fast_exp2(__uint_as_float(r[2 * i]) * p.scale_log2 - m_run) : 0.f;
-                    const float p1 =
-                        c0 + 1 < nvalid ? fast_exp2(__uint_as_float(r[2 * i + 1]) * p.scale_log2 - m_run) : 0.f;
+                    const int c0 = cc * 32 + 2 * i;
+                    float p0 = fast_exp2(fmaf(__uint_as_float(sv[c0]), c, nm));
+                    float p1 = fast_exp2(fmaf(__uint_as_float(sv[c0 + 1]), c, nm));
+                    if (nvalid < kTcTile) {
+                        p0 = c0 < nvalid ? p0 : 0.f;
+                        p1 = c0 + 1 < nvalid ? p1 : 0.f;
+                    }
+                    lsum += p0 + p1;
                     pk[i] = pack_bf16x2(p0, p1);
-                    lsum += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
                 }
-                tmem_st16(s_col + c * 16, pk);
+                tmem_st16(s_col + cc * 16, pk);
+            }
+            l_run += lsum;
+            // O was accumulated against the old reference max: rescale it
+            // once the previous P V has landed (rare: only when the max grows
+            // by more than 2^kTau)
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                if (!(ok = wait_warp(B_O + mb, (uint32_t)(j - 1) & 1u)))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    tmem_ld32(o_col + cc * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st32(o_col + cc * 32, r);
+                }
             }
             tmem_st_wait();
-            l_run += lsum;
             if (mb == 0 && nvalid < kTcTile) {
                 // last, partial tile: rows past the node hold whatever the
                 // pool holds there; zero their V so 0 * garbage stays 0
                 const int st = j & 1;
-                if (!(ok = wait_all(B_VFULL + st, (uint32_t)(j >> 1) & 1u)))
+                if (!(ok = wait_warp(B_VFULL + st, (uint32_t)(j >> 1) & 1u)))
                     break;
                 if (rr >= nvalid) {
                     for (int h = 0; h < kHalves; ++h) {
-                        uint4 *vrow = reinterpret_cast<uint4 *>(smem + L::kV + st * L::kTile + h * L::kRegion + rr * 128);
+                        uint4 *vrow =
+                            reinterpret_cast<uint4 *>(smem + L::kV + st * L::kTile + h * L::kRegion + rr * 128);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            vrow[c] = make_uint4(0u, 0u, 0u, 0u);
+                        for (int q = 0; q < 8; ++q)
+                            vrow[q] = make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
                 fence_proxy_async_smem();
@@ -398,14 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1) hp_tc_kernel(const __grid_constan
             mbar_arrive(bar(B_P + mb));
         }
         if (ok && mb < nmb) {
-            if (wait_all(B_O + mb, (uint32_t)(n_tiles - 1) & 1u)) {
+            if (wait_warp(B_O + mb, (uint32_t)(n_tiles - 1) & 1u)) {
                 tc_fence_after();
                 const float inv = 1.f / l_run;
                 const float lse = (m_run + fast_log2(l_run)) * kLn2;
                 float *dst = p.part_o + (size_t)(g.part_row + row) * D;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    tmem_ld32(o_col + c * 32, r);
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    tmem_ld32(o_col + cc * 32, r);
                     tmem_ld_wait();
                     if (row < rows_total) {
 #pragma unroll
@@ -413,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_tc_kernel(const __grid_constan
                             float4 v = make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
                                                    __uint_as_float(r[i + 2]) * inv,
                                                    __uint_as_float(r[i + 3]) * inv);
-                            *reinterpret_cast<float4 *>(dst + c * 32 + i) = v;
+                            *reinterpret_cast<float4 *>(dst + cc * 32 + i) = v;
                         }
                     }
                 }
@@ -424,6 +492,11 @@ __global__ void __launch_bounds__(kThreads, 1) hp_tc_kernel(const __grid_constan
         tc_fence_before();
     }
 
+    // Lanes 1-31 of warps 0 and 1 reach this point while their lane 0 still
+    // runs the producer / MMA loop: converge each warp before the CTA barrier
+    // (an aligned barrier must be reached by whole warps), so TMEM is freed
+    // only after every role has finished.
+    __syncwarp();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -440,6 +513,12 @@ cudaError_t launch_tc_d(const TcParams &p, int grid, cudaStream_t s)
         cudaError_t e = cudaFuncSetAttribute(hp_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess)
             return e;
+        // the register split assumes this launch allocation per thread
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, hp_tc_kernel<D>)) != cudaSuccess)
+            return e;
+        if (fa.numRegs != (int)kRegsLaunch)
+            return cudaErrorInvalidConfiguration;
         configured = true;
     }
     hp_tc_kernel<D><<<grid, kThreads, bytes, s>>>(p);
