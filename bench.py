@@ -255,7 +255,7 @@ def main():
     for s in sets:
         s["plan"].ws = ws_shared
     info = sets[0]["plan"].info
-    kernels_per_step = int(info.n_tc_items > 0) + int(info.n_small_items > 0) + 1
+    kernels_per_step = int(info.n_tc_items + info.n_small_items > 0) + 1
     stream = torch.cuda.Stream(device=dev)
 
     def step(s, st=None):
@@ -347,16 +347,15 @@ def main():
             s["plan"], s["wg"].q, s["wl"].scale, s["out"], s["lse"], evs, stream=stream))
         ev_sets.append((g, evs))
     torch.cuda.synchronize(dev)
-    k_ms = {"tc": [], "small": [], "merge": []}
+    k_ms = {"cascade": [], "merge": []}
     passes = max(1, min(200, args.steps // max(R, 1)))
     for _ in range(passes):
         for g, _ in ev_sets:
             g.replay()
         torch.cuda.synchronize(dev)
         for _, evs in ev_sets:
-            k_ms["tc"].append(evs[0].elapsed_time(evs[1]))
-            k_ms["small"].append(evs[1].elapsed_time(evs[2]))
-            k_ms["merge"].append(evs[2].elapsed_time(evs[3]))
+            k_ms["cascade"].append(evs[0].elapsed_time(evs[1]))
+            k_ms["merge"].append(evs[1].elapsed_time(evs[2]))
     k_us = {k: statistics.mean(v) * 1e3 for k, v in k_ms.items()}
 
     # algorithmic bytes per launch of each kernel
@@ -374,11 +373,8 @@ def main():
     merge_bytes = statistics.mean(
         s["plan"].info.n_part_rows * (s["wl"].d + 1) * 4 + s["wl"].B * s["wl"].Hq * (s["wl"].d * 2 + 4)
         for s in sets)
-    kb = {"tc": tc_bytes, "small": small_bytes, "merge": merge_bytes}
-    kname = {"tc": "hp_tc_kernel", "small": "hp_small_kernel", "merge": "hp_merge_kernel"}
-    ksrc = {"tc": ["shared_prefix_decode_gb300/csrc/hp_tc_kernel.cu", "shared_prefix_decode_gb300/csrc/hp_ptx.cuh"],
-            "small": ["shared_prefix_decode_gb300/csrc/hp_small_kernel.cu", "shared_prefix_decode_gb300/csrc/hp_ptx.cuh"],
-            "merge": ["shared_prefix_decode_gb300/csrc/hp_merge_kernel.cu"]}
+    kb = {"cascade": tc_bytes + small_bytes, "merge": merge_bytes}
+    kname = {"cascade": "hp_cascade_kernel", "merge": "hp_merge_kernel"}
     dom = max(k_us, key=lambda k: k_us[k])
     achieved = kb[dom] / (k_us[dom] * 1e-6) / 1e9
     tr = load_traffic(kname[dom])
@@ -472,7 +468,7 @@ def main():
             "clocks": clock_summary,
             "naive": naive,
             "parity_spot": parity,
-            "plan": {"tc_items": info.n_tc_items, "small_items": info.n_small_items, "grid_small": info.grid_small,
+            "plan": {"tc_items": info.n_tc_items, "small_items": info.n_small_items, "grid": info.grid,
                      "part_rows": info.n_part_rows},
             "device": props.name,
         }

@@ -193,9 +193,10 @@ typedef struct {
  * through the status word on a mismatch. */
 typedef struct {
     int32_t B, Hq, Hkv, d;
-    int32_t n_tc_items;    /* shared-node items on the tensor-core kernel */
+    int32_t n_tc_items;    /* shared-node items (tensor-core role) */
     int32_t n_small_items; /* small-row items (private suffixes, narrow nodes) */
-    int32_t grid_tc, grid_small;
+    int32_t grid;          /* CTAs of the step's persistent launch (one per SM) */
+    int32_t reserved;
     int64_t n_part_rows;   /* partial (O, LSE) rows in the workspace */
     int64_t plan_bytes;
     int64_t ws_bytes;      /* workspace hp_cascade_decode needs */
@@ -227,9 +228,11 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
 
 /* The same step, recording caller-created CUDA events (cudaEvent_t handles;
  * any may be NULL) on `stream` -- as external event nodes when the stream is
- * being captured, so they time each replay: events[0] before the shared-node kernel,
- * events[1] after it, events[2] after the small-row kernel, events[3] after
- * the merge -- for timing each kernel of the step on its own stream. */
+ * being captured, so they time each replay: events[0] before the step's
+ * persistent kernel (prefix and suffix passes), events[1] after it,
+ * events[2] after the merge kernel (events[3] is not used) -- for timing each
+ * kernel of the step on its own stream.  With events[1] given, the merge is
+ * launched after it instead of overlapping the persistent kernel's tail. */
 hp_status hp_cascade_decode_profiled(const void *plan_dev, const hp_plan_info *info, const void *q,
                                      int64_t q_sb, int64_t q_sh, float scale, void *out,
                                      hp_dtype out_dt, int64_t o_sb, int64_t o_sh, float *lse,

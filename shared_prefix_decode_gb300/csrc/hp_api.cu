@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <numeric>
+#include <queue>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -23,7 +24,7 @@ constexpr int32_t kAbiVersion = 1;
 // A tensor-core item processes at least this many 128-key tiles (its fixed
 // set-up -- TMEM allocation, Q staging, pipeline fill -- is amortised over
 // them) and at most kMaxTcTiles (its page ids must fit the staging area).
-constexpr int64_t kMinTcTiles = 4;
+constexpr int64_t kMinTcTiles = 2;
 constexpr int64_t kMaxTcTiles = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -178,8 +179,58 @@ struct HostPlan {
     std::vector<WorkItem> tc, small;
     std::vector<int32_t> page_ids;
     std::vector<int32_t> merge_ptr, merge_idx;
+    std::vector<int32_t> cta_ptr, cta_ntc, cta_items;  // per-CTA schedule of the fused kernel
     std::vector<int32_t> contexts;  // (level, node, seq_begin, seq_end, pass) x n
 };
+
+// Longest-first greedy schedule of the fused kernel's items over `grid` CTAs.
+// Cost of an item: a fixed set-up plus its KV bytes at one SM's share of HBM
+// bandwidth (~44 GB/s when every SM streams).  Each CTA runs its tensor-core
+// items first, then its paged items, each group longest first.
+void schedule(HostPlan &P, int grid, int d)
+{
+    const double kBytesPerNs = 44.0;
+    struct Job {
+        double cost;
+        int32_t id;
+        bool tc;
+    };
+    std::vector<Job> jobs;
+    const int n_tc = (int)P.tc.size();
+    for (int i = 0; i < n_tc; ++i) {
+        const WorkItem &w = P.tc[i];
+        const double bytes = (double)(w.k1 - w.k0) * d * 4;
+        jobs.push_back({2000.0 + bytes / kBytesPerNs, i, true});
+    }
+    const int nh = P.hdr.small_nh;
+    for (size_t j = 0; j < P.small.size(); ++j) {
+        const WorkItem &w = P.small[j];
+        const double bytes = (double)(w.k1 - w.k0) * nh * w.n_seq * d * 4;
+        jobs.push_back({500.0 + bytes / kBytesPerNs, (int32_t)(n_tc + j), false});
+    }
+    std::stable_sort(jobs.begin(), jobs.end(), [](const Job &a, const Job &b) { return a.cost > b.cost; });
+    using Slot = std::pair<double, int>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int c = 0; c < grid; ++c)
+        heap.push({0.0, c});
+    std::vector<std::vector<int32_t>> tc_of(grid), sm_of(grid);
+    for (const Job &j : jobs) {
+        Slot sl = heap.top();
+        heap.pop();
+        (j.tc ? tc_of : sm_of)[sl.second].push_back(j.id);
+        sl.first += j.cost;
+        heap.push(sl);
+    }
+    P.cta_ptr.assign(grid + 1, 0);
+    P.cta_ntc.assign(grid, 0);
+    P.cta_items.clear();
+    for (int c = 0; c < grid; ++c) {
+        P.cta_ntc[c] = (int32_t)tc_of[c].size();
+        P.cta_items.insert(P.cta_items.end(), tc_of[c].begin(), tc_of[c].end());
+        P.cta_items.insert(P.cta_items.end(), sm_of[c].begin(), sm_of[c].end());
+        P.cta_ptr[c + 1] = (int32_t)P.cta_items.size();
+    }
+}
 
 hp_status validate_desc(const hp_tree_desc *d)
 {
@@ -275,7 +326,7 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     // Split sizes.  Shared (tensor-core) work: total 128-key tiles spread over
     // one wave of CTAs (one per SM).  Small-row work: 16-key chunks spread
     // over ~8 warps per SM.
-    const int nh = small_heads_per_item(d->Hkv);
+    const int nh = cascade_heads_per_item(d->Hkv);
     H.small_nh = nh;
     int64_t tc_tiles = 0, small_chunks = 0;
     for (int l = 0; l < d->num_levels; ++l)
@@ -293,8 +344,7 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
         }
     const int64_t tc_split =
         kTcTile * std::min(kMaxTcTiles, std::max<int64_t>(kMinTcTiles, ceil_div(tc_tiles, sms)));
-    const int64_t small_split =
-        kChunk * std::max<int64_t>(4, ceil_div(small_chunks, (int64_t)sms * small_ctas_per_sm(d->d) * 3));
+    const int64_t small_split = kChunk * std::max<int64_t>(2, ceil_div(small_chunks, (int64_t)sms * 2));
 
     // Items and partial rows, level by level; merge lists per (b, kvh).
     std::vector<std::vector<int32_t>> lists((size_t)d->B * d->Hkv);
@@ -347,6 +397,8 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     }
     H.n_tc = (int32_t)P.tc.size();
     H.n_small = (int32_t)P.small.size();
+    H.grid = sms;
+    schedule(P, sms, d->d);
     H.n_part_rows = (int32_t)part;
     H.n_merge = (int32_t)P.merge_idx.size();
 
@@ -369,6 +421,15 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     off = round_up(off, 64);
     H.off_merge_idx = (int64_t)off;
     off += 4 * std::max<size_t>(P.merge_idx.size(), 1);
+    off = round_up(off, 64);
+    H.off_cta_ptr = (int64_t)off;
+    off += 4 * P.cta_ptr.size();
+    off = round_up(off, 64);
+    H.off_cta_ntc = (int64_t)off;
+    off += 4 * P.cta_ntc.size();
+    off = round_up(off, 64);
+    H.off_cta_items = (int64_t)off;
+    off += 4 * std::max<size_t>(P.cta_items.size(), 1);
     H.total_bytes = (int64_t)round_up(off, 256);
     const WsLayout ws = ws_layout(part, d->d);
     H.ws_off_lse = (int64_t)ws.off_lse;
@@ -655,11 +716,14 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
     std::memcpy(img.data() + H.off_merge_ptr, P.merge_ptr.data(), 4 * P.merge_ptr.size());
     if (!P.merge_idx.empty())
         std::memcpy(img.data() + H.off_merge_idx, P.merge_idx.data(), 4 * P.merge_idx.size());
+    std::memcpy(img.data() + H.off_cta_ptr, P.cta_ptr.data(), 4 * P.cta_ptr.size());
+    std::memcpy(img.data() + H.off_cta_ntc, P.cta_ntc.data(), 4 * P.cta_ntc.size());
+    if (!P.cta_items.empty())
+        std::memcpy(img.data() + H.off_cta_items, P.cta_items.data(), 4 * P.cta_items.size());
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(plan_dev, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return HP_ERR_CUDA;
-    const int sms = desc->num_sms > 0 ? desc->num_sms : device_sms();
     std::memset(info, 0, sizeof(*info));
     info->B = H.B;
     info->Hq = H.Hq;
@@ -667,8 +731,7 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
     info->d = H.d;
     info->n_tc_items = H.n_tc;
     info->n_small_items = H.n_small;
-    info->grid_tc = H.n_tc;
-    info->grid_small = (int32_t)std::min<int64_t>(H.n_small, (int64_t)sms * small_ctas_per_sm(H.d));
+    info->grid = H.grid;
     info->n_part_rows = H.n_part_rows;
     info->plan_bytes = H.total_bytes;
     info->ws_bytes = H.ws_bytes;
@@ -703,45 +766,22 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
     float *part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
 
     mark(0);
-    if (info->n_tc_items > 0) {
-        TcParams tp;
-        std::memset(&tp, 0, sizeof(tp));
-        tp.q = static_cast<const uint16_t *>(q);
-        tp.q_sb = q_sb;
-        tp.q_sh = q_sh;
-        tp.G = G;
-        tp.Hkv = info->Hkv;
-        tp.scale_log2 = scale * kLog2e;
-        tp.plan = plan;
-        tp.tag = info->tag;
-        tp.n_items = info->n_tc_items;
-        tp.part_o = part_o;
-        tp.part_lse = part_lse;
-        tp.status = status_ptr(ws);
-        if (launch_tc(tp, info->grid_tc, info->d, s) != cudaSuccess)
+    if (info->n_tc_items + info->n_small_items > 0) {
+        CascadeParams cp;
+        std::memset(&cp, 0, sizeof(cp));
+        cp.plan = plan;
+        cp.tag = info->tag;
+        cp.q = static_cast<const uint16_t *>(q);
+        cp.q_sb = q_sb;
+        cp.q_sh = q_sh;
+        cp.scale_log2 = scale * kLog2e;
+        cp.part_o = part_o;
+        cp.part_lse = part_lse;
+        cp.status = status_ptr(ws);
+        if (launch_cascade(cp, info->grid, info->d, s) != cudaSuccess)
             return HP_ERR_CUDA;
     }
     mark(1);
-    if (info->n_small_items > 0) {
-        SmallParams sp;
-        std::memset(&sp, 0, sizeof(sp));
-        sp.q = static_cast<const uint16_t *>(q);
-        sp.q_sb = q_sb;
-        sp.q_sh = q_sh;
-        sp.G = G;
-        sp.Hkv = info->Hkv;
-        sp.scale_log2 = scale * kLog2e;
-        sp.plan = plan;
-        sp.tag = info->tag;
-        sp.n_items = info->n_small_items;
-        sp.nh = small_heads_per_item(info->Hkv);
-        sp.part_o = part_o;
-        sp.part_lse = part_lse;
-        sp.status = status_ptr(ws);
-        if (launch_small(sp, info->grid_small, info->d, s) != cudaSuccess)
-            return HP_ERR_CUDA;
-    }
-    mark(2);
     MergeParams mp;
     std::memset(&mp, 0, sizeof(mp));
     mp.part_o = part_o;
@@ -760,9 +800,13 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
     mp.lse = lse;
     mp.lse_sb = lse_sb;
     mp.status = status_ptr(ws);
-    if (launch_merge(mp, (int64_t)info->B * info->Hq, s) != cudaSuccess)
+    // the merge overlaps its launch with the fused kernel's tail unless an
+    // event was recorded in between
+    const bool dependent = !(events && events[1]);
+    if ((dependent ? launch_merge_dependent(mp, (int64_t)info->B * info->Hq, s)
+                   : launch_merge(mp, (int64_t)info->B * info->Hq, s)) != cudaSuccess)
         return HP_ERR_CUDA;
-    mark(3);
+    mark(2);
     return HP_OK;
 }
 

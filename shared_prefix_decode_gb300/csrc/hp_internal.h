@@ -57,13 +57,16 @@ struct alignas(64) PlanHeader {
     int32_t B, Hq, Hkv, d, G, num_levels;
     int32_t n_tc, n_small, n_part_rows, n_merge;
     int32_t small_nh;       // KV heads per small-row item
-    int32_t pad0;
+    int32_t grid;           // CTAs of the fused kernel (one schedule per CTA)
     int64_t off_maps;       // byte offsets from the plan base
     int64_t off_tc;
     int64_t off_small;
     int64_t off_page_ids;
     int64_t off_merge_ptr;  // [B*Hkv + 1] int32
     int64_t off_merge_idx;  // [n_merge] int32: partial row of (b, g = 0)
+    int64_t off_cta_ptr;    // [grid + 1] int32: each CTA's schedule in cta_items
+    int64_t off_cta_ntc;    // [grid] int32: how many of them are tensor-core items
+    int64_t off_cta_items;  // int32: tensor-core item i as i, small item j as n_tc + j
     int64_t total_bytes;
     int64_t ws_bytes;
     int64_t ws_off_lse;     // byte offsets into the workspace
@@ -115,6 +118,18 @@ struct SmallParams {
     uint32_t *status;
 };
 
+// Fused cascade kernel (tensor-core and paged roles, one persistent launch).
+struct CascadeParams {
+    const PlanHeader *plan;
+    uint64_t tag;
+    const uint16_t *q;
+    int64_t q_sb, q_sh;
+    float scale_log2;
+    float *part_o;
+    float *part_lse;
+    uint32_t *status;
+};
+
 // Merge kernel: combines the partial rows of each output row.
 struct MergeParams {
     const float *part_o;
@@ -128,6 +143,7 @@ struct MergeParams {
     const int32_t *seq_lens; // mode 1
     int32_t split_len, n_split, seqs_per_item, row_begin, rows, n_rc;
     int32_t nh;  // mode 1: KV heads per small-kernel item
+    int32_t wait_prior;  // launched as a programmatic dependent: wait for the prior grid first
     void *out;
     int32_t out_f32;
     int64_t o_sb, o_sh;
@@ -146,6 +162,10 @@ __host__ __device__ inline const T *plan_array(const PlanHeader *h, int64_t off)
 cudaError_t launch_tc(const TcParams &p, int grid, int d, cudaStream_t s);
 cudaError_t launch_small(const SmallParams &p, int grid, int d, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams &p, int64_t out_rows, cudaStream_t s);
+// The merge as a programmatic dependent launch of the preceding kernel.
+cudaError_t launch_merge_dependent(const MergeParams &p, int64_t out_rows, cudaStream_t s);
+cudaError_t launch_cascade(const CascadeParams &p, int grid, int d, cudaStream_t s);
+int cascade_heads_per_item(int Hkv);
 cudaError_t launch_merge2(const float *oa, const float *la, const float *ob, const float *lb,
                           void *o, int out_f32, float *lse, int64_t rows, int d, cudaStream_t s);
 size_t tc_smem_bytes(int d);

@@ -48,6 +48,8 @@ template <int VPT>  // values per lane: d / 32
 __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeParams p)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (p.wait_prior)
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the partial states are complete
     const int64_t row = (int64_t)blockIdx.x * kMergeWarps + warp;
     const int64_t n_rows = (int64_t)p.B * p.Hq;
     if (row >= n_rows)
@@ -199,6 +201,27 @@ cudaError_t launch_merge(const MergeParams &p, int64_t out_rows, cudaStream_t s)
     else
         hp_merge_kernel<2><<<(unsigned)grid, kMergeWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_merge_dependent(const MergeParams &p_in, int64_t out_rows, cudaStream_t s)
+{
+    if (out_rows <= 0)
+        return cudaSuccess;
+    MergeParams p = p_in;
+    p.wait_prior = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((out_rows + kMergeWarps - 1) / kMergeWarps));
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.d == 128)
+        return cudaLaunchKernelEx(&cfg, hp_merge_kernel<4>, p);
+    return cudaLaunchKernelEx(&cfg, hp_merge_kernel<2>, p);
 }
 
 cudaError_t launch_merge2(const float *oa, const float *la, const float *ob, const float *lb, void *o,

@@ -1,0 +1,337 @@
+// hp_small_role.cuh -- the paged-decode role: up to 16 query rows per KV
+// head against one key range (a private suffix, or a node shared by very few
+// sequences).  Shared by the standalone paged-decode kernel and the fused
+// cascade kernel.
+//
+// Method: the sequence-first phase of ChunkAttention ("The Sequence-First
+// Phase Kernel in Detail") / Hydragen's suffix attention: per sequence, the
+// keys of its private chunks are walked through the page list, with an
+// online softmax carrying the running (m, n, O) state of ChunkAttention
+// Eq. 1-2.  The G query heads that share a KV head are processed together
+// (each KV byte is loaded once for the whole group).
+//
+// A work item is (sequences, a group of nh consecutive KV heads, a key
+// range); consumer warp w computes KV head kvh0 + w.  A page holds all KV
+// heads of its tokens contiguously, so one TMA box covers 16 tokens x 64
+// columns x nh heads: the TMA engine costs about the same per box whatever its
+// size, and one-head 2 KB boxes would cap an SM far below HBM bandwidth.  One
+// producer warp fills a ring of K and V chunks (128-byte swizzled, so the
+// ldmatrix reads are conflict free) and writes, per stage, the item fields
+// the consumers need; the consumers release a stage by arriving on its
+// "empty" barrier.  Scores and P V use the m16n8k16 bf16 MMA with f32
+// accumulation: rows are the (up to 16) query rows of a head, S = Q K^T for
+// 16 keys is two n8 tiles, and O = P V reuses the S accumulator layout as the
+// A operand.  The producer runs ahead across item boundaries.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "hp_internal.h"
+#include "hp_ptx.cuh"
+
+namespace hp {
+namespace smr {
+
+constexpr float kLn2 = 0.69314718055994530942f;
+
+// Shared memory of the role for NC consumer warps and S stages.
+template <int D, int NC, int S>
+struct Layout {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kHeadBox = 16 * 128;     // one head: [16 tokens][64 bf16], swizzled
+    static constexpr int kHalf = NC * kHeadBox;   // one column half of the head group
+    static constexpr int kChunk = kHalves * kHalf;  // K (or V) of one 16-token chunk
+    static constexpr int kStage = 2 * kChunk;       // K then V
+    static constexpr int kEnd = S * kStage;
+};
+
+// What the consumers need about the chunk in a stage.
+struct StageMeta {
+    int seq_begin, n_seq, kvh0, part_row;
+    int nvalid;  // valid keys of the chunk (0 when its page id was out of range)
+    int first, last;
+    int pad;
+};
+
+// The geometry of one item.
+struct Desc {
+    int valid;
+    int seq_begin, n_seq, kvh0, k0, k1, part_row;
+    const int32_t *pages;
+    int ps, num_pages;
+    const void *map_k;
+    const void *map_v;
+};
+
+struct Ctx {
+    uint8_t *smem;   // 1024-aligned base of the ring
+    uint32_t sbase;
+    uint32_t full0;  // S "full" barriers (count 1 + transaction bytes)
+    uint32_t empty0; // S "empty" barriers (count nh)
+    StageMeta *meta; // S entries
+    volatile int *abort;
+    uint32_t *status;
+};
+
+struct Args {
+    const uint16_t *q;
+    int64_t q_sb, q_sh;
+    int G, nh;
+    float scale_log2;
+    float *part_o;
+    float *part_lse;
+};
+
+// Producer warp: walks items k = 0, 1, ... of `src` (src(k) -> Desc, with
+// n_items entries), then closes the ring with a sentinel stage (n_seq = -1,
+// completed by a plain arrival) that tells the consumers to stop.  All 32
+// lanes call it.
+template <int D, int NC, int S, class Src>
+__device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src &src, int n_items, int lane)
+{
+    using L = Layout<D, NC, S>;
+    constexpr int kHalves = D / 64;
+    auto wait_warp = [&](uint32_t b, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
+    };
+    uint32_t k = 0;  // chunks issued
+    bool ok = true;
+    bool prefetched = false;
+    for (int it = 0; ok && it < n_items; ++it) {
+        const Desc d = src(it);
+        if (!d.valid)
+            continue;
+        if (!prefetched && lane == 0) {
+            prefetch_tensormap(d.map_k);
+            prefetch_tensormap(d.map_v);
+            prefetched = true;
+        }
+        const int nchunks = (d.k1 - d.k0 + kChunk - 1) / kChunk;
+        int pg = 0;
+        for (int ch = 0; ch < nchunks; ++ch, ++k) {
+            if ((ch & 31) == 0) {  // page ids of the next 32 chunks, one per lane
+                const int cc = ch + lane;
+                pg = cc < nchunks ? __ldg(d.pages + (d.k0 + cc * kChunk) / d.ps) : 0;
+            }
+            const uint32_t st = k % S;
+            if (k >= (uint32_t)S && !(ok = wait_warp(c.empty0 + 8 * st, ((k / S) - 1) & 1u)))
+                break;
+            int page = __shfl_sync(0xffffffffu, pg, ch & 31);
+            const bool oob = (unsigned)page >= (unsigned)d.num_pages;
+            if (oob)
+                page = d.num_pages;  // zero-filled boxes, chunk masked
+            const int t = d.k0 + ch * kChunk;
+            const uint32_t bar = c.full0 + 8 * st;
+            if (lane == 0) {
+                if (oob)
+                    atomicOr(c.status, kStBounds);
+                StageMeta m;
+                m.seq_begin = d.seq_begin;
+                m.n_seq = d.n_seq;
+                m.kvh0 = d.kvh0;
+                m.part_row = d.part_row;
+                m.nvalid = oob ? 0 : min(kChunk, d.k1 - t);
+                m.first = ch == 0;
+                m.last = ch + 1 == nchunks;
+                m.pad = 0;
+                c.meta[st] = m;
+                mbar_arrive_expect_tx(bar, 2 * kHalves * a.nh * L::kHeadBox);
+            }
+            __syncwarp();
+            if (lane < 2 * kHalves) {
+                const int h = lane % kHalves;
+                const bool is_v = lane >= kHalves;
+                tma_load_4d(c.sbase + st * L::kStage + (is_v ? L::kChunk : 0) + h * L::kHalf,
+                            is_v ? d.map_v : d.map_k, bar, h * 64, t % d.ps, d.kvh0, page);
+            }
+        }
+    }
+    // sentinel stage
+    {
+        const uint32_t st = k % S;
+        if (k >= (uint32_t)S)
+            wait_warp(c.empty0 + 8 * st, ((k / S) - 1) & 1u);
+        if (lane == 0) {
+            StageMeta m{};
+            m.n_seq = -1;
+            c.meta[st] = m;
+            mbar_arrive(c.full0 + 8 * st);
+        }
+        __syncwarp();
+        ++k;
+    }
+    // every copy issued has landed before the role ends
+    if (lane == 0)
+        for (uint32_t j = k > (uint32_t)S ? k - S : 0; j < k; ++j)
+            mbar_wait_drain(c.full0 + 8 * (j % S), (j / S) & 1u);
+}
+
+// Consumer warp w (0 <= w < nh): processes the chunks in ring order until
+// the producer's sentinel stage.
+template <int D, int NC, int S>
+__device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int lane)
+{
+    using L = Layout<D, NC, S>;
+    constexpr int kHalves = D / 64;
+    constexpr int kKs = D / 16;  // k-steps of the S MMA
+    constexpr int kNt = D / 8;   // n8 tiles of O
+    auto wait_warp = [&](uint32_t b, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
+    };
+    uint32_t qa[kKs][4];
+    float o[kNt][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int r0 = lane >> 2, r1 = r0 + 8;
+    const int tq = 2 * (lane & 3);
+    const uint32_t hoff = (uint32_t)w * L::kHeadBox;  // this warp's head within a box
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t st = k % S;
+        if (!wait_warp(c.full0 + 8 * st, (k / S) & 1u))
+            break;
+        const StageMeta m = c.meta[st];
+        if (m.n_seq < 0)
+            break;  // sentinel: the producer's walk is over
+        const int rows = m.n_seq * a.G;
+        const int kvh = m.kvh0 + w;
+        if (m.first) {
+            // new item: query fragments (A operand, rows r0 / r1) and state
+            const uint16_t *q0 = nullptr, *q1 = nullptr;
+            if (r0 < rows)
+                q0 = a.q + (int64_t)(m.seq_begin + r0 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r0 % a.G) * a.q_sh;
+            if (r1 < rows)
+                q1 = a.q + (int64_t)(m.seq_begin + r1 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r1 % a.G) * a.q_sh;
+#pragma unroll
+            for (int ks = 0; ks < kKs; ++ks) {
+                qa[ks][0] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + ks * 16 + tq)) : 0u;
+                qa[ks][1] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + ks * 16 + tq)) : 0u;
+                qa[ks][2] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + ks * 16 + 8 + tq)) : 0u;
+                qa[ks][3] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + ks * 16 + 8 + tq)) : 0u;
+            }
+#pragma unroll
+            for (int n = 0; n < kNt; ++n)
+                o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+        }
+        const uint32_t kst = c.sbase + st * L::kStage + hoff;
+        const uint32_t vst = kst + L::kChunk;
+        const int nvalid = m.nvalid;
+        if (nvalid < kChunk) {
+            // rows past the valid keys: zero this head's V so that
+            // 0 * (whatever the pool holds there) stays 0
+            uint8_t *vp = c.smem + (vst - c.sbase);
+            const int nz = (kChunk - nvalid) * 8 * kHalves;
+            for (int i = lane; i < nz; i += 32) {
+                const int row = nvalid + i / (8 * kHalves);
+                const int rem = i % (8 * kHalves);
+                const int h = rem >> 3, ch = rem & 7;
+                *reinterpret_cast<uint4 *>(vp + h * L::kHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // S = Q K^T over 16 keys: n8 tile 0 = keys 0-7, tile 1 = keys 8-15
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int tok = ri + ((mi >> 1) << 3);
+#pragma unroll
+            for (int ks = 0; ks < kKs; ++ks) {
+                const int dch = 2 * ks + (mi & 1);
+                const uint32_t addr = kst + (dch >> 3) * L::kHalf + tok * 128 + (((dch & 7) ^ (tok & 7)) << 4);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(addr, b0, b1, b2, b3);
+                mma_bf16_16816(s0, qa[ks], b0, b1);
+                mma_bf16_16816(s1, qa[ks], b2, b3);
+            }
+        }
+        // online softmax (rows r0: elements 0,1; rows r1: elements 2,3)
+        const float cs = a.scale_log2;
+        float x[2][4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int tk = tq + (e & 1);
+            x[0][e] = tk < nvalid ? s0[e] * cs : -INFINITY;
+            x[1][e] = tk + 8 < nvalid ? s1[e] * cs : -INFINITY;
+        }
+        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;  // all keys so far masked: nothing to scale
+        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float a0 = fast_exp2(m0 - ms0), a1 = fast_exp2(m1 - ms1);
+        m0 = mn0;
+        m1 = mn1;
+        if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+            for (int n = 0; n < kNt; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
+            }
+            l0 *= a0;
+            l1 *= a1;
+        }
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(fast_exp2(x[0][0] - ms0), fast_exp2(x[0][1] - ms0));
+        pa[1] = pack_bf16x2(fast_exp2(x[0][2] - ms1), fast_exp2(x[0][3] - ms1));
+        pa[2] = pack_bf16x2(fast_exp2(x[1][0] - ms0), fast_exp2(x[1][1] - ms0));
+        pa[3] = pack_bf16x2(fast_exp2(x[1][2] - ms1), fast_exp2(x[1][3] - ms1));
+        l0 += bf16lo_to_f32(pa[0]) + bf16hi_to_f32(pa[0]) + bf16lo_to_f32(pa[2]) + bf16hi_to_f32(pa[2]);
+        l1 += bf16lo_to_f32(pa[1]) + bf16hi_to_f32(pa[1]) + bf16lo_to_f32(pa[3]) + bf16hi_to_f32(pa[3]);
+
+        // O += P V
+        {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int tok = ri + ((mi & 1) << 3);
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+                const int dch = 2 * dp + (mi >> 1);
+                const uint32_t addr = vst + (dch >> 3) * L::kHalf + tok * 128 + (((dch & 7) ^ (tok & 7)) << 4);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * dp], pa, b0, b1);
+                mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+            }
+        }
+        // release the stage to the producer
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(c.empty0 + 8 * st);
+
+        if (m.last) {
+            float L0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+            L0 += __shfl_xor_sync(0xffffffffu, L0, 2);
+            float L1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+            L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
+            const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f;
+            const float inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+            const int base = m.part_row + w * rows;  // this head's rows
+            if (r0 < rows) {
+                float *dst = a.part_o + (size_t)(base + r0) * D + tq;
+#pragma unroll
+                for (int n = 0; n < kNt; ++n)
+                    *reinterpret_cast<float2 *>(dst + n * 8) = make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                if ((lane & 3) == 0)
+                    a.part_lse[base + r0] = L0 > 0.f ? (m0 + fast_log2(L0)) * kLn2 : -INFINITY;
+            }
+            if (r1 < rows) {
+                float *dst = a.part_o + (size_t)(base + r1) * D + tq;
+#pragma unroll
+                for (int n = 0; n < kNt; ++n)
+                    *reinterpret_cast<float2 *>(dst + n * 8) = make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                if ((lane & 3) == 0)
+                    a.part_lse[base + r1] = L1 > 0.f ? (m1 + fast_log2(L1)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+}
+
+}  // namespace smr
+}  // namespace hp

@@ -1,0 +1,489 @@
+// hp_tc_role.cuh -- the tensor-core role: batched attention of stacked
+// queries against one shared tree node, for one work item, by a 384-thread
+// CTA.  Shared by the standalone prefix kernel and the fused cascade kernel.
+//
+// Method: the queries of every sequence below a shared node are stacked into
+// one matrix (Hydragen, "Inter-Sequence Batched Prefix Attention"; with GQA
+// the G query heads of a KV head are further rows, shared-prefix KV caching
+// blog, "Splitting attention at the prefix boundary"), so S = Q K^T and
+// O = P V are matrix-matrix products and the node's KV is read once.  The key
+// range of a node is split across items (ChunkAttention's extra partition of
+// the chunk axis, "The Chunk-First Phase Kernel in Detail"); an item runs an
+// online softmax over its 128-key tiles (the running max / sum state of
+// ChunkAttention Eq. 1-2) and writes a partial (O, LSE) per row, merged later
+// by log-sum-exp.
+//
+// One item: up to 256 query rows (two M=128 blocks) x one key range.  Roles:
+//   warp 0      TMA producer: K and V tiles (128 keys x d, 128-byte swizzle)
+//               through a 2-stage ring, all boxes of a tile issued by several
+//               lanes in one instruction (a TMA box costs about the same
+//               whatever its size; one thread issuing boxes one by one caps
+//               an SM far below HBM bandwidth).  The first two tiles are
+//               issued before Q is staged.
+//   warp 1      TMEM owner and MMA issuer (one thread):
+//               S_mb = Q_mb K^T (A, B from shared memory) into TMEM,
+//               O_mb += P_mb V   (A = P from TMEM, B = V from shared memory).
+//   warps 1-11  stage Q (warp 0 stages page ids meanwhile).
+//   warps 4-7   softmax for rows 0-127, warps 8-11 for rows 128-255: read a
+//               128-column score row from TMEM, max / exp2 / row sum, write P
+//               (bf16) over the S columns, rescale O in TMEM when the max
+//               grows by more than 2^8 (the reference max is kept otherwise;
+//               exact, since the final O / l uses the same reference), and at
+//               the end stage O through shared memory so the partial rows are
+//               written as whole 512-byte rows.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
+// The two row blocks ping-pong: S of block 1 is computed while block 0 runs
+// its softmax, and S of tile j+1 is issued right after P V of tile j.
+//
+// Register split: warpgroup 0 (producer, MMA, two helpers) lowers its count,
+// the softmax warpgroups raise theirs; the caller issues setmaxnreg at the
+// top of each branch so the compiler budgets each role's code accordingly.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "hp_internal.h"
+#include "hp_ptx.cuh"
+
+namespace hp {
+namespace tcr {
+
+constexpr int kMaxBoxes = 1024;  // page-id slots staged per item
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 136, kRegsSoftmax = 184;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax == kThreads * kRegsLaunch, "register split");
+constexpr float kTau = 8.0f;  // lazy rescale threshold, log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct Layout {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kRegion = 128 * 128;  // [128 rows][64 bf16] swizzled, 16 KB
+    static constexpr int kTile = kHalves * kRegion;
+    static constexpr int kQ = 0;  // [mb][half] regions
+    static constexpr int kK = kQ + 2 * kTile;
+    static constexpr int kV = kK + 2 * kTile;
+    static constexpr int kEnd = kV + 2 * kTile;  // O staging reuses K (block 0) and V (block 1)
+    static_assert(2 * kTile >= 128 * D * 4, "O staging must fit one ring");
+};
+
+// barrier slots (8 bytes each) at the caller's barrier area
+enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_S = 8, B_P = 10, B_O = 12, B_DRAIN = 14,
+       B_COUNT = 15 };
+
+struct ItemGeo {
+    int seq_begin, n_seq, kvh, k0, k1, part_row;
+    const int32_t *pages;  // the node's page list (paged mode)
+    int paged, ps, box, num_pages;
+    const void *map_k;
+    const void *map_v;
+};
+
+// Per-CTA resources of the role.
+struct Ctx {
+    uint8_t *smem;        // 1024-aligned base of the role's layout
+    uint32_t sbase;       // its shared-window address
+    uint32_t bar0;        // B_COUNT barriers
+    int32_t *s_pages;     // kMaxBoxes page-id slots
+    uint32_t *tmem_slot;  // TMEM base address written by tcgen05.alloc
+    volatile int *abort;
+    uint32_t *status;
+};
+
+struct Args {
+    const uint16_t *q;
+    int64_t q_sb, q_sh;
+    int G;
+    float scale_log2;  // > 0
+    float *part_o;
+    float *part_lse;
+};
+
+__device__ __forceinline__ uint32_t bar_at(const Ctx &c, int i) { return c.bar0 + 8u * (uint32_t)i; }
+
+__device__ __forceinline__ void named_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void mbar_inval(uint32_t bar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool item_ok(const ItemGeo &g, int G)
+{
+    const int nmb = (g.n_seq * G + 127) >> 7;
+    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
+    const int n_boxes = g.paged ? n_tiles * (kTcTile / g.box) : 0;
+    return nmb >= 1 && nmb <= 2 && n_tiles > 0 && n_boxes <= kMaxBoxes;
+}
+
+// Issue the TMA copies of one 128-key tile (K or V) into `dst`, one box per
+// lane (box, column half).  Paged items take each box's page from the ids
+// staged in shared memory.
+template <int D>
+__device__ __forceinline__ void issue_tile(const ItemGeo &g, const int32_t *s_pages, const void *map,
+                                           uint32_t dst, uint32_t bar, int tile, int lane)
+{
+    constexpr int kHalves = D / 64;
+    if (lane == 0)
+        mbar_arrive_expect_tx(bar, Layout<D>::kTile);
+    __syncwarp();
+    const int kt0 = g.k0 + tile * kTcTile;
+    if (g.paged) {
+        const int nbox = kTcTile / g.box;
+        for (int l = lane; l < nbox * kHalves; l += 32) {
+            const int bx = l / kHalves, h = l - bx * kHalves;
+            const int t = kt0 + bx * g.box;
+            tma_load_4d(dst + h * Layout<D>::kRegion + bx * g.box * 128, map, bar, h * 64, t % g.ps, g.kvh,
+                        s_pages[tile * nbox + bx]);
+        }
+    } else if (lane < kHalves) {
+        tma_load_3d(dst + lane * Layout<D>::kRegion, map, bar, lane * 64, g.kvh, kt0);
+    }
+}
+
+// Q staging share of one thread (qt in [0, nthreads)): rows r = s*G + g of
+// the item (rows past the item zero) in the 128-byte-swizzled K-major layout
+// the MMA descriptors describe.  All loads of a thread before its stores.
+template <int D, int kQThreads>
+__device__ __forceinline__ void stage_q(const Ctx &c, const ItemGeo &g, const Args &a, int qt)
+{
+    constexpr int kHalves = D / 64;
+    constexpr int kCpr = D / 8;  // 16-byte chunks per row
+    constexpr int kPer = (2 * 128 * kCpr + kQThreads - 1) / kQThreads;
+    const int rows_total = g.n_seq * a.G;
+    const int nmb = (rows_total + 127) >> 7;
+    const int total = nmb * 128 * kCpr;
+    uint4 buf[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = qt + k * kQThreads;
+        const int r = i / kCpr;
+        buf[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < total && r < rows_total) {
+            const int ch = i % kCpr;
+            const int s = r / a.G;
+            const int gg = r - s * a.G;
+            const uint16_t *src =
+                a.q + (int64_t)(g.seq_begin + s) * a.q_sb + (int64_t)(g.kvh * a.G + gg) * a.q_sh + ch * 8;
+            buf[k] = __ldg(reinterpret_cast<const uint4 *>(src));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = qt + k * kQThreads;
+        if (i < total) {
+            const int r = i / kCpr, ch = i % kCpr;
+            const int mb = r >> 7, rr = r & 127, h = ch >> 3, cc = ch & 7;
+            uint8_t *dst =
+                c.smem + Layout<D>::kQ + ((mb * kHalves + h) * 128 + rr) * 128 + ((cc ^ (rr & 7)) << 4);
+            *reinterpret_cast<uint4 *>(dst) = buf[k];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- phase A
+// Warp 0: (re)initialise the barriers, stage the page ids, issue the first
+// tiles.  Call with all 32 lanes; `reinit` when the barriers were used by an
+// earlier item (the CTA has synchronised since).
+template <int D>
+__device__ __forceinline__ void producer_prologue(const Ctx &c, const ItemGeo &g, bool reinit, int lane)
+{
+    using L = Layout<D>;
+    if (lane == 0) {
+        for (int i = 0; i < B_COUNT; ++i) {
+            if (reinit)
+                mbar_inval(bar_at(c, i));
+            mbar_init(bar_at(c, i), (i == B_P || i == B_P + 1) ? 128u : 1u);
+        }
+        *c.abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(g.map_k);
+        prefetch_tensormap(g.map_v);
+    }
+    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
+    if (g.paged) {
+        const int nbox = kTcTile / g.box;
+        const int n_boxes = n_tiles * nbox;
+        for (int i = lane; i < n_boxes; i += 32) {
+            const int t = g.k0 + (i / nbox) * kTcTile + (i % nbox) * g.box;
+            int page = g.num_pages;  // out of range: the box is zero-filled
+            if (t < g.k1) {
+                page = __ldg(g.pages + t / g.ps);
+                if ((unsigned)page >= (unsigned)g.num_pages) {
+                    atomicOr(c.status, kStBounds);
+                    page = g.num_pages;
+                }
+            }
+            c.s_pages[i] = page;
+        }
+    }
+    __syncwarp();
+    const int pre = n_tiles < 2 ? n_tiles : 2;
+    for (int j = 0; j < pre; ++j) {
+        issue_tile<D>(g, c.s_pages, g.map_k, c.sbase + L::kK + j * L::kTile, bar_at(c, B_KFULL + j), j, lane);
+        issue_tile<D>(g, c.s_pages, g.map_v, c.sbase + L::kV + j * L::kTile, bar_at(c, B_VFULL + j), j, lane);
+    }
+}
+
+// ---------------------------------------------------------------- phase B
+template <int D>
+__device__ __forceinline__ void producer_loop(const Ctx &c, const ItemGeo &g, int lane)
+{
+    using L = Layout<D>;
+    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
+    const int pre = n_tiles < 2 ? n_tiles : 2;
+    auto wait_warp = [&](int b, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar_at(c, b), parity, c.status, c.abort)) != 0;
+    };
+    int issued = pre;
+    for (int j = pre; j < n_tiles; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+        if (!wait_warp(B_KEMPTY + st, ph ^ 1u))
+            break;
+        issue_tile<D>(g, c.s_pages, g.map_k, c.sbase + L::kK + st * L::kTile, bar_at(c, B_KFULL + st), j, lane);
+        if (!wait_warp(B_VEMPTY + st, ph ^ 1u)) {
+            if (lane == 0)
+                mbar_wait_drain(bar_at(c, B_KFULL + st), ph);  // K of tile j is in flight
+            break;
+        }
+        issue_tile<D>(g, c.s_pages, g.map_v, c.sbase + L::kV + st * L::kTile, bar_at(c, B_VFULL + st), j, lane);
+        issued = j + 1;
+    }
+    // every load issued has landed before the item ends
+    if (lane == 0) {
+        for (int j = max(0, issued - 2); j < issued; ++j) {
+            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+            mbar_wait_drain(bar_at(c, B_KFULL + (j & 1)), ph);
+            mbar_wait_drain(bar_at(c, B_VFULL + (j & 1)), ph);
+        }
+    }
+}
+
+// One thread (warp 1, lane 0).
+template <int D>
+__device__ __forceinline__ void mma_loop(const Ctx &c, const ItemGeo &g, int G, uint32_t tmem)
+{
+    using L = Layout<D>;
+    constexpr int kHalves = D / 64;
+    constexpr uint32_t kIdescQK = umma_idesc_bf16(128, 128, false);
+    constexpr uint32_t kIdescPV = umma_idesc_bf16(128, D, true);
+    const int nmb = (g.n_seq * G + 127) >> 7;
+    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
+    const uint32_t qa = c.sbase + L::kQ;
+    auto issue_s = [&](int mb, int st) {
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const int h = ks >> 2, kin = ks & 3;
+            const uint64_t a = umma_desc_sw128(qa + (mb * kHalves + h) * L::kRegion + kin * 32, 16, 1024);
+            const uint64_t b =
+                umma_desc_sw128(c.sbase + L::kK + st * L::kTile + h * L::kRegion + kin * 32, 16, 1024);
+            tc_mma_ss(tmem + mb * 128, a, b, kIdescQK, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(bar_at(c, B_S + mb));
+    };
+    auto issue_pv = [&](int mb, int st, int j) {
+        for (int ks = 0; ks < kTcTile / 16; ++ks) {
+            const uint64_t b = umma_desc_sw128(c.sbase + L::kV + st * L::kTile + ks * 2048, L::kRegion, 1024);
+            tc_mma_ts(tmem + 256 + mb * 128, tmem + mb * 128 + ks * 8, b, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc_commit(bar_at(c, B_O + mb));
+    };
+    bool ok = mbar_wait(bar_at(c, B_KFULL + 0), 0u, c.status, c.abort);
+    if (ok) {
+        tc_fence_after();
+        for (int mb = 0; mb < nmb; ++mb)
+            issue_s(mb, 0);
+        tc_commit(bar_at(c, B_KEMPTY + 0));
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+        if (!(ok = mbar_wait(bar_at(c, B_VFULL + st), ph, c.status, c.abort)))
+            break;
+        const bool more = j + 1 < n_tiles;
+        const int st1 = (j + 1) & 1;
+        for (int mb = 0; mb < nmb; ++mb) {
+            if (!(ok = mbar_wait(bar_at(c, B_P + mb), (uint32_t)j & 1u, c.status, c.abort)))
+                break;
+            tc_fence_after();
+            issue_pv(mb, st, j);
+            if (more) {
+                if (mb == 0) {
+                    if (!(ok = mbar_wait(bar_at(c, B_KFULL + st1), (uint32_t)((j + 1) >> 1) & 1u, c.status,
+                                         c.abort)))
+                        break;
+                    tc_fence_after();
+                }
+                issue_s(mb, st1);
+            }
+        }
+        if (!ok)
+            break;
+        tc_commit(bar_at(c, B_VEMPTY + st));
+        if (more)
+            tc_commit(bar_at(c, B_KEMPTY + st1));
+    }
+    // every MMA issued has completed before the item ends
+    tc_commit(bar_at(c, B_DRAIN));
+    mbar_wait_drain(bar_at(c, B_DRAIN), 0u);
+}
+
+// Warps 4-11 (mb = 0 for warps 4-7, 1 for 8-11).
+template <int D>
+__device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, const Args &a, uint32_t tmem,
+                                             int warp, int lane, int tid)
+{
+    using L = Layout<D>;
+    constexpr int kHalves = D / 64;
+    const int rows_total = g.n_seq * a.G;
+    const int nmb = (rows_total + 127) >> 7;
+    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
+    const int mb = (warp - 4) >> 2;
+    const int rr = tid - 128 * (1 + mb);  // row within the block == TMEM lane
+    const int row = mb * 128 + rr;
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = tl + mb * 128;
+    const uint32_t o_col = tl + 256 + mb * 128;
+    const float cs = a.scale_log2;
+    auto wait_warp = [&](int b, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar_at(c, b), parity, c.status, c.abort)) != 0;
+    };
+    float m_run = -INFINITY;  // reference max, log2 units
+    float l_run = 0.f;
+    bool ok = mb < nmb;
+    uint32_t sv[128];
+    uint32_t r[32];
+    for (int j = 0; ok && j < n_tiles; ++j) {
+        if (!(ok = wait_warp(B_S + mb, (uint32_t)j & 1u)))
+            break;
+        tc_fence_after();
+        const int nvalid = min(kTcTile, g.k1 - (g.k0 + j * kTcTile));
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+            tmem_ld32(s_col + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[cc * 32]));
+        tmem_ld_wait();
+        // the scale is positive: the largest scaled score is the largest raw
+        // score times the scale
+        float mx = -INFINITY;
+        if (nvalid >= kTcTile) {
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+                mx = fmaxf(mx, __uint_as_float(sv[i]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+                if (i < nvalid)
+                    mx = fmaxf(mx, __uint_as_float(sv[i]));
+        }
+        const float tmax = mx * cs;
+        const bool need = tmax > m_run + kTau;
+        const float alpha = need ? fast_exp2(m_run - tmax) : 1.f;
+        if (need) {
+            l_run *= alpha;
+            m_run = tmax;
+        }
+        // P = exp2(s * c - m) as bf16 pairs over the S columns
+        const float nm = -m_run;
+        float lsum = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int c0 = cc * 32 + 2 * i;
+                float p0 = fast_exp2(fmaf(__uint_as_float(sv[c0]), cs, nm));
+                float p1 = fast_exp2(fmaf(__uint_as_float(sv[c0 + 1]), cs, nm));
+                if (nvalid < kTcTile) {
+                    p0 = c0 < nvalid ? p0 : 0.f;
+                    p1 = c0 + 1 < nvalid ? p1 : 0.f;
+                }
+                lsum += p0 + p1;
+                pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(s_col + cc * 16, pk);
+        }
+        l_run += lsum;
+        // O was accumulated against the old reference max: rescale it once
+        // the previous P V has landed (rare: the max grew by more than 2^kTau)
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+            if (!(ok = wait_warp(B_O + mb, (uint32_t)(j - 1) & 1u)))
+                break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                tmem_ld32(o_col + cc * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                tmem_st32(o_col + cc * 32, r);
+            }
+        }
+        tmem_st_wait();
+        if (mb == 0 && nvalid < kTcTile) {
+            // last, partial tile: rows past the node hold whatever the pool
+            // holds there; zero their V so 0 * garbage stays 0
+            const int st = j & 1;
+            if (!(ok = wait_warp(B_VFULL + st, (uint32_t)(j >> 1) & 1u)))
+                break;
+            if (rr >= nvalid) {
+                for (int h = 0; h < kHalves; ++h) {
+                    uint4 *vrow = reinterpret_cast<uint4 *>(c.smem + L::kV + st * L::kTile + h * L::kRegion + rr * 128);
+#pragma unroll
+                    for (int qd = 0; qd < 8; ++qd)
+                        vrow[qd] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(bar_at(c, B_P + mb));
+    }
+    // Epilogue: O / l through shared memory (block 0 over the K ring, block 1
+    // over the V ring, both idle once the last P V has completed), row-major
+    // with the 16-byte chunks of each 128-byte group permuted by the row
+    // (conflict-free writes), then each warp writes whole rows.
+    const bool have = ok && mb < nmb;
+    if (have && wait_warp(B_O + mb, (uint32_t)(n_tiles - 1) & 1u)) {
+        tc_fence_after();
+        const float inv = 1.f / l_run;
+        uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+            tmem_ld32(o_col + cc * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int ch = cc * 8 + i;                       // logical 16-byte chunk
+                const int pc = (ch & ~7) | ((ch ^ rr) & 7);      // physical chunk
+                *reinterpret_cast<float4 *>(stg + rr * (D * 4) + pc * 16) =
+                    make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+            }
+        }
+        if (row < rows_total)
+            a.part_lse[g.part_row + row] = (m_run + fast_log2(l_run)) * kLn2;
+    }
+    tc_fence_before();
+    named_sync(1 + mb, 128);
+    if (have) {
+        const uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
+        const int wq = warp & 3;
+        const int rows_here = min(128, rows_total - mb * 128);
+        constexpr int kChunksRow = D / 4;  // 16-byte chunks per f32 row
+        for (int rw = wq; rw < rows_here; rw += 4) {
+            float *dst = a.part_o + (size_t)(g.part_row + mb * 128 + rw) * D;
+            for (int ch = lane; ch < kChunksRow; ch += 32) {
+                const int pc = (ch & ~7) | ((ch ^ rw) & 7);
+                *reinterpret_cast<float4 *>(dst + ch * 4) =
+                    *reinterpret_cast<const float4 *>(stg + rw * (D * 4) + pc * 16);
+            }
+        }
+    }
+}
+
+}  // namespace tcr
+}  // namespace hp
