@@ -196,6 +196,8 @@ typedef struct {
     int32_t n_tc_items;    /* shared-node items (tensor-core role) */
     int32_t n_small_items; /* small-row items (private suffixes, narrow nodes) */
     int32_t grid;          /* CTAs of the step's persistent launch (one per SM) */
+    int32_t rec_stride;    /* bytes of each CTA's schedule record in the plan */
+    int32_t num_levels;
     int32_t reserved;
     int64_t n_part_rows;   /* partial (O, LSE) rows in the workspace */
     int64_t plan_bytes;
@@ -219,7 +221,11 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
 
 /* One cascade decode step: every sequence, every head, all levels, merged.
  * q, out, lse as in the conventions above, for all B sequences; q strides
- * multiples of 8 elements and q 16-byte aligned.  ws: >= info->ws_bytes.
+ * multiples of 8 elements, positive, and q 16-byte aligned (q is read by TMA).
+ * ws: >= info->ws_bytes.  plan_dev must hold the plan hp_cascade_plan last
+ * wrote there in this process, and info must describe a plan no larger than
+ * it (HP_ERR_ARG otherwise, before any launch); an info of another plan of the
+ * same size is reported by the kernels through the status word.
  * No host synchronisation, no allocation; graph-capturable. */
 hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, const void *q,
                             int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,

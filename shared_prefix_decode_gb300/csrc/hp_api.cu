@@ -10,6 +10,7 @@
 #include <mutex>
 #include <numeric>
 #include <queue>
+#include <unordered_map>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -20,7 +21,7 @@ using namespace hp;
 
 namespace {
 
-constexpr int32_t kAbiVersion = 1;
+constexpr int32_t kAbiVersion = 2;
 // A tensor-core item processes at least this many 128-key tiles (its fixed
 // set-up -- TMEM allocation, Q staging, pipeline fill -- is amortised over
 // them) and at most kMaxTcTiles (its page ids must fit the staging area).
@@ -101,11 +102,12 @@ bool encode_prefix_map(CUtensorMap *m, const void *base, int len, int Hkv, int d
 
 bool supported_d(int d) { return d == 64 || d == 128; }
 
-// q (and out) rows are read as 16-byte vectors by the tensor-core kernel and
-// 4-byte words by the small kernel.
-bool q_layout_ok(const void *q, int64_t q_sb, int64_t q_sh)
+// q rows are read by TMA (16-byte aligned base and strides, positive
+// strides where the dimension has more than one entry).
+bool q_layout_ok(const void *q, int64_t q_sb, int64_t q_sh, int B, int Hq)
 {
-    return aligned(q, 16) && q_sb % 8 == 0 && q_sh % 8 == 0 && q_sb >= 0 && q_sh >= 0;
+    return aligned(q, 16) && q_sb % 8 == 0 && q_sh % 8 == 0 && (B == 1 || q_sb > 0) && (Hq == 1 || q_sh > 0) &&
+           q_sb >= 0 && q_sh >= 0 && q_sb < ((int64_t)1 << 38) && q_sh < ((int64_t)1 << 38);
 }
 
 bool out_layout_ok(const void *out, hp_dtype dt, int64_t o_sb, int64_t o_sh, int d)
@@ -160,7 +162,7 @@ struct PrefixGeo {
 PrefixGeo prefix_geo(int rows, int G, int Hkv, int len, int sms)
 {
     PrefixGeo g{};
-    g.spi = std::max(1, kTcMaxRows / G);
+    g.spi = 2 * (kTcTile / G);
     g.spi = std::min(g.spi, std::max(rows, 1));
     g.n_rc = (int)ceil_div(rows, g.spi);
     const int64_t tiles = ceil_div(std::max(len, 1), kTcTile);
@@ -177,66 +179,111 @@ struct HostPlan {
     PlanHeader hdr;
     std::vector<CUtensorMap> maps;
     std::vector<WorkItem> tc, small;
-    std::vector<int32_t> page_ids;
+    std::vector<int32_t> page_ids;     // all levels' page ids, concatenated
+    std::vector<int32_t> level_ps;     // page size per level
     std::vector<int32_t> merge_ptr, merge_idx;
-    std::vector<int32_t> cta_ptr, cta_ntc, cta_items;  // per-CTA schedule of the fused kernel
+    std::vector<std::vector<int32_t>> cta_tc, cta_small;  // item ids per CTA of the fused kernel
+    std::vector<std::vector<uint8_t>> records;           // one per CTA, without the tag
     std::vector<int32_t> contexts;  // (level, node, seq_begin, seq_end, pass) x n
 };
 
-// Longest-first greedy schedule of the fused kernel's items over `grid` CTAs.
-// Cost of an item: a fixed set-up plus its KV bytes at one SM's share of HBM
-// bandwidth (~44 GB/s when every SM streams).  Each CTA runs its tensor-core
-// items first, then its paged items, each group longest first.
-void schedule(HostPlan &P, int grid, int d)
+// Page ids an item's record entry holds: the pages of keys [k0, k1).
+int64_t item_pages(const WorkItem &w, int ps) { return (int64_t)(w.k1 - 1) / ps - w.k0 / ps + 1; }
+
+// Longest-first greedy schedule of the fused kernel's items over `grid` CTAs,
+// each CTA's record kept within kRecMaxBytes.  Cost of an item: a fixed
+// set-up plus its KV bytes at one SM's share of HBM bandwidth (~44 GB/s when
+// every SM streams); a tensor-core item's set-up (Q, TMEM, two row blocks of
+// epilogue) is larger.  Each CTA runs its tensor-core items first.
+hp_status schedule(HostPlan &P, int grid, int d)
 {
     const double kBytesPerNs = 44.0;
     struct Job {
         double cost;
         int32_t id;
         bool tc;
+        int64_t rec_bytes;
     };
     std::vector<Job> jobs;
-    const int n_tc = (int)P.tc.size();
-    for (int i = 0; i < n_tc; ++i) {
+    for (size_t i = 0; i < P.tc.size(); ++i) {
         const WorkItem &w = P.tc[i];
         const double bytes = (double)(w.k1 - w.k0) * d * 4;
-        jobs.push_back({2000.0 + bytes / kBytesPerNs, i, true});
+        jobs.push_back({4000.0 + bytes / kBytesPerNs, (int32_t)i, true,
+                        (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
     }
     const int nh = P.hdr.small_nh;
     for (size_t j = 0; j < P.small.size(); ++j) {
         const WorkItem &w = P.small[j];
         const double bytes = (double)(w.k1 - w.k0) * nh * w.n_seq * d * 4;
-        jobs.push_back({500.0 + bytes / kBytesPerNs, (int32_t)(n_tc + j), false});
+        jobs.push_back({800.0 + bytes / kBytesPerNs, (int32_t)j, false,
+                        (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
     }
     std::stable_sort(jobs.begin(), jobs.end(), [](const Job &a, const Job &b) { return a.cost > b.cost; });
-    using Slot = std::pair<double, int>;
-    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-    for (int c = 0; c < grid; ++c)
-        heap.push({0.0, c});
-    std::vector<std::vector<int32_t>> tc_of(grid), sm_of(grid);
+    std::vector<double> load(grid, 0.0);
+    std::vector<int64_t> used(grid, (int64_t)sizeof(RecHead));
+    P.cta_tc.assign(grid, {});
+    P.cta_small.assign(grid, {});
     for (const Job &j : jobs) {
-        Slot sl = heap.top();
-        heap.pop();
-        (j.tc ? tc_of : sm_of)[sl.second].push_back(j.id);
-        sl.first += j.cost;
-        heap.push(sl);
+        int best = -1;
+        for (int c = 0; c < grid; ++c)
+            if (used[c] + j.rec_bytes <= kRecMaxBytes && (best < 0 || load[c] < load[best]))
+                best = c;
+        if (best < 0)
+            return HP_ERR_UNSUPPORTED;  // the step's page lists exceed what the CTAs' records hold
+        (j.tc ? P.cta_tc : P.cta_small)[best].push_back(j.id);
+        load[best] += j.cost;
+        used[best] += j.rec_bytes;
     }
-    P.cta_ptr.assign(grid + 1, 0);
-    P.cta_ntc.assign(grid, 0);
-    P.cta_items.clear();
+    // records
+    P.records.assign(grid, {});
     for (int c = 0; c < grid; ++c) {
-        P.cta_ntc[c] = (int32_t)tc_of[c].size();
-        P.cta_items.insert(P.cta_items.end(), tc_of[c].begin(), tc_of[c].end());
-        P.cta_items.insert(P.cta_items.end(), sm_of[c].begin(), sm_of[c].end());
-        P.cta_ptr[c + 1] = (int32_t)P.cta_items.size();
+        RecHead h{};
+        h.n_tc = (int32_t)P.cta_tc[c].size();
+        h.n_small = (int32_t)P.cta_small[c].size();
+        std::vector<RecItem> items;
+        std::vector<int32_t> pages;
+        auto add = [&](const WorkItem &w) {
+            const int ps = P.level_ps[w.level];
+            const LevelDev &L = P.hdr.levels[w.level];
+            RecItem r{};
+            r.seq_begin = w.seq_begin;
+            r.n_seq = w.n_seq;
+            r.kvh = w.kvh;
+            r.k0 = w.k0;
+            r.k1 = w.k1;
+            r.part_row = w.part_row;
+            r.level = w.level;
+            r.page_off = (int32_t)pages.size();
+            r.ps = ps;
+            r.box = L.tc_box;
+            r.num_pages = L.num_pages;
+            const int64_t first = w.k0 / ps, n = item_pages(w, ps);
+            for (int64_t i = 0; i < n; ++i)
+                pages.push_back(P.page_ids[(size_t)(w.page_base + first + i)]);
+            items.push_back(r);
+        };
+        for (int32_t id : P.cta_tc[c])
+            add(P.tc[id]);
+        for (int32_t id : P.cta_small[c])
+            add(P.small[id]);
+        h.n_pages = (int32_t)pages.size();
+        std::vector<uint8_t> &rec = P.records[c];
+        rec.resize(sizeof(RecHead) + sizeof(RecItem) * items.size() + 4 * pages.size());
+        std::memcpy(rec.data(), &h, sizeof(h));
+        if (!items.empty())
+            std::memcpy(rec.data() + sizeof(RecHead), items.data(), sizeof(RecItem) * items.size());
+        if (!pages.empty())
+            std::memcpy(rec.data() + sizeof(RecHead) + sizeof(RecItem) * items.size(), pages.data(),
+                        4 * pages.size());
     }
+    return HP_OK;
 }
 
 hp_status validate_desc(const hp_tree_desc *d)
 {
     if (!d || !d->levels || d->num_levels < 1 || d->B < 1 || d->Hq < 1 || d->Hkv < 1 || d->Hq % d->Hkv)
         return HP_ERR_ARG;
-    if (d->num_levels > kMaxLevels || !supported_d(d->d) || d->Hq / d->Hkv > kTcMaxRows)
+    if (d->num_levels > kMaxLevels || !supported_d(d->d) || d->Hq / d->Hkv > kTcTile)
         return HP_ERR_UNSUPPORTED;
     for (int l = 0; l < d->num_levels; ++l) {
         const hp_tree_level &L = d->levels[l];
@@ -311,8 +358,10 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
 
     // page ids of all levels, concatenated
     std::vector<int32_t> level_page_off(d->num_levels);
+    P.level_ps.assign(d->num_levels, 0);
     for (int l = 0; l < d->num_levels; ++l) {
         const hp_tree_level &L = d->levels[l];
+        P.level_ps[l] = L.page_size;
         level_page_off[l] = (int32_t)P.page_ids.size();
         P.page_ids.insert(P.page_ids.end(), L.page_ids, L.page_ids + L.num_page_ids);
         LevelDev &LD = H.levels[l];
@@ -336,7 +385,7 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
             if (N.kv_len == 0)
                 continue;
             if (rows > kSmallRows) {
-                const int spc = std::max(1, kTcMaxRows / G);
+                const int spc = 2 * (kTcTile / G);
                 tc_tiles += ceil_div(N.seq_end - N.seq_begin, spc) * d->Hkv * ceil_div(N.kv_len, kTcTile);
             } else {
                 small_chunks += (int64_t)(d->Hkv / nh) * ceil_div(N.kv_len, kChunk);
@@ -357,7 +406,7 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
                 continue;
             const int nseq = N.seq_end - N.seq_begin;
             const bool tc = (int64_t)nseq * G > kSmallRows;
-            const int spc = tc ? std::max(1, kTcMaxRows / G) : nseq;
+            const int spc = tc ? 2 * (kTcTile / G) : nseq;
             const int64_t split = tc ? tc_split : small_split;
             // tensor-core items take one KV head; small-row items a group of
             // nh heads whose rows are laid out [head in group][sequence][g]
@@ -387,9 +436,6 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     }
     if (part > INT32_MAX)
         return HP_ERR_UNSUPPORTED;
-    // longest items first: the static round-robin over warps then balances
-    std::stable_sort(P.small.begin(), P.small.end(),
-                     [](const WorkItem &a, const WorkItem &b) { return (a.k1 - a.k0) > (b.k1 - b.k0); });
     P.merge_ptr.assign((size_t)d->B * d->Hkv + 1, 0);
     for (size_t i = 0; i < lists.size(); ++i) {
         P.merge_ptr[i + 1] = P.merge_ptr[i] + (int32_t)lists[i].size();
@@ -398,38 +444,23 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     H.n_tc = (int32_t)P.tc.size();
     H.n_small = (int32_t)P.small.size();
     H.grid = sms;
-    schedule(P, sms, d->d);
+    if ((st = schedule(P, sms, d->d)) != HP_OK)
+        return st;
     H.n_part_rows = (int32_t)part;
     H.n_merge = (int32_t)P.merge_idx.size();
 
-    // device layout
-    size_t off = round_up(sizeof(PlanHeader), 128);
-    H.off_maps = (int64_t)off;
-    off += sizeof(CUtensorMap) * kMapsPerLevel * d->num_levels;
-    off = round_up(off, 64);
-    H.off_tc = (int64_t)off;
-    off += sizeof(WorkItem) * P.tc.size();
-    off = round_up(off, 64);
-    H.off_small = (int64_t)off;
-    off += sizeof(WorkItem) * P.small.size();
-    off = round_up(off, 64);
-    H.off_page_ids = (int64_t)off;
-    off += 4 * std::max<size_t>(P.page_ids.size(), 1);
+    // device layout: header, maps and records at fixed offsets, merge lists
+    size_t rec_max = sizeof(RecHead);
+    for (const auto &r : P.records)
+        rec_max = std::max(rec_max, r.size());
+    H.rec_stride = (int32_t)round_up(rec_max, 128);
+    size_t off = kPlanRecOff + (size_t)H.rec_stride * sms;
     off = round_up(off, 64);
     H.off_merge_ptr = (int64_t)off;
     off += 4 * P.merge_ptr.size();
     off = round_up(off, 64);
     H.off_merge_idx = (int64_t)off;
     off += 4 * std::max<size_t>(P.merge_idx.size(), 1);
-    off = round_up(off, 64);
-    H.off_cta_ptr = (int64_t)off;
-    off += 4 * P.cta_ptr.size();
-    off = round_up(off, 64);
-    H.off_cta_ntc = (int64_t)off;
-    off += 4 * P.cta_ntc.size();
-    off = round_up(off, 64);
-    H.off_cta_items = (int64_t)off;
-    off += 4 * std::max<size_t>(P.cta_items.size(), 1);
     H.total_bytes = (int64_t)round_up(off, 256);
     const WsLayout ws = ws_layout(part, d->d);
     H.ws_off_lse = (int64_t)ws.off_lse;
@@ -463,7 +494,55 @@ uint64_t new_tag()
 
 uint32_t *status_ptr(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
 
+// Plans this library wrote, by device address: the persistent kernel copies
+// its schedule record from plan + kPlanRecOff + cta * rec_stride before it can
+// check the plan's tag, so a decode call is only launched when the grid and
+// record stride it was given stay inside the plan image last written there.
+struct PlanExtent {
+    uint64_t tag;
+    int64_t total_bytes;
+};
+std::mutex g_plans_mu;
+std::unordered_map<const void *, PlanExtent> g_plans;
+
+void register_plan(const void *plan_dev, uint64_t tag, int64_t total)
+{
+    std::lock_guard<std::mutex> lk(g_plans_mu);
+    g_plans[plan_dev] = PlanExtent{tag, total};
+}
+
+bool plan_extent_ok(const void *plan_dev, const hp_plan_info *info)
+{
+    std::lock_guard<std::mutex> lk(g_plans_mu);
+    auto it = g_plans.find(plan_dev);
+    if (it == g_plans.end())
+        return false;
+    const int64_t need = (int64_t)kPlanRecOff + (int64_t)info->grid * info->rec_stride;
+    return need <= it->second.total_bytes;
+}
+
 }  // namespace
+
+// Queries q[b][h][:] (bf16; strides in elements, 16-byte multiples): box
+// 64 columns x box_h heads x box_b rows, 128-byte swizzle, rows past B
+// zero-filled.
+bool hp::encode_q_map(CUtensorMap *m, const void *q, int B, int Hq, int d, int64_t q_sb, int64_t q_sh, int box_h,
+                  int box_b)
+{
+    auto fn = encode_fn();
+    if (!fn || box_h < 1 || box_h > 256 || box_b < 1 || box_b > 256)
+        return false;
+    const cuuint64_t sh = Hq > 1 ? (cuuint64_t)q_sh * 2 : (cuuint64_t)d * 2;
+    const cuuint64_t sb = B > 1 ? (cuuint64_t)q_sb * 2 : sh * (cuuint64_t)Hq;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hq, (cuuint64_t)B};
+    cuuint64_t strides[2] = {sh, sb};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_h, (cuuint32_t)box_b};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 
 // =================================================================== C ABI
 extern "C" {
@@ -524,7 +603,7 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
         return HP_ERR_ARG;
     if (!supported_d(d) || page_size < 16 || page_size > 256 || page_size % 16 || Hq / Hkv > kSmallRows)
         return HP_ERR_UNSUPPORTED;
-    if (!q_layout_ok(q, q_sb, q_sh) || !out_layout_ok(out, out_dt, o_sb, o_sh, d) || !aligned(k_pool, 16) ||
+    if (!q_layout_ok(q, q_sb, q_sh, B, Hq) || !out_layout_ok(out, out_dt, o_sb, o_sh, d) || !aligned(k_pool, 16) ||
         !aligned(v_pool, 16))
         return HP_ERR_UNSUPPORTED;
     if ((int64_t)pt_stride * page_size > INT32_MAX)
@@ -546,13 +625,15 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
     if (!encode_pool_map(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, kChunk, nh) ||
         !encode_pool_map(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, kChunk, nh))
         return HP_ERR_CUDA;
+    sp.q_slot = nh * G <= small_q_rows();
+    if (sp.q_slot && !encode_q_map(&sp.map_q, q, B, Hq, d, q_sb, q_sh, nh * G, 1))
+        return HP_ERR_CUDA;
     sp.q = static_cast<const uint16_t *>(q);
     sp.q_sb = q_sb;
     sp.q_sh = q_sh;
     sp.G = G;
     sp.Hkv = Hkv;
     sp.scale_log2 = scale * kLog2e;
-    sp.plan = nullptr;
     sp.n_items = B * (Hkv / nh) * n_split;
     sp.nh = nh;
     sp.page_table = page_table;
@@ -563,7 +644,6 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
     sp.page_size = page_size;
     sp.split_len = split;
     sp.n_split = n_split;
-    sp.seqs_per_item = 1;
     sp.part_o = reinterpret_cast<float *>(wsb + wl.off_o);
     sp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
     sp.status = status_ptr(ws);
@@ -613,9 +693,9 @@ hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_
         return HP_ERR_ARG;
     if (prefix_len > 0 && (!k || !v))
         return HP_ERR_ARG;
-    if (!supported_d(d) || Hq / Hkv > kTcMaxRows)
+    if (!supported_d(d) || Hq / Hkv > kTcTile)
         return HP_ERR_UNSUPPORTED;
-    if (!q_layout_ok(q, q_sb, q_sh) || !out_layout_ok(out, out_dt, o_sb, o_sh, d))
+    if (!q_layout_ok(q, q_sb, q_sh, row_begin + rows, Hq) || !out_layout_ok(out, out_dt, o_sb, o_sh, d))
         return HP_ERR_UNSUPPORTED;
     if (prefix_len > 0 &&
         (!aligned(k, 16) || !aligned(v, 16) || kv_st % 8 || kv_sh % 8 || kv_st <= 0 || kv_sh < 0))
@@ -633,15 +713,12 @@ hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_
     std::memset(&tp, 0, sizeof(tp));
     if (g.n_items > 0) {
         if (!encode_prefix_map(&tp.map_k, k, prefix_len, Hkv, d, kv_st, kv_sh) ||
-            !encode_prefix_map(&tp.map_v, v, prefix_len, Hkv, d, kv_st, kv_sh))
+            !encode_prefix_map(&tp.map_v, v, prefix_len, Hkv, d, kv_st, kv_sh) ||
+            !encode_q_map(&tp.map_q, q, row_begin + rows, Hq, d, q_sb, q_sh, G, kTcTile / G))
             return HP_ERR_CUDA;
-        tp.q = static_cast<const uint16_t *>(q);
-        tp.q_sb = q_sb;
-        tp.q_sh = q_sh;
         tp.G = G;
         tp.Hkv = Hkv;
         tp.scale_log2 = scale * kLog2e;
-        tp.plan = nullptr;
         tp.n_items = g.n_items;
         tp.imp_row_begin = row_begin;
         tp.imp_rows = rows;
@@ -706,24 +783,20 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
     std::vector<uint8_t> img((size_t)H.total_bytes, 0);
     std::memcpy(img.data(), &H, sizeof(H));
     if (!P.maps.empty())
-        std::memcpy(img.data() + H.off_maps, P.maps.data(), sizeof(CUtensorMap) * P.maps.size());
-    if (!P.tc.empty())
-        std::memcpy(img.data() + H.off_tc, P.tc.data(), sizeof(WorkItem) * P.tc.size());
-    if (!P.small.empty())
-        std::memcpy(img.data() + H.off_small, P.small.data(), sizeof(WorkItem) * P.small.size());
-    if (!P.page_ids.empty())
-        std::memcpy(img.data() + H.off_page_ids, P.page_ids.data(), 4 * P.page_ids.size());
+        std::memcpy(img.data() + kPlanMapsOff, P.maps.data(), sizeof(CUtensorMap) * P.maps.size());
+    for (size_t c = 0; c < P.records.size(); ++c) {
+        uint8_t *dst = img.data() + kPlanRecOff + c * (size_t)H.rec_stride;
+        std::memcpy(dst, P.records[c].data(), P.records[c].size());
+        std::memcpy(dst, &H.tag, sizeof(H.tag));  // RecHead::tag
+    }
     std::memcpy(img.data() + H.off_merge_ptr, P.merge_ptr.data(), 4 * P.merge_ptr.size());
     if (!P.merge_idx.empty())
         std::memcpy(img.data() + H.off_merge_idx, P.merge_idx.data(), 4 * P.merge_idx.size());
-    std::memcpy(img.data() + H.off_cta_ptr, P.cta_ptr.data(), 4 * P.cta_ptr.size());
-    std::memcpy(img.data() + H.off_cta_ntc, P.cta_ntc.data(), 4 * P.cta_ntc.size());
-    if (!P.cta_items.empty())
-        std::memcpy(img.data() + H.off_cta_items, P.cta_items.data(), 4 * P.cta_items.size());
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(plan_dev, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return HP_ERR_CUDA;
+    register_plan(plan_dev, H.tag, H.total_bytes);
     std::memset(info, 0, sizeof(*info));
     info->B = H.B;
     info->Hq = H.Hq;
@@ -732,6 +805,8 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
     info->n_tc_items = H.n_tc;
     info->n_small_items = H.n_small;
     info->grid = H.grid;
+    info->rec_stride = H.rec_stride;
+    info->num_levels = H.num_levels;
     info->n_part_rows = H.n_part_rows;
     info->plan_bytes = H.total_bytes;
     info->ws_bytes = H.ws_bytes;
@@ -753,8 +828,12 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         return HP_ERR_ARG;
     if (info->B < 1 || info->Hq < 1 || info->Hkv < 1 || info->Hq % info->Hkv || !supported_d(info->d))
         return HP_ERR_ARG;
-    if (!q_layout_ok(q, q_sb, q_sh) || !out_layout_ok(out, out_dt, o_sb, o_sh, info->d))
+    if (!q_layout_ok(q, q_sb, q_sh, info->B, info->Hq) || !out_layout_ok(out, out_dt, o_sb, o_sh, info->d))
         return HP_ERR_UNSUPPORTED;
+    if (info->Hq / info->Hkv > kTcTile || info->grid < 1 || info->num_levels < 1 ||
+        info->num_levels > kMaxLevels || info->rec_stride < (int32_t)sizeof(RecHead) ||
+        info->rec_stride > kRecMaxBytes || info->rec_stride % 128 || !plan_extent_ok(plan_dev, info))
+        return HP_ERR_ARG;
     if (ws_bytes < (size_t)info->ws_bytes || !aligned(ws, 256))
         return HP_ERR_WORKSPACE;
     const WsLayout wl = ws_layout(info->n_part_rows, info->d);
@@ -769,8 +848,17 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
     if (info->n_tc_items + info->n_small_items > 0) {
         CascadeParams cp;
         std::memset(&cp, 0, sizeof(cp));
-        cp.plan = plan;
+        const int nh = cascade_heads_per_item(info->Hkv);
+        cp.q_slot = nh * G <= cascade_q_rows();
+        if (!encode_q_map(&cp.q_tc, q, info->B, info->Hq, info->d, q_sb, q_sh, G, kTcTile / G) ||
+            (cp.q_slot && !encode_q_map(&cp.q_sm, q, info->B, info->Hq, info->d, q_sb, q_sh, nh * G, 1)))
+            return HP_ERR_CUDA;
+        cp.plan = static_cast<const uint8_t *>(plan_dev);
         cp.tag = info->tag;
+        cp.rec_stride = info->rec_stride;
+        cp.num_levels = info->num_levels;
+        cp.G = G;
+        cp.small_nh = nh;
         cp.q = static_cast<const uint16_t *>(q);
         cp.q_sb = q_sb;
         cp.q_sh = q_sh;

@@ -31,52 +31,60 @@ namespace {
 constexpr int kThreads = tcr::kThreads;
 constexpr int kNC = 8;  // paged-role consumer warps (warps 4..11)
 constexpr int kSmallStages = 3;
+constexpr int kQRows = 32;  // paged-role Q slot rows per stage: nh * G <= 32
 
 template <int D>
 struct FusedLayout {
     using T = tcr::Layout<D>;
-    using S = smr::Layout<D, kNC, kSmallStages>;
+    using S = smr::Layout<D, kNC, kSmallStages, kQRows>;
     static constexpr int kRing = T::kEnd > S::kEnd ? T::kEnd : S::kEnd;
     static constexpr int kTcBar = kRing;           // tcr::B_COUNT barriers, then tmem slot, abort
     static constexpr int kSmBar = kTcBar + 256;    // full[S], empty[S]
-    static constexpr int kMeta = kSmBar + 64;      // StageMeta[S], then abort
-    static constexpr int kPages = kMeta + 256;     // tcr::kMaxBoxes page ids
-    static constexpr int kBytes = kPages + 4 * tcr::kMaxBoxes;
-    static_assert(2 * kSmallStages * 8 <= 64, "small barriers");
-    static_assert(kSmallStages * (int)sizeof(smr::StageMeta) + 4 <= 256, "stage metadata");
+    static constexpr int kMeta = kSmBar + 64;      // StageMeta[S]
+    static constexpr int kZero = kMeta + 128;      // 16 zero bytes, then the paged role's abort flag
+    static constexpr int kRecBar = kZero + 32;     // the record's barrier
+    static constexpr int kRec = kRecBar + 32;      // the CTA record
+    static constexpr int kBytes = kRec + kRecMaxBytes;
+    static_assert(tcr::B_COUNT * 8 <= 128, "tensor-core barriers");
+    static_assert(2 * kSmallStages * 8 <= 64, "paged barriers");
+    static_assert(kSmallStages * (int)sizeof(smr::StageMeta) <= 128, "stage metadata");
+    static_assert(kRec % 16 == 0, "bulk copy destination");
 };
 
-__device__ __forceinline__ tcr::ItemGeo tc_geo(const PlanHeader *ph, int idx)
+__device__ __forceinline__ const CUtensorMap *level_maps(const CascadeParams &p, int level)
 {
-    const WorkItem it = plan_array<WorkItem>(ph, ph->off_tc)[idx];
-    const LevelDev &lv = ph->levels[it.level];
-    const CUtensorMap *maps = plan_array<CUtensorMap>(ph, ph->off_maps);
+    return reinterpret_cast<const CUtensorMap *>(p.plan + kPlanMapsOff) + level * kMapsPerLevel;
+}
+
+__device__ __forceinline__ tcr::ItemGeo tc_geo(const CascadeParams &p, const RecItem &it, const int32_t *pages)
+{
     tcr::ItemGeo g;
     g.seq_begin = it.seq_begin;
     g.n_seq = it.n_seq;
     g.kvh = it.kvh;
     g.k0 = it.k0;
     g.k1 = it.k1;
-    g.pages = plan_array<int32_t>(ph, ph->off_page_ids) + it.page_base;
     g.part_row = it.part_row;
+    g.spb = kTcTile / p.G;
     g.paged = 1;
-    g.ps = lv.page_size;
-    g.box = lv.tc_box;
-    g.num_pages = lv.num_pages;
-    g.map_k = maps + it.level * kMapsPerLevel + 0;
-    g.map_v = maps + it.level * kMapsPerLevel + 1;
+    g.ps = it.ps;
+    g.box = it.box;
+    g.num_pages = it.num_pages;
+    g.pages = pages + it.page_off;
+    g.map_k = level_maps(p, it.level) + 0;
+    g.map_v = level_maps(p, it.level) + 1;
+    g.map_q = &p.q_tc;
     return g;
 }
 
-// This CTA's paged items: entries of its schedule after its tensor-core items.
-struct PlanSmallItems {
-    const PlanHeader *ph;
-    const int32_t *list;  // schedule entries (small items numbered after the tensor-core ones)
+// The paged items of this CTA's record.
+struct RecordItems {
+    const CascadeParams *p;
+    const RecItem *items;  // the record's paged items
+    const int32_t *pages;  // the record's page list
     __device__ smr::Desc operator()(int k) const
     {
-        const WorkItem w = plan_array<WorkItem>(ph, ph->off_small)[list[k] - ph->n_tc];
-        const LevelDev &lv = ph->levels[w.level];
-        const CUtensorMap *maps = plan_array<CUtensorMap>(ph, ph->off_maps);
+        const RecItem w = items[k];
         smr::Desc d;
         d.seq_begin = w.seq_begin;
         d.n_seq = w.n_seq;
@@ -84,11 +92,12 @@ struct PlanSmallItems {
         d.k0 = w.k0;
         d.k1 = w.k1;
         d.part_row = w.part_row;
-        d.pages = plan_array<int32_t>(ph, ph->off_page_ids) + w.page_base;
-        d.ps = lv.page_size;
-        d.num_pages = lv.num_pages;
-        d.map_k = maps + w.level * kMapsPerLevel + 2;
-        d.map_v = maps + w.level * kMapsPerLevel + 3;
+        d.pages = pages + w.page_off;
+        d.pbase = w.k0 / w.ps;
+        d.ps = w.ps;
+        d.num_pages = w.num_pages;
+        d.map_k = level_maps(*p, w.level) + 2;
+        d.map_v = level_maps(*p, w.level) + 3;
         d.valid = d.k0 < d.k1;
         return d;
     }
@@ -102,23 +111,9 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const PlanHeader *ph = p.plan;
-    if (ph->magic != kPlanMagic || ph->tag != p.tag || (int)gridDim.x != ph->grid) {
-        if (tid == 0)
-            atomicOr(p.status, kStPlan);
-        return;  // uniform across the CTA
-    }
     // let the merge kernel launch as soon as every CTA has started; it waits
     // for this grid to finish before reading the partial states
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-    const int32_t *cta_ptr = plan_array<int32_t>(ph, ph->off_cta_ptr);
-    const int32_t *cta_ntc = plan_array<int32_t>(ph, ph->off_cta_ntc);
-    const int32_t *cta_items = plan_array<int32_t>(ph, ph->off_cta_items);
-    const int beg = __ldg(cta_ptr + blockIdx.x);
-    const int end = __ldg(cta_ptr + blockIdx.x + 1);
-    const int n_tc = __ldg(cta_ntc + blockIdx.x);
-    const int n_small = end - beg - n_tc;
 
     tcr::Ctx tc;
     tc.smem = smem;
@@ -126,9 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
     tc.bar0 = tc.sbase + FL::kTcBar;
     tc.tmem_slot = reinterpret_cast<uint32_t *>(smem + FL::kTcBar + 128);
     tc.abort = reinterpret_cast<volatile int *>(smem + FL::kTcBar + 132);
-    tc.s_pages = reinterpret_cast<int32_t *>(smem + FL::kPages);
     tc.status = p.status;
-    const tcr::Args ta{p.q, p.q_sb, p.q_sh, ph->G, p.scale_log2, p.part_o, p.part_lse};
+    const tcr::Args ta{p.G, p.scale_log2, p.part_o, p.part_lse};
 
     smr::Ctx sc;
     sc.smem = smem;
@@ -136,72 +130,114 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
     sc.full0 = tc.sbase + FL::kSmBar;
     sc.empty0 = sc.full0 + kSmallStages * 8;
     sc.meta = reinterpret_cast<smr::StageMeta *>(smem + FL::kMeta);
-    sc.abort = reinterpret_cast<volatile int *>(smem + FL::kMeta + kSmallStages * sizeof(smr::StageMeta));
+    sc.zero16 = tc.sbase + FL::kZero;
+    sc.abort = reinterpret_cast<volatile int *>(smem + FL::kZero + 16);
     sc.status = p.status;
-    const smr::Args sa{p.q, p.q_sb, p.q_sh, ph->G, ph->small_nh, p.scale_log2, p.part_o, p.part_lse};
+    const smr::Args sa{p.q,  p.q_sb,          p.q_sh,   p.q_slot ? &p.q_sm : nullptr, p.G, p.small_nh,
+                       p.scale_log2, p.part_o, p.part_lse};
 
+    const uint32_t rec_bar = tc.sbase + FL::kRecBar;
+    const RecHead *rec = reinterpret_cast<const RecHead *>(smem + FL::kRec);
     if (tid == 0) {
+        // the record first: everything else of the CTA's work depends on it
+        mbar_init(rec_bar, 1);
+        tcr::init_barriers(tc, false);
         for (int s = 0; s < kSmallStages; ++s) {
             mbar_init(sc.full0 + 8 * s, 1);
-            mbar_init(sc.empty0 + 8 * s, (uint32_t)ph->small_nh);
+            mbar_init(sc.empty0 + 8 * s, (uint32_t)p.small_nh);
         }
         *sc.abort = 0;
         fence_mbar_init();
+        mbar_arrive_expect_tx(rec_bar, (uint32_t)p.rec_stride);
+        bulk_load(tc.sbase + FL::kRec, p.plan + kPlanRecOff + (size_t)blockIdx.x * p.rec_stride,
+                  (uint32_t)p.rec_stride, rec_bar);
+    } else if (tid == 32) {
+        prefetch_tensormap(&p.q_tc);
+        if (p.q_slot)
+            prefetch_tensormap(&p.q_sm);
+        for (int l = 0; l < p.num_levels; ++l)
+            for (int m = 0; m < kMapsPerLevel; ++m)
+                prefetch_tensormap(level_maps(p, l) + m);
+    } else if (tid >= 64 && tid < 68) {
+        reinterpret_cast<uint32_t *>(smem + FL::kZero)[tid - 64] = 0u;
     }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tc.tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tc.tmem_slot;
+
+    // the record: its tag must match the launch's, its contents its size
+    bool good = mbar_wait(rec_bar, 0u, p.status, tc.abort);
+    int n_tc = 0, n_small = 0;
+    if (good) {
+        n_tc = rec->n_tc;
+        n_small = rec->n_small;
+        good = rec->tag == p.tag && n_tc >= 0 && n_small >= 0 &&
+               (int64_t)sizeof(RecHead) + (int64_t)sizeof(RecItem) * (n_tc + n_small) + 4 * (int64_t)rec->n_pages <=
+                   p.rec_stride;
+        if (!good && tid == 0)
+            atomicOr(p.status, kStPlan);
+    }
+    if (!good) {
+        n_tc = 0;
+        n_small = 0;
+    }
+    const RecItem *items = reinterpret_cast<const RecItem *>(rec + 1);
+    const int32_t *pages = reinterpret_cast<const int32_t *>(items + n_tc + n_small);
 
     if (warp < 4) {
         setmaxnreg_dec<tcr::kRegsCtl>();
-        uint32_t tmem = 0;
         for (int i = 0; i < n_tc; ++i) {
-            const tcr::ItemGeo g = tc_geo(ph, __ldg(cta_items + beg + i));
-            if (warp == 0)
-                tcr::producer_prologue<D>(tc, g, i > 0, lane);
-            else {
-                if (warp == 1 && i == 0) {
-                    tmem_alloc(smem_u32(tc.tmem_slot), 512);
-                    tmem_relinquish();
-                }
-                tcr::stage_q<D, kThreads - 32>(tc, g, ta, tid - 32);
+            const tcr::ItemGeo g = tc_geo(p, items[i], pages);
+            if (i > 0) {
+                // barriers of the previous item: re-initialise before any wait
+                if (tid == 0)
+                    tcr::init_barriers(tc, true);
+                __syncwarp();
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            tcr::named_sync(0, kThreads);
-            tc_fence_after();
-            tmem = *tc.tmem_slot;
-            if (warp == 0)
-                tcr::producer_loop<D>(tc, g, lane);
-            else if (warp == 1 && lane == 0)
-                tcr::mma_loop<D>(tc, g, ph->G, tmem);
+            if (warp == 0 && tcr::item_ok(g))
+                tcr::producer_prologue<D>(tc, g, ta, lane);
+            if (i > 0) {
+                fence_proxy_async_smem();
+                tcr::named_sync(0, kThreads);
+            }
+            if (tcr::item_ok(g)) {
+                if (warp == 0)
+                    tcr::producer_loop<D>(tc, g, lane);
+                else if (warp == 1 && lane == 0)
+                    tcr::mma_loop<D>(tc, g, tmem);
+            } else if (tid == 0) {
+                atomicOr(p.status, kStPlan);
+            }
             __syncwarp();
             tc_fence_before();
             tcr::named_sync(0, kThreads);
         }
-        if (n_tc > 0 && warp == 1) {
+        if (warp == 0)
+            smr::producer<D, kNC, kSmallStages, kQRows>(sc, sa, RecordItems{&p, items + n_tc, pages}, n_small, lane);
+        if (warp == 1) {
             tc_fence_after();
             tmem_dealloc(tmem, 512);
         }
-        if (warp == 0)
-            smr::producer<D, kNC, kSmallStages>(sc, sa, PlanSmallItems{ph, cta_items + beg + n_tc}, n_small, lane);
     } else {
         setmaxnreg_inc<tcr::kRegsSoftmax>();
         for (int i = 0; i < n_tc; ++i) {
-            const tcr::ItemGeo g = tc_geo(ph, __ldg(cta_items + beg + i));
-            tcr::stage_q<D, kThreads - 32>(tc, g, ta, tid - 32);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            tcr::named_sync(0, kThreads);
-            tc_fence_after();
-            const uint32_t tmem = *tc.tmem_slot;
-            tcr::softmax_loop<D>(tc, g, ta, tmem, warp, lane, tid);
+            const tcr::ItemGeo g = tc_geo(p, items[i], pages);
+            if (i > 0)
+                tcr::named_sync(0, kThreads);
+            if (tcr::item_ok(g))
+                tcr::softmax_loop<D>(tc, g, ta, tmem, warp, lane, tid);
             // the epilogue wrote shared memory that TMA refills next
             fence_proxy_async_smem();
             tc_fence_before();
             tcr::named_sync(0, kThreads);
         }
-        if (warp - 4 < ph->small_nh)
-            smr::consumer<D, kNC, kSmallStages>(sc, sa, warp - 4, lane);
+        if (warp - 4 < p.small_nh)
+            smr::consumer<D, kNC, kSmallStages, kQRows>(sc, sa, warp - 4, lane);
     }
     __syncwarp();
 }
@@ -211,6 +247,7 @@ cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
 {
     static bool configured = false;
     const int bytes = FusedLayout<D>::kBytes + 1024;
+    static_assert(FusedLayout<D>::kBytes + 1024 <= 227 * 1024, "shared memory per CTA");
     if (!configured) {
         cudaError_t e =
             cudaFuncSetAttribute(hp_cascade_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -228,6 +265,8 @@ cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
 }
 
 }  // namespace
+
+int cascade_q_rows() { return kQRows; }
 
 int cascade_heads_per_item(int Hkv)
 {

@@ -25,14 +25,14 @@ enum : uint32_t { kStBounds = 1u, kStTimeout = 2u, kStPlan = 4u };
 
 // One unit of work: query rows (sequences [seq_begin, seq_begin+n_seq) x the
 // G heads of KV head kvh) against keys [k0, k1) of one tree node.  Its rows
-// land in partial rows part_row + s*G + g.
+// land in partial rows part_row + s*G + g.  (Host-side planning form.)
 struct WorkItem {
     int32_t level;
     int32_t seq_begin;
     int32_t n_seq;
     int32_t kvh;
     int32_t k0, k1;
-    int32_t page_base;  // index in the plan's page-id array of the node's first page
+    int32_t page_base;  // index in the level's page-id list of the node's first page
     int32_t part_row;
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
@@ -46,8 +46,8 @@ struct LevelDev {
     int32_t pad;
 };
 
-// Tensor maps per level: [0] K for the tensor-core kernel, [1] V likewise,
-// [2] K for the small kernel (16-token boxes), [3] V likewise.
+// Tensor maps per level: [0] K for the tensor-core role, [1] V likewise,
+// [2] K for the paged role (16-token boxes of a head group), [3] V likewise.
 constexpr int kMapsPerLevel = 4;
 
 struct alignas(64) PlanHeader {
@@ -56,17 +56,12 @@ struct alignas(64) PlanHeader {
     uint64_t tag;
     int32_t B, Hq, Hkv, d, G, num_levels;
     int32_t n_tc, n_small, n_part_rows, n_merge;
-    int32_t small_nh;       // KV heads per small-row item
-    int32_t grid;           // CTAs of the fused kernel (one schedule per CTA)
-    int64_t off_maps;       // byte offsets from the plan base
-    int64_t off_tc;
-    int64_t off_small;
-    int64_t off_page_ids;
+    int32_t small_nh;       // KV heads per paged item
+    int32_t grid;           // CTAs of the fused kernel (one record per CTA)
+    int32_t rec_stride;     // bytes per CTA record (multiple of 128)
+    int32_t pad0;
     int64_t off_merge_ptr;  // [B*Hkv + 1] int32
     int64_t off_merge_idx;  // [n_merge] int32: partial row of (b, g = 0)
-    int64_t off_cta_ptr;    // [grid + 1] int32: each CTA's schedule in cta_items
-    int64_t off_cta_ntc;    // [grid] int32: how many of them are tensor-core items
-    int64_t off_cta_items;  // int32: tensor-core item i as i, small item j as n_tc + j
     int64_t total_bytes;
     int64_t ws_bytes;
     int64_t ws_off_lse;     // byte offsets into the workspace
@@ -74,45 +69,63 @@ struct alignas(64) PlanHeader {
     LevelDev levels[kMaxLevels];
 };
 
+// Fixed places in the plan image: the tensor maps (kMapsPerLevel per level,
+// kMaxLevels slots), then one record per CTA of the fused kernel.
+constexpr size_t kPlanMapsOff = (sizeof(PlanHeader) + 127) / 128 * 128;
+constexpr size_t kPlanRecOff = kPlanMapsOff + (size_t)kMaxLevels * kMapsPerLevel * sizeof(CUtensorMap);
+
+// ------------------------------------------------------------ CTA records
+// Everything one CTA of the fused kernel needs to start its work, fetched
+// with a single bulk copy: its items (tensor-core items first) and the page
+// ids of their key ranges.  The page of key t of an item is
+// pages[page_off + t / ps - k0 / ps].
+struct RecHead {
+    uint64_t tag;
+    int32_t n_tc, n_small;
+    int32_t n_pages;
+    int32_t pad[3];
+};
+struct RecItem {
+    int32_t seq_begin, n_seq, kvh, k0, k1, part_row;
+    int32_t level, page_off;
+    int32_t ps, box, num_pages;
+    int32_t pad;
+};
+static_assert(sizeof(RecHead) == 32 && sizeof(RecItem) == 48, "record layout");
+constexpr int kRecMaxBytes = 8192;
+
 // ----------------------------------------------------------- kernel params
-// Tensor-core (prefix / shared-node) kernel.
+// Standalone tensor-core kernel over a contiguous prefix (hp_prefix_attn).
 struct TcParams {
-    CUtensorMap map_k;  // used when maps == nullptr (contiguous prefix)
+    CUtensorMap map_k;  // [len][Hkv][d]: box 64 columns x 1 head x 128 tokens
     CUtensorMap map_v;
-    const uint16_t *q;
-    int64_t q_sb, q_sh;
+    CUtensorMap map_q;  // [B][Hq][d]: box 64 columns x G heads x (128 / G) rows
     int32_t G, Hkv;
     float scale_log2;   // softmax scale * log2(e)
-    // item source: the device plan (items, maps, page ids are found through
-    // its header), or implicit items over a contiguous prefix (plan == nullptr)
-    const PlanHeader *plan;
-    uint64_t tag;             // expected plan tag (plan mode)
     int32_t n_items;
-    // implicit mode
     int32_t imp_row_begin, imp_rows, imp_seqs_per_item, imp_split_len, imp_n_split, imp_len;
     float *part_o;
     float *part_lse;
     uint32_t *status;
 };
 
-// Small-row (paged decode) kernel.
+// Standalone paged decode kernel (hp_suffix_decode_paged and its
+// allocation-free variant): items (b, kvh group, split) from a page table.
 struct SmallParams {
-    CUtensorMap map_k;  // used when maps == nullptr (standalone paged decode)
+    CUtensorMap map_k;  // head-group boxes: 64 columns x 16 tokens x nh heads
     CUtensorMap map_v;
-    const uint16_t *q;
-    int64_t q_sb, q_sh;
+    CUtensorMap map_q;  // [B][Hq][d]: box 64 columns x (nh * G) heads x 1 row
     int32_t G, Hkv;
     float scale_log2;
-    // plan mode (plan != nullptr): items, maps and page ids via the header
-    const PlanHeader *plan;
-    uint64_t tag;
     int32_t n_items;
-    // standalone mode: items (b, kvh, split) from the page table
     const int32_t *page_table;
     int32_t pt_stride;
     const int32_t *seq_lens;
-    int32_t B, num_pages, page_size, split_len, n_split, seqs_per_item;
+    int32_t B, num_pages, page_size, split_len, n_split;
     int32_t nh;  // KV heads per item (a group of consecutive heads; 1, 2 or 4)
+    int32_t q_slot;  // map_q is valid (nh * G <= small_q_rows()): Q rows arrive with each item's first chunk
+    const uint16_t *q;  // otherwise the consumers read q[b][h][:] themselves
+    int64_t q_sb, q_sh;
     float *part_o;
     float *part_lse;
     uint32_t *status;
@@ -120,9 +133,15 @@ struct SmallParams {
 
 // Fused cascade kernel (tensor-core and paged roles, one persistent launch).
 struct CascadeParams {
-    const PlanHeader *plan;
+    CUtensorMap q_tc;      // box 64 columns x G heads x (128 / G) rows
+    CUtensorMap q_sm;      // box 64 columns x (nh * G) heads x 1 row
+    const uint8_t *plan;   // plan image (maps at kPlanMapsOff, records at kPlanRecOff)
     uint64_t tag;
-    const uint16_t *q;
+    int32_t rec_stride;
+    int32_t num_levels;
+    int32_t G, small_nh;
+    int32_t q_slot;        // q_sm is valid (small_nh * G <= cascade_q_rows())
+    const uint16_t *q;     // otherwise the paged role reads q[b][h][:] itself
     int64_t q_sb, q_sh;
     float scale_log2;
     float *part_o;
@@ -166,9 +185,15 @@ cudaError_t launch_merge(const MergeParams &p, int64_t out_rows, cudaStream_t s)
 cudaError_t launch_merge_dependent(const MergeParams &p, int64_t out_rows, cudaStream_t s);
 cudaError_t launch_cascade(const CascadeParams &p, int grid, int d, cudaStream_t s);
 int cascade_heads_per_item(int Hkv);
+int cascade_q_rows();  // paged-role Q slot rows of the fused kernel
+int small_q_rows();    // Q slot rows of the standalone paged kernel
 cudaError_t launch_merge2(const float *oa, const float *la, const float *ob, const float *lb,
                           void *o, int out_f32, float *lse, int64_t rows, int d, cudaStream_t s);
 size_t tc_smem_bytes(int d);
+// TMA map of the queries q[b][h][:] (bf16, strides in elements): box 64
+// columns x box_h heads x box_b rows, 128-byte swizzle.
+bool encode_q_map(CUtensorMap *m, const void *q, int B, int Hq, int d, int64_t q_sb, int64_t q_sh, int box_h,
+                  int box_b);
 size_t small_smem_bytes(int d);
 int small_heads_per_item(int Hkv);
 

@@ -155,13 +155,16 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
         !encode_pool(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, nh))
         return HP_ERR_CUDA;
     const int G = Hq / Hkv;
+    // Q rows by TMA with each item's first chunk when the strides allow a
+    // tensor map; the consumers read them themselves otherwise
+    sp.q_slot = nh * G <= small_q_rows() && (B == 1 || q_sb > 0) && (Hq == 1 || q_sh > 0) &&
+                encode_q_map(&sp.map_q, q, B, Hq, d, q_sb, q_sh, nh * G, 1);
     sp.q = static_cast<const uint16_t *>(q);
     sp.q_sb = q_sb;
     sp.q_sh = q_sh;
     sp.G = G;
     sp.Hkv = Hkv;
     sp.scale_log2 = scale * 1.4426950408889634f;
-    sp.plan = nullptr;
     sp.n_items = B * (Hkv / nh) * n_split;
     sp.nh = nh;
     sp.page_table = page_table;
@@ -172,7 +175,6 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
     sp.page_size = page_size;
     sp.split_len = (int)split;
     sp.n_split = n_split;
-    sp.seqs_per_item = 1;
     sp.part_o = reinterpret_cast<float *>(base + off_o);
     sp.part_lse = reinterpret_cast<float *>(base + off_lse);
     sp.status = reinterpret_cast<uint32_t *>(base);

@@ -126,6 +126,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *map, uint3
                  : "memory");
 }
 
+// Plain bulk copy global -> shared (both addresses 16-byte aligned, size a
+// multiple of 16), completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {

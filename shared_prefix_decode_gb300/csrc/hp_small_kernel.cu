@@ -15,13 +15,16 @@ namespace {
 constexpr int kConsumers = 4;
 constexpr int kStages = 3;
 constexpr int kThreadsSmall = (kConsumers + 1) * 32;
+constexpr int kQRows = 16;  // Q slot rows per stage: nh * G <= 16
 
 template <int D>
 struct SmallKernelLayout {
-    using R = smr::Layout<D, kConsumers, kStages>;
+    using R = smr::Layout<D, kConsumers, kStages, kQRows>;
     static constexpr int kBar = R::kEnd;
     static constexpr int kMeta = kBar + 2 * kStages * 8;
-    static constexpr int kBytes = kMeta + kStages * (int)sizeof(smr::StageMeta) + 64;
+    static constexpr int kZero = kMeta + 128;  // 16 zero bytes, then the abort flag
+    static constexpr int kBytes = kZero + 32;
+    static_assert(kStages * (int)sizeof(smr::StageMeta) <= 128, "stage metadata");
 };
 
 // Items of the page-table form: idx -> (sequence, head group, split).
@@ -50,6 +53,7 @@ struct TableItems {
         d.k1 = min(d.k0 + p->split_len, len);
         d.part_row = idx * p->nh * p->G;
         d.pages = p->page_table + (int64_t)b * p->pt_stride;
+        d.pbase = 0;
         d.ps = p->page_size;
         d.num_pages = p->num_pages;
         d.map_k = &p->map_k;
@@ -73,9 +77,12 @@ __global__ void __launch_bounds__(kThreadsSmall) hp_small_kernel(const __grid_co
     c.full0 = c.sbase + KL::kBar;
     c.empty0 = c.full0 + kStages * 8;
     c.meta = reinterpret_cast<smr::StageMeta *>(smem + KL::kMeta);
-    c.abort = reinterpret_cast<volatile int *>(smem + KL::kMeta + kStages * sizeof(smr::StageMeta));
+    c.zero16 = c.sbase + KL::kZero;
+    c.abort = reinterpret_cast<volatile int *>(smem + KL::kZero + 16);
     c.status = p.status;
-    smr::Args a{p.q, p.q_sb, p.q_sh, p.G, p.nh, p.scale_log2, p.part_o, p.part_lse};
+    smr::Args a{p.q, p.q_sb, p.q_sh, p.q_slot ? &p.map_q : nullptr, p.G, p.nh, p.scale_log2, p.part_o, p.part_lse};
+    if (threadIdx.x < 4)
+        reinterpret_cast<uint32_t *>(smem + KL::kZero)[threadIdx.x] = 0u;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(c.full0 + 8 * s, 1);
@@ -87,9 +94,9 @@ __global__ void __launch_bounds__(kThreadsSmall) hp_small_kernel(const __grid_co
     __syncthreads();
     const int n_items = p.n_items > (int)blockIdx.x ? (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     if (warp == kConsumers)
-        smr::producer<D, kConsumers, kStages>(c, a, TableItems{&p, (int)blockIdx.x, (int)gridDim.x}, n_items, lane);
+        smr::producer<D, kConsumers, kStages, kQRows>(c, a, TableItems{&p, (int)blockIdx.x, (int)gridDim.x}, n_items, lane);
     else if (warp < p.nh)
-        smr::consumer<D, kConsumers, kStages>(c, a, warp, lane);
+        smr::consumer<D, kConsumers, kStages, kQRows>(c, a, warp, lane);
     __syncwarp();
 }
 
@@ -114,6 +121,8 @@ size_t small_smem_bytes(int d)
 {
     return d == 64 ? SmallKernelLayout<64>::kBytes + 1024 : SmallKernelLayout<128>::kBytes + 1024;
 }
+
+int small_q_rows() { return kQRows; }
 
 int small_heads_per_item(int Hkv)
 {

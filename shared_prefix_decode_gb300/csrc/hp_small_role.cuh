@@ -18,7 +18,9 @@
 // producer warp fills a ring of K and V chunks (128-byte swizzled, so the
 // ldmatrix reads are conflict free) and writes, per stage, the item fields
 // the consumers need; the consumers release a stage by arriving on its
-// "empty" barrier.  Scores and P V use the m16n8k16 bf16 MMA with f32
+// "empty" barrier.  With an item's first chunk the producer also loads the
+// item's query rows (one sequence: G rows per head of the group) into the
+// stage's Q slot, so a new item costs the consumers no dependent global load.  Scores and P V use the m16n8k16 bf16 MMA with f32
 // accumulation: rows are the (up to 16) query rows of a head, S = Q K^T for
 // 16 keys is two n8 tiles, and O = P V reuses the S accumulator layout as the
 // A operand.  The producer runs ahead across item boundaries.
@@ -34,14 +36,18 @@ namespace smr {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// Shared memory of the role for NC consumer warps and S stages.
-template <int D, int NC, int S>
+// Shared memory of the role for NC consumer warps, S stages and a Q slot of
+// QR rows per stage.
+template <int D, int NC, int S, int QR>
 struct Layout {
     static constexpr int kHalves = D / 64;
     static constexpr int kHeadBox = 16 * 128;     // one head: [16 tokens][64 bf16], swizzled
     static constexpr int kHalf = NC * kHeadBox;   // one column half of the head group
     static constexpr int kChunk = kHalves * kHalf;  // K (or V) of one 16-token chunk
-    static constexpr int kStage = 2 * kChunk;       // K then V
+    static constexpr int kQRows = QR;                // Q slot: nh * G <= QR rows of one sequence
+    static constexpr int kQHalf = kQRows * 128;
+    static constexpr int kQSlot = kHalves * kQHalf;
+    static constexpr int kStage = 2 * kChunk + kQSlot;  // K, V, Q slot
     static constexpr int kEnd = S * kStage;
 };
 
@@ -50,14 +56,15 @@ struct StageMeta {
     int seq_begin, n_seq, kvh0, part_row;
     int nvalid;  // valid keys of the chunk (0 when its page id was out of range)
     int first, last;
-    int pad;
+    int qslot;   // first chunk only: the item's Q rows are in this stage's Q slot
 };
 
 // The geometry of one item.
 struct Desc {
     int valid;
     int seq_begin, n_seq, kvh0, k0, k1, part_row;
-    const int32_t *pages;
+    const int32_t *pages;  // page of key t: pages[t / ps - pbase] (generic address)
+    int pbase;
     int ps, num_pages;
     const void *map_k;
     const void *map_v;
@@ -69,13 +76,15 @@ struct Ctx {
     uint32_t full0;  // S "full" barriers (count 1 + transaction bytes)
     uint32_t empty0; // S "empty" barriers (count nh)
     StageMeta *meta; // S entries
+    uint32_t zero16; // 16 zero bytes (shared address): ldmatrix rows past the item
     volatile int *abort;
     uint32_t *status;
 };
 
 struct Args {
-    const uint16_t *q;
+    const uint16_t *q;      // rows read by the consumers when Q is not in the slot
     int64_t q_sb, q_sh;
+    const void *map_q;      // box 64 columns x (nh * G) heads x 1 row (nh * G <= QR); null: no Q slot
     int G, nh;
     float scale_log2;
     float *part_o;
@@ -86,10 +95,10 @@ struct Args {
 // n_items entries), then closes the ring with a sentinel stage (n_seq = -1,
 // completed by a plain arrival) that tells the consumers to stop.  All 32
 // lanes call it.
-template <int D, int NC, int S, class Src>
+template <int D, int NC, int S, int QR, class Src>
 __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src &src, int n_items, int lane)
 {
-    using L = Layout<D, NC, S>;
+    using L = Layout<D, NC, S, QR>;
     constexpr int kHalves = D / 64;
     auto wait_warp = [&](uint32_t b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
@@ -107,11 +116,12 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
             prefetched = true;
         }
         const int nchunks = (d.k1 - d.k0 + kChunk - 1) / kChunk;
+        const bool qslot = a.map_q != nullptr && d.n_seq == 1;
         int pg = 0;
         for (int ch = 0; ch < nchunks; ++ch, ++k) {
             if ((ch & 31) == 0) {  // page ids of the next 32 chunks, one per lane
                 const int cc = ch + lane;
-                pg = cc < nchunks ? __ldg(d.pages + (d.k0 + cc * kChunk) / d.ps) : 0;
+                pg = cc < nchunks ? d.pages[(d.k0 + cc * kChunk) / d.ps - d.pbase] : 0;
             }
             const uint32_t st = k % S;
             if (k >= (uint32_t)S && !(ok = wait_warp(c.empty0 + 8 * st, ((k / S) - 1) & 1u)))
@@ -133,9 +143,10 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 m.nvalid = oob ? 0 : min(kChunk, d.k1 - t);
                 m.first = ch == 0;
                 m.last = ch + 1 == nchunks;
-                m.pad = 0;
+                m.qslot = ch == 0 && qslot;
                 c.meta[st] = m;
-                mbar_arrive_expect_tx(bar, 2 * kHalves * a.nh * L::kHeadBox);
+                mbar_arrive_expect_tx(bar, 2 * kHalves * a.nh * L::kHeadBox +
+                                               (m.qslot ? kHalves * a.nh * a.G * 128 : 0));
             }
             __syncwarp();
             if (lane < 2 * kHalves) {
@@ -143,6 +154,10 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 const bool is_v = lane >= kHalves;
                 tma_load_4d(c.sbase + st * L::kStage + (is_v ? L::kChunk : 0) + h * L::kHalf,
                             is_v ? d.map_v : d.map_k, bar, h * 64, t % d.ps, d.kvh0, page);
+            } else if (ch == 0 && qslot && lane < 3 * kHalves) {
+                const int h = lane - 2 * kHalves;
+                tma_load_3d(c.sbase + st * L::kStage + 2 * L::kChunk + h * L::kQHalf, a.map_q, bar, h * 64,
+                            d.kvh0 * a.G, d.seq_begin);
             }
         }
     }
@@ -168,10 +183,10 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
 
 // Consumer warp w (0 <= w < nh): processes the chunks in ring order until
 // the producer's sentinel stage.
-template <int D, int NC, int S>
+template <int D, int NC, int S, int QR>
 __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int lane)
 {
-    using L = Layout<D, NC, S>;
+    using L = Layout<D, NC, S, QR>;
     constexpr int kHalves = D / 64;
     constexpr int kKs = D / 16;  // k-steps of the S MMA
     constexpr int kNt = D / 8;   // n8 tiles of O
@@ -193,7 +208,26 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
             break;  // sentinel: the producer's walk is over
         const int rows = m.n_seq * a.G;
         const int kvh = m.kvh0 + w;
-        if (m.first) {
+        if (m.first && m.qslot) {
+            // new item, Q rows in the stage: head w's rows are slot rows
+            // w*G .. w*G+G-1; rows past G read a zero chunk
+            const int mi = lane >> 3, ri = (lane & 7) + ((mi & 1) << 3);
+            const uint32_t qs = c.sbase + st * L::kStage + 2 * L::kChunk;
+            const int srow = w * a.G + ri;
+#pragma unroll
+            for (int ks = 0; ks < kKs; ++ks) {
+                const int dch = 2 * ks + (mi >> 1);
+                const uint32_t addr = ri < rows ? qs + (dch >> 3) * L::kQHalf + srow * 128 +
+                                                      (((dch & 7) ^ (srow & 7)) << 4)
+                                                : c.zero16;
+                ldmatrix_x4(addr, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+            }
+#pragma unroll
+            for (int n = 0; n < kNt; ++n)
+                o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+        } else if (m.first) {
             // new item: query fragments (A operand, rows r0 / r1) and state
             const uint16_t *q0 = nullptr, *q1 = nullptr;
             if (r0 < rows)

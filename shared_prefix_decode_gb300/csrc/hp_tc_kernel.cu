@@ -15,8 +15,7 @@ template <int D>
 struct TcKernelLayout {
     using R = tcr::Layout<D>;
     static constexpr int kBar = R::kEnd;
-    static constexpr int kPages = kBar + 256;
-    static constexpr int kBytes = kPages + 4 * tcr::kMaxBoxes;
+    static constexpr int kBytes = kBar + 256;
 };
 
 // Item idx of a contiguous prefix: (row chunk, KV head, key split).
@@ -32,14 +31,16 @@ __device__ __forceinline__ tcr::ItemGeo contiguous_item(const TcParams &p, int i
     g.kvh = kvh;
     g.k0 = split * p.imp_split_len;
     g.k1 = min(g.k0 + p.imp_split_len, p.imp_len);
-    g.pages = nullptr;
     g.part_row = idx * p.imp_seqs_per_item * p.G;
+    g.spb = kTcTile / p.G;
     g.paged = 0;
     g.ps = 0;
     g.box = kTcTile;
     g.num_pages = 0;
+    g.pages = nullptr;
     g.map_k = &p.map_k;
     g.map_v = &p.map_v;
+    g.map_q = &p.map_q;
     return g;
 }
 
@@ -57,37 +58,37 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
     c.bar0 = c.sbase + KL::kBar;
     c.tmem_slot = reinterpret_cast<uint32_t *>(smem + KL::kBar + 128);
     c.abort = reinterpret_cast<volatile int *>(smem + KL::kBar + 132);
-    c.s_pages = reinterpret_cast<int32_t *>(smem + KL::kPages);
     c.status = p.status;
-    tcr::Args a{p.q, p.q_sb, p.q_sh, p.G, p.scale_log2, p.part_o, p.part_lse};
+    const tcr::Args a{p.G, p.scale_log2, p.part_o, p.part_lse};
 
     const tcr::ItemGeo g = contiguous_item(p, blockIdx.x);
-    if (!tcr::item_ok(g, p.G)) {
+    if (!tcr::item_ok(g)) {
         if (tid == 0)
             atomicOr(p.status, kStPlan);
         return;  // uniform across the CTA: nothing allocated yet
     }
+    if (tid == 0) {
+        tcr::init_barriers(c, false);
+        prefetch_tensormap(g.map_q);
+        prefetch_tensormap(g.map_k);
+        prefetch_tensormap(g.map_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(c.tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *c.tmem_slot;
     if (warp < 4) {
         setmaxnreg_dec<tcr::kRegsCtl>();
-        if (warp == 0)
-            tcr::producer_prologue<D>(c, g, false, lane);
-        else {
-            if (warp == 1) {
-                tmem_alloc(smem_u32(c.tmem_slot), 512);
-                tmem_relinquish();
-            }
-            tcr::stage_q<D, tcr::kThreads - 32>(c, g, a, tid - 32);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        tcr::named_sync(0, tcr::kThreads);
-        tc_fence_after();
-        const uint32_t tmem = *c.tmem_slot;
-        if (warp == 0)
+        if (warp == 0) {
+            tcr::producer_prologue<D>(c, g, a, lane);
             tcr::producer_loop<D>(c, g, lane);
-        else if (warp == 1 && lane == 0)
-            tcr::mma_loop<D>(c, g, p.G, tmem);
+        } else if (warp == 1 && lane == 0) {
+            tcr::mma_loop<D>(c, g, tmem);
+        }
         __syncwarp();
         tc_fence_before();
         tcr::named_sync(0, tcr::kThreads);
@@ -97,12 +98,6 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
         }
     } else {
         setmaxnreg_inc<tcr::kRegsSoftmax>();
-        tcr::stage_q<D, tcr::kThreads - 32>(c, g, a, tid - 32);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        tcr::named_sync(0, tcr::kThreads);
-        tc_fence_after();
-        const uint32_t tmem = *c.tmem_slot;
         tcr::softmax_loop<D>(c, g, a, tmem, warp, lane, tid);
         tc_fence_before();
         tcr::named_sync(0, tcr::kThreads);

@@ -13,31 +13,34 @@
 // ChunkAttention Eq. 1-2) and writes a partial (O, LSE) per row, merged later
 // by log-sum-exp.
 //
-// One item: up to 256 query rows (two M=128 blocks) x one key range.  Roles:
-//   warp 0      TMA producer: K and V tiles (128 keys x d, 128-byte swizzle)
-//               through a 2-stage ring, all boxes of a tile issued by several
-//               lanes in one instruction (a TMA box costs about the same
+// One item: up to two blocks of 128 query rows x one key range.  A block
+// holds 128 / G sequences x G heads (rows s*G + g), loaded by one TMA box per
+// 64 columns straight from q[b][h][:], so the rows of a block need no
+// staging by threads.  Roles:
+//   warp 0      TMA producer: Q, then K and V tiles (128 keys x d, 128-byte
+//               swizzle) through a 2-stage ring, all boxes of a tile issued
+//               by several lanes at once (a TMA box costs about the same
 //               whatever its size; one thread issuing boxes one by one caps
-//               an SM far below HBM bandwidth).  The first two tiles are
-//               issued before Q is staged.
+//               an SM far below HBM bandwidth).
 //   warp 1      TMEM owner and MMA issuer (one thread):
 //               S_mb = Q_mb K^T (A, B from shared memory) into TMEM,
 //               O_mb += P_mb V   (A = P from TMEM, B = V from shared memory).
-//   warps 1-11  stage Q (warp 0 stages page ids meanwhile).
-//   warps 4-7   softmax for rows 0-127, warps 8-11 for rows 128-255: read a
-//               128-column score row from TMEM, max / exp2 / row sum, write P
-//               (bf16) over the S columns, rescale O in TMEM when the max
-//               grows by more than 2^8 (the reference max is kept otherwise;
-//               exact, since the final O / l uses the same reference), and at
-//               the end stage O through shared memory so the partial rows are
-//               written as whole 512-byte rows.
+//   warps 4-7   softmax for block 0, warps 8-11 for block 1: read a 128-column
+//               score row from TMEM, max / exp2 / row sum, write P (bf16)
+//               over the S columns, rescale O in TMEM when the max grows by
+//               more than 2^8 (the reference max is kept otherwise; exact,
+//               since the final O / l uses the same reference), and at the end
+//               stage O through shared memory so the partial rows are written
+//               as whole rows.  The loops walk the row in 32-column chunks
+//               (short code: a cold instruction cache costs microseconds
+//               when HBM is saturated).
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
 // The two row blocks ping-pong: S of block 1 is computed while block 0 runs
 // its softmax, and S of tile j+1 is issued right after P V of tile j.
 //
-// Register split: warpgroup 0 (producer, MMA, two helpers) lowers its count,
-// the softmax warpgroups raise theirs; the caller issues setmaxnreg at the
-// top of each branch so the compiler budgets each role's code accordingly.
+// Register split: warpgroup 0 (producer, MMA, two idle warps) lowers its
+// count, the softmax warpgroups raise theirs; the caller issues setmaxnreg at
+// the top of each branch.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -48,7 +51,6 @@
 namespace hp {
 namespace tcr {
 
-constexpr int kMaxBoxes = 1024;  // page-id slots staged per item
 constexpr int kThreads = 384;
 constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 136, kRegsSoftmax = 184;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax == kThreads * kRegsLaunch, "register split");
@@ -69,14 +71,16 @@ struct Layout {
 
 // barrier slots (8 bytes each) at the caller's barrier area
 enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_S = 8, B_P = 10, B_O = 12, B_DRAIN = 14,
-       B_COUNT = 15 };
+       B_Q = 15, B_COUNT = 16 };
 
 struct ItemGeo {
     int seq_begin, n_seq, kvh, k0, k1, part_row;
-    const int32_t *pages;  // the node's page list (paged mode)
+    int spb;               // sequences per 128-row block: 128 / G
     int paged, ps, box, num_pages;
+    const int32_t *pages;  // paged: page of key t is pages[t / ps - k0 / ps] (generic address)
     const void *map_k;
     const void *map_v;
+    const void *map_q;
 };
 
 // Per-CTA resources of the role.
@@ -84,15 +88,12 @@ struct Ctx {
     uint8_t *smem;        // 1024-aligned base of the role's layout
     uint32_t sbase;       // its shared-window address
     uint32_t bar0;        // B_COUNT barriers
-    int32_t *s_pages;     // kMaxBoxes page-id slots
     uint32_t *tmem_slot;  // TMEM base address written by tcgen05.alloc
     volatile int *abort;
     uint32_t *status;
 };
 
 struct Args {
-    const uint16_t *q;
-    int64_t q_sb, q_sh;
     int G;
     float scale_log2;  // > 0
     float *part_o;
@@ -111,20 +112,35 @@ __device__ __forceinline__ void mbar_inval(uint32_t bar)
     asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ bool item_ok(const ItemGeo &g, int G)
+__device__ __forceinline__ int n_tiles_of(const ItemGeo &g) { return (g.k1 - g.k0 + kTcTile - 1) / kTcTile; }
+__device__ __forceinline__ int n_blocks_of(const ItemGeo &g) { return (g.n_seq + g.spb - 1) / g.spb; }
+
+__device__ __forceinline__ bool item_ok(const ItemGeo &g)
 {
-    const int nmb = (g.n_seq * G + 127) >> 7;
-    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
-    const int n_boxes = g.paged ? n_tiles * (kTcTile / g.box) : 0;
-    return nmb >= 1 && nmb <= 2 && n_tiles > 0 && n_boxes <= kMaxBoxes;
+    const int nmb = n_blocks_of(g);
+    return g.spb >= 1 && nmb >= 1 && nmb <= 2 && g.k1 > g.k0 &&
+           (!g.paged || (g.box >= 1 && kTcTile % g.box == 0 && g.ps % g.box == 0));
+}
+
+// One thread: (re)initialise the role's barriers.  `reinit` when an earlier
+// item used them (the CTA has synchronised since).
+__device__ __forceinline__ void init_barriers(const Ctx &c, bool reinit)
+{
+    for (int i = 0; i < B_COUNT; ++i) {
+        if (reinit)
+            mbar_inval(bar_at(c, i));
+        mbar_init(bar_at(c, i), (i == B_P || i == B_P + 1) ? 128u : 1u);
+    }
+    *c.abort = 0;
+    fence_mbar_init();
 }
 
 // Issue the TMA copies of one 128-key tile (K or V) into `dst`, one box per
-// lane (box, column half).  Paged items take each box's page from the ids
-// staged in shared memory.
+// lane (box, column half).  Boxes past the item's keys read page num_pages,
+// which the map zero-fills.
 template <int D>
-__device__ __forceinline__ void issue_tile(const ItemGeo &g, const int32_t *s_pages, const void *map,
-                                           uint32_t dst, uint32_t bar, int tile, int lane)
+__device__ __forceinline__ void issue_tile(const Ctx &c, const ItemGeo &g, const void *map, uint32_t dst,
+                                           uint32_t bar, int tile, int lane)
 {
     constexpr int kHalves = D / 64;
     if (lane == 0)
@@ -133,98 +149,46 @@ __device__ __forceinline__ void issue_tile(const ItemGeo &g, const int32_t *s_pa
     const int kt0 = g.k0 + tile * kTcTile;
     if (g.paged) {
         const int nbox = kTcTile / g.box;
+        const int pbase = g.k0 / g.ps;
         for (int l = lane; l < nbox * kHalves; l += 32) {
             const int bx = l / kHalves, h = l - bx * kHalves;
             const int t = kt0 + bx * g.box;
-            tma_load_4d(dst + h * Layout<D>::kRegion + bx * g.box * 128, map, bar, h * 64, t % g.ps, g.kvh,
-                        s_pages[tile * nbox + bx]);
+            int page = g.num_pages;
+            if (t < g.k1) {
+                page = g.pages[t / g.ps - pbase];
+                if ((unsigned)page >= (unsigned)g.num_pages) {
+                    atomicOr(c.status, kStBounds);
+                    page = g.num_pages;
+                }
+            }
+            tma_load_4d(dst + h * Layout<D>::kRegion + bx * g.box * 128, map, bar, h * 64, t % g.ps, g.kvh, page);
         }
     } else if (lane < kHalves) {
         tma_load_3d(dst + lane * Layout<D>::kRegion, map, bar, lane * 64, g.kvh, kt0);
     }
 }
 
-// Q staging share of one thread (qt in [0, nthreads)): rows r = s*G + g of
-// the item (rows past the item zero) in the 128-byte-swizzled K-major layout
-// the MMA descriptors describe.  All loads of a thread before its stores.
-template <int D, int kQThreads>
-__device__ __forceinline__ void stage_q(const Ctx &c, const ItemGeo &g, const Args &a, int qt)
-{
-    constexpr int kHalves = D / 64;
-    constexpr int kCpr = D / 8;  // 16-byte chunks per row
-    constexpr int kPer = (2 * 128 * kCpr + kQThreads - 1) / kQThreads;
-    const int rows_total = g.n_seq * a.G;
-    const int nmb = (rows_total + 127) >> 7;
-    const int total = nmb * 128 * kCpr;
-    uint4 buf[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        const int i = qt + k * kQThreads;
-        const int r = i / kCpr;
-        buf[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (i < total && r < rows_total) {
-            const int ch = i % kCpr;
-            const int s = r / a.G;
-            const int gg = r - s * a.G;
-            const uint16_t *src =
-                a.q + (int64_t)(g.seq_begin + s) * a.q_sb + (int64_t)(g.kvh * a.G + gg) * a.q_sh + ch * 8;
-            buf[k] = __ldg(reinterpret_cast<const uint4 *>(src));
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        const int i = qt + k * kQThreads;
-        if (i < total) {
-            const int r = i / kCpr, ch = i % kCpr;
-            const int mb = r >> 7, rr = r & 127, h = ch >> 3, cc = ch & 7;
-            uint8_t *dst =
-                c.smem + Layout<D>::kQ + ((mb * kHalves + h) * 128 + rr) * 128 + ((cc ^ (rr & 7)) << 4);
-            *reinterpret_cast<uint4 *>(dst) = buf[k];
-        }
-    }
-}
-
 // ---------------------------------------------------------------- phase A
-// Warp 0: (re)initialise the barriers, stage the page ids, issue the first
-// tiles.  Call with all 32 lanes; `reinit` when the barriers were used by an
-// earlier item (the CTA has synchronised since).
+// Warp 0: the item's Q blocks and its first two tiles.
 template <int D>
-__device__ __forceinline__ void producer_prologue(const Ctx &c, const ItemGeo &g, bool reinit, int lane)
+__device__ __forceinline__ void producer_prologue(const Ctx &c, const ItemGeo &g, const Args &a, int lane)
 {
     using L = Layout<D>;
-    if (lane == 0) {
-        for (int i = 0; i < B_COUNT; ++i) {
-            if (reinit)
-                mbar_inval(bar_at(c, i));
-            mbar_init(bar_at(c, i), (i == B_P || i == B_P + 1) ? 128u : 1u);
-        }
-        *c.abort = 0;
-        fence_mbar_init();
-        prefetch_tensormap(g.map_k);
-        prefetch_tensormap(g.map_v);
-    }
-    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
-    if (g.paged) {
-        const int nbox = kTcTile / g.box;
-        const int n_boxes = n_tiles * nbox;
-        for (int i = lane; i < n_boxes; i += 32) {
-            const int t = g.k0 + (i / nbox) * kTcTile + (i % nbox) * g.box;
-            int page = g.num_pages;  // out of range: the box is zero-filled
-            if (t < g.k1) {
-                page = __ldg(g.pages + t / g.ps);
-                if ((unsigned)page >= (unsigned)g.num_pages) {
-                    atomicOr(c.status, kStBounds);
-                    page = g.num_pages;
-                }
-            }
-            c.s_pages[i] = page;
-        }
-    }
+    constexpr int kHalves = D / 64;
+    const int nmb = n_blocks_of(g);
+    if (lane == 0)
+        mbar_arrive_expect_tx(bar_at(c, B_Q), (uint32_t)(nmb * kHalves * g.spb * a.G * 128));
     __syncwarp();
+    if (lane < nmb * kHalves) {
+        const int mb = lane / kHalves, h = lane % kHalves;
+        tma_load_3d(c.sbase + L::kQ + (mb * kHalves + h) * L::kRegion, g.map_q, bar_at(c, B_Q), h * 64,
+                    g.kvh * a.G, g.seq_begin + mb * g.spb);
+    }
+    const int n_tiles = n_tiles_of(g);
     const int pre = n_tiles < 2 ? n_tiles : 2;
     for (int j = 0; j < pre; ++j) {
-        issue_tile<D>(g, c.s_pages, g.map_k, c.sbase + L::kK + j * L::kTile, bar_at(c, B_KFULL + j), j, lane);
-        issue_tile<D>(g, c.s_pages, g.map_v, c.sbase + L::kV + j * L::kTile, bar_at(c, B_VFULL + j), j, lane);
+        issue_tile<D>(c, g, g.map_k, c.sbase + L::kK + j * L::kTile, bar_at(c, B_KFULL + j), j, lane);
+        issue_tile<D>(c, g, g.map_v, c.sbase + L::kV + j * L::kTile, bar_at(c, B_VFULL + j), j, lane);
     }
 }
 
@@ -233,7 +197,7 @@ template <int D>
 __device__ __forceinline__ void producer_loop(const Ctx &c, const ItemGeo &g, int lane)
 {
     using L = Layout<D>;
-    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
+    const int n_tiles = n_tiles_of(g);
     const int pre = n_tiles < 2 ? n_tiles : 2;
     auto wait_warp = [&](int b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar_at(c, b), parity, c.status, c.abort)) != 0;
@@ -244,17 +208,18 @@ __device__ __forceinline__ void producer_loop(const Ctx &c, const ItemGeo &g, in
         const uint32_t ph = (uint32_t)(j >> 1) & 1u;
         if (!wait_warp(B_KEMPTY + st, ph ^ 1u))
             break;
-        issue_tile<D>(g, c.s_pages, g.map_k, c.sbase + L::kK + st * L::kTile, bar_at(c, B_KFULL + st), j, lane);
+        issue_tile<D>(c, g, g.map_k, c.sbase + L::kK + st * L::kTile, bar_at(c, B_KFULL + st), j, lane);
         if (!wait_warp(B_VEMPTY + st, ph ^ 1u)) {
             if (lane == 0)
                 mbar_wait_drain(bar_at(c, B_KFULL + st), ph);  // K of tile j is in flight
             break;
         }
-        issue_tile<D>(g, c.s_pages, g.map_v, c.sbase + L::kV + st * L::kTile, bar_at(c, B_VFULL + st), j, lane);
+        issue_tile<D>(c, g, g.map_v, c.sbase + L::kV + st * L::kTile, bar_at(c, B_VFULL + st), j, lane);
         issued = j + 1;
     }
     // every load issued has landed before the item ends
     if (lane == 0) {
+        mbar_wait_drain(bar_at(c, B_Q), 0u);
         for (int j = max(0, issued - 2); j < issued; ++j) {
             const uint32_t ph = (uint32_t)(j >> 1) & 1u;
             mbar_wait_drain(bar_at(c, B_KFULL + (j & 1)), ph);
@@ -265,14 +230,14 @@ __device__ __forceinline__ void producer_loop(const Ctx &c, const ItemGeo &g, in
 
 // One thread (warp 1, lane 0).
 template <int D>
-__device__ __forceinline__ void mma_loop(const Ctx &c, const ItemGeo &g, int G, uint32_t tmem)
+__device__ __forceinline__ void mma_loop(const Ctx &c, const ItemGeo &g, uint32_t tmem)
 {
     using L = Layout<D>;
     constexpr int kHalves = D / 64;
     constexpr uint32_t kIdescQK = umma_idesc_bf16(128, 128, false);
     constexpr uint32_t kIdescPV = umma_idesc_bf16(128, D, true);
-    const int nmb = (g.n_seq * G + 127) >> 7;
-    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
+    const int nmb = n_blocks_of(g);
+    const int n_tiles = n_tiles_of(g);
     const uint32_t qa = c.sbase + L::kQ;
     auto issue_s = [&](int mb, int st) {
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -291,7 +256,8 @@ __device__ __forceinline__ void mma_loop(const Ctx &c, const ItemGeo &g, int G, 
         }
         tc_commit(bar_at(c, B_O + mb));
     };
-    bool ok = mbar_wait(bar_at(c, B_KFULL + 0), 0u, c.status, c.abort);
+    bool ok = mbar_wait(bar_at(c, B_Q), 0u, c.status, c.abort) &&
+              mbar_wait(bar_at(c, B_KFULL + 0), 0u, c.status, c.abort);
     if (ok) {
         tc_fence_after();
         for (int mb = 0; mb < nmb; ++mb)
@@ -339,11 +305,12 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
     using L = Layout<D>;
     constexpr int kHalves = D / 64;
     const int rows_total = g.n_seq * a.G;
-    const int nmb = (rows_total + 127) >> 7;
-    const int n_tiles = (g.k1 - g.k0 + kTcTile - 1) / kTcTile;
+    const int rpb = g.spb * a.G;  // rows per block
+    const int nmb = n_blocks_of(g);
+    const int n_tiles = n_tiles_of(g);
     const int mb = (warp - 4) >> 2;
     const int rr = tid - 128 * (1 + mb);  // row within the block == TMEM lane
-    const int row = mb * 128 + rr;
+    const int rows_here = min(rpb, rows_total - mb * rpb);
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = tl + mb * 128;
     const uint32_t o_col = tl + 256 + mb * 128;
@@ -354,29 +321,23 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
     float m_run = -INFINITY;  // reference max, log2 units
     float l_run = 0.f;
     bool ok = mb < nmb;
-    uint32_t sv[128];
     uint32_t r[32];
     for (int j = 0; ok && j < n_tiles; ++j) {
         if (!(ok = wait_warp(B_S + mb, (uint32_t)j & 1u)))
             break;
         tc_fence_after();
         const int nvalid = min(kTcTile, g.k1 - (g.k0 + j * kTcTile));
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-            tmem_ld32(s_col + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[cc * 32]));
-        tmem_ld_wait();
-        // the scale is positive: the largest scaled score is the largest raw
-        // score times the scale
+        // largest valid score (the scale is positive: the largest scaled
+        // score is the largest raw score times the scale)
         float mx = -INFINITY;
-        if (nvalid >= kTcTile) {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+            tmem_ld32(s_col + cc * 32, r);
+            tmem_ld_wait();
+            const int lim = nvalid - cc * 32;
 #pragma unroll
-            for (int i = 0; i < 128; ++i)
-                mx = fmaxf(mx, __uint_as_float(sv[i]));
-        } else {
-#pragma unroll
-            for (int i = 0; i < 128; ++i)
-                if (i < nvalid)
-                    mx = fmaxf(mx, __uint_as_float(sv[i]));
+            for (int i = 0; i < 32; ++i)
+                mx = fmaxf(mx, i < lim ? __uint_as_float(r[i]) : -INFINITY);
         }
         const float tmax = mx * cs;
         const bool need = tmax > m_run + kTau;
@@ -385,21 +346,22 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
             l_run *= alpha;
             m_run = tmax;
         }
-        // P = exp2(s * c - m) as bf16 pairs over the S columns
+        // P = exp2(s * c - m) as bf16 pairs over the S columns (chunk cc's P
+        // lands in columns already read); invalid keys get P = 0
         const float nm = -m_run;
         float lsum = 0.f;
-#pragma unroll
+#pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
+            tmem_ld32(s_col + cc * 32, r);
+            tmem_ld_wait();
+            const int lim = nvalid - cc * 32;
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const int c0 = cc * 32 + 2 * i;
-                float p0 = fast_exp2(fmaf(__uint_as_float(sv[c0]), cs, nm));
-                float p1 = fast_exp2(fmaf(__uint_as_float(sv[c0 + 1]), cs, nm));
-                if (nvalid < kTcTile) {
-                    p0 = c0 < nvalid ? p0 : 0.f;
-                    p1 = c0 + 1 < nvalid ? p1 : 0.f;
-                }
+                float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), cs, nm));
+                float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), cs, nm));
+                p0 = 2 * i < lim ? p0 : 0.f;
+                p1 = 2 * i + 1 < lim ? p1 : 0.f;
                 lsum += p0 + p1;
                 pk[i] = pack_bf16x2(p0, p1);
             }
@@ -412,7 +374,7 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
             if (!(ok = wait_warp(B_O + mb, (uint32_t)(j - 1) & 1u)))
                 break;
             tc_fence_after();
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 tmem_ld32(o_col + cc * 32, r);
                 tmem_ld_wait();
@@ -451,31 +413,30 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
         tc_fence_after();
         const float inv = 1.f / l_run;
         uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
-#pragma unroll
+#pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
             tmem_ld32(o_col + cc * 32, r);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int ch = cc * 8 + i;                       // logical 16-byte chunk
-                const int pc = (ch & ~7) | ((ch ^ rr) & 7);      // physical chunk
+                const int ch = cc * 8 + i;                   // logical 16-byte chunk
+                const int pc = (ch & ~7) | ((ch ^ rr) & 7);  // physical chunk
                 *reinterpret_cast<float4 *>(stg + rr * (D * 4) + pc * 16) =
                     make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
                                 __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
             }
         }
-        if (row < rows_total)
-            a.part_lse[g.part_row + row] = (m_run + fast_log2(l_run)) * kLn2;
+        if (rr < rows_here)
+            a.part_lse[g.part_row + mb * rpb + rr] = (m_run + fast_log2(l_run)) * kLn2;
     }
     tc_fence_before();
     named_sync(1 + mb, 128);
     if (have) {
         const uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
         const int wq = warp & 3;
-        const int rows_here = min(128, rows_total - mb * 128);
         constexpr int kChunksRow = D / 4;  // 16-byte chunks per f32 row
         for (int rw = wq; rw < rows_here; rw += 4) {
-            float *dst = a.part_o + (size_t)(g.part_row + mb * 128 + rw) * D;
+            float *dst = a.part_o + (size_t)(g.part_row + mb * rpb + rw) * D;
             for (int ch = lane; ch < kChunksRow; ch += 32) {
                 const int pc = (ch & ~7) | ((ch ^ rw) & 7);
                 *reinterpret_cast<float4 *>(dst + ch * 4) =

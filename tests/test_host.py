@@ -30,7 +30,7 @@ def test_library_loads_and_exports_every_declared_symbol():
         assert hasattr(lib, name), f"{name} declared in hp.h but not exported"
     assert set(declared) == set(hb.exported_symbols())
     assert lib.hp_build_arch() == 103
-    assert lib.hp_abi_version() == 1
+    assert lib.hp_abi_version() == 2
 
 
 def test_status_strings():
