@@ -22,10 +22,7 @@ using namespace hp;
 namespace {
 
 constexpr int32_t kAbiVersion = 2;
-// A tensor-core item processes at least this many 128-key tiles (its fixed
-// set-up -- TMEM allocation, Q staging, pipeline fill -- is amortised over
-// them) and at most kMaxTcTiles (its page ids must fit the staging area).
-constexpr int64_t kMinTcTiles = 2;
+// A tensor-core item processes at most kMaxTcTiles 128-key tiles.
 constexpr int64_t kMaxTcTiles = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -100,6 +97,22 @@ bool encode_prefix_map(CUtensorMap *m, const void *base, int len, int Hkv, int d
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Partial O rows [rows][d] f32 for the tensor-core role's stores: box 32
+// columns x 128 rows, 128-byte swizzle.
+bool encode_o_map(CUtensorMap *m, float *part_o, int64_t rows, int d)
+{
+    auto fn = encode_fn();
+    if (!fn || rows < 1)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)kTcTile};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_o, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool supported_d(int d) { return d == 64 || d == 128; }
 
 // q rows are read by TMA (16-byte aligned base and strides, positive
@@ -166,11 +179,11 @@ PrefixGeo prefix_geo(int rows, int G, int Hkv, int len, int sms)
     g.spi = std::min(g.spi, std::max(rows, 1));
     g.n_rc = (int)ceil_div(rows, g.spi);
     const int64_t tiles = ceil_div(std::max(len, 1), kTcTile);
-    const int64_t per = std::max<int64_t>(kMinTcTiles, ceil_div((int64_t)g.n_rc * Hkv * tiles, sms));
+    const int64_t per = std::max<int64_t>(2, ceil_div((int64_t)g.n_rc * Hkv * tiles, sms));
     g.split_len = (int)(per * kTcTile);
     g.n_split = len > 0 ? (int)ceil_div(len, g.split_len) : 0;
     g.n_items = g.n_rc * Hkv * g.n_split;
-    g.part_rows = (int64_t)g.n_items * g.spi * G;
+    g.part_rows = (int64_t)g.n_items * 2 * kTcTile;  // two 128-row blocks per item
     return g;
 }
 
@@ -190,51 +203,92 @@ struct HostPlan {
 // Page ids an item's record entry holds: the pages of keys [k0, k1).
 int64_t item_pages(const WorkItem &w, int ps) { return (int64_t)(w.k1 - 1) / ps - w.k0 / ps + 1; }
 
-// Longest-first greedy schedule of the fused kernel's items over `grid` CTAs,
-// each CTA's record kept within kRecMaxBytes.  Cost of an item: a fixed
-// set-up plus its KV bytes at one SM's share of HBM bandwidth (~44 GB/s when
-// every SM streams); a tensor-core item's set-up (Q, TMEM, two row blocks of
-// epilogue) is larger.  Each CTA runs its tensor-core items first.
-hp_status schedule(HostPlan &P, int grid, int d)
+// Time model of the fused kernel (ns), from timelines of the step on GB300:
+// every CTA waits for its record; a tensor-core item pays for its Q, the
+// latency of its first tiles and its epilogue, then per 128-key tile (TMA
+// and exp2 bound, proportional to d); a CTA with paged items waits for its
+// first chunks, then each item streams its KV.
+struct CostModel {
+    double cta = 1500, tc_item = 6000, tc_tile = 2200, sm_start = 1000, sm_item = 200, sm_bytes_per_ns = 60;
+    double tc(const WorkItem &w, int d) const
+    {
+        return tc_item + tc_tile * (double)ceil_div(w.k1 - w.k0, kTcTile) * d / 128.0;
+    }
+    double small(const WorkItem &w, int d, int nh) const
+    {
+        return sm_item + (double)(w.k1 - w.k0) * nh * w.n_seq * d * 4 / sm_bytes_per_ns;
+    }
+};
+
+struct Job {
+    double cost;
+    int32_t id;
+    bool tc;
+    int64_t rec_bytes;
+};
+
+// Longest-first greedy assignment of `jobs` to CTAs [c0, c1), each CTA's
+// record kept within kRecMaxBytes; false when a job fits no record.
+bool lpt(std::vector<Job> jobs, int c0, int c1, std::vector<double> &load, std::vector<int64_t> &used,
+         std::vector<std::vector<int32_t>> &tc_of, std::vector<std::vector<int32_t>> &sm_of, double start_cost)
 {
-    const double kBytesPerNs = 44.0;
-    struct Job {
-        double cost;
-        int32_t id;
-        bool tc;
-        int64_t rec_bytes;
-    };
-    std::vector<Job> jobs;
+    std::stable_sort(jobs.begin(), jobs.end(), [](const Job &a, const Job &b) { return a.cost > b.cost; });
+    for (const Job &j : jobs) {
+        int best = -1;
+        for (int c = c0; c < c1; ++c)
+            if (used[c] + j.rec_bytes <= kRecMaxBytes && (best < 0 || load[c] < load[best]))
+                best = c;
+        if (best < 0)
+            return false;
+        if (!j.tc && sm_of[best].empty())
+            load[best] += start_cost;
+        (j.tc ? tc_of : sm_of)[best].push_back(j.id);
+        load[best] += j.cost;
+        used[best] += j.rec_bytes;
+    }
+    return true;
+}
+
+// Schedule of the fused kernel's items over `grid` CTAs: CTAs [0, n_tc_ctas)
+// take the tensor-core items, the others the paged items (n_tc_ctas = grid:
+// every CTA may take both, tensor-core items first).  Returns the modelled
+// makespan, or a negative value when the records cannot hold the items.
+double schedule(HostPlan &P, int grid, int n_tc_ctas, int d, const CostModel &cm)
+{
+    std::vector<Job> tcj, smj;
     for (size_t i = 0; i < P.tc.size(); ++i) {
         const WorkItem &w = P.tc[i];
-        const double bytes = (double)(w.k1 - w.k0) * d * 4;
-        jobs.push_back({4000.0 + bytes / kBytesPerNs, (int32_t)i, true,
-                        (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
+        tcj.push_back({cm.tc(w, d), (int32_t)i, true,
+                       (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
     }
     const int nh = P.hdr.small_nh;
     for (size_t j = 0; j < P.small.size(); ++j) {
         const WorkItem &w = P.small[j];
-        const double bytes = (double)(w.k1 - w.k0) * nh * w.n_seq * d * 4;
-        jobs.push_back({800.0 + bytes / kBytesPerNs, (int32_t)j, false,
-                        (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
+        smj.push_back({cm.small(w, d, nh), (int32_t)j, false,
+                       (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
     }
-    std::stable_sort(jobs.begin(), jobs.end(), [](const Job &a, const Job &b) { return a.cost > b.cost; });
-    std::vector<double> load(grid, 0.0);
+    std::vector<double> load(grid, cm.cta);
     std::vector<int64_t> used(grid, (int64_t)sizeof(RecHead));
     P.cta_tc.assign(grid, {});
     P.cta_small.assign(grid, {});
-    for (const Job &j : jobs) {
-        int best = -1;
-        for (int c = 0; c < grid; ++c)
-            if (used[c] + j.rec_bytes <= kRecMaxBytes && (best < 0 || load[c] < load[best]))
-                best = c;
-        if (best < 0)
-            return HP_ERR_UNSUPPORTED;  // the step's page lists exceed what the CTAs' records hold
-        (j.tc ? P.cta_tc : P.cta_small)[best].push_back(j.id);
-        load[best] += j.cost;
-        used[best] += j.rec_bytes;
+    bool ok;
+    if (n_tc_ctas >= grid) {
+        std::vector<Job> all = tcj;
+        all.insert(all.end(), smj.begin(), smj.end());
+        ok = lpt(all, 0, grid, load, used, P.cta_tc, P.cta_small, cm.sm_start);
+    } else {
+        ok = lpt(tcj, 0, n_tc_ctas, load, used, P.cta_tc, P.cta_small, cm.sm_start) &&
+             lpt(smj, n_tc_ctas, grid, load, used, P.cta_tc, P.cta_small, cm.sm_start);
     }
-    // records
+    if (!ok)
+        return -1.0;
+    return *std::max_element(load.begin(), load.end());
+}
+
+// The records of the schedule in P (one per CTA, tag left zero).
+void build_records(HostPlan &P)
+{
+    const int grid = (int)P.cta_tc.size();
     P.records.assign(grid, {});
     for (int c = 0; c < grid; ++c) {
         RecHead h{};
@@ -276,7 +330,67 @@ hp_status schedule(HostPlan &P, int grid, int d)
             std::memcpy(rec.data() + sizeof(RecHead) + sizeof(RecItem) * items.size(), pages.data(),
                         4 * pages.size());
     }
-    return HP_OK;
+}
+
+// Work items of the tree for the given key splits (tensor-core items: one KV
+// head, up to two blocks of 128 / G sequences; paged items: a group of nh KV
+// heads of a node's sequences), with their partial rows and, when `lists`
+// is given, the merge list of every (b, kvh).  Returns the partial row count.
+int64_t make_items(const hp_tree_desc *d, int G, int nh, int64_t tc_split, int64_t small_split,
+                   const std::vector<int32_t> &level_page_off, HostPlan &P,
+                   std::vector<std::vector<int32_t>> *lists)
+{
+    P.tc.clear();
+    P.small.clear();
+    int64_t part = 0;
+    for (int l = 0; l < d->num_levels; ++l) {
+        const hp_tree_level &L = d->levels[l];
+        for (int n = 0; n < L.num_nodes; ++n) {
+            const hp_tree_node &N = L.nodes[n];
+            if (N.kv_len == 0)
+                continue;
+            const int nseq = N.seq_end - N.seq_begin;
+            const bool tc = (int64_t)nseq * G > kSmallRows;
+            const int spc = tc ? 2 * (kTcTile / G) : nseq;
+            const int64_t split = tc ? tc_split : small_split;
+            // tensor-core items take one KV head; small-row items a group of
+            // nh heads whose rows are laid out [head in group][sequence][g]
+            const int hstep = tc ? 1 : nh;
+            for (int s0 = N.seq_begin; s0 < N.seq_end; s0 += spc) {
+                const int ns = std::min(spc, N.seq_end - s0);
+                for (int kvh = 0; kvh < d->Hkv; kvh += hstep)
+                    for (int64_t k0 = 0; k0 < N.kv_len; k0 += split) {
+                        WorkItem w;
+                        w.level = l;
+                        w.seq_begin = s0;
+                        w.n_seq = ns;
+                        w.kvh = kvh;
+                        w.k0 = (int32_t)k0;
+                        w.k1 = (int32_t)std::min<int64_t>(k0 + split, N.kv_len);
+                        w.page_base = level_page_off[l] + N.page_off;
+                        w.part_row = (int32_t)std::min<int64_t>(part, INT32_MAX);
+                        if (tc) {
+                            // 128 rows per block of 128 / G sequences (the
+                            // block is stored whole by a TMA tensor store)
+                            if (lists)
+                                for (int b = s0; b < s0 + ns; ++b)
+                                    (*lists)[(size_t)b * d->Hkv + kvh].push_back(
+                                        (int32_t)std::min<int64_t>(tc_part_row(part, b - s0, 0, G), INT32_MAX));
+                            part += ceil_div(ns, kTcTile / G) * kTcTile;
+                        } else {
+                            if (lists)
+                                for (int hw = 0; hw < hstep; ++hw)
+                                    for (int b = s0; b < s0 + ns; ++b)
+                                        (*lists)[(size_t)b * d->Hkv + kvh + hw].push_back(
+                                            (int32_t)(part + ((int64_t)hw * ns + (b - s0)) * G));
+                            part += (int64_t)ns * G * hstep;
+                        }
+                        (tc ? P.tc : P.small).push_back(w);
+                    }
+            }
+        }
+    }
+    return part;
 }
 
 hp_status validate_desc(const hp_tree_desc *d)
@@ -372,9 +486,8 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
         LD.tc_box = std::gcd(L.page_size, kTcTile);
     }
 
-    // Split sizes.  Shared (tensor-core) work: total 128-key tiles spread over
-    // one wave of CTAs (one per SM).  Small-row work: 16-key chunks spread
-    // over ~8 warps per SM.
+    // Work sizes: 128-key tiles of the shared (tensor-core) nodes, 16-key
+    // chunks of the paged ones.
     const int nh = cascade_heads_per_item(d->Hkv);
     H.small_nh = nh;
     int64_t tc_tiles = 0, small_chunks = 0;
@@ -391,49 +504,39 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
                 small_chunks += (int64_t)(d->Hkv / nh) * ceil_div(N.kv_len, kChunk);
             }
         }
-    const int64_t tc_split =
-        kTcTile * std::min(kMaxTcTiles, std::max<int64_t>(kMinTcTiles, ceil_div(tc_tiles, sms)));
-    const int64_t small_split = kChunk * std::max<int64_t>(2, ceil_div(small_chunks, (int64_t)sms * 2));
 
-    // Items and partial rows, level by level; merge lists per (b, kvh).
-    std::vector<std::vector<int32_t>> lists((size_t)d->B * d->Hkv);
-    int64_t part = 0;
-    for (int l = 0; l < d->num_levels; ++l) {
-        const hp_tree_level &L = d->levels[l];
-        for (int n = 0; n < L.num_nodes; ++n) {
-            const hp_tree_node &N = L.nodes[n];
-            if (N.kv_len == 0)
-                continue;
-            const int nseq = N.seq_end - N.seq_begin;
-            const bool tc = (int64_t)nseq * G > kSmallRows;
-            const int spc = tc ? 2 * (kTcTile / G) : nseq;
-            const int64_t split = tc ? tc_split : small_split;
-            // tensor-core items take one KV head; small-row items a group of
-            // nh heads whose rows are laid out [head in group][sequence][g]
-            const int hstep = tc ? 1 : nh;
-            for (int s0 = N.seq_begin; s0 < N.seq_end; s0 += spc) {
-                const int ns = std::min(spc, N.seq_end - s0);
-                for (int kvh = 0; kvh < d->Hkv; kvh += hstep)
-                    for (int64_t k0 = 0; k0 < N.kv_len; k0 += split) {
-                        WorkItem w;
-                        w.level = l;
-                        w.seq_begin = s0;
-                        w.n_seq = ns;
-                        w.kvh = kvh;
-                        w.k0 = (int32_t)k0;
-                        w.k1 = (int32_t)std::min<int64_t>(k0 + split, N.kv_len);
-                        w.page_base = level_page_off[l] + N.page_off;
-                        w.part_row = (int32_t)part;
-                        for (int hw = 0; hw < hstep; ++hw)
-                            for (int b = s0; b < s0 + ns; ++b)
-                                lists[(size_t)b * d->Hkv + kvh + hw].push_back(
-                                    (int32_t)(part + ((int64_t)hw * ns + (b - s0)) * G));
-                        part += (int64_t)ns * G * hstep;
-                        (tc ? P.tc : P.small).push_back(w);
-                    }
+    // Split of the CTAs between the two roles: n_tc CTAs run the tensor-core
+    // items (about one each: the key split is the shared tiles over n_tc), the
+    // others stream the paged items (about three each); the n_tc with the
+    // shortest modelled makespan wins.  Without one of the two kinds, or with
+    // a single CTA, every CTA may take both.
+    const CostModel cm;
+    auto splits_for = [&](int n_tc_ctas, int64_t &tc_split, int64_t &small_split) {
+        const int64_t per = std::max<int64_t>(1, ceil_div(tc_tiles, std::max(1, n_tc_ctas)));
+        tc_split = kTcTile * std::min(kMaxTcTiles, per);
+        const int n_sm = std::max(1, sms - (n_tc_ctas < sms ? n_tc_ctas : 0));
+        small_split = kChunk * std::max<int64_t>(2, ceil_div(small_chunks, 3 * (int64_t)n_sm));
+    };
+    int best_k = sms;
+    if (tc_tiles > 0 && small_chunks > 0 && sms > 1) {
+        double best = -1.0;
+        for (int k = 1; k < sms; ++k) {
+            int64_t ts, ss;
+            splits_for(k, ts, ss);
+            make_items(d, G, nh, ts, ss, level_page_off, P, nullptr);
+            const double t = schedule(P, sms, k, d->d, cm);
+            if (t >= 0.0 && (best < 0.0 || t < best)) {
+                best = t;
+                best_k = k;
             }
         }
     }
+    int64_t tc_split, small_split;
+    splits_for(best_k, tc_split, small_split);
+
+    // Items and partial rows, level by level; merge lists per (b, kvh).
+    std::vector<std::vector<int32_t>> lists((size_t)d->B * d->Hkv);
+    const int64_t part = make_items(d, G, nh, tc_split, small_split, level_page_off, P, &lists);
     if (part > INT32_MAX)
         return HP_ERR_UNSUPPORTED;
     P.merge_ptr.assign((size_t)d->B * d->Hkv + 1, 0);
@@ -444,8 +547,9 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     H.n_tc = (int32_t)P.tc.size();
     H.n_small = (int32_t)P.small.size();
     H.grid = sms;
-    if ((st = schedule(P, sms, d->d)) != HP_OK)
-        return st;
+    if (schedule(P, sms, best_k, d->d, cm) < 0.0)
+        return HP_ERR_UNSUPPORTED;  // the step's page lists exceed what the CTAs' records hold
+    build_records(P);
     H.n_part_rows = (int32_t)part;
     H.n_merge = (int32_t)P.merge_idx.size();
 
@@ -714,7 +818,8 @@ hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_
     if (g.n_items > 0) {
         if (!encode_prefix_map(&tp.map_k, k, prefix_len, Hkv, d, kv_st, kv_sh) ||
             !encode_prefix_map(&tp.map_v, v, prefix_len, Hkv, d, kv_st, kv_sh) ||
-            !encode_q_map(&tp.map_q, q, row_begin + rows, Hq, d, q_sb, q_sh, G, kTcTile / G))
+            !encode_q_map(&tp.map_q, q, row_begin + rows, Hq, d, q_sb, q_sh, G, kTcTile / G) ||
+            !encode_o_map(&tp.map_o, reinterpret_cast<float *>(wsb + wl.off_o), g.part_rows, d))
             return HP_ERR_CUDA;
         tp.G = G;
         tp.Hkv = Hkv;
@@ -726,7 +831,6 @@ hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_
         tp.imp_split_len = g.split_len;
         tp.imp_n_split = g.n_split;
         tp.imp_len = prefix_len;
-        tp.part_o = reinterpret_cast<float *>(wsb + wl.off_o);
         tp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
         tp.status = status_ptr(ws);
         if (launch_tc(tp, g.n_items, d, s) != cudaSuccess)
@@ -851,7 +955,8 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         const int nh = cascade_heads_per_item(info->Hkv);
         cp.q_slot = nh * G <= cascade_q_rows();
         if (!encode_q_map(&cp.q_tc, q, info->B, info->Hq, info->d, q_sb, q_sh, G, kTcTile / G) ||
-            (cp.q_slot && !encode_q_map(&cp.q_sm, q, info->B, info->Hq, info->d, q_sb, q_sh, nh * G, 1)))
+            (cp.q_slot && !encode_q_map(&cp.q_sm, q, info->B, info->Hq, info->d, q_sb, q_sh, nh * G, 1)) ||
+            !encode_o_map(&cp.o_tc, part_o, std::max<int64_t>(info->n_part_rows, 1), info->d))
             return HP_ERR_CUDA;
         cp.plan = static_cast<const uint8_t *>(plan_dev);
         cp.tag = info->tag;

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
     tc.tmem_slot = reinterpret_cast<uint32_t *>(smem + FL::kTcBar + 128);
     tc.abort = reinterpret_cast<volatile int *>(smem + FL::kTcBar + 132);
     tc.status = p.status;
-    const tcr::Args ta{p.G, p.scale_log2, p.part_o, p.part_lse};
+    const tcr::Args ta{p.G, p.scale_log2, &p.o_tc, p.part_lse};
 
     smr::Ctx sc;
     sc.smem = smem;
@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
                   (uint32_t)p.rec_stride, rec_bar);
     } else if (tid == 32) {
         prefetch_tensormap(&p.q_tc);
+        prefetch_tensormap(&p.o_tc);
         if (p.q_slot)
             prefetch_tensormap(&p.q_sm);
         for (int l = 0; l < p.num_levels; ++l)

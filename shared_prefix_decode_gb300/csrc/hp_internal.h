@@ -100,11 +100,11 @@ struct TcParams {
     CUtensorMap map_k;  // [len][Hkv][d]: box 64 columns x 1 head x 128 tokens
     CUtensorMap map_v;
     CUtensorMap map_q;  // [B][Hq][d]: box 64 columns x G heads x (128 / G) rows
+    CUtensorMap map_o;  // partial O [rows][d] f32: box 32 columns x 128 rows
     int32_t G, Hkv;
     float scale_log2;   // softmax scale * log2(e)
-    int32_t n_items;
+    int32_t n_items;    // item i owns partial rows [256 i, 256 i + 256)
     int32_t imp_row_begin, imp_rows, imp_seqs_per_item, imp_split_len, imp_n_split, imp_len;
-    float *part_o;
     float *part_lse;
     uint32_t *status;
 };
@@ -135,6 +135,7 @@ struct SmallParams {
 struct CascadeParams {
     CUtensorMap q_tc;      // box 64 columns x G heads x (128 / G) rows
     CUtensorMap q_sm;      // box 64 columns x (nh * G) heads x 1 row
+    CUtensorMap o_tc;      // partial O [rows][d] f32: box 32 columns x 128 rows (tensor-core stores)
     const uint8_t *plan;   // plan image (maps at kPlanMapsOff, records at kPlanRecOff)
     uint64_t tag;
     int32_t rec_stride;
@@ -194,6 +195,14 @@ size_t tc_smem_bytes(int d);
 // columns x box_h heads x box_b rows, 128-byte swizzle.
 bool encode_q_map(CUtensorMap *m, const void *q, int B, int Hq, int d, int64_t q_sb, int64_t q_sh, int box_h,
                   int box_b);
+// Rows of a tensor-core item: block mb of 128 / G sequences owns partial rows
+// part_row + 128 mb .. + 127; sequence s, head g of the item is row
+// part_row + 128 (s / spb) + (s % spb) G + g with spb = 128 / G.
+__host__ __device__ inline int64_t tc_part_row(int64_t part_row, int s, int g, int G)
+{
+    const int spb = kTcTile / G;
+    return part_row + (int64_t)(s / spb) * kTcTile + (int64_t)(s % spb) * G + g;
+}
 size_t small_smem_bytes(int d);
 int small_heads_per_item(int Hkv);
 

@@ -38,18 +38,17 @@ __device__ __forceinline__ int part_row(const MergeParams &p, const PartList &L,
         const int item = ((L.b * groups + L.kvh / p.nh) * p.n_split + e);
         return (item * p.nh + L.kvh % p.nh) * p.G + L.g;
     }
-    // mode 2: contiguous prefix items (rc, kvh, split), rows (s, g)
+    // mode 2: contiguous prefix items (rc, kvh, split) of two 128-row blocks
     const int rel = L.b - p.row_begin;
     const int rc = rel / p.seqs_per_item, sl = rel % p.seqs_per_item;
-    return (((rc * p.Hkv + L.kvh) * p.n_split + e) * p.seqs_per_item + sl) * p.G + L.g;
+    const int item = (rc * p.Hkv + L.kvh) * p.n_split + e;
+    return (int)tc_part_row((int64_t)item * 2 * kTcTile, sl, L.g, p.G);
 }
 
 template <int VPT>  // values per lane: d / 32
 __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeParams p)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (p.wait_prior)
-        asm volatile("griddepcontrol.wait;" ::: "memory");  // the partial states are complete
     const int64_t row = (int64_t)blockIdx.x * kMergeWarps + warp;
     const int64_t n_rows = (int64_t)p.B * p.Hq;
     if (row >= n_rows)
@@ -77,12 +76,21 @@ __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeP
         L.n = p.n_split;
         L.base = 0;
     }
+    // Everything above depends on the plan alone: when launched as a
+    // dependent of the kernel that writes the partial states, it overlaps that
+    // kernel's tail, and so does the lookup of this lane's first two parts.
+    const int pr_a = lane < L.n ? part_row(p, L, lane) : 0;
+    const int pr_b = lane + 32 < L.n ? part_row(p, L, lane + 32) : 0;
+    if (p.wait_prior)
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the partial states are complete
+    auto row_of = [&](int e) { return e == lane ? pr_a : (e == lane + 32 ? pr_b : part_row(p, L, e)); };
+
     // Lanes own parts e = lane, lane + 32, ...: gather their rows and LSEs in
     // parallel, then the weighted sum walks the parts in their fixed order
     // with the row loads of 8 parts in flight at a time.
     float M = -INFINITY;
     for (int e = lane; e < L.n; e += 32)
-        M = fmaxf(M, __ldg(p.part_lse + part_row(p, L, e)));
+        M = fmaxf(M, __ldg(p.part_lse + row_of(e)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -97,7 +105,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeP
             int pr = 0;
             float w = 0.f;
             if (e < L.n) {
-                pr = part_row(p, L, e);
+                pr = row_of(e);
                 w = fast_exp2((__ldg(p.part_lse + pr) - M) * kLog2e);
             }
             den += w;

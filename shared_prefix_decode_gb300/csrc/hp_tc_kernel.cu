@@ -31,7 +31,7 @@ __device__ __forceinline__ tcr::ItemGeo contiguous_item(const TcParams &p, int i
     g.kvh = kvh;
     g.k0 = split * p.imp_split_len;
     g.k1 = min(g.k0 + p.imp_split_len, p.imp_len);
-    g.part_row = idx * p.imp_seqs_per_item * p.G;
+    g.part_row = idx * 2 * kTcTile;
     g.spb = kTcTile / p.G;
     g.paged = 0;
     g.ps = 0;
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
     c.tmem_slot = reinterpret_cast<uint32_t *>(smem + KL::kBar + 128);
     c.abort = reinterpret_cast<volatile int *>(smem + KL::kBar + 132);
     c.status = p.status;
-    const tcr::Args a{p.G, p.scale_log2, p.part_o, p.part_lse};
+    const tcr::Args a{p.G, p.scale_log2, &p.map_o, p.part_lse};
 
     const tcr::ItemGeo g = contiguous_item(p, blockIdx.x);
     if (!tcr::item_ok(g)) {
@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
         prefetch_tensormap(g.map_q);
         prefetch_tensormap(g.map_k);
         prefetch_tensormap(g.map_v);
+        prefetch_tensormap(&p.map_o);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(c.tmem_slot), 512);

@@ -30,8 +30,10 @@
 //               over the S columns, rescale O in TMEM when the max grows by
 //               more than 2^8 (the reference max is kept otherwise; exact,
 //               since the final O / l uses the same reference), and at the end
-//               stage O through shared memory so the partial rows are written
-//               as whole rows.  The loops walk the row in 32-column chunks
+//               stage O / l in shared memory as 128-row x 32-column boxes
+//               that one thread writes out with TMA tensor stores (the
+//               partial rows of a block are 128 reserved rows of the
+//               workspace).  The loops walk the row in 32-column chunks
 //               (short code: a cold instruction cache costs microseconds
 //               when HBM is saturated).
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
@@ -66,7 +68,8 @@ struct Layout {
     static constexpr int kK = kQ + 2 * kTile;
     static constexpr int kV = kK + 2 * kTile;
     static constexpr int kEnd = kV + 2 * kTile;  // O staging reuses K (block 0) and V (block 1)
-    static_assert(2 * kTile >= 128 * D * 4, "O staging must fit one ring");
+    static constexpr int kOBox = 128 * 128;      // [128 rows][32 f32], 128-byte swizzle
+    static_assert(2 * kTile >= (D / 32) * kOBox, "O staging must fit one ring");
 };
 
 // barrier slots (8 bytes each) at the caller's barrier area
@@ -96,7 +99,7 @@ struct Ctx {
 struct Args {
     int G;
     float scale_log2;  // > 0
-    float *part_o;
+    const void *map_o;  // partial O rows [rows][D] f32: box 32 columns x 128 rows, 128-byte swizzle
     float *part_lse;
 };
 
@@ -404,45 +407,45 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
         tc_fence_before();
         mbar_arrive(bar_at(c, B_P + mb));
     }
-    // Epilogue: O / l through shared memory (block 0 over the K ring, block 1
-    // over the V ring, both idle once the last P V has completed), row-major
-    // with the 16-byte chunks of each 128-byte group permuted by the row
-    // (conflict-free writes), then each warp writes whole rows.
+    // Epilogue: O / l into shared memory (block 0 over the K ring, block 1
+    // over the V ring, both idle once the last P V has completed) as D/32
+    // boxes of [128 rows][32 f32] in the 128-byte swizzled order the tensor
+    // map expects (conflict-free: 8 consecutive rows hit 8 distinct 16-byte
+    // slots), then one thread of the block stores the boxes to partial rows
+    // part_row + mb*128 .. +127 and waits until they have been read.
     const bool have = ok && mb < nmb;
+    uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
     if (have && wait_warp(B_O + mb, (uint32_t)(n_tiles - 1) & 1u)) {
         tc_fence_after();
         const float inv = 1.f / l_run;
-        uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
+        uint32_t r2[32];
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 32; cc += 2) {
             tmem_ld32(o_col + cc * 32, r);
+            tmem_ld32(o_col + cc * 32 + 32, r2);
             tmem_ld_wait();
+            uint8_t *box = stg + cc * L::kOBox + rr * 128;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int ch = cc * 8 + i;                   // logical 16-byte chunk
-                const int pc = (ch & ~7) | ((ch ^ rr) & 7);  // physical chunk
-                *reinterpret_cast<float4 *>(stg + rr * (D * 4) + pc * 16) =
+                *reinterpret_cast<float4 *>(box + ((i ^ (rr & 7)) << 4)) =
                     make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
                                 __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                *reinterpret_cast<float4 *>(box + L::kOBox + ((i ^ (rr & 7)) << 4)) =
+                    make_float4(__uint_as_float(r2[4 * i]) * inv, __uint_as_float(r2[4 * i + 1]) * inv,
+                                __uint_as_float(r2[4 * i + 2]) * inv, __uint_as_float(r2[4 * i + 3]) * inv);
             }
         }
         if (rr < rows_here)
-            a.part_lse[g.part_row + mb * rpb + rr] = (m_run + fast_log2(l_run)) * kLn2;
+            a.part_lse[g.part_row + mb * 128 + rr] = (m_run + fast_log2(l_run)) * kLn2;
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     named_sync(1 + mb, 128);
-    if (have) {
-        const uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
-        const int wq = warp & 3;
-        constexpr int kChunksRow = D / 4;  // 16-byte chunks per f32 row
-        for (int rw = wq; rw < rows_here; rw += 4) {
-            float *dst = a.part_o + (size_t)(g.part_row + mb * rpb + rw) * D;
-            for (int ch = lane; ch < kChunksRow; ch += 32) {
-                const int pc = (ch & ~7) | ((ch ^ rw) & 7);
-                *reinterpret_cast<float4 *>(dst + ch * 4) =
-                    *reinterpret_cast<const float4 *>(stg + rw * (D * 4) + pc * 16);
-            }
-        }
+    if (have && rr == 0) {
+        for (int cc = 0; cc < D / 32; ++cc)
+            tma_store_2d(a.map_o, smem_u32(stg + cc * L::kOBox), cc * 32, g.part_row + mb * 128);
+        bulk_commit_group();
+        bulk_wait_read_all();
     }
 }
 
