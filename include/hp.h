@@ -198,7 +198,7 @@ typedef struct {
     int32_t grid;          /* CTAs of the step's persistent launch (one per SM) */
     int32_t rec_stride;    /* bytes of each CTA's schedule record in the plan */
     int32_t num_levels;
-    int32_t reserved;
+    int32_t merge_stride;  /* int32 per row of the plan's merge table */
     int64_t n_part_rows;   /* partial (O, LSE) rows in the workspace */
     int64_t plan_bytes;
     int64_t ws_bytes;      /* workspace hp_cascade_decode needs */

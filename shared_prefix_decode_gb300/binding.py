@@ -40,7 +40,7 @@ class HpTreeDesc(ctypes.Structure):
 class HpPlanInfo(ctypes.Structure):
     _fields_ = [("B", c_i32), ("Hq", c_i32), ("Hkv", c_i32), ("d", c_i32), ("n_tc_items", c_i32),
                 ("n_small_items", c_i32), ("grid", c_i32), ("rec_stride", c_i32),
-                ("num_levels", c_i32), ("reserved", c_i32),
+                ("num_levels", c_i32), ("merge_stride", c_i32),
                 ("n_part_rows", c_i64), ("plan_bytes", c_i64), ("ws_bytes", c_i64),
                 ("tag", ctypes.c_uint64)]
 

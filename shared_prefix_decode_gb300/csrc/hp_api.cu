@@ -97,18 +97,18 @@ bool encode_prefix_map(CUtensorMap *m, const void *base, int len, int Hkv, int d
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Partial O rows [rows][d] f32 for the tensor-core role's stores: box 32
+// Partial O rows [rows][d] bf16 for the tensor-core role's stores: box 64
 // columns x 128 rows, 128-byte swizzle.
-bool encode_o_map(CUtensorMap *m, float *part_o, int64_t rows, int d)
+bool encode_o_map(CUtensorMap *m, uint16_t *part_o, int64_t rows, int d)
 {
     auto fn = encode_fn();
     if (!fn || rows < 1)
         return false;
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)d * 4};
-    cuuint32_t box[2] = {32, (cuuint32_t)kTcTile};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kTcTile};
     cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_o, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, part_o, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -150,7 +150,7 @@ WsLayout ws_layout(int64_t part_rows, int d)
     WsLayout w;
     w.off_lse = kWsHeader;
     w.off_o = round_up(w.off_lse + (size_t)std::max<int64_t>(part_rows, 1) * 4, 256);
-    w.total = round_up(w.off_o + (size_t)std::max<int64_t>(part_rows, 1) * d * 4, 256);
+    w.total = round_up(w.off_o + (size_t)std::max<int64_t>(part_rows, 1) * d * 2, 256);
     return w;
 }
 
@@ -194,7 +194,7 @@ struct HostPlan {
     std::vector<WorkItem> tc, small;
     std::vector<int32_t> page_ids;     // all levels' page ids, concatenated
     std::vector<int32_t> level_ps;     // page size per level
-    std::vector<int32_t> merge_ptr, merge_idx;
+    std::vector<int32_t> merge_tab;  // [B*Hkv][merge_stride]
     std::vector<std::vector<int32_t>> cta_tc, cta_small;  // item ids per CTA of the fused kernel
     std::vector<std::vector<uint8_t>> records;           // one per CTA, without the tag
     std::vector<int32_t> contexts;  // (level, node, seq_begin, seq_end, pass) x n
@@ -539,10 +539,18 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     const int64_t part = make_items(d, G, nh, tc_split, small_split, level_page_off, P, &lists);
     if (part > INT32_MAX)
         return HP_ERR_UNSUPPORTED;
-    P.merge_ptr.assign((size_t)d->B * d->Hkv + 1, 0);
+    // merge table: one row per (b, kvh), its count then its partial rows
+    size_t max_parts = 0, n_merge = 0;
+    for (const auto &l : lists) {
+        max_parts = std::max(max_parts, l.size());
+        n_merge += l.size();
+    }
+    H.merge_stride = (int32_t)round_up(max_parts + 1, 4);
+    P.merge_tab.assign(lists.size() * (size_t)H.merge_stride, 0);
     for (size_t i = 0; i < lists.size(); ++i) {
-        P.merge_ptr[i + 1] = P.merge_ptr[i] + (int32_t)lists[i].size();
-        P.merge_idx.insert(P.merge_idx.end(), lists[i].begin(), lists[i].end());
+        int32_t *row = &P.merge_tab[i * (size_t)H.merge_stride];
+        row[0] = (int32_t)lists[i].size();
+        std::copy(lists[i].begin(), lists[i].end(), row + 1);
     }
     H.n_tc = (int32_t)P.tc.size();
     H.n_small = (int32_t)P.small.size();
@@ -551,20 +559,16 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
         return HP_ERR_UNSUPPORTED;  // the step's page lists exceed what the CTAs' records hold
     build_records(P);
     H.n_part_rows = (int32_t)part;
-    H.n_merge = (int32_t)P.merge_idx.size();
+    H.n_merge = (int32_t)n_merge;
 
     // device layout: header, maps and records at fixed offsets, merge lists
     size_t rec_max = sizeof(RecHead);
     for (const auto &r : P.records)
         rec_max = std::max(rec_max, r.size());
     H.rec_stride = (int32_t)round_up(rec_max, 128);
-    size_t off = kPlanRecOff + (size_t)H.rec_stride * sms;
-    off = round_up(off, 64);
-    H.off_merge_ptr = (int64_t)off;
-    off += 4 * P.merge_ptr.size();
-    off = round_up(off, 64);
-    H.off_merge_idx = (int64_t)off;
-    off += 4 * std::max<size_t>(P.merge_idx.size(), 1);
+    size_t off = plan_tab_offset(sms, H.rec_stride);
+    H.off_merge_tab = (int64_t)off;
+    off += 4 * P.merge_tab.size();
     H.total_bytes = (int64_t)round_up(off, 256);
     const WsLayout ws = ws_layout(part, d->d);
     H.ws_off_lse = (int64_t)ws.off_lse;
@@ -621,8 +625,9 @@ bool plan_extent_ok(const void *plan_dev, const hp_plan_info *info)
     auto it = g_plans.find(plan_dev);
     if (it == g_plans.end())
         return false;
-    const int64_t need = (int64_t)kPlanRecOff + (int64_t)info->grid * info->rec_stride;
-    return need <= it->second.total_bytes;
+    const int64_t need = (int64_t)plan_tab_offset(info->grid, info->rec_stride) +
+                         4 * (int64_t)info->B * info->Hkv * info->merge_stride;
+    return info->merge_stride >= 1 && need <= it->second.total_bytes;
 }
 
 }  // namespace
@@ -748,7 +753,7 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
     sp.page_size = page_size;
     sp.split_len = split;
     sp.n_split = n_split;
-    sp.part_o = reinterpret_cast<float *>(wsb + wl.off_o);
+    sp.part_o = reinterpret_cast<uint16_t *>(wsb + wl.off_o);
     sp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
     sp.status = status_ptr(ws);
     const int grid = (int)std::min<int64_t>(sp.n_items, (int64_t)sms * small_ctas_per_sm(d));
@@ -819,7 +824,7 @@ hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_
         if (!encode_prefix_map(&tp.map_k, k, prefix_len, Hkv, d, kv_st, kv_sh) ||
             !encode_prefix_map(&tp.map_v, v, prefix_len, Hkv, d, kv_st, kv_sh) ||
             !encode_q_map(&tp.map_q, q, row_begin + rows, Hq, d, q_sb, q_sh, G, kTcTile / G) ||
-            !encode_o_map(&tp.map_o, reinterpret_cast<float *>(wsb + wl.off_o), g.part_rows, d))
+            !encode_o_map(&tp.map_o, reinterpret_cast<uint16_t *>(wsb + wl.off_o), g.part_rows, d))
             return HP_ERR_CUDA;
         tp.G = G;
         tp.Hkv = Hkv;
@@ -838,7 +843,7 @@ hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_
     }
     MergeParams mp;
     std::memset(&mp, 0, sizeof(mp));
-    mp.part_o = reinterpret_cast<float *>(wsb + wl.off_o);
+    mp.part_o = reinterpret_cast<const uint16_t *>(wsb + wl.off_o);
     mp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
     mp.d = d;
     mp.G = G;
@@ -893,9 +898,7 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
         std::memcpy(dst, P.records[c].data(), P.records[c].size());
         std::memcpy(dst, &H.tag, sizeof(H.tag));  // RecHead::tag
     }
-    std::memcpy(img.data() + H.off_merge_ptr, P.merge_ptr.data(), 4 * P.merge_ptr.size());
-    if (!P.merge_idx.empty())
-        std::memcpy(img.data() + H.off_merge_idx, P.merge_idx.data(), 4 * P.merge_idx.size());
+    std::memcpy(img.data() + H.off_merge_tab, P.merge_tab.data(), 4 * P.merge_tab.size());
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(plan_dev, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
@@ -911,6 +914,7 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
     info->grid = H.grid;
     info->rec_stride = H.rec_stride;
     info->num_levels = H.num_levels;
+    info->merge_stride = H.merge_stride;
     info->n_part_rows = H.n_part_rows;
     info->plan_bytes = H.total_bytes;
     info->ws_bytes = H.ws_bytes;
@@ -945,7 +949,7 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     const PlanHeader *plan = static_cast<const PlanHeader *>(plan_dev);
     const int G = info->Hq / info->Hkv;
-    float *part_o = reinterpret_cast<float *>(wsb + wl.off_o);
+    uint16_t *part_o = reinterpret_cast<uint16_t *>(wsb + wl.off_o);
     float *part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
 
     mark(0);
@@ -986,6 +990,9 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
     mp.B = info->B;
     mp.plan = plan;
     mp.tag = info->tag;
+    mp.tab = reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(plan_dev) +
+                                               plan_tab_offset(info->grid, info->rec_stride));
+    mp.tab_stride = info->merge_stride;
     mp.out = out;
     mp.out_f32 = out_dt == HP_F32;
     mp.o_sb = o_sb;

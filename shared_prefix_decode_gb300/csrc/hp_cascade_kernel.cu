@@ -38,14 +38,14 @@ struct FusedLayout {
     using T = tcr::Layout<D>;
     using S = smr::Layout<D, kNC, kSmallStages, kQRows>;
     static constexpr int kRing = T::kEnd > S::kEnd ? T::kEnd : S::kEnd;
-    static constexpr int kTcBar = kRing;           // tcr::B_COUNT barriers, then tmem slot, abort
+    static constexpr int kTcBar = kRing;           // tcr::B_COUNT barriers, tmem slot, abort (256 bytes)
     static constexpr int kSmBar = kTcBar + 256;    // full[S], empty[S]
     static constexpr int kMeta = kSmBar + 64;      // StageMeta[S]
     static constexpr int kZero = kMeta + 128;      // 16 zero bytes, then the paged role's abort flag
     static constexpr int kRecBar = kZero + 32;     // the record's barrier
     static constexpr int kRec = kRecBar + 32;      // the CTA record
     static constexpr int kBytes = kRec + kRecMaxBytes;
-    static_assert(tcr::B_COUNT * 8 <= 128, "tensor-core barriers");
+    static_assert(tcr::kBarAbort + 4 <= 256, "tensor-core barrier area");
     static_assert(2 * kSmallStages * 8 <= 64, "paged barriers");
     static_assert(kSmallStages * (int)sizeof(smr::StageMeta) <= 128, "stage metadata");
     static_assert(kRec % 16 == 0, "bulk copy destination");
@@ -119,8 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
     tc.smem = smem;
     tc.sbase = smem_u32(smem);
     tc.bar0 = tc.sbase + FL::kTcBar;
-    tc.tmem_slot = reinterpret_cast<uint32_t *>(smem + FL::kTcBar + 128);
-    tc.abort = reinterpret_cast<volatile int *>(smem + FL::kTcBar + 132);
+    tc.tmem_slot = reinterpret_cast<uint32_t *>(smem + FL::kTcBar + tcr::kBarTmemSlot);
+    tc.abort = reinterpret_cast<volatile int *>(smem + FL::kTcBar + tcr::kBarAbort);
     tc.status = p.status;
     const tcr::Args ta{p.G, p.scale_log2, &p.o_tc, p.part_lse};
 
@@ -187,6 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
         n_tc = 0;
         n_small = 0;
     }
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: everything above read only the plan.  The queries, the KV pages
+    // and the workspace (which that kernel may still be producing or
+    // reading) are touched only after it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const RecItem *items = reinterpret_cast<const RecItem *>(rec + 1);
     const int32_t *pages = reinterpret_cast<const int32_t *>(items + n_tc + n_small);
 
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
                 if (warp == 0)
                     tcr::producer_loop<D>(tc, g, lane);
                 else if (warp == 1 && lane == 0)
-                    tcr::mma_loop<D>(tc, g, tmem);
+                    tcr::mma_loop<D>(tc, g, tmem, i == 0);
             } else if (tid == 0) {
                 atomicOr(p.status, kStPlan);
             }
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
             if (i > 0)
                 tcr::named_sync(0, kThreads);
             if (tcr::item_ok(g))
-                tcr::softmax_loop<D>(tc, g, ta, tmem, warp, lane, tid);
+                tcr::softmax_loop<D>(tc, g, ta, tmem, warp, lane, tid, i == 0);
             // the epilogue wrote shared memory that TMA refills next
             fence_proxy_async_smem();
             tc_fence_before();
@@ -261,8 +266,19 @@ cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
             return cudaErrorInvalidConfiguration;  // the register split assumes this allocation
         configured = true;
     }
-    hp_cascade_kernel<D><<<grid, kThreads, bytes, s>>>(p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the CTAs may start (and fetch their
+    // records) while the previous kernel finishes; see griddepcontrol.wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, hp_cascade_kernel<D>, p);
 }
 
 }  // namespace

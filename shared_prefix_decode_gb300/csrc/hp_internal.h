@@ -19,6 +19,10 @@ constexpr int kTcMaxRows = 256;               // query rows per tensor-core item
 constexpr int kSmallRows = 16;                // query rows per small item (one m16 tile)
 constexpr int kChunk = 16;                    // keys per small-kernel chunk
 constexpr size_t kWsHeader = 256;             // status word + reserved
+// Partial attention states in the workspace: LSE as f32, O / l as bf16 (raw
+// bits) -- the partial rows are written once and read once, and their bytes
+// cross the SMs' ports twice; bf16 keeps 8 significant bits, the precision
+// of the bf16 output.
 
 // Device status bits (the first word of every workspace).
 enum : uint32_t { kStBounds = 1u, kStTimeout = 2u, kStPlan = 4u };
@@ -59,9 +63,8 @@ struct alignas(64) PlanHeader {
     int32_t small_nh;       // KV heads per paged item
     int32_t grid;           // CTAs of the fused kernel (one record per CTA)
     int32_t rec_stride;     // bytes per CTA record (multiple of 128)
-    int32_t pad0;
-    int64_t off_merge_ptr;  // [B*Hkv + 1] int32
-    int64_t off_merge_idx;  // [n_merge] int32: partial row of (b, g = 0)
+    int32_t merge_stride;   // int32 per merge-table row
+    int64_t off_merge_tab;  // [B*Hkv][merge_stride] int32: count, then partial rows of (b, g = 0)
     int64_t total_bytes;
     int64_t ws_bytes;
     int64_t ws_off_lse;     // byte offsets into the workspace
@@ -73,6 +76,11 @@ struct alignas(64) PlanHeader {
 // kMaxLevels slots), then one record per CTA of the fused kernel.
 constexpr size_t kPlanMapsOff = (sizeof(PlanHeader) + 127) / 128 * 128;
 constexpr size_t kPlanRecOff = kPlanMapsOff + (size_t)kMaxLevels * kMapsPerLevel * sizeof(CUtensorMap);
+// The merge table follows the records.
+inline size_t plan_tab_offset(int grid, int rec_stride)
+{
+    return (kPlanRecOff + (size_t)grid * rec_stride + 63) / 64 * 64;
+}
 
 // ------------------------------------------------------------ CTA records
 // Everything one CTA of the fused kernel needs to start its work, fetched
@@ -100,7 +108,7 @@ struct TcParams {
     CUtensorMap map_k;  // [len][Hkv][d]: box 64 columns x 1 head x 128 tokens
     CUtensorMap map_v;
     CUtensorMap map_q;  // [B][Hq][d]: box 64 columns x G heads x (128 / G) rows
-    CUtensorMap map_o;  // partial O [rows][d] f32: box 32 columns x 128 rows
+    CUtensorMap map_o;  // partial O [rows][d] bf16: box 64 columns x 128 rows
     int32_t G, Hkv;
     float scale_log2;   // softmax scale * log2(e)
     int32_t n_items;    // item i owns partial rows [256 i, 256 i + 256)
@@ -126,7 +134,7 @@ struct SmallParams {
     int32_t q_slot;  // map_q is valid (nh * G <= small_q_rows()): Q rows arrive with each item's first chunk
     const uint16_t *q;  // otherwise the consumers read q[b][h][:] themselves
     int64_t q_sb, q_sh;
-    float *part_o;
+    uint16_t *part_o;   // bf16
     float *part_lse;
     uint32_t *status;
 };
@@ -135,7 +143,7 @@ struct SmallParams {
 struct CascadeParams {
     CUtensorMap q_tc;      // box 64 columns x G heads x (128 / G) rows
     CUtensorMap q_sm;      // box 64 columns x (nh * G) heads x 1 row
-    CUtensorMap o_tc;      // partial O [rows][d] f32: box 32 columns x 128 rows (tensor-core stores)
+    CUtensorMap o_tc;      // partial O [rows][d] bf16: box 64 columns x 128 rows (tensor-core stores)
     const uint8_t *plan;   // plan image (maps at kPlanMapsOff, records at kPlanRecOff)
     uint64_t tag;
     int32_t rec_stride;
@@ -145,19 +153,21 @@ struct CascadeParams {
     const uint16_t *q;     // otherwise the paged role reads q[b][h][:] itself
     int64_t q_sb, q_sh;
     float scale_log2;
-    float *part_o;
+    uint16_t *part_o;      // bf16 (paged role; the tensor-core role stores through o_tc)
     float *part_lse;
     uint32_t *status;
 };
 
 // Merge kernel: combines the partial rows of each output row.
 struct MergeParams {
-    const float *part_o;
+    const uint16_t *part_o;  // bf16
     const float *part_lse;
     int32_t d, G, Hq, Hkv, B;
-    // plan mode (plan != nullptr): CSR over (b, kvh) found through the header
+    // plan mode (plan != nullptr): the plan's merge table, one row per (b, kvh)
     const PlanHeader *plan;
     uint64_t tag;
+    const int32_t *tab;
+    int32_t tab_stride;
     // implicit modes (plan == nullptr)
     int32_t mode;            // 1: paged decode splits; 2: contiguous prefix splits
     const int32_t *seq_lens; // mode 1

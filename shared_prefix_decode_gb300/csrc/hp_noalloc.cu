@@ -123,7 +123,7 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
     // Split each sequence into as few key ranges as fit the scratch: at
     // least 64 keys per range, and no more ranges than the scratch holds.
     const int max_len = pt_stride * page_size;
-    const size_t per_row = (size_t)(d + 1) * 4;  // partial O row + its LSE
+    const size_t per_row = (size_t)d * 2 + 4;  // partial O row (bf16) + its LSE
     const size_t avail = kNoAllocScratchBytes - 2 * kWsHeader;
     const int64_t rows_per_split = (int64_t)B * Hq;
     const int64_t max_splits = (int64_t)(avail / per_row) / rows_per_split;
@@ -141,7 +141,7 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
     uint8_t *base = static_cast<uint8_t *>(scratch);
     const size_t off_lse = kWsHeader;
     const size_t off_o = up(off_lse + (size_t)part_rows * 4, 256);
-    if (off_o + (size_t)part_rows * d * 4 > kNoAllocScratchBytes)
+    if (off_o + (size_t)part_rows * d * 2 > kNoAllocScratchBytes)
         return HP_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // the status word is the only scratch that must start at zero
@@ -175,7 +175,7 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
     sp.page_size = page_size;
     sp.split_len = (int)split;
     sp.n_split = n_split;
-    sp.part_o = reinterpret_cast<float *>(base + off_o);
+    sp.part_o = reinterpret_cast<uint16_t *>(base + off_o);
     sp.part_lse = reinterpret_cast<float *>(base + off_lse);
     sp.status = reinterpret_cast<uint32_t *>(base);
     int dev = 0, sms = 152;

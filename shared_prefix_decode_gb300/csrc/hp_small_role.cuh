@@ -87,7 +87,7 @@ struct Args {
     const void *map_q;      // box 64 columns x (nh * G) heads x 1 row (nh * G <= QR); null: no Q slot
     int G, nh;
     float scale_log2;
-    float *part_o;
+    uint16_t *part_o;  // bf16
     float *part_lse;
 };
 
@@ -348,18 +348,18 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
             const float inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
             const int base = m.part_row + w * rows;  // this head's rows
             if (r0 < rows) {
-                float *dst = a.part_o + (size_t)(base + r0) * D + tq;
+                uint16_t *dst = a.part_o + (size_t)(base + r0) * D + tq;
 #pragma unroll
                 for (int n = 0; n < kNt; ++n)
-                    *reinterpret_cast<float2 *>(dst + n * 8) = make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                    *reinterpret_cast<uint32_t *>(dst + n * 8) = pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
                 if ((lane & 3) == 0)
                     a.part_lse[base + r0] = L0 > 0.f ? (m0 + fast_log2(L0)) * kLn2 : -INFINITY;
             }
             if (r1 < rows) {
-                float *dst = a.part_o + (size_t)(base + r1) * D + tq;
+                uint16_t *dst = a.part_o + (size_t)(base + r1) * D + tq;
 #pragma unroll
                 for (int n = 0; n < kNt; ++n)
-                    *reinterpret_cast<float2 *>(dst + n * 8) = make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                    *reinterpret_cast<uint32_t *>(dst + n * 8) = pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
                 if ((lane & 3) == 0)
                     a.part_lse[base + r1] = L1 > 0.f ? (m1 + fast_log2(L1)) * kLn2 : -INFINITY;
             }

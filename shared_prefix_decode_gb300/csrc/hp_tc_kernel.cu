@@ -56,8 +56,8 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
     c.smem = smem;
     c.sbase = smem_u32(smem);
     c.bar0 = c.sbase + KL::kBar;
-    c.tmem_slot = reinterpret_cast<uint32_t *>(smem + KL::kBar + 128);
-    c.abort = reinterpret_cast<volatile int *>(smem + KL::kBar + 132);
+    c.tmem_slot = reinterpret_cast<uint32_t *>(smem + KL::kBar + tcr::kBarTmemSlot);
+    c.abort = reinterpret_cast<volatile int *>(smem + KL::kBar + tcr::kBarAbort);
     c.status = p.status;
     const tcr::Args a{p.G, p.scale_log2, &p.map_o, p.part_lse};
 
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
             tcr::producer_prologue<D>(c, g, a, lane);
             tcr::producer_loop<D>(c, g, lane);
         } else if (warp == 1 && lane == 0) {
-            tcr::mma_loop<D>(c, g, tmem);
+            tcr::mma_loop<D>(c, g, tmem, true);
         }
         __syncwarp();
         tc_fence_before();
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
         }
     } else {
         setmaxnreg_inc<tcr::kRegsSoftmax>();
-        tcr::softmax_loop<D>(c, g, a, tmem, warp, lane, tid);
+        tcr::softmax_loop<D>(c, g, a, tmem, warp, lane, tid, true);
         tc_fence_before();
         tcr::named_sync(0, tcr::kThreads);
     }

@@ -30,7 +30,7 @@
 //               over the S columns, rescale O in TMEM when the max grows by
 //               more than 2^8 (the reference max is kept otherwise; exact,
 //               since the final O / l uses the same reference), and at the end
-//               stage O / l in shared memory as 128-row x 32-column boxes
+//               stage O / l (bf16) in shared memory as 128-row x 64-column boxes
 //               that one thread writes out with TMA tensor stores (the
 //               partial rows of a block are 128 reserved rows of the
 //               workspace).  The loops walk the row in 32-column chunks
@@ -68,13 +68,16 @@ struct Layout {
     static constexpr int kK = kQ + 2 * kTile;
     static constexpr int kV = kK + 2 * kTile;
     static constexpr int kEnd = kV + 2 * kTile;  // O staging reuses K (block 0) and V (block 1)
-    static constexpr int kOBox = 128 * 128;      // [128 rows][32 f32], 128-byte swizzle
-    static_assert(2 * kTile >= (D / 32) * kOBox, "O staging must fit one ring");
+    static constexpr int kOBox = 128 * 128;      // [128 rows][64 bf16], 128-byte swizzle
+    static_assert(2 * kTile >= (D / 64) * kOBox, "O staging must fit one ring");
 };
 
 // barrier slots (8 bytes each) at the caller's barrier area
 enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_S = 8, B_P = 10, B_O = 12, B_DRAIN = 14,
-       B_Q = 15, B_COUNT = 16 };
+       B_Q = 15, B_WARM = 16, B_COUNT = 18 };
+// Byte offsets in the caller's 256-byte barrier area.
+constexpr int kBarTmemSlot = 192, kBarAbort = 196;
+static_assert(B_COUNT * 8 <= kBarTmemSlot, "barrier area");
 
 struct ItemGeo {
     int seq_begin, n_seq, kvh, k0, k1, part_row;
@@ -99,7 +102,7 @@ struct Ctx {
 struct Args {
     int G;
     float scale_log2;  // > 0
-    const void *map_o;  // partial O rows [rows][D] f32: box 32 columns x 128 rows, 128-byte swizzle
+    const void *map_o;  // partial O rows [rows][D] bf16: box 64 columns x 128 rows, 128-byte swizzle
     float *part_lse;
 };
 
@@ -132,7 +135,7 @@ __device__ __forceinline__ void init_barriers(const Ctx &c, bool reinit)
     for (int i = 0; i < B_COUNT; ++i) {
         if (reinit)
             mbar_inval(bar_at(c, i));
-        mbar_init(bar_at(c, i), (i == B_P || i == B_P + 1) ? 128u : 1u);
+        mbar_init(bar_at(c, i), (i == B_P || i == B_P + 1 || i == B_WARM || i == B_WARM + 1) ? 128u : 1u);
     }
     *c.abort = 0;
     fence_mbar_init();
@@ -232,8 +235,10 @@ __device__ __forceinline__ void producer_loop(const Ctx &c, const ItemGeo &g, in
 }
 
 // One thread (warp 1, lane 0).
+// `warm`: the softmax warps first run a dry pass over the S columns (see
+// softmax_loop); the first S waits for it.
 template <int D>
-__device__ __forceinline__ void mma_loop(const Ctx &c, const ItemGeo &g, uint32_t tmem)
+__device__ __forceinline__ void mma_loop(const Ctx &c, const ItemGeo &g, uint32_t tmem, bool warm)
 {
     using L = Layout<D>;
     constexpr int kHalves = D / 64;
@@ -261,6 +266,8 @@ __device__ __forceinline__ void mma_loop(const Ctx &c, const ItemGeo &g, uint32_
     };
     bool ok = mbar_wait(bar_at(c, B_Q), 0u, c.status, c.abort) &&
               mbar_wait(bar_at(c, B_KFULL + 0), 0u, c.status, c.abort);
+    for (int mb = 0; ok && warm && mb < nmb; ++mb)
+        ok = mbar_wait(bar_at(c, B_WARM + mb), 0u, c.status, c.abort);
     if (ok) {
         tc_fence_after();
         for (int mb = 0; mb < nmb; ++mb)
@@ -300,10 +307,14 @@ __device__ __forceinline__ void mma_loop(const Ctx &c, const ItemGeo &g, uint32_
     mbar_wait_drain(bar_at(c, B_DRAIN), 0u);
 }
 
-// Warps 4-11 (mb = 0 for warps 4-7, 1 for 8-11).
+// Warps 4-11 (mb = 0 for warps 4-7, 1 for 8-11).  `warm`: before the first
+// tile, run the loop body once on whatever the S columns hold and discard
+// the result (the MMA waits for it through B_WARM): the body's instructions
+// are then in the instruction cache when the first scores land, instead of
+// being fetched while HBM is saturated.
 template <int D>
 __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, const Args &a, uint32_t tmem,
-                                             int warp, int lane, int tid)
+                                             int warp, int lane, int tid, bool warm)
 {
     using L = Layout<D>;
     constexpr int kHalves = D / 64;
@@ -318,6 +329,7 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
     const uint32_t s_col = tl + mb * 128;
     const uint32_t o_col = tl + 256 + mb * 128;
     const float cs = a.scale_log2;
+    const uint64_t cs2 = f32x2_pack(cs, cs);
     auto wait_warp = [&](int b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar_at(c, b), parity, c.status, c.abort)) != 0;
     };
@@ -325,11 +337,12 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
     float l_run = 0.f;
     bool ok = mb < nmb;
     uint32_t r[32];
-    for (int j = 0; ok && j < n_tiles; ++j) {
-        if (!(ok = wait_warp(B_S + mb, (uint32_t)j & 1u)))
+    for (int j = warm ? -1 : 0; ok && j < n_tiles; ++j) {
+        const bool dry = j < 0;
+        if (!dry && !(ok = wait_warp(B_S + mb, (uint32_t)j & 1u)))
             break;
         tc_fence_after();
-        const int nvalid = min(kTcTile, g.k1 - (g.k0 + j * kTcTile));
+        const int nvalid = dry ? kTcTile : min(kTcTile, g.k1 - (g.k0 + j * kTcTile));
         // largest valid score (the scale is positive: the largest scaled
         // score is the largest raw score times the scale)
         float mx = -INFINITY;
@@ -338,9 +351,15 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
             tmem_ld32(s_col + cc * 32, r);
             tmem_ld_wait();
             const int lim = nvalid - cc * 32;
+            if (lim >= 32) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                mx = fmaxf(mx, i < lim ? __uint_as_float(r[i]) : -INFINITY);
+                for (int i = 0; i < 32; i += 2)
+                    mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    mx = fmaxf(mx, i < lim ? __uint_as_float(r[i]) : -INFINITY);
+            }
         }
         const float tmax = mx * cs;
         const bool need = tmax > m_run + kTau;
@@ -350,25 +369,52 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
             m_run = tmax;
         }
         // P = exp2(s * c - m) as bf16 pairs over the S columns (chunk cc's P
-        // lands in columns already read); invalid keys get P = 0
+        // lands in columns already read); invalid keys get P = 0.  Pairs of
+        // scores go through the packed f32x2 fma / add.
         const float nm = -m_run;
-        float lsum = 0.f;
+        const uint64_t nm2 = f32x2_pack(nm, nm);
+        uint64_t acc2 = f32x2_pack(0.f, 0.f);
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
             tmem_ld32(s_col + cc * 32, r);
             tmem_ld_wait();
             const int lim = nvalid - cc * 32;
             uint32_t pk[16];
+            if (lim >= 32) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), cs, nm));
-                float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), cs, nm));
-                p0 = 2 * i < lim ? p0 : 0.f;
-                p1 = 2 * i + 1 < lim ? p1 : 0.f;
-                lsum += p0 + p1;
-                pk[i] = pack_bf16x2(p0, p1);
+                for (int i = 0; i < 16; ++i) {
+                    float x0, x1;
+                    f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                           cs2, nm2),
+                                 x0, x1);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    acc2 = f32x2_add(acc2, f32x2_pack(p0, p1));
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), cs, nm));
+                    float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), cs, nm));
+                    p0 = 2 * i < lim ? p0 : 0.f;
+                    p1 = 2 * i + 1 < lim ? p1 : 0.f;
+                    acc2 = f32x2_add(acc2, f32x2_pack(p0, p1));
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
             }
             tmem_st16(s_col + cc * 16, pk);
+        }
+        float lsum0, lsum1;
+        f32x2_unpack(acc2, lsum0, lsum1);
+        const float lsum = lsum0 + lsum1;
+        if (dry) {
+            // the result of the dry pass is discarded
+            m_run = -INFINITY;
+            l_run = 0.f;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_at(c, B_WARM + mb));
+            continue;
         }
         l_run += lsum;
         // O was accumulated against the old reference max: rescale it once
@@ -408,11 +454,12 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
         mbar_arrive(bar_at(c, B_P + mb));
     }
     // Epilogue: O / l into shared memory (block 0 over the K ring, block 1
-    // over the V ring, both idle once the last P V has completed) as D/32
-    // boxes of [128 rows][32 f32] in the 128-byte swizzled order the tensor
-    // map expects (conflict-free: 8 consecutive rows hit 8 distinct 16-byte
-    // slots), then one thread of the block stores the boxes to partial rows
-    // part_row + mb*128 .. +127 and waits until they have been read.
+    // over the V ring, both idle once the last P V has completed) as D/64
+    // bf16 boxes of [128 rows][64 columns] in the 128-byte swizzled order the
+    // tensor map expects (conflict-free: 8 consecutive rows hit 8 distinct
+    // 16-byte slots), then one thread of the block stores the boxes to
+    // partial rows part_row + mb*128 .. +127 and waits until they have been
+    // read.
     const bool have = ok && mb < nmb;
     uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
     if (have && wait_warp(B_O + mb, (uint32_t)(n_tiles - 1) & 1u)) {
@@ -420,19 +467,20 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
         const float inv = 1.f / l_run;
         uint32_t r2[32];
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; cc += 2) {
-            tmem_ld32(o_col + cc * 32, r);
-            tmem_ld32(o_col + cc * 32 + 32, r2);
+        for (int bx = 0; bx < D / 64; ++bx) {
+            tmem_ld32(o_col + bx * 64, r);
+            tmem_ld32(o_col + bx * 64 + 32, r2);
             tmem_ld_wait();
-            uint8_t *box = stg + cc * L::kOBox + rr * 128;
+            uint8_t *row = stg + bx * L::kOBox + rr * 128;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                *reinterpret_cast<float4 *>(box + ((i ^ (rr & 7)) << 4)) =
-                    make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
-                *reinterpret_cast<float4 *>(box + L::kOBox + ((i ^ (rr & 7)) << 4)) =
-                    make_float4(__uint_as_float(r2[4 * i]) * inv, __uint_as_float(r2[4 * i + 1]) * inv,
-                                __uint_as_float(r2[4 * i + 2]) * inv, __uint_as_float(r2[4 * i + 3]) * inv);
+            for (int i = 0; i < 8; ++i) {  // 16-byte piece i: columns bx*64 + 8i .. +7
+                const uint32_t *src = i < 4 ? &r[8 * i] : &r2[8 * (i - 4)];
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
+                v.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
+                v.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
+                v.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
+                *reinterpret_cast<uint4 *>(row + ((i ^ (rr & 7)) << 4)) = v;
             }
         }
         if (rr < rows_here)
@@ -442,8 +490,8 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
     tc_fence_before();
     named_sync(1 + mb, 128);
     if (have && rr == 0) {
-        for (int cc = 0; cc < D / 32; ++cc)
-            tma_store_2d(a.map_o, smem_u32(stg + cc * L::kOBox), cc * 32, g.part_row + mb * 128);
+        for (int bx = 0; bx < D / 64; ++bx)
+            tma_store_2d(a.map_o, smem_u32(stg + bx * L::kOBox), bx * 64, g.part_row + mb * 128);
         bulk_commit_group();
         bulk_wait_read_all();
     }
