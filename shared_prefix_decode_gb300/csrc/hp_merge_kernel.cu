@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "hp_internal.h"
+#include "hp_merge_row.cuh"
 #include "hp_ptx.cuh"
 
 namespace hp {
@@ -20,7 +21,6 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMergeWarps = 4;
-constexpr int kChunkParts = 16;  // parts of a row loaded together
 
 // Partial row of entry e of output row (b, h).
 struct PartList {
@@ -49,9 +49,6 @@ __device__ __forceinline__ int part_row(const MergeParams &p, const PartList &L,
 template <int VPT>  // values per lane: d / 32
 __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeParams p)
 {
-    // a kernel launched after this one as a programmatic dependent (the next
-    // step's persistent kernel) may start its plan-only set-up meanwhile
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * kMergeWarps + warp;
     const int64_t n_rows = (int64_t)p.B * p.Hq;
@@ -91,213 +88,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeP
         pr_a = lane < L.n ? part_row(p, L, lane) : 0;
         pr_b = lane + 32 < L.n ? part_row(p, L, lane + 32) : 0;
     }
-    // Everything above depends on the plan alone: when launched as a
-    // dependent of the kernel that writes the partial states, it overlaps that
-    // kernel's tail.
     if (p.wait_prior)
         asm volatile("griddepcontrol.wait;" ::: "memory");  // the partial states are complete
-
-    // Online merge over chunks of up to kChunkParts parts: every LSE and O row
-    // of a chunk is loaded before any is used (one memory round trip per
-    // chunk), then the chunk joins the running state -- max M, denominator,
-    // weighted sum, rescaled when M grows.  The parts are taken in their fixed
-    // order, so the result is deterministic.  Every lane reads the same LSEs
-    // and its own VPT columns of each O row.
-    float M = -INFINITY, den = 0.f;
-    float acc[VPT];
-#pragma unroll
-    for (int i = 0; i < VPT; ++i)
-        acc[i] = 0.f;
-    for (int e0 = 0; e0 < L.n; e0 += kChunkParts) {
-        const int cnt = min(kChunkParts, L.n - e0);
-        float ls[kChunkParts];
-        float v[kChunkParts][VPT];
-#pragma unroll
-        for (int k = 0; k < kChunkParts; ++k) {
-            const int e = e0 + k;
-            int pr = __shfl_sync(0xffffffffu, e < 32 ? pr_a : pr_b, e & 31);
-            if (e >= 64 && k < cnt)
-                pr = part_row(p, L, e);
-            ls[k] = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < VPT; ++i)
-                v[k][i] = 0.f;
-            if (k < cnt) {
-                ls[k] = __ldg(p.part_lse + pr);
-                const uint16_t *src = p.part_o + (size_t)pr * p.d + lane * VPT;  // bf16
-                if (VPT == 4) {
-                    const uint2 x = __ldg(reinterpret_cast<const uint2 *>(src));
-                    v[k][0] = bf16lo_to_f32(x.x);
-                    v[k][1] = bf16hi_to_f32(x.x);
-                    v[k][2] = bf16lo_to_f32(x.y);
-                    v[k][3] = bf16hi_to_f32(x.y);
-                } else {
-                    const uint32_t x = __ldg(reinterpret_cast<const uint32_t *>(src));
-                    v[k][0] = bf16lo_to_f32(x);
-                    v[k][1] = bf16hi_to_f32(x);
-                }
-            }
-        }
-        float mc = M;
-#pragma unroll
-        for (int k = 0; k < kChunkParts; ++k)
-            mc = fmaxf(mc, ls[k]);
-        if (mc == -INFINITY)
-            continue;  // every part so far is empty
-        const float sc = fast_exp2((M - mc) * kLog2e);  // 0 while M = -inf
-        den *= sc;
-#pragma unroll
-        for (int i = 0; i < VPT; ++i)
-            acc[i] *= sc;
-#pragma unroll
-        for (int k = 0; k < kChunkParts; ++k) {
-            const float w = fast_exp2((ls[k] - mc) * kLog2e);  // 0 for an empty part
-            den += w;
-#pragma unroll
-            for (int i = 0; i < VPT; ++i)
-                acc[i] = fmaf(w, v[k][i], acc[i]);
-        }
-        M = mc;
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    const int64_t off = (int64_t)L.b * p.o_sb + (int64_t)h * p.o_sh + lane * VPT;
-    if (p.out_f32) {
-        float *dst = reinterpret_cast<float *>(p.out) + off;
-#pragma unroll
-        for (int i = 0; i < VPT; ++i)
-            dst[i] = acc[i] * inv;
-    } else {
-        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + off;
-#pragma unroll
-        for (int i = 0; i < VPT; i += 2)
-            *reinterpret_cast<__nv_bfloat162 *>(dst + i) = __floats2bfloat162_rn(acc[i] * inv, acc[i + 1] * inv);
-    }
-    if (lane == 0 && p.lse != nullptr)
-        p.lse[(int64_t)L.b * p.lse_sb + h] = den > 0.f ? M + __logf(den) : -INFINITY;
-}
-
-// Grouped merge: one warp per kRowsPerWarp = 512 / D consecutive query heads
-// of one KV head.  Those heads share their list of parts, and a part's rows
-// for them are contiguous, so lane l owns 16 columns of row l / (32 /
-// kRowsPerWarp): per part, one LSE and one 32-byte load per lane.  Same
-// online merge and part order as hp_merge_kernel.
-constexpr int kGroupWarps = 2;
-constexpr int kGroupChunk = 16;
-
-template <int D>
-__global__ void __launch_bounds__(kGroupWarps * 32) hp_merge_group_kernel(const MergeParams p)
-{
-    constexpr int kRowsPerWarp = 512 / D, kLanesPerRow = 32 / kRowsPerWarp, kVals = D / kLanesPerRow;
-    static_assert(kVals == 16, "16 columns per lane");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int per_kvh = p.G / kRowsPerWarp;  // warps per (b, kvh)
-    const int64_t gw = (int64_t)blockIdx.x * kGroupWarps + warp;
-    if (gw >= (int64_t)p.B * p.Hkv * per_kvh)
-        return;
-    PartList L;
-    L.b = (int)(gw / ((int64_t)p.Hkv * per_kvh));
-    const int rem = (int)(gw % ((int64_t)p.Hkv * per_kvh));
-    L.kvh = rem / per_kvh;
-    const int g = (rem % per_kvh) * kRowsPerWarp + lane / kLanesPerRow;  // this lane's head in the group
-    const int c0 = (lane % kLanesPerRow) * kVals;                       // and its first column
-    L.g = 0;  // rows below are of head 0; each lane adds its own g
-    int base_a = 0, base_b = 0;
-    if (p.plan != nullptr) {
-        L.trow = p.tab + (size_t)(L.b * p.Hkv + L.kvh) * p.tab_stride;
-        const uint32_t magic = p.plan->magic;
-        const uint64_t tag = p.plan->tag;
-        L.n = __ldg(L.trow);
-        base_a = lane + 1 < p.tab_stride ? __ldg(L.trow + 1 + lane) : 0;
-        base_b = lane + 33 < p.tab_stride ? __ldg(L.trow + 33 + lane) : 0;
-        if (magic != kPlanMagic || tag != p.tag || L.n < 0 || L.n >= p.tab_stride) {
-            if (lane == 0)
-                atomicOr(p.status, kStPlan);
-            return;
-        }
-    } else {
-        L.trow = nullptr;
-        if (p.mode == 1) {
-            int len = __ldg(p.seq_lens + L.b);
-            len = max(0, len);
-            L.n = min(p.n_split, (len + p.split_len - 1) / p.split_len);
-        } else {
-            L.n = p.n_split;
-        }
-        base_a = lane < L.n ? part_row(p, L, lane) : 0;
-        base_b = lane + 32 < L.n ? part_row(p, L, lane + 32) : 0;
-    }
-    if (p.wait_prior)
-        asm volatile("griddepcontrol.wait;" ::: "memory");  // the partial states are complete
-    float M = -INFINITY, den = 0.f;
-    float acc[kVals];
-#pragma unroll
-    for (int i = 0; i < kVals; ++i)
-        acc[i] = 0.f;
-    {
-        for (int e0 = 0; e0 < L.n; e0 += kGroupChunk) {
-            const int cnt = min(kGroupChunk, L.n - e0);
-            float ls[kGroupChunk];
-            uint4 v[kGroupChunk][2];
-#pragma unroll
-            for (int k = 0; k < kGroupChunk; ++k) {
-                const int e = e0 + k;
-                int pr = __shfl_sync(0xffffffffu, e < 32 ? base_a : base_b, e & 31);
-                if (e >= 64 && k < cnt)
-                    pr = part_row(p, L, e);
-                pr += g;
-                ls[k] = -INFINITY;
-                v[k][0] = v[k][1] = make_uint4(0u, 0u, 0u, 0u);
-                if (k < cnt) {
-                    // L2 only (.cg): each partial row is read once
-                    ls[k] = __ldcg(p.part_lse + pr);
-                    const uint4 *src = reinterpret_cast<const uint4 *>(p.part_o + (size_t)pr * D + c0);
-                    v[k][0] = __ldcg(src);
-                    v[k][1] = __ldcg(src + 1);
-                }
-            }
-            float mc = M;
-#pragma unroll
-            for (int k = 0; k < kGroupChunk; ++k)
-                mc = fmaxf(mc, ls[k]);
-            if (mc == -INFINITY)
-                continue;  // every part so far is empty
-            const float sc = fast_exp2((M - mc) * kLog2e);  // 0 while M = -inf
-            den *= sc;
-#pragma unroll
-            for (int i = 0; i < kVals; ++i)
-                acc[i] *= sc;
-#pragma unroll
-            for (int k = 0; k < kGroupChunk; ++k) {
-                const float w = fast_exp2((ls[k] - mc) * kLog2e);  // 0 for an empty part
-                den += w;
-                const uint32_t x[8] = {v[k][0].x, v[k][0].y, v[k][0].z, v[k][0].w,
-                                       v[k][1].x, v[k][1].y, v[k][1].z, v[k][1].w};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    acc[2 * j] = fmaf(w, bf16lo_to_f32(x[j]), acc[2 * j]);
-                    acc[2 * j + 1] = fmaf(w, bf16hi_to_f32(x[j]), acc[2 * j + 1]);
-                }
-            }
-            M = mc;
-        }
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    const int h = L.kvh * p.G + g;
-    const int64_t off = (int64_t)L.b * p.o_sb + (int64_t)h * p.o_sh + c0;
-    if (p.out_f32) {
-        float *dst = reinterpret_cast<float *>(p.out) + off;
-#pragma unroll
-        for (int j = 0; j < kVals; j += 2)
-            *reinterpret_cast<float2 *>(dst + j) = make_float2(acc[j] * inv, acc[j + 1] * inv);
-    } else {
-        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + off;
-#pragma unroll
-        for (int j = 0; j < kVals; j += 2)
-            *reinterpret_cast<__nv_bfloat162 *>(dst + j) = __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
-    }
-    if (lane % kLanesPerRow == 0 && p.lse != nullptr)
-        p.lse[(int64_t)L.b * p.lse_sb + h] = den > 0.f ? M + __logf(den) : -INFINITY;
+    const size_t esz = p.out_f32 ? 4 : 2;
+    mrg::RowOut o;
+    o.out = static_cast<uint8_t *>(p.out) + ((int64_t)L.b * p.o_sb + (int64_t)h * p.o_sh) * esz;
+    o.out_f32 = p.out_f32;
+    o.lse = p.lse != nullptr ? p.lse + (int64_t)L.b * p.lse_sb + h : nullptr;
+    mrg::merge_row<VPT * 32, 2>(p.part_o, p.part_lse, L.n, pr_a, pr_b, [&](int e) { return part_row(p, L, e); }, lane, o);
 }
 
 // Two-state merge of arbitrary d: one warp per row.
@@ -346,20 +144,11 @@ static cudaError_t merge_configure()
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(hp_merge2_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
-        if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(hp_merge_group_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     (int)cudaSharedmemCarveoutMaxShared);
-        if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(hp_merge_group_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     (int)cudaSharedmemCarveoutMaxShared);
+
         return r;
     }();
     return e;
 }
-
-// The grouped kernel when a KV head's query heads split into whole warps of
-// 512 / d heads; the per-row kernel otherwise.
-static bool use_group(const MergeParams &p) { return (p.d == 128 && p.G % 4 == 0) || (p.d == 64 && p.G % 8 == 0); }
 
 template <class K>
 static cudaError_t launch_with(K kernel, const MergeParams &p, int64_t warps, int per_cta, bool dependent, cudaStream_t s)
@@ -385,11 +174,6 @@ static cudaError_t launch_merge_any(const MergeParams &p_in, int64_t out_rows, b
         return e;
     MergeParams p = p_in;
     p.wait_prior = dependent ? 1 : 0;
-    if (use_group(p)) {
-        const int64_t warps = out_rows / (512 / p.d);
-        return p.d == 128 ? launch_with(hp_merge_group_kernel<128>, p, warps, kGroupWarps, dependent, s)
-                          : launch_with(hp_merge_group_kernel<64>, p, warps, kGroupWarps, dependent, s);
-    }
     return p.d == 128 ? launch_with(hp_merge_kernel<4>, p, out_rows, kMergeWarps, dependent, s)
                       : launch_with(hp_merge_kernel<2>, p, out_rows, kMergeWarps, dependent, s);
 }
