@@ -220,13 +220,12 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
                           hp_plan_info *info, hp_stream_t stream);
 
 /* One cascade decode step: every sequence, every head, all levels, merged
- * (normally one cooperative launch that also merges; a second, merge kernel
- * when the device cannot hold every CTA of that launch at once).
+ * (two launches: the persistent kernel of both passes, then the merge kernel
+ * as its programmatic dependent).
  * q, out, lse as in the conventions above, for all B sequences; q strides
  * multiples of 8 elements, positive, and q 16-byte aligned (q is read by TMA).
- * ws: >= info->ws_bytes; its first 256 bytes must be zero before its first
- * use (zeroed memory; every call leaves them so, hp_read_device_status too),
- * and one workspace serves one call at a time.  plan_dev must hold the plan hp_cascade_plan last
+ * ws: >= info->ws_bytes; one workspace serves one call at a time.
+ * plan_dev must hold the plan hp_cascade_plan last
  * wrote there in this process, and info must describe a plan no larger than
  * it (HP_ERR_ARG otherwise, before any launch); an info of another plan of the
  * same size is reported by the kernels through the status word.
@@ -239,10 +238,9 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
 /* The same step, recording caller-created CUDA events (cudaEvent_t handles;
  * any may be NULL) on `stream` -- as external event nodes when the stream is
  * being captured, so they time each replay: events[0] before the step's
- * persistent kernel (prefix and suffix passes, and the merge when it is done
- * in the same launch), events[1] after it, events[2] after the merge kernel
- * (right after events[1] when there is none; events[3] is not used) -- for
- * timing each kernel of the step on its own stream.  With events[1] given, the merge is
+ * persistent kernel (prefix and suffix passes), events[1] after it,
+ * events[2] after the merge kernel (events[3] is not used) -- for timing each
+ * kernel of the step on its own stream.  With events[1] given, the merge is
  * launched after it instead of overlapping the persistent kernel's tail. */
 hp_status hp_cascade_decode_profiled(const void *plan_dev, const hp_plan_info *info, const void *q,
                                      int64_t q_sb, int64_t q_sh, float scale, void *out,

@@ -127,7 +127,8 @@ bool out_layout_ok(const void *out, hp_dtype dt, int64_t o_sb, int64_t o_sh, int
 {
     if (dt != HP_BF16 && dt != HP_F32)
         return false;
-    // each lane of the merge writes d/32 consecutive values
+    // the merge writes pairs of values; rows and strides aligned to d/32
+    // values (a rule of earlier lane layouts, kept: stricter than pairs need)
     const size_t esz = dt == HP_F32 ? 4 : 2;
     const size_t lane_bytes = esz * (size_t)(d / 32);
     return aligned(out, lane_bytes) && (o_sb * (int64_t)esz) % (int64_t)lane_bytes == 0 &&
@@ -285,33 +286,15 @@ double schedule(HostPlan &P, int grid, int n_tc_ctas, int d, const CostModel &cm
     return *std::max_element(load.begin(), load.end());
 }
 
-// The records of the schedule in P (one per CTA, tag left zero).  The output
-// rows of the in-kernel merge go to the CTAs without tensor-core items (they
-// finish first and wait for the others), in equal contiguous ranges; to all
-// CTAs when every CTA has tensor-core items.
+// The records of the schedule in P (one per CTA, tag left zero).
 void build_records(HostPlan &P)
 {
     const int grid = (int)P.cta_tc.size();
-    std::vector<int> mergers;
-    for (int c = 0; c < grid; ++c)
-        if (P.cta_tc[c].empty())
-            mergers.push_back(c);
-    if (mergers.empty())
-        for (int c = 0; c < grid; ++c)
-            mergers.push_back(c);
-    const int64_t rows = (int64_t)P.hdr.B * P.hdr.Hq;
-    std::vector<int32_t> mb(grid, 0), me(grid, 0);
-    for (size_t i = 0; i < mergers.size(); ++i) {
-        mb[mergers[i]] = (int32_t)(rows * (int64_t)i / (int64_t)mergers.size());
-        me[mergers[i]] = (int32_t)(rows * (int64_t)(i + 1) / (int64_t)mergers.size());
-    }
     P.records.assign(grid, {});
     for (int c = 0; c < grid; ++c) {
         RecHead h{};
         h.n_tc = (int32_t)P.cta_tc[c].size();
         h.n_small = (int32_t)P.cta_small[c].size();
-        h.merge_begin = mb[c];
-        h.merge_end = me[c];
         std::vector<RecItem> items;
         std::vector<int32_t> pages;
         auto add = [&](const WorkItem &w) {
@@ -993,38 +976,8 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         cp.part_o = part_o;
         cp.part_lse = part_lse;
         cp.status = status_ptr(ws);
-        // The merge can run in the same (cooperative) launch, every CTA
-        // waiting for all partial states; measured on the Llama-3-8B shape it
-        // is slower than the separate merge kernel launched as a programmatic
-        // dependent (24.5 vs 31.4 us per step), which is the default.
-        cp.merge = 0;
-        cp.B = info->B;
-        cp.Hq = info->Hq;
-        cp.Hkv = info->Hkv;
-        cp.tab = reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(plan_dev) +
-                                                   plan_tab_offset(info->grid, info->rec_stride));
-        cp.tab_stride = info->merge_stride;
-        cp.out = out;
-        cp.out_f32 = out_dt == HP_F32;
-        cp.o_sb = o_sb;
-        cp.o_sh = o_sh;
-        cp.lse = lse;
-        cp.lse_sb = lse_sb;
-        cp.done = reinterpret_cast<uint32_t *>(wsb + kWsDoneOff);
-        cp.exitc = reinterpret_cast<uint32_t *>(wsb + kWsExitOff);
-        cudaError_t e = launch_cascade(cp, info->grid, info->d, s);
-        if (e == cudaErrorCooperativeLaunchTooLarge) {
-            cudaGetLastError();
-            cp.merge = 0;
-            e = launch_cascade(cp, info->grid, info->d, s);
-        }
-        if (e != cudaSuccess)
+        if (launch_cascade(cp, info->grid, info->d, s) != cudaSuccess)
             return HP_ERR_CUDA;
-        if (cp.merge) {
-            mark(1);
-            mark(2);
-            return HP_OK;
-        }
     }
     mark(1);
     MergeParams mp;

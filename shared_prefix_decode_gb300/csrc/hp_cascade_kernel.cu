@@ -20,7 +20,6 @@
 #include <cuda_runtime.h>
 
 #include "hp_internal.h"
-#include "hp_merge_row.cuh"
 #include "hp_ptx.cuh"
 #include "hp_small_role.cuh"
 #include "hp_tc_role.cuh"
@@ -104,75 +103,6 @@ struct RecordItems {
     }
 };
 
-// The in-kernel merge (Hydragen Eq. 5 over each output row's parts, as the
-// merge kernel does), run by the 256 threads of warpgroups 1-2 (mw = warp - 4,
-// mt = tid - 128): every CTA reports its partial states complete (a release
-// on p.done), the CTAs the plan gave output rows wait until all have (an
-// acquire, bounded), then warp mw merges rows merge_begin + mw, +8, ...; the
-// last CTA past the phase returns both counters to zero for the next launch.
-// The launch is cooperative, so every CTA is resident and the wait ends; it
-// is bounded all the same.
-constexpr int kMergeBar = 3, kMergeThreads = 256;
-
-__device__ __forceinline__ void merge_sync() { tcr::named_sync(kMergeBar, kMergeThreads); }
-
-template <int D>
-__device__ __forceinline__ void merge_phase(const CascadeParams &p, int merge_begin, int merge_end, int mw,
-                                            int lane, int mt, volatile int *flag)
-{
-    __syncwarp();
-    merge_sync();  // this CTA's partial rows are written; they precede the release
-    if (mt == 0) {
-        __threadfence();
-        atomicAdd(p.done, 1u);
-        int ok = 1;
-        if (merge_begin < merge_end) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(p.done) < gridDim.x) {
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    atomicOr(p.status, kStTimeout);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-        *flag = ok;
-    }
-    merge_sync();
-    if (*flag && merge_begin < merge_end) {
-        const size_t esz = p.out_f32 ? 4 : 2;
-        for (int row = merge_begin + mw; row < merge_end; row += kMergeThreads / 32) {
-            const int b = row / p.Hq, h = row % p.Hq;
-            const int G = p.Hq / p.Hkv, kvh = h / G, g = h % G;
-            const int32_t *trow = p.tab + (size_t)(b * p.Hkv + kvh) * p.tab_stride;
-            const int n = __ldg(trow);
-            const int pr_a = (lane + 1 < p.tab_stride ? __ldg(trow + 1 + lane) : 0) + g;
-            const int pr_b = (lane + 33 < p.tab_stride ? __ldg(trow + 33 + lane) : 0) + g;
-            if (n < 0 || n >= p.tab_stride) {
-                if (lane == 0)
-                    atomicOr(p.status, kStPlan);
-                continue;
-            }
-            mrg::RowOut o;
-            o.out = static_cast<uint8_t *>(p.out) + ((int64_t)b * p.o_sb + (int64_t)h * p.o_sh) * esz;
-            o.out_f32 = p.out_f32;
-            o.lse = p.lse != nullptr ? p.lse + (int64_t)b * p.lse_sb + h : nullptr;
-            mrg::merge_row<D, 4>(p.part_o, p.part_lse, n, pr_a, pr_b,
-                                    [&](int e) { return __ldg(trow + 1 + e) + g; }, lane, o);
-        }
-    }
-    __syncwarp();
-    merge_sync();
-    if (mt == 0) {
-        if (atomicAdd(p.exitc, 1u) == gridDim.x - 1) {
-            // the last CTA: every CTA has passed its wait on p.done
-            *p.done = 0u;
-            *p.exitc = 0u;
-            __threadfence();
-        }
-    }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_constant__ CascadeParams p)
 {
@@ -192,9 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
     tc.tmem_slot = reinterpret_cast<uint32_t *>(smem + FL::kTcBar + tcr::kBarTmemSlot);
     tc.abort = reinterpret_cast<volatile int *>(smem + FL::kTcBar + tcr::kBarAbort);
     tc.status = p.status;
-    // with the in-kernel merge, the partial rows must be in memory (not only
-    // read out of shared memory) before the CTA reports them complete
-    const tcr::Args ta{p.G, p.scale_log2, &p.o_tc, p.part_lse, p.merge};
+    const tcr::Args ta{p.G, p.scale_log2, &p.o_tc, p.part_lse};
 
     smr::Ctx sc;
     sc.smem = smem;
@@ -259,11 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
         n_tc = 0;
         n_small = 0;
     }
-    int merge_begin = 0, merge_end = 0;
-    if (good && p.merge) {
-        merge_begin = max(0, rec->merge_begin);
-        merge_end = min(rec->merge_end, p.B * p.Hq);
-    }
     const RecItem *items = reinterpret_cast<const RecItem *>(rec + 1);
     const int32_t *pages = reinterpret_cast<const int32_t *>(items + n_tc + n_small);
 
@@ -316,11 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
         }
         if (warp - 4 < p.small_nh)
             smr::consumer<D, kNC, kSmallStages, kQRows>(sc, sa, warp - 4, lane);
-        // every partial row of this CTA was written by these 256 threads
-        // (paged rows directly, tensor-core rows by their TMA stores)
-        if (p.merge)
-            merge_phase<D>(p, merge_begin, merge_end, warp - 4, lane, tid - 128,
-                           reinterpret_cast<volatile int *>(smem + FL::kRecBar + 8));
     }
     __syncwarp();
 }
@@ -343,38 +261,8 @@ cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
             return cudaErrorInvalidConfiguration;  // the register split assumes this allocation
         configured = true;
     }
-    if (!p.merge) {
-        hp_cascade_kernel<D><<<grid, kThreads, bytes, s>>>(p);
-        return cudaGetLastError();
-    }
-    // the in-kernel merge waits for every CTA: a cooperative launch
-    // guarantees they are all resident (it fails otherwise, and the caller
-    // falls back to the separate merge kernel)
-    static int coresident = -1;
-    if (coresident < 0) {
-        int per_sm = 0, dev = 0, sms = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hp_cascade_kernel<D>, kThreads, bytes) !=
-                cudaSuccess ||
-            cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return cudaErrorCooperativeLaunchTooLarge;
-        }
-        coresident = per_sm * sms;
-    }
-    if (grid > coresident)
-        return cudaErrorCooperativeLaunchTooLarge;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = (size_t)bytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, hp_cascade_kernel<D>, p);
+    hp_cascade_kernel<D><<<grid, kThreads, bytes, s>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace

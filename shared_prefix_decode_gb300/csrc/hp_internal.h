@@ -26,9 +26,6 @@ constexpr size_t kWsHeader = 256;             // status word + reserved
 
 // Device status bits (the first word of every workspace).
 enum : uint32_t { kStBounds = 1u, kStTimeout = 2u, kStPlan = 4u };
-// Counters of the persistent kernel's in-kernel merge in the workspace header
-// (byte offsets; zero between calls).
-constexpr size_t kWsDoneOff = 64, kWsExitOff = 128;
 
 // One unit of work: query rows (sequences [seq_begin, seq_begin+n_seq) x the
 // G heads of KV head kvh) against keys [k0, k1) of one tree node.  Its rows
@@ -94,8 +91,7 @@ struct RecHead {
     uint64_t tag;
     int32_t n_tc, n_small;
     int32_t n_pages;
-    int32_t merge_begin, merge_end;  // output rows (b * Hq + h) this CTA merges (in-kernel merge)
-    int32_t pad;
+    int32_t pad[3];
 };
 struct RecItem {
     int32_t seq_begin, n_seq, kvh, k0, k1, part_row;
@@ -160,18 +156,6 @@ struct CascadeParams {
     uint16_t *part_o;      // bf16 (paged role; the tensor-core role stores through o_tc)
     float *part_lse;
     uint32_t *status;
-    // in-kernel merge (merge != 0: cooperative launch, every CTA co-resident)
-    int32_t merge;
-    int32_t B, Hq, Hkv;
-    const int32_t *tab;    // the plan's merge table
-    int32_t tab_stride;
-    void *out;
-    int32_t out_f32;
-    int64_t o_sb, o_sh;
-    float *lse;
-    int64_t lse_sb;
-    uint32_t *done;        // CTAs whose partial states are complete
-    uint32_t *exitc;       // CTAs past the merge phase
 };
 
 // Merge kernel: combines the partial rows of each output row.

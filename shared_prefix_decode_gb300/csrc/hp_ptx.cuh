@@ -154,22 +154,6 @@ __device__ __forceinline__ void bulk_wait_read_all()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// Wait until every bulk group of this thread has completed (its global
-// writes performed), then order them before this thread's later generic
-// accesses (a release by this thread then covers them).
-__device__ __forceinline__ void bulk_wait_all()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {

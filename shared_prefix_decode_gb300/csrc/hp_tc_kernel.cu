@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
     c.tmem_slot = reinterpret_cast<uint32_t *>(smem + KL::kBar + tcr::kBarTmemSlot);
     c.abort = reinterpret_cast<volatile int *>(smem + KL::kBar + tcr::kBarAbort);
     c.status = p.status;
-    const tcr::Args a{p.G, p.scale_log2, &p.map_o, p.part_lse, 0};
+    const tcr::Args a{p.G, p.scale_log2, &p.map_o, p.part_lse};
 
     const tcr::ItemGeo g = contiguous_item(p, blockIdx.x);
     if (!tcr::item_ok(g)) {

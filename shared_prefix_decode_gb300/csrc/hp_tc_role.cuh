@@ -104,7 +104,6 @@ struct Args {
     float scale_log2;  // > 0
     const void *map_o;  // partial O rows [rows][D] bf16: box 64 columns x 128 rows, 128-byte swizzle
     float *part_lse;
-    int wait_stores;    // the storing thread waits until the stores are performed (not only read)
 };
 
 __device__ __forceinline__ uint32_t bar_at(const Ctx &c, int i) { return c.bar0 + 8u * (uint32_t)i; }
@@ -494,10 +493,7 @@ __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, con
         for (int bx = 0; bx < D / 64; ++bx)
             tma_store_2d(a.map_o, smem_u32(stg + bx * L::kOBox), bx * 64, g.part_row + mb * 128);
         bulk_commit_group();
-        if (a.wait_stores)
-            bulk_wait_all();
-        else
-            bulk_wait_read_all();
+        bulk_wait_read_all();
     }
 }
 
