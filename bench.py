@@ -371,7 +371,7 @@ def main():
     tc_bytes = statistics.mean(level_bytes(s["wl"], True) for s in sets)
     small_bytes = statistics.mean(level_bytes(s["wl"], False) for s in sets)
     merge_bytes = statistics.mean(
-        s["plan"].info.n_part_rows * (s["wl"].d + 1) * 4 + s["wl"].B * s["wl"].Hq * (s["wl"].d * 2 + 4)
+        s["plan"].info.n_part_rows * (s["wl"].d * 2 + 4) + s["wl"].B * s["wl"].Hq * (s["wl"].d * 2 + 4)
         for s in sets)
     kb = {"cascade": tc_bytes + small_bytes, "merge": merge_bytes}
     kname = {"cascade": "hp_cascade_kernel", "merge": "hp_merge_kernel"}
