@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeP
     o.out = static_cast<uint8_t *>(p.out) + ((int64_t)L.b * p.o_sb + (int64_t)h * p.o_sh) * esz;
     o.out_f32 = p.out_f32;
     o.lse = p.lse != nullptr ? p.lse + (int64_t)L.b * p.lse_sb + h : nullptr;
-    mrg::merge_row<VPT * 32, 2>(p.part_o, p.part_lse, L.n, pr_a, pr_b, [&](int e) { return part_row(p, L, e); }, lane, o);
+    mrg::merge_row<VPT * 32, 8>(p.part_o, p.part_lse, L.n, pr_a, pr_b, [&p, L](int e) { return part_row(p, L, e); }, lane, o);
 }
 
 // Two-state merge of arbitrary d: one warp per row.

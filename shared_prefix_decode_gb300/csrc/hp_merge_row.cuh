@@ -35,24 +35,35 @@ struct RowOut {
 
 // One warp merges the n parts of a row.  Lane l holds the partial rows of
 // parts l and l + 32 in pr_a / pr_b; far(e) gives the row of part e >= 64.
-// Load instructions, not bytes, bound this code (each costs the SM about as
-// much whatever its width), so:
-//   1. lane e loads the LSE of part e (one instruction per 32 parts); the
-//      max and the denominator are warp reductions;
-//   2. O rows are read 16 bytes (8 columns) per lane, 32 / (D / 8) parts per
-//      instruction, each lane weighting its own part; the part groups are
-//      summed by shuffles at the end.
-// The sums run over the parts in a fixed lane order, so the result is
-// deterministic.
+// Load instructions and round trips, not bytes, bound this code, so the
+// first kFirst = kUnroll * 32 / (D / 8) parts are fetched in one round:
+//   - lane e loads the LSE of part e (one instruction per 32 parts);
+//   - the O rows are read 16 bytes (8 columns) per lane, 32 / (D / 8) parts
+//     per instruction, each lane holding its own part's slice;
+// then the max and the denominator are warp reductions and each lane weights
+// its part; the part groups are summed by shuffles at the end.  Further
+// parts (rows with more than kFirst) take further rounds.  The sums run over
+// the parts in a fixed lane order, so the result is deterministic.
 template <int D, int kUnroll, class Far>
 __device__ __forceinline__ void merge_row(const uint16_t *part_o, const float *part_lse, int n, int pr_a, int pr_b,
                                           const Far &far, int lane, const RowOut &o)
 {
     constexpr int kLpp = D / 8;      // lanes per part row (8 bf16 columns each)
     constexpr int kPpi = 32 / kLpp;  // parts per load instruction
-    // 1. LSEs, max, weights of the first 64 parts, denominator
+    const int sub = lane / kLpp;     // which part of an instruction's group
+    const int col = (lane % kLpp) * 8;
+    // one round: every LSE of the first 64 parts and the O slices of the
+    // first kUnroll * kPpi parts
     const float la = lane < n ? __ldcg(part_lse + pr_a) : -INFINITY;
     const float lb = lane + 32 < n ? __ldcg(part_lse + pr_b) : -INFINITY;
+    uint4 x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int e = u * kPpi + sub;
+        const int pr = __shfl_sync(0xffffffffu, e < 32 ? pr_a : pr_b, e & 31);
+        x[u] = e < n ? __ldcg(reinterpret_cast<const uint4 *>(part_o + (size_t)pr * D + col))
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
     float M = fmaxf(la, lb);
     for (int e = lane + 64; e < n; e += 32)
         M = fmaxf(M, __ldcg(part_lse + far(e)));
@@ -67,41 +78,38 @@ __device__ __forceinline__ void merge_row(const uint16_t *part_o, const float *p
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         den += __shfl_xor_sync(0xffffffffu, den, off);
-    // 2. weighted O rows
-    const int sub = lane / kLpp;            // which part of an instruction's group
-    const int col = (lane % kLpp) * 8;      // this lane's 8 columns
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         acc[i] = 0.f;
-    for (int e0 = 0; e0 < n; e0 += kPpi * kUnroll) {
-        uint4 x[kUnroll];
-        float w[kUnroll];
+    auto add = [&](const uint4 &xv, float w) {
+        acc[0] = fmaf(w, bf16lo_to_f32(xv.x), acc[0]);
+        acc[1] = fmaf(w, bf16hi_to_f32(xv.x), acc[1]);
+        acc[2] = fmaf(w, bf16lo_to_f32(xv.y), acc[2]);
+        acc[3] = fmaf(w, bf16hi_to_f32(xv.y), acc[3]);
+        acc[4] = fmaf(w, bf16lo_to_f32(xv.z), acc[4]);
+        acc[5] = fmaf(w, bf16hi_to_f32(xv.z), acc[5]);
+        acc[6] = fmaf(w, bf16lo_to_f32(xv.w), acc[6]);
+        acc[7] = fmaf(w, bf16hi_to_f32(xv.w), acc[7]);
+    };
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int e = e0 + u * kPpi + sub;
-            const int src = e & 31;
-            int pr = __shfl_sync(0xffffffffu, e < 32 ? pr_a : pr_b, src);
-            w[u] = __shfl_sync(0xffffffffu, e < 32 ? wa : wb, src);
-            x[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (e < n) {
-                if (e >= 64) {
-                    pr = far(e);
-                    w[u] = fast_exp2((__ldcg(part_lse + pr) - Ms) * kLog2e);
-                }
-                x[u] = __ldcg(reinterpret_cast<const uint4 *>(part_o + (size_t)pr * D + col));
-            } else {
-                w[u] = 0.f;
+    for (int u = 0; u < kUnroll; ++u) {
+        const int e = u * kPpi + sub;
+        const float w = __shfl_sync(0xffffffffu, e < 32 ? wa : wb, e & 31);
+        add(x[u], e < n ? w : 0.f);
+    }
+    // rows with more parts: one more round per kPpi parts
+    for (int e0 = kUnroll * kPpi; e0 < n; e0 += kPpi) {
+        const int e = e0 + sub;
+        const int src = e & 31;
+        int pr = __shfl_sync(0xffffffffu, e < 32 ? pr_a : pr_b, src);
+        float w = __shfl_sync(0xffffffffu, e < 32 ? wa : wb, src);
+        if (e < n) {
+            if (e >= 64) {
+                pr = far(e);
+                w = fast_exp2((__ldcg(part_lse + pr) - Ms) * kLog2e);
             }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc[2 * j] = fmaf(w[u], bf16lo_to_f32(xv[j]), acc[2 * j]);
-                acc[2 * j + 1] = fmaf(w[u], bf16hi_to_f32(xv[j]), acc[2 * j + 1]);
-            }
+            add(__ldcg(reinterpret_cast<const uint4 *>(part_o + (size_t)pr * D + col)), w);
         }
     }
 #pragma unroll
