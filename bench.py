@@ -12,11 +12,15 @@ Metric: microseconds per step and effective KV TB/s = unique KV bytes (each
 stored token once) / step time; also as a fraction of the roofline
 max(prefix FLOPs / bf16 peak, unique KV bytes / HBM peak).
 
-Timing: inputs resident in HBM; the step is a CUDA graph; R distinct input
-sets (own pools, tables, q and plan each) are rotated so that R x working set
-exceeds 3x the L2 size read at run time, which keeps every step's KV cold in
-L2; the sets share one workspace (partial states), as a decode loop reuses one.  CUDA events on the launching stream, W warm-up steps, exactly K timed
-steps, barrier + synchronize on both sides, max over ranks.
+Timing: inputs resident in HBM; R distinct input sets (own pools, tables, q
+and plan each) are rotated so that R x working set exceeds 3x the L2 size
+read at run time, which keeps every step's KV cold in L2; the sets share one
+workspace (partial states), as a decode loop reuses one.  One CUDA graph
+holds R consecutive steps, one per input set, as a decode loop captures its
+whole forward pass (so steps follow one another kernel to kernel, not graph
+launch to graph launch); a remainder of K mod R steps replays one-step
+graphs.  CUDA events on the launching stream, W warm-up steps, exactly K
+timed steps, barrier + synchronize on both sides, max over ranks.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hp|reference]
 Prints one JSON line (rank 0).
@@ -49,6 +53,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["hp", "reference"], default="hp")
     ap.add_argument("--config", default="llama3_8b")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: enough for 3x L2)")
+    ap.add_argument("--graph-steps", type=int, default=0,
+                    help="steps per CUDA graph: 0 = one per input set, 1 = one graph per step")
     ap.add_argument("--no-naive", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -250,6 +256,7 @@ def main():
         sets.append({"wl": wl, "wg": wg, "plan": plan, "out": out, "lse": lse})
     l2_note = (f"rotating {R} input sets, {R * set_bytes / 1e6:.0f} MB >= 3x L2 ({l2 / 2**20:.0f} MiB); "
                f"no flush")
+    gsteps = R if args.graph_steps <= 0 else min(args.graph_steps, R)
     # one workspace for every input set, as a decode loop reuses one buffer
     ws_shared = hb.alloc_workspace(max(s["plan"].info.ws_bytes for s in sets), dev)
     for s in sets:
@@ -277,7 +284,17 @@ def main():
             fn()
         return g
 
-    graphs = [capture(lambda s=s: step(s, stream)) for s in sets]
+    def capture_runs(fn, items):
+        """One-step graphs and, when gsteps > 1, graphs of gsteps consecutive
+        steps (items in rotation order)."""
+        singles = [capture(lambda it=it: fn(it)) for it in items]
+        runs = []
+        if gsteps > 1:
+            for k in range(0, len(items) - gsteps + 1, gsteps):
+                runs.append(capture(lambda k=k: [fn(it) for it in items[k:k + gsteps]]))
+        return singles, runs
+
+    graphs = capture_runs(lambda s: step(s, stream), sets)
     torch.cuda.synchronize(dev)
 
     # parity spot check on rank 0 (oracle on a few rows of set 0)
@@ -298,9 +315,22 @@ def main():
         if dist is not None:
             dist.barrier()
 
-    def timed(graph_list, steps, warmup):
-        for i in range(warmup):
-            graph_list[i % len(graph_list)].replay()
+    def replay(graph_runs, n):
+        """Replays exactly n steps in rotation order: whole multi-step graphs
+        where they fit, one-step graphs for the rest."""
+        singles, runs = graph_runs
+        i = 0
+        while i < n:
+            k = i % len(singles)
+            if runs and k % gsteps == 0 and k // gsteps < len(runs) and n - i >= gsteps:
+                runs[k // gsteps].replay()
+                i += gsteps
+            else:
+                singles[k].replay()
+                i += 1
+
+    def timed(graph_runs, steps, warmup):
+        replay(graph_runs, warmup)
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
@@ -309,8 +339,7 @@ def main():
         t_wall0 = time.time()
         e0.record(stream)
         with torch.cuda.stream(stream):
-            for i in range(steps):
-                graph_list[i % len(graph_list)].replay()
+            replay(graph_runs, steps)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         t_wall1 = time.time()
@@ -399,7 +428,7 @@ def main():
         s["o_host"].copy_(s["out"], non_blocking=True)
         s["l_host"].copy_(s["lse"], non_blocking=True)
 
-    e2e_graphs = [capture(lambda s=s: e2e_step(s)) for s in sets]
+    e2e_graphs = capture_runs(e2e_step, sets)
     e2e_steps = args.steps
     ms_e2e, _, _ = timed(e2e_graphs, e2e_steps, min(args.warmup, 50))
     us_e2e = ms_e2e * 1e3 / e2e_steps
@@ -427,7 +456,7 @@ def main():
             for n in nsets:
                 nstep(n)
         torch.cuda.synchronize(dev)
-        ngraphs = [capture(lambda n=n: nstep(n)) for n in nsets]
+        ngraphs = capture_runs(nstep, nsets)
         nk = max(R, min(args.steps, 2000))
         ms_n, _, _ = timed(ngraphs, nk, min(args.warmup, 20))
         naive = {"us_per_step": ms_n * 1e3 / nk, "steps": nk,
@@ -455,7 +484,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": us_step / 1e3, "us_per_step": us_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(wl0, l2_note),
+            "data": "synthetic", "config": dict(workload_config(wl0, l2_note), graph_steps=gsteps),
             "roofline_step": {"bound": "hbm" if t_bytes >= t_flops else "tensor", "roofline_us": roof_us,
                               "frac": roof_us / us_step, "t_bytes_us": t_bytes * 1e6, "t_flops_us": t_flops * 1e6,
                               "unique_kv_bytes": bytes_per_step, "prefix_flops": flops_per_step,

@@ -170,6 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tc.tmem_slot;
+    // This grid may start before the kernel ahead of it in the stream has
+    // finished (programmatic dependent launch).  Only the set-up above and
+    // the record load (plan memory, written by uploads alone) come before
+    // this point; q, the pools and the workspace are touched after it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // the record: its tag must match the launch's, its contents its size
     bool good = mbar_wait(rec_bar, 0u, p.status, tc.abort);
@@ -261,8 +266,20 @@ cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
             return cudaErrorInvalidConfiguration;  // the register split assumes this allocation
         configured = true;
     }
-    hp_cascade_kernel<D><<<grid, kThreads, bytes, s>>>(p);
-    return cudaGetLastError();
+    // launched as a programmatic dependent: the CTAs may set up (barriers,
+    // TMEM, the record) while the previous kernel in the stream drains; the
+    // kernel waits for that kernel to complete before it reads its inputs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, hp_cascade_kernel<D>, p);
 }
 
 }  // namespace

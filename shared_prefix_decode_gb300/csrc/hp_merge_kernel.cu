@@ -49,6 +49,10 @@ __device__ __forceinline__ int part_row(const MergeParams &p, const PartList &L,
 template <int VPT>  // values per lane: d / 32
 __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeParams p)
 {
+    // a following cascade launch may start its set-up on the SMs this grid
+    // frees; it waits for this grid to complete before it touches memory
+    // this kernel reads or writes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * kMergeWarps + warp;
     const int64_t n_rows = (int64_t)p.B * p.Hq;
