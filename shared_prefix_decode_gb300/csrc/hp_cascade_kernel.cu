@@ -149,8 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
         *sc.abort = 0;
         fence_mbar_init();
         mbar_arrive_expect_tx(rec_bar, (uint32_t)p.rec_stride);
-        bulk_load(tc.sbase + FL::kRec, p.plan + kPlanRecOff + (size_t)blockIdx.x * p.rec_stride,
-                  (uint32_t)p.rec_stride, rec_bar);
+        // evict_last: the plan is re-read every step, the pools stream through
+        bulk_load_h(tc.sbase + FL::kRec, p.plan + kPlanRecOff + (size_t)blockIdx.x * p.rec_stride,
+                    (uint32_t)p.rec_stride, rec_bar, l2_evict_last());
     } else if (tid == 32) {
         prefetch_tensormap(&p.q_tc);
         prefetch_tensormap(&p.o_tc);

@@ -152,8 +152,8 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
             if (lane < 2 * kHalves) {
                 const int h = lane % kHalves;
                 const bool is_v = lane >= kHalves;
-                tma_load_4d(c.sbase + st * L::kStage + (is_v ? L::kChunk : 0) + h * L::kHalf,
-                            is_v ? d.map_v : d.map_k, bar, h * 64, t % d.ps, d.kvh0, page);
+                tma_load_4d_h(c.sbase + st * L::kStage + (is_v ? L::kChunk : 0) + h * L::kHalf,
+                              is_v ? d.map_v : d.map_k, bar, h * 64, t % d.ps, d.kvh0, page, l2_evict_first());
             } else if (ch == 0 && qslot && lane < 3 * kHalves) {
                 const int h = lane - 2 * kHalves;
                 tma_load_3d(c.sbase + st * L::kStage + 2 * L::kChunk + h * L::kQHalf, a.map_q, bar, h * 64,

@@ -167,10 +167,11 @@ __device__ __forceinline__ void issue_tile(const Ctx &c, const ItemGeo &g, const
                     page = g.num_pages;
                 }
             }
-            tma_load_4d(dst + h * Layout<D>::kRegion + bx * g.box * 128, map, bar, h * 64, t % g.ps, g.kvh, page);
+            tma_load_4d_h(dst + h * Layout<D>::kRegion + bx * g.box * 128, map, bar, h * 64, t % g.ps, g.kvh, page,
+                          l2_evict_first());
         }
     } else if (lane < kHalves) {
-        tma_load_3d(dst + lane * Layout<D>::kRegion, map, bar, lane * 64, g.kvh, kt0);
+        tma_load_3d_h(dst + lane * Layout<D>::kRegion, map, bar, lane * 64, g.kvh, kt0, l2_evict_first());
     }
 }
 
