@@ -251,10 +251,12 @@ bool lpt(std::vector<Job> jobs, int c0, int c1, std::vector<double> &load, std::
 }
 
 // Schedule of the fused kernel's items over `grid` CTAs: CTAs [0, n_tc_ctas)
-// take the tensor-core items, the others the paged items (n_tc_ctas = grid:
-// every CTA may take both, tensor-core items first).  Returns the modelled
-// makespan, or a negative value when the records cannot hold the items.
-double schedule(HostPlan &P, int grid, int n_tc_ctas, int d, const CostModel &cm)
+// take the tensor-core items, the others the paged items -- or, `mixed`,
+// every CTA the paged items once its tensor-core items are done (n_tc_ctas =
+// grid: every CTA may take both, tensor-core items first).  Returns the
+// modelled makespan, or a negative value when the records cannot hold the
+// items.
+double schedule(HostPlan &P, int grid, int n_tc_ctas, bool mixed, int d, const CostModel &cm)
 {
     std::vector<Job> tcj, smj;
     for (size_t i = 0; i < P.tc.size(); ++i) {
@@ -279,7 +281,7 @@ double schedule(HostPlan &P, int grid, int n_tc_ctas, int d, const CostModel &cm
         ok = lpt(all, 0, grid, load, used, P.cta_tc, P.cta_small, cm.sm_start);
     } else {
         ok = lpt(tcj, 0, n_tc_ctas, load, used, P.cta_tc, P.cta_small, cm.sm_start) &&
-             lpt(smj, n_tc_ctas, grid, load, used, P.cta_tc, P.cta_small, cm.sm_start);
+             lpt(smj, mixed ? 0 : n_tc_ctas, grid, load, used, P.cta_tc, P.cta_small, cm.sm_start);
     }
     if (!ok)
         return -1.0;
@@ -519,18 +521,21 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
         small_split = kChunk * std::max<int64_t>(2, ceil_div(small_chunks, 3 * (int64_t)n_sm));
     };
     int best_k = sms;
+    bool best_mixed = false;
     if (tc_tiles > 0 && small_chunks > 0 && sms > 1) {
         double best = -1.0;
-        for (int k = 1; k < sms; ++k) {
-            int64_t ts, ss;
-            splits_for(k, ts, ss);
-            make_items(d, G, nh, ts, ss, level_page_off, P, nullptr);
-            const double t = schedule(P, sms, k, d->d, cm);
-            if (t >= 0.0 && (best < 0.0 || t < best)) {
-                best = t;
-                best_k = k;
+        for (int mixed = 0; mixed < 2; ++mixed)
+            for (int k = 1; k < sms; ++k) {
+                int64_t ts, ss;
+                splits_for(k, ts, ss);
+                make_items(d, G, nh, ts, ss, level_page_off, P, nullptr);
+                const double t = schedule(P, sms, k, mixed != 0, d->d, cm);
+                if (t >= 0.0 && (best < 0.0 || t < best)) {
+                    best = t;
+                    best_k = k;
+                    best_mixed = mixed != 0;
+                }
             }
-        }
     }
     int64_t tc_split, small_split;
     splits_for(best_k, tc_split, small_split);
@@ -556,7 +561,7 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     H.n_tc = (int32_t)P.tc.size();
     H.n_small = (int32_t)P.small.size();
     H.grid = sms;
-    if (schedule(P, sms, best_k, d->d, cm) < 0.0)
+    if (schedule(P, sms, best_k, best_mixed, d->d, cm) < 0.0)
         return HP_ERR_UNSUPPORTED;  // the step's page lists exceed what the CTAs' records hold
     build_records(P);
     H.n_part_rows = (int32_t)part;
