@@ -47,7 +47,7 @@ __device__ __forceinline__ int part_row(const MergeParams &p, const PartList &L,
 }
 
 template <int VPT>  // values per lane: d / 32
-__global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeParams p)
+__global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const __grid_constant__ MergeParams p)
 {
     // a following cascade launch may start its set-up on the SMs this grid
     // frees; it waits for this grid to complete before it touches memory
@@ -99,7 +99,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const MergeP
     o.out = static_cast<uint8_t *>(p.out) + ((int64_t)L.b * p.o_sb + (int64_t)h * p.o_sh) * esz;
     o.out_f32 = p.out_f32;
     o.lse = p.lse != nullptr ? p.lse + (int64_t)L.b * p.lse_sb + h : nullptr;
-    mrg::merge_row<VPT * 32, 8>(p.part_o, p.part_lse, L.n, pr_a, pr_b, [&p, L](int e) { return part_row(p, L, e); }, lane, o);
+    if (L.trow != nullptr) {
+        // parts past the first 64: straight from the table row
+        const int32_t *trow = L.trow;
+        const int g = L.g;
+        mrg::merge_row<VPT * 32, 8>(p.part_o, p.part_lse, L.n, pr_a, pr_b,
+                                    [trow, g](int e) { return __ldg(trow + 1 + e) + g; }, lane, o);
+    } else {
+        mrg::merge_row<VPT * 32, 8>(p.part_o, p.part_lse, L.n, pr_a, pr_b,
+                                    [&p, L](int e) { return part_row(p, L, e); }, lane, o);
+    }
 }
 
 // Two-state merge of arbitrary d: one warp per row.
