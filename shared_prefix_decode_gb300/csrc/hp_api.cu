@@ -210,14 +210,19 @@ int64_t item_pages(const WorkItem &w, int ps) { return (int64_t)(w.k1 - 1) / ps 
 // and exp2 bound, proportional to d); a CTA with paged items waits for its
 // first chunks, then each item streams its KV.
 struct CostModel {
-    double cta = 1500, tc_item = 6000, tc_tile = 2200, sm_start = 1000, sm_item = 200, sm_bytes_per_ns = 60;
-    double tc(const WorkItem &w, int d) const
+    // ns; a tensor-core tile costs tc_tile with two 128-row blocks, tc_tile1
+    // with one (timelines: about 2.1-2.5 us and 1.85 us at d = 128)
+    double cta = 1500, tc_item = 6000, tc_tile = 2300, tc_tile1 = 1850, sm_start = 1000, sm_item = 200,
+           sm_bytes_per_ns = 60;
+    double tc(const WorkItem &w, int G, int d) const
     {
-        return tc_item + tc_tile * (double)ceil_div(w.k1 - w.k0, kTcTile) * d / 128.0;
+        const bool two = w.n_seq > kTcTile / G;
+        return tc_item + (two ? tc_tile : tc_tile1) * (double)ceil_div(w.k1 - w.k0, kTcTile) * d / 128.0;
     }
+    // a paged item loads its keys and values once for all its sequences
     double small(const WorkItem &w, int d, int nh) const
     {
-        return sm_item + (double)(w.k1 - w.k0) * nh * w.n_seq * d * 4 / sm_bytes_per_ns;
+        return sm_item + (double)(w.k1 - w.k0) * nh * d * 4 / sm_bytes_per_ns;
     }
 };
 
@@ -261,7 +266,7 @@ double schedule(HostPlan &P, int grid, int n_tc_ctas, bool mixed, int d, const C
     std::vector<Job> tcj, smj;
     for (size_t i = 0; i < P.tc.size(); ++i) {
         const WorkItem &w = P.tc[i];
-        tcj.push_back({cm.tc(w, d), (int32_t)i, true,
+        tcj.push_back({cm.tc(w, P.hdr.G, d), (int32_t)i, true,
                        (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
     }
     const int nh = P.hdr.small_nh;

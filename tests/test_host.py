@@ -107,6 +107,17 @@ def test_plan_stats_configs(name):
         assert st[0] == 0
 
 
+def test_plan_spreads_shared_nodes_of_narrow_groups():
+    """Two-level tree (G = 1): a level-2 node's 16 sequences share one paged
+    item, whose keys are loaded once -- its modelled cost must not scale with
+    the sequence count, or the planner piles the private suffixes onto a few
+    CTAs and gives the tensor-core items to a handful of CTAs (a step 3x the
+    roofline).  Every KV head's shared prefix then gets its own CTAs."""
+    wl = W.make_config("tree2", seed=0)
+    n_tc, n_small, _, _ = hb.hp_cascade_plan_stats(hb._levels_of(wl), wl.B, wl.Hq, wl.Hkv, wl.d, num_sms=152)
+    assert n_tc >= wl.Hkv
+
+
 def _desc_levels(nodes, ids, num_pages=8, ps=16, pool=None):
     pool = pool if pool is not None else _pool()
     return [(pool.data_ptr(), pool.data_ptr(), num_pages, ps, nodes, ids)]
