@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
             tc_fence_before();
             tcr::named_sync(0, kThreads);
         }
-        if (warp == 0)
+        // (a CTA without paged items skips the role: its code is not fetched
+        // at the end of the step's longest chain)
+        if (warp == 0 && n_small > 0)
             smr::producer<D, kNC, kSmallStages, kQRows>(sc, sa, RecordItems{&p, items + n_tc, pages}, n_small, lane);
         if (warp == 1) {
             tc_fence_after();
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
             tc_fence_before();
             tcr::named_sync(0, kThreads);
         }
-        if (warp - 4 < p.small_nh)
+        if (warp - 4 < p.small_nh && n_small > 0)
             smr::consumer<D, kNC, kSmallStages, kQRows>(sc, sa, warp - 4, lane);
     }
     __syncwarp();
