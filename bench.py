@@ -216,6 +216,25 @@ def load_traffic(kernel: str):
     return None
 
 
+# ------------------------------------------------------------ multi-rank
+# One independent replica per rank (the step needs no exchange): the job's
+# time is the slowest rank's, its throughput the units all ranks processed.
+def job_time_ms(local_ms: float, dist, device) -> float:
+    """Max over ranks of a timed region (ms); `dist` is None on one rank."""
+    if dist is None:
+        return local_ms
+    import torch
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tbs(world: int, bytes_per_step: float, us_step: float) -> float:
+    """Whole-job effective KV TB/s: every rank's replica moves bytes_per_step
+    per step of us_step microseconds."""
+    return world * bytes_per_step / (us_step * 1e-6) / 1e12
+
+
 # -------------------------------------------------------------------- main
 def main():
     args = parse_args()
@@ -344,11 +363,7 @@ def main():
         torch.cuda.synchronize(dev)
         t_wall1 = time.time()
         barrier()
-        ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = job_time_ms(e0.elapsed_time(e1), dist, dev)
         return ms, t_wall0, t_wall1
 
     clocks = ClockSampler(getattr(props, "uuid", "") and str(props.uuid))
@@ -361,7 +376,7 @@ def main():
     us_step = ms * 1e3 / args.steps
     bytes_per_step = statistics.mean(s["wl"].unique_kv_bytes() for s in sets)
     flops_per_step = statistics.mean(s["wl"].shared_flops() for s in sets)
-    value = world * bytes_per_step / (us_step * 1e-6) / 1e12
+    value = whole_job_tbs(world, bytes_per_step, us_step)
     t_bytes = bytes_per_step / (peaks["hbm_gbs"] * 1e9)
     t_flops = flops_per_step / (peaks["bf16_tflops"] * 1e12)
     roof_us = max(t_bytes, t_flops) * 1e6
@@ -432,7 +447,7 @@ def main():
     e2e_steps = args.steps
     ms_e2e, _, _ = timed(e2e_graphs, e2e_steps, min(args.warmup, 50))
     us_e2e = ms_e2e * 1e3 / e2e_steps
-    e2e = {"value": world * bytes_per_step / (us_e2e * 1e-6) / 1e12, "unit": "TB/s", "us_per_step": us_e2e,
+    e2e = {"value": whole_job_tbs(world, bytes_per_step, us_e2e), "unit": "TB/s", "us_per_step": us_e2e,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "path": "pinned host q -> device, hp_cascade_decode, device O and LSE -> pinned host"}
 
