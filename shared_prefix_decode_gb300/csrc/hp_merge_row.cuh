@@ -1,6 +1,5 @@
 // hp_merge_row.cuh -- exact log-sum-exp merge of the partial attention
-// states of one output row by one warp.  Shared by the merge kernel and the
-// merge phase of the persistent cascade kernel.
+// states of one output row by one warp (the merge kernel's row body).
 //
 // Each output row (b, h) has a fixed, ordered list of partial states (O_i
 // normalised over its own keys, LSE_i); the merge is Hydragen Eq. 5 applied
@@ -11,8 +10,9 @@
 // only empty ones, gets O = 0 and LSE = -inf.  The parts are taken in their
 // fixed order, so the result is deterministic.
 //
-// Partial rows are read through L2 only (ld.global.cg): in the persistent
-// kernel they were written by other CTAs of the same launch.
+// Partial rows are read through L2 only (ld.global.cg): other SMs wrote them,
+// and an L1 line of the same workspace address could still hold an earlier
+// step's row.
 #pragma once
 
 #include <cuda_bf16.h>
