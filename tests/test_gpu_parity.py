@@ -153,6 +153,26 @@ def test_prefix_attn(Hq, Hkv, d, B, P):
     _check(out, lse, O, L, f"prefix {Hq}/{Hkv}/{d} B={B} P={P}")
 
 
+@pytest.mark.parametrize("d,Hq,Hkv,B", [(128, 4, 1, 40), (64, 8, 2, 20)])
+def test_prefix_attn_running_max_rescale(d, Hq, Hkv, B):
+    """Scores that grow by about 17 log2 units from one 128-key tile to the
+    next: every tile moves the reference max past the lazy-rescale threshold,
+    so O is rescaled in TMEM (by both column halves) at every tile."""
+    g = torch.Generator().manual_seed(11 + d)
+    P, scale = 1024, 1 / math.sqrt(d)
+    base = torch.randn(d, generator=g)
+    base = base / base.norm() * 4.0
+    q = (base + 0.1 * torch.randn(B, Hq, d, generator=g)).to(torch.bfloat16)
+    ramp = (torch.arange(P) // 128).float() * 12.0 / scale  # + 12 natural units per tile
+    k = torch.randn(P, Hkv, d, generator=g) + (ramp[:, None, None] * base / base.norm() ** 2)
+    k = k.to(torch.bfloat16)
+    v = torch.randn(P, Hkv, d, generator=g).to(torch.bfloat16)
+    O, L = oracle.prefix(q, k, v, scale)
+    out, lse = hb.hp_prefix_attn(q.to(DEV), k.to(DEV), v.to(DEV), scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _check(out, lse, O, L, f"rescale d={d}")
+
+
 def test_prefix_attn_row_window_and_strides():
     """rows [3, 3+20) only; K/V as a strided view of a wider [len][2*Hkv][d]."""
     g = torch.Generator().manual_seed(5)
