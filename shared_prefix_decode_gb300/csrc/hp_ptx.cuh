@@ -117,24 +117,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint3
                  : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *map, uint32_t bar, int c0,
-                                            int c1, int c2, int c3)
-{
-    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-                 "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-                 : "memory");
-}
-
-// Plain bulk copy global -> shared (both addresses 16-byte aligned, size a
-// multiple of 16), completing as transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // L2 eviction priorities for bulk and tensor loads.  Keys and values are read
 // once per step: evict_first keeps them from displacing what is reused from
 // step to step (q, the plan's records and merge table, the code).
@@ -166,7 +148,10 @@ __device__ __forceinline__ void tma_load_4d_h(uint32_t dst, const void *map, uin
                  "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(pol)
                  : "memory");
 }
-__device__ __forceinline__ void bulk_load_h(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint64_t pol)
+// Plain bulk copy global -> shared (both addresses 16-byte aligned, size a
+// multiple of 16), completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load_h(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                            uint64_t pol)
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
                  " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
