@@ -221,7 +221,10 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
 
 /* One cascade decode step: every sequence, every head, all levels, merged
  * (two launches: the persistent kernel of both passes, then the merge kernel
- * as its programmatic dependent).
+ * as its programmatic dependent).  The persistent kernel is itself launched
+ * as a programmatic dependent of the kernel before it in the stream: it sets
+ * up while that kernel drains and waits for it to complete before it reads
+ * q, the pools or the workspace.
  * q, out, lse as in the conventions above, for all B sequences; q strides
  * multiples of 8 elements, positive, and q 16-byte aligned (q is read by TMA).
  * ws: >= info->ws_bytes; one workspace serves one call at a time.
@@ -229,7 +232,11 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
  * wrote there in this process, and info must describe a plan no larger than
  * it (HP_ERR_ARG otherwise, before any launch); an info of another plan of the
  * same size is reported by the kernels through the status word.
- * No host synchronisation, no allocation; graph-capturable. */
+ * No host synchronisation, no allocation; graph-capturable.
+ * Failure detection tests only: with HP_TEST_WITHHOLD_TILE=1 in the
+ * environment, CTA 0 arms its first key tile's barrier but issues no copy;
+ * its bounded waits run out and the step reports HP_ERR_DEVICE_TIMEOUT
+ * through the status word (results of that step are not valid). */
 hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, const void *q,
                             int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,
                             int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,

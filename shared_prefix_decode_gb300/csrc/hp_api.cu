@@ -6,6 +6,7 @@
 #include <atomic>
 #include <chrono>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <numeric>
@@ -986,6 +987,12 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         cp.part_o = part_o;
         cp.part_lse = part_lse;
         cp.status = status_ptr(ws);
+        // Failure detection test hook: with HP_TEST_WITHHOLD_TILE=1 in the
+        // environment, CTA 0 arms its first K tile's barrier without issuing
+        // the copy; its bounded waits then run out, and the step reports
+        // HP_ERR_DEVICE_TIMEOUT through the status word.
+        const char *wh = std::getenv("HP_TEST_WITHHOLD_TILE");
+        cp.withhold = wh != nullptr && wh[0] == '1';
         if (launch_cascade(cp, info->grid, info->d, s) != cudaSuccess)
             return HP_ERR_CUDA;
     }

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
                 __syncwarp();
             }
             if (warp == 0 && tcr::item_ok(g))
-                tcr::producer_prologue<D>(tc, g, ta, lane);
+                tcr::producer_prologue<D>(tc, g, ta, lane, p.withhold != 0 && blockIdx.x == 0 && i == 0);
             if (i > 0) {
                 fence_proxy_async_smem();
                 tcr::named_sync(0, kThreads);

@@ -156,6 +156,7 @@ struct CascadeParams {
     uint16_t *part_o;      // bf16 (paged role; the tensor-core role stores through o_tc)
     float *part_lse;
     uint32_t *status;
+    int32_t withhold;      // failure detection tests: CTA 0 withholds its first K tile
 };
 
 // Merge kernel: combines the partial rows of each output row.

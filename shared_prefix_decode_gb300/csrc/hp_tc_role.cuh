@@ -180,9 +180,12 @@ __device__ __forceinline__ void issue_tile(const Ctx &c, const ItemGeo &g, const
 }
 
 // ---------------------------------------------------------------- phase A
-// Warp 0: the item's Q blocks and its first two tiles.
+// Warp 0: the item's Q blocks and its first two tiles.  `withhold` (failure
+// detection tests only): arm the first K tile's barrier for its bytes but
+// issue no copy, so the waits on it run out their time limit.
 template <int D>
-__device__ __forceinline__ void producer_prologue(const Ctx &c, const ItemGeo &g, const Args &a, int lane)
+__device__ __forceinline__ void producer_prologue(const Ctx &c, const ItemGeo &g, const Args &a, int lane,
+                                                  bool withhold = false)
 {
     using L = Layout<D>;
     constexpr int kHalves = D / 64;
@@ -198,7 +201,13 @@ __device__ __forceinline__ void producer_prologue(const Ctx &c, const ItemGeo &g
     const int n_tiles = n_tiles_of(g);
     const int pre = n_tiles < 2 ? n_tiles : 2;
     for (int j = 0; j < pre; ++j) {
-        issue_tile<D>(c, g, g.map_k, c.sbase + L::kK + j * L::kTile, bar_at(c, B_KFULL + j), j, lane);
+        if (withhold && j == 0) {
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar_at(c, B_KFULL + 0), L::kTile);
+            __syncwarp();
+        } else {
+            issue_tile<D>(c, g, g.map_k, c.sbase + L::kK + j * L::kTile, bar_at(c, B_KFULL + j), j, lane);
+        }
         issue_tile<D>(c, g, g.map_v, c.sbase + L::kV + j * L::kTile, bar_at(c, B_VFULL + j), j, lane);
     }
 }
