@@ -16,9 +16,9 @@ Timing: inputs resident in HBM; R distinct input sets (own pools, tables, q
 and plan each) are rotated so that R x working set exceeds 3x the L2 size
 read at run time, which keeps every step's KV cold in L2; the sets share one
 workspace (partial states), as a decode loop reuses one.  One CUDA graph
-holds R consecutive steps, one per input set, as a decode loop captures its
-whole forward pass (so steps follow one another kernel to kernel, not graph
-launch to graph launch); a remainder of K mod R steps replays one-step
+holds 4R consecutive steps (four rounds of the input sets), as a decode loop
+captures its whole forward pass (so steps follow one another kernel to
+kernel, not graph launch to graph launch); a remainder replays one-step
 graphs.  CUDA events on the launching stream, W warm-up steps, exactly K
 timed steps, barrier + synchronize on both sides, max over ranks.
 
@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--config", default="llama3_8b")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: enough for 3x L2)")
     ap.add_argument("--graph-steps", type=int, default=0,
-                    help="steps per CUDA graph: 0 = one per input set, 1 = one graph per step")
+                    help="steps per CUDA graph: 0 = four rounds of the input sets, 1 = one graph per step")
     ap.add_argument("--no-naive", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -278,7 +278,10 @@ def main():
         sets.append({"wl": wl, "wg": wg, "plan": plan, "out": out, "lse": lse, "res": res})
     l2_note = (f"rotating {R} input sets, {R * set_bytes / 1e6:.0f} MB >= 3x L2 ({l2 / 2**20:.0f} MiB); "
                f"no flush")
-    gsteps = R if args.graph_steps <= 0 else min(args.graph_steps, R)
+    # steps per graph: whole rounds of the input sets when at least one round
+    gsteps = 4 * R if args.graph_steps <= 0 else args.graph_steps
+    if gsteps > R:
+        gsteps = (gsteps + R - 1) // R * R
     # one workspace for every input set, as a decode loop reuses one buffer
     ws_shared = hb.alloc_workspace(max(s["plan"].info.ws_bytes for s in sets), dev)
     for s in sets:
@@ -308,12 +311,12 @@ def main():
 
     def capture_runs(fn, items):
         """One-step graphs and, when gsteps > 1, graphs of gsteps consecutive
-        steps (items in rotation order)."""
+        steps in rotation order: {first item: graph}."""
         singles = [capture(lambda it=it: fn(it)) for it in items]
-        runs = []
+        runs = {}
         if gsteps > 1:
-            for k in range(0, len(items) - gsteps + 1, gsteps):
-                runs.append(capture(lambda k=k: [fn(it) for it in items[k:k + gsteps]]))
+            for k in range(0, max(1, len(items) - gsteps + 1), gsteps):
+                runs[k] = capture(lambda k=k: [fn(items[(k + i) % len(items)]) for i in range(gsteps)])
         return singles, runs
 
     graphs = capture_runs(lambda s: step(s, stream), sets)
@@ -344,8 +347,8 @@ def main():
         i = 0
         while i < n:
             k = i % len(singles)
-            if runs and k % gsteps == 0 and k // gsteps < len(runs) and n - i >= gsteps:
-                runs[k // gsteps].replay()
+            if k in runs and n - i >= gsteps:
+                runs[k].replay()
                 i += gsteps
             else:
                 singles[k].replay()
