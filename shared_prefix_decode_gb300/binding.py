@@ -309,17 +309,31 @@ def hp_cascade_plan(levels, B, Hq, Hkv, d, device="cuda", stream=None, num_sms: 
     return CascadePlan(levels, B, Hq, Hkv, d, device=device, stream=stream, num_sms=num_sms)
 
 
+def _check_step_tensors(plan: CascadePlan, q: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+                        ws: torch.Tensor):
+    """The layouts hp_cascade_decode reads: q [B][Hq][d] bf16 and out
+    [B][Hq][d] with unit stride along d, lse [B][Hq] f32 with unit stride
+    along heads, all on the device; the workspace a byte tensor."""
+    _need(q.dim() == 3 and tuple(q.shape) == (plan.B, plan.Hq, plan.d), "q shape does not match the plan")
+    _need(q.dtype == torch.bfloat16 and q.is_cuda and q.stride(2) == 1, "q must be bf16 on the GPU, d contiguous")
+    _need(tuple(out.shape) == tuple(q.shape) and out.dtype in (torch.bfloat16, torch.float32) and out.is_cuda
+          and out.stride(2) == 1, "out must be [B][Hq][d] bf16 or f32 on the GPU, d contiguous")
+    _need(tuple(lse.shape) == (plan.B, plan.Hq) and lse.dtype == torch.float32 and lse.is_cuda
+          and lse.stride(1) == 1, "lse must be [B][Hq] f32 on the GPU, heads contiguous")
+    _need(ws is not None and ws.dtype == torch.uint8 and ws.is_cuda, "workspace must be a uint8 GPU tensor")
+
+
 def hp_cascade_decode(plan: CascadePlan, q: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
                       lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
                       out_dtype=torch.bfloat16, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     B, Hq, d = q.shape
-    _need((B, Hq, d) == (plan.B, plan.Hq, plan.d), "q shape does not match the plan")
     if out is None:
         out = torch.empty(B, Hq, d, dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
     if ws is None:
         ws = plan.ws
+    _check_step_tensors(plan, q, out, lse, ws)
     _check(library().hp_cascade_decode(
         _ptr(plan.plan), ctypes.byref(plan.info), _ptr(q), q.stride(0), q.stride(1), float(scale), _ptr(out),
         _dt(out.dtype), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(),
@@ -330,7 +344,9 @@ def hp_cascade_decode(plan: CascadePlan, q: torch.Tensor, scale: float, out: Opt
 def hp_cascade_decode_profiled(plan: CascadePlan, q: torch.Tensor, scale: float, out: torch.Tensor,
                                lse: torch.Tensor, events: Sequence[Optional[torch.cuda.Event]],
                                ws: Optional[torch.Tensor] = None, stream=None) -> None:
-    """hp_cascade_decode that records events[0..3] around its three kernels."""
+    """hp_cascade_decode that records events[0..2] around its two kernels
+    (events[3] is not used)."""
+    _check_step_tensors(plan, q, out, lse, plan.ws if ws is None else ws)
     ev = (c_vp * 4)(*[None if e is None else e.cuda_event for e in events])
     _check(library().hp_cascade_decode_profiled(
         _ptr(plan.plan), ctypes.byref(plan.info), _ptr(q), q.stride(0), q.stride(1), float(scale), _ptr(out),

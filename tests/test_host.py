@@ -160,3 +160,17 @@ def test_workspace_sizes_are_positive_and_rejections_are_zero():
     assert hb.suffix_workspace_bytes(4, 32, 96, 16, 16) == 0
     assert hb.prefix_workspace_bytes(64, 32, 8, 128, 4096) >= 256
     assert hb.prefix_workspace_bytes(64, 30, 8, 128, 4096) == 0
+
+
+def test_decode_binding_rejects_wrong_step_tensors():
+    """q, out, lse and the workspace are checked before the library is called:
+    dtype, shape, unit inner stride and device."""
+    class Plan:
+        B, Hq, d = 2, 4, 64
+
+    q = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(2, 4)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    for bad in (q.float(), q[:, :, ::2], q[:1], q):  # wrong dtype, stride, shape, host memory
+        with pytest.raises(hb.HpError):
+            hb._check_step_tensors(Plan, bad, q, lse, ws)
