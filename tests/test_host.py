@@ -172,5 +172,5 @@ def test_decode_binding_rejects_wrong_step_tensors():
     lse = torch.zeros(2, 4)
     ws = torch.zeros(256, dtype=torch.uint8)
     for bad in (q.float(), q[:, :, ::2], q[:1], q):  # wrong dtype, stride, shape, host memory
-        with pytest.raises(hb.HpError):
+        with pytest.raises(ValueError):
             hb._check_step_tensors(Plan, bad, q, lse, ws)
