@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
                 if (warp == 0)
                     tcr::producer_loop<D>(tc, g, lane);
                 else if (warp == 1 && lane == 0)
-                    tcr::mma_loop<D>(tc, g, tmem, i == 0);
+                    tcr::mma_loop<D>(tc, g, tmem);
             } else if (tid == 0) {
                 atomicOr(p.status, kStPlan);
             }
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
             if (i > 0)
                 tcr::named_sync(0, kThreads);
             if (tcr::item_ok(g))
-                tcr::softmax_loop<D>(tc, g, ta, tmem, warp, lane, tid, i == 0);
+                tcr::softmax_loop<D>(tc, g, ta, tmem, warp, lane, tid);
             // the epilogue wrote shared memory that TMA refills next
             fence_proxy_async_smem();
             tc_fence_before();

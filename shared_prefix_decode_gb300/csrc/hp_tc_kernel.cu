@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
             tcr::producer_prologue<D>(c, g, a, lane);
             tcr::producer_loop<D>(c, g, lane);
         } else if (warp == 1 && lane == 0) {
-            tcr::mma_loop<D>(c, g, tmem, true);
+            tcr::mma_loop<D>(c, g, tmem);
         }
         __syncwarp();
         tc_fence_before();
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
         }
     } else {
         setmaxnreg_inc<tcr::kRegsSoftmax>();
-        tcr::softmax_loop<D>(c, g, a, tmem, warp, lane, tid, true);
+        tcr::softmax_loop<D>(c, g, a, tmem, warp, lane, tid);
         tc_fence_before();
         tcr::named_sync(0, tcr::kThreads);
     }
