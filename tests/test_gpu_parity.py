@@ -429,3 +429,35 @@ def test_cascade_device_timeout_is_reported_and_the_context_stays_usable(monkeyp
     _status_ok(plan.ws)
     O, L = oracle.cascade(wl)
     _check(out, lse, O, L, "after a device timeout")
+
+
+def _random_tree(seed):
+    """A random cascade: 1-3 shared levels, each a random partition of the
+    sequences into contiguous nodes (lengths 0..300, some single-sequence),
+    private suffixes 0..100, random GQA group size, head dim and page size."""
+    rng = np.random.default_rng(seed)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    ps = int(rng.choice([16, 32, 64]))
+    B = int(rng.integers(1, 41))
+    shared = []
+    for _ in range(int(rng.integers(1, 4))):
+        cuts = sorted(set(rng.integers(1, B, size=int(rng.integers(0, 4))).tolist())) if B > 1 else []
+        bounds = [0] + cuts + [B]
+        shared.append([(a, b, int(rng.integers(0, 301))) for a, b in zip(bounds[:-1], bounds[1:])])
+    return W.build_cascade(f"random{seed}", B=B, Hq=Hkv * G, Hkv=Hkv, d=d, page_size=ps, shared=shared,
+                           suffix_range=(0, 100), seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_cascade_random_trees(seed):
+    """Irregular trees through the whole path (planner, both roles, merge):
+    every output row against the oracle."""
+    wl = _random_tree(seed)
+    O, L = oracle.cascade(wl)
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    out, lse = plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
+    _status_ok(plan.ws)
+    _check(out, lse, O, L, f"random tree {seed}: B={wl.B} Hq={wl.Hq} Hkv={wl.Hkv} d={wl.d} ps={wl.page_size}")
