@@ -25,22 +25,20 @@
 //   warp 1      TMEM owner and MMA issuer (one thread):
 //               S_mb = Q_mb K^T (A, B from shared memory) into TMEM,
 //               O_mb += P_mb V   (A = P from TMEM, B = V from shared memory).
-//   warps 4-11  softmax, two warps per TMEM lane quarter, each taking one
-//               half of a row's columns; all eight work on block 0, then on
-//               block 1.  They read the scores from TMEM, exchange the
-//               halves' row maxima through shared memory, compute exp2 and
-//               the row sums, and write P (bf16) over the S columns.  They
-//               rescale O in TMEM only when the max grows by more than 2^8.
-//               Otherwise the reference max is kept, which is exact because
-//               the final O / l uses the same reference.  At the end they
-//               stage O / l (bf16) in shared memory as 128-row x 64-column
-//               boxes, and one thread writes them out with TMA tensor stores.
-//               The partial rows of a block are 128 reserved rows of the
-//               workspace.
+//   warps 4-7   softmax for block 0, warps 8-11 for block 1: read a 128-column
+//               score row from TMEM, max / exp2 / row sum, write P (bf16)
+//               over the S columns, rescale O in TMEM when the max grows by
+//               more than 2^8 (the reference max is kept otherwise; exact,
+//               since the final O / l uses the same reference), and at the end
+//               stage O / l (bf16) in shared memory as 128-row x 64-column boxes
+//               that one thread writes out with TMA tensor stores (the
+//               partial rows of a block are 128 reserved rows of the
+//               workspace).  The loops walk the row in 32-column chunks
+//               (short code: a cold instruction cache costs microseconds
+//               when HBM is saturated).
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
-// The two row blocks ping-pong: while the warps run one block's softmax, the
-// tensor cores compute the other's P V and next S.  S of tile j+1 is issued
-// right after P V of tile j.
+// The two row blocks ping-pong: S of block 1 is computed while block 0 runs
+// its softmax, and S of tile j+1 is issued right after P V of tile j.
 //
 // Register split: warpgroup 0 (producer, MMA, two idle warps) lowers its
 // count, the softmax warpgroups raise theirs; the caller issues setmaxnreg at
@@ -60,7 +58,6 @@ constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 136, kRegsSoftmax = 184;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax == kThreads * kRegsLaunch, "register split");
 constexpr float kTau = 8.0f;  // lazy rescale threshold, log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr int kSoftmaxBar = 1;  // named barrier of the 256 softmax threads
 
 template <int D>
 struct Layout {
@@ -70,8 +67,7 @@ struct Layout {
     static constexpr int kQ = 0;  // [mb][half] regions
     static constexpr int kK = kQ + 2 * kTile;
     static constexpr int kV = kK + 2 * kTile;
-    static constexpr int kXch = kV + 2 * kTile;  // softmax half-row exchange: maxima, then sums
-    static constexpr int kEnd = kXch + (4 + 2) * 2 * kTcTile * 4;  // O staging reuses K (block 0) and V (block 1)
+    static constexpr int kEnd = kV + 2 * kTile;  // O staging reuses K (block 0) and V (block 1)
     static constexpr int kOBox = 128 * 128;      // [128 rows][64 bf16], 128-byte swizzle
     static_assert(2 * kTile >= (D / 64) * kOBox, "O staging must fit one ring");
 };
@@ -139,7 +135,7 @@ __device__ __forceinline__ void init_barriers(const Ctx &c, bool reinit)
     for (int i = 0; i < B_COUNT; ++i) {
         if (reinit)
             mbar_inval(bar_at(c, i));
-        mbar_init(bar_at(c, i), (i == B_P || i == B_P + 1) ? 256u : 1u);
+        mbar_init(bar_at(c, i), (i == B_P || i == B_P + 1) ? 128u : 1u);
     }
     *c.abort = 0;
     fence_mbar_init();
@@ -317,223 +313,181 @@ __device__ __forceinline__ void mma_loop(const Ctx &c, const ItemGeo &g, uint32_
     mbar_wait_drain(bar_at(c, B_DRAIN), 0u);
 }
 
-// Warps 4-11, two per TMEM lane quarter: warp w takes rows 32 (w % 4) .. +31
-// of every block (TMEM lanes) and one half of the columns, hf = (w - 4) / 4:
-// score columns 64 hf .. +63 and O columns hf D/2 .. +D/2.  All eight warps
-// run block 0's softmax, then block 1's, so the tensor cores compute one
-// block's P V and next S while the warps work on the other, and each block's
-// softmax takes half the time it would on four warps.  The two warps of a
-// row combine their halves' maxima (and, at the end, their sums) through
-// shared memory.  Every warp passes the same named barriers whatever its
-// waits return (a failed wait only stops its work), so none is left behind.
-// (A dry pass of the body before the first tile, to have its instructions
-// cached when the scores land, measured 0.34 us slower per step.)
+// Warps 4-11 (mb = 0 for warps 4-7, 1 for 8-11).  Each thread owns one row
+// of its block (its TMEM lane).
 template <int D>
 __device__ __forceinline__ void softmax_loop(const Ctx &c, const ItemGeo &g, const Args &a, uint32_t tmem,
                                              int warp, int lane, int tid)
 {
     using L = Layout<D>;
     constexpr int kHalves = D / 64;
-    constexpr int kOC = D / 2;  // O columns per warp
     const int rows_total = g.n_seq * a.G;
     const int rpb = g.spb * a.G;  // rows per block
     const int nmb = n_blocks_of(g);
     const int n_tiles = n_tiles_of(g);
-    const int hf = (warp - 4) >> 2;
-    const int rr = (warp & 3) * 32 + lane;  // row within a block == TMEM lane
+    const int mb = (warp - 4) >> 2;
+    const int rr = tid - 128 * (1 + mb);  // row within the block == TMEM lane
+    const int rows_here = min(rpb, rows_total - mb * rpb);
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    float *xmax = reinterpret_cast<float *>(c.smem + L::kXch);  // [4 uses][2 halves][128 rows]
-    float *xsum = xmax + 4 * 2 * kTcTile;                       // [2 blocks][2 halves][128 rows]
+    const uint32_t s_col = tl + mb * 128;
+    const uint32_t o_col = tl + 256 + mb * 128;
     const float cs = a.scale_log2;
     const uint64_t cs2 = f32x2_pack(cs, cs);
     auto wait_warp = [&](int b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar_at(c, b), parity, c.status, c.abort)) != 0;
     };
-    float m0 = -INFINITY, m1 = -INFINITY;  // reference max per block, log2 units
-    float l0 = 0.f, l1 = 0.f;              // this half's running sum per block
-    bool ok = true;
-    int use = 0;
-    uint32_t r[32], r2[32];
-    for (int j = 0; j < n_tiles; ++j) {
+    float m_run = -INFINITY;  // reference max, log2 units
+    float l_run = 0.f;
+    bool ok = mb < nmb;
+    uint32_t r[32];
+    for (int j = 0; ok && j < n_tiles; ++j) {
+        if (!(ok = wait_warp(B_S + mb, (uint32_t)j & 1u)))
+            break;
+        tc_fence_after();
         const int nvalid = min(kTcTile, g.k1 - (g.k0 + j * kTcTile));
+        // largest valid score (the scale is positive: the largest scaled
+        // score is the largest raw score times the scale)
+        float mx = -INFINITY;
 #pragma unroll 1
-        for (int mb = 0; mb < nmb; ++mb) {
-            if (ok)
-                ok = wait_warp(B_S + mb, (uint32_t)j & 1u);
-            tc_fence_after();
-            const uint32_t s_col = tl + mb * 128 + hf * 64;
-            float mx = -INFINITY;
-            if (ok) {
-                tmem_ld32(s_col, r);
-                tmem_ld32(s_col + 32, r2);
-                tmem_ld_wait();
-                if (nvalid < kTcTile) {
-                    // keys past the node score -inf: P = exp2(-inf) = 0
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        if (hf * 64 + i >= nvalid)
-                            r[i] = __float_as_uint(-INFINITY);
-                        if (hf * 64 + 32 + i >= nvalid)
-                            r2[i] = __float_as_uint(-INFINITY);
-                    }
-                }
-                // the scale is positive: the largest scaled score is the
-                // largest raw score times the scale
+        for (int cc = 0; cc < 4; ++cc) {
+            tmem_ld32(s_col + cc * 32, r);
+            tmem_ld_wait();
+            const int lim = nvalid - cc * 32;
+            if (lim >= 32) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 2)
                     mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-#pragma unroll
-                for (int i = 0; i < 32; i += 2)
-                    mx = fmax3(mx, __uint_as_float(r2[i]), __uint_as_float(r2[i + 1]));
-            }
-            float *xs = xmax + (use & 3) * 2 * kTcTile;
-            ++use;
-            xs[hf * kTcTile + rr] = mx;
-            named_sync(kSoftmaxBar, 256);
-            mx = fmaxf(mx, xs[(hf ^ 1) * kTcTile + rr]);
-            float m_run = mb ? m1 : m0, l_run = mb ? l1 : l0;
-            const float tmax = mx * cs;
-            const bool need = tmax > m_run + kTau;
-            const float alpha = need ? fast_exp2(m_run - tmax) : 1.f;
-            if (need) {
-                l_run *= alpha;
-                m_run = tmax;
-            }
-            if (ok) {
-                // P = exp2(s * c - m) as bf16 pairs over the score columns
-                // already read (this half's keys land in P columns
-                // 32 hf .. +31).  Pairs go through the packed f32x2 fma / add.
-                const float nm = -m_run;
-                const uint64_t nm2 = f32x2_pack(nm, nm);
-                uint64_t acc2 = f32x2_pack(0.f, 0.f);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float x0, x1;
-                    f32x2_unpack(
-                        f32x2_fma(f32x2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), cs2, nm2),
-                        x0, x1);
-                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                    acc2 = f32x2_add(acc2, f32x2_pack(p0, p1));
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tl + mb * 128 + hf * 32, pk);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float x0, x1;
-                    f32x2_unpack(
-                        f32x2_fma(f32x2_pack(__uint_as_float(r2[2 * i]), __uint_as_float(r2[2 * i + 1])), cs2, nm2),
-                        x0, x1);
-                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                    acc2 = f32x2_add(acc2, f32x2_pack(p0, p1));
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tl + mb * 128 + hf * 32 + 16, pk);
-                float lsum0, lsum1;
-                f32x2_unpack(acc2, lsum0, lsum1);
-                l_run += lsum0 + lsum1;
-            }
-            if (mb) {
-                m1 = m_run;
-                l1 = l_run;
             } else {
-                m0 = m_run;
-                l0 = l_run;
-            }
-            // O was accumulated against the old reference max: rescale this
-            // half of it once the previous P V has landed (rare: the max grew
-            // by more than 2^kTau)
-            if (ok && j > 0 && __any_sync(0xffffffffu, need)) {
-                ok = wait_warp(B_O + mb, (uint32_t)(j - 1) & 1u);
-                if (ok) {
-                    tc_fence_after();
-                    const uint32_t o_col = tl + 256 + mb * 128 + hf * kOC;
-#pragma unroll 1
-                    for (int cc = 0; cc < kOC / 32; ++cc) {
-                        tmem_ld32(o_col + cc * 32, r);
-                        tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(o_col + cc * 32, r);
-                    }
-                }
+                for (int i = 0; i < 32; ++i)
+                    mx = fmaxf(mx, i < lim ? __uint_as_float(r[i]) : -INFINITY);
             }
-            tmem_st_wait();
-            if (ok && mb == 0 && nvalid < kTcTile) {
-                // last, partial tile: rows past the node hold whatever the
-                // pool holds there; zero their V (this half's column halves)
-                // so 0 * garbage stays 0
-                const int st = j & 1;
-                ok = wait_warp(B_VFULL + st, (uint32_t)(j >> 1) & 1u);
-                if (ok && rr >= nvalid) {
-                    for (int h = hf; h < kHalves; h += 2) {
-                        uint4 *vrow =
-                            reinterpret_cast<uint4 *>(c.smem + L::kV + st * L::kTile + h * L::kRegion + rr * 128);
-#pragma unroll
-                        for (int qd = 0; qd < 8; ++qd)
-                            vrow[qd] = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-                fence_proxy_async_smem();
-            }
-            tc_fence_before();
-            if (ok)
-                mbar_arrive(bar_at(c, B_P + mb));
         }
-    }
-    // Epilogue, block by block: O / l into shared memory (block 0 over the K
-    // ring, block 1 over the V ring, both idle once the last P V has
-    // completed) as D/64 bf16 boxes of [128 rows][64 columns] in the 128-byte
-    // swizzled order the tensor map expects (conflict-free: 8 consecutive
-    // rows hit 8 distinct 16-byte slots); one thread stores a block's boxes
-    // to partial rows part_row + mb*128 .. +127 and waits until they have
-    // been read.
-    const bool storer = warp == 4 && lane == 0;
+        const float tmax = mx * cs;
+        const bool need = tmax > m_run + kTau;
+        const float alpha = need ? fast_exp2(m_run - tmax) : 1.f;
+        if (need) {
+            l_run *= alpha;
+            m_run = tmax;
+        }
+        // P = exp2(s * c - m) as bf16 pairs over the S columns (chunk cc's P
+        // lands in columns already read); invalid keys get P = 0.  Pairs of
+        // scores go through the packed f32x2 fma / add.
+        const float nm = -m_run;
+        const uint64_t nm2 = f32x2_pack(nm, nm);
+        uint64_t acc2 = f32x2_pack(0.f, 0.f);
 #pragma unroll 1
-    for (int mb = 0; mb < nmb; ++mb) {
-        if (ok)
-            ok = wait_warp(B_O + mb, (uint32_t)(n_tiles - 1) & 1u);
-        const float lh = mb ? l1 : l0;
-        xsum[(mb * 2 + hf) * kTcTile + rr] = lh;
-        named_sync(kSoftmaxBar, 256);
-        const float l_run = lh + xsum[(mb * 2 + (hf ^ 1)) * kTcTile + rr];
-        const float m_run = mb ? m1 : m0;
-        uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
-        if (ok) {
+        for (int cc = 0; cc < 4; ++cc) {
+            tmem_ld32(s_col + cc * 32, r);
+            tmem_ld_wait();
+            const int lim = nvalid - cc * 32;
+            uint32_t pk[16];
+            if (lim >= 32) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float x0, x1;
+                    f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                           cs2, nm2),
+                                 x0, x1);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    acc2 = f32x2_add(acc2, f32x2_pack(p0, p1));
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), cs, nm));
+                    float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), cs, nm));
+                    p0 = 2 * i < lim ? p0 : 0.f;
+                    p1 = 2 * i + 1 < lim ? p1 : 0.f;
+                    acc2 = f32x2_add(acc2, f32x2_pack(p0, p1));
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+            }
+            tmem_st16(s_col + cc * 16, pk);
+        }
+        float lsum0, lsum1;
+        f32x2_unpack(acc2, lsum0, lsum1);
+        const float lsum = lsum0 + lsum1;
+        l_run += lsum;
+        // O was accumulated against the old reference max: rescale it once
+        // the previous P V has landed (rare: the max grew by more than 2^kTau)
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+            if (!(ok = wait_warp(B_O + mb, (uint32_t)(j - 1) & 1u)))
+                break;
             tc_fence_after();
-            const float inv = 1.f / l_run;
-            const uint32_t o_col = tl + 256 + mb * 128 + hf * kOC;
 #pragma unroll 1
-            for (int cc = 0; cc < kOC / 32; ++cc) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 tmem_ld32(o_col + cc * 32, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {  // 16-byte piece: columns hf*kOC + cc*32 + 8i .. +7
-                    const int gp = (hf * kOC + cc * 32) / 8 + i;
-                    uint4 v;
-                    v.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv, __uint_as_float(r[8 * i + 1]) * inv);
-                    v.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv);
-                    v.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv);
-                    v.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv);
-                    *reinterpret_cast<uint4 *>(stg + (gp >> 3) * L::kOBox + rr * 128 + (((gp & 7) ^ (rr & 7)) << 4)) =
-                        v;
+                for (int i = 0; i < 32; ++i)
+                    r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                tmem_st32(o_col + cc * 32, r);
+            }
+        }
+        tmem_st_wait();
+        if (mb == 0 && nvalid < kTcTile) {
+            // last, partial tile: rows past the node hold whatever the pool
+            // holds there; zero their V so 0 * garbage stays 0
+            const int st = j & 1;
+            if (!(ok = wait_warp(B_VFULL + st, (uint32_t)(j >> 1) & 1u)))
+                break;
+            if (rr >= nvalid) {
+                for (int h = 0; h < kHalves; ++h) {
+                    uint4 *vrow = reinterpret_cast<uint4 *>(c.smem + L::kV + st * L::kTile + h * L::kRegion + rr * 128);
+#pragma unroll
+                    for (int qd = 0; qd < 8; ++qd)
+                        vrow[qd] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            if (hf == 0 && rr < min(rpb, rows_total - mb * rpb))
-                a.part_lse[g.part_row + mb * 128 + rr] = (m_run + fast_log2(l_run)) * kLn2;
             fence_proxy_async_smem();
         }
         tc_fence_before();
-        named_sync(kSoftmaxBar, 256);
-        if (ok && storer) {
-            for (int bx = 0; bx < D / 64; ++bx)
-                tma_store_2d(a.map_o, smem_u32(stg + bx * L::kOBox), bx * 64, g.part_row + mb * 128);
-            bulk_commit_group();
-        }
+        mbar_arrive(bar_at(c, B_P + mb));
     }
-    if (storer)
+    // Epilogue: O / l into shared memory (block 0 over the K ring, block 1
+    // over the V ring, both idle once the last P V has completed) as D/64
+    // bf16 boxes of [128 rows][64 columns] in the 128-byte swizzled order the
+    // tensor map expects (conflict-free: 8 consecutive rows hit 8 distinct
+    // 16-byte slots), then one thread of the block stores the boxes to
+    // partial rows part_row + mb*128 .. +127 and waits until they have been
+    // read.
+    const bool have = ok && mb < nmb;
+    uint8_t *stg = c.smem + (mb == 0 ? L::kK : L::kV);
+    if (have && wait_warp(B_O + mb, (uint32_t)(n_tiles - 1) & 1u)) {
+        tc_fence_after();
+        const float inv = 1.f / l_run;
+        uint32_t r2[32];
+#pragma unroll 1
+        for (int bx = 0; bx < D / 64; ++bx) {
+            tmem_ld32(o_col + bx * 64, r);
+            tmem_ld32(o_col + bx * 64 + 32, r2);
+            tmem_ld_wait();
+            uint8_t *row = stg + bx * L::kOBox + rr * 128;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {  // 16-byte piece i: columns bx*64 + 8i .. +7
+                const uint32_t *src = i < 4 ? &r[8 * i] : &r2[8 * (i - 4)];
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
+                v.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
+                v.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
+                v.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
+                *reinterpret_cast<uint4 *>(row + ((i ^ (rr & 7)) << 4)) = v;
+            }
+        }
+        if (rr < rows_here)
+            a.part_lse[g.part_row + mb * 128 + rr] = (m_run + fast_log2(l_run)) * kLn2;
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    named_sync(1 + mb, 128);
+    if (have && rr == 0) {
+        for (int bx = 0; bx < D / 64; ++bx)
+            tma_store_2d(a.map_o, smem_u32(stg + bx * L::kOBox), bx * 64, g.part_row + mb * 128);
+        bulk_commit_group();
         bulk_wait_read_all();
+    }
 }
 
 }  // namespace tcr

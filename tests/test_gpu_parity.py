@@ -157,7 +157,7 @@ def test_prefix_attn(Hq, Hkv, d, B, P):
 def test_prefix_attn_running_max_rescale(d, Hq, Hkv, B):
     """Scores that grow by about 17 log2 units from one 128-key tile to the
     next: every tile moves the reference max past the lazy-rescale threshold,
-    so O is rescaled in TMEM (by both column halves) at every tile."""
+    so O is rescaled in TMEM at every tile."""
     g = torch.Generator().manual_seed(11 + d)
     P, scale = 1024, 1 / math.sqrt(d)
     base = torch.randn(d, generator=g)
