@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--graph-steps", type=int, default=0,
                     help="steps per CUDA graph: 0 = four rounds of the input sets, 1 = one graph per step")
     ap.add_argument("--no-naive", action="store_true")
+    ap.add_argument("--loop-steps", type=int, default=64,
+                    help="decode-loop measurement: steps per input set in one graph (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -483,6 +485,93 @@ def main():
                            "re-read per sequence)",
                  "speedup_of_cascade": (ms_n / nk) / (ms / args.steps)}
 
+    # ------------------------------------------------------ decode loop
+    # The same workload as a decode loop: each step appends one token per
+    # sequence (hp_cascade_append_kv) and decodes over the grown suffixes
+    # (hp_cascade_decode_loop) with a plan built once.  One graph holds
+    # loop_steps steps of every input set in rotation, after resetting the
+    # suffix lengths; the pools are not reset (each replay rewrites the same
+    # slots).
+    loop = None
+    if args.loop_steps > 0:
+        from shared_prefix_decode_gb300.workloads import decode_tokens, with_suffix_capacity
+        T = args.loop_steps
+        lsets = []
+        for i, s in enumerate(sets):
+            cap = int(s["wl"].levels[-1].nodes[:, 2].max()) + T
+            host = with_suffix_capacity(s["wl"], cap, seed=1000 * rank + i)
+            lg = host.to(dev)
+            lp = hb.LoopPlan.from_workload(lg, cap)
+            lp.ws = ws_shared
+            toks = decode_tokens(host, T, seed=1000 * rank + i)
+            qs, ks, vs = (torch.stack([t[j] for t in toks]).to(dev) for j in range(3))
+            lsets.append({"wl": host, "wg": lg, "plan": lp, "n0": lp.suffix_len.clone(), "qs": qs, "ks": ks,
+                          "vs": vs, "out": s["out"], "lse": s["lse"]})
+
+        def loop_run():
+            for ls in lsets:
+                ls["plan"].suffix_len.copy_(ls["n0"], non_blocking=True)
+            for t in range(T):
+                for ls in lsets:
+                    hb.hp_cascade_append_kv(ls["plan"], ls["ks"][t], ls["vs"][t], stream=stream)
+                    hb.hp_cascade_decode_loop(ls["plan"], ls["qs"][t], ls["wl"].scale, out=ls["out"],
+                                              lse=ls["lse"], stream=stream)
+
+        with torch.cuda.stream(stream):
+            loop_run()
+        torch.cuda.synchronize(dev)
+        st = hb.hp_read_device_status(ws_shared)
+        if st != 0:
+            raise RuntimeError(f"decode loop: device status {hb.status_str(st)}")
+        g_loop = capture(loop_run)
+        n_loop = T * len(lsets)
+        reps = max(3, min(200, args.steps // n_loop))
+        for _ in range(2):
+            g_loop.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g_loop.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        st = hb.hp_read_device_status(ws_shared)
+        if st != 0:
+            raise RuntimeError(f"decode loop: device status {hb.status_str(st)}")
+        us_loop = job_time_ms(e0.elapsed_time(e1), dist, dev) * 1e3 / (reps * n_loop)
+
+        # the same steps without the appends, at the loop's mean suffix
+        # lengths (the slots hold tokens of the replays above)
+        def decode_only_run():
+            for ls in lsets:
+                ls["plan"].suffix_len.copy_(ls["n0"] + T // 2, non_blocking=True)
+            for t in range(T):
+                for ls in lsets:
+                    hb.hp_cascade_decode_loop(ls["plan"], ls["qs"][t], ls["wl"].scale, out=ls["out"],
+                                              lse=ls["lse"], stream=stream)
+
+        g_dec = capture(decode_only_run)
+        for _ in range(2):
+            g_dec.replay()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g_dec.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us_dec = job_time_ms(e0.elapsed_time(e1), dist, dev) * 1e3 / (reps * n_loop)
+        # keys grow by one token per sequence per step: mean over the loop
+        grow = lsets[0]["wl"].B * (T + 1) / 2 * wl0.Hkv * wl0.d * 4
+        loop_bytes = bytes_per_step + grow
+        loop = {"us_per_step": us_loop, "value": whole_job_tbs(world, loop_bytes, us_loop), "unit": "TB/s",
+                "steps_per_graph": n_loop, "graph_replays": reps, "loop_steps": T,
+                "kernels_per_step": 3, "mean_kv_bytes_per_step": loop_bytes,
+                "decode_only_us_per_step": us_dec,
+                "step": "hp_cascade_append_kv + hp_cascade_decode_loop (plan built once; suffix lengths on the "
+                        "device)"}
+
     # ---------------------------------------------------- cpu baseline
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -515,6 +604,7 @@ def main():
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": clock_summary,
             "naive": naive,
+            "decode_loop": loop,
             "parity_spot": parity,
             "plan": {"tc_items": info.n_tc_items, "small_items": info.n_small_items, "grid": info.grid,
                      "part_rows": info.n_part_rows},

@@ -255,6 +255,69 @@ hp_status hp_cascade_decode_profiled(const void *plan_dev, const hp_plan_info *i
                                      int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream,
                                      void *const *events);
 
+/* ---------------------------------------------------------------------------
+ * Decode loop: many steps over one tree whose private suffixes grow.
+ *
+ * Each decoding step appends one token per sequence to that sequence's
+ * private suffix, and the next step attends over it (Hydragen, "Inter-Sequence
+ * Batched Prefix Attention", on autoregressive decoding).  The shared nodes
+ * do not change.  Hydragen's suffix kernel accepts suffix lengths that change
+ * from step to step while the loop stays inside CUDA graphs ("Implementation
+ * Details", attention primitives).  ChunkAttention keeps the kernel context
+ * on the GPU and copies it again only when the tree's structure changes
+ * ("Context Generation and GPU-CPU Coordination", lazy context copy).
+ *
+ * Here a loop plan is built once with a capacity per suffix.  Each
+ * sequence's current suffix length lives in a device array,
+ * suffix_len[B] (int32).  hp_cascade_append_kv writes one token and
+ * increments the length; hp_cascade_decode_loop reads it.  Both are
+ * graph-capturable, so a whole multi-step loop can be one CUDA graph.
+ *
+ * The tree's last level must hold exactly one node per sequence, the node
+ * of sequence b covering only b: its suffix.  Its kv_len is the length at
+ * plan time.  Its page list must hold ceil(capacity / page_size) valid page
+ * ids, distinct from each other and from every page that another node of
+ * the same pools uses.  hp_cascade_append_kv writes into those pages.
+ * Hq / Hkv must be at most 16.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of the device plan buffer of a loop plan (host only, no CUDA calls
+ * when desc->num_sms > 0); 0 on an invalid descriptor or capacity.
+ * capacity: maximum suffix length, >= every suffix node's kv_len, >= 1. */
+size_t hp_cascade_loop_plan_bytes(const hp_tree_desc *desc, int32_t capacity);
+
+/* hp_cascade_plan for a decode loop: the same validation, work items and
+ * upload, plus the suffixes' page lists for hp_cascade_append_kv.  The
+ * suffix work items reach to `capacity`; at run time each one ends at the
+ * sequence's current length.  A loop plan is used only through
+ * hp_cascade_append_kv and hp_cascade_decode_loop (hp_cascade_decode returns
+ * HP_ERR_ARG on it).  Waits for the upload, like hp_cascade_plan. */
+hp_status hp_cascade_loop_plan(const hp_tree_desc *desc, int32_t capacity, void *plan_dev,
+                               size_t plan_bytes, hp_plan_info *info, hp_stream_t stream);
+
+/* Append one token per sequence: K and V rows k_new / v_new, bf16 [B][Hkv][d]
+ * at k_new + b*kv_sb + h*kv_sh (element strides, multiples of 8; head
+ * dimension contiguous; both 16-byte aligned).  Sequence b's token goes to
+ * position suffix_len[b] of its suffix, in the page of that position.  Then
+ * suffix_len[b] (device, int32 [B]) is incremented.
+ * A length outside [0, capacity) writes nothing, leaves the length as it was
+ * and sets HP_ERR_BOUNDS in the status word of ws (>= 256 bytes, the step's
+ * workspace).  One launch, no allocation, graph-capturable. */
+hp_status hp_cascade_append_kv(const void *plan_dev, const hp_plan_info *info, const void *k_new,
+                               const void *v_new, int64_t kv_sb, int64_t kv_sh, int32_t *suffix_len,
+                               void *ws, size_t ws_bytes, hp_stream_t stream);
+
+/* hp_cascade_decode over a loop plan: sequence b's suffix is its first
+ * suffix_len[b] tokens (device, int32 [B], read on the device after the
+ * kernels before it in the stream have completed).  A length below the
+ * suffix's plan-time kv_len (or 0), or above the capacity, sets HP_ERR_BOUNDS
+ * in the status word; the step then still runs within the reserved pages,
+ * but its results are not valid.  Otherwise as hp_cascade_decode. */
+hp_status hp_cascade_decode_loop(const void *plan_dev, const hp_plan_info *info, const int32_t *suffix_len,
+                                 const void *q, int64_t q_sb, int64_t q_sh, float scale, void *out,
+                                 hp_dtype out_dt, int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb,
+                                 void *ws, size_t ws_bytes, hp_stream_t stream);
+
 /* Host-side description of a plan for inspection and tests: the (level, node,
  * seq_begin, seq_end, pass) context list in the order the pages list it --
  * shared nodes (more than one sequence; batched pass = 1) level by level,

@@ -69,6 +69,13 @@ _SIGNATURES = {
     "hp_cascade_decode_profiled": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_i64, c_i64, c_f32, c_vp,
                                            c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz, c_vp,
                                            ctypes.POINTER(c_vp)]),
+    "hp_cascade_loop_plan_bytes": (c_sz, [ctypes.POINTER(HpTreeDesc), c_i32]),
+    "hp_cascade_loop_plan": (c_i32, [ctypes.POINTER(HpTreeDesc), c_i32, c_vp, c_sz, ctypes.POINTER(HpPlanInfo),
+                                     c_vp]),
+    "hp_cascade_append_kv": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_vp, c_i64, c_i64, c_vp, c_vp,
+                                     c_sz, c_vp]),
+    "hp_cascade_decode_loop": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_vp, c_i64, c_i64, c_f32, c_vp,
+                                       c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz, c_vp]),
     "hp_cascade_contexts": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i32), c_i32]),
     "hp_cascade_plan_stats": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i64)]),
     "hp_read_device_status": (c_i32, [c_vp, c_vp]),
@@ -283,16 +290,25 @@ class CascadePlan:
     changes).  Owns the plan buffer and a workspace sized for it."""
 
     def __init__(self, levels, B: int, Hq: int, Hkv: int, d: int, device="cuda", stream=None,
-                 num_sms: int = 0, workspace: bool = True):
+                 num_sms: int = 0, workspace: bool = True, capacity: int = 0):
         D = _Desc(levels, B, Hq, Hkv, d, num_sms=num_sms)
-        nbytes = int(library().hp_cascade_plan_bytes(ctypes.byref(D.desc)))
+        lib = library()
+        if capacity:
+            nbytes = int(lib.hp_cascade_loop_plan_bytes(ctypes.byref(D.desc), int(capacity)))
+        else:
+            nbytes = int(lib.hp_cascade_plan_bytes(ctypes.byref(D.desc)))
         if nbytes == 0:
-            raise HpError(HP_ERR_ARG, "hp_cascade_plan_bytes")
+            raise HpError(HP_ERR_ARG, "hp_cascade_loop_plan_bytes" if capacity else "hp_cascade_plan_bytes")
         self.plan = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.info = HpPlanInfo()
-        _check(library().hp_cascade_plan(ctypes.byref(D.desc), _ptr(self.plan), nbytes,
-                                         ctypes.byref(self.info), _stream(stream)), "hp_cascade_plan")
+        if capacity:
+            _check(lib.hp_cascade_loop_plan(ctypes.byref(D.desc), int(capacity), _ptr(self.plan), nbytes,
+                                            ctypes.byref(self.info), _stream(stream)), "hp_cascade_loop_plan")
+        else:
+            _check(lib.hp_cascade_plan(ctypes.byref(D.desc), _ptr(self.plan), nbytes,
+                                       ctypes.byref(self.info), _stream(stream)), "hp_cascade_plan")
         self.B, self.Hq, self.Hkv, self.d = B, Hq, Hkv, d
+        self.capacity = int(capacity)
         self.ws = alloc_workspace(self.info.ws_bytes, device) if workspace else None
 
     @classmethod
@@ -352,6 +368,80 @@ def hp_cascade_decode_profiled(plan: CascadePlan, q: torch.Tensor, scale: float,
         _ptr(plan.plan), ctypes.byref(plan.info), _ptr(q), q.stride(0), q.stride(1), float(scale), _ptr(out),
         _dt(out.dtype), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(plan.ws if ws is None else ws),
         (plan.ws if ws is None else ws).numel(), _stream(stream), ev), "hp_cascade_decode_profiled")
+
+
+# ---------------------------------------------------------- decode loop
+def hp_cascade_loop_plan_bytes(levels, B, Hq, Hkv, d, capacity: int, num_sms: int = 0) -> int:
+    D = _Desc(levels, B, Hq, Hkv, d, num_sms=num_sms)
+    return int(library().hp_cascade_loop_plan_bytes(ctypes.byref(D.desc), int(capacity)))
+
+
+class LoopPlan(CascadePlan):
+    """A decode-loop plan (hp_cascade_loop_plan): the tree's last level holds
+    each sequence's suffix, with pages reserved up to ``capacity`` tokens.
+    ``suffix_len`` (device int32 [B], owned here) starts at the suffixes'
+    plan-time lengths; ``append`` writes one token per sequence and moves it
+    on, ``decode`` attends over the current lengths."""
+
+    def __init__(self, levels, B: int, Hq: int, Hkv: int, d: int, capacity: int, device="cuda",
+                 stream=None, num_sms: int = 0):
+        _need(int(capacity) >= 1, "capacity must be at least 1")
+        super().__init__(levels, B, Hq, Hkv, d, device=device, stream=stream, num_sms=num_sms,
+                         capacity=int(capacity))
+        lens = [0] * B
+        for sb, se, kl, _ in levels[-1][4]:
+            lens[int(sb)] = int(kl)
+        self.suffix_len = torch.tensor(lens, dtype=torch.int32, device=device)
+
+    @classmethod
+    def from_workload(cls, wl, capacity: int, **kw) -> "LoopPlan":
+        return cls(_levels_of(wl), wl.B, wl.Hq, wl.Hkv, wl.d, capacity, device=wl.q.device, **kw)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+        hp_cascade_append_kv(self, k_new, v_new, stream=stream)
+
+    def decode(self, q: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+               lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+               out_dtype=torch.bfloat16, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        return hp_cascade_decode_loop(self, q, scale, out=out, lse=lse, ws=ws, out_dtype=out_dtype, stream=stream)
+
+
+def hp_cascade_append_kv(plan: LoopPlan, k_new: torch.Tensor, v_new: torch.Tensor, ws: Optional[torch.Tensor] = None,
+                         stream=None) -> None:
+    """One token per sequence: k_new / v_new bf16 [B][Hkv][d] (head dimension
+    contiguous) go to position plan.suffix_len[b] of each suffix."""
+    shape = (plan.B, plan.Hkv, plan.d)
+    for t, nm in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(tuple(t.shape) == shape and t.dtype == torch.bfloat16 and t.is_cuda and t.stride(2) == 1,
+              f"{nm} must be bf16 [B][Hkv][d] on the GPU, d contiguous")
+    _need(k_new.stride() == v_new.stride(), "k_new and v_new must have the same strides")
+    ws = plan.ws if ws is None else ws
+    _need(ws is not None and ws.dtype == torch.uint8 and ws.is_cuda, "workspace must be a uint8 GPU tensor")
+    _check(library().hp_cascade_append_kv(
+        _ptr(plan.plan), ctypes.byref(plan.info), _ptr(k_new), _ptr(v_new), k_new.stride(0), k_new.stride(1),
+        _ptr(plan.suffix_len), _ptr(ws), ws.numel(), _stream(stream)), "hp_cascade_append_kv")
+
+
+def hp_cascade_decode_loop(plan: LoopPlan, q: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                           lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                           out_dtype=torch.bfloat16, stream=None,
+                           suffix_len: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    B, Hq, d = q.shape
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = plan.ws
+    lens = plan.suffix_len if suffix_len is None else suffix_len
+    _need(lens.dtype == torch.int32 and lens.is_cuda and tuple(lens.shape) == (plan.B,) and lens.is_contiguous(),
+          "suffix_len must be a contiguous int32 [B] GPU tensor")
+    _check_step_tensors(plan, q, out, lse, ws)
+    _check(library().hp_cascade_decode_loop(
+        _ptr(plan.plan), ctypes.byref(plan.info), _ptr(lens), _ptr(q), q.stride(0), q.stride(1), float(scale),
+        _ptr(out), _dt(out.dtype), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(),
+        _stream(stream)), "hp_cascade_decode_loop")
+    return out, lse
 
 
 def hp_read_device_status(ws: torch.Tensor, stream=None) -> int:

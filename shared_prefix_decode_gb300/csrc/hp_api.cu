@@ -22,7 +22,7 @@ using namespace hp;
 
 namespace {
 
-constexpr int32_t kAbiVersion = 2;
+constexpr int32_t kAbiVersion = 3;
 // A tensor-core item processes at most kMaxTcTiles 128-key tiles.
 constexpr int64_t kMaxTcTiles = 128;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -197,6 +197,7 @@ struct HostPlan {
     std::vector<int32_t> page_ids;     // all levels' page ids, concatenated
     std::vector<int32_t> level_ps;     // page size per level
     std::vector<int32_t> merge_tab;  // [B*Hkv][merge_stride]
+    std::vector<int32_t> leaf_tab;   // decode loop: [B][leaf_stride] suffix page ids
     std::vector<std::vector<int32_t>> cta_tc, cta_small;  // item ids per CTA of the fused kernel
     std::vector<std::vector<uint8_t>> records;           // one per CTA, without the tag
     std::vector<int32_t> contexts;  // (level, node, seq_begin, seq_end, pass) x n
@@ -218,12 +219,12 @@ struct CostModel {
     double tc(const WorkItem &w, int G, int d) const
     {
         const bool two = w.n_seq > kTcTile / G;
-        return tc_item + (two ? tc_tile : tc_tile1) * (double)ceil_div(w.k1 - w.k0, kTcTile) * d / 128.0;
+        return tc_item + (two ? tc_tile : tc_tile1) * (double)ceil_div(w.k1_model - w.k0, kTcTile) * d / 128.0;
     }
     // a paged item loads its keys and values once for all its sequences
     double small(const WorkItem &w, int d, int nh) const
     {
-        return sm_item + (double)(w.k1 - w.k0) * nh * d * 4 / sm_bytes_per_ns;
+        return sm_item + (double)(w.k1_model - w.k0) * nh * d * 4 / sm_bytes_per_ns;
     }
 };
 
@@ -320,6 +321,7 @@ void build_records(HostPlan &P)
             r.ps = ps;
             r.box = L.tc_box;
             r.num_pages = L.num_pages;
+            r.len_seq = w.len_seq;
             const int64_t first = w.k0 / ps, n = item_pages(w, ps);
             for (int64_t i = 0; i < n; ++i)
                 pages.push_back(P.page_ids[(size_t)(w.page_base + first + i)]);
@@ -345,19 +347,25 @@ void build_records(HostPlan &P)
 // head, up to two blocks of 128 / G sequences; paged items: a group of nh KV
 // heads of a node's sequences), with their partial rows and, when `lists`
 // is given, the merge list of every (b, kvh).  Returns the partial row count.
+// With capacity > 0 (a decode-loop plan) the last level's suffixes are split
+// over their plan-time length as usual, but each suffix's last item reaches
+// to the capacity (a suffix of length 0 gets one item [0, capacity)); at run
+// time the items end at the sequence's current length.
 int64_t make_items(const hp_tree_desc *d, int G, int nh, int64_t tc_split, int64_t small_split,
                    const std::vector<int32_t> &level_page_off, HostPlan &P,
-                   std::vector<std::vector<int32_t>> *lists)
+                   std::vector<std::vector<int32_t>> *lists, int capacity = 0)
 {
     P.tc.clear();
     P.small.clear();
     int64_t part = 0;
     for (int l = 0; l < d->num_levels; ++l) {
         const hp_tree_level &L = d->levels[l];
+        const bool loop = capacity > 0 && l == d->num_levels - 1;
         for (int n = 0; n < L.num_nodes; ++n) {
             const hp_tree_node &N = L.nodes[n];
-            if (N.kv_len == 0)
+            if (N.kv_len == 0 && !loop)
                 continue;
+            const int64_t klen = loop ? std::max(N.kv_len, 1) : N.kv_len;
             const int nseq = N.seq_end - N.seq_begin;
             const bool tc = (int64_t)nseq * G > kSmallRows;
             const int spc = tc ? 2 * (kTcTile / G) : nseq;
@@ -368,14 +376,22 @@ int64_t make_items(const hp_tree_desc *d, int G, int nh, int64_t tc_split, int64
             for (int s0 = N.seq_begin; s0 < N.seq_end; s0 += spc) {
                 const int ns = std::min(spc, N.seq_end - s0);
                 for (int kvh = 0; kvh < d->Hkv; kvh += hstep)
-                    for (int64_t k0 = 0; k0 < N.kv_len; k0 += split) {
+                    for (int64_t k0 = 0; k0 < klen; k0 += split) {
                         WorkItem w;
                         w.level = l;
                         w.seq_begin = s0;
                         w.n_seq = ns;
                         w.kvh = kvh;
                         w.k0 = (int32_t)k0;
-                        w.k1 = (int32_t)std::min<int64_t>(k0 + split, N.kv_len);
+                        w.k1 = (int32_t)std::min<int64_t>(k0 + split, klen);
+                        w.len_seq = loop ? s0 : -1;
+                        w.k1_model = w.k1;
+                        if (loop && w.k1 == klen) {
+                            // reaches to the capacity; over the loop it holds
+                            // half of the headroom on average
+                            w.k1 = capacity;
+                            w.k1_model = (int32_t)std::max<int64_t>(k0 + 1, (N.kv_len + (int64_t)capacity) / 2);
+                        }
                         w.page_base = level_page_off[l] + N.page_off;
                         w.part_row = (int32_t)std::min<int64_t>(part, INT32_MAX);
                         if (tc) {
@@ -441,6 +457,53 @@ hp_status validate_desc(const hp_tree_desc *d)
     return HP_OK;
 }
 
+// A decode-loop tree: the last level holds one single-sequence node per
+// sequence (node n covers sequence n), each with page ids for `capacity`
+// tokens that no other node of the same pools uses, and every suffix's rows
+// fit one paged item (G <= 16).
+hp_status validate_loop(const hp_tree_desc *d, int capacity)
+{
+    if (capacity < 1 || capacity > (1 << 24))
+        return HP_ERR_ARG;
+    if (d->Hq / d->Hkv > kSmallRows)
+        return HP_ERR_UNSUPPORTED;
+    const int last = d->num_levels - 1;
+    const hp_tree_level &S = d->levels[last];
+    if (S.num_nodes != d->B)
+        return HP_ERR_ARG;
+    const int64_t cap_pages = ceil_div(capacity, S.page_size);
+    std::vector<char> mine((size_t)S.num_pages, 0);
+    for (int n = 0; n < S.num_nodes; ++n) {
+        const hp_tree_node &N = S.nodes[n];
+        if (N.seq_begin != n || N.seq_end != n + 1 || N.kv_len > capacity)
+            return HP_ERR_ARG;
+        if ((int64_t)N.page_off + cap_pages > S.num_page_ids)
+            return HP_ERR_ARG;
+        for (int64_t i = 0; i < cap_pages; ++i) {
+            const int32_t pid = S.page_ids[N.page_off + i];
+            if (pid < 0 || pid >= S.num_pages || mine[(size_t)pid])
+                return HP_ERR_ARG;  // out of range, or reserved twice
+            mine[(size_t)pid] = 1;
+        }
+    }
+    // pages of the other levels in the same pools stay read-only
+    for (int l = 0; l < last; ++l) {
+        const hp_tree_level &L = d->levels[l];
+        if (L.k_pool != S.k_pool && L.v_pool != S.v_pool && L.k_pool != S.v_pool && L.v_pool != S.k_pool)
+            continue;
+        for (int n = 0; n < L.num_nodes; ++n) {
+            const hp_tree_node &N = L.nodes[n];
+            const int64_t npg = ceil_div(N.kv_len, L.page_size);
+            for (int64_t i = 0; i < npg; ++i) {
+                const int32_t pid = L.page_ids[N.page_off + i];
+                if (L.page_size != S.page_size || (pid < S.num_pages && mine[(size_t)pid]))
+                    return HP_ERR_ARG;
+            }
+        }
+    }
+    return HP_OK;
+}
+
 // Context list in the pages' order: shared nodes level by level, then each
 // sequence's private nodes in level order.
 void build_contexts(const hp_tree_desc *d, std::vector<int32_t> &out)
@@ -461,9 +524,11 @@ void build_contexts(const hp_tree_desc *d, std::vector<int32_t> &out)
             }
 }
 
-hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
+hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capacity = 0)
 {
     hp_status st = validate_desc(d);
+    if (st == HP_OK && capacity != 0)
+        st = validate_loop(d, capacity);
     if (st != HP_OK)
         return st;
     const int G = d->Hq / d->Hkv;
@@ -534,7 +599,7 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
             for (int k = 1; k < sms; ++k) {
                 int64_t ts, ss;
                 splits_for(k, ts, ss);
-                make_items(d, G, nh, ts, ss, level_page_off, P, nullptr);
+                make_items(d, G, nh, ts, ss, level_page_off, P, nullptr, capacity);
                 const double t = schedule(P, sms, k, mixed != 0, d->d, cm);
                 if (t >= 0.0 && (best < 0.0 || t < best)) {
                     best = t;
@@ -548,7 +613,7 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
 
     // Items and partial rows, level by level; merge lists per (b, kvh).
     std::vector<std::vector<int32_t>> lists((size_t)d->B * d->Hkv);
-    const int64_t part = make_items(d, G, nh, tc_split, small_split, level_page_off, P, &lists);
+    const int64_t part = make_items(d, G, nh, tc_split, small_split, level_page_off, P, &lists, capacity);
     if (part > INT32_MAX)
         return HP_ERR_UNSUPPORTED;
     // merge table: one row per (b, kvh), its count then its partial rows
@@ -581,6 +646,21 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode)
     size_t off = plan_tab_offset(sms, H.rec_stride);
     H.off_merge_tab = (int64_t)off;
     off += 4 * P.merge_tab.size();
+    if (capacity > 0) {
+        // each sequence's suffix pages, for the appends of the loop
+        const int last = d->num_levels - 1;
+        const hp_tree_level &S = d->levels[last];
+        H.loop_capacity = capacity;
+        H.loop_level = last;
+        H.leaf_stride = (int32_t)ceil_div(capacity, S.page_size);
+        off = round_up(off, 64);
+        H.off_leaf_tab = (int64_t)off;
+        P.leaf_tab.assign((size_t)d->B * H.leaf_stride, 0);
+        for (int b = 0; b < d->B; ++b)
+            std::copy(S.page_ids + S.nodes[b].page_off, S.page_ids + S.nodes[b].page_off + H.leaf_stride,
+                      P.leaf_tab.begin() + (size_t)b * H.leaf_stride);
+        off += 4 * P.leaf_tab.size();
+    }
     H.total_bytes = (int64_t)round_up(off, 256);
     const WsLayout ws = ws_layout(part, d->d);
     H.ws_off_lse = (int64_t)ws.off_lse;
@@ -618,20 +698,26 @@ uint32_t *status_ptr(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
 // its schedule record from plan + kPlanRecOff + cta * rec_stride before it can
 // check the plan's tag, so a decode call is only launched when the grid and
 // record stride it was given stay inside the plan image last written there.
+// A decode-loop plan also keeps, on the host, what its appends need.
 struct PlanExtent {
     uint64_t tag;
     int64_t total_bytes;
+    int32_t loop_capacity;  // 0: not a decode-loop plan
+    int32_t leaf_stride, page_size, num_pages;
+    int64_t off_leaf_tab;
+    void *k_pool, *v_pool;  // the suffix level's pools
 };
 std::mutex g_plans_mu;
 std::unordered_map<const void *, PlanExtent> g_plans;
 
-void register_plan(const void *plan_dev, uint64_t tag, int64_t total)
+void register_plan(const void *plan_dev, const PlanExtent &e)
 {
     std::lock_guard<std::mutex> lk(g_plans_mu);
-    g_plans[plan_dev] = PlanExtent{tag, total};
+    g_plans[plan_dev] = e;
 }
 
-bool plan_extent_ok(const void *plan_dev, const hp_plan_info *info)
+// The plan last written at plan_dev, if info's geometry stays inside it.
+bool plan_extent(const void *plan_dev, const hp_plan_info *info, PlanExtent *out)
 {
     std::lock_guard<std::mutex> lk(g_plans_mu);
     auto it = g_plans.find(plan_dev);
@@ -639,7 +725,10 @@ bool plan_extent_ok(const void *plan_dev, const hp_plan_info *info)
         return false;
     const int64_t need = (int64_t)plan_tab_offset(info->grid, info->rec_stride) +
                          4 * (int64_t)info->B * info->Hkv * info->merge_stride;
-    return info->merge_stride >= 1 && need <= it->second.total_bytes;
+    if (info->merge_stride < 1 || need > it->second.total_bytes)
+        return false;
+    *out = it->second;
+    return true;
 }
 
 }  // namespace
@@ -888,13 +977,13 @@ size_t hp_cascade_plan_bytes(const hp_tree_desc *desc)
     return (size_t)P.hdr.total_bytes;
 }
 
-hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_bytes, hp_plan_info *info,
-                          hp_stream_t stream)
+static hp_status cascade_plan_impl(const hp_tree_desc *desc, int capacity, void *plan_dev, size_t plan_bytes,
+                                   hp_plan_info *info, hp_stream_t stream)
 {
     if (!plan_dev || !info)
         return HP_ERR_ARG;
     HostPlan P;
-    hp_status st = build_plan(desc, P, true);
+    hp_status st = build_plan(desc, P, true, capacity);
     if (st != HP_OK)
         return st;
     PlanHeader &H = P.hdr;
@@ -911,11 +1000,26 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
         std::memcpy(dst, &H.tag, sizeof(H.tag));  // RecHead::tag
     }
     std::memcpy(img.data() + H.off_merge_tab, P.merge_tab.data(), 4 * P.merge_tab.size());
+    if (!P.leaf_tab.empty())
+        std::memcpy(img.data() + H.off_leaf_tab, P.leaf_tab.data(), 4 * P.leaf_tab.size());
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(plan_dev, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return HP_ERR_CUDA;
-    register_plan(plan_dev, H.tag, H.total_bytes);
+    PlanExtent ext{};
+    ext.tag = H.tag;
+    ext.total_bytes = H.total_bytes;
+    if (capacity > 0) {
+        const hp_tree_level &S = desc->levels[desc->num_levels - 1];
+        ext.loop_capacity = capacity;
+        ext.leaf_stride = H.leaf_stride;
+        ext.page_size = S.page_size;
+        ext.num_pages = S.num_pages;
+        ext.off_leaf_tab = H.off_leaf_tab;
+        ext.k_pool = const_cast<void *>(S.k_pool);
+        ext.v_pool = const_cast<void *>(S.v_pool);
+    }
+    register_plan(plan_dev, ext);
     std::memset(info, 0, sizeof(*info));
     info->B = H.B;
     info->Hq = H.Hq;
@@ -934,10 +1038,33 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
     return HP_OK;
 }
 
+hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_bytes, hp_plan_info *info,
+                          hp_stream_t stream)
+{
+    return cascade_plan_impl(desc, 0, plan_dev, plan_bytes, info, stream);
+}
+
+size_t hp_cascade_loop_plan_bytes(const hp_tree_desc *desc, int32_t capacity)
+{
+    HostPlan P;
+    if (capacity < 1 || build_plan(desc, P, false, capacity) != HP_OK)
+        return 0;
+    return (size_t)P.hdr.total_bytes;
+}
+
+hp_status hp_cascade_loop_plan(const hp_tree_desc *desc, int32_t capacity, void *plan_dev, size_t plan_bytes,
+                               hp_plan_info *info, hp_stream_t stream)
+{
+    if (capacity < 1)
+        return HP_ERR_ARG;
+    return cascade_plan_impl(desc, capacity, plan_dev, plan_bytes, info, stream);
+}
+
 static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *info, const void *q,
                                      int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,
                                      int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
-                                     size_t ws_bytes, hp_stream_t stream, void *const *events)
+                                     size_t ws_bytes, hp_stream_t stream, void *const *events,
+                                     const int32_t *suffix_len = nullptr)
 {
     auto mark = [&](int i) {
         if (events && events[i])
@@ -952,7 +1079,13 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         return HP_ERR_UNSUPPORTED;
     if (info->Hq / info->Hkv > kTcTile || info->grid < 1 || info->num_levels < 1 ||
         info->num_levels > kMaxLevels || info->rec_stride < (int32_t)sizeof(RecHead) ||
-        info->rec_stride > kRecMaxBytes || info->rec_stride % 128 || !plan_extent_ok(plan_dev, info))
+        info->rec_stride > kRecMaxBytes || info->rec_stride % 128)
+        return HP_ERR_ARG;
+    PlanExtent ext;
+    if (!plan_extent(plan_dev, info, &ext))
+        return HP_ERR_ARG;
+    // a decode-loop plan runs with the current suffix lengths, a plain plan without
+    if ((ext.loop_capacity > 0) != (suffix_len != nullptr) || (suffix_len && !aligned(suffix_len, 4)))
         return HP_ERR_ARG;
     if (ws_bytes < (size_t)info->ws_bytes || !aligned(ws, 256))
         return HP_ERR_WORKSPACE;
@@ -993,6 +1126,8 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         // HP_ERR_DEVICE_TIMEOUT through the status word.
         const char *wh = std::getenv("HP_TEST_WITHHOLD_TILE");
         cp.withhold = wh != nullptr && wh[0] == '1';
+        cp.suffix_len = suffix_len;
+        cp.loop_capacity = ext.loop_capacity;
         if (launch_cascade(cp, info->grid, info->d, s) != cudaSuccess)
             return HP_ERR_CUDA;
     }
@@ -1034,6 +1169,54 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
 {
     return cascade_decode_impl(plan_dev, info, q, q_sb, q_sh, scale, out, out_dt, o_sb, o_sh, lse, lse_sb, ws,
                                ws_bytes, stream, nullptr);
+}
+
+hp_status hp_cascade_decode_loop(const void *plan_dev, const hp_plan_info *info, const int32_t *suffix_len,
+                                 const void *q, int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,
+                                 int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws, size_t ws_bytes,
+                                 hp_stream_t stream)
+{
+    if (!suffix_len)
+        return HP_ERR_ARG;
+    return cascade_decode_impl(plan_dev, info, q, q_sb, q_sh, scale, out, out_dt, o_sb, o_sh, lse, lse_sb, ws,
+                               ws_bytes, stream, nullptr, suffix_len);
+}
+
+hp_status hp_cascade_append_kv(const void *plan_dev, const hp_plan_info *info, const void *k_new, const void *v_new,
+                               int64_t kv_sb, int64_t kv_sh, int32_t *suffix_len, void *ws, size_t ws_bytes,
+                               hp_stream_t stream)
+{
+    if (!plan_dev || !info || !k_new || !v_new || !suffix_len || !ws)
+        return HP_ERR_ARG;
+    if (info->B < 1 || info->Hkv < 1 || !supported_d(info->d) || info->grid < 1 || info->rec_stride < 1)
+        return HP_ERR_ARG;
+    PlanExtent ext;
+    if (!plan_extent(plan_dev, info, &ext) || ext.loop_capacity < 1)
+        return HP_ERR_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(suffix_len, 4) || kv_sb <= 0 || kv_sh <= 0 ||
+        kv_sb % 8 || kv_sh % 8)
+        return HP_ERR_UNSUPPORTED;
+    if (ws_bytes < kWsHeader || !aligned(ws, 256))
+        return HP_ERR_WORKSPACE;
+    AppendParams ap;
+    std::memset(&ap, 0, sizeof(ap));
+    ap.leaf_tab = reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(plan_dev) + ext.off_leaf_tab);
+    ap.leaf_stride = ext.leaf_stride;
+    ap.capacity = ext.loop_capacity;
+    ap.page_size = ext.page_size;
+    ap.num_pages = ext.num_pages;
+    ap.B = info->B;
+    ap.Hkv = info->Hkv;
+    ap.d = info->d;
+    ap.k_pool = static_cast<uint16_t *>(ext.k_pool);
+    ap.v_pool = static_cast<uint16_t *>(ext.v_pool);
+    ap.k_new = static_cast<const uint16_t *>(k_new);
+    ap.v_new = static_cast<const uint16_t *>(v_new);
+    ap.kv_sb = kv_sb;
+    ap.kv_sh = kv_sh;
+    ap.suffix_len = suffix_len;
+    ap.status = status_ptr(ws);
+    return launch_append(ap, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? HP_OK : HP_ERR_CUDA;
 }
 
 hp_status hp_cascade_decode_profiled(const void *plan_dev, const hp_plan_info *info, const void *q,

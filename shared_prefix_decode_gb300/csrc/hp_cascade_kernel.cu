@@ -77,7 +77,11 @@ __device__ __forceinline__ tcr::ItemGeo tc_geo(const CascadeParams &p, const Rec
     return g;
 }
 
-// The paged items of this CTA's record.
+// The paged items of this CTA's record.  In a decode loop a suffix item's
+// key range ends at its sequence's current length (at most the planned end,
+// which is the capacity for the suffix's last item).  A length that leaves
+// the item empty or passes the capacity is reported; the item then keeps one
+// key, inside its reserved pages, so the step stays in bounds.
 struct RecordItems {
     const CascadeParams *p;
     const RecItem *items;  // the record's paged items
@@ -91,6 +95,14 @@ struct RecordItems {
         d.kvh0 = w.kvh;
         d.k0 = w.k0;
         d.k1 = w.k1;
+        if (w.len_seq >= 0 && p->suffix_len) {
+            const int len = p->suffix_len[w.len_seq];
+            d.k1 = min(w.k1, len);
+            if (d.k1 <= w.k0 || len > p->loop_capacity) {
+                atomicOr(p->status, kStBounds);
+                d.k1 = max(d.k1, w.k0 + 1);
+            }
+        }
         d.part_row = w.part_row;
         d.pages = pages + w.page_off;
         d.pbase = w.k0 / w.ps;

@@ -38,8 +38,10 @@ struct WorkItem {
     int32_t k0, k1;
     int32_t page_base;  // index in the level's page-id list of the node's first page
     int32_t part_row;
+    int32_t len_seq;    // decode-loop suffix items: the sequence whose length ends the range; else -1
+    int32_t k1_model;   // the key end the cost model assumes (k1, or a loop item's mean end)
 };
-static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+static_assert(sizeof(WorkItem) == 40, "WorkItem layout");
 
 struct LevelDev {
     const void *k_pool;
@@ -69,6 +71,12 @@ struct alignas(64) PlanHeader {
     int64_t ws_bytes;
     int64_t ws_off_lse;     // byte offsets into the workspace
     int64_t ws_off_o;
+    // decode-loop plans (loop_capacity > 0): the suffix level, and each
+    // sequence's suffix pages for appends, [B][leaf_stride] int32 at
+    // off_leaf_tab (after the merge table)
+    int32_t loop_capacity, loop_level;
+    int32_t leaf_stride, pad0;
+    int64_t off_leaf_tab;
     LevelDev levels[kMaxLevels];
 };
 
@@ -97,7 +105,7 @@ struct RecItem {
     int32_t seq_begin, n_seq, kvh, k0, k1, part_row;
     int32_t level, page_off;
     int32_t ps, box, num_pages;
-    int32_t pad;
+    int32_t len_seq;  // decode-loop suffix items: the sequence whose current length ends [k0, k1); else -1
 };
 static_assert(sizeof(RecHead) == 32 && sizeof(RecItem) == 48, "record layout");
 constexpr int kRecMaxBytes = 8192;
@@ -157,6 +165,23 @@ struct CascadeParams {
     float *part_lse;
     uint32_t *status;
     int32_t withhold;      // failure detection tests: CTA 0 withholds its first K tile
+    // decode-loop plans: suffix item ends come from suffix_len[len_seq]
+    const int32_t *suffix_len;
+    int32_t loop_capacity;
+};
+
+// Decode-loop append: one token per sequence into its suffix pages.
+struct AppendParams {
+    const int32_t *leaf_tab;  // [B][leaf_stride] page ids (the plan's)
+    int32_t leaf_stride, capacity, page_size, num_pages;
+    int32_t B, Hkv, d;
+    uint16_t *k_pool;  // bf16 [num_pages][Hkv][page_size][d]
+    uint16_t *v_pool;
+    const uint16_t *k_new;  // bf16 row (b, h) at b*kv_sb + h*kv_sh
+    const uint16_t *v_new;
+    int64_t kv_sb, kv_sh;
+    int32_t *suffix_len;
+    uint32_t *status;
 };
 
 // Merge kernel: combines the partial rows of each output row.
@@ -196,6 +221,7 @@ cudaError_t launch_merge(const MergeParams &p, int64_t out_rows, cudaStream_t s)
 // The merge as a programmatic dependent launch of the preceding kernel.
 cudaError_t launch_merge_dependent(const MergeParams &p, int64_t out_rows, cudaStream_t s);
 cudaError_t launch_cascade(const CascadeParams &p, int grid, int d, cudaStream_t s);
+cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
 int cascade_heads_per_item(int Hkv);
 int cascade_q_rows();  // paged-role Q slot rows of the fused kernel
 int small_q_rows();    // Q slot rows of the standalone paged kernel

@@ -39,6 +39,9 @@ __all__ = [
     "CONFIG_NAMES",
     "full_page_tables",
     "apply_probe",
+    "with_suffix_capacity",
+    "append_token",
+    "decode_tokens",
 ]
 
 
@@ -264,6 +267,69 @@ def full_page_tables(wl: CascadeWorkload) -> Tuple[torch.Tensor, torch.Tensor]:
         if p:
             pt[b, :len(p)] = torch.tensor(p, dtype=torch.int32)
     return pt, torch.tensor(lens, dtype=torch.int32)
+
+
+# ------------------------------------------------------------ decode loop
+def with_suffix_capacity(wl: CascadeWorkload, capacity: int, seed: int = 0) -> CascadeWorkload:
+    """The same workload with every private suffix's page list reserved up to
+    ``capacity`` tokens, for a decode loop that appends one token per sequence
+    per step.  The new pages go at the end of the pool, filled with N(0,1)
+    bf16 (what a reused page would hold: never visible until written), and
+    are handed out in a seeded random order.  The last level must hold one
+    node per sequence, node b covering sequence b."""
+    last = wl.levels[-1]
+    nodes = last.nodes.tolist()
+    assert len(nodes) == wl.B and all(n[0] == b and n[1] == b + 1 for b, n in enumerate(nodes))
+    ps = wl.page_size
+    cap_pages = (capacity + ps - 1) // ps
+    assert all(n[2] <= capacity for n in nodes)
+    g = torch.Generator().manual_seed(seed + 7919)
+    extra = sum(cap_pages - (n[2] + ps - 1) // ps for n in nodes)
+    base = wl.num_pages
+    order = (base + torch.randperm(max(extra, 1), generator=g))[:extra].tolist()
+    shape = (extra, wl.Hkv, ps, wl.d)
+    k_pool = torch.cat([wl.k_pool.cpu(), torch.randn(shape, generator=g).to(torch.bfloat16)])
+    v_pool = torch.cat([wl.v_pool.cpu(), torch.randn(shape, generator=g).to(torch.bfloat16)])
+    ids_old = last.page_ids.tolist()
+    ids, new_nodes, it = [], [], 0
+    for sb, se, kl, off in nodes:
+        npg = (kl + ps - 1) // ps
+        new_nodes.append((sb, se, kl, len(ids)))
+        ids.extend(ids_old[off:off + npg])
+        ids.extend(order[it:it + cap_pages - npg])
+        it += cap_pages - npg
+    levels = [TreeLevel(l.nodes.clone(), l.page_ids.cpu().clone()) for l in wl.levels[:-1]]
+    levels.append(TreeLevel(torch.tensor(new_nodes, dtype=torch.int32).reshape(-1, 4),
+                            torch.tensor(ids, dtype=torch.int32)))
+    return CascadeWorkload(wl.name, wl.B, wl.Hq, wl.Hkv, wl.d, ps, wl.scale, wl.q.cpu().clone(), k_pool,
+                           v_pool, levels, wl.seed)
+
+
+def decode_tokens(wl: CascadeWorkload, steps: int, seed: int = 0):
+    """Seeded inputs of a decode loop: per step, a new query [B][Hq][d] and
+    the new token's K and V rows [B][Hkv][d] (N(0,1) rounded to bf16)."""
+    g = torch.Generator().manual_seed(seed + 104729)
+    out = []
+    for _ in range(steps):
+        q = torch.randn(wl.B, wl.Hq, wl.d, generator=g).to(torch.bfloat16)
+        k = torch.randn(wl.B, wl.Hkv, wl.d, generator=g).to(torch.bfloat16)
+        v = torch.randn(wl.B, wl.Hkv, wl.d, generator=g).to(torch.bfloat16)
+        out.append((q, k, v))
+    return out
+
+
+def append_token(wl: CascadeWorkload, k_new: torch.Tensor, v_new: torch.Tensor) -> None:
+    """Host-side append (in place, CPU tensors): sequence b's new K / V rows
+    go to slot kv_len % ps of page ``page_ids[page_off + kv_len // ps]`` of its
+    suffix, and its kv_len grows by one."""
+    last = wl.levels[-1]
+    ps = wl.page_size
+    ids = last.page_ids.tolist()
+    for b, (sb, se, kl, off) in enumerate(last.nodes.tolist()):
+        page = ids[off + kl // ps]
+        wl.k_pool[page, :, kl % ps, :] = k_new[b].cpu()
+        wl.v_pool[page, :, kl % ps, :] = v_new[b].cpu()
+        last.nodes[b, 2] = kl + 1
 
 
 def _probe_code(b: int, d: int) -> torch.Tensor:

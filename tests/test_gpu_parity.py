@@ -461,3 +461,133 @@ def test_cascade_random_trees(seed):
     out, lse = plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
     _status_ok(plan.ws)
     _check(out, lse, O, L, f"random tree {seed}: B={wl.B} Hq={wl.Hq} Hkv={wl.Hkv} d={wl.d} ps={wl.page_size}")
+
+
+# ------------------------------------------------------------ decode loop
+def _loop_host(name, kw, steps, seed):
+    if name == "edges":
+        # suffixes of length 0, 1 and at page edges; capacity just covers the loop
+        wl = W.build_cascade("edges", B=6, Hq=8, Hkv=2, d=128, page_size=16, shared=[[(0, 6, 100)]],
+                             suffix_lens=[0, 1, 15, 16, 17, 33], seed=seed)
+    else:
+        wl = W.make_config(name, seed=seed, **kw)
+    cap = int(wl.levels[-1].nodes[:, 2].max()) + steps
+    return W.with_suffix_capacity(wl, cap, seed=seed), cap
+
+
+@pytest.mark.parametrize("name,kw,steps", [
+    ("llama3_8b", dict(B=8, prefix=512), 40),
+    ("tiny", {}, 24),
+    ("tree2", dict(B=16, prefix=128), 20),
+    ("no_sharing", dict(B=4, prefix=100), 20),
+    ("edges", {}, 34),
+])
+def test_decode_loop_matches_oracle_every_step(name, kw, steps):
+    """A decode loop through the C ABI: each step appends one token per
+    sequence into its suffix pages and attends over the grown suffixes with
+    the plan built once.  Every step's rows against the oracle over the same
+    tree with the token appended on the host; at the end the device pools and
+    lengths equal the host's, byte for byte."""
+    host, cap = _loop_host(name, kw, steps, seed=5)
+    dev = host.to(DEV)
+    plan = hb.LoopPlan.from_workload(dev, cap)
+    for s, (q, k, v) in enumerate(W.decode_tokens(host, steps, seed=5)):
+        plan.append(k.to(DEV), v.to(DEV))
+        out, lse = plan.decode(q.to(DEV), host.scale, out_dtype=torch.float32)
+        W.append_token(host, k, v)
+        host.q = q
+        O, L = oracle.cascade(host)
+        _check(out, lse, O, L, f"decode loop {name} step {s}")
+    _status_ok(plan.ws)
+    assert torch.equal(plan.suffix_len.cpu(), host.levels[-1].nodes[:, 2])
+    assert torch.equal(dev.k_pool.cpu(), host.k_pool) and torch.equal(dev.v_pool.cpu(), host.v_pool)
+
+
+def test_decode_loop_as_one_graph():
+    """A 32-step loop (append + decode per step) captured as one CUDA graph
+    and replayed from the same starting state gives the eager loop's results
+    bit for bit."""
+    steps = 32
+    host, cap = _loop_host("llama3_8b", dict(B=8, prefix=256), steps, seed=9)
+    toks = W.decode_tokens(host, steps, seed=9)
+    qs, ks, vs = (torch.stack([t[i] for t in toks]).to(DEV) for i in range(3))
+    dev = host.to(DEV)
+    plan = hb.LoopPlan.from_workload(dev, cap)
+    k0, v0, n0 = dev.k_pool.clone(), dev.v_pool.clone(), plan.suffix_len.clone()
+    B, Hq, d = host.B, host.Hq, host.d
+    oe = torch.empty(steps, B, Hq, d, device=DEV)
+    le = torch.empty(steps, B, Hq, device=DEV)
+    for s in range(steps):
+        plan.append(ks[s], vs[s])
+        plan.decode(qs[s], host.scale, out=oe[s], lse=le[s])
+    torch.cuda.synchronize()
+    _status_ok(plan.ws)
+    og, lg = torch.zeros_like(oe), torch.zeros_like(le)
+
+    def reset():
+        dev.k_pool.copy_(k0)
+        dev.v_pool.copy_(v0)
+        plan.suffix_len.copy_(n0)
+
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        reset()
+        plan.append(ks[0], vs[0])  # warm-up on the capture stream
+        plan.decode(qs[0], host.scale, out=og[0], lse=lg[0])
+    torch.cuda.current_stream().wait_stream(st)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for s in range(steps):
+            plan.append(ks[s], vs[s])
+            plan.decode(qs[s], host.scale, out=og[s], lse=lg[s])
+    for _ in range(2):
+        reset()
+        og.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(og, oe) and torch.equal(lg, le)
+        assert torch.equal(plan.suffix_len, n0 + steps)
+    _status_ok(plan.ws)
+
+
+def test_decode_loop_length_errors_are_reported():
+    """Lengths the loop plan cannot serve are reported through the status
+    word, inside the reserved pages: an append at the capacity writes nothing
+    and keeps the length; a decode with a length below the plan-time suffix
+    (here 0) flags HP_ERR_BOUNDS.  A loop plan through the plain decode call,
+    and a plain plan through the loop calls, are argument errors."""
+    host, cap = _loop_host("llama3_8b", dict(B=4, prefix=128), 4, seed=2)
+    dev = host.to(DEV)
+    plan = hb.LoopPlan.from_workload(dev, cap)
+    (q, k, v), = W.decode_tokens(host, 1, seed=2)
+    q, k, v = q.to(DEV), k.to(DEV), v.to(DEV)
+    full = plan.suffix_len.clone()
+    full[1] = cap
+    plan.suffix_len.copy_(full)
+    kp = dev.k_pool.clone()
+    plan.append(k, v)
+    torch.cuda.synchronize()
+    assert hb.hp_read_device_status(plan.ws) == hb.HP_ERR_BOUNDS
+    n = plan.suffix_len.cpu()
+    assert n[1] == cap and n[0] == full[0] + 1
+    changed = (dev.k_pool != kp).flatten(1).any(1).nonzero().flatten().tolist()
+    assert len(changed) == 3  # one page for each of the other three sequences
+    plan.decode(q, host.scale)  # length == capacity is valid
+    _status_ok(plan.ws)
+    low = plan.suffix_len.clone()
+    low[2] = 0
+    hb.hp_cascade_decode_loop(plan, q, host.scale, suffix_len=low)
+    torch.cuda.synchronize()
+    assert hb.hp_read_device_status(plan.ws) == hb.HP_ERR_BOUNDS
+    with pytest.raises(hb.HpError):
+        hb.hp_cascade_decode(plan, q, host.scale)
+    static = hb.CascadePlan.from_workload(dev)
+    with pytest.raises(hb.HpError):
+        hb.hp_cascade_decode_loop(static, q, host.scale, suffix_len=plan.suffix_len)
+    static.suffix_len = plan.suffix_len
+    with pytest.raises(hb.HpError):
+        hb.hp_cascade_append_kv(static, k, v)
+    torch.cuda.synchronize()
+    assert hb.hp_read_device_status(plan.ws) == hb.HP_OK

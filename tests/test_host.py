@@ -30,7 +30,7 @@ def test_library_loads_and_exports_every_declared_symbol():
         assert hasattr(lib, name), f"{name} declared in hp.h but not exported"
     assert set(declared) == set(hb.exported_symbols())
     assert lib.hp_build_arch() == 103
-    assert lib.hp_abi_version() == 2
+    assert lib.hp_abi_version() == 3
 
 
 def test_status_strings():
@@ -174,3 +174,75 @@ def test_decode_binding_rejects_wrong_step_tensors():
     for bad in (q.float(), q[:, :, ::2], q[:1], q):  # wrong dtype, stride, shape, host memory
         with pytest.raises(ValueError):
             hb._check_step_tensors(Plan, bad, q, lse, ws)
+
+
+# ------------------------------------------------------------ decode loop
+def _loop_levels(B=4, ps=16, cap_pages=3, shared_len=32, lens=(5, 16, 0, 20), pool=None):
+    """A shared node over all B sequences (pages 0..), then one suffix per
+    sequence with cap_pages reserved pages each (distinct ids after the
+    shared ones)."""
+    pool = pool if pool is not None else _pool()
+    n_sh = (shared_len + ps - 1) // ps
+    shared = (pool.data_ptr(), pool.data_ptr(), 64, ps, [(0, B, shared_len, 0)], list(range(n_sh)))
+    nodes = [(b, b + 1, lens[b], b * cap_pages) for b in range(B)]
+    ids = [n_sh + i for i in range(B * cap_pages)]
+    return [shared, (pool.data_ptr(), pool.data_ptr(), 64, ps, nodes, ids)]
+
+
+def test_loop_plan_is_the_static_plan_plus_the_suffix_page_table():
+    lv = _loop_levels()
+    static = hb.hp_cascade_plan_bytes(lv, 4, 4, 4, 128, num_sms=152)
+    loop = hb.hp_cascade_loop_plan_bytes(lv, 4, 4, 4, 128, capacity=48, num_sms=152)
+    assert static > 0 and loop > static
+    # capacity exactly the reserved pages, and a capacity of one token
+    assert hb.hp_cascade_loop_plan_bytes(_loop_levels(lens=(1, 1, 0, 1), cap_pages=1), 4, 4, 4, 128,
+                                         capacity=1, num_sms=152) > 0
+
+
+@pytest.mark.parametrize("mutate,why", [
+    (lambda lv: lv, "capacity beyond the reserved pages"),
+    (lambda lv: [lv[0], lv[1][:4] + ([(0, 2, 5, 0), (2, 3, 0, 6), (3, 4, 20, 9)],) + lv[1][5:]],
+     "a suffix node covering two sequences"),
+    (lambda lv: [lv[0], lv[1][:5] + ([1] + lv[1][5][1:],)], "a suffix page that a shared node uses"),
+    (lambda lv: [lv[0], lv[1][:5] + ([lv[1][5][3]] + lv[1][5][1:],)], "a page reserved for two suffixes"),
+    (lambda lv: [lv[0], lv[1][:4] + ([(0, 1, 5, 0), (1, 2, 16, 3), (2, 3, 0, 6)],) + lv[1][5:]],
+     "a sequence without a suffix node"),
+])
+def test_loop_plan_rejects_trees_it_cannot_grow(mutate, why):
+    cap = 64 if why.startswith("capacity") else 48
+    assert hb.hp_cascade_loop_plan_bytes(mutate(_loop_levels()), 4, 4, 4, 128, capacity=cap, num_sms=152) == 0, why
+
+
+def test_loop_plan_rejects_bad_capacity_and_wide_groups():
+    lv = _loop_levels()
+    assert hb.hp_cascade_loop_plan_bytes(lv, 4, 4, 4, 128, capacity=0, num_sms=152) == 0
+    assert hb.hp_cascade_loop_plan_bytes(lv, 4, 4, 4, 128, capacity=19, num_sms=152) == 0  # below a length
+    assert hb.hp_cascade_loop_plan_bytes(lv, 4, 32, 1, 128, capacity=48, num_sms=152) == 0  # G = 32 > 16
+    assert hb.hp_cascade_loop_plan_bytes(lv, 4, 16, 1, 128, capacity=48, num_sms=152) > 0   # G = 16
+
+
+def test_suffix_capacity_and_host_append():
+    wl = W.make_config("llama3_8b", B=5, prefix=48, seed=3)
+    cap = 300
+    w2 = W.with_suffix_capacity(wl, cap, seed=3)
+    ps = wl.page_size
+    last = w2.levels[-1]
+    ids = last.page_ids.tolist()
+    per = (cap + ps - 1) // ps
+    assert len(ids) == wl.B * per and len(set(ids)) == len(ids)
+    shared_ids = set(w2.levels[0].page_ids.tolist())
+    assert not shared_ids & set(ids)
+    # the visible keys are unchanged
+    for a, b in zip(wl.levels[-1].nodes.tolist(), last.nodes.tolist()):
+        assert a[2] == b[2]
+        npg = (a[2] + ps - 1) // ps
+        old = wl.levels[-1].page_ids[a[3]:a[3] + npg]
+        assert torch.equal(wl.k_pool[old], w2.k_pool[last.page_ids[b[3]:b[3] + npg]])
+    (q, k, v), = W.decode_tokens(w2, 1, seed=3)
+    before = last.nodes[:, 2].clone()
+    W.append_token(w2, k, v)
+    assert torch.equal(last.nodes[:, 2], before + 1)
+    for b in range(wl.B):
+        t = int(before[b])
+        page = ids[int(last.nodes[b, 3]) + t // ps]
+        assert torch.equal(w2.k_pool[page, :, t % ps], k[b]) and torch.equal(w2.v_pool[page, :, t % ps], v[b])
