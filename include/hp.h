@@ -318,6 +318,20 @@ hp_status hp_cascade_decode_loop(const void *plan_dev, const hp_plan_info *info,
                                  hp_dtype out_dt, int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb,
                                  void *ws, size_t ws_bytes, hp_stream_t stream);
 
+/* hp_cascade_append_kv followed by hp_cascade_decode_loop, in the two
+ * launches of one step: the persistent kernel writes each sequence's new
+ * token (k_new, v_new as in hp_cascade_append_kv) into its suffix pages just
+ * before it loads that chunk, and attends over the first suffix_len[b] + 1
+ * suffix tokens; the merge kernel then advances suffix_len[b] by one.  The
+ * results, the pools and the lengths equal those of the two separate calls.
+ * A length outside [0, capacity) sets HP_ERR_BOUNDS, writes nothing for
+ * that sequence and keeps its length. */
+hp_status hp_cascade_decode_append(const void *plan_dev, const hp_plan_info *info, int32_t *suffix_len,
+                                   const void *k_new, const void *v_new, int64_t kv_sb, int64_t kv_sh,
+                                   const void *q, int64_t q_sb, int64_t q_sh, float scale, void *out,
+                                   hp_dtype out_dt, int64_t o_sb, int64_t o_sh, float *lse,
+                                   int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream);
+
 /* Host-side description of a plan for inspection and tests: the (level, node,
  * seq_begin, seq_end, pass) context list in the order the pages list it --
  * shared nodes (more than one sequence; batched pass = 1) level by level,

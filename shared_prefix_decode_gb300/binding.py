@@ -76,6 +76,9 @@ _SIGNATURES = {
                                      c_sz, c_vp]),
     "hp_cascade_decode_loop": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_vp, c_i64, c_i64, c_f32, c_vp,
                                        c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz, c_vp]),
+    "hp_cascade_decode_append": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_vp, c_vp, c_i64, c_i64, c_vp,
+                                         c_i64, c_i64, c_f32, c_vp, c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz,
+                                         c_vp]),
     "hp_cascade_contexts": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i32), c_i32]),
     "hp_cascade_plan_stats": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i64)]),
     "hp_read_device_status": (c_i32, [c_vp, c_vp]),
@@ -400,21 +403,31 @@ class LoopPlan(CascadePlan):
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
         hp_cascade_append_kv(self, k_new, v_new, stream=stream)
 
+    def decode_append(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, scale: float,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      out_dtype=torch.bfloat16, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        return hp_cascade_decode_append(self, q, k_new, v_new, scale, out=out, lse=lse, out_dtype=out_dtype,
+                                        stream=stream)
+
     def decode(self, q: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
                lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
                out_dtype=torch.bfloat16, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
         return hp_cascade_decode_loop(self, q, scale, out=out, lse=lse, ws=ws, out_dtype=out_dtype, stream=stream)
 
 
-def hp_cascade_append_kv(plan: LoopPlan, k_new: torch.Tensor, v_new: torch.Tensor, ws: Optional[torch.Tensor] = None,
-                         stream=None) -> None:
-    """One token per sequence: k_new / v_new bf16 [B][Hkv][d] (head dimension
-    contiguous) go to position plan.suffix_len[b] of each suffix."""
+def _check_token_rows(plan, k_new: torch.Tensor, v_new: torch.Tensor):
     shape = (plan.B, plan.Hkv, plan.d)
     for t, nm in ((k_new, "k_new"), (v_new, "v_new")):
         _need(tuple(t.shape) == shape and t.dtype == torch.bfloat16 and t.is_cuda and t.stride(2) == 1,
               f"{nm} must be bf16 [B][Hkv][d] on the GPU, d contiguous")
     _need(k_new.stride() == v_new.stride(), "k_new and v_new must have the same strides")
+
+
+def hp_cascade_append_kv(plan: LoopPlan, k_new: torch.Tensor, v_new: torch.Tensor, ws: Optional[torch.Tensor] = None,
+                         stream=None) -> None:
+    """One token per sequence: k_new / v_new bf16 [B][Hkv][d] (head dimension
+    contiguous) go to position plan.suffix_len[b] of each suffix."""
+    _check_token_rows(plan, k_new, v_new)
     ws = plan.ws if ws is None else ws
     _need(ws is not None and ws.dtype == torch.uint8 and ws.is_cuda, "workspace must be a uint8 GPU tensor")
     _check(library().hp_cascade_append_kv(
@@ -441,6 +454,28 @@ def hp_cascade_decode_loop(plan: LoopPlan, q: torch.Tensor, scale: float, out: O
         _ptr(plan.plan), ctypes.byref(plan.info), _ptr(lens), _ptr(q), q.stride(0), q.stride(1), float(scale),
         _ptr(out), _dt(out.dtype), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(),
         _stream(stream)), "hp_cascade_decode_loop")
+    return out, lse
+
+
+def hp_cascade_decode_append(plan: LoopPlan, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                             scale: float, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                             ws: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                             stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Append and decode in one step's two launches (plan.suffix_len advances)."""
+    B, Hq, d = q.shape
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = plan.ws
+    _check_token_rows(plan, k_new, v_new)
+    _check_step_tensors(plan, q, out, lse, ws)
+    lens = plan.suffix_len
+    _check(library().hp_cascade_decode_append(
+        _ptr(plan.plan), ctypes.byref(plan.info), _ptr(lens), _ptr(k_new), _ptr(v_new), k_new.stride(0),
+        k_new.stride(1), _ptr(q), q.stride(0), q.stride(1), float(scale), _ptr(out), _dt(out.dtype), out.stride(0),
+        out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(), _stream(stream)), "hp_cascade_decode_append")
     return out, lse
 
 

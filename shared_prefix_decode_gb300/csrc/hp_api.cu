@@ -1064,7 +1064,8 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
                                      int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,
                                      int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
                                      size_t ws_bytes, hp_stream_t stream, void *const *events,
-                                     const int32_t *suffix_len = nullptr)
+                                     const int32_t *suffix_len = nullptr, const void *k_new = nullptr,
+                                     const void *v_new = nullptr, int64_t kv_sb = 0, int64_t kv_sh = 0)
 {
     auto mark = [&](int i) {
         if (events && events[i])
@@ -1087,6 +1088,9 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
     // a decode-loop plan runs with the current suffix lengths, a plain plan without
     if ((ext.loop_capacity > 0) != (suffix_len != nullptr) || (suffix_len && !aligned(suffix_len, 4)))
         return HP_ERR_ARG;
+    if (k_new && (!v_new || !aligned(k_new, 16) || !aligned(v_new, 16) || kv_sb <= 0 || kv_sh <= 0 || kv_sb % 8 ||
+                  kv_sh % 8))
+        return HP_ERR_UNSUPPORTED;
     if (ws_bytes < (size_t)info->ws_bytes || !aligned(ws, 256))
         return HP_ERR_WORKSPACE;
     const WsLayout wl = ws_layout(info->n_part_rows, info->d);
@@ -1128,6 +1132,14 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         cp.withhold = wh != nullptr && wh[0] == '1';
         cp.suffix_len = suffix_len;
         cp.loop_capacity = ext.loop_capacity;
+        cp.k_new = static_cast<const uint16_t *>(k_new);
+        cp.v_new = static_cast<const uint16_t *>(v_new);
+        cp.kv_sb = kv_sb;
+        cp.kv_sh = kv_sh;
+        cp.loop_k_pool = static_cast<uint16_t *>(ext.k_pool);
+        cp.loop_v_pool = static_cast<uint16_t *>(ext.v_pool);
+        cp.Hkv = info->Hkv;
+        cp.d = info->d;
         if (launch_cascade(cp, info->grid, info->d, s) != cudaSuccess)
             return HP_ERR_CUDA;
     }
@@ -1153,6 +1165,10 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
     mp.lse = lse;
     mp.lse_sb = lse_sb;
     mp.status = status_ptr(ws);
+    if (k_new) {
+        mp.len_inc = const_cast<int32_t *>(suffix_len);
+        mp.len_capacity = ext.loop_capacity;
+    }
     // the merge overlaps its launch with the fused kernel's tail unless an
     // event was recorded in between
     const bool dependent = !(events && events[1]);
@@ -1180,6 +1196,18 @@ hp_status hp_cascade_decode_loop(const void *plan_dev, const hp_plan_info *info,
         return HP_ERR_ARG;
     return cascade_decode_impl(plan_dev, info, q, q_sb, q_sh, scale, out, out_dt, o_sb, o_sh, lse, lse_sb, ws,
                                ws_bytes, stream, nullptr, suffix_len);
+}
+
+hp_status hp_cascade_decode_append(const void *plan_dev, const hp_plan_info *info, int32_t *suffix_len,
+                                   const void *k_new, const void *v_new, int64_t kv_sb, int64_t kv_sh, const void *q,
+                                   int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt, int64_t o_sb,
+                                   int64_t o_sh, float *lse, int64_t lse_sb, void *ws, size_t ws_bytes,
+                                   hp_stream_t stream)
+{
+    if (!suffix_len || !k_new || !v_new)
+        return HP_ERR_ARG;
+    return cascade_decode_impl(plan_dev, info, q, q_sb, q_sh, scale, out, out_dt, o_sb, o_sh, lse, lse_sb, ws,
+                               ws_bytes, stream, nullptr, suffix_len, k_new, v_new, kv_sb, kv_sh);
 }
 
 hp_status hp_cascade_append_kv(const void *plan_dev, const hp_plan_info *info, const void *k_new, const void *v_new,

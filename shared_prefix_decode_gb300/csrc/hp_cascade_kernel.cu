@@ -82,11 +82,23 @@ __device__ __forceinline__ tcr::ItemGeo tc_geo(const CascadeParams &p, const Rec
 // which is the capacity for the suffix's last item).  A length that leaves
 // the item empty or passes the capacity is reported; the item then keeps one
 // key, inside its reserved pages, so the step stays in bounds.
+// Loop: the decode-loop instantiation (lengths on the device, the append
+// possibly fused); the static step's instantiation carries none of that code.
+template <bool Loop>
 struct RecordItems {
+    static constexpr bool kPrefetch = Loop, kTokens = Loop;
     const CascadeParams *p;
     const RecItem *items;  // the record's paged items
     const int32_t *pages;  // the record's page list
-    __device__ smr::Desc operator()(int k) const
+    // a suffix item's current length (decode loops), loaded ahead
+    __device__ int prefetch(int k) const
+    {
+        if (!Loop || k < 0 || p->suffix_len == nullptr)
+            return 0;
+        const int s = items[k].len_seq;
+        return s >= 0 ? p->suffix_len[s] : 0;
+    }
+    __device__ smr::Desc operator()(int k, int pre_len) const
     {
         const RecItem w = items[k];
         smr::Desc d;
@@ -95,12 +107,27 @@ struct RecordItems {
         d.kvh0 = w.kvh;
         d.k0 = w.k0;
         d.k1 = w.k1;
-        if (w.len_seq >= 0 && p->suffix_len) {
-            const int len = p->suffix_len[w.len_seq];
-            d.k1 = min(w.k1, len);
-            if (d.k1 <= w.k0 || len > p->loop_capacity) {
+        if (Loop && w.len_seq >= 0 && p->suffix_len) {
+            const int len = pre_len;
+            // with the append fused, the step's own token is key `len`
+            const bool app = p->k_new != nullptr && len >= 0 && len < p->loop_capacity;
+            const int n = app ? len + 1 : len;
+            d.k1 = min(w.k1, n);
+            if (d.k1 <= w.k0 || n > p->loop_capacity || (p->k_new != nullptr && !app)) {
                 atomicOr(p->status, kStBounds);
                 d.k1 = max(d.k1, w.k0 + 1);
+            }
+            if (app && len >= w.k0 && len < w.k1) {
+                const int pid = pages[w.page_off + len / w.ps - w.k0 / w.ps];
+                if ((unsigned)pid < (unsigned)w.num_pages) {
+                    const int64_t dst = (((int64_t)pid * p->Hkv + w.kvh) * w.ps + len % w.ps) * (int64_t)p->d;
+                    d.tok_k_src = p->k_new + (int64_t)w.len_seq * p->kv_sb + (int64_t)w.kvh * p->kv_sh;
+                    d.tok_v_src = p->v_new + (int64_t)w.len_seq * p->kv_sb + (int64_t)w.kvh * p->kv_sh;
+                    d.tok_k_dst = p->loop_k_pool + dst;
+                    d.tok_v_dst = p->loop_v_pool + dst;
+                    d.tok_src_sh = p->kv_sh;
+                    d.tok_dst_sh = (int64_t)w.ps * p->d;
+                }
             }
         }
         d.part_row = w.part_row;
@@ -115,7 +142,7 @@ struct RecordItems {
     }
 };
 
-template <int D>
+template <int D, bool Loop>
 __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_constant__ CascadeParams p)
 {
     using FL = FusedLayout<D>;
@@ -239,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
         // (a CTA without paged items skips the role: its code is not fetched
         // at the end of the step's longest chain)
         if (warp == 0 && n_small > 0)
-            smr::producer<D, kNC, kSmallStages, kQRows>(sc, sa, RecordItems{&p, items + n_tc, pages}, n_small, lane);
+            smr::producer<D, kNC, kSmallStages, kQRows>(sc, sa, RecordItems<Loop>{&p, items + n_tc, pages}, n_small, lane);
         if (warp == 1) {
             tc_fence_after();
             tmem_dealloc(tmem, 512);
@@ -263,19 +290,19 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
     __syncwarp();
 }
 
-template <int D>
+template <int D, bool Loop>
 cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
 {
-    static bool configured = false;
+    static bool configured = false;  // per instantiation
     const int bytes = FusedLayout<D>::kBytes + 1024;
     static_assert(FusedLayout<D>::kBytes + 1024 <= 227 * 1024, "shared memory per CTA");
     if (!configured) {
         cudaError_t e =
-            cudaFuncSetAttribute(hp_cascade_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            cudaFuncSetAttribute(hp_cascade_kernel<D, Loop>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess)
             return e;
         cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, hp_cascade_kernel<D>)) != cudaSuccess)
+        if ((e = cudaFuncGetAttributes(&fa, hp_cascade_kernel<D, Loop>)) != cudaSuccess)
             return e;
         if (fa.numRegs != (int)tcr::kRegsLaunch)
             return cudaErrorInvalidConfiguration;  // the register split assumes this allocation
@@ -294,7 +321,7 @@ cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, hp_cascade_kernel<D>, p);
+    return cudaLaunchKernelEx(&cfg, hp_cascade_kernel<D, Loop>, p);
 }
 
 }  // namespace
@@ -310,7 +337,9 @@ cudaError_t launch_cascade(const CascadeParams &p, int grid, int d, cudaStream_t
 {
     if (grid <= 0)
         return cudaSuccess;
-    return d == 64 ? launch_cascade_d<64>(p, grid, s) : launch_cascade_d<128>(p, grid, s);
+    if (p.suffix_len != nullptr)
+        return d == 64 ? launch_cascade_d<64, true>(p, grid, s) : launch_cascade_d<128, true>(p, grid, s);
+    return d == 64 ? launch_cascade_d<64, false>(p, grid, s) : launch_cascade_d<128, false>(p, grid, s);
 }
 
 }  // namespace hp

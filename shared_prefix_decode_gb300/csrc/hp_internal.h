@@ -168,6 +168,16 @@ struct CascadeParams {
     // decode-loop plans: suffix item ends come from suffix_len[len_seq]
     const int32_t *suffix_len;
     int32_t loop_capacity;
+    // the append fused into the step (k_new != null): the suffix of sequence
+    // b also holds the token k_new / v_new[b] at position suffix_len[b], which
+    // the paged producer writes into the suffix pools (bf16
+    // [num_pages][Hkv][ps][d]) before it loads that chunk
+    const uint16_t *k_new;
+    const uint16_t *v_new;
+    int64_t kv_sb, kv_sh;
+    uint16_t *loop_k_pool;
+    uint16_t *loop_v_pool;
+    int32_t Hkv, d;
 };
 
 // Decode-loop append: one token per sequence into its suffix pages.
@@ -206,6 +216,10 @@ struct MergeParams {
     float *lse;
     int64_t lse_sb;
     uint32_t *status;
+    // the append fused into the step: after the partial states are complete,
+    // suffix_len[b] < len_capacity moves on by one (row (b, 0) does it)
+    int32_t *len_inc;
+    int32_t len_capacity;
 };
 
 template <typename T>

@@ -97,6 +97,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const __grid
     }
     if (p.wait_prior)
         asm volatile("griddepcontrol.wait;" ::: "memory");  // the partial states are complete
+    if (p.len_inc != nullptr && h == 0 && lane == 0) {
+        // the step appended its token: the suffix is one longer from now on
+        const int len = p.len_inc[L.b];
+        if (len >= 0 && len < p.len_capacity)
+            p.len_inc[L.b] = len + 1;
+    }
     const size_t esz = p.out_f32 ? 4 : 2;
     mrg::RowOut o;
     o.out = static_cast<uint8_t *>(p.out) + ((int64_t)L.b * p.o_sb + (int64_t)h * p.o_sh) * esz;

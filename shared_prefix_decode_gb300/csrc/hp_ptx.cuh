@@ -101,6 +101,13 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// This thread's generic-proxy writes to global memory, ordered before
+// async-proxy (TMA) reads issued after it (and, with a warp or CTA barrier,
+// after it by other threads).
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 __device__ __forceinline__ void prefetch_tensormap(const void *map)
 {

@@ -31,7 +31,9 @@ struct SmallKernelLayout {
 struct TableItems {
     const SmallParams *p;
     int first, stride;
-    __device__ smr::Desc operator()(int k) const
+    static constexpr bool kPrefetch = false, kTokens = false;
+    __device__ int prefetch(int) const { return 0; }
+    __device__ smr::Desc operator()(int k, int) const
     {
         const int idx = first + k * stride;
         smr::Desc d;

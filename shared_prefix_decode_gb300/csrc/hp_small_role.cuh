@@ -68,6 +68,17 @@ struct Desc {
     int ps, num_pages;
     const void *map_k;
     const void *map_v;
+    // A decode step with the append fused: the item holds the step's new
+    // token (its last key).  The producer copies the token's K and V rows of
+    // the item's nh heads (head h at src + h * src_sh) to the pool (head h
+    // at dst + h * dst_sh) before it loads the item's last chunk.  Null: no
+    // token to write.
+    const uint16_t *tok_k_src = nullptr;
+    const uint16_t *tok_v_src = nullptr;
+    uint16_t *tok_k_dst = nullptr;
+    uint16_t *tok_v_dst = nullptr;
+    int64_t tok_src_sh = 0;
+    int64_t tok_dst_sh = 0;
 };
 
 struct Ctx {
@@ -91,10 +102,12 @@ struct Args {
     float *part_lse;
 };
 
-// Producer warp: walks items k = 0, 1, ... of `src` (src(k) -> Desc, with
-// n_items entries), then closes the ring with a sentinel stage (n_seq = -1,
-// completed by a plain arrival) that tells the consumers to stop.  All 32
-// lanes call it.
+// Producer warp: walks items k = 0, 1, ... of `src` (src(k, pre) -> Desc,
+// with n_items entries; pre = src.prefetch(k), loaded for 32 items at a time,
+// one per lane, so that a value an item needs from global memory is not a
+// dependent load at the item's start), then closes the ring with a sentinel
+// stage (n_seq = -1, completed by a plain arrival) that tells the consumers
+// to stop.  All 32 lanes call it.
 template <int D, int NC, int S, int QR, class Src>
 __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src &src, int n_items, int lane)
 {
@@ -106,10 +119,29 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
     uint32_t k = 0;  // chunks issued
     bool ok = true;
     bool prefetched = false;
+    int pre = 0;
     for (int it = 0; ok && it < n_items; ++it) {
-        const Desc d = src(it);
+        if (Src::kPrefetch && (it & 31) == 0)
+            pre = src.prefetch(it + lane < n_items ? it + lane : -1);
+        const Desc d = src(it, Src::kPrefetch ? __shfl_sync(0xffffffffu, pre, it & 31) : 0);
         if (!d.valid)
             continue;
+        // the step's new token (a decode step with the append fused): its K
+        // and V rows are loaded now and stored before the item's last chunk
+        constexpr int kPer = D / 8;  // 16-byte pieces of one head's row
+        constexpr int kTokRegs = Src::kTokens ? (2 * 8 * kPer + 31) / 32 : 1;  // nh <= 8
+        uint4 tok[kTokRegs];
+        const int ntok = Src::kTokens && d.tok_k_dst != nullptr ? 2 * a.nh * kPer : 0;
+#pragma unroll
+        for (int r = 0; r < kTokRegs; ++r) {
+            const int i = lane + 32 * r;
+            if (i < ntok) {
+                const bool is_v = i >= ntok / 2;
+                const int j = is_v ? i - ntok / 2 : i;
+                tok[r] = *reinterpret_cast<const uint4 *>((is_v ? d.tok_v_src : d.tok_k_src) +
+                                                          (j / kPer) * d.tok_src_sh + (j % kPer) * 8);
+            }
+        }
         if (!prefetched && lane == 0) {
             prefetch_tensormap(d.map_k);
             prefetch_tensormap(d.map_v);
@@ -132,6 +164,23 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 page = d.num_pages;  // zero-filled boxes, chunk masked
             const int t = d.k0 + ch * kChunk;
             const uint32_t bar = c.full0 + 8 * st;
+            if (Src::kTokens && ntok > 0 && ch + 1 == nchunks) {
+                // the new token, in this chunk: its rows go to the pool first,
+                // visible to the copy below (generic writes, proxy fence, warp
+                // barrier, then the TMA issue)
+#pragma unroll
+                for (int r = 0; r < kTokRegs; ++r) {
+                    const int i = lane + 32 * r;
+                    if (i < ntok) {
+                        const bool is_v = i >= ntok / 2;
+                        const int j = is_v ? i - ntok / 2 : i;
+                        *reinterpret_cast<uint4 *>((is_v ? d.tok_v_dst : d.tok_k_dst) + (j / kPer) * d.tok_dst_sh +
+                                                   (j % kPer) * 8) = tok[r];
+                    }
+                }
+                fence_proxy_async_global();
+                __syncwarp();
+            }
             if (lane == 0) {
                 if (oob)
                     atomicOr(c.status, kStBounds);

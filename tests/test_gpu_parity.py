@@ -550,6 +550,19 @@ def test_decode_loop_as_one_graph():
         assert torch.equal(og, oe) and torch.equal(lg, le)
         assert torch.equal(plan.suffix_len, n0 + steps)
     _status_ok(plan.ws)
+    # the same loop with the append fused into each step, as one graph
+    gf = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gf):
+        for s in range(steps):
+            plan.decode_append(qs[s], ks[s], vs[s], host.scale, out=og[s], lse=lg[s])
+    for _ in range(2):
+        reset()
+        og.zero_()
+        gf.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(og, oe) and torch.equal(lg, le)
+        assert torch.equal(plan.suffix_len, n0 + steps)
+    _status_ok(plan.ws)
 
 
 def test_decode_loop_length_errors_are_reported():
@@ -576,6 +589,16 @@ def test_decode_loop_length_errors_are_reported():
     assert len(changed) == 3  # one page for each of the other three sequences
     plan.decode(q, host.scale)  # length == capacity is valid
     _status_ok(plan.ws)
+    # the fused step at the capacity: nothing written for that sequence, its
+    # length kept, the others appended
+    kp = dev.k_pool.clone()
+    before = plan.suffix_len.clone()
+    plan.decode_append(q, k, v, host.scale)
+    torch.cuda.synchronize()
+    assert hb.hp_read_device_status(plan.ws) == hb.HP_ERR_BOUNDS
+    n = plan.suffix_len.cpu()
+    assert n[1] == cap and torch.equal(n[[0, 2, 3]], before.cpu()[[0, 2, 3]] + 1)
+    assert len((dev.k_pool != kp).flatten(1).any(1).nonzero()) == 3
     low = plan.suffix_len.clone()
     low[2] = 0
     hb.hp_cascade_decode_loop(plan, q, host.scale, suffix_len=low)
@@ -591,3 +614,38 @@ def test_decode_loop_length_errors_are_reported():
         hb.hp_cascade_append_kv(static, k, v)
     torch.cuda.synchronize()
     assert hb.hp_read_device_status(plan.ws) == hb.HP_OK
+
+
+@pytest.mark.parametrize("name,kw,steps", [
+    ("llama3_8b", dict(B=8, prefix=512), 24),
+    ("tree2", dict(B=16, prefix=128), 12),
+    ("tiny", {}, 16),
+    ("edges", {}, 34),
+])
+def test_decode_loop_fused_append_equals_separate_calls(name, kw, steps):
+    """hp_cascade_decode_append (the token written by the persistent kernel,
+    the length advanced by the merge) against hp_cascade_append_kv +
+    hp_cascade_decode_loop on a second copy of the same tree: every step's
+    results bit for bit, and the pools and lengths at the end; every eighth
+    step also against the oracle."""
+    host, cap = _loop_host(name, kw, steps, seed=7)
+    da, db = host.to(DEV), host.to(DEV)
+    pa = hb.LoopPlan.from_workload(da, cap)
+    pb = hb.LoopPlan.from_workload(db, cap)
+    for s, (q, k, v) in enumerate(W.decode_tokens(host, steps, seed=7)):
+        qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+        pa.append(kd, vd)
+        oa, la = pa.decode(qd, host.scale, out_dtype=torch.float32)
+        ob, lb = pb.decode_append(qd, kd, vd, host.scale, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob) and torch.equal(la, lb), f"step {s}"
+        W.append_token(host, k, v)
+        if s % 8 == 7 or s == steps - 1:
+            host.q = q
+            O, L = oracle.cascade(host)
+            _check(ob, lb, O, L, f"fused decode loop {name} step {s}")
+    _status_ok(pa.ws)
+    _status_ok(pb.ws)
+    assert torch.equal(pa.suffix_len, pb.suffix_len)
+    assert torch.equal(pb.suffix_len.cpu(), host.levels[-1].nodes[:, 2])
+    assert torch.equal(da.k_pool, db.k_pool) and torch.equal(da.v_pool, db.v_pool)
