@@ -20,6 +20,11 @@ it.  Each wrapper names the passage it follows:
 * ``paged_decode``   - per-sequence attention through a page table.
 * ``prefix``         - attention of a batch of queries against one contiguous
                        prefix laid out [len][Hkv][d].
+* ``stream_visible`` / ``stream_masked`` - the Parallel Prompting stream mask
+                       (Read Once, Answer Many, Section 3, Eq. 2): one KV row
+                       per request holding the document and every stream's
+                       interleaved tokens; a query of stream s sees the
+                       document and stream s's own earlier slots.
 """
 from __future__ import annotations
 
@@ -195,6 +200,38 @@ def cascade(wl, rows: Optional[Sequence[Sequence[int]]] = None):
                          _ptr(rows_np, _i32p), _ptr(O, _dp), _ptr(L, _dp))
     if rc != 0:
         raise ValueError(f"hpo_cascade rejected its arguments ({rc})")
+    return O, L
+
+
+def stream_visible(q_sid, q_pos, slot_sid, slot_pos) -> np.ndarray:
+    """Read Once, Answer Many, Section 3, Eq. 2: a query of stream q_sid at
+    position q_pos may attend to a slot iff the slot is not after it (causal
+    over positions; streams share positions) and the slot belongs to the
+    document (sid -1) or to the query's own stream.  Returns the [nq, nk]
+    boolean mask."""
+    q_sid = np.asarray(q_sid).reshape(-1, 1)
+    q_pos = np.asarray(q_pos).reshape(-1, 1)
+    slot_sid = np.asarray(slot_sid).reshape(1, -1)
+    slot_pos = np.asarray(slot_pos).reshape(1, -1)
+    causal = slot_pos <= q_pos
+    same = (slot_sid == -1) | (slot_sid == q_sid)
+    return causal & same
+
+
+def stream_masked(Q, K, V, q_sid, q_pos, slot_sid, slot_pos, scale: float):
+    """Attention of query rows Q [nq, d] over one request's KV row K, V
+    [nk, d] under the stream mask (``stream_visible``): each row is SDP over
+    its visible slots (``sdp``).  Returns (O [nq, d], lse [nq]); a row with
+    no visible slot gets (0, -inf)."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    vis = stream_visible(q_sid, q_pos, slot_sid, slot_pos)
+    O = np.zeros((Q.shape[0], Q.shape[1]))
+    L = np.full(Q.shape[0], -np.inf)
+    for i in range(Q.shape[0]):
+        idx = np.nonzero(vis[i])[0]
+        if idx.size:
+            o, l = sdp(Q[i:i + 1], K[idx], V[idx], scale)
+            O[i], L[i] = o[0], l[0]
     return O, L
 
 

@@ -42,6 +42,9 @@ __all__ = [
     "with_suffix_capacity",
     "append_token",
     "decode_tokens",
+    "StreamRequests",
+    "stream_requests",
+    "streams_as_tree",
 ]
 
 
@@ -330,6 +333,106 @@ def append_token(wl: CascadeWorkload, k_new: torch.Tensor, v_new: torch.Tensor) 
         wl.k_pool[page, :, kl % ps, :] = k_new[b].cpu()
         wl.v_pool[page, :, kl % ps, :] = v_new[b].cpu()
         last.nodes[b, 2] = kl + 1
+
+
+# ------------------------------------------------- parallel prompting layout
+@dataclass
+class StreamRequests:
+    """Requests in the Parallel Prompting layout (Read Once, Answer Many,
+    Section 3): one KV row per request holding the document, then the P
+    streams' questions one after another, then the answer tokens interleaved
+    by step (step 1 of streams 0..P-1, then step 2, ...).  Slot ids: -1 for
+    the document, s for stream s's question and answers.  Positions: the
+    document's run from 0; every stream's start right after the document.
+
+    ``rows[r]`` = (slot_sid [nk], slot_pos [nk], K [nk, Hkv, d], V [nk, Hkv, d])
+    for request r; ``q`` [R*P, Hq, d] the step's queries, stream s of request
+    r being sequence r*P + s (the newest answer token of each stream, at
+    ``q_pos``).
+    """
+
+    R: int
+    P: int
+    Hq: int
+    Hkv: int
+    d: int
+    doc_len: int
+    q_lens: List[List[int]]
+    T: int
+    scale: float
+    rows: list
+    q: torch.Tensor
+    q_pos: List[int]
+
+
+def stream_requests(R: int, P: int, Hq: int, Hkv: int, d: int, doc_len: int, q_len_range: Tuple[int, int],
+                    T: int, seed: int = 0) -> StreamRequests:
+    """Seeded requests at decode step T (T >= 1 answer tokens per stream, the
+    last one being the step's new token).  Question lengths are drawn from
+    ``q_len_range`` (inclusive), then K, V and q as N(0,1) rounded to bf16."""
+    g = torch.Generator().manual_seed(seed)
+    lo, hi = q_len_range
+    q_lens = [torch.randint(lo, hi + 1, (P,), generator=g).tolist() for _ in range(R)]
+    rows, q_pos = [], []
+    for r in range(R):
+        sid = [-1] * doc_len
+        pos = list(range(doc_len))
+        for s in range(P):
+            sid += [s] * q_lens[r][s]
+            pos += [doc_len + i for i in range(q_lens[r][s])]
+        for t in range(T):
+            for s in range(P):
+                sid.append(s)
+                pos.append(doc_len + q_lens[r][s] + t)
+        nk = len(sid)
+        k = torch.randn(nk, Hkv, d, generator=g).to(torch.bfloat16)
+        v = torch.randn(nk, Hkv, d, generator=g).to(torch.bfloat16)
+        rows.append((torch.tensor(sid, dtype=torch.int32), torch.tensor(pos, dtype=torch.int32), k, v))
+        q_pos += [doc_len + q_lens[r][s] + T - 1 for s in range(P)]
+    q = torch.randn(R * P, Hq, d, generator=g).to(torch.bfloat16)
+    return StreamRequests(R, P, Hq, Hkv, d, doc_len, q_lens, T, 1.0 / math.sqrt(d), rows, q, q_pos)
+
+
+def streams_as_tree(req: StreamRequests, page_size: int = 16) -> CascadeWorkload:
+    """The same requests as a prefix tree (the form the cascade path runs):
+    sequence r*P + s is stream s of request r; level 0 holds each request's
+    document as a node shared by its P streams, level 1 each stream's own
+    slots (question, then answers, in row order) as a private node.  Every
+    node starts on a fresh page; pages are laid out in node order."""
+    ps = page_size
+    pages_k, pages_v = [], []
+
+    def put(k, v):
+        first = len(pages_k)
+        n = k.shape[0]
+        for p0 in range(0, n, ps):
+            pk = torch.zeros(req.Hkv, ps, req.d, dtype=torch.bfloat16)
+            pv = torch.zeros(req.Hkv, ps, req.d, dtype=torch.bfloat16)
+            m = min(ps, n - p0)
+            pk[:, :m] = k[p0:p0 + m].transpose(0, 1)
+            pv[:, :m] = v[p0:p0 + m].transpose(0, 1)
+            pages_k.append(pk)
+            pages_v.append(pv)
+        return list(range(first, len(pages_k)))
+
+    doc_nodes, doc_ids, own_nodes, own_ids = [], [], [], []
+    for r, (sid, _, k, v) in enumerate(req.rows):
+        doc = (sid == -1).nonzero().flatten()
+        doc_nodes.append((r * req.P, (r + 1) * req.P, int(doc.numel()), len(doc_ids)))
+        doc_ids += put(k[doc], v[doc])
+        for s in range(req.P):
+            own = (sid == s).nonzero().flatten()
+            own_nodes.append((r * req.P + s, r * req.P + s + 1, int(own.numel()), len(own_ids)))
+            own_ids += put(k[own], v[own])
+    if not pages_k:
+        pages_k.append(torch.zeros(req.Hkv, ps, req.d, dtype=torch.bfloat16))
+        pages_v.append(torch.zeros(req.Hkv, ps, req.d, dtype=torch.bfloat16))
+    levels = [TreeLevel(torch.tensor(doc_nodes, dtype=torch.int32).reshape(-1, 4),
+                        torch.tensor(doc_ids, dtype=torch.int32)),
+              TreeLevel(torch.tensor(own_nodes, dtype=torch.int32).reshape(-1, 4),
+                        torch.tensor(own_ids, dtype=torch.int32))]
+    return CascadeWorkload("parallel_prompting", req.R * req.P, req.Hq, req.Hkv, req.d, ps, req.scale,
+                           req.q.clone(), torch.stack(pages_k), torch.stack(pages_v), levels, 0)
 
 
 def _probe_code(b: int, d: int) -> torch.Tensor:

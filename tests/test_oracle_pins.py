@@ -385,3 +385,84 @@ def test_pins_catch_planted_oracle_mistake(name, tmp_path):
         return  # the mutant crashed: caught
     line = [l for l in r.stdout.splitlines() if l.startswith("FAILED_PINS")][-1]
     assert int(line.split()[1]) > 0, f"planted mistake {name!r} passed every pin"
+
+
+# ------------------------------------------------ parallel prompting layout
+def test_parallel_prompting_fig2_mask():
+    """The worked example printed as Figure 2 of Read Once, Answer Many: a
+    3-token document, 3 streams with 1-token questions, decode step 2.  The
+    layout generator reproduces the figure's slot ids and positions, and the
+    oracle's Eq. 2 mask gives the new token of stream 1 exactly the slots the
+    figure marks visible."""
+    g = json.load(open(os.path.join(GOLDEN, "parallel_prompting_fig2_mask.json")))
+    req = W.stream_requests(R=1, P=g["request"]["streams"], Hq=1, Hkv=1, d=8,
+                            doc_len=g["request"]["document_tokens"],
+                            q_len_range=(g["request"]["question_tokens_per_stream"],) * 2,
+                            T=g["request"]["decode_step"], seed=0)
+    sid, pos, _, _ = req.rows[0]
+    assert sid.tolist() == g["slot_sid"] and pos.tolist() == g["position"]
+    qy = g["query"]
+    assert req.q_pos[qy["sid"]] == qy["position"]
+    vis = oracle.stream_visible([qy["sid"]], [qy["position"]], g["slot_sid"], g["position"])[0]
+    assert [g["slots"][i] for i in np.nonzero(vis)[0]] == g["visible_to_query"]
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_stream_mask_equals_its_cascade_form(seed):
+    """Each stream of a Parallel Prompting request sees the document plus its
+    own question and answers (Eq. 2), which is the prefix tree of one shared
+    document node and one private node per stream: the oracle of the masked
+    row equals the oracle of that tree, row by row (documents of 37 and 300
+    tokens, up to 5 streams with questions of 1-4 tokens, 3 answer steps)."""
+    req = W.stream_requests(R=2, P=5, Hq=4, Hkv=2, d=32, doc_len=37 if seed == 0 else 300,
+                            q_len_range=(1, 4), T=3, seed=seed)
+    wl = W.streams_as_tree(req, page_size=16)
+    O, L = oracle.cascade(wl)
+    G = req.Hq // req.Hkv
+    q = req.q.double().numpy()
+    row = 0
+    for r in range(req.R):
+        sid, pos, k, v = req.rows[r]
+        for s in range(req.P):
+            b = r * req.P + s
+            for h in range(req.Hq):
+                Om, Lm = oracle.stream_masked(q[b, h][None], k[:, h // G].double().numpy(),
+                                              v[:, h // G].double().numpy(), [s], [req.q_pos[b]],
+                                              sid.numpy(), pos.numpy(), req.scale)
+                np.testing.assert_allclose(O[row], Om[0], atol=1e-12)
+                assert L[row] == pytest.approx(Lm[0], abs=1e-12)
+                row += 1
+    # another stream's slots are never visible
+    vis = oracle.stream_visible([0, 1], [req.q_pos[0], req.q_pos[1]], req.rows[0][0].numpy(),
+                                req.rows[0][1].numpy())
+    assert not (vis[0] & (req.rows[0][0].numpy() == 1)).any()
+    assert not (vis[1] & (req.rows[0][0].numpy() == 0)).any()
+
+
+_STREAM_MUTANTS = {
+    "causal_strict": ("causal = slot_pos <= q_pos", "causal = slot_pos < q_pos"),
+    "document_hidden": ("same = (slot_sid == -1) | (slot_sid == q_sid)", "same = slot_sid == q_sid"),
+    "streams_unmasked": ("return causal & same", "return causal"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(_STREAM_MUTANTS))
+def test_stream_pins_catch_planted_mask_mistake(name, monkeypatch):
+    """Plant one mistake in the oracle's stream mask (a copy of its source,
+    loaded in place of the real one); the Figure 2 pin or the cascade-form
+    pin must fail."""
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(oracle.stream_visible))
+    old, new = _STREAM_MUTANTS[name]
+    assert old in src, f"mutation anchor for {name} not found"
+    ns = {"np": np}
+    exec(src.replace(old, new), ns)
+    monkeypatch.setattr(oracle, "stream_visible", ns["stream_visible"])
+    failed = 0
+    for pin in (test_parallel_prompting_fig2_mask, lambda: test_stream_mask_equals_its_cascade_form(0)):
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, f"planted mistake {name!r} passed every pin"
