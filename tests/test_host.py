@@ -246,3 +246,17 @@ def test_suffix_capacity_and_host_append():
         t = int(before[b])
         page = ids[int(last.nodes[b, 3]) + t // ps]
         assert torch.equal(w2.k_pool[page, :, t % ps], k[b]) and torch.equal(w2.v_pool[page, :, t % ps], v[b])
+
+
+def test_loop_binding_rejects_wrong_token_rows():
+    """The new token's K and V rows are checked before the library is called:
+    bf16 [B][Hkv][d], head dimension contiguous, on the GPU, equal strides."""
+    class Plan:
+        B, Hkv, d = 3, 2, 64
+
+    k = torch.zeros(3, 2, 64, dtype=torch.bfloat16)
+    for bad in (k.float(), k[:, :, ::2], k[:2], k):  # dtype, stride, shape, host memory
+        with pytest.raises(ValueError):
+            hb._check_token_rows(Plan, bad, bad)
+    with pytest.raises(ValueError):
+        hb.LoopPlan([], 1, 1, 1, 64, capacity=0)
