@@ -649,3 +649,27 @@ def test_decode_loop_fused_append_equals_separate_calls(name, kw, steps):
     assert torch.equal(pa.suffix_len, pb.suffix_len)
     assert torch.equal(pb.suffix_len.cpu(), host.levels[-1].nodes[:, 2])
     assert torch.equal(da.k_pool, db.k_pool) and torch.equal(da.v_pool, db.v_pool)
+
+
+def test_decode_loop_full_size_sampled():
+    """The benchmarked shape at full size (B=64, 32/8 heads, d=128, 4K shared
+    prefix, suffixes U[1,256]) as a decode loop: 8 fused steps, each checked
+    on 64 sampled rows against the oracle over the host-appended tree."""
+    steps = 8
+    host, cap = _loop_host("llama3_8b", {}, steps, seed=11)
+    dev = host.to(DEV)
+    plan = hb.LoopPlan.from_workload(dev, cap)
+    g = torch.Generator().manual_seed(11)
+    for s, (q, k, v) in enumerate(W.decode_tokens(host, steps, seed=11)):
+        out, lse = plan.decode_append(q.to(DEV), k.to(DEV), v.to(DEV), host.scale, out_dtype=torch.float32)
+        W.append_token(host, k, v)
+        host.q = q
+        bs = torch.randint(0, host.B, (64,), generator=g).tolist()
+        hs = torch.randint(0, host.Hq, (64,), generator=g).tolist()
+        rows = list(zip(bs, hs))
+        O, L = oracle.cascade(host, rows)
+        o = torch.stack([out[b, h] for b, h in rows])
+        l = torch.stack([lse[b, h] for b, h in rows])
+        _check(o, l, O, L, f"full-size decode loop step {s}")
+    _status_ok(plan.ws)
+    assert torch.equal(plan.suffix_len.cpu(), host.levels[-1].nodes[:, 2])
