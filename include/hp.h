@@ -344,6 +344,17 @@ int32_t hp_cascade_contexts(const hp_tree_desc *desc, int32_t *out, int32_t cap)
  * [1] small-row items, [2] partial rows, [3] merge entries.  -1 on error. */
 int32_t hp_cascade_plan_stats(const hp_tree_desc *desc, int64_t *stats4);
 
+/* The work items of the plan for a descriptor (capacity 0: hp_cascade_plan's;
+ * > 0: hp_cascade_loop_plan's), host only, for inspection and tests; no CUDA
+ * calls when desc->num_sms > 0.  Each item is 11 int32: level, first
+ * sequence, sequences, first KV head, KV heads, k0, k1 (node-relative keys
+ * [k0, k1)), first partial row, CTA of the persistent kernel, tensor-core
+ * role (1) or paged role (0), and the sequence whose length ends the item
+ * in a loop plan (-1 otherwise).  Items are listed CTA by CTA, in the order
+ * each CTA runs them.  Writes at most cap items into out (may be NULL);
+ * returns the item count, or -1 on an invalid descriptor. */
+int32_t hp_cascade_plan_items(const hp_tree_desc *desc, int32_t capacity, int32_t *out, int32_t cap);
+
 /* ---------------------------------------------------------------------------
  * Device status: reads and clears the status word of a workspace.  This call
  * synchronises `stream`.  Returns HP_OK, HP_ERR_BOUNDS, HP_ERR_DEVICE_TIMEOUT

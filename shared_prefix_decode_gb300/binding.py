@@ -81,6 +81,7 @@ _SIGNATURES = {
                                          c_vp]),
     "hp_cascade_contexts": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i32), c_i32]),
     "hp_cascade_plan_stats": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i64)]),
+    "hp_cascade_plan_items": (c_i32, [ctypes.POINTER(HpTreeDesc), c_i32, ctypes.POINTER(c_i32), c_i32]),
     "hp_read_device_status": (c_i32, [c_vp, c_vp]),
 }
 
@@ -281,6 +282,20 @@ def hp_cascade_plan_stats(levels, B, Hq, Hkv, d, num_sms: int = 152) -> Tuple[in
     if library().hp_cascade_plan_stats(ctypes.byref(D.desc), st) != 0:
         raise HpError(HP_ERR_ARG, "hp_cascade_plan_stats")
     return tuple(int(x) for x in st)
+
+
+PLAN_ITEM_FIELDS = ("level", "seq_begin", "n_seq", "kvh", "n_kvh", "k0", "k1", "part_row", "cta", "tc", "len_seq")
+
+
+def hp_cascade_plan_items(levels, B, Hq, Hkv, d, capacity: int = 0, num_sms: int = 152) -> List[dict]:
+    """The plan's work items (host only), CTA by CTA: dicts of PLAN_ITEM_FIELDS."""
+    D = _Desc(levels, B, Hq, Hkv, d, num_sms=num_sms)
+    n = library().hp_cascade_plan_items(ctypes.byref(D.desc), int(capacity), None, 0)
+    if n < 0:
+        raise HpError(HP_ERR_ARG, "hp_cascade_plan_items")
+    buf = (c_i32 * (11 * max(n, 1)))()
+    library().hp_cascade_plan_items(ctypes.byref(D.desc), int(capacity), buf, n)
+    return [dict(zip(PLAN_ITEM_FIELDS, buf[11 * i:11 * i + 11])) for i in range(n)]
 
 
 def hp_cascade_plan_bytes(levels, B, Hq, Hkv, d, num_sms: int = 0) -> int:

@@ -1280,6 +1280,33 @@ int32_t hp_cascade_plan_stats(const hp_tree_desc *desc, int64_t *stats4)
     return 0;
 }
 
+int32_t hp_cascade_plan_items(const hp_tree_desc *desc, int32_t capacity, int32_t *out, int32_t cap)
+{
+    HostPlan P;
+    if (capacity < 0 || build_plan(desc, P, false, capacity) != HP_OK)
+        return -1;
+    const int32_t n = (int32_t)(P.tc.size() + P.small.size());
+    if (!out)
+        return n;
+    int32_t k = 0;
+    auto put = [&](const WorkItem &w, int cta, int tc) {
+        if (k >= cap)
+            return;
+        int32_t *e = out + (size_t)k * 11;
+        const int32_t v[11] = {w.level, w.seq_begin, w.n_seq, w.kvh, tc ? 1 : P.hdr.small_nh, w.k0, w.k1,
+                               w.part_row, cta, tc, w.len_seq};
+        std::memcpy(e, v, sizeof(v));
+        ++k;
+    };
+    for (size_t c = 0; c < P.cta_tc.size(); ++c) {
+        for (int32_t id : P.cta_tc[c])
+            put(P.tc[id], (int)c, 1);
+        for (int32_t id : P.cta_small[c])
+            put(P.small[id], (int)c, 0);
+    }
+    return n;
+}
+
 hp_status hp_read_device_status(void *ws, hp_stream_t stream)
 {
     if (!ws)

@@ -260,3 +260,93 @@ def test_loop_binding_rejects_wrong_token_rows():
             hb._check_token_rows(Plan, bad, bad)
     with pytest.raises(ValueError):
         hb.LoopPlan([], 1, 1, 1, 64, capacity=0)
+
+
+# --------------------------------------------------- plan item invariants
+def _check_plan_items(wl, capacity=0, num_sms=152):
+    """Every key of every node is covered exactly once per (sequence, KV
+    head), each item sits in the role its node's query rows call for
+    (tensor cores above 16 rows), partial-row
+    ranges are disjoint and inside the plan's, and each CTA runs its
+    tensor-core items before its paged items."""
+    levels = hb._levels_of(wl)
+    items = hb.hp_cascade_plan_items(levels, wl.B, wl.Hq, wl.Hkv, wl.d, capacity=capacity, num_sms=num_sms)
+    n_tc, n_small, n_part, _ = hb.hp_cascade_plan_stats(levels, wl.B, wl.Hq, wl.Hkv, wl.d, num_sms=num_sms) \
+        if capacity == 0 else (None, None, None, None)
+    G = wl.G
+    last = len(wl.levels) - 1
+    cover = {}
+    spans = []
+    prev_cta, seen_paged = -1, False
+    for it in items:
+        assert 0 <= it["cta"] < num_sms
+        if it["cta"] != prev_cta:
+            prev_cta, seen_paged = it["cta"], False
+        node_rows = next((se - sb) * G for sb, se, _, _ in wl.levels[it["level"]].nodes.tolist()
+                         if sb <= it["seq_begin"] < se)
+        assert bool(it["tc"]) == (node_rows > 16), "role must follow the node's query rows"
+        if it["tc"]:
+            assert not seen_paged, "a tensor-core item after a paged item in one CTA"
+            assert it["n_kvh"] == 1 and it["n_seq"] <= 2 * (128 // G)
+            rows = -(-it["n_seq"] // (128 // G)) * 128
+        else:
+            seen_paged = True
+            rows = it["n_seq"] * G * it["n_kvh"]
+        assert 0 <= it["k0"] < it["k1"]
+        loop_item = capacity > 0 and it["level"] == last
+        assert it["len_seq"] == (it["seq_begin"] if loop_item else -1)
+        spans.append((it["part_row"], it["part_row"] + rows))
+        for b in range(it["seq_begin"], it["seq_begin"] + it["n_seq"]):
+            for h in range(it["kvh"], it["kvh"] + it["n_kvh"]):
+                cover.setdefault((it["level"], b, h), []).append((it["k0"], it["k1"]))
+    spans.sort()
+    for (a0, a1), (b0, _) in zip(spans, spans[1:]):
+        assert a1 <= b0, "partial-row ranges overlap"
+    if n_part is not None:
+        assert spans[-1][1] <= n_part and len(items) == n_tc + n_small
+    expect = set()
+    for l, lv in enumerate(wl.levels):
+        for sb, se, kl, _ in lv.nodes.tolist():
+            end = capacity if (capacity > 0 and l == last) else kl
+            if end == 0:
+                continue
+            for b in range(sb, se):
+                for h in range(wl.Hkv):
+                    expect.add((l, b, h))
+                    rng = sorted(cover.get((l, b, h), []))
+                    assert rng and rng[0][0] == 0 and rng[-1][1] == end, (l, b, h, rng[:3])
+                    for (x0, x1), (y0, _) in zip(rng, rng[1:]):
+                        assert x1 == y0, f"keys of node (level {l}, sequence {b}, head {h}) not covered once"
+    assert set(cover) == expect
+    return items
+
+
+@pytest.mark.parametrize("name", W.CONFIG_NAMES)
+def test_plan_items_cover_every_key_once(name):
+    wl = W.make_config(name, seed=0)
+    items = _check_plan_items(wl)
+    assert items
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_plan_items_on_random_trees(seed):
+    import numpy as np
+    rng = np.random.default_rng(100 + seed)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    B = int(rng.integers(1, 300))
+    shared = []
+    for _ in range(int(rng.integers(0, 4))):
+        cuts = sorted(set(rng.integers(1, B, size=int(rng.integers(0, 6))).tolist())) if B > 1 else []
+        bounds = [0] + cuts + [B]
+        shared.append([(a, b, int(rng.integers(0, 3000))) for a, b in zip(bounds[:-1], bounds[1:])])
+    wl = W.build_cascade(f"r{seed}", B=B, Hq=Hkv * G, Hkv=Hkv, d=int(rng.choice([64, 128])),
+                         page_size=int(rng.choice([16, 32, 64])), shared=shared, suffix_range=(0, 400), seed=seed)
+    _check_plan_items(wl, num_sms=int(rng.choice([16, 152])))
+
+
+@pytest.mark.parametrize("name,kw,cap", [("llama3_8b", {}, 300), ("tree2", {}, 300), ("tiny", {}, 40),
+                                         ("no_sharing", dict(B=16, prefix=512), 600)])
+def test_loop_plan_items_reach_the_capacity(name, kw, cap):
+    wl = W.with_suffix_capacity(W.make_config(name, seed=1, **kw), cap, seed=1)
+    _check_plan_items(wl, capacity=cap)
