@@ -355,6 +355,13 @@ int32_t hp_cascade_plan_stats(const hp_tree_desc *desc, int64_t *stats4);
  * returns the item count, or -1 on an invalid descriptor. */
 int32_t hp_cascade_plan_items(const hp_tree_desc *desc, int32_t capacity, int32_t *out, int32_t cap);
 
+/* The merge table of the same plan (host only, as above): one row of
+ * `stride` int32 per (sequence b, KV head), row b*Hkv + kvh, holding the
+ * part count and then the partial row of each part for query head g = 0 of
+ * the group (head g adds g).  Writes at most cap int32 into out (may be
+ * NULL); returns the stride, or -1 on an invalid descriptor. */
+int32_t hp_cascade_plan_merge_table(const hp_tree_desc *desc, int32_t capacity, int32_t *out, int64_t cap);
+
 /* ---------------------------------------------------------------------------
  * Device status: reads and clears the status word of a workspace.  This call
  * synchronises `stream`.  Returns HP_OK, HP_ERR_BOUNDS, HP_ERR_DEVICE_TIMEOUT

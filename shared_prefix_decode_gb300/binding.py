@@ -82,6 +82,7 @@ _SIGNATURES = {
     "hp_cascade_contexts": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i32), c_i32]),
     "hp_cascade_plan_stats": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i64)]),
     "hp_cascade_plan_items": (c_i32, [ctypes.POINTER(HpTreeDesc), c_i32, ctypes.POINTER(c_i32), c_i32]),
+    "hp_cascade_plan_merge_table": (c_i32, [ctypes.POINTER(HpTreeDesc), c_i32, ctypes.POINTER(c_i32), c_i64]),
     "hp_read_device_status": (c_i32, [c_vp, c_vp]),
 }
 
@@ -296,6 +297,19 @@ def hp_cascade_plan_items(levels, B, Hq, Hkv, d, capacity: int = 0, num_sms: int
     buf = (c_i32 * (11 * max(n, 1)))()
     library().hp_cascade_plan_items(ctypes.byref(D.desc), int(capacity), buf, n)
     return [dict(zip(PLAN_ITEM_FIELDS, buf[11 * i:11 * i + 11])) for i in range(n)]
+
+
+def hp_cascade_plan_merge_table(levels, B, Hq, Hkv, d, capacity: int = 0, num_sms: int = 152) -> List[List[int]]:
+    """The plan's merge lists (host only): entry b*Hkv + kvh lists the partial
+    rows (query head g = 0 of the group) merged into row (b, kvh*G + g)."""
+    D = _Desc(levels, B, Hq, Hkv, d, num_sms=num_sms)
+    stride = library().hp_cascade_plan_merge_table(ctypes.byref(D.desc), int(capacity), None, 0)
+    if stride < 0:
+        raise HpError(HP_ERR_ARG, "hp_cascade_plan_merge_table")
+    n = B * Hkv * stride
+    buf = (c_i32 * max(n, 1))()
+    library().hp_cascade_plan_merge_table(ctypes.byref(D.desc), int(capacity), buf, n)
+    return [list(buf[i * stride + 1:i * stride + 1 + buf[i * stride]]) for i in range(B * Hkv)]
 
 
 def hp_cascade_plan_bytes(levels, B, Hq, Hkv, d, num_sms: int = 0) -> int:

@@ -1307,6 +1307,17 @@ int32_t hp_cascade_plan_items(const hp_tree_desc *desc, int32_t capacity, int32_
     return n;
 }
 
+int32_t hp_cascade_plan_merge_table(const hp_tree_desc *desc, int32_t capacity, int32_t *out, int64_t cap)
+{
+    HostPlan P;
+    if (capacity < 0 || build_plan(desc, P, false, capacity) != HP_OK)
+        return -1;
+    if (out)
+        std::memcpy(out, P.merge_tab.data(),
+                    sizeof(int32_t) * (size_t)std::min<int64_t>((int64_t)P.merge_tab.size(), std::max<int64_t>(cap, 0)));
+    return P.hdr.merge_stride;
+}
+
 hp_status hp_read_device_status(void *ws, hp_stream_t stream)
 {
     if (!ws)

@@ -318,6 +318,22 @@ def _check_plan_items(wl, capacity=0, num_sms=152):
                     for (x0, x1), (y0, _) in zip(rng, rng[1:]):
                         assert x1 == y0, f"keys of node (level {l}, sequence {b}, head {h}) not covered once"
     assert set(cover) == expect
+    # merge lists: row (b, kvh) merges exactly the partial rows of the items
+    # covering it, at the item's row layout (tensor-core items: blocks of
+    # 128 rows of 128 / G sequences; paged items: [head in group][sequence][g])
+    tab = hb.hp_cascade_plan_merge_table(levels, wl.B, wl.Hq, wl.Hkv, wl.d, capacity=capacity, num_sms=num_sms)
+    want = [[] for _ in range(wl.B * wl.Hkv)]
+    spb = 128 // G
+    for it in items:
+        for b in range(it["seq_begin"], it["seq_begin"] + it["n_seq"]):
+            s_ = b - it["seq_begin"]
+            for h in range(it["kvh"], it["kvh"] + it["n_kvh"]):
+                if it["tc"]:
+                    row = it["part_row"] + (s_ // spb) * 128 + (s_ % spb) * G
+                else:
+                    row = it["part_row"] + ((h - it["kvh"]) * it["n_seq"] + s_) * G
+                want[b * wl.Hkv + h].append(row)
+    assert [sorted(x) for x in tab] == [sorted(x) for x in want]
     return items
 
 
