@@ -20,10 +20,11 @@
 // the consumers need; the consumers release a stage by arriving on its
 // "empty" barrier.  With an item's first chunk the producer also loads the
 // item's query rows (one sequence: G rows per head of the group) into the
-// stage's Q slot, so a new item costs the consumers no dependent global load.  Scores and P V use the m16n8k16 bf16 MMA with f32
-// accumulation: rows are the (up to 16) query rows of a head, S = Q K^T for
-// 16 keys is two n8 tiles, and O = P V reuses the S accumulator layout as the
-// A operand.  The producer runs ahead across item boundaries.
+// stage's Q slot, so a new item costs the consumers no dependent global load.
+// Scores and P V use the m16n8k16 bf16 MMA with f32 accumulation: rows are
+// the (up to 16) query rows of a head, S = Q K^T for 16 keys is two n8
+// tiles, and O = P V reuses the S accumulator layout as the A operand.  The
+// producer runs ahead across item boundaries.
 #pragma once
 
 #include <cuda_runtime.h>
