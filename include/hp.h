@@ -355,6 +355,14 @@ int32_t hp_cascade_plan_stats(const hp_tree_desc *desc, int64_t *stats4);
  * returns the item count, or -1 on an invalid descriptor. */
 int32_t hp_cascade_plan_items(const hp_tree_desc *desc, int32_t capacity, int32_t *out, int32_t cap);
 
+/* The page ids each of those items carries in its CTA's record (host only,
+ * as above), items in hp_cascade_plan_items' order: item i's key t (of its
+ * level's node) is in page pages[offsets[i] + t / page_size - k0 / page_size].
+ * offsets (n + 1 entries) and pages (at most cap written) may be NULL;
+ * returns the total page count, or -1 on an invalid descriptor. */
+int64_t hp_cascade_plan_item_pages(const hp_tree_desc *desc, int32_t capacity, int64_t *offsets,
+                                   int32_t *pages, int64_t cap);
+
 /* The merge table of the same plan (host only, as above): one row of
  * `stride` int32 per (sequence b, KV head), row b*Hkv + kvh, holding the
  * part count and then the partial row of each part for query head g = 0 of

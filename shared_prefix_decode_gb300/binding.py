@@ -83,6 +83,8 @@ _SIGNATURES = {
     "hp_cascade_plan_stats": (c_i32, [ctypes.POINTER(HpTreeDesc), ctypes.POINTER(c_i64)]),
     "hp_cascade_plan_items": (c_i32, [ctypes.POINTER(HpTreeDesc), c_i32, ctypes.POINTER(c_i32), c_i32]),
     "hp_cascade_plan_merge_table": (c_i32, [ctypes.POINTER(HpTreeDesc), c_i32, ctypes.POINTER(c_i32), c_i64]),
+    "hp_cascade_plan_item_pages": (c_i64, [ctypes.POINTER(HpTreeDesc), c_i32, ctypes.POINTER(c_i64),
+                                           ctypes.POINTER(c_i32), c_i64]),
     "hp_read_device_status": (c_i32, [c_vp, c_vp]),
 }
 
@@ -297,6 +299,20 @@ def hp_cascade_plan_items(levels, B, Hq, Hkv, d, capacity: int = 0, num_sms: int
     buf = (c_i32 * (11 * max(n, 1)))()
     library().hp_cascade_plan_items(ctypes.byref(D.desc), int(capacity), buf, n)
     return [dict(zip(PLAN_ITEM_FIELDS, buf[11 * i:11 * i + 11])) for i in range(n)]
+
+
+def hp_cascade_plan_item_pages(levels, B, Hq, Hkv, d, capacity: int = 0, num_sms: int = 152) -> List[List[int]]:
+    """Per item (hp_cascade_plan_items' order) the page ids its record carries."""
+    D = _Desc(levels, B, Hq, Hkv, d, num_sms=num_sms)
+    lib = library()
+    n_items = lib.hp_cascade_plan_items(ctypes.byref(D.desc), int(capacity), None, 0)
+    if n_items < 0:
+        raise HpError(HP_ERR_ARG, "hp_cascade_plan_item_pages")
+    offs = (c_i64 * (n_items + 1))()
+    total = lib.hp_cascade_plan_item_pages(ctypes.byref(D.desc), int(capacity), offs, None, 0)
+    pages = (c_i32 * max(total, 1))()
+    lib.hp_cascade_plan_item_pages(ctypes.byref(D.desc), int(capacity), offs, pages, total)
+    return [list(pages[offs[i]:offs[i + 1]]) for i in range(n_items)]
 
 
 def hp_cascade_plan_merge_table(levels, B, Hq, Hkv, d, capacity: int = 0, num_sms: int = 152) -> List[List[int]]:

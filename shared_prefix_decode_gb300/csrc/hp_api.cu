@@ -1307,6 +1307,35 @@ int32_t hp_cascade_plan_items(const hp_tree_desc *desc, int32_t capacity, int32_
     return n;
 }
 
+int64_t hp_cascade_plan_item_pages(const hp_tree_desc *desc, int32_t capacity, int64_t *offsets, int32_t *pages,
+                                   int64_t cap)
+{
+    HostPlan P;
+    if (capacity < 0 || build_plan(desc, P, false, capacity) != HP_OK)
+        return -1;
+    // the page ids each item's record entry carries, in hp_cascade_plan_items' order
+    int64_t total = 0, k = 0;
+    auto put = [&](const WorkItem &w) {
+        const int ps = P.level_ps[w.level];
+        const int64_t first = w.k0 / ps, n = item_pages(w, ps);
+        if (offsets)
+            offsets[k] = total;
+        for (int64_t i = 0; i < n; ++i, ++total)
+            if (pages && total < cap)
+                pages[total] = P.page_ids[(size_t)(w.page_base + first + i)];
+        ++k;
+    };
+    for (size_t c = 0; c < P.cta_tc.size(); ++c) {
+        for (int32_t id : P.cta_tc[c])
+            put(P.tc[id]);
+        for (int32_t id : P.cta_small[c])
+            put(P.small[id]);
+    }
+    if (offsets)
+        offsets[k] = total;
+    return total;
+}
+
 int32_t hp_cascade_plan_merge_table(const hp_tree_desc *desc, int32_t capacity, int32_t *out, int64_t cap)
 {
     HostPlan P;

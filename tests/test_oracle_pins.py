@@ -466,3 +466,98 @@ def test_stream_pins_catch_planted_mask_mistake(name, monkeypatch):
         except AssertionError:
             failed += 1
     assert failed > 0, f"planted mistake {name!r} passed every pin"
+
+
+# ------------------------------------------------------ the plan, replayed
+def _replay_plan(wl, capacity=0, num_sms=152, plan_wl=None):
+    """The planner's output run on the oracle: each work item's rows attend
+    (oracle.sdp) to the keys its record's pages hold over its key range, and
+    each output row merges (oracle.merge) the partial states its merge list
+    names.  The plan is built from ``plan_wl`` (default ``wl``); the keys,
+    queries and current suffix lengths come from ``wl``.  Returns (O, LSE)
+    in oracle.cascade's row order."""
+    from shared_prefix_decode_gb300 import binding as hb
+    levels = hb._levels_of(plan_wl if plan_wl is not None else wl)
+    args = (levels, wl.B, wl.Hq, wl.Hkv, wl.d)
+    items = hb.hp_cascade_plan_items(*args, capacity=capacity, num_sms=num_sms)
+    pages = hb.hp_cascade_plan_item_pages(*args, capacity=capacity, num_sms=num_sms)
+    tab = hb.hp_cascade_plan_merge_table(*args, capacity=capacity, num_sms=num_sms)
+    G, ps = wl.G, wl.page_size
+    K, V, q = wl.k_pool.double().numpy(), wl.v_pool.double().numpy(), wl.q.double().numpy()
+    part = {}
+    for it, pg in zip(items, pages):
+        k0, k1 = it["k0"], it["k1"]
+        if it["len_seq"] >= 0:  # a loop item ends at its sequence's current length
+            k1 = min(k1, int(wl.levels[it["level"]].nodes[it["len_seq"], 2]))
+        pid = [pg[t // ps - k0 // ps] for t in range(k0, k1)]
+        slot = [t % ps for t in range(k0, k1)]
+        seqs = range(it["seq_begin"], it["seq_begin"] + it["n_seq"])
+        for h in range(it["kvh"], it["kvh"] + it["n_kvh"]):
+            Q = np.stack([q[b, h * G + g] for b in seqs for g in range(G)])
+            O, L = oracle.sdp(Q, K[pid, h, slot], V[pid, h, slot], wl.scale)
+            for i, b in enumerate(seqs):
+                s_ = b - it["seq_begin"]
+                if it["tc"]:
+                    row = it["part_row"] + (s_ // (128 // G)) * 128 + (s_ % (128 // G)) * G
+                else:
+                    row = it["part_row"] + ((h - it["kvh"]) * it["n_seq"] + s_) * G
+                for g in range(G):
+                    part[row + g] = (O[i * G + g], L[i * G + g])
+    Oo = np.zeros((wl.B * wl.Hq, wl.d))
+    Lo = np.full(wl.B * wl.Hq, -np.inf)
+    for b in range(wl.B):
+        for h in range(wl.Hq):
+            o, l = np.zeros((1, wl.d)), np.full(1, -np.inf)
+            for r in tab[b * wl.Hkv + h // G]:
+                po, pl = part[r + h % G]
+                o, l = oracle.merge(o, l, po[None], np.array([pl]))
+            Oo[b * wl.Hq + h], Lo[b * wl.Hq + h] = o[0], l[0]
+    return Oo, Lo
+
+
+@pytest.mark.parametrize("name,kw", [("llama3_8b", {}), ("tree2", dict(B=32, prefix=256)),
+                                     ("codellama13b", dict(B=24, prefix=512)), ("no_sharing", dict(B=6, prefix=300)),
+                                     ("tiny", {})])
+def test_plan_replayed_on_the_oracle_equals_the_definition(name, kw):
+    """The plan (items, their record pages, the merge lists) computes the
+    definition: replayed on the oracle it equals oracle.cascade row by row
+    (1e-12), the benchmarked workload at full size included."""
+    wl = W.make_config(name, seed=2, **kw)
+    O, L = oracle.cascade(wl)
+    Or, Lr = _replay_plan(wl)
+    np.testing.assert_allclose(Or, O, atol=1e-12)
+    fin = np.isfinite(L)
+    assert np.array_equal(np.isfinite(Lr), fin)
+    np.testing.assert_allclose(Lr[fin], L[fin], atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_plan_replayed_on_random_trees_and_loop_plans(seed):
+    rng = np.random.default_rng(200 + seed)
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    B = int(rng.integers(1, 40))
+    shared = []
+    for _ in range(int(rng.integers(1, 4))):
+        cuts = sorted(set(rng.integers(1, B, size=int(rng.integers(0, 4))).tolist())) if B > 1 else []
+        bounds = [0] + cuts + [B]
+        shared.append([(a, b, int(rng.integers(0, 300))) for a, b in zip(bounds[:-1], bounds[1:])])
+    wl = W.build_cascade(f"r{seed}", B=B, Hq=Hkv * G, Hkv=Hkv, d=64, page_size=int(rng.choice([16, 32])),
+                         shared=shared, suffix_range=(0, 100), seed=seed)
+    O, L = oracle.cascade(wl)
+    Or, Lr = _replay_plan(wl, num_sms=int(rng.choice([16, 152])))
+    np.testing.assert_allclose(Or, O, atol=1e-12)
+    np.testing.assert_allclose(Lr[np.isfinite(L)], L[np.isfinite(L)], atol=1e-12)
+    # the same tree as a decode loop: the plan built at the start, replayed
+    # after each of five appended tokens with the grown suffixes
+    cap = int(wl.levels[-1].nodes[:, 2].max()) + 5
+    lw = W.with_suffix_capacity(wl, cap, seed=seed)
+    start = W.CascadeWorkload(lw.name, lw.B, lw.Hq, lw.Hkv, lw.d, lw.page_size, lw.scale, lw.q, lw.k_pool,
+                              lw.v_pool, [W.TreeLevel(l.nodes.clone(), l.page_ids) for l in lw.levels])
+    for q, k, v in W.decode_tokens(lw, 5, seed=seed):
+        W.append_token(lw, k, v)
+        lw.q = q
+        O, L = oracle.cascade(lw)
+        Or, Lr = _replay_plan(lw, capacity=cap, plan_wl=start)
+        np.testing.assert_allclose(Or, O, atol=1e-12)
+        np.testing.assert_allclose(Lr, L, atol=1e-12)
