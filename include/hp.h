@@ -215,7 +215,11 @@ size_t hp_cascade_plan_bytes(const hp_tree_desc *desc);
  * the pools, and copy the plan into plan_dev (device, >= plan_bytes,
  * 256-byte aligned) on `stream`.  The call waits for that copy, so it is not
  * for use inside stream capture.  Re-run only when the tree changes; a plan
- * is reused across steps while the tree and the pools are unchanged. */
+ * is reused across steps while the tree and the pools are unchanged.
+ * A sequence's own nodes at several levels (nodes covering only that
+ * sequence, at most 16 query rows, in the same pools) are planned as one
+ * node when every one of them but the last ends on a page boundary: one
+ * partial state for that sequence instead of one per node. */
 hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_bytes,
                           hp_plan_info *info, hp_stream_t stream);
 

@@ -190,8 +190,21 @@ PrefixGeo prefix_geo(int rows, int G, int Hkv, int len, int sms)
 }
 
 // --------------------------------------------------------------- planner
+// A node as the planner schedules it: a tree node, or several single-sequence
+// nodes of one sequence fused into one (their keys back to back, over the
+// concatenation of their page lists).
+struct PNode {
+    int level;  // the level whose pools and tensor maps the items use
+    int seq_begin, seq_end;
+    int64_t kv_len;
+    int32_t page_base;  // index in the plan's page-id list of the node's first page
+    bool loop;          // a decode-loop suffix (grows at run time)
+    int fused;          // tree nodes it stands for
+};
+
 struct HostPlan {
     PlanHeader hdr;
+    std::vector<PNode> nodes;
     std::vector<CUtensorMap> maps;
     std::vector<WorkItem> tc, small;
     std::vector<int32_t> page_ids;     // all levels' page ids, concatenated
@@ -351,68 +364,64 @@ void build_records(HostPlan &P)
 // over their plan-time length as usual, but each suffix's last item reaches
 // to the capacity (a suffix of length 0 gets one item [0, capacity)); at run
 // time the items end at the sequence's current length.
-int64_t make_items(const hp_tree_desc *d, int G, int nh, int64_t tc_split, int64_t small_split,
-                   const std::vector<int32_t> &level_page_off, HostPlan &P,
+int64_t make_items(const hp_tree_desc *d, int G, int nh, int64_t tc_split, int64_t small_split, HostPlan &P,
                    std::vector<std::vector<int32_t>> *lists, int capacity = 0)
 {
     P.tc.clear();
     P.small.clear();
     int64_t part = 0;
-    for (int l = 0; l < d->num_levels; ++l) {
-        const hp_tree_level &L = d->levels[l];
-        const bool loop = capacity > 0 && l == d->num_levels - 1;
-        for (int n = 0; n < L.num_nodes; ++n) {
-            const hp_tree_node &N = L.nodes[n];
-            if (N.kv_len == 0 && !loop)
-                continue;
-            const int64_t klen = loop ? std::max(N.kv_len, 1) : N.kv_len;
-            const int nseq = N.seq_end - N.seq_begin;
-            const bool tc = (int64_t)nseq * G > kSmallRows;
-            const int spc = tc ? 2 * (kTcTile / G) : nseq;
-            const int64_t split = tc ? tc_split : small_split;
-            // tensor-core items take one KV head; small-row items a group of
-            // nh heads whose rows are laid out [head in group][sequence][g]
-            const int hstep = tc ? 1 : nh;
-            for (int s0 = N.seq_begin; s0 < N.seq_end; s0 += spc) {
-                const int ns = std::min(spc, N.seq_end - s0);
-                for (int kvh = 0; kvh < d->Hkv; kvh += hstep)
-                    for (int64_t k0 = 0; k0 < klen; k0 += split) {
-                        WorkItem w;
-                        w.level = l;
-                        w.seq_begin = s0;
-                        w.n_seq = ns;
-                        w.kvh = kvh;
-                        w.k0 = (int32_t)k0;
-                        w.k1 = (int32_t)std::min<int64_t>(k0 + split, klen);
-                        w.len_seq = loop ? s0 : -1;
-                        w.k1_model = w.k1;
-                        if (loop && w.k1 == klen) {
-                            // reaches to the capacity; over the loop it holds
-                            // half of the headroom on average
-                            w.k1 = capacity;
-                            w.k1_model = (int32_t)std::max<int64_t>(k0 + 1, (N.kv_len + (int64_t)capacity) / 2);
-                        }
-                        w.page_base = level_page_off[l] + N.page_off;
-                        w.part_row = (int32_t)std::min<int64_t>(part, INT32_MAX);
-                        if (tc) {
-                            // 128 rows per block of 128 / G sequences (the
-                            // block is stored whole by a TMA tensor store)
-                            if (lists)
-                                for (int b = s0; b < s0 + ns; ++b)
-                                    (*lists)[(size_t)b * d->Hkv + kvh].push_back(
-                                        (int32_t)std::min<int64_t>(tc_part_row(part, b - s0, 0, G), INT32_MAX));
-                            part += ceil_div(ns, kTcTile / G) * kTcTile;
-                        } else {
-                            if (lists)
-                                for (int hw = 0; hw < hstep; ++hw)
-                                    for (int b = s0; b < s0 + ns; ++b)
-                                        (*lists)[(size_t)b * d->Hkv + kvh + hw].push_back(
-                                            (int32_t)(part + ((int64_t)hw * ns + (b - s0)) * G));
-                            part += (int64_t)ns * G * hstep;
-                        }
-                        (tc ? P.tc : P.small).push_back(w);
+    for (const PNode &N : P.nodes) {
+        const int l = N.level;
+        const bool loop = N.loop;
+        if (N.kv_len == 0 && !loop)
+            continue;
+        const int64_t klen = loop ? std::max<int64_t>(N.kv_len, 1) : N.kv_len;
+        const int nseq = N.seq_end - N.seq_begin;
+        const bool tc = (int64_t)nseq * G > kSmallRows;
+        const int spc = tc ? 2 * (kTcTile / G) : nseq;
+        const int64_t split = tc ? tc_split : small_split;
+        // tensor-core items take one KV head; small-row items a group of
+        // nh heads whose rows are laid out [head in group][sequence][g]
+        const int hstep = tc ? 1 : nh;
+        for (int s0 = N.seq_begin; s0 < N.seq_end; s0 += spc) {
+            const int ns = std::min(spc, N.seq_end - s0);
+            for (int kvh = 0; kvh < d->Hkv; kvh += hstep)
+                for (int64_t k0 = 0; k0 < klen; k0 += split) {
+                    WorkItem w;
+                    w.level = l;
+                    w.seq_begin = s0;
+                    w.n_seq = ns;
+                    w.kvh = kvh;
+                    w.k0 = (int32_t)k0;
+                    w.k1 = (int32_t)std::min<int64_t>(k0 + split, klen);
+                    w.len_seq = loop ? s0 : -1;
+                    w.k1_model = w.k1;
+                    if (loop && w.k1 == klen) {
+                        // reaches to the capacity; over the loop it holds
+                        // half of the headroom on average
+                        w.k1 = capacity;
+                        w.k1_model = (int32_t)std::max<int64_t>(k0 + 1, (N.kv_len + (int64_t)capacity) / 2);
                     }
-            }
+                    w.page_base = N.page_base;
+                    w.part_row = (int32_t)std::min<int64_t>(part, INT32_MAX);
+                    if (tc) {
+                        // 128 rows per block of 128 / G sequences (the
+                        // block is stored whole by a TMA tensor store)
+                        if (lists)
+                            for (int b = s0; b < s0 + ns; ++b)
+                                (*lists)[(size_t)b * d->Hkv + kvh].push_back(
+                                    (int32_t)std::min<int64_t>(tc_part_row(part, b - s0, 0, G), INT32_MAX));
+                        part += ceil_div(ns, kTcTile / G) * kTcTile;
+                    } else {
+                        if (lists)
+                            for (int hw = 0; hw < hstep; ++hw)
+                                for (int b = s0; b < s0 + ns; ++b)
+                                    (*lists)[(size_t)b * d->Hkv + kvh + hw].push_back(
+                                        (int32_t)(part + ((int64_t)hw * ns + (b - s0)) * G));
+                        part += (int64_t)ns * G * hstep;
+                    }
+                    (tc ? P.tc : P.small).push_back(w);
+                }
         }
     }
     return part;
@@ -524,6 +533,102 @@ void build_contexts(const hp_tree_desc *d, std::vector<int32_t> &out)
             }
 }
 
+// The nodes the planner schedules, level by level in tree order.  Several
+// single-sequence nodes of one sequence on the paged path (G <= 16 rows) are
+// fused into one: attention over a set of keys does not depend on their
+// order, so one item can walk the nodes' keys back to back over the
+// concatenation of their page lists.  That needs every node but the last to
+// end on a page boundary, and all of them to use the same pools and page
+// size.  The fused node takes the place of its first member; the sequence
+// then has one partial state, not one per node, for the same bytes.  Nodes
+// that grow in a decode loop stay on their own.  Concatenated page lists are
+// appended to P.page_ids.
+void plan_nodes(const hp_tree_desc *d, int G, int capacity, const std::vector<int32_t> &level_page_off, HostPlan &P)
+{
+    const int last = d->num_levels - 1;
+    P.nodes.clear();
+    auto fusable = [&](int l, const hp_tree_node &N) {
+        return N.seq_end - N.seq_begin == 1 && G <= kSmallRows && N.kv_len > 0 && !(capacity > 0 && l == last);
+    };
+    auto same_pools = [&](int a, int b) {
+        const hp_tree_level &A = d->levels[a], &Bl = d->levels[b];
+        return A.k_pool == Bl.k_pool && A.v_pool == Bl.v_pool && A.num_pages == Bl.num_pages &&
+               A.page_size == Bl.page_size;
+    };
+    // members[l][n]: the (level, node) list a fused node starts with; skip[l][n]: fused into another
+    std::vector<std::vector<std::vector<std::pair<int, int>>>> members(d->num_levels);
+    std::vector<std::vector<char>> skip(d->num_levels);
+    for (int l = 0; l < d->num_levels; ++l) {
+        members[l].assign(d->levels[l].num_nodes, {});
+        skip[l].assign(d->levels[l].num_nodes, 0);
+    }
+    // own[l][b]: the fusable node of level l that covers only sequence b, or -1
+    std::vector<std::vector<int>> own(d->num_levels, std::vector<int>(d->B, -1));
+    for (int l = 0; l < d->num_levels; ++l)
+        for (int n = 0; n < d->levels[l].num_nodes; ++n)
+            if (fusable(l, d->levels[l].nodes[n]))
+                own[l][d->levels[l].nodes[n].seq_begin] = n;
+    for (int b = 0; b < d->B; ++b) {
+        // this sequence's fusable nodes, level by level
+        std::vector<std::pair<int, int>> cand;
+        for (int l = 0; l < d->num_levels; ++l)
+            if (own[l][b] >= 0 && (cand.empty() || same_pools(cand[0].first, l)))
+                cand.emplace_back(l, own[l][b]);
+        if (cand.size() < 2)
+            continue;
+        // page-aligned nodes first, then at most one that ends mid-page
+        std::vector<std::pair<int, int>> chain;
+        int ragged = -1;
+        for (size_t i = 0; i < cand.size(); ++i) {
+            const hp_tree_level &L = d->levels[cand[i].first];
+            if (L.nodes[cand[i].second].kv_len % L.page_size == 0)
+                chain.push_back(cand[i]);
+            else if (ragged < 0)
+                ragged = (int)i;
+        }
+        if (ragged >= 0)
+            chain.push_back(cand[ragged]);
+        if (chain.size() < 2)
+            continue;
+        // the fused node sits where its first member (in tree order) was
+        const auto head = *std::min_element(chain.begin(), chain.end());
+        members[head.first][head.second] = chain;
+        for (const auto &m : chain)
+            if (m != head)
+                skip[m.first][m.second] = 1;
+    }
+    for (int l = 0; l < d->num_levels; ++l) {
+        const hp_tree_level &L = d->levels[l];
+        for (int n = 0; n < L.num_nodes; ++n) {
+            if (skip[l][n])
+                continue;
+            const hp_tree_node &N = L.nodes[n];
+            PNode pn;
+            pn.level = l;
+            pn.seq_begin = N.seq_begin;
+            pn.seq_end = N.seq_end;
+            pn.loop = capacity > 0 && l == last;
+            pn.fused = 1;
+            pn.kv_len = N.kv_len;
+            pn.page_base = level_page_off[l] + N.page_off;
+            const auto &ch = members[l][n];
+            if (!ch.empty()) {
+                pn.kv_len = 0;
+                pn.page_base = (int32_t)P.page_ids.size();
+                pn.fused = (int)ch.size();
+                for (const auto &m : ch) {
+                    const hp_tree_level &ML = d->levels[m.first];
+                    const hp_tree_node &MN = ML.nodes[m.second];
+                    const int64_t npg = ceil_div(MN.kv_len, ML.page_size);
+                    P.page_ids.insert(P.page_ids.end(), ML.page_ids + MN.page_off, ML.page_ids + MN.page_off + npg);
+                    pn.kv_len += MN.kv_len;
+                }
+            }
+            P.nodes.push_back(pn);
+        }
+    }
+}
+
 hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capacity = 0)
 {
     hp_status st = validate_desc(d);
@@ -560,24 +665,24 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
         LD.tc_box = std::gcd(L.page_size, kTcTile);
     }
 
+    plan_nodes(d, G, capacity, level_page_off, P);
+
     // Work sizes: 128-key tiles of the shared (tensor-core) nodes, 16-key
     // chunks of the paged ones.
     const int nh = cascade_heads_per_item(d->Hkv);
     H.small_nh = nh;
     int64_t tc_tiles = 0, small_chunks = 0;
-    for (int l = 0; l < d->num_levels; ++l)
-        for (int n = 0; n < d->levels[l].num_nodes; ++n) {
-            const hp_tree_node &N = d->levels[l].nodes[n];
-            const int64_t rows = (int64_t)(N.seq_end - N.seq_begin) * G;
-            if (N.kv_len == 0)
-                continue;
-            if (rows > kSmallRows) {
-                const int spc = 2 * (kTcTile / G);
-                tc_tiles += ceil_div(N.seq_end - N.seq_begin, spc) * d->Hkv * ceil_div(N.kv_len, kTcTile);
-            } else {
-                small_chunks += (int64_t)(d->Hkv / nh) * ceil_div(N.kv_len, kChunk);
-            }
+    for (const PNode &N : P.nodes) {
+        const int64_t rows = (int64_t)(N.seq_end - N.seq_begin) * G;
+        if (N.kv_len == 0)
+            continue;
+        if (rows > kSmallRows) {
+            const int spc = 2 * (kTcTile / G);
+            tc_tiles += ceil_div(N.seq_end - N.seq_begin, spc) * d->Hkv * ceil_div(N.kv_len, kTcTile);
+        } else {
+            small_chunks += (int64_t)(d->Hkv / nh) * ceil_div(N.kv_len, kChunk);
         }
+    }
 
     // Split of the CTAs between the two roles: n_tc CTAs run the tensor-core
     // items (about one each: the key split is the shared tiles over n_tc), the
@@ -599,7 +704,7 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
             for (int k = 1; k < sms; ++k) {
                 int64_t ts, ss;
                 splits_for(k, ts, ss);
-                make_items(d, G, nh, ts, ss, level_page_off, P, nullptr, capacity);
+                make_items(d, G, nh, ts, ss, P, nullptr, capacity);
                 const double t = schedule(P, sms, k, mixed != 0, d->d, cm);
                 if (t >= 0.0 && (best < 0.0 || t < best)) {
                     best = t;
@@ -613,7 +718,7 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
 
     // Items and partial rows, level by level; merge lists per (b, kvh).
     std::vector<std::vector<int32_t>> lists((size_t)d->B * d->Hkv);
-    const int64_t part = make_items(d, G, nh, tc_split, small_split, level_page_off, P, &lists, capacity);
+    const int64_t part = make_items(d, G, nh, tc_split, small_split, P, &lists, capacity);
     if (part > INT32_MAX)
         return HP_ERR_UNSUPPORTED;
     // merge table: one row per (b, kvh), its count then its partial rows

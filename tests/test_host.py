@@ -276,6 +276,7 @@ def _check_plan_items(wl, capacity=0, num_sms=152):
     G = wl.G
     last = len(wl.levels) - 1
     cover = {}
+    total = {}
     spans = []
     prev_cta, seen_paged = -1, False
     for it in items:
@@ -299,25 +300,29 @@ def _check_plan_items(wl, capacity=0, num_sms=152):
         for b in range(it["seq_begin"], it["seq_begin"] + it["n_seq"]):
             for h in range(it["kvh"], it["kvh"] + it["n_kvh"]):
                 cover.setdefault((it["level"], b, h), []).append((it["k0"], it["k1"]))
+                total[(b, h)] = total.get((b, h), 0) + it["k1"] - it["k0"]
     spans.sort()
     for (a0, a1), (b0, _) in zip(spans, spans[1:]):
         assert a1 <= b0, "partial-row ranges overlap"
     if n_part is not None:
         assert spans[-1][1] <= n_part and len(items) == n_tc + n_small
-    expect = set()
+    # per (level, sequence, head): one node (a tree node, or single-sequence
+    # nodes of that sequence fused into the first of them), its keys covered
+    # once from 0; per (sequence, head): every key of every node
+    for key, rng in cover.items():
+        rng = sorted(rng)
+        assert rng[0][0] == 0, key
+        for (x0, x1), (y0, _) in zip(rng, rng[1:]):
+            assert x1 == y0, f"keys of (level, sequence, head) {key} not covered once"
+    want_total = {}
     for l, lv in enumerate(wl.levels):
         for sb, se, kl, _ in lv.nodes.tolist():
             end = capacity if (capacity > 0 and l == last) else kl
-            if end == 0:
-                continue
             for b in range(sb, se):
                 for h in range(wl.Hkv):
-                    expect.add((l, b, h))
-                    rng = sorted(cover.get((l, b, h), []))
-                    assert rng and rng[0][0] == 0 and rng[-1][1] == end, (l, b, h, rng[:3])
-                    for (x0, x1), (y0, _) in zip(rng, rng[1:]):
-                        assert x1 == y0, f"keys of node (level {l}, sequence {b}, head {h}) not covered once"
-    assert set(cover) == expect
+                    if end:
+                        want_total[(b, h)] = want_total.get((b, h), 0) + end
+    assert total == want_total
     # merge lists: row (b, kvh) merges exactly the partial rows of the items
     # covering it, at the item's row layout (tensor-core items: blocks of
     # 128 rows of 128 / G sequences; paged items: [head in group][sequence][g])
@@ -366,3 +371,30 @@ def test_plan_items_on_random_trees(seed):
 def test_loop_plan_items_reach_the_capacity(name, kw, cap):
     wl = W.with_suffix_capacity(W.make_config(name, seed=1, **kw), cap, seed=1)
     _check_plan_items(wl, capacity=cap)
+
+
+
+def _chain_tree(seed, ps=16, mid=32, loop_cap=0):
+    """A shared document, then one single-sequence node per sequence (a
+    question of `mid` tokens), then the private suffixes."""
+    B = 6
+    return W.build_cascade(f"chain{seed}", B=B, Hq=8, Hkv=2, d=64, page_size=ps,
+                           shared=[[(0, B, 100)], [(b, b + 1, mid) for b in range(B)]],
+                           suffix_range=(1, 40), seed=seed)
+
+
+def test_single_sequence_chains_are_fused():
+    """A sequence's own question node (page-aligned) and its suffix are one
+    planning node: its items sit at the question's level and cover both
+    nodes' keys; none are left at the suffix's level.  A question that
+    ends mid-page is not fused with a suffix (only the last fused node may
+    end mid-page), nor is a growing decode-loop suffix."""
+    wl = _chain_tree(0)
+    items = _check_plan_items(wl)
+    assert {it["level"] for it in items} == {0, 1}
+    for b, (_, _, kl, _) in enumerate(wl.levels[2].nodes.tolist()):
+        assert max(it["k1"] for it in items if it["level"] == 1 and it["seq_begin"] == b) == 32 + kl
+    ragged = _chain_tree(0, mid=20)
+    assert {it["level"] for it in _check_plan_items(ragged)} == {0, 1, 2}
+    loop = W.with_suffix_capacity(wl, 64, seed=0)
+    assert {it["level"] for it in _check_plan_items(loop, capacity=64)} == {0, 1, 2}

@@ -561,3 +561,44 @@ def test_plan_replayed_on_random_trees_and_loop_plans(seed):
         Or, Lr = _replay_plan(lw, capacity=cap, plan_wl=start)
         np.testing.assert_allclose(Or, O, atol=1e-12)
         np.testing.assert_allclose(Lr, L, atol=1e-12)
+
+
+@pytest.mark.parametrize("mid,ps", [(32, 16), (20, 16), (64, 32), (0, 16)])
+def test_plan_with_fused_single_sequence_chains_replayed(mid, ps):
+    """Trees whose sequences each own a question node below a shared document
+    (page-aligned or not, or empty) above their suffix: the planner fuses a
+    sequence's own nodes into one where it can, and the replayed plan still
+    equals the definition, also as a decode loop as the suffixes grow."""
+    B = 6
+    wl = W.build_cascade("chain", B=B, Hq=8, Hkv=2, d=64, page_size=ps,
+                         shared=[[(0, B, 100)], [(b, b + 1, mid) for b in range(B)]],
+                         suffix_range=(0, 40), seed=mid)
+    O, L = oracle.cascade(wl)
+    Or, Lr = _replay_plan(wl)
+    np.testing.assert_allclose(Or, O, atol=1e-12)
+    np.testing.assert_allclose(Lr, L, atol=1e-12)
+    cap = int(wl.levels[-1].nodes[:, 2].max()) + 3
+    lw = W.with_suffix_capacity(wl, cap, seed=1)
+    start = W.CascadeWorkload(lw.name, lw.B, lw.Hq, lw.Hkv, lw.d, lw.page_size, lw.scale, lw.q, lw.k_pool,
+                              lw.v_pool, [W.TreeLevel(l.nodes.clone(), l.page_ids) for l in lw.levels])
+    for q, k, v in W.decode_tokens(lw, 3, seed=1):
+        W.append_token(lw, k, v)
+        lw.q = q
+        O, L = oracle.cascade(lw)
+        Or, Lr = _replay_plan(lw, capacity=cap, plan_wl=start)
+        np.testing.assert_allclose(Or, O, atol=1e-12)
+        np.testing.assert_allclose(Lr, L, atol=1e-12)
+
+
+def test_plans_of_the_gpu_random_trees_replayed():
+    """The twelve random trees of the GPU parity tests: their plans,
+    replayed on the oracle, equal the definition."""
+    from test_gpu_parity import _random_tree
+    for seed in range(12):
+        wl = _random_tree(seed)
+        O, L = oracle.cascade(wl)
+        Or, Lr = _replay_plan(wl)
+        np.testing.assert_allclose(Or, O, atol=1e-12, err_msg=f"tree {seed}")
+        fin = np.isfinite(L)
+        assert np.array_equal(np.isfinite(Lr), fin)
+        np.testing.assert_allclose(Lr[fin], L[fin], atol=1e-12, err_msg=f"tree {seed}")
