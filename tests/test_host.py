@@ -398,3 +398,25 @@ def test_single_sequence_chains_are_fused():
     assert {it["level"] for it in _check_plan_items(ragged)} == {0, 1, 2}
     loop = W.with_suffix_capacity(wl, 64, seed=0)
     assert {it["level"] for it in _check_plan_items(loop, capacity=64)} == {0, 1, 2}
+
+
+def test_chunkattention_fig2_private_chunks_are_planned_as_one():
+    """In ChunkAttention's Figure 2 tree, sequence 1 owns chunks C4 then C6
+    and sequence 2 owns C5 then C7 (one page each).  The context list keeps
+    them apart, as the page lists it; the planner walks each pair as one
+    node of two pages at C4's / C5's level, and sequence 0's single C3
+    stays as it is."""
+    pool = _pool()
+    g, levels, names = _fig2_levels(pool)
+    ps = 16
+    items = hb.hp_cascade_plan_items(levels, 3, 4, 4, 128, num_sms=152)
+    lvl = {names[k]: k[0] for k in names}
+    by_seq = {}
+    for it in items:
+        if it["n_seq"] == 1:
+            by_seq.setdefault(it["seq_begin"], set()).add((it["level"], max(
+                x["k1"] for x in items if x["n_seq"] == 1 and x["seq_begin"] == it["seq_begin"]
+                and x["level"] == it["level"])))
+    assert by_seq[0] == {(lvl["C3"], ps)}
+    assert by_seq[1] == {(lvl["C4"], 2 * ps)}
+    assert by_seq[2] == {(lvl["C5"], 2 * ps)}
