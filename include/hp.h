@@ -181,7 +181,8 @@ typedef struct {
 } hp_tree_level;
 
 typedef struct {
-    int32_t num_levels; /* 1 .. 8 */
+    int32_t num_levels; /* 1 .. 64; at most 8 distinct pool sets (K pool, V pool,
+                           num_pages, page_size) across the levels */
     int32_t B, Hq, Hkv, d;
     const hp_tree_level *levels; /* host */
     int32_t num_sms;             /* SMs to plan for; 0 = the current device's count */
@@ -197,7 +198,7 @@ typedef struct {
     int32_t n_small_items; /* small-row items (private suffixes, narrow nodes) */
     int32_t grid;          /* CTAs of the step's persistent launch (one per SM) */
     int32_t rec_stride;    /* bytes of each CTA's schedule record in the plan */
-    int32_t num_levels;
+    int32_t num_levels;    /* distinct pool sets of the tree (tensor-map slots) */
     int32_t merge_stride;  /* int32 per row of the plan's merge table */
     int64_t n_part_rows;   /* partial (O, LSE) rows in the workspace */
     int64_t plan_bytes;

@@ -209,6 +209,7 @@ struct HostPlan {
     std::vector<WorkItem> tc, small;
     std::vector<int32_t> page_ids;     // all levels' page ids, concatenated
     std::vector<int32_t> level_ps;     // page size per level
+    std::vector<int32_t> level_slot;   // pool slot of each level (levels with the same pools share one)
     std::vector<int32_t> merge_tab;  // [B*Hkv][merge_stride]
     std::vector<int32_t> leaf_tab;   // decode loop: [B][leaf_stride] suffix page ids
     std::vector<std::vector<int32_t>> cta_tc, cta_small;  // item ids per CTA of the fused kernel
@@ -321,7 +322,8 @@ void build_records(HostPlan &P)
         std::vector<int32_t> pages;
         auto add = [&](const WorkItem &w) {
             const int ps = P.level_ps[w.level];
-            const LevelDev &L = P.hdr.levels[w.level];
+            const int slot = P.level_slot[w.level];
+            const LevelDev &L = P.hdr.levels[slot];
             RecItem r{};
             r.seq_begin = w.seq_begin;
             r.n_seq = w.n_seq;
@@ -329,7 +331,7 @@ void build_records(HostPlan &P)
             r.k0 = w.k0;
             r.k1 = w.k1;
             r.part_row = w.part_row;
-            r.level = w.level;
+            r.level = slot;
             r.page_off = (int32_t)pages.size();
             r.ps = ps;
             r.box = L.tc_box;
@@ -431,7 +433,7 @@ hp_status validate_desc(const hp_tree_desc *d)
 {
     if (!d || !d->levels || d->num_levels < 1 || d->B < 1 || d->Hq < 1 || d->Hkv < 1 || d->Hq % d->Hkv)
         return HP_ERR_ARG;
-    if (d->num_levels > kMaxLevels || !supported_d(d->d) || d->Hq / d->Hkv > kTcTile)
+    if (d->num_levels > kMaxTreeLevels || !supported_d(d->d) || d->Hq / d->Hkv > kTcTile)
         return HP_ERR_UNSUPPORTED;
     for (int l = 0; l < d->num_levels; ++l) {
         const hp_tree_level &L = d->levels[l];
@@ -647,23 +649,39 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
     H.Hkv = d->Hkv;
     H.d = d->d;
     H.G = G;
-    H.num_levels = d->num_levels;
 
-    // page ids of all levels, concatenated
+    // page ids of all levels, concatenated; one pool slot per distinct pool set
     std::vector<int32_t> level_page_off(d->num_levels);
+    std::vector<int> slot_level;  // the first level of each slot
     P.level_ps.assign(d->num_levels, 0);
+    P.level_slot.assign(d->num_levels, 0);
     for (int l = 0; l < d->num_levels; ++l) {
         const hp_tree_level &L = d->levels[l];
         P.level_ps[l] = L.page_size;
         level_page_off[l] = (int32_t)P.page_ids.size();
         P.page_ids.insert(P.page_ids.end(), L.page_ids, L.page_ids + L.num_page_ids);
-        LevelDev &LD = H.levels[l];
-        LD.k_pool = L.k_pool;
-        LD.v_pool = L.v_pool;
-        LD.num_pages = L.num_pages;
-        LD.page_size = L.page_size;
-        LD.tc_box = std::gcd(L.page_size, kTcTile);
+        int slot = 0;
+        while (slot < (int)slot_level.size()) {
+            const hp_tree_level &S = d->levels[slot_level[slot]];
+            if (S.k_pool == L.k_pool && S.v_pool == L.v_pool && S.num_pages == L.num_pages &&
+                S.page_size == L.page_size)
+                break;
+            ++slot;
+        }
+        if (slot == (int)slot_level.size()) {
+            if (slot == kMaxLevels)
+                return HP_ERR_UNSUPPORTED;  // more distinct pools than a plan holds tensor maps for
+            slot_level.push_back(l);
+            LevelDev &LD = H.levels[slot];
+            LD.k_pool = L.k_pool;
+            LD.v_pool = L.v_pool;
+            LD.num_pages = L.num_pages;
+            LD.page_size = L.page_size;
+            LD.tc_box = std::gcd(L.page_size, kTcTile);
+        }
+        P.level_slot[l] = slot;
     }
+    H.num_levels = (int32_t)slot_level.size();
 
     plan_nodes(d, G, capacity, level_page_off, P);
 
@@ -775,11 +793,11 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
     build_contexts(d, P.contexts);
 
     if (encode) {
-        P.maps.resize((size_t)kMapsPerLevel * d->num_levels);
-        for (int l = 0; l < d->num_levels; ++l) {
-            const hp_tree_level &L = d->levels[l];
-            const int tcb = H.levels[l].tc_box;
-            CUtensorMap *m = &P.maps[(size_t)l * kMapsPerLevel];
+        P.maps.resize((size_t)kMapsPerLevel * slot_level.size());
+        for (size_t sl = 0; sl < slot_level.size(); ++sl) {
+            const hp_tree_level &L = d->levels[slot_level[sl]];
+            const int tcb = H.levels[sl].tc_box;
+            CUtensorMap *m = &P.maps[sl * kMapsPerLevel];
             if (!encode_pool_map(m + 0, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, tcb) ||
                 !encode_pool_map(m + 1, L.v_pool, L.num_pages, d->Hkv, L.page_size, d->d, tcb) ||
                 !encode_pool_map(m + 2, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk, nh) ||

@@ -12,7 +12,11 @@
 
 namespace hp {
 
+// A plan keeps pool information and tensor maps per distinct pool set (a
+// "pool slot": K pool, V pool, page count, page size), at most kMaxLevels of
+// them; a tree may have up to kMaxTreeLevels levels that share them.
 constexpr int kMaxLevels = 8;
+constexpr int kMaxTreeLevels = 64;
 constexpr uint32_t kPlanMagic = 0x31504C48u;  // "HLP1"
 constexpr int kTcTile = 128;                  // keys per tensor-core tile
 constexpr int kTcMaxRows = 256;               // query rows per tensor-core item (2 x M=128)
@@ -103,7 +107,7 @@ struct RecHead {
 };
 struct RecItem {
     int32_t seq_begin, n_seq, kvh, k0, k1, part_row;
-    int32_t level, page_off;
+    int32_t level, page_off;  // level: the pool slot (tensor maps) of the item's keys
     int32_t ps, box, num_pages;
     int32_t len_seq;  // decode-loop suffix items: the sequence whose current length ends [k0, k1); else -1
 };

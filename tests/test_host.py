@@ -420,3 +420,22 @@ def test_chunkattention_fig2_private_chunks_are_planned_as_one():
     assert by_seq[0] == {(lvl["C3"], ps)}
     assert by_seq[1] == {(lvl["C4"], 2 * ps)}
     assert by_seq[2] == {(lvl["C5"], 2 * ps)}
+
+
+def test_deep_trees_and_pool_slot_limit():
+    """Up to 64 levels plan as long as at most 8 distinct pool sets serve
+    them; 65 levels, or a ninth pool set, are rejected."""
+    pool = _pool()
+    node = [(0, 2, 16, 0)]
+    deep = [(pool.data_ptr(), pool.data_ptr(), 8, 16, node, [0]) for _ in range(64)]
+    assert hb.hp_cascade_plan_bytes(deep, 4, 4, 4, 128, num_sms=152) > 0
+    assert hb.hp_cascade_plan_bytes(deep + deep[:1], 4, 4, 4, 128, num_sms=152) == 0
+    bufs = [torch.zeros(64, dtype=torch.uint8) for _ in range(9)]
+    eight = [(b.data_ptr(), b.data_ptr(), 8, 16, node, [0]) for b in bufs[:8]]
+    assert hb.hp_cascade_plan_bytes(eight + eight[:4], 4, 4, 4, 128, num_sms=152) > 0
+    nine = [(b.data_ptr(), b.data_ptr(), 8, 16, node, [0]) for b in bufs]
+    assert hb.hp_cascade_plan_bytes(nine, 4, 4, 4, 128, num_sms=152) == 0
+    # the same pools with another page size are another pool set
+    other_ps = [(bufs[0].data_ptr(), bufs[0].data_ptr(), 8, 32, node, [0])]
+    assert hb.hp_cascade_plan_bytes(eight[:7] + other_ps, 4, 4, 4, 128, num_sms=152) > 0
+    assert hb.hp_cascade_plan_bytes(eight + other_ps, 4, 4, 4, 128, num_sms=152) == 0

@@ -602,3 +602,27 @@ def test_plans_of_the_gpu_random_trees_replayed():
         fin = np.isfinite(L)
         assert np.array_equal(np.isfinite(Lr), fin)
         np.testing.assert_allclose(Lr[fin], L[fin], atol=1e-12, err_msg=f"tree {seed}")
+
+
+def test_deep_chunk_tree_replayed():
+    """A ChunkAttention-style tree: a 64-token system prompt shared by all
+    sequences, then each sequence's private keys as a chain of 16-token
+    chunk nodes, one level per chunk (up to 20 levels).  The chunks of each
+    sequence plan as one node, and the replayed plan equals the definition."""
+    from shared_prefix_decode_gb300 import binding as hb
+    B, ps = 5, 16
+    lens = [0, 3, 7, 12, 19]  # chunks per sequence
+    levels = [[(0, B, 64)]] + [[(b, b + 1, ps) for b in range(B) if lens[b] > c] for c in range(max(lens))]
+    levels = [lv for lv in levels if lv]
+    wl = W.build_cascade("chunks", B=B, Hq=8, Hkv=2, d=64, page_size=ps, shared=levels, suffix_lens=[5] * B,
+                         seed=3)
+    assert len(wl.levels) == 21
+    items = hb.hp_cascade_plan_items(hb._levels_of(wl), wl.B, wl.Hq, wl.Hkv, wl.d)
+    # each sequence's chunks and suffix are one node at its first chunk's
+    # level; sequence 0 has no chunk, so its suffix stays at the last level
+    own = {(it["seq_begin"], it["level"]) for it in items if it["n_seq"] == 1}
+    assert own == {(0, 20)} | {(b, 1) for b in range(1, B)}
+    O, L = oracle.cascade(wl)
+    Or, Lr = _replay_plan(wl)
+    np.testing.assert_allclose(Or, O, atol=1e-12)
+    np.testing.assert_allclose(Lr, L, atol=1e-12)
