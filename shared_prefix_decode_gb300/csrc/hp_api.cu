@@ -199,7 +199,6 @@ struct PNode {
     int64_t kv_len;
     int32_t page_base;  // index in the plan's page-id list of the node's first page
     bool loop;          // a decode-loop suffix (grows at run time)
-    int fused;          // tree nodes it stands for
 };
 
 struct HostPlan {
@@ -610,14 +609,12 @@ void plan_nodes(const hp_tree_desc *d, int G, int capacity, const std::vector<in
             pn.seq_begin = N.seq_begin;
             pn.seq_end = N.seq_end;
             pn.loop = capacity > 0 && l == last;
-            pn.fused = 1;
             pn.kv_len = N.kv_len;
             pn.page_base = level_page_off[l] + N.page_off;
             const auto &ch = members[l][n];
             if (!ch.empty()) {
                 pn.kv_len = 0;
                 pn.page_base = (int32_t)P.page_ids.size();
-                pn.fused = (int)ch.size();
                 for (const auto &m : ch) {
                     const hp_tree_level &ML = d->levels[m.first];
                     const hp_tree_node &MN = ML.nodes[m.second];
