@@ -17,6 +17,11 @@
 //
 // Every partial (O, LSE) row goes to the workspace; the merge kernel, launched
 // as a programmatic dependent of this one, combines them.
+//
+// Two instantiations: the static step, and the decode loop's (Loop = true),
+// in which suffix items end at the sequences' current lengths on the device
+// and, with the append fused, the paged producer writes each sequence's new
+// token into its suffix pages before it loads that chunk.
 #include <cuda_runtime.h>
 
 #include "hp_internal.h"
