@@ -201,6 +201,14 @@ struct PNode {
     bool loop;          // a decode-loop suffix (grows at run time)
 };
 
+// One item for the scheduler: its modelled cost and its record bytes.
+struct Job {
+    double cost;
+    int32_t id;
+    bool tc;
+    int64_t rec_bytes;
+};
+
 struct HostPlan {
     PlanHeader hdr;
     std::vector<PNode> nodes;
@@ -212,6 +220,10 @@ struct HostPlan {
     std::vector<int32_t> merge_tab;  // [B*Hkv][merge_stride]
     std::vector<int32_t> leaf_tab;   // decode loop: [B][leaf_stride] suffix page ids
     std::vector<std::vector<int32_t>> cta_tc, cta_small;  // item ids per CTA of the fused kernel
+    // the items as scheduler jobs, longest first (tensor-core, paged, both),
+    // valid until make_items runs again
+    std::vector<Job> jobs_tc, jobs_sm, jobs_all;
+    bool jobs_ready = false;
     std::vector<std::vector<uint8_t>> records;           // one per CTA, without the tag
     std::vector<int32_t> contexts;  // (level, node, seq_begin, seq_end, pass) x n
 };
@@ -241,31 +253,43 @@ struct CostModel {
     }
 };
 
-struct Job {
-    double cost;
-    int32_t id;
-    bool tc;
-    int64_t rec_bytes;
-};
 
 // Longest-first greedy assignment of `jobs` to CTAs [c0, c1), each CTA's
 // record kept within kRecMaxBytes; false when a job fits no record.
-bool lpt(std::vector<Job> jobs, int c0, int c1, std::vector<double> &load, std::vector<int64_t> &used,
-         std::vector<std::vector<int32_t>> &tc_of, std::vector<std::vector<int32_t>> &sm_of, double start_cost)
+bool lpt(const std::vector<Job> &jobs, int c0, int c1, std::vector<double> &load, std::vector<int64_t> &used,
+         std::vector<int> &n_sm, std::vector<std::vector<int32_t>> *tc_of, std::vector<std::vector<int32_t>> *sm_of,
+         double start_cost)
 {
-    std::stable_sort(jobs.begin(), jobs.end(), [](const Job &a, const Job &b) { return a.cost > b.cost; });
+    // the least-loaded CTA with room in its record (the lowest index among
+    // equal loads), from a heap of (load, CTA)
+    using Slot = std::pair<double, int>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int c = c0; c < c1; ++c)
+        heap.push({load[c], c});
+    std::vector<Slot> full;
     for (const Job &j : jobs) {
         int best = -1;
-        for (int c = c0; c < c1; ++c)
-            if (used[c] + j.rec_bytes <= kRecMaxBytes && (best < 0 || load[c] < load[best]))
-                best = c;
+        while (!heap.empty()) {
+            const Slot e = heap.top();
+            heap.pop();
+            if (used[e.second] + j.rec_bytes <= kRecMaxBytes) {
+                best = e.second;
+                break;
+            }
+            full.push_back(e);
+        }
+        for (const Slot &e : full)
+            heap.push(e);
+        full.clear();
         if (best < 0)
             return false;
-        if (!j.tc && sm_of[best].empty())
+        if (!j.tc && n_sm[best]++ == 0)
             load[best] += start_cost;
-        (j.tc ? tc_of : sm_of)[best].push_back(j.id);
+        if (tc_of)
+            (j.tc ? *tc_of : *sm_of)[best].push_back(j.id);
         load[best] += j.cost;
         used[best] += j.rec_bytes;
+        heap.push({load[best], best});
     }
     return true;
 }
@@ -276,32 +300,48 @@ bool lpt(std::vector<Job> jobs, int c0, int c1, std::vector<double> &load, std::
 // grid: every CTA may take both, tensor-core items first).  Returns the
 // modelled makespan, or a negative value when the records cannot hold the
 // items.
-double schedule(HostPlan &P, int grid, int n_tc_ctas, bool mixed, int d, const CostModel &cm)
+double schedule(HostPlan &P, int grid, int n_tc_ctas, bool mixed, int d, const CostModel &cm, bool record = true)
 {
-    std::vector<Job> tcj, smj;
-    for (size_t i = 0; i < P.tc.size(); ++i) {
-        const WorkItem &w = P.tc[i];
-        tcj.push_back({cm.tc(w, P.hdr.G, d), (int32_t)i, true,
-                       (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
+    if (!P.jobs_ready) {
+        auto longest_first = [](std::vector<Job> &v) {
+            std::stable_sort(v.begin(), v.end(), [](const Job &a, const Job &b) { return a.cost > b.cost; });
+        };
+        P.jobs_tc.clear();
+        P.jobs_sm.clear();
+        for (size_t i = 0; i < P.tc.size(); ++i) {
+            const WorkItem &w = P.tc[i];
+            P.jobs_tc.push_back({cm.tc(w, P.hdr.G, d), (int32_t)i, true,
+                                 (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
+        }
+        const int nh = P.hdr.small_nh;
+        for (size_t j = 0; j < P.small.size(); ++j) {
+            const WorkItem &w = P.small[j];
+            P.jobs_sm.push_back({cm.small(w, d, nh), (int32_t)j, false,
+                                 (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
+        }
+        P.jobs_all = P.jobs_tc;
+        P.jobs_all.insert(P.jobs_all.end(), P.jobs_sm.begin(), P.jobs_sm.end());
+        longest_first(P.jobs_tc);
+        longest_first(P.jobs_sm);
+        longest_first(P.jobs_all);
+        P.jobs_ready = true;
     }
-    const int nh = P.hdr.small_nh;
-    for (size_t j = 0; j < P.small.size(); ++j) {
-        const WorkItem &w = P.small[j];
-        smj.push_back({cm.small(w, d, nh), (int32_t)j, false,
-                       (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
-    }
+    const std::vector<Job> &tcj = P.jobs_tc, &smj = P.jobs_sm;
     std::vector<double> load(grid, cm.cta);
     std::vector<int64_t> used(grid, (int64_t)sizeof(RecHead));
-    P.cta_tc.assign(grid, {});
-    P.cta_small.assign(grid, {});
+    std::vector<int> n_sm(grid, 0);
+    auto *tc_of = record ? &P.cta_tc : nullptr;
+    auto *sm_of = record ? &P.cta_small : nullptr;
+    if (record) {
+        P.cta_tc.assign(grid, {});
+        P.cta_small.assign(grid, {});
+    }
     bool ok;
     if (n_tc_ctas >= grid) {
-        std::vector<Job> all = tcj;
-        all.insert(all.end(), smj.begin(), smj.end());
-        ok = lpt(all, 0, grid, load, used, P.cta_tc, P.cta_small, cm.sm_start);
+        ok = lpt(P.jobs_all, 0, grid, load, used, n_sm, tc_of, sm_of, cm.sm_start);
     } else {
-        ok = lpt(tcj, 0, n_tc_ctas, load, used, P.cta_tc, P.cta_small, cm.sm_start) &&
-             lpt(smj, mixed ? 0 : n_tc_ctas, grid, load, used, P.cta_tc, P.cta_small, cm.sm_start);
+        ok = lpt(tcj, 0, n_tc_ctas, load, used, n_sm, tc_of, sm_of, cm.sm_start) &&
+             lpt(smj, mixed ? 0 : n_tc_ctas, grid, load, used, n_sm, tc_of, sm_of, cm.sm_start);
     }
     if (!ok)
         return -1.0;
@@ -370,6 +410,7 @@ int64_t make_items(const hp_tree_desc *d, int G, int nh, int64_t tc_split, int64
 {
     P.tc.clear();
     P.small.clear();
+    P.jobs_ready = false;
     int64_t part = 0;
     for (const PNode &N : P.nodes) {
         const int l = N.level;
@@ -715,12 +756,17 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
     bool best_mixed = false;
     if (tc_tiles > 0 && small_chunks > 0 && sms > 1) {
         double best = -1.0;
+        int64_t made_ts = -1, made_ss = -1;  // the splits P's items were made for
         for (int mixed = 0; mixed < 2; ++mixed)
             for (int k = 1; k < sms; ++k) {
                 int64_t ts, ss;
                 splits_for(k, ts, ss);
-                make_items(d, G, nh, ts, ss, P, nullptr, capacity);
-                const double t = schedule(P, sms, k, mixed != 0, d->d, cm);
+                if (ts != made_ts || ss != made_ss) {
+                    make_items(d, G, nh, ts, ss, P, nullptr, capacity);
+                    made_ts = ts;
+                    made_ss = ss;
+                }
+                const double t = schedule(P, sms, k, mixed != 0, d->d, cm, false);
                 if (t >= 0.0 && (best < 0.0 || t < best)) {
                     best = t;
                     best_k = k;
