@@ -15,12 +15,15 @@ max(prefix FLOPs / bf16 peak, unique KV bytes / HBM peak).
 Timing: inputs resident in HBM; R distinct input sets (own pools, tables, q
 and plan each) are rotated so that R x working set exceeds 3x the L2 size
 read at run time, which keeps every step's KV cold in L2; the sets share one
-workspace (partial states), as a decode loop reuses one.  One CUDA graph
-holds 4R consecutive steps (four rounds of the input sets), as a decode loop
-captures its whole forward pass (so steps follow one another kernel to
-kernel, not graph launch to graph launch); a remainder replays one-step
-graphs.  CUDA events on the launching stream, W warm-up steps, exactly K
-timed steps, barrier + synchronize on both sides, max over ranks.
+workspace (partial states), as a decode loop reuses one.  The K timed steps
+are consecutive steps captured in CUDA graphs (one graph of all K steps when
+K <= --graph-max; otherwise graphs of --graph-max steps and one of the
+remainder), so steps follow one another kernel to kernel, as in a captured
+forward pass.  A timed pass is exactly K steps between CUDA events on the
+launching stream, bracketed by a barrier and a synchronize; passes repeat
+until --min-timed-s seconds of GPU time (at least 20 passes), after W
+warm-up steps.  ms_per_step is the median pass / K (min and p90 alongside),
+the max over ranks of each pass.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hp|reference]
 Prints one JSON line (rank 0).
@@ -48,14 +51,19 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000, help="K: consecutive steps per timed pass")
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["hp", "reference"], default="hp")
     ap.add_argument("--config", default="llama3_8b")
+    ap.add_argument("--part", choices=["all", "prefix", "suffix"], default="all",
+                    help="time the whole step, or its shared levels / private suffixes alone")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: enough for 3x L2)")
-    ap.add_argument("--graph-steps", type=int, default=0,
-                    help="steps per CUDA graph: 0 = four rounds of the input sets, 1 = one graph per step")
+    ap.add_argument("--graph-max", type=int, default=256, help="most steps captured in one CUDA graph")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="timed passes repeat until this much GPU time (at least 20 passes)")
     ap.add_argument("--no-naive", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the warm-L2, one-pass, per-workload and one-graph-per-step figures")
     ap.add_argument("--loop-steps", type=int, default=64,
                     help="decode-loop measurement: steps per input set in one graph (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -175,13 +183,34 @@ def run_reference(args, rank: int):
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "us_per_step": t_step * 1e6,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(wl, None),
+        "config": workload_config(wl, l2_plan(wl, device_l2_bytes())[1]),
         "cpu_baseline": {"value": val, "unit": "TB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{len(sample)} of {len(rows_all)} output rows per step (seed 0), "
                                    f"scaled to the full step"},
         "e2e": {"value": val, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def l2_plan(wl, l2: int, n_sets: int = 0):
+    """Input sets to rotate (R x working set >= 3x L2, at least 2) and the
+    config note that says so."""
+    set_bytes = wl.unique_kv_bytes() + wl.q.numel() * 2 * 2
+    R = n_sets or max(2, math.ceil(3 * l2 / set_bytes))
+    return R, f"cold: rotating {R} input sets, {R * set_bytes / 1e6:.0f} MB >= 3x L2 ({l2 / 2**20:.0f} MiB); no flush"
+
+
+def device_l2_bytes() -> int:
+    """L2 size of the current CUDA device (GB300's 126 MiB when none)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            v = int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0) or 0)
+            if v > 0:
+                return v
+    except Exception:
+        pass
+    return 126 * 2 ** 20
 
 
 def workload_config(wl, l2_note):
@@ -194,6 +223,8 @@ def workload_config(wl, l2_note):
            "prefix_flops": wl.shared_flops()}
     if l2_note:
         cfg["l2"] = l2_note
+    if getattr(wl, "part", "all") != "all":
+        cfg["part"] = wl.part
     return cfg
 
 
@@ -237,6 +268,101 @@ def whole_job_tbs(world: int, bytes_per_step: float, us_step: float) -> float:
     return world * bytes_per_step / (us_step * 1e-6) / 1e12
 
 
+# ------------------------------------------------------------ graph timing
+class StepGraphs:
+    """CUDA graphs of consecutive steps over `items` in rotation order (step i
+    uses items[i % R]): a pass of exactly K steps is K // full replays of a
+    graph of `full` steps (a multiple of R, so it starts every replay at item
+    0) and one replay of a graph of the remaining K % full steps."""
+
+    def __init__(self, fn, items, K: int, graph_max: int, stream):
+        import torch
+        R = len(items)
+        self.K = K
+        self.full = R * max(1, graph_max // R)
+        self.n_full = K // self.full if K >= self.full else 0
+        rem = K - self.n_full * self.full
+
+        def capture(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    fn(items[i % R])
+            return g
+
+        self.g_full = capture(self.full) if self.n_full > 0 else None
+        self.g_rem = capture(rem) if rem > 0 else None
+
+    def run_pass(self):
+        for _ in range(self.n_full):
+            self.g_full.replay()
+        if self.g_rem is not None:
+            self.g_rem.replay()
+
+
+def timed_passes(graphs: StepGraphs, warmup: int, min_s: float, stream, dev, dist, min_passes: int = 20,
+                 max_passes: int = 20000):
+    """Warm-up passes (at least `warmup` steps), then timed passes of exactly
+    K steps each, every pass between CUDA events on `stream`, a barrier and a
+    synchronize on both sides; at least `min_passes` and until `min_s` seconds
+    of GPU time.  Returns (per-pass ms, max over ranks; wall start; wall end)."""
+    import torch
+    K = graphs.K
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(warmup / K))):
+            graphs.run_pass()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+    times = []
+    n_target = min_passes
+    t_wall0 = time.time()
+    i = 0
+    while i < n_target:
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = ev[i & 1]
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            graphs.run_pass()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+        i += 1
+        if i == min_passes:
+            # passes for min_s of GPU time, the same count on every rank
+            med = statistics.median(times)
+            want = min(max_passes, max(min_passes, math.ceil(min_s * 1e3 / max(med, 1e-6))))
+            n_target = int(job_time_ms(float(want), dist, dev))
+    t_wall1 = time.time()
+    barrier()
+    if dist is not None:
+        t = torch.tensor(times, dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        times = t.tolist()
+    return times, t_wall0, t_wall1
+
+
+def pass_stats(times_ms, K: int) -> dict:
+    """Per-step microseconds of the timed passes: median, min, p90."""
+    per = sorted(t * 1e3 / K for t in times_ms)
+    p90 = per[min(len(per) - 1, int(math.ceil(0.9 * len(per))) - 1)]
+    return {"median_us": statistics.median(per), "min_us": per[0], "p90_us": p90, "passes": len(per)}
+
+
+def roofline_step(bytes_step: float, flops_step: float, us_step: float, peaks: dict) -> dict:
+    t_bytes = bytes_step / (peaks["hbm_gbs"] * 1e9)
+    t_flops = flops_step / (peaks["bf16_tflops"] * 1e12)
+    roof_us = max(t_bytes, t_flops) * 1e6
+    return {"bound": "hbm" if t_bytes >= t_flops else "tensor", "roofline_us": roof_us, "frac": roof_us / us_step,
+            "t_bytes_us": t_bytes * 1e6, "t_flops_us": t_flops * 1e6, "unique_kv_bytes": bytes_step,
+            "prefix_flops": flops_step}
+
+
 # -------------------------------------------------------------------- main
 def main():
     args = parse_args()
@@ -246,6 +372,8 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps must be >= 1 and --warmup >= 0")
 
     import numpy as np
     import torch
@@ -261,67 +389,52 @@ def main():
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
     peaks, peak_src = load_peaks()
-
-    # ---------------------------------------------------------- inputs
-    wl0 = make_config(args.config, seed=1000 * rank)
-    set_bytes = wl0.unique_kv_bytes() + wl0.q.numel() * 2 * 2
-    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
-    R = args.sets or max(2, math.ceil(3 * l2 / set_bytes))
-    sets = []
-    for i in range(R):
-        wl = wl0 if i == 0 else make_config(args.config, seed=1000 * rank + i)
-        wg = wl.to(dev)
-        plan = hb.CascadePlan.from_workload(wg)
-        # O and LSE share one buffer, so a host read of the result is one copy
-        n_o = wl.B * wl.Hq * wl.d * 2
-        res = torch.empty(n_o + wl.B * wl.Hq * 4, dtype=torch.uint8, device=dev)
-        out = res[:n_o].view(torch.bfloat16).view(wl.B, wl.Hq, wl.d)
-        lse = res[n_o:].view(torch.float32).view(wl.B, wl.Hq)
-        sets.append({"wl": wl, "wg": wg, "plan": plan, "out": out, "lse": lse, "res": res})
-    l2_note = (f"rotating {R} input sets, {R * set_bytes / 1e6:.0f} MB >= 3x L2 ({l2 / 2**20:.0f} MiB); "
-               f"no flush")
-    # steps per graph: whole rounds of the input sets when at least one round
-    gsteps = 4 * R if args.graph_steps <= 0 else args.graph_steps
-    if gsteps > R:
-        gsteps = (gsteps + R - 1) // R * R
-    # one workspace for every input set, as a decode loop reuses one buffer
-    ws_shared = hb.alloc_workspace(max(s["plan"].info.ws_bytes for s in sets), dev)
-    for s in sets:
-        s["plan"].ws = ws_shared
-    info = sets[0]["plan"].info
-    kernels_per_step = int(info.n_tc_items + info.n_small_items > 0) + 1
+    K = args.steps
     stream = torch.cuda.Stream(device=dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
+
+    def make_sets(name, part, seed0, n_sets=0, device=None):
+        """Input sets of one workload (R of them: R x working set >= 3x L2,
+        at least 2), each with its plan and a result buffer; one workspace
+        shared by all."""
+        first = make_config(name, seed=seed0, part=part, device=device)
+        R, note = l2_plan(first, l2, n_sets)
+        out = []
+        for i in range(R):
+            wl = first if i == 0 else make_config(name, seed=seed0 + i, part=part, device=device)
+            wg = wl.to(dev)
+            plan = hb.CascadePlan.from_workload(wg)
+            # O and LSE share one buffer, so a host read of the result is one copy
+            n_o = wl.B * wl.Hq * wl.d * 2
+            res = torch.empty(n_o + wl.B * wl.Hq * 4, dtype=torch.uint8, device=dev)
+            o = res[:n_o].view(torch.bfloat16).view(wl.B, wl.Hq, wl.d)
+            ls = res[n_o:].view(torch.float32).view(wl.B, wl.Hq)
+            out.append({"wl": wl, "wg": wg, "plan": plan, "out": o, "lse": ls, "res": res})
+        ws = hb.alloc_workspace(max(s["plan"].info.ws_bytes for s in out), dev)
+        for s in out:
+            s["plan"].ws = ws
+        return out, ws, note
 
     def step(s, st=None):
         hb.hp_cascade_decode(s["plan"], s["wg"].q, s["wl"].scale, out=s["out"], lse=s["lse"], stream=st)
 
-    # warm up eagerly, check status, then capture one graph per input set
-    with torch.cuda.stream(stream):
-        for s in sets:
-            step(s, stream)
-    torch.cuda.synchronize(dev)
-    for s in sets:
-        st = hb.hp_read_device_status(s["plan"].ws)
+    def warm_and_check(items, fn, ws):
+        with torch.cuda.stream(stream):
+            for it in items:
+                fn(it)
+        torch.cuda.synchronize(dev)
+        st = hb.hp_read_device_status(ws)
         if st != 0:
             raise RuntimeError(f"device status {hb.status_str(st)}")
 
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            fn()
-        return g
-
-    def capture_runs(fn, items):
-        """One-step graphs and, when gsteps > 1, graphs of gsteps consecutive
-        steps in rotation order: {first item: graph}."""
-        singles = [capture(lambda it=it: fn(it)) for it in items]
-        runs = {}
-        if gsteps > 1:
-            for k in range(0, max(1, len(items) - gsteps + 1), gsteps):
-                runs[k] = capture(lambda k=k: [fn(items[(k + i) % len(items)]) for i in range(gsteps)])
-        return singles, runs
-
-    graphs = capture_runs(lambda s: step(s, stream), sets)
+    # ---------------------------------------------------------- inputs
+    sets, ws_shared, l2_note = make_sets(args.config, args.part, 1000 * rank, args.sets)
+    R = len(sets)
+    wl0 = sets[0]["wl"]
+    info = sets[0]["plan"].info
+    kernels_per_step = int(info.n_tc_items + info.n_small_items > 0) + 1
+    warm_and_check(sets, lambda s: step(s, stream), ws_shared)
+    graphs = StepGraphs(lambda s: step(s, stream), sets, K, args.graph_max, stream)
     torch.cuda.synchronize(dev)
 
     # parity spot check on rank 0 (oracle on a few rows of set 0)
@@ -332,62 +445,27 @@ def main():
         rows = [(b, h) for b in range(0, wl0.B, max(1, wl0.B // 8)) for h in range(0, wl0.Hq, max(1, wl0.Hq // 4))]
         O, L = oracle.cascade(wl0, rows)
         o = sets[0]["out"].float().cpu().numpy()
-        l = sets[0]["lse"].cpu().numpy()
+        lv = sets[0]["lse"].cpu().numpy()
         ob = np.stack([o[b, h] for b, h in rows])
-        lb = np.array([l[b, h] for b, h in rows])
+        lb = np.array([lv[b, h] for b, h in rows])
         parity = {"rows": len(rows), "max_abs_o": float(np.abs(ob - O).max()),
                   "max_abs_lse": float(np.abs(lb - L).max())}
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def replay(graph_runs, n):
-        """Replays exactly n steps in rotation order: whole multi-step graphs
-        where they fit, one-step graphs for the rest."""
-        singles, runs = graph_runs
-        i = 0
-        while i < n:
-            k = i % len(singles)
-            if k in runs and n - i >= gsteps:
-                runs[k].replay()
-                i += gsteps
-            else:
-                singles[k].replay()
-                i += 1
-
-    def timed(graph_runs, steps, warmup):
-        replay(graph_runs, warmup)
-        torch.cuda.synchronize(dev)
-        barrier()
-        torch.cuda.synchronize(dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        t_wall0 = time.time()
-        e0.record(stream)
-        with torch.cuda.stream(stream):
-            replay(graph_runs, steps)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        t_wall1 = time.time()
-        barrier()
-        ms = job_time_ms(e0.elapsed_time(e1), dist, dev)
-        return ms, t_wall0, t_wall1
 
     clocks = ClockSampler(getattr(props, "uuid", "") and str(props.uuid))
     clocks.start()
     time.sleep(0.3)
-    ms, tw0, tw1 = timed(graphs, args.steps, args.warmup)
+    times, tw0, tw1 = timed_passes(graphs, args.warmup, args.min_timed_s, stream, dev, dist)
     clock_summary = clocks.summary(tw0, tw1)
     clocks.stop()
-
-    us_step = ms * 1e3 / args.steps
+    stats = pass_stats(times, K)
+    us_step = stats["median_us"]
     bytes_per_step = statistics.mean(s["wl"].unique_kv_bytes() for s in sets)
     flops_per_step = statistics.mean(s["wl"].shared_flops() for s in sets)
     value = whole_job_tbs(world, bytes_per_step, us_step)
-    t_bytes = bytes_per_step / (peaks["hbm_gbs"] * 1e9)
-    t_flops = flops_per_step / (peaks["bf16_tflops"] * 1e12)
-    roof_us = max(t_bytes, t_flops) * 1e6
+    roof = dict(roofline_step(bytes_per_step, flops_per_step, us_step, peaks), peak_source=peak_src)
+    timing = dict(stats, steps_per_pass=K, graph_steps=min(K, graphs.full), timed_s=sum(times) / 1e3,
+                  form="CUDA graphs of the K consecutive steps (rotating input sets), one pass per timed "
+                       "region; median / min / p90 over passes")
 
     # ------------------------------------------- per-kernel event pass
     ev_sets = []
@@ -395,13 +473,14 @@ def main():
         evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
         for e in evs:
             e.record(stream)  # creates the CUDA event behind the handle
-        g = capture(lambda s=s, evs=evs: hb.hp_cascade_decode_profiled(
-            s["plan"], s["wg"].q, s["wl"].scale, s["out"], s["lse"], evs, stream=stream))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            hb.hp_cascade_decode_profiled(s["plan"], s["wg"].q, s["wl"].scale, s["out"], s["lse"], evs,
+                                          stream=stream)
         ev_sets.append((g, evs))
     torch.cuda.synchronize(dev)
     k_ms = {"cascade": [], "merge": []}
-    passes = max(1, min(200, args.steps // max(R, 1)))
-    for _ in range(passes):
+    for _ in range(max(3, min(200, 2000 // max(R, 1)))):
         for g, _ in ev_sets:
             g.replay()
         torch.cuda.synchronize(dev)
@@ -415,8 +494,8 @@ def main():
         tot = 0
         for lv in wl.levels:
             for sb, se, kl, _ in lv.nodes.tolist():
-                rows = (se - sb) * wl.G
-                if (rows > 16) == shared:
+                rows_ = (se - sb) * wl.G
+                if (rows_ > 16) == shared:
                     tot += kl * wl.Hkv * wl.d * 4
         return tot
 
@@ -449,11 +528,12 @@ def main():
         step(s, stream)
         s["res_host"].copy_(s["res"], non_blocking=True)  # O and LSE
 
-    e2e_graphs = capture_runs(e2e_step, sets)
-    e2e_steps = args.steps
-    ms_e2e, _, _ = timed(e2e_graphs, e2e_steps, min(args.warmup, 50))
-    us_e2e = ms_e2e * 1e3 / e2e_steps
+    e2e_graphs = StepGraphs(e2e_step, sets, K, args.graph_max, stream)
+    t_e2e, _, _ = timed_passes(e2e_graphs, min(args.warmup, 50), min(args.min_timed_s, 0.5), stream, dev, dist)
+    st_e2e = pass_stats(t_e2e, K)
+    us_e2e = st_e2e["median_us"]
     e2e = {"value": whole_job_tbs(world, bytes_per_step, us_e2e), "unit": "TB/s", "us_per_step": us_e2e,
+           "min_us": st_e2e["min_us"], "p90_us": st_e2e["p90_us"],
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "path": "pinned host q -> device, hp_cascade_decode, device O and LSE (one buffer) -> pinned host"}
 
@@ -477,13 +557,15 @@ def main():
             for n in nsets:
                 nstep(n)
         torch.cuda.synchronize(dev)
-        ngraphs = capture_runs(nstep, nsets)
-        nk = max(R, min(args.steps, 2000))
-        ms_n, _, _ = timed(ngraphs, nk, min(args.warmup, 20))
-        naive = {"us_per_step": ms_n * 1e3 / nk, "steps": nk,
+        nk = 4 * R
+        t_n, _, _ = timed_passes(StepGraphs(nstep, nsets, nk, args.graph_max, stream), min(args.warmup, 20), 0.2,
+                                 stream, dev, dist)
+        st_n = pass_stats(t_n, nk)
+        naive = {"us_per_step": st_n["median_us"], "min_us": st_n["min_us"], "p90_us": st_n["p90_us"],
+                 "steps_per_pass": nk, "passes": st_n["passes"],
                  "kernel": "per-sequence paged decode over the whole context (prefix pages aliased, "
                            "re-read per sequence)",
-                 "speedup_of_cascade": (ms_n / nk) / (ms / args.steps)}
+                 "speedup_of_cascade": st_n["median_us"] / us_step}
 
     # ------------------------------------------------------ decode loop
     # The same workload as a decode loop: each step appends one token per
@@ -493,7 +575,7 @@ def main():
     # suffix lengths; the pools are not reset (each replay rewrites the same
     # slots).
     loop = None
-    if args.loop_steps > 0:
+    if args.loop_steps > 0 and args.part == "all":
         from shared_prefix_decode_gb300.workloads import decode_tokens, with_suffix_capacity
         T = args.loop_steps
         lsets = []
@@ -529,8 +611,14 @@ def main():
         if st != 0:
             raise RuntimeError(f"decode loop: device status {hb.status_str(st)}")
         n_loop = T * len(lsets)
-        reps = max(3, min(200, args.steps // n_loop))
+        reps = max(3, min(200, 20000 // n_loop))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def capture(fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            return g
 
         def time_graph(g):
             for _ in range(2):
@@ -566,11 +654,68 @@ def main():
         grow = lsets[0]["wl"].B * (T + 1) / 2 * wl0.Hkv * wl0.d * 4
         loop_bytes = bytes_per_step + grow
         loop = {"us_per_step": us_loop, "value": whole_job_tbs(world, loop_bytes, us_loop), "unit": "TB/s",
+                "roofline_frac": loop_bytes / (peaks["hbm_gbs"] * 1e9) / (us_loop * 1e-6),
                 "steps_per_graph": n_loop, "graph_replays": reps, "loop_steps": T,
                 "kernels_per_step": 2, "mean_kv_bytes_per_step": loop_bytes,
                 "separate_append_us_per_step": us_sep, "decode_only_us_per_step": us_dec,
                 "step": "hp_cascade_decode_append: the token written by the persistent kernel, the length advanced "
                         "by the merge (plan built once; suffix lengths on the device)"}
+        del lsets
+
+    # ------------------------------------------------------- extras
+    extras = None
+    if not args.no_extras:
+        extras = {}
+
+        def measure(items, ws, bytes_step, flops_step, k_steps, min_s=0.2):
+            warm_and_check(items, lambda s: step(s, stream), ws)
+            g = StepGraphs(lambda s: step(s, stream), items, k_steps, args.graph_max, stream)
+            t, _, _ = timed_passes(g, 2 * len(items), min_s, stream, dev, dist)
+            stt = pass_stats(t, k_steps)
+            return dict(stt, steps_per_pass=k_steps, tbs=bytes_step / (stt["median_us"] * 1e-6) / 1e12,
+                        roofline=roofline_step(bytes_step, flops_step, stt["median_us"], peaks))
+
+        # the same K steps on one input set over and over (its KV stays in L2)
+        extras["warm_l2"] = dict(measure([sets[0]], ws_shared, wl0.unique_kv_bytes(), wl0.shared_flops(), K),
+                                 note="WARM L2: input set 0 every step (53 MB < L2), not the cold-L2 headline")
+        # the one-graph-per-step form (each step its own graph launch)
+        singles = [StepGraphs(lambda s: step(s, stream), [sets[i]], 1, 1, stream) for i in range(R)]
+
+        class _PerStep:
+            K = 4 * R
+
+            @staticmethod
+            def run_pass():
+                for j in range(4 * R):
+                    singles[j % R].run_pass()
+
+        t1g, _, _ = timed_passes(_PerStep, R, 0.2, stream, dev, dist)
+        extras["graph_per_step"] = dict(pass_stats(t1g, 4 * R),
+                                        note="one CUDA graph launch per step (graph launch overhead included)")
+        # the step's passes alone (same kernels, same shapes)
+        if args.part == "all":
+            for part in ("prefix", "suffix"):
+                ps_sets, ps_ws, _ = make_sets(args.config, part, 1000 * rank + 500, device=dev)
+                b = statistics.mean(s["wl"].unique_kv_bytes() for s in ps_sets)
+                f = statistics.mean(s["wl"].shared_flops() for s in ps_sets)
+                extras[f"{part}_only"] = measure(ps_sets, ps_ws, b, f, 4 * len(ps_sets))
+                del ps_sets, ps_ws
+                torch.cuda.empty_cache()
+        # the other workloads at full size, cold L2
+        per_cfg = {}
+        for name in ("codellama13b", "tree2", "doc_streams", "no_sharing"):
+            if name == args.config:
+                continue
+            c_sets, c_ws, c_note = make_sets(name, "all", 1000 * rank + 700, device=dev)
+            b = statistics.mean(s["wl"].unique_kv_bytes() for s in c_sets)
+            f = statistics.mean(s["wl"].shared_flops() for s in c_sets)
+            per_cfg[name] = dict(measure(c_sets, c_ws, b, f, 8 * len(c_sets)), l2=c_note,
+                                 plan={"tc_items": c_sets[0]["plan"].info.n_tc_items,
+                                       "small_items": c_sets[0]["plan"].info.n_small_items,
+                                       "part_rows": c_sets[0]["plan"].info.n_part_rows})
+            del c_sets, c_ws
+            torch.cuda.empty_cache()
+        extras["workloads"] = per_cfg
 
     # ---------------------------------------------------- cpu baseline
     cpu = None
@@ -586,25 +731,42 @@ def main():
         cpu = {"value": wl0.unique_kv_bytes() / t_cpu / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
                "sample": f"the full step of input set 0 ({wl0.B * wl0.Hq} output rows), {reps} repeats",
                "us_per_step": t_cpu * 1e6}
+        # one thread, the tiny workload (whole steps) and this workload (a
+        # sample of its rows, scaled to the full step)
+        oracle.set_num_threads(1)
+        one = {}
+        tiny = make_config("tiny", seed=0)
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 1.0 or reps < 1:
+            oracle.cascade(tiny)
+            reps += 1
+        one["tiny_us_per_step"] = (time.perf_counter() - t0) / reps * 1e6
+        rows_all = [(b, h) for b in range(wl0.B) for h in range(wl0.Hq)]
+        sample = rows_all[::16]
+        t0 = time.perf_counter()
+        oracle.cascade(wl0, sample)
+        one[f"{wl0.name}_us_per_step"] = (time.perf_counter() - t0) * len(rows_all) / len(sample) * 1e6
+        one["sample"] = f"tiny: whole steps; {wl0.name}: {len(sample)} of {len(rows_all)} rows, scaled"
+        cpu["one_thread"] = one
+        oracle.set_num_threads(cores)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": us_step / 1e3, "us_per_step": us_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": dict(workload_config(wl0, l2_note), graph_steps=gsteps),
-            "roofline_step": {"bound": "hbm" if t_bytes >= t_flops else "tensor", "roofline_us": roof_us,
-                              "frac": roof_us / us_step, "t_bytes_us": t_bytes * 1e6, "t_flops_us": t_flops * 1e6,
-                              "unique_kv_bytes": bytes_per_step, "prefix_flops": flops_per_step,
-                              "peak_source": peak_src},
+            "data": "synthetic", "config": workload_config(wl0, l2_note),
+            "timing": timing,
+            "roofline_step": roof,
             "roofline": roofline,
             "kernels_us": k_us,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": kernels_per_step * args.steps,
+            "gpu_launches": kernels_per_step * K,
             "clocks": clock_summary,
             "naive": naive,
             "decode_loop": loop,
+            "extras": extras,
             "parity_spot": parity,
             "plan": {"tc_items": info.n_tc_items, "small_items": info.n_small_items, "grid": info.grid,
                      "part_rows": info.n_part_rows},

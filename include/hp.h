@@ -113,15 +113,18 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
  * Arguments and results are those of hp_suffix_decode_paged without the
  * workspace.  Scratch lives in one fixed 16 MiB device array inside the
  * library, resident on every GPU that loads the library until the process
- * exits; the call itself allocates and frees nothing.  Each call needs
- * B*Hq*(d+1)*4 bytes per key split; the call picks splits that fit and
- * returns HP_ERR_WORKSPACE when even one split per sequence does not
- * (B*Hq above about 32,000 rows at d = 128).  The first call on each device
- * looks up the array's device address (a host call made with that device
- * current); make that first call before any stream capture.  All calls share
- * the array and it keeps the last call's contents: calls that run at the same
- * time on the GPU race with each other, so serialise them.  Device bounds
- * errors are not reported (there is no status word to read back).
+ * exits; the call itself allocates and frees nothing.  Each key split of a
+ * call needs B*Hq partial rows of 2*d + 4 bytes (a bf16 O row and its f32
+ * LSE); the call picks the fewest splits of at least 64 keys that fit, and
+ * returns HP_ERR_WORKSPACE when even one split does not: B*Hq above 64,525
+ * rows at d = 128, 127,096 at d = 64.  The first call in each CUDA context
+ * (the first on a device, and the first after cudaDeviceReset) looks up the
+ * array's device address, a host call made with that device current; make
+ * that first call before any stream capture.  All calls share the array and
+ * it keeps the last call's contents: calls that run at the same time on the
+ * GPU race with each other, so serialise them.  The kernels keep a status
+ * word at the start of the array (cleared by each call), but it is not
+ * returned to the caller: device bounds errors go unreported.
  * ------------------------------------------------------------------------- */
 hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb, int64_t q_sh, int32_t B,
                                          const void *k_pool, const void *v_pool,
@@ -237,11 +240,7 @@ hp_status hp_cascade_plan(const hp_tree_desc *desc, void *plan_dev, size_t plan_
  * wrote there in this process, and info must describe a plan no larger than
  * it (HP_ERR_ARG otherwise, before any launch); an info of another plan of the
  * same size is reported by the kernels through the status word.
- * No host synchronisation, no allocation; graph-capturable.
- * Failure detection tests only: with HP_TEST_WITHHOLD_TILE=1 in the
- * environment, CTA 0 arms its first key tile's barrier but issues no copy;
- * its bounded waits run out and the step reports HP_ERR_DEVICE_TIMEOUT
- * through the status word (results of that step are not valid). */
+ * No host synchronisation, no allocation; graph-capturable. */
 hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, const void *q,
                             int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,
                             int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
@@ -381,6 +380,14 @@ int32_t hp_cascade_plan_merge_table(const hp_tree_desc *desc, int32_t capacity, 
  * or HP_ERR_CUDA.
  * ------------------------------------------------------------------------- */
 hp_status hp_read_device_status(void *ws, hp_stream_t stream);
+
+/* Failure detection tests only.  While enabled (non-zero), every
+ * hp_cascade_decode* launch makes CTA 0 arm its first key tile's barrier
+ * but issue no copy: its bounded waits (2 s each) run out, the CTA drains and
+ * returns, and the step reports HP_ERR_DEVICE_TIMEOUT through the status word
+ * (that step's results are not valid; later steps are correct).  A
+ * process-wide switch, off by default; it never faults the GPU. */
+void hp_test_withhold_first_tile(int32_t enable);
 
 /* Library build information: the SM architecture compiled for (103 for
  * sm_103a) and the library ABI version. */

@@ -86,6 +86,7 @@ _SIGNATURES = {
     "hp_cascade_plan_item_pages": (c_i64, [ctypes.POINTER(HpTreeDesc), c_i32, ctypes.POINTER(c_i64),
                                            ctypes.POINTER(c_i32), c_i64]),
     "hp_read_device_status": (c_i32, [c_vp, c_vp]),
+    "hp_test_withhold_first_tile": (None, [c_i32]),
 }
 
 _lib = None

@@ -153,6 +153,9 @@ uint64_t new_tag()
 
 uint32_t *status_ptr(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
 
+// Failure detection tests: set by hp_test_withhold_first_tile.
+std::atomic<int> g_withhold{0};
+
 // Plans this library wrote, by device address: the persistent kernel copies
 // its schedule record from plan + kPlanRecOff + cta * rec_stride before it can
 // check the plan's tag, so a decode call is only launched when the grid and
@@ -623,12 +626,8 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         cp.part_o = part_o;
         cp.part_lse = part_lse;
         cp.status = status_ptr(ws);
-        // Failure detection test hook: with HP_TEST_WITHHOLD_TILE=1 in the
-        // environment, CTA 0 arms its first K tile's barrier without issuing
-        // the copy; its bounded waits then run out, and the step reports
-        // HP_ERR_DEVICE_TIMEOUT through the status word.
-        const char *wh = std::getenv("HP_TEST_WITHHOLD_TILE");
-        cp.withhold = wh != nullptr && wh[0] == '1';
+        // failure detection tests only (hp_test_withhold_first_tile)
+        cp.withhold = g_withhold.load(std::memory_order_relaxed);
         cp.suffix_len = suffix_len;
         cp.loop_capacity = ext.loop_capacity;
         cp.k_new = static_cast<const uint16_t *>(k_new);
@@ -845,6 +844,8 @@ int32_t hp_cascade_plan_merge_table(const hp_tree_desc *desc, int32_t capacity, 
                     sizeof(int32_t) * (size_t)std::min<int64_t>((int64_t)P.merge_tab.size(), std::max<int64_t>(cap, 0)));
     return P.hdr.merge_stride;
 }
+
+void hp_test_withhold_first_tile(int32_t enable) { g_withhold.store(enable != 0 ? 1 : 0); }
 
 hp_status hp_read_device_status(void *ws, hp_stream_t stream)
 {

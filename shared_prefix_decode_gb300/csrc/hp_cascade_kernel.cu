@@ -298,21 +298,22 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
 template <int D, bool Loop>
 cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
 {
-    static bool configured = false;  // per instantiation
+    static DeviceOnce once;  // per instantiation and device
     const int bytes = FusedLayout<D>::kBytes + 1024;
     static_assert(FusedLayout<D>::kBytes + 1024 <= 227 * 1024, "shared memory per CTA");
-    if (!configured) {
-        cudaError_t e =
+    cudaError_t e = once.run([bytes] {
+        cudaError_t r =
             cudaFuncSetAttribute(hp_cascade_kernel<D, Loop>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess)
-            return e;
+        if (r != cudaSuccess)
+            return r;
         cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, hp_cascade_kernel<D, Loop>)) != cudaSuccess)
-            return e;
-        if (fa.numRegs != (int)tcr::kRegsLaunch)
-            return cudaErrorInvalidConfiguration;  // the register split assumes this allocation
-        configured = true;
-    }
+        if ((r = cudaFuncGetAttributes(&fa, hp_cascade_kernel<D, Loop>)) != cudaSuccess)
+            return r;
+        // the register split assumes this allocation
+        return fa.numRegs == (int)tcr::kRegsLaunch ? cudaSuccess : cudaErrorInvalidConfiguration;
+    });
+    if (e != cudaSuccess)
+        return e;
     // launched as a programmatic dependent: the CTAs may set up (barriers,
     // TMEM, the record) while the previous kernel in the stream drains; the
     // kernel waits for that kernel to complete before it reads its inputs

@@ -3,14 +3,48 @@
 // maps) and the launch entry points of each kernel translation unit.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/hp.h"
 
 namespace hp {
+
+// One-time set-up per device, for state the CUDA runtime keeps per device
+// (a kernel's shared-memory limit and carveout): run(f) calls f with the
+// device current, the first time any thread reaches it on that device;
+// other threads wait for it.  A failed f is tried again by the next caller.
+class DeviceOnce {
+  public:
+    template <class F>
+    cudaError_t run(F &&f)
+    {
+        int dev = -1;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 0 || dev >= kMaxDev)
+            return cudaErrorInvalidDevice;
+        if (done_[dev].load(std::memory_order_acquire))
+            return cudaSuccess;
+        std::lock_guard<std::mutex> g(mu_);
+        if (done_[dev].load(std::memory_order_relaxed))
+            return cudaSuccess;
+        e = f();
+        if (e == cudaSuccess)
+            done_[dev].store(true, std::memory_order_release);
+        return e;
+    }
+
+  private:
+    static constexpr int kMaxDev = 64;
+    std::mutex mu_;
+    std::atomic<bool> done_[kMaxDev] = {};
+};
 
 // A plan keeps pool information and tensor maps per distinct pool set (a
 // "pool slot": K pool, V pool, page count, page size), at most kMaxLevels of

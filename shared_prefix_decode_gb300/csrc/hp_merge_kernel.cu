@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 // keep the same carveout so the SMs need no reconfiguration in between.
 static cudaError_t merge_configure()
 {
-    static const cudaError_t e = [] {
+    static DeviceOnce once;
+    return once.run([] {
         cudaError_t r = cudaFuncSetAttribute(hp_merge_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                              (int)cudaSharedmemCarveoutMaxShared);
         if (r == cudaSuccess)
@@ -168,8 +169,7 @@ static cudaError_t merge_configure()
                                      (int)cudaSharedmemCarveoutMaxShared);
 
         return r;
-    }();
-    return e;
+    });
 }
 
 template <class K>

@@ -12,11 +12,13 @@
 //
 // The array below is created when the library's device code is loaded and
 // stays resident on every GPU that loads it until the process exits.  Its
-// device address is looked up once per device (cudaGetSymbolAddress, with
-// that device current) during the first call on that device.  Every call
-// shares the one array, so calls that run at the same time on the GPU (on
-// different streams, or from different host threads) overwrite each other's
-// partial states: serialise them.
+// device address is looked up (cudaGetSymbolAddress, with the device
+// current) during the first call in each CUDA context -- the first call on a
+// device, and again after cudaDeviceReset has replaced that device's context
+// and the array may have moved.  Every call shares the one array, so calls
+// that run at the same time on the GPU (on different streams, or from
+// different host threads) overwrite each other's partial states: serialise
+// them.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -24,6 +26,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "hp_host.h"
 #include "hp_internal.h"
 
 namespace {
@@ -36,61 +39,61 @@ static __device__ __align__(256) unsigned char g_hp_noalloc_scratch[kNoAllocScra
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_lock;
-void *g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id;  // the CUDA context the address belongs to (0: none yet)
+    void *ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up on the
-// first call per device).  Returns nullptr if the lookup failed.
+// Unique id of the current CUDA context (ids are never reused), via the
+// driver entry points the runtime hands out; 0 if it cannot be read.
+unsigned long long current_context_id()
+{
+    static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+        cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current device's context,
+// looked up once per context.  Returns nullptr if the lookup failed.
 void *scratch_on_current_device()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return nullptr;
+    // (before the first runtime call on a device its context may not exist
+    // yet: id 0, and the lookup below creates it)
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> g(g_setup_lock);
-    if (g_scratch_ptr[dev] == nullptr) {
+    ScratchAddr &a = g_scratch[dev];
+    if (a.ptr == nullptr || ctx == 0 || a.ctx_id != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_hp_noalloc_scratch) != cudaSuccess || p == nullptr) {
             cudaGetLastError();
+            a.ptr = nullptr;
             return nullptr;
         }
-        g_scratch_ptr[dev] = p;
+        a.ptr = p;
+        a.ctx_id = current_context_id();
     }
-    return g_scratch_ptr[dev];
+    return a.ptr;
 }
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn_noalloc()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
-bool encode_pool(CUtensorMap *m, const void *pool, int num_pages, int Hkv, int ps, int d, int heads)
-{
-    auto fn = encode_fn_noalloc();
-    if (!fn)
-        return false;
-    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
-    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)ps * d * 2, (cuuint64_t)Hkv * ps * d * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)hp::kChunk, (cuuint32_t)heads, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool is_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
@@ -113,15 +116,18 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
         return HP_ERR_ARG;
     const size_t esz = out_dt == HP_F32 ? 4 : 2;
     const size_t lane_bytes = esz * (size_t)(d / 32);
-    if (!is_aligned(q, 16) || q_sb % 8 || q_sh % 8 || q_sb < 0 || q_sh < 0 || !is_aligned(out, lane_bytes) ||
+    if (!aligned(q, 16) || q_sb % 8 || q_sh % 8 || q_sb < 0 || q_sh < 0 || !aligned(out, lane_bytes) ||
         (o_sb * (int64_t)esz) % (int64_t)lane_bytes || (o_sh * (int64_t)esz) % (int64_t)lane_bytes ||
-        !is_aligned(k_pool, 16) || !is_aligned(v_pool, 16))
+        !aligned(k_pool, 16) || !aligned(v_pool, 16))
         return HP_ERR_UNSUPPORTED;
     if ((int64_t)pt_stride * page_size > INT32_MAX)
         return HP_ERR_UNSUPPORTED;
 
     // Split each sequence into as few key ranges as fit the scratch: at
     // least 64 keys per range, and no more ranges than the scratch holds.
+    // Each split needs B * Hq partial rows of 2d + 4 bytes (the bf16 O row
+    // and its f32 LSE); one split fits while B * Hq <= 64,525 at d = 128
+    // (127,096 at d = 64).
     const int max_len = pt_stride * page_size;
     const size_t per_row = (size_t)d * 2 + 4;  // partial O row (bf16) + its LSE
     const size_t avail = kNoAllocScratchBytes - 2 * kWsHeader;
@@ -130,9 +136,9 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
     if (max_splits < 1)
         return HP_ERR_WORKSPACE;  // B * Hq partial rows exceed the fixed scratch
     int64_t split = 64;
-    while (cdiv(max_len, split) > max_splits)
+    while (ceil_div(max_len, split) > max_splits)
         split *= 2;
-    const int n_split = (int)cdiv(max_len, split);
+    const int n_split = (int)ceil_div(max_len, split);
     const int64_t part_rows = rows_per_split * n_split;
 
     void *scratch = scratch_on_current_device();
@@ -140,7 +146,7 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
         return HP_ERR_CUDA;
     uint8_t *base = static_cast<uint8_t *>(scratch);
     const size_t off_lse = kWsHeader;
-    const size_t off_o = up(off_lse + (size_t)part_rows * 4, 256);
+    const size_t off_o = round_up(off_lse + (size_t)part_rows * 4, 256);
     if (off_o + (size_t)part_rows * d * 2 > kNoAllocScratchBytes)
         return HP_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -151,8 +157,8 @@ extern "C" hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb,
     SmallParams sp;
     std::memset(&sp, 0, sizeof(sp));
     const int nh = small_heads_per_item(Hkv);
-    if (!encode_pool(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, nh) ||
-        !encode_pool(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, nh))
+    if (!encode_pool_map(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, kChunk, nh) ||
+        !encode_pool_map(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, kChunk, nh))
         return HP_ERR_CUDA;
     const int G = Hq / Hkv;
     // Q rows by TMA with each item's first chunk when the strides allow a

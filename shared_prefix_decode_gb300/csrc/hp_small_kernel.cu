@@ -105,14 +105,12 @@ __global__ void __launch_bounds__(kThreadsSmall) hp_small_kernel(const __grid_co
 template <int D>
 cudaError_t launch_small_d(const SmallParams &p, int grid, cudaStream_t s)
 {
-    static bool configured = false;
+    static DeviceOnce once;  // per instantiation and device
     const int bytes = SmallKernelLayout<D>::kBytes + 1024;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(hp_small_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess)
-            return e;
-        configured = true;
-    }
+    cudaError_t e = once.run(
+        [bytes] { return cudaFuncSetAttribute(hp_small_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes); });
+    if (e != cudaSuccess)
+        return e;
     hp_small_kernel<D><<<grid, kThreadsSmall, bytes, s>>>(p);
     return cudaGetLastError();
 }

@@ -108,20 +108,20 @@ __global__ void __launch_bounds__(tcr::kThreads, 1) hp_tc_kernel(const __grid_co
 template <int D>
 cudaError_t launch_tc_d(const TcParams &p, int grid, cudaStream_t s)
 {
-    static bool configured = false;
+    static DeviceOnce once;  // per instantiation and device
     const int bytes = TcKernelLayout<D>::kBytes + 1024;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(hp_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess)
-            return e;
+    cudaError_t e = once.run([bytes] {
+        cudaError_t r = cudaFuncSetAttribute(hp_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (r != cudaSuccess)
+            return r;
         // the register split assumes this launch allocation per thread
         cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, hp_tc_kernel<D>)) != cudaSuccess)
-            return e;
-        if (fa.numRegs != (int)tcr::kRegsLaunch)
-            return cudaErrorInvalidConfiguration;
-        configured = true;
-    }
+        if ((r = cudaFuncGetAttributes(&fa, hp_tc_kernel<D>)) != cudaSuccess)
+            return r;
+        return fa.numRegs == (int)tcr::kRegsLaunch ? cudaSuccess : cudaErrorInvalidConfiguration;
+    });
+    if (e != cudaSuccess)
+        return e;
     hp_tc_kernel<D><<<grid, tcr::kThreads, bytes, s>>>(p);
     return cudaGetLastError();
 }

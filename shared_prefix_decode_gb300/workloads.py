@@ -78,6 +78,7 @@ class CascadeWorkload:
     v_pool: torch.Tensor
     levels: List[TreeLevel] = field(default_factory=list)
     seed: int = 0
+    part: str = "all"  # make_config's part: the whole workload, or one pass of it
 
     @property
     def G(self) -> int:
@@ -117,7 +118,7 @@ class CascadeWorkload:
         lv = [TreeLevel(l.nodes.clone(), l.page_ids.to(device)) for l in self.levels]
         return CascadeWorkload(self.name, self.B, self.Hq, self.Hkv, self.d, self.page_size,
                                self.scale, self.q.to(device), self.k_pool.to(device),
-                               self.v_pool.to(device), lv, self.seed)
+                               self.v_pool.to(device), lv, self.seed, self.part)
 
 
 def build_cascade(
@@ -135,13 +136,18 @@ def build_cascade(
     scale: Optional[float] = None,
     shuffle: bool = True,
     extra_suffix_range: Optional[Tuple[int, int]] = None,
+    device=None,
 ) -> CascadeWorkload:
     """Build a workload.
 
     ``shared`` lists the shared levels, each a list of ``(seq_begin, seq_end,
     kv_len)`` nodes.  Private suffix lengths are either given or drawn from
     ``suffix_range`` (inclusive); ``extra_suffix_range`` adds a second drawn
-    length to each suffix (question + answer-so-far).
+    length to each suffix (question + answer-so-far).  ``device``: where q, K
+    and V are drawn (a CUDA device draws them there from a generator of that
+    device, seeded alike: the same tree and distributions, other values --
+    for timing runs of the large shapes; the oracle's inputs come from the
+    CPU draw).
     """
     g = torch.Generator().manual_seed(seed)
     if suffix_lens is None:
@@ -169,9 +175,11 @@ def build_cascade(
     n_pages = max(n_logical, 1)
     perm = torch.randperm(n_pages, generator=g) if shuffle else torch.arange(n_pages)
 
-    q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16)
-    k_pool = torch.randn(n_pages, Hkv, ps, d, generator=g).to(torch.bfloat16)
-    v_pool = torch.randn(n_pages, Hkv, ps, d, generator=g).to(torch.bfloat16)
+    dev = torch.device(device) if device is not None else torch.device("cpu")
+    gv = g if dev.type == "cpu" else torch.Generator(device=dev).manual_seed(seed)
+    q = torch.randn(B, Hq, d, generator=gv, device=dev).to(torch.bfloat16)
+    k_pool = torch.randn(n_pages, Hkv, ps, d, generator=gv, device=dev).to(torch.bfloat16)
+    v_pool = torch.randn(n_pages, Hkv, ps, d, generator=gv, device=dev).to(torch.bfloat16)
 
     levels = []
     for rows in level_nodes:
@@ -194,28 +202,42 @@ CONFIG_NAMES = ("tiny", "llama3_8b", "codellama13b", "tree2", "doc_streams", "no
 
 
 def make_config(name: str, seed: int = 0, B: Optional[int] = None, prefix: Optional[int] = None,
-                shuffle: bool = True) -> CascadeWorkload:
+                shuffle: bool = True, part: str = "all", device=None) -> CascadeWorkload:
     """Named workloads; ``B``/``prefix`` override the batch and the first-level
-    prefix length to make smaller variants of the same structure."""
+    prefix length to make smaller variants of the same structure.  ``part``:
+    "all" (the workload), "prefix" (its shared levels alone: every private
+    suffix empty) or "suffix" (its private suffixes alone: no shared level),
+    to time or profile one pass of the step on its own.  ``device`` as in
+    ``build_cascade``."""
+    if part not in ("all", "prefix", "suffix"):
+        raise ValueError(f"part must be all, prefix or suffix, not {part!r}")
+
+    def mk(shared, **kw):
+        if part == "suffix":
+            shared = []
+        if part == "prefix":
+            kw.pop("suffix_range", None)
+            kw.pop("extra_suffix_range", None)
+            kw["suffix_lens"] = [0] * kw["B"]
+        wl = build_cascade(name, shared=shared, seed=seed, shuffle=shuffle, device=device, **kw)
+        wl.part = part
+        return wl
+
     if name == "tiny":
         B_ = B or 4
         P = 256 if prefix is None else prefix
-        return build_cascade(name, B=B_, Hq=4, Hkv=1, d=64, page_size=16,
-                             shared=[[(0, B_, P)]] if P > 0 else [],
-                             suffix_range=(0, 32), seed=seed, scale=1.0 / math.sqrt(64),
-                             shuffle=shuffle)
+        return mk([[(0, B_, P)]] if P > 0 else [], B=B_, Hq=4, Hkv=1, d=64, page_size=16,
+                  suffix_range=(0, 32), scale=1.0 / math.sqrt(64))
     if name == "llama3_8b":
         B_ = B or 64
         P = 4096 if prefix is None else prefix
-        return build_cascade(name, B=B_, Hq=32, Hkv=8, d=128, page_size=16,
-                             shared=[[(0, B_, P)]] if P > 0 else [],
-                             suffix_range=(1, 256), seed=seed, shuffle=shuffle)
+        return mk([[(0, B_, P)]] if P > 0 else [], B=B_, Hq=32, Hkv=8, d=128, page_size=16,
+                  suffix_range=(1, 256))
     if name == "codellama13b":
         B_ = B or 256
         P = 16384 if prefix is None else prefix
-        return build_cascade(name, B=B_, Hq=40, Hkv=40, d=128, page_size=16,
-                             shared=[[(0, B_, P)]] if P > 0 else [],
-                             suffix_range=(1, 512), seed=seed, shuffle=shuffle)
+        return mk([[(0, B_, P)]] if P > 0 else [], B=B_, Hq=40, Hkv=40, d=128, page_size=16,
+                  suffix_range=(1, 512))
     if name == "tree2":
         # global prefix shared by all sequences, then 8 contiguous subgroups
         # sharing a second-level prefix, then private suffixes; 64-token chunks
@@ -225,23 +247,18 @@ def make_config(name: str, seed: int = 0, B: Optional[int] = None, prefix: Optio
         per = B_ // groups
         P2 = 1024 if prefix is None else max(prefix // 2, 64)
         lvl2 = [(gi * per, (gi + 1) * per, P2) for gi in range(groups)]
-        return build_cascade(name, B=B_, Hq=32, Hkv=32, d=128, page_size=64,
-                             shared=[[(0, B_, P)], lvl2], suffix_range=(64, 256),
-                             seed=seed, shuffle=shuffle)
+        return mk([[(0, B_, P)], lvl2], B=B_, Hq=32, Hkv=32, d=128, page_size=64, suffix_range=(64, 256))
     if name == "doc_streams":
         # one document shared by all streams; each stream's private segment is
         # its question (32..64 tokens) plus its answer so far (0..256 tokens)
         B_ = B or 256
         P = 16384 if prefix is None else prefix
-        return build_cascade(name, B=B_, Hq=32, Hkv=32, d=128, page_size=16,
-                             shared=[[(0, B_, P)]] if P > 0 else [],
-                             suffix_range=(32, 64), extra_suffix_range=(0, 256),
-                             seed=seed, shuffle=shuffle)
+        return mk([[(0, B_, P)]] if P > 0 else [], B=B_, Hq=32, Hkv=32, d=128, page_size=16,
+                  suffix_range=(32, 64), extra_suffix_range=(0, 256))
     if name == "no_sharing":
         B_ = B or 64
         L = 2048 if prefix is None else prefix
-        return build_cascade(name, B=B_, Hq=32, Hkv=32, d=128, page_size=16, shared=[],
-                             suffix_lens=[L] * B_, seed=seed, shuffle=shuffle)
+        return mk([], B=B_, Hq=32, Hkv=32, d=128, page_size=16, suffix_lens=[L] * B_)
     raise ValueError(f"unknown config {name!r}; known: {CONFIG_NAMES}")
 
 

@@ -410,9 +410,9 @@ def test_cascade_matches_naive_per_sequence_decode():
     assert (lc - ln).abs().max().item() <= LSE_ABS
 
 
-def test_cascade_device_timeout_is_reported_and_the_context_stays_usable(monkeypatch):
-    """Failure detection without a fault: with HP_TEST_WITHHOLD_TILE=1 one CTA
-    arms a tile barrier but issues no copy, so its bounded waits (2 s of
+def test_cascade_device_timeout_is_reported_and_the_context_stays_usable():
+    """Failure detection without a fault: with hp_test_withhold_first_tile on,
+    one CTA arms a tile barrier but issues no copy, so its bounded waits (2 s of
     %globaltimer) run out; the kernel drains, frees its tensor memory and
     returns, and the step reports HP_ERR_DEVICE_TIMEOUT through the status
     word.  The next step on the same workspace is correct."""
@@ -420,10 +420,12 @@ def test_cascade_device_timeout_is_reported_and_the_context_stays_usable(monkeyp
     wg = wl.to(DEV)
     plan = hb.CascadePlan.from_workload(wg)
     assert plan.info.n_tc_items > 0  # CTA 0 runs a tensor-core item
-    monkeypatch.setenv("HP_TEST_WITHHOLD_TILE", "1")
-    plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
-    torch.cuda.synchronize()
-    monkeypatch.delenv("HP_TEST_WITHHOLD_TILE")
+    hb.library().hp_test_withhold_first_tile(1)
+    try:
+        plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+    finally:
+        hb.library().hp_test_withhold_first_tile(0)
     assert hb.hp_read_device_status(plan.ws) == hb.HP_ERR_DEVICE_TIMEOUT
     out, lse = plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
     _status_ok(plan.ws)
