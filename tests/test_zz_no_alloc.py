@@ -99,7 +99,7 @@ def test_noalloc_benchmarked_shape_uses_wider_splits():
 def test_noalloc_broadcast_query_reads_q_without_a_tensor_map():
     """q with a zero batch stride (one query row set shared by every
     sequence): the queries are read by the consumer warps, not by TMA."""
-    wl, wg, pt, sl = _case("llama3_8b", 8, B=6, prefix=300)
+    wl, wg, pt, sl = _case("llama3_8b", 8, B=6, prefix=304)
     q1 = wg.q[:1].expand(wl.B, wl.Hq, wl.d)
     assert q1.stride(0) == 0
     out = torch.empty(wl.B, wl.Hq, wl.d, dtype=torch.float32, device="cuda")
