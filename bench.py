@@ -378,7 +378,7 @@ def main():
     import numpy as np
     import torch
     from shared_prefix_decode_gb300 import binding as hb
-    from shared_prefix_decode_gb300.workloads import full_page_tables, make_config
+    from shared_prefix_decode_gb300.workloads import full_page_tables, make_config, with_e4m3_levels
 
     dist = None
     if world > 1:
@@ -393,15 +393,20 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
 
-    def make_sets(name, part, seed0, n_sets=0, device=None):
+    def make_sets(name, part, seed0, n_sets=0, device=None, e4m3=False):
         """Input sets of one workload (R of them: R x working set >= 3x L2,
         at least 2), each with its plan and a result buffer; one workspace
-        shared by all."""
-        first = make_config(name, seed=seed0, part=part, device=device)
+        shared by all.  e4m3: the levels of the per-sequence pass read E4M3
+        copies of the pools."""
+        def gen(seed):
+            wl = make_config(name, seed=seed, part=part, device=device)
+            return with_e4m3_levels(wl) if e4m3 else wl
+
+        first = gen(seed0)
         R, note = l2_plan(first, l2, n_sets)
         out = []
         for i in range(R):
-            wl = first if i == 0 else make_config(name, seed=seed0 + i, part=part, device=device)
+            wl = first if i == 0 else gen(seed0 + i)
             wg = wl.to(dev)
             plan = hb.CascadePlan.from_workload(wg)
             # O and LSE share one buffer, so a host read of the result is one copy
@@ -701,6 +706,16 @@ def main():
                 extras[f"{part}_only"] = measure(ps_sets, ps_ws, b, f, 4 * len(ps_sets))
                 del ps_sets, ps_ws
                 torch.cuda.empty_cache()
+        # the same workload with its private suffixes in E4M3 (bf16 prefix)
+        if args.part == "all":
+            e_sets, e_ws, e_note = make_sets(args.config, "all", 1000 * rank + 600, device=dev, e4m3=True)
+            b = statistics.mean(s["wl"].unique_kv_bytes() for s in e_sets)
+            f = statistics.mean(s["wl"].shared_flops() for s in e_sets)
+            extras["e4m3_suffix"] = dict(measure(e_sets, e_ws, b, f, 4 * len(e_sets)), l2=e_note,
+                                         note="suffix KV as E4M3 codes + f32 scale per (page, KV head); "
+                                              "unique bytes count codes and scales")
+            del e_sets, e_ws
+            torch.cuda.empty_cache()
         # the other workloads at full size, cold L2
         per_cfg = {}
         for name in ("codellama13b", "tree2", "doc_streams", "no_sharing"):

@@ -62,6 +62,21 @@ typedef enum {
 
 typedef enum { HP_BF16 = 0, HP_F32 = 1 } hp_dtype;
 
+/* Storage of a level's (or a paged decode's) keys and values.
+ * HP_KV_BF16: bf16 pools [num_pages][Hkv][page_size][d].
+ * HP_KV_E4M3: reduced-precision pools for the memory-bound per-sequence pass
+ * (Hydragen, "Implications and Future Directions": quantising the KV cache
+ * is the complementary remedy for suffix attention, which stays bound by its
+ * bytes).  One byte per element: an E4M3 code (the OCP 8-bit floating-point
+ * format with 4 exponent bits, bias 7, 3 mantissa bits, no infinities;
+ * S.1111.111 is not a number and must not be stored), laid out
+ * [num_pages][Hkv][page_size][d]; plus one f32 scale per (page, KV head) for K
+ * and one for V, device arrays [num_pages][Hkv].  The stored value of a code
+ * is its E4M3 value times the scale of its page and KV head.  Only d = 128;
+ * queries stay bf16 and must lie within f16's range (|q| < 65504): the kernels
+ * use f16 tensor-core products for these levels. */
+typedef enum { HP_KV_BF16 = 0, HP_KV_E4M3 = 1 } hp_kv_type;
+
 const char *hp_status_str(hp_status s);
 
 /* ---------------------------------------------------------------------------
@@ -136,6 +151,21 @@ hp_status hp_suffix_decode_paged_noalloc(const void *q, int64_t q_sb, int64_t q_
                                          hp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * hp_suffix_decode_paged_e4m3 -- hp_suffix_decode_paged over E4M3 pools
+ * (hp_kv_type HP_KV_E4M3): k_pool / v_pool hold the codes, k_scale / v_scale
+ * the f32 scales [num_pages][Hkv] (device, 4-byte aligned).  d = 128 only.
+ * Workspace: hp_suffix_workspace_bytes.  Otherwise as hp_suffix_decode_paged.
+ * ------------------------------------------------------------------------- */
+hp_status hp_suffix_decode_paged_e4m3(const void *q, int64_t q_sb, int64_t q_sh, int32_t B,
+                                      const void *k_pool, const void *v_pool, const float *k_scale,
+                                      const float *v_scale, int32_t num_pages, int32_t page_size,
+                                      const int32_t *page_table, int32_t pt_stride,
+                                      const int32_t *seq_lens, int32_t Hq, int32_t Hkv, int32_t d,
+                                      float scale, void *out, hp_dtype out_dt, int64_t o_sb,
+                                      int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
+                                      size_t ws_bytes, hp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * hp_prefix_attn -- inter-sequence batched attention against one contiguous
  * shared prefix (Hydragen, "Inter-Sequence Batched Prefix Attention": the
  * queries of sequences [row_begin, row_begin + rows) are stacked and attend
@@ -167,13 +197,20 @@ hp_status hp_prefix_attn(const void *q, int64_t q_sb, int64_t q_sh, int32_t row_
  *
  * The nodes and page ids are HOST arrays, read only during hp_cascade_plan.
  * The pools are device pointers; they must stay valid while the plan is used.
+ *
+ * E4M3 levels (kv_type = HP_KV_E4M3, d = 128) serve nodes that run the
+ * per-sequence pass: every node of such a level covers at most 16 / (Hq/Hkv)
+ * sequences.  A tree with an E4M3 level keeps its batched (shared) nodes in
+ * bf16 levels, and every level it runs in the per-sequence pass must then be
+ * E4M3 (HP_ERR_UNSUPPORTED otherwise); decode-loop plans take bf16 levels
+ * only.
  * ------------------------------------------------------------------------- */
 typedef struct {
     int32_t seq_begin, seq_end, kv_len, page_off;
 } hp_tree_node;
 
 typedef struct {
-    const void *k_pool; /* device, bf16 [num_pages][Hkv][page_size][d], 16-byte aligned */
+    const void *k_pool; /* device, [num_pages][Hkv][page_size][d] of kv_type, 16-byte aligned */
     const void *v_pool;
     int32_t num_pages;
     int32_t page_size;
@@ -181,6 +218,9 @@ typedef struct {
     const hp_tree_node *nodes; /* host */
     const int32_t *page_ids;   /* host */
     int32_t num_page_ids;
+    int32_t kv_type;           /* hp_kv_type; 0 (bf16) when the struct is zero-initialised */
+    const float *k_scale;      /* HP_KV_E4M3: device f32 [num_pages][Hkv], 4-byte aligned; else NULL */
+    const float *v_scale;
 } hp_tree_level;
 
 typedef struct {

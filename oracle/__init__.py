@@ -20,6 +20,15 @@ it.  Each wrapper names the passage it follows:
 * ``paged_decode``   - per-sequence attention through a page table.
 * ``prefix``         - attention of a batch of queries against one contiguous
                        prefix laid out [len][Hkv][d].
+* ``e4m3_decode``    - the value of an 8-bit E4M3 code, by the format's
+                       definition (sign, 4 exponent bits with bias 7, 3
+                       mantissa bits, subnormals, no infinities); levels of a
+                       workload stored as E4M3 codes times an f32 scale per
+                       (page, KV head) are decoded element by element before
+                       the same definition runs (Hydragen, "Implications and
+                       Future Directions": KV quantisation for the
+                       memory-bound suffix pass).
+* ``paged_decode_e4m3`` - ``paged_decode`` over E4M3 pools.
 * ``stream_visible`` / ``stream_masked`` - the Parallel Prompting stream mask
                        (Read Once, Answer Many, Section 3, Eq. 2): one KV row
                        per request holding the document and every stream's
@@ -46,6 +55,8 @@ _lib = None
 _dp = ctypes.POINTER(ctypes.c_double)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_fp = ctypes.POINTER(ctypes.c_float)
 
 
 def build(force: bool = False) -> str:
@@ -84,6 +95,16 @@ def _load():
                 ctypes.c_double, _u16p, ctypes.c_long, ctypes.c_long, _u16p, _u16p, ctypes.c_long,
                 ctypes.c_long, ctypes.c_int, _dp, _dp]
             lib.hpo_prefix.restype = ctypes.c_int
+            lib.hpo_e4m3_decode.argtypes = [ctypes.c_long, _u8p, _dp]
+            lib.hpo_cascade_q.argtypes = [ctypes.c_int] * 4 + [
+                ctypes.c_double, _u16p, ctypes.c_int, ctypes.POINTER(ctypes.c_void_p),
+                ctypes.POINTER(ctypes.c_void_p), _i32p, ctypes.POINTER(_fp), ctypes.POINTER(_fp), _i32p, _i32p,
+                ctypes.POINTER(_i32p), ctypes.POINTER(_i32p), ctypes.c_long, _i32p, _dp, _dp]
+            lib.hpo_cascade_q.restype = ctypes.c_int
+            lib.hpo_paged_decode_e4m3.argtypes = [ctypes.c_int] * 4 + [
+                ctypes.c_double, _u16p, ctypes.c_long, ctypes.c_long, _u8p, _u8p, _fp, _fp, ctypes.c_int,
+                _i32p, ctypes.c_int, _i32p, _dp, _dp]
+            lib.hpo_paged_decode_e4m3.restype = ctypes.c_int
             lib.hpo_num_threads.restype = ctypes.c_int
             lib.hpo_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -163,10 +184,85 @@ def attn_reduce(o_c, m_c: float, n_c: float, state):
     return state
 
 
+def _u8_bytes(t) -> np.ndarray:
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8:
+        raise TypeError("expected a torch.uint8 tensor of E4M3 codes")
+    return t.detach().cpu().contiguous().numpy()
+
+
+def _f32(t) -> np.ndarray:
+    return np.ascontiguousarray(t.detach().cpu().numpy().astype(np.float32))
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of 8-bit E4M3 codes (any shape of uint8) as float64."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.zeros(c.shape, dtype=np.float64)
+    _load().hpo_e4m3_decode(c.size, _ptr(c, _u8p), _ptr(out, _dp))
+    return out
+
+
+def _cascade_e4m3(wl, rows_np):
+    """``cascade`` for a workload with levels marked e4m3 (their keys and
+    values decoded from wl.q8's codes and scales)."""
+    lib = _load()
+    n = rows_np.shape[0]
+    q = _bf16_bits(wl.q)
+    kp, vp = _bf16_bits(wl.k_pool), _bf16_bits(wl.v_pool)
+    k8 = v8 = ks = vs = None
+    if wl.q8 is not None:
+        k8, v8 = _u8_bytes(wl.q8.k), _u8_bytes(wl.q8.v)
+        ks, vs = _f32(wl.q8.k_scale), _f32(wl.q8.v_scale)
+    nl = len(wl.levels)
+    keep = []
+    k_arr = (ctypes.c_void_p * max(nl, 1))()
+    v_arr = (ctypes.c_void_p * max(nl, 1))()
+    ks_arr = (_fp * max(nl, 1))()
+    vs_arr = (_fp * max(nl, 1))()
+    dt = np.zeros(max(nl, 1), dtype=np.int32)
+    nodes_arr = (_i32p * max(nl, 1))()
+    ids_arr = (_i32p * max(nl, 1))()
+    ps_arr = np.full(max(nl, 1), wl.page_size, dtype=np.int32)
+    nn_arr = np.zeros(max(nl, 1), dtype=np.int32)
+    for i, lv in enumerate(wl.levels):
+        nodes = np.ascontiguousarray(lv.nodes.cpu().numpy().astype(np.int32))
+        ids = np.ascontiguousarray(lv.page_ids.cpu().numpy().astype(np.int32))
+        if ids.size == 0:
+            ids = np.zeros(1, dtype=np.int32)
+        keep += [nodes, ids]
+        if lv.e4m3:
+            if k8 is None:
+                raise ValueError("a level is marked e4m3 but the workload has no E4M3 pools")
+            dt[i] = 1
+            k_arr[i] = k8.ctypes.data
+            v_arr[i] = v8.ctypes.data
+            ks_arr[i] = _ptr(ks, _fp)
+            vs_arr[i] = _ptr(vs, _fp)
+        else:
+            k_arr[i] = kp.ctypes.data
+            v_arr[i] = vp.ctypes.data
+        nodes_arr[i] = _ptr(nodes, _i32p)
+        ids_arr[i] = _ptr(ids, _i32p)
+        nn_arr[i] = nodes.shape[0]
+    O = np.zeros((n, wl.d))
+    L = np.zeros(n)
+    rc = lib.hpo_cascade_q(wl.B, wl.Hq, wl.Hkv, wl.d, float(wl.scale), _ptr(q, _u16p), nl, k_arr, v_arr,
+                           _ptr(dt, _i32p), ks_arr, vs_arr, _ptr(ps_arr, _i32p), _ptr(nn_arr, _i32p), nodes_arr,
+                           ids_arr, n, _ptr(rows_np, _i32p), _ptr(O, _dp), _ptr(L, _dp))
+    if rc != 0:
+        raise ValueError(f"hpo_cascade_q rejected its arguments ({rc})")
+    return O, L
+
+
 def cascade(wl, rows: Optional[Sequence[Sequence[int]]] = None):
     """Attention of rows (b, h) of a ``CascadeWorkload`` over each sequence's
     concatenated tree keys.  Default: every row.  Returns (O [n,d], lse [n])."""
     lib = _load()
+    if any(getattr(lv, "e4m3", False) for lv in wl.levels):
+        if rows is None:
+            rows = [(b, h) for b in range(wl.B) for h in range(wl.Hq)]
+        return _cascade_e4m3(wl, np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2)))
     if rows is None:
         rows = [(b, h) for b in range(wl.B) for h in range(wl.Hq)]
     rows_np = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
@@ -255,6 +351,27 @@ def paged_decode(q, k_pool, v_pool, page_table, seq_lens, scale: float):
     return O, L
 
 
+def paged_decode_e4m3(q, k8, v8, k_scale, v_scale, page_table, seq_lens, scale: float):
+    """``paged_decode`` over E4M3 pools: k8/v8 uint8 [P,Hkv,ps,d] codes,
+    k_scale/v_scale f32 [P,Hkv] -> (O [B,Hq,d], lse [B,Hq])."""
+    lib = _load()
+    B, Hq, d = q.shape
+    _, Hkv, ps, _ = k8.shape
+    qb = _bf16_bits(q)
+    kb, vb = _u8_bytes(k8), _u8_bytes(v8)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    pt = np.ascontiguousarray(np.asarray(page_table, dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    O = np.zeros((B, Hq, d))
+    L = np.zeros((B, Hq))
+    rc = lib.hpo_paged_decode_e4m3(B, Hq, Hkv, d, float(scale), _ptr(qb, _u16p), Hq * d, d, _ptr(kb, _u8p),
+                                   _ptr(vb, _u8p), _ptr(ks, _fp), _ptr(vs, _fp), ps, _ptr(pt, _i32p), pt.shape[1],
+                                   _ptr(sl, _i32p), _ptr(O, _dp), _ptr(L, _dp))
+    if rc != 0:
+        raise ValueError("hpo_paged_decode_e4m3 rejected its arguments")
+    return O, L
+
+
 def prefix(q, k, v, scale: float):
     """q [nb,Hq,d] bf16; k/v [len,Hkv,d] bf16 -> (O [nb,Hq,d], lse [nb,Hq])."""
     lib = _load()
@@ -287,7 +404,7 @@ class use_library:
         lib = ctypes.CDLL(self.so_path)
         for name in ("hpo_sdp_f64", "hpo_merge", "hpo_partial_attn", "hpo_attn_reduce",
                      "hpo_cascade", "hpo_paged_decode", "hpo_prefix", "hpo_num_threads",
-                     "hpo_set_num_threads"):
+                     "hpo_set_num_threads", "hpo_e4m3_decode", "hpo_cascade_q", "hpo_paged_decode_e4m3"):
             f, g = getattr(lib, name), getattr(base, name)
             f.argtypes = g.argtypes
             f.restype = g.restype

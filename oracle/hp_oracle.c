@@ -28,6 +28,14 @@
  * KV head: the grouped-query reading of "each KV head serves its group of
  * query heads", shared-prefix KV caching blog, "Splitting attention at the
  * prefix boundary").
+ *
+ * Reduced-precision KV (Hydragen, "Implications and Future Directions": the
+ * suffix pass stays memory-bound, and quantising the KV cache is the
+ * complementary remedy).  A level may store its keys and values as 8-bit
+ * E4M3 codes with one f32 scale per (page, KV head) for K and one for V: the
+ * stored value is decode(code) * scale.  The oracle decodes every code by the
+ * format's definition (hpo_e4m3_to_f64) and then evaluates the same plain
+ * definition above in double precision.
  */
 #include <math.h>
 #include <stdint.h>
@@ -206,6 +214,82 @@ void hpo_attn_reduce(int d, const double *o_c, double m_c, double n_c, double *O
 }
 
 /* ---------------------------------------------------------------------------
+ * 8-bit E4M3 codes (the OCP 8-bit floating-point format E4M3, which has no
+ * infinities): bit 7 is the sign s, bits 6..3 the exponent field e (bias 7),
+ * bits 2..0 the mantissa field m.
+ *   e = 0:               (-1)^s * 2^-6 * (m / 8)       (zero and subnormals)
+ *   e = 1..15:           (-1)^s * 2^(e - 7) * (1 + m / 8)
+ *   e = 15 and m = 7:    not a number (the largest finite value is 448)
+ * ------------------------------------------------------------------------- */
+double hpo_e4m3_to_f64(uint8_t c)
+{
+    int s = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+void hpo_e4m3_decode(long n, const uint8_t *codes, double *out)
+{
+    long i;
+    for (i = 0; i < n; ++i)
+        out[i] = hpo_e4m3_to_f64(codes[i]);
+}
+
+/* One key of a row's key list: its K and V rows (bf16, or E4M3 codes with the
+ * scales of their page and KV head). */
+typedef struct {
+    const void *k, *v;
+    double k_scale, v_scale;
+    int e4m3;
+} hpo_key;
+
+static double key_elem(const void *row, int e4m3, double sc, int i)
+{
+    if (e4m3)
+        return hpo_e4m3_to_f64(((const uint8_t *)row)[i]) * sc;
+    return bf16_to_f64(((const uint16_t *)row)[i]);
+}
+
+/* SDP over an explicit key list of mixed storage (the definition, as in
+ * sdp_rows_bf16, with each element decoded from its storage first). */
+static void sdp_keys(int d, const double *q, int nk, const hpo_key *keys, double scale, double *o,
+                     double *lse, double *s)
+{
+    int j, i;
+    for (i = 0; i < d; ++i)
+        o[i] = 0.0;
+    if (nk == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (j = 0; j < nk; ++j) {
+        double acc = 0.0;
+        for (i = 0; i < d; ++i)
+            acc += q[i] * key_elem(keys[j].k, keys[j].e4m3, keys[j].k_scale, i);
+        s[j] = scale * acc;
+        if (s[j] > m)
+            m = s[j];
+    }
+    double sum = 0.0;
+    for (j = 0; j < nk; ++j)
+        sum += exp(s[j] - m);
+    double L = m + log(sum);
+    for (j = 0; j < nk; ++j) {
+        double w = exp(s[j] - L);
+        for (i = 0; i < d; ++i)
+            o[i] += w * key_elem(keys[j].v, keys[j].e4m3, keys[j].v_scale, i);
+    }
+    *lse = L;
+}
+
+/* ---------------------------------------------------------------------------
  * Cascade attention over a level-by-level prefix tree stored in pages.
  *
  * Pool layout [page][Hkv][ps][d] bf16.  Level l has num_nodes[l] nodes, each
@@ -300,6 +384,112 @@ int hpo_cascade(int B, int Hq, int Hkv, int d, double scale, const uint16_t *q,
         free(qd);
     }
     free(lv);
+    return 0;
+}
+
+/* Cascade attention over a tree whose levels may store E4M3 codes:
+ * kv_dtypes[l] = 0 for bf16 pools, 1 for E4M3 pools ([page][Hkv][ps][d]
+ * bytes) with f32 scales k_scales[l][page * Hkv + kvh] (and v_scales[l]
+ * likewise).  Otherwise as hpo_cascade. */
+int hpo_cascade_q(int B, int Hq, int Hkv, int d, double scale, const uint16_t *q, int num_levels,
+                  const void *const *k_pools, const void *const *v_pools, const int32_t *kv_dtypes,
+                  const float *const *k_scales, const float *const *v_scales, const int32_t *page_sizes,
+                  const int32_t *num_nodes, const int32_t *const *nodes, const int32_t *const *page_ids,
+                  long n_rows, const int32_t *rows, double *O, double *lse)
+{
+    long r;
+    int G;
+    if (Hkv <= 0 || Hq % Hkv != 0 || num_levels < 0)
+        return -1;
+    for (r = 0; r < n_rows; ++r)
+        if (rows[2 * r] < 0 || rows[2 * r] >= B || rows[2 * r + 1] < 0 || rows[2 * r + 1] >= Hq)
+            return -2;
+    G = Hq / Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (r = 0; r < n_rows; ++r) {
+        int b = rows[2 * r], h = rows[2 * r + 1];
+        int kvh = h / G;
+        int nk = 0, l, k, t;
+        for (l = 0; l < num_levels; ++l)
+            for (k = 0; k < num_nodes[l]; ++k) {
+                const int32_t *nd = nodes[l] + 4 * k;
+                if (b >= nd[0] && b < nd[1]) {
+                    nk += nd[2];
+                    break;
+                }
+            }
+        hpo_key *keys = (hpo_key *)malloc(sizeof(hpo_key) * (size_t)(nk + 1));
+        double *s = (double *)malloc(sizeof(double) * (size_t)(nk + 1));
+        double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+        int n = 0;
+        for (l = 0; l < num_levels; ++l) {
+            const int ps = page_sizes[l];
+            for (k = 0; k < num_nodes[l]; ++k) {
+                const int32_t *nd = nodes[l] + 4 * k;
+                if (b < nd[0] || b >= nd[1])
+                    continue;
+                for (t = 0; t < nd[2]; ++t, ++n) {
+                    long page = page_ids[l][nd[3] + t / ps];
+                    long slot = t % ps;
+                    size_t off = (((size_t)page * Hkv + kvh) * ps + slot) * d;
+                    keys[n].e4m3 = kv_dtypes[l] == 1;
+                    if (keys[n].e4m3) {
+                        keys[n].k = (const uint8_t *)k_pools[l] + off;
+                        keys[n].v = (const uint8_t *)v_pools[l] + off;
+                        keys[n].k_scale = k_scales[l][page * Hkv + kvh];
+                        keys[n].v_scale = v_scales[l][page * Hkv + kvh];
+                    } else {
+                        keys[n].k = (const uint16_t *)k_pools[l] + off;
+                        keys[n].v = (const uint16_t *)v_pools[l] + off;
+                        keys[n].k_scale = keys[n].v_scale = 1.0;
+                    }
+                }
+                break; /* nodes of one level cover disjoint ranges */
+            }
+        }
+        load_q(d, q + ((size_t)b * Hq + h) * d, qd);
+        sdp_keys(d, qd, nk, keys, scale, O + (size_t)r * d, lse + r, s);
+        free(keys);
+        free(s);
+        free(qd);
+    }
+    return 0;
+}
+
+/* Per-sequence paged decode over E4M3 pools (codes [page][Hkv][ps][d] bytes,
+ * f32 scales [page][Hkv] for K and for V); otherwise as hpo_paged_decode. */
+int hpo_paged_decode_e4m3(int B, int Hq, int Hkv, int d, double scale, const uint16_t *q, long q_sb,
+                          long q_sh, const uint8_t *k_pool, const uint8_t *v_pool, const float *k_scale,
+                          const float *v_scale, int page_size, const int32_t *page_table, int pt_stride,
+                          const int32_t *seq_lens, double *O, double *lse)
+{
+    long r;
+    int G;
+    if (Hkv <= 0 || Hq % Hkv != 0)
+        return -1;
+    G = Hq / Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (r = 0; r < (long)B * Hq; ++r) {
+        int b = (int)(r / Hq), h = (int)(r % Hq), kvh = h / G, t;
+        int nk = seq_lens[b];
+        hpo_key *keys = (hpo_key *)malloc(sizeof(hpo_key) * (size_t)(nk + 1));
+        double *s = (double *)malloc(sizeof(double) * (size_t)(nk + 1));
+        double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+        for (t = 0; t < nk; ++t) {
+            long page = page_table[(size_t)b * pt_stride + t / page_size];
+            size_t off = (((size_t)page * Hkv + kvh) * page_size + t % page_size) * d;
+            keys[t].k = k_pool + off;
+            keys[t].v = v_pool + off;
+            keys[t].k_scale = k_scale[page * Hkv + kvh];
+            keys[t].v_scale = v_scale[page * Hkv + kvh];
+            keys[t].e4m3 = 1;
+        }
+        load_q(d, q + (size_t)b * q_sb + (size_t)h * q_sh, qd);
+        sdp_keys(d, qd, nk, keys, scale, O + (size_t)r * d, lse + r, s);
+        free(keys);
+        free(s);
+        free(qd);
+    }
     return 0;
 }
 

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libhp.so")
 
 HP_OK, HP_ERR_ARG, HP_ERR_UNSUPPORTED, HP_ERR_WORKSPACE, HP_ERR_CUDA, HP_ERR_BOUNDS, HP_ERR_DEVICE_TIMEOUT = range(7)
 HP_BF16, HP_F32 = 0, 1
+HP_KV_BF16, HP_KV_E4M3 = 0, 1
 
 c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
@@ -29,7 +30,8 @@ class HpTreeNode(ctypes.Structure):
 class HpTreeLevel(ctypes.Structure):
     _fields_ = [("k_pool", c_vp), ("v_pool", c_vp), ("num_pages", c_i32), ("page_size", c_i32),
                 ("num_nodes", c_i32), ("nodes", ctypes.POINTER(HpTreeNode)),
-                ("page_ids", ctypes.POINTER(c_i32)), ("num_page_ids", c_i32)]
+                ("page_ids", ctypes.POINTER(c_i32)), ("num_page_ids", c_i32), ("kv_type", c_i32),
+                ("k_scale", c_vp), ("v_scale", c_vp)]
 
 
 class HpTreeDesc(ctypes.Structure):
@@ -58,6 +60,9 @@ _SIGNATURES = {
     "hp_suffix_decode_paged_noalloc": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_i32, c_i32, c_vp,
                                                c_i32, c_vp, c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64,
                                                c_i64, c_vp, c_i64, c_vp]),
+    "hp_suffix_decode_paged_e4m3": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp,
+                                            c_i32, c_vp, c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64, c_i64,
+                                            c_vp, c_i64, c_vp, c_sz, c_vp]),
     "hp_prefix_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "hp_prefix_attn": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_i64, c_i64, c_i32,
                                c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64, c_i64, c_vp, c_i64,
@@ -209,6 +214,36 @@ def hp_suffix_decode_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     return out, lse
 
 
+def hp_suffix_decode_paged_e4m3(q: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, k_scale: torch.Tensor,
+                                v_scale: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                                ws: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                                stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """hp_suffix_decode_paged over E4M3 pools: k8/v8 uint8 [P,Hkv,ps,d] codes,
+    k_scale/v_scale f32 [P,Hkv] (device)."""
+    B, Hq, d = q.shape
+    P, Hkv, ps, d2 = k8.shape
+    _need(d2 == d and v8.shape == k8.shape and k8.dtype == torch.uint8 and v8.dtype == torch.uint8,
+          "E4M3 pools must be uint8 [P,Hkv,ps,d]")
+    _need(k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32 and tuple(k_scale.shape) == (P, Hkv)
+          and tuple(v_scale.shape) == (P, Hkv) and k_scale.is_contiguous() and v_scale.is_contiguous(),
+          "scales must be contiguous f32 [P,Hkv]")
+    _need(page_table.dtype == torch.int32 and seq_lens.dtype == torch.int32, "int32 tables")
+    _need(page_table.is_contiguous() and k8.is_contiguous() and v8.is_contiguous(), "contiguous")
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = alloc_workspace(suffix_workspace_bytes(B, Hq, d, page_table.shape[1], ps), q.device)
+    _check(library().hp_suffix_decode_paged_e4m3(
+        _ptr(q), q.stride(0), q.stride(1), B, _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale), P, ps,
+        _ptr(page_table), page_table.stride(0), _ptr(seq_lens), Hq, Hkv, d, float(scale), _ptr(out), _dt(out.dtype),
+        out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(), _stream(stream)),
+        "hp_suffix_decode_paged_e4m3")
+    return out, lse
+
+
 # --------------------------------------------------- contiguous prefix
 def prefix_workspace_bytes(rows: int, Hq: int, Hkv: int, d: int, prefix_len: int) -> int:
     return int(library().hp_prefix_workspace_bytes(rows, Hq, Hkv, d, prefix_len))
@@ -245,7 +280,10 @@ class _Desc:
     def __init__(self, levels, B: int, Hq: int, Hkv: int, d: int, num_sms: int = 0):
         self.keep = []
         arr = (HpTreeLevel * max(len(levels), 1))()
-        for i, (k_pool, v_pool, num_pages, page_size, nodes, page_ids) in enumerate(levels):
+        for i, lv in enumerate(levels):
+            # (k_pool, v_pool, num_pages, page_size, nodes, page_ids[, kv_type, k_scale, v_scale])
+            k_pool, v_pool, num_pages, page_size, nodes, page_ids = lv[:6]
+            kv_type, k_scale, v_scale = tuple(lv[6:9]) if len(lv) >= 9 else (HP_KV_BF16, None, None)
             nodes = [tuple(int(x) for x in n) for n in nodes]
             n_arr = (HpTreeNode * max(len(nodes), 1))(*[HpTreeNode(*n) for n in nodes])
             ids = [int(x) for x in page_ids]
@@ -253,7 +291,7 @@ class _Desc:
             self.keep += [n_arr, i_arr]
             arr[i] = HpTreeLevel(k_pool, v_pool, num_pages, page_size, len(nodes),
                                  ctypes.cast(n_arr, ctypes.POINTER(HpTreeNode)),
-                                 ctypes.cast(i_arr, ctypes.POINTER(c_i32)), len(ids))
+                                 ctypes.cast(i_arr, ctypes.POINTER(c_i32)), len(ids), int(kv_type), k_scale, v_scale)
         self.keep.append(arr)
         self.desc = HpTreeDesc(len(levels), B, Hq, Hkv, d, ctypes.cast(arr, ctypes.POINTER(HpTreeLevel)),
                                num_sms)
@@ -261,11 +299,17 @@ class _Desc:
 
 def _levels_of(wl) -> list:
     """Tree levels of a ``workloads.CascadeWorkload`` (pools must be on the GPU
-    for planning; host-only inspection accepts CPU pools)."""
+    for planning; host-only inspection accepts CPU pools).  Levels marked
+    e4m3 read the workload's E4M3 pools and scales."""
     out = []
     for lv in wl.levels:
-        out.append((wl.k_pool.data_ptr(), wl.v_pool.data_ptr(), wl.num_pages, wl.page_size,
-                    lv.nodes.tolist(), lv.page_ids.cpu().tolist()))
+        if getattr(lv, "e4m3", False):
+            q8 = wl.q8
+            out.append((q8.k.data_ptr(), q8.v.data_ptr(), wl.num_pages, wl.page_size, lv.nodes.tolist(),
+                        lv.page_ids.cpu().tolist(), HP_KV_E4M3, q8.k_scale.data_ptr(), q8.v_scale.data_ptr()))
+        else:
+            out.append((wl.k_pool.data_ptr(), wl.v_pool.data_ptr(), wl.num_pages, wl.page_size,
+                        lv.nodes.tolist(), lv.page_ids.cpu().tolist()))
     return out
 
 

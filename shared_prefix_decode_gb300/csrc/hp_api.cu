@@ -25,7 +25,7 @@ using namespace hp;
 
 namespace {
 
-constexpr int32_t kAbiVersion = 3;
+constexpr int32_t kAbiVersion = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------- utilities
@@ -104,9 +104,9 @@ bool out_layout_ok(const void *out, hp_dtype dt, int64_t o_sb, int64_t o_sh, int
 
 // CTAs of the small-row kernel resident per SM (shared memory bound); its
 // grid is one such wave, each warp walking several items.
-int small_ctas_per_sm(int d)
+int small_ctas_per_sm(int d, bool q8 = false)
 {
-    return (int)std::max<size_t>(1, std::min<size_t>(4, (size_t)(227 * 1024) / small_smem_bytes(d)));
+    return (int)std::max<size_t>(1, std::min<size_t>(4, (size_t)(227 * 1024) / small_smem_bytes(d, q8)));
 }
 
 
@@ -168,6 +168,10 @@ struct PlanExtent {
     int32_t leaf_stride, page_size, num_pages;
     int64_t off_leaf_tab;
     void *k_pool, *v_pool;  // the suffix level's pools
+    // E4M3 paged levels: the scales of each pool slot
+    int32_t q8;
+    const float *k_scale[kMaxLevels];
+    const float *v_scale[kMaxLevels];
 };
 std::mutex g_plans_mu;
 std::unordered_map<const void *, PlanExtent> g_plans;
@@ -212,18 +216,19 @@ int hp::device_sms()
 }
 
 bool hp::encode_pool_map(CUtensorMap *m, const void *pool, int num_pages, int Hkv, int ps, int d, int box_tok,
-                         int box_heads)
+                         int box_heads, bool e4m3)
 {
     auto fn = encode_fn();
-    if (!fn)
+    if (!fn || (e4m3 && d != 128))
         return false;
+    const cuuint64_t es_b = e4m3 ? 1 : 2;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
-    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)ps * d * 2, (cuuint64_t)Hkv * ps * d * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)box_tok, (cuuint32_t)box_heads, 1};
+    cuuint64_t strides[3] = {(cuuint64_t)d * es_b, (cuuint64_t)ps * d * es_b, (cuuint64_t)Hkv * ps * d * es_b};
+    cuuint32_t box[4] = {e4m3 ? (cuuint32_t)d : 64u, (cuuint32_t)box_tok, (cuuint32_t)box_heads, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool),
+              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 hp::WsLayout hp::ws_layout(int64_t part_rows, int d)
@@ -302,15 +307,19 @@ size_t hp_suffix_workspace_bytes(int32_t B, int32_t Hq, int32_t d, int32_t pt_st
     return ws_layout((int64_t)B * Hq * n_split_max, d).total;
 }
 
-hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int32_t B, const void *k_pool,
-                                 const void *v_pool, int32_t num_pages, int32_t page_size,
-                                 const int32_t *page_table, int32_t pt_stride, const int32_t *seq_lens,
-                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void *out, hp_dtype out_dt,
-                                 int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
-                                 size_t ws_bytes, hp_stream_t stream)
+static hp_status suffix_decode_impl(const void *q, int64_t q_sb, int64_t q_sh, int32_t B, const void *k_pool,
+                                    const void *v_pool, const float *k_scale, const float *v_scale, bool q8,
+                                    int32_t num_pages, int32_t page_size, const int32_t *page_table, int32_t pt_stride,
+                                    const int32_t *seq_lens, int32_t Hq, int32_t Hkv, int32_t d, float scale, void *out,
+                                    hp_dtype out_dt, int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
+                                    size_t ws_bytes, hp_stream_t stream)
 {
     if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out || !ws)
         return HP_ERR_ARG;
+    if (q8 && (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4)))
+        return HP_ERR_ARG;
+    if (q8 && d != 128)
+        return HP_ERR_UNSUPPORTED;
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || num_pages < 1 || pt_stride < 1 || !std::isfinite(scale))
         return HP_ERR_ARG;
     if (!supported_d(d) || page_size < 16 || page_size > 256 || page_size % 16 || Hq / Hkv > kSmallRows)
@@ -334,9 +343,12 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
 
     SmallParams sp;
     std::memset(&sp, 0, sizeof(sp));
-    if (!encode_pool_map(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, kChunk, nh) ||
-        !encode_pool_map(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, kChunk, nh))
+    if (!encode_pool_map(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, kChunk, nh, q8) ||
+        !encode_pool_map(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, kChunk, nh, q8))
         return HP_ERR_CUDA;
+    sp.q8 = q8 ? 1 : 0;
+    sp.k_scale = k_scale;
+    sp.v_scale = v_scale;
     sp.q_slot = nh * G <= small_q_rows();
     if (sp.q_slot && !encode_q_map(&sp.map_q, q, B, Hq, d, q_sb, q_sh, nh * G, 1))
         return HP_ERR_CUDA;
@@ -359,7 +371,7 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
     sp.part_o = reinterpret_cast<uint16_t *>(wsb + wl.off_o);
     sp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
     sp.status = status_ptr(ws);
-    const int grid = (int)std::min<int64_t>(sp.n_items, (int64_t)sms * small_ctas_per_sm(d));
+    const int grid = (int)std::min<int64_t>(sp.n_items, (int64_t)sms * small_ctas_per_sm(d, q8));
     if (launch_small(sp, grid, d, s) != cudaSuccess)
         return HP_ERR_CUDA;
 
@@ -385,6 +397,30 @@ hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int3
     mp.lse_sb = lse_sb;
     mp.status = status_ptr(ws);
     return launch_merge(mp, (int64_t)B * Hq, s) == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
+
+hp_status hp_suffix_decode_paged(const void *q, int64_t q_sb, int64_t q_sh, int32_t B, const void *k_pool,
+                                 const void *v_pool, int32_t num_pages, int32_t page_size,
+                                 const int32_t *page_table, int32_t pt_stride, const int32_t *seq_lens,
+                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void *out, hp_dtype out_dt,
+                                 int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
+                                 size_t ws_bytes, hp_stream_t stream)
+{
+    return suffix_decode_impl(q, q_sb, q_sh, B, k_pool, v_pool, nullptr, nullptr, false, num_pages, page_size,
+                              page_table, pt_stride, seq_lens, Hq, Hkv, d, scale, out, out_dt, o_sb, o_sh, lse,
+                              lse_sb, ws, ws_bytes, stream);
+}
+
+hp_status hp_suffix_decode_paged_e4m3(const void *q, int64_t q_sb, int64_t q_sh, int32_t B, const void *k_pool,
+                                      const void *v_pool, const float *k_scale, const float *v_scale,
+                                      int32_t num_pages, int32_t page_size, const int32_t *page_table,
+                                      int32_t pt_stride, const int32_t *seq_lens, int32_t Hq, int32_t Hkv, int32_t d,
+                                      float scale, void *out, hp_dtype out_dt, int64_t o_sb, int64_t o_sh,
+                                      float *lse, int64_t lse_sb, void *ws, size_t ws_bytes, hp_stream_t stream)
+{
+    return suffix_decode_impl(q, q_sb, q_sh, B, k_pool, v_pool, k_scale, v_scale, true, num_pages, page_size,
+                              page_table, pt_stride, seq_lens, Hq, Hkv, d, scale, out, out_dt, o_sb, o_sh, lse,
+                              lse_sb, ws, ws_bytes, stream);
 }
 
 size_t hp_prefix_workspace_bytes(int32_t rows, int32_t Hq, int32_t Hkv, int32_t d, int32_t prefix_len)
@@ -511,6 +547,11 @@ static hp_status cascade_plan_impl(const hp_tree_desc *desc, int capacity, void 
     PlanExtent ext{};
     ext.tag = H.tag;
     ext.total_bytes = H.total_bytes;
+    ext.q8 = P.q8 ? 1 : 0;
+    for (size_t sl = 0; sl < P.slot_kv.size() && sl < (size_t)kMaxLevels; ++sl) {
+        ext.k_scale[sl] = P.slot_k_scale[sl];
+        ext.v_scale[sl] = P.slot_v_scale[sl];
+    }
     if (capacity > 0) {
         const hp_tree_level &S = desc->levels[desc->num_levels - 1];
         ext.loop_capacity = capacity;
@@ -638,6 +679,11 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
         cp.loop_v_pool = static_cast<uint16_t *>(ext.v_pool);
         cp.Hkv = info->Hkv;
         cp.d = info->d;
+        cp.q8 = ext.q8;
+        for (int sl = 0; sl < kMaxLevels; ++sl) {
+            cp.k_scale[sl] = ext.k_scale[sl];
+            cp.v_scale[sl] = ext.v_scale[sl];
+        }
         if (launch_cascade(cp, info->grid, info->d, s) != cudaSuccess)
             return HP_ERR_CUDA;
     }

@@ -18,10 +18,12 @@
 // Every partial (O, LSE) row goes to the workspace; the merge kernel, launched
 // as a programmatic dependent of this one, combines them.
 //
-// Two instantiations: the static step, and the decode loop's (Loop = true),
+// Three instantiations: the static step, the decode loop's (Loop = true),
 // in which suffix items end at the sequences' current lengths on the device
 // and, with the append fused, the paged producer writes each sequence's new
-// token into its suffix pages before it loads that chunk.
+// token into its suffix pages before it loads that chunk, and the static
+// step over trees whose paged levels hold E4M3 codes (Q8 = true, d = 128:
+// the paged role's ring then holds 5 stages of half-size chunks).
 #include <cuda_runtime.h>
 
 #include "hp_internal.h"
@@ -35,24 +37,25 @@ namespace {
 
 constexpr int kThreads = tcr::kThreads;
 constexpr int kNC = 8;  // paged-role consumer warps (warps 4..11)
-constexpr int kSmallStages = 3;
 constexpr int kQRows = 32;  // paged-role Q slot rows per stage: nh * G <= 32
 
-template <int D>
+// Q8: the paged role reads E4M3 pools (half-size chunks, more stages)
+template <int D, bool Q8>
 struct FusedLayout {
+    static constexpr int kSmallStages = Q8 ? 5 : 3;
     using T = tcr::Layout<D>;
-    using S = smr::Layout<D, kNC, kSmallStages, kQRows>;
+    using S = smr::Layout<D, kNC, kSmallStages, kQRows, Q8>;
     static constexpr int kRing = T::kEnd > S::kEnd ? T::kEnd : S::kEnd;
     static constexpr int kTcBar = kRing;           // tcr::B_COUNT barriers, tmem slot, abort (256 bytes)
     static constexpr int kSmBar = kTcBar + 256;    // full[S], empty[S]
-    static constexpr int kMeta = kSmBar + 64;      // StageMeta[S]
-    static constexpr int kZero = kMeta + 128;      // 16 zero bytes, then the paged role's abort flag
+    static constexpr int kMeta = kSmBar + 128;     // StageMeta[S]
+    static constexpr int kZero = kMeta + 256;      // 16 zero bytes, then the paged role's abort flag
     static constexpr int kRecBar = kZero + 32;     // the record's barrier
     static constexpr int kRec = kRecBar + 32;      // the CTA record
     static constexpr int kBytes = kRec + kRecMaxBytes;
     static_assert(tcr::kBarAbort + 4 <= 256, "tensor-core barrier area");
-    static_assert(2 * kSmallStages * 8 <= 64, "paged barriers");
-    static_assert(kSmallStages * (int)sizeof(smr::StageMeta) <= 128, "stage metadata");
+    static_assert(2 * kSmallStages * 8 <= 128, "paged barriers");
+    static_assert(kSmallStages * (int)sizeof(smr::StageMeta) <= 256, "stage metadata");
     static_assert(kRec % 16 == 0, "bulk copy destination");
 };
 
@@ -89,7 +92,7 @@ __device__ __forceinline__ tcr::ItemGeo tc_geo(const CascadeParams &p, const Rec
 // key, inside its reserved pages, so the step stays in bounds.
 // Loop: the decode-loop instantiation (lengths on the device, the append
 // possibly fused); the static step's instantiation carries none of that code.
-template <bool Loop>
+template <bool Loop, bool Q8>
 struct RecordItems {
     static constexpr bool kPrefetch = Loop, kTokens = Loop;
     const CascadeParams *p;
@@ -142,15 +145,21 @@ struct RecordItems {
         d.num_pages = w.num_pages;
         d.map_k = level_maps(*p, w.level) + 2;
         d.map_v = level_maps(*p, w.level) + 3;
+        if (Q8) {
+            d.k_scale = p->k_scale[w.level];
+            d.v_scale = p->v_scale[w.level];
+            d.Hkv = p->Hkv;
+        }
         d.valid = d.k0 < d.k1;
         return d;
     }
 };
 
-template <int D, bool Loop>
+template <int D, bool Loop, bool Q8>
 __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_constant__ CascadeParams p)
 {
-    using FL = FusedLayout<D>;
+    using FL = FusedLayout<D, Q8>;
+    constexpr int kSmallStages = FL::kSmallStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -271,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
         // (a CTA without paged items skips the role: its code is not fetched
         // at the end of the step's longest chain)
         if (warp == 0 && n_small > 0)
-            smr::producer<D, kNC, kSmallStages, kQRows>(sc, sa, RecordItems<Loop>{&p, items + n_tc, pages}, n_small, lane);
+            smr::producer<D, kNC, kSmallStages, kQRows, RecordItems<Loop, Q8>, Q8>(
+                sc, sa, RecordItems<Loop, Q8>{&p, items + n_tc, pages}, n_small, lane);
         if (warp == 1) {
             tc_fence_after();
             tmem_dealloc(tmem, 512);
@@ -289,25 +299,29 @@ __global__ void __launch_bounds__(kThreads, 1) hp_cascade_kernel(const __grid_co
             tc_fence_before();
             tcr::named_sync(0, kThreads);
         }
-        if (warp - 4 < p.small_nh && n_small > 0)
-            smr::consumer<D, kNC, kSmallStages, kQRows>(sc, sa, warp - 4, lane);
+        if (warp - 4 < p.small_nh && n_small > 0) {
+            if constexpr (Q8)
+                smr::consumer_q8<D, kNC, kSmallStages, kQRows>(sc, sa, warp - 4, lane);
+            else
+                smr::consumer<D, kNC, kSmallStages, kQRows>(sc, sa, warp - 4, lane);
+        }
     }
     __syncwarp();
 }
 
-template <int D, bool Loop>
+template <int D, bool Loop, bool Q8>
 cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
 {
     static DeviceOnce once;  // per instantiation and device
-    const int bytes = FusedLayout<D>::kBytes + 1024;
-    static_assert(FusedLayout<D>::kBytes + 1024 <= 227 * 1024, "shared memory per CTA");
+    const int bytes = FusedLayout<D, Q8>::kBytes + 1024;
+    static_assert(FusedLayout<D, Q8>::kBytes + 1024 <= 227 * 1024, "shared memory per CTA");
     cudaError_t e = once.run([bytes] {
         cudaError_t r =
-            cudaFuncSetAttribute(hp_cascade_kernel<D, Loop>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            cudaFuncSetAttribute(hp_cascade_kernel<D, Loop, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (r != cudaSuccess)
             return r;
         cudaFuncAttributes fa;
-        if ((r = cudaFuncGetAttributes(&fa, hp_cascade_kernel<D, Loop>)) != cudaSuccess)
+        if ((r = cudaFuncGetAttributes(&fa, hp_cascade_kernel<D, Loop, Q8>)) != cudaSuccess)
             return r;
         // the register split assumes this allocation
         return fa.numRegs == (int)tcr::kRegsLaunch ? cudaSuccess : cudaErrorInvalidConfiguration;
@@ -327,7 +341,7 @@ cudaError_t launch_cascade_d(const CascadeParams &p, int grid, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, hp_cascade_kernel<D, Loop>, p);
+    return cudaLaunchKernelEx(&cfg, hp_cascade_kernel<D, Loop, Q8>, p);
 }
 
 }  // namespace
@@ -343,9 +357,12 @@ cudaError_t launch_cascade(const CascadeParams &p, int grid, int d, cudaStream_t
 {
     if (grid <= 0)
         return cudaSuccess;
+    if (p.q8)
+        return d == 128 && p.suffix_len == nullptr ? launch_cascade_d<128, false, true>(p, grid, s)
+                                                   : cudaErrorInvalidValue;
     if (p.suffix_len != nullptr)
-        return d == 64 ? launch_cascade_d<64, true>(p, grid, s) : launch_cascade_d<128, true>(p, grid, s);
-    return d == 64 ? launch_cascade_d<64, false>(p, grid, s) : launch_cascade_d<128, false>(p, grid, s);
+        return d == 64 ? launch_cascade_d<64, true, false>(p, grid, s) : launch_cascade_d<128, true, false>(p, grid, s);
+    return d == 64 ? launch_cascade_d<64, false, false>(p, grid, s) : launch_cascade_d<128, false, false>(p, grid, s);
 }
 
 }  // namespace hp

@@ -20,10 +20,11 @@ constexpr int64_t kMaxTcTiles = 128;
 // SMs of the current device (152 when none can be queried).
 int device_sms();
 
-// Paged pool [num_pages][Hkv][ps][d] bf16, box = 64 columns x box_tok tokens
-// x box_heads heads, 128-byte swizzle.
+// Paged pool [num_pages][Hkv][ps][d], 128-byte swizzle: bf16, box = 64
+// columns x box_tok tokens x box_heads heads; or (e4m3) one byte per element,
+// box = d (128) bytes x box_tok tokens x box_heads heads.
 bool encode_pool_map(CUtensorMap *m, const void *pool, int num_pages, int Hkv, int ps, int d, int box_tok,
-                     int box_heads = 1);
+                     int box_heads = 1, bool e4m3 = false);
 
 // The step's workspace: status word, partial LSE [rows] f32, partial O
 // [rows][d] bf16.

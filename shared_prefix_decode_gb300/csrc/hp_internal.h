@@ -183,6 +183,11 @@ struct SmallParams {
     uint16_t *part_o;   // bf16
     float *part_lse;
     uint32_t *status;
+    // E4M3 pools (q8 != 0): codes [num_pages][Hkv][page_size][d] bytes, scales
+    // of (page, KV head) at k_scale / v_scale[page * Hkv + head]
+    int32_t q8;
+    const float *k_scale;
+    const float *v_scale;
 };
 
 // Fused cascade kernel (tensor-core and paged roles, one persistent launch).
@@ -216,6 +221,11 @@ struct CascadeParams {
     uint16_t *loop_k_pool;
     uint16_t *loop_v_pool;
     int32_t Hkv, d;
+    // trees whose paged levels hold E4M3 codes (q8 != 0): the scales of each
+    // pool slot, (page, KV head) at k_scale[slot][page * Hkv + head]
+    int32_t q8;
+    const float *k_scale[kMaxLevels];
+    const float *v_scale[kMaxLevels];
 };
 
 // Decode-loop append: one token per sequence into its suffix pages.
@@ -292,7 +302,7 @@ __host__ __device__ inline int64_t tc_part_row(int64_t part_row, int s, int g, i
     const int spb = kTcTile / G;
     return part_row + (int64_t)(s / spb) * kTcTile + (int64_t)(s % spb) * G + g;
 }
-size_t small_smem_bytes(int d);
+size_t small_smem_bytes(int d, bool q8 = false);
 int small_heads_per_item(int Hkv);
 
 }  // namespace hp

@@ -32,9 +32,10 @@ struct CostModel {
         return tc_item + (two ? tc_tile : tc_tile1) * (double)ceil_div(w.k1_model - w.k0, kTcTile) * d / 128.0;
     }
     // a paged item loads its keys and values once for all its sequences
-    double small(const WorkItem &w, int d, int nh) const
+    // (bytes_kv: bytes of one key's K and V elements, 4 for bf16, 2 for E4M3)
+    double small(const WorkItem &w, int d, int nh, int bytes_kv = 4) const
     {
-        return sm_item + (double)(w.k1_model - w.k0) * nh * d * 4 / sm_bytes_per_ns;
+        return sm_item + (double)(w.k1_model - w.k0) * nh * d * bytes_kv / sm_bytes_per_ns;
     }
 };
 
@@ -101,7 +102,7 @@ double schedule(HostPlan &P, int grid, int n_tc_ctas, bool mixed, int d, const C
         const int nh = P.hdr.small_nh;
         for (size_t j = 0; j < P.small.size(); ++j) {
             const WorkItem &w = P.small[j];
-            P.jobs_sm.push_back({cm.small(w, d, nh), (int32_t)j, false,
+            P.jobs_sm.push_back({cm.small(w, d, nh, P.level_kv[w.level] == HP_KV_E4M3 ? 2 : 4), (int32_t)j, false,
                                  (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
         }
         P.jobs_all = P.jobs_tc;
@@ -323,7 +324,8 @@ void plan_nodes(const hp_tree_desc *d, int G, int capacity, const std::vector<in
     auto same_pools = [&](int a, int b) {
         const hp_tree_level &A = d->levels[a], &Bl = d->levels[b];
         return A.k_pool == Bl.k_pool && A.v_pool == Bl.v_pool && A.num_pages == Bl.num_pages &&
-               A.page_size == Bl.page_size;
+               A.page_size == Bl.page_size && A.kv_type == Bl.kv_type && A.k_scale == Bl.k_scale &&
+               A.v_scale == Bl.v_scale;
     };
     // members[l][n]: the (level, node) list a fused node starts with; skip[l][n]: fused into another
     std::vector<std::vector<std::vector<std::pair<int, int>>>> members(d->num_levels);
@@ -414,6 +416,14 @@ hp_status validate_desc(const hp_tree_desc *d)
             return HP_ERR_UNSUPPORTED;
         if (!L.k_pool || !L.v_pool || !aligned(L.k_pool, 16) || !aligned(L.v_pool, 16))
             return HP_ERR_ARG;
+        if (L.kv_type != HP_KV_BF16 && L.kv_type != HP_KV_E4M3)
+            return HP_ERR_ARG;
+        if (L.kv_type == HP_KV_E4M3) {
+            if (d->d != 128)
+                return HP_ERR_UNSUPPORTED;
+            if (!L.k_scale || !L.v_scale || !aligned(L.k_scale, 4) || !aligned(L.v_scale, 4))
+                return HP_ERR_ARG;
+        }
         if ((L.num_nodes > 0 && !L.nodes) || (L.num_page_ids > 0 && !L.page_ids))
             return HP_ERR_ARG;
         std::vector<std::pair<int, int>> ranges;
@@ -481,16 +491,22 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
     std::vector<int> slot_level;  // the first level of each slot
     P.level_ps.assign(d->num_levels, 0);
     P.level_slot.assign(d->num_levels, 0);
+    P.level_kv.assign(d->num_levels, HP_KV_BF16);
+    P.slot_kv.clear();
+    P.slot_k_scale.clear();
+    P.slot_v_scale.clear();
     for (int l = 0; l < d->num_levels; ++l) {
         const hp_tree_level &L = d->levels[l];
         P.level_ps[l] = L.page_size;
+        P.level_kv[l] = L.kv_type;
         level_page_off[l] = (int32_t)P.page_ids.size();
         P.page_ids.insert(P.page_ids.end(), L.page_ids, L.page_ids + L.num_page_ids);
         int slot = 0;
         while (slot < (int)slot_level.size()) {
             const hp_tree_level &S = d->levels[slot_level[slot]];
             if (S.k_pool == L.k_pool && S.v_pool == L.v_pool && S.num_pages == L.num_pages &&
-                S.page_size == L.page_size)
+                S.page_size == L.page_size && S.kv_type == L.kv_type && S.k_scale == L.k_scale &&
+                S.v_scale == L.v_scale)
                 break;
             ++slot;
         }
@@ -504,12 +520,34 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
             LD.num_pages = L.num_pages;
             LD.page_size = L.page_size;
             LD.tc_box = std::gcd(L.page_size, kTcTile);
+            LD.pad = L.kv_type;
+            P.slot_kv.push_back(L.kv_type);
+            P.slot_k_scale.push_back(L.kv_type == HP_KV_E4M3 ? L.k_scale : nullptr);
+            P.slot_v_scale.push_back(L.kv_type == HP_KV_E4M3 ? L.v_scale : nullptr);
         }
         P.level_slot[l] = slot;
     }
     H.num_levels = (int32_t)slot_level.size();
 
     plan_nodes(d, G, capacity, level_page_off, P);
+
+    // E4M3 levels: only nodes of the per-sequence pass, and then every node
+    // of that pass in an E4M3 level (the kernel's paged role runs one
+    // storage); none in decode-loop plans
+    P.q8 = false;
+    for (int l = 0; l < d->num_levels; ++l)
+        P.q8 = P.q8 || P.level_kv[l] == HP_KV_E4M3;
+    if (P.q8) {
+        if (capacity > 0)
+            return HP_ERR_UNSUPPORTED;
+        for (const PNode &N : P.nodes) {
+            if (N.kv_len == 0)
+                continue;
+            const bool tc = (int64_t)(N.seq_end - N.seq_begin) * G > kSmallRows;
+            if (tc == (P.level_kv[N.level] == HP_KV_E4M3))
+                return HP_ERR_UNSUPPORTED;
+        }
+    }
 
     // Work sizes: 128-key tiles of the shared (tensor-core) nodes, 16-key
     // chunks of the paged ones.
@@ -629,6 +667,15 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
             const hp_tree_level &L = d->levels[slot_level[sl]];
             const int tcb = H.levels[sl].tc_box;
             CUtensorMap *m = &P.maps[sl * kMapsPerLevel];
+            if (L.kv_type == HP_KV_E4M3) {
+                // paged boxes only; the tensor-core slots hold copies (never used)
+                if (!encode_pool_map(m + 2, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk, nh, true) ||
+                    !encode_pool_map(m + 3, L.v_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk, nh, true))
+                    return HP_ERR_CUDA;
+                m[0] = m[2];
+                m[1] = m[3];
+                continue;
+            }
             if (!encode_pool_map(m + 0, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, tcb) ||
                 !encode_pool_map(m + 1, L.v_pool, L.num_pages, d->Hkv, L.page_size, d->d, tcb) ||
                 !encode_pool_map(m + 2, L.k_pool, L.num_pages, d->Hkv, L.page_size, d->d, kChunk, nh) ||

@@ -38,6 +38,11 @@ struct HostPlan {
     std::vector<int32_t> page_ids;     // all levels' page ids, concatenated
     std::vector<int32_t> level_ps;     // page size per level
     std::vector<int32_t> level_slot;   // pool slot of each level (levels with the same pools share one)
+    std::vector<int32_t> level_kv;     // hp_kv_type of each level
+    // per pool slot: hp_kv_type and the E4M3 scale arrays (device pointers)
+    std::vector<int32_t> slot_kv;
+    std::vector<const float *> slot_k_scale, slot_v_scale;
+    bool q8 = false;  // the paged levels hold E4M3 codes
     std::vector<int32_t> merge_tab;  // [B*Hkv][merge_stride]
     std::vector<int32_t> leaf_tab;   // decode loop: [B][leaf_stride] suffix page ids
     std::vector<std::vector<int32_t>> cta_tc, cta_small;  // item ids per CTA of the fused kernel

@@ -1,7 +1,8 @@
-// hp_small_kernel.cu -- standalone paged decode (hp_suffix_decode_paged and
-// its allocation-free variant): the paged-decode role (hp_small_role.cuh)
-// with one producer warp and four consumer warps per CTA; CTA c walks items
-// c, c + grid, ... of (sequence, KV-head group, key split).
+// hp_small_kernel.cu -- standalone paged decode (hp_suffix_decode_paged, its
+// allocation-free variant, and hp_suffix_decode_paged_e4m3): the
+// paged-decode role (hp_small_role.cuh) with one producer warp and four
+// consumer warps per CTA; CTA c walks items c, c + grid, ... of (sequence,
+// KV-head group, key split).  Q8: E4M3 pools with per-(page, KV head) scales.
 #include <cuda_runtime.h>
 
 #include "hp_internal.h"
@@ -13,18 +14,19 @@ namespace hp {
 namespace {
 
 constexpr int kConsumers = 4;
-constexpr int kStages = 3;
 constexpr int kThreadsSmall = (kConsumers + 1) * 32;
 constexpr int kQRows = 16;  // Q slot rows per stage: nh * G <= 16
 
-template <int D>
+// bf16 pools: 3 stages of 16-token chunks; E4M3 pools: 5 (half the bytes each)
+template <int D, bool Q8>
 struct SmallKernelLayout {
-    using R = smr::Layout<D, kConsumers, kStages, kQRows>;
+    static constexpr int kStages = Q8 ? 5 : 3;
+    using R = smr::Layout<D, kConsumers, kStages, kQRows, Q8>;
     static constexpr int kBar = R::kEnd;
     static constexpr int kMeta = kBar + 2 * kStages * 8;
-    static constexpr int kZero = kMeta + 128;  // 16 zero bytes, then the abort flag
+    static constexpr int kZero = kMeta + 256;  // 16 zero bytes, then the abort flag
     static constexpr int kBytes = kZero + 32;
-    static_assert(kStages * (int)sizeof(smr::StageMeta) <= 128, "stage metadata");
+    static_assert(kStages * (int)sizeof(smr::StageMeta) <= 256, "stage metadata");
 };
 
 // Items of the page-table form: idx -> (sequence, head group, split).
@@ -60,15 +62,19 @@ struct TableItems {
         d.num_pages = p->num_pages;
         d.map_k = &p->map_k;
         d.map_v = &p->map_v;
+        d.k_scale = p->k_scale;
+        d.v_scale = p->v_scale;
+        d.Hkv = p->Hkv;
         d.valid = d.k0 < d.k1;
         return d;
     }
 };
 
-template <int D>
+template <int D, bool Q8>
 __global__ void __launch_bounds__(kThreadsSmall) hp_small_kernel(const __grid_constant__ SmallParams p)
 {
-    using KL = SmallKernelLayout<D>;
+    using KL = SmallKernelLayout<D, Q8>;
+    constexpr int kStages = KL::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -96,30 +102,38 @@ __global__ void __launch_bounds__(kThreadsSmall) hp_small_kernel(const __grid_co
     __syncthreads();
     const int n_items = p.n_items > (int)blockIdx.x ? (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     if (warp == kConsumers)
-        smr::producer<D, kConsumers, kStages, kQRows>(c, a, TableItems{&p, (int)blockIdx.x, (int)gridDim.x}, n_items, lane);
-    else if (warp < p.nh)
-        smr::consumer<D, kConsumers, kStages, kQRows>(c, a, warp, lane);
+        smr::producer<D, kConsumers, kStages, kQRows, TableItems, Q8>(
+            c, a, TableItems{&p, (int)blockIdx.x, (int)gridDim.x}, n_items, lane);
+    else if (warp < p.nh) {
+        if constexpr (Q8)
+            smr::consumer_q8<D, kConsumers, kStages, kQRows>(c, a, warp, lane);
+        else
+            smr::consumer<D, kConsumers, kStages, kQRows>(c, a, warp, lane);
+    }
     __syncwarp();
 }
 
-template <int D>
+template <int D, bool Q8>
 cudaError_t launch_small_d(const SmallParams &p, int grid, cudaStream_t s)
 {
     static DeviceOnce once;  // per instantiation and device
-    const int bytes = SmallKernelLayout<D>::kBytes + 1024;
-    cudaError_t e = once.run(
-        [bytes] { return cudaFuncSetAttribute(hp_small_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes); });
+    const int bytes = SmallKernelLayout<D, Q8>::kBytes + 1024;
+    cudaError_t e = once.run([bytes] {
+        return cudaFuncSetAttribute(hp_small_kernel<D, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
     if (e != cudaSuccess)
         return e;
-    hp_small_kernel<D><<<grid, kThreadsSmall, bytes, s>>>(p);
+    hp_small_kernel<D, Q8><<<grid, kThreadsSmall, bytes, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t small_smem_bytes(int d)
+size_t small_smem_bytes(int d, bool q8)
 {
-    return d == 64 ? SmallKernelLayout<64>::kBytes + 1024 : SmallKernelLayout<128>::kBytes + 1024;
+    if (q8)
+        return SmallKernelLayout<128, true>::kBytes + 1024;
+    return d == 64 ? SmallKernelLayout<64, false>::kBytes + 1024 : SmallKernelLayout<128, false>::kBytes + 1024;
 }
 
 int small_q_rows() { return kQRows; }
@@ -133,7 +147,9 @@ cudaError_t launch_small(const SmallParams &p, int grid, int d, cudaStream_t s)
 {
     if (grid <= 0)
         return cudaSuccess;
-    return d == 64 ? launch_small_d<64>(p, grid, s) : launch_small_d<128>(p, grid, s);
+    if (p.q8)
+        return d == 128 ? launch_small_d<128, true>(p, grid, s) : cudaErrorInvalidValue;
+    return d == 64 ? launch_small_d<64, false>(p, grid, s) : launch_small_d<128, false>(p, grid, s);
 }
 
 }  // namespace hp

@@ -25,6 +25,24 @@
 // the (up to 16) query rows of a head, S = Q K^T for 16 keys is two n8
 // tiles, and O = P V reuses the S accumulator layout as the A operand.  The
 // producer runs ahead across item boundaries.
+//
+// Reduced-precision KV (Q8 instantiations, d = 128): the pools hold E4M3
+// codes, one byte per element, with an f32 scale per (page, KV head) for K
+// and one for V (Hydragen, "Implications and Future Directions": the suffix
+// pass is memory-bound and quantising its KV cache halves its bytes).  A
+// stage holds the 16-token chunk's codes (one box of 16 tokens x 128 bytes x
+// nh heads per K and per V) and the chunk's scales, which the producer copies
+// with cp.async tracked by the stage's barrier.  The consumers convert codes
+// to f16 in registers (exact) and use the f16 MMA: the queries are rounded
+// from bf16 to f16 once per item (exact for |q| in f16's normal range),
+// scores are scaled by the chunk's K scale, and P is multiplied by the V
+// scale before it is rounded to f16 for P V.  For S = Q K^T each thread reads
+// its 32-byte slice of a key row with two 16-byte loads and uses byte 4i..4i+3
+// at k-step i: the head dimension is visited in a permuted order, the same
+// for Q and K, so the dot product is unchanged.  For P V each thread reads
+// 16 consecutive columns of four key rows and pairs the bytes of two rows per
+// B register; the output columns come out in a matching permuted order that
+// the epilogue undoes (each thread ends with 32 consecutive columns).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -38,18 +56,21 @@ namespace smr {
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // Shared memory of the role for NC consumer warps, S stages and a Q slot of
-// QR rows per stage.
-template <int D, int NC, int S, int QR>
+// QR rows per stage; Q8: E4M3 pools (d = 128).
+template <int D, int NC, int S, int QR, bool Q8 = false>
 struct Layout {
+    static_assert(!Q8 || D == 128, "E4M3 pools: d = 128");
     static constexpr int kHalves = D / 64;
-    static constexpr int kHeadBox = 16 * 128;     // one head: [16 tokens][64 bf16], swizzled
-    static constexpr int kHalf = NC * kHeadBox;   // one column half of the head group
-    static constexpr int kChunk = kHalves * kHalf;  // K (or V) of one 16-token chunk
+    static constexpr int kHeadBox = 16 * 128;     // one head: [16 tokens][64 bf16] or [16 tokens][128 E4M3], swizzled
+    static constexpr int kHalf = NC * kHeadBox;   // one column half of the head group (bf16)
+    static constexpr int kChunk = Q8 ? kHalf : kHalves * kHalf;  // K (or V) of one 16-token chunk
     static constexpr int kQRows = QR;                // Q slot: nh * G <= QR rows of one sequence
     static constexpr int kQHalf = kQRows * 128;
     static constexpr int kQSlot = kHalves * kQHalf;
-    static constexpr int kStage = 2 * kChunk + kQSlot;  // K, V, Q slot
+    static constexpr int kScales = Q8 ? 1024 : 0;  // Q8: K scales [NC], then V scales at +128 bytes (f32)
+    static constexpr int kStage = 2 * kChunk + kQSlot + kScales;  // K, V, Q slot, scales
     static constexpr int kEnd = S * kStage;
+    static_assert(NC * 4 <= 128, "scale slots");
 };
 
 // What the consumers need about the chunk in a stage.
@@ -69,6 +90,10 @@ struct Desc {
     int ps, num_pages;
     const void *map_k;
     const void *map_v;
+    // E4M3 pools: scale of (page, KV head h) at k_scale[page * Hkv + h]
+    const float *k_scale = nullptr;
+    const float *v_scale = nullptr;
+    int Hkv = 0;
     // A decode step with the append fused: the item holds the step's new
     // token (its last key).  The producer copies the token's K and V rows of
     // the item's nh heads (head h at src + h * src_sh) to the pool (head h
@@ -109,10 +134,10 @@ struct Args {
 // dependent load at the item's start), then closes the ring with a sentinel
 // stage (n_seq = -1, completed by a plain arrival) that tells the consumers
 // to stop.  All 32 lanes call it.
-template <int D, int NC, int S, int QR, class Src>
+template <int D, int NC, int S, int QR, class Src, bool Q8 = false>
 __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src &src, int n_items, int lane)
 {
-    using L = Layout<D, NC, S, QR>;
+    using L = Layout<D, NC, S, QR, Q8>;
     constexpr int kHalves = D / 64;
     auto wait_warp = [&](uint32_t b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
@@ -182,6 +207,23 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 fence_proxy_async_global();
                 __syncwarp();
             }
+            if constexpr (Q8) {
+                // the chunk's scales: K of heads kvh0 .. kvh0 + nh - 1 by lanes
+                // 8.., V by lanes 16..; tracked by the stage's barrier (its
+                // pending count rises before the producer's own arrival)
+                const int hi = lane & 7;
+                if (lane >= 8 && lane < 24 && hi < a.nh) {
+                    const bool is_v = lane >= 16;
+                    const uint32_t dst = c.sbase + st * L::kStage + 2 * L::kChunk + L::kQSlot + (is_v ? 128 : 0) + 4 * hi;
+                    if (oob) {
+                        st_shared_f32(dst, 0.f);
+                    } else {
+                        cp_async_4(dst, (is_v ? d.v_scale : d.k_scale) + (int64_t)page * d.Hkv + d.kvh0 + hi);
+                        cp_async_mbar_arrive(bar);
+                    }
+                }
+                __syncwarp();
+            }
             if (lane == 0) {
                 if (oob)
                     atomicOr(c.status, kStBounds);
@@ -195,17 +237,18 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 m.last = ch + 1 == nchunks;
                 m.qslot = ch == 0 && qslot;
                 c.meta[st] = m;
-                mbar_arrive_expect_tx(bar, 2 * kHalves * a.nh * L::kHeadBox +
+                mbar_arrive_expect_tx(bar, (Q8 ? 2 : 2 * kHalves) * a.nh * L::kHeadBox +
                                                (m.qslot ? kHalves * a.nh * a.G * 128 : 0));
             }
             __syncwarp();
-            if (lane < 2 * kHalves) {
-                const int h = lane % kHalves;
-                const bool is_v = lane >= kHalves;
+            constexpr int kBoxLanes = Q8 ? 2 : 2 * kHalves;  // K and V boxes (one per column half for bf16)
+            if (lane < kBoxLanes) {
+                const int h = Q8 ? 0 : lane % kHalves;
+                const bool is_v = Q8 ? lane == 1 : lane >= kHalves;
                 tma_load_4d_h(c.sbase + st * L::kStage + (is_v ? L::kChunk : 0) + h * L::kHalf,
                               is_v ? d.map_v : d.map_k, bar, h * 64, t % d.ps, d.kvh0, page, l2_evict_first());
-            } else if (ch == 0 && qslot && lane < 3 * kHalves) {
-                const int h = lane - 2 * kHalves;
+            } else if (ch == 0 && qslot && lane < kBoxLanes + kHalves) {
+                const int h = lane - kBoxLanes;
                 tma_load_3d(c.sbase + st * L::kStage + 2 * L::kChunk + h * L::kQHalf, a.map_q, bar, h * 64,
                             d.kvh0 * a.G, d.seq_begin);
             }
@@ -412,6 +455,224 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
                     *reinterpret_cast<uint32_t *>(dst + n * 8) = pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
                 if ((lane & 3) == 0)
                     a.part_lse[base + r1] = L1 > 0.f ? (m1 + fast_log2(L1)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+}
+
+// E4M3 consumer warp w (0 <= w < nh), d = 128: as `consumer`, with codes
+// converted to f16 in registers.  The running output o' is kept in units of
+// the V scale of the latest chunk (vcur); when the next chunk's V scale
+// differs, o' is rescaled by vcur / vsc, folded into the softmax rescale, so
+// P stays in [0, 1] when it is rounded to f16.  A chunk whose V scale is 0
+// adds nothing to O (its weights still count in the denominator).
+template <int D, int NC, int S, int QR>
+__device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, int lane)
+{
+    using L = Layout<D, NC, S, QR, true>;
+    static_assert(D == 128, "E4M3 pools: d = 128");
+    constexpr int kKs = D / 16;  // k-steps of the S MMA
+    constexpr int kNt = D / 8;   // n8 tiles of O
+    auto wait_warp = [&](uint32_t b, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
+    };
+    uint32_t qa[kKs][4];
+    float o[kNt][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, vcur = 0.f;
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = g, r1 = g + 8;
+    const uint32_t hoff = (uint32_t)w * L::kHeadBox;  // this warp's head within a box
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t st = k % S;
+        if (!wait_warp(c.full0 + 8 * st, (k / S) & 1u))
+            break;
+        const StageMeta m = c.meta[st];
+        if (m.n_seq < 0)
+            break;  // sentinel: the producer's walk is over
+        const int rows = m.n_seq * a.G;
+        const int kvh = m.kvh0 + w;
+        const uint32_t stage = c.sbase + st * L::kStage;
+        if (m.first) {
+            // query rows r0 / r1 of head w as f16: k-step i takes columns
+            // 32t + 4i .. 32t + 4i + 3 (a0/a1: the first pair, a2/a3: the second)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = rr ? r1 : r0;
+                uint4 x[4];
+                if (r < rows && m.qslot) {
+                    const int srow = w * a.G + r;
+                    const uint32_t qs = stage + 2 * L::kChunk + (t >> 1) * L::kQHalf + srow * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        x[cc] = ld_shared_v4(qs + (((4 * (t & 1) + cc) ^ (srow & 7)) << 4));
+                } else if (r < rows) {
+                    const uint16_t *q = a.q + (int64_t)(m.seq_begin + r / a.G) * a.q_sb +
+                                        (int64_t)(kvh * a.G + r % a.G) * a.q_sh + 32 * t;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        x[cc] = __ldg(reinterpret_cast<const uint4 *>(q) + cc);
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        x[cc] = make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    qa[2 * cc][rr] = pack_f16x2(bf16lo_to_f32(x[cc].x), bf16hi_to_f32(x[cc].x));
+                    qa[2 * cc][2 + rr] = pack_f16x2(bf16lo_to_f32(x[cc].y), bf16hi_to_f32(x[cc].y));
+                    qa[2 * cc + 1][rr] = pack_f16x2(bf16lo_to_f32(x[cc].z), bf16hi_to_f32(x[cc].z));
+                    qa[2 * cc + 1][2 + rr] = pack_f16x2(bf16lo_to_f32(x[cc].w), bf16hi_to_f32(x[cc].w));
+                }
+            }
+#pragma unroll
+            for (int n = 0; n < kNt; ++n)
+                o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+            vcur = 0.f;
+        }
+        const uint32_t kst = stage + hoff;
+        const uint32_t vst = stage + L::kChunk + hoff;
+        const float ksc = ld_shared_f32(stage + 2 * L::kChunk + L::kQSlot + 4 * w);
+        const float vsc = ld_shared_f32(stage + 2 * L::kChunk + L::kQSlot + 128 + 4 * w);
+        const int nvalid = m.nvalid;
+        if (nvalid < kChunk) {
+            // rows past the valid keys: zero this head's V codes so that
+            // 0 * (whatever the pool holds there) stays 0
+            uint8_t *vp = c.smem + (vst - c.sbase);
+            const int nz = (kChunk - nvalid) * 8;
+            for (int i = lane; i < nz; i += 32)
+                *reinterpret_cast<uint4 *>(vp + (nvalid + i / 8) * 128 + (i % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // S = Q K^T over 16 keys: n8 tile 0 = keys 0-7, tile 1 = keys 8-15;
+        // thread (g, t) reads bytes 32t .. 32t+31 of key rows g and g + 8
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const uint4 ka = ld_shared_v4(kst + r0 * 128 + (((2 * t) ^ (r0 & 7)) << 4));
+            const uint4 kb = ld_shared_v4(kst + r0 * 128 + (((2 * t + 1) ^ (r0 & 7)) << 4));
+            const uint4 kc = ld_shared_v4(kst + r1 * 128 + (((2 * t) ^ (r1 & 7)) << 4));
+            const uint4 kd = ld_shared_v4(kst + r1 * 128 + (((2 * t + 1) ^ (r1 & 7)) << 4));
+            const uint32_t w0[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+            const uint32_t w1[8] = {kc.x, kc.y, kc.z, kc.w, kd.x, kd.y, kd.z, kd.w};
+#pragma unroll
+            for (int ks = 0; ks < kKs; ++ks) {
+                mma_f16_16816(s0, qa[ks], e4m3x2_to_f16x2(w0[ks]), e4m3x2_to_f16x2(w0[ks] >> 16));
+                mma_f16_16816(s1, qa[ks], e4m3x2_to_f16x2(w1[ks]), e4m3x2_to_f16x2(w1[ks] >> 16));
+            }
+        }
+        // online softmax (rows r0: elements 0,1; rows r1: elements 2,3); the
+        // chunk's K scale multiplies the scores
+        const float cs = a.scale_log2 * ksc;
+        const int tq = 2 * t;
+        float x[2][4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int tk = tq + (e & 1);
+            x[0][e] = tk < nvalid ? s0[e] * cs : -INFINITY;
+            x[1][e] = tk + 8 < nvalid ? s1[e] * cs : -INFINITY;
+        }
+        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;  // all keys so far masked: nothing to scale
+        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float a0 = fast_exp2(m0 - ms0), a1 = fast_exp2(m1 - ms1);
+        m0 = mn0;
+        m1 = mn1;
+        // o' follows the V scale of this chunk (a chunk with scale 0 adds nothing)
+        const bool vuse = vsc != 0.f;
+        const float vr = (vuse && vcur != 0.f) ? vcur / vsc : 1.f;
+        if (vuse)
+            vcur = vsc;
+        const float f0 = a0 * vr, f1 = a1 * vr;
+        if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
+#pragma unroll
+            for (int n = 0; n < kNt; ++n) {
+                o[n][0] *= f0;
+                o[n][1] *= f0;
+                o[n][2] *= f1;
+                o[n][3] *= f1;
+            }
+        }
+        l0 *= a0;
+        l1 *= a1;
+        float p[2][4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            p[0][e] = fast_exp2(x[0][e] - ((e & 2) ? ms1 : ms0));
+            p[1][e] = fast_exp2(x[1][e] - ((e & 2) ? ms1 : ms0));
+        }
+        l0 += p[0][0] + p[0][1] + p[1][0] + p[1][1];
+        l1 += p[0][2] + p[0][3] + p[1][2] + p[1][3];
+        uint32_t pa[4];
+        const float pz = vuse ? 1.f : 0.f;
+        pa[0] = pack_f16x2(p[0][0] * pz, p[0][1] * pz);
+        pa[1] = pack_f16x2(p[0][2] * pz, p[0][3] * pz);
+        pa[2] = pack_f16x2(p[1][0] * pz, p[1][1] * pz);
+        pa[3] = pack_f16x2(p[1][2] * pz, p[1][3] * pz);
+
+        // O' += P V: thread (g, t) reads columns 16g .. 16g+15 of key rows 2t,
+        // 2t+1, 2t+8, 2t+9; n8 tile j takes column 16g + j as its column g
+        {
+            const int ta = 2 * t, tb = 2 * t + 1;
+            const uint4 va = ld_shared_v4(vst + ta * 128 + ((g ^ (ta & 7)) << 4));
+            const uint4 vb = ld_shared_v4(vst + tb * 128 + ((g ^ (tb & 7)) << 4));
+            const uint4 vc = ld_shared_v4(vst + (ta + 8) * 128 + ((g ^ (ta & 7)) << 4));
+            const uint4 vd = ld_shared_v4(vst + (tb + 8) * 128 + ((g ^ (tb & 7)) << 4));
+            const uint32_t A[4] = {va.x, va.y, va.z, va.w}, B[4] = {vb.x, vb.y, vb.z, vb.w};
+            const uint32_t C[4] = {vc.x, vc.y, vc.z, vc.w}, E[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                // byte pairs (row 2t, row 2t+1) and (row 2t+8, row 2t+9) of columns 4q4 .. 4q4+3
+                const uint32_t lo01 = __byte_perm(A[q4], B[q4], 0x5140), hi01 = __byte_perm(A[q4], B[q4], 0x7362);
+                const uint32_t lo89 = __byte_perm(C[q4], E[q4], 0x5140), hi89 = __byte_perm(C[q4], E[q4], 0x7362);
+                mma_f16_16816(o[4 * q4 + 0], pa, e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo89));
+                mma_f16_16816(o[4 * q4 + 1], pa, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(lo89 >> 16));
+                mma_f16_16816(o[4 * q4 + 2], pa, e4m3x2_to_f16x2(hi01), e4m3x2_to_f16x2(hi89));
+                mma_f16_16816(o[4 * q4 + 3], pa, e4m3x2_to_f16x2(hi01 >> 16), e4m3x2_to_f16x2(hi89 >> 16));
+            }
+        }
+        // release the stage to the producer
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(c.empty0 + 8 * st);
+
+        if (m.last) {
+            float L0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+            L0 += __shfl_xor_sync(0xffffffffu, L0, 2);
+            float L1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+            L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
+            const float inv0 = L0 > 0.f ? vcur / L0 : 0.f;
+            const float inv1 = L1 > 0.f ? vcur / L1 : 0.f;
+            const int base = m.part_row + w * rows;  // this head's rows
+            // o[j][0|2]: column 32t + j, o[j][1|3]: column 32t + 16 + j
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = rr ? r1 : r0;
+                if (r >= rows)
+                    continue;
+                const float inv = rr ? inv1 : inv0;
+                uint4 *dst = reinterpret_cast<uint4 *>(a.part_o + (size_t)(base + r) * D + 32 * t);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // columns 32t + 16h .. + 15
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        pk[i] = pack_bf16x2(o[2 * i][2 * rr + h] * inv, o[2 * i + 1][2 * rr + h] * inv);
+                    dst[2 * h] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[2 * h + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+                if (t == 0) {
+                    const float Lr = rr ? L1 : L0;
+                    a.part_lse[base + r] = Lr > 0.f ? ((rr ? m1 : m0) + fast_log2(Lr)) * kLn2 : -INFINITY;
+                }
             }
         }
     }

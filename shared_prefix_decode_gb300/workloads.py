@@ -45,7 +45,12 @@ __all__ = [
     "StreamRequests",
     "stream_requests",
     "streams_as_tree",
+    "E4M3Pools",
+    "quantize_e4m3",
+    "with_e4m3_levels",
 ]
+
+E4M3_MAX = 448.0  # largest finite value of the E4M3 format
 
 
 @dataclass
@@ -58,10 +63,27 @@ class TreeLevel:
 
     nodes: torch.Tensor
     page_ids: torch.Tensor
+    e4m3: bool = False  # keys and values of this level come from the workload's E4M3 pools
 
     @property
     def num_nodes(self) -> int:
         return int(self.nodes.shape[0])
+
+
+@dataclass
+class E4M3Pools:
+    """Reduced-precision copies of a workload's pools: E4M3 codes (raw bytes,
+    uint8 ``[num_pages, Hkv, ps, d]``) with one f32 scale per (page, KV head)
+    for K and for V; the stored value of a code is its E4M3 value times the
+    scale of its page and head."""
+
+    k: torch.Tensor
+    v: torch.Tensor
+    k_scale: torch.Tensor  # f32 [num_pages, Hkv]
+    v_scale: torch.Tensor
+
+    def to(self, device) -> "E4M3Pools":
+        return E4M3Pools(self.k.to(device), self.v.to(device), self.k_scale.to(device), self.v_scale.to(device))
 
 
 @dataclass
@@ -79,6 +101,7 @@ class CascadeWorkload:
     levels: List[TreeLevel] = field(default_factory=list)
     seed: int = 0
     part: str = "all"  # make_config's part: the whole workload, or one pass of it
+    q8: Optional[E4M3Pools] = None  # pools of the levels marked e4m3
 
     @property
     def G(self) -> int:
@@ -102,7 +125,17 @@ class CascadeWorkload:
         return sum(int(lv.nodes[:, 2].sum()) for lv in self.levels)
 
     def unique_kv_bytes(self) -> int:
-        return self.unique_kv_tokens() * self.Hkv * self.d * 2 * 2
+        """Bytes of K and V stored once: 2 bytes per element for bf16 levels,
+        1 for E4M3 levels plus their two f32 scales per (page, KV head)."""
+        tot = 0
+        for lv in self.levels:
+            toks = int(lv.nodes[:, 2].sum())
+            if lv.e4m3:
+                pages = sum((int(n[2]) + self.page_size - 1) // self.page_size for n in lv.nodes.tolist())
+                tot += toks * self.Hkv * self.d * 2 + pages * self.Hkv * 8
+            else:
+                tot += toks * self.Hkv * self.d * 4
+        return tot
 
     def shared_flops(self) -> int:
         """4 * rows * keys * d over nodes that cover more than one sequence
@@ -115,10 +148,11 @@ class CascadeWorkload:
         return tot
 
     def to(self, device) -> "CascadeWorkload":
-        lv = [TreeLevel(l.nodes.clone(), l.page_ids.to(device)) for l in self.levels]
+        lv = [TreeLevel(l.nodes.clone(), l.page_ids.to(device), l.e4m3) for l in self.levels]
         return CascadeWorkload(self.name, self.B, self.Hq, self.Hkv, self.d, self.page_size,
                                self.scale, self.q.to(device), self.k_pool.to(device),
-                               self.v_pool.to(device), lv, self.seed, self.part)
+                               self.v_pool.to(device), lv, self.seed, self.part,
+                               self.q8.to(device) if self.q8 is not None else None)
 
 
 def build_cascade(
@@ -450,6 +484,39 @@ def streams_as_tree(req: StreamRequests, page_size: int = 16) -> CascadeWorkload
                         torch.tensor(own_ids, dtype=torch.int32))]
     return CascadeWorkload("parallel_prompting", req.R * req.P, req.Hq, req.Hkv, req.d, ps, req.scale,
                            req.q.clone(), torch.stack(pages_k), torch.stack(pages_v), levels, 0)
+
+
+# ------------------------------------------------- reduced-precision pools
+def quantize_e4m3(k_pool: torch.Tensor, v_pool: torch.Tensor) -> E4M3Pools:
+    """E4M3 copies of bf16 pools ``[num_pages, Hkv, ps, d]``: per (page, KV
+    head) the scale is the largest magnitude over the page's tokens and
+    columns divided by 448 (1 for an all-zero slice), and each element is
+    rounded to the nearest E4M3 value of element / scale (ties to even, by
+    torch's float8_e4m3fn conversion).  Input preparation only: the attention
+    arithmetic never runs here."""
+    out = []
+    for pool in (k_pool, v_pool):
+        x = pool.float()
+        amax = x.abs().amax(dim=(2, 3))
+        sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).to(torch.float32)
+        y = (x / sc[:, :, None, None]).clamp(-E4M3_MAX, E4M3_MAX)
+        out.append((y.to(torch.float8_e4m3fn).view(torch.uint8).contiguous(), sc.contiguous()))
+    return E4M3Pools(out[0][0], out[1][0], out[0][1], out[1][1])
+
+
+def with_e4m3_levels(wl: CascadeWorkload, levels="paged") -> CascadeWorkload:
+    """The same workload with some levels read from E4M3 copies of its pools
+    (``quantize_e4m3`` of every page; the levels keep their page ids).
+    ``levels``: level indices, or "paged" (default) for every level whose
+    nodes all run the per-sequence pass (at most 16 query rows: sequences x
+    Hq/Hkv) -- the private suffixes and narrow shared nodes."""
+    if levels == "paged":
+        levels = [i for i, lv in enumerate(wl.levels)
+                  if all((int(n[1]) - int(n[0])) * wl.G <= 16 for n in lv.nodes.tolist())]
+    marks = {l % len(wl.levels) for l in levels}
+    lv = [TreeLevel(l.nodes.clone(), l.page_ids.clone(), i in marks or l.e4m3) for i, l in enumerate(wl.levels)]
+    return CascadeWorkload(wl.name, wl.B, wl.Hq, wl.Hkv, wl.d, wl.page_size, wl.scale, wl.q, wl.k_pool, wl.v_pool,
+                           lv, wl.seed, wl.part, quantize_e4m3(wl.k_pool, wl.v_pool))
 
 
 def _probe_code(b: int, d: int) -> torch.Tensor:

@@ -30,7 +30,7 @@ def test_library_loads_and_exports_every_declared_symbol():
         assert hasattr(lib, name), f"{name} declared in hp.h but not exported"
     assert set(declared) == set(hb.exported_symbols())
     assert lib.hp_build_arch() == 103
-    assert lib.hp_abi_version() == 3
+    assert lib.hp_abi_version() == 4
 
 
 def test_status_strings():
@@ -439,3 +439,61 @@ def test_deep_trees_and_pool_slot_limit():
     other_ps = [(bufs[0].data_ptr(), bufs[0].data_ptr(), 8, 32, node, [0])]
     assert hb.hp_cascade_plan_bytes(eight[:7] + other_ps, 4, 4, 4, 128, num_sms=152) > 0
     assert hb.hp_cascade_plan_bytes(eight + other_ps, 4, 4, 4, 128, num_sms=152) == 0
+
+
+# ------------------------------------------------ reduced-precision (E4M3) levels
+@pytest.mark.parametrize("name,kw", [("llama3_8b", {}), ("tree2", dict(B=32, prefix=256)),
+                                     ("codellama13b", dict(B=32, prefix=256)), ("no_sharing", {})])
+def test_e4m3_suffix_plans_cover_every_key_once(name, kw):
+    """Trees whose suffix level holds E4M3 codes plan like their bf16 twins:
+    the same coverage, roles and merge lists."""
+    wl = W.with_e4m3_levels(W.make_config(name, seed=0, **kw))
+    items = _check_plan_items(wl)
+    assert any(not it["tc"] for it in items)
+
+
+def test_e4m3_levels_are_rejected_where_the_kernels_do_not_read_them():
+    """E4M3 storage is for the per-sequence pass: a batched node in an E4M3
+    level, a per-sequence node left in bf16 next to an E4M3 level, d = 64,
+    missing scales and decode-loop plans are refused on the host."""
+    wl = W.make_config("llama3_8b", seed=0, B=8, prefix=256)
+    bad_tc = W.with_e4m3_levels(wl, levels=(0, -1))
+    assert hb.hp_cascade_plan_bytes(hb._levels_of(bad_tc), wl.B, wl.Hq, wl.Hkv, wl.d, num_sms=152) == 0
+    # a narrow shared node (4 sequences x G=4 = 16 rows: per-sequence pass) kept in bf16
+    narrow = W.build_cascade("n", B=8, Hq=32, Hkv=8, d=128, page_size=16, shared=[[(0, 4, 64), (4, 8, 64)]],
+                             suffix_range=(1, 40), seed=1)
+    mixed = W.with_e4m3_levels(narrow, levels=(-1,))
+    assert hb.hp_cascade_plan_bytes(hb._levels_of(mixed), 8, 32, 8, 128, num_sms=152) == 0
+    both = W.with_e4m3_levels(narrow, levels=(0, -1))
+    assert hb.hp_cascade_plan_bytes(hb._levels_of(both), 8, 32, 8, 128, num_sms=152) > 0
+    tiny = W.with_e4m3_levels(W.make_config("tiny", seed=0))  # d = 64
+    assert hb.hp_cascade_plan_bytes(hb._levels_of(tiny), tiny.B, tiny.Hq, tiny.Hkv, tiny.d, num_sms=152) == 0
+    lv = hb._levels_of(W.with_e4m3_levels(wl))
+    lv[-1] = lv[-1][:7] + (None, None)
+    assert hb.hp_cascade_plan_bytes(lv, wl.B, wl.Hq, wl.Hkv, wl.d, num_sms=152) == 0
+    cap = W.with_suffix_capacity(wl, 300)
+    loop = W.with_e4m3_levels(cap)
+    assert hb.hp_cascade_loop_plan_bytes(hb._levels_of(loop), wl.B, wl.Hq, wl.Hkv, wl.d, 300, num_sms=152) == 0
+    assert hb.hp_cascade_loop_plan_bytes(hb._levels_of(cap), wl.B, wl.Hq, wl.Hkv, wl.d, 300, num_sms=152) > 0
+
+
+def test_e4m3_unique_bytes_and_quantiser():
+    """An E4M3 level stores one byte per element plus two f32 scales per
+    (page, KV head); the quantiser's scales map each slice's largest
+    magnitude to 448, and decoding its codes stays within half an E4M3 step."""
+    wl = W.make_config("llama3_8b", seed=0, B=8, prefix=64)
+    w8 = W.with_e4m3_levels(wl)
+    assert [lv.e4m3 for lv in w8.levels] == [False, True]
+    ps = wl.page_size
+    suf = wl.levels[-1].nodes.tolist()
+    toks = sum(n[2] for n in suf)
+    pages = sum((n[2] + ps - 1) // ps for n in suf)
+    assert w8.unique_kv_bytes() == 64 * wl.Hkv * wl.d * 4 + toks * wl.Hkv * wl.d * 2 + pages * wl.Hkv * 8
+    q8 = w8.q8
+    x = wl.k_pool.float()
+    amax = x.abs().amax(dim=(2, 3))
+    assert torch.allclose(q8.k_scale * 448.0, amax, rtol=1e-6)
+    dec = q8.k.view(torch.float8_e4m3fn).float() * q8.k_scale[:, :, None, None]
+    # relative step of E4M3 is 2^-3 in the normal range: error <= 2^-4 of the value's binade
+    err = (dec - x).abs()
+    assert (err <= x.abs() * 2.0 ** -4 + q8.k_scale[:, :, None, None] * 2.0 ** -10).all()

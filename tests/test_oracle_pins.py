@@ -322,6 +322,112 @@ def test_gqa_mapping_consecutive_heads():
     assert np.abs(O[0] - O[2]).max() > 1e-3
 
 
+# ------------------------------------------------ reduced-precision KV (E4M3)
+def test_e4m3_decoder_special_values():
+    """The E4M3 values that close forms fix: +-0, the smallest subnormal
+    2^-9, the largest subnormal 7 * 2^-9, the smallest normal 2^-6, 1, 1.875,
+    2, the largest finite value 448 (S.1111.110) and the two NaN codes
+    (S.1111.111); there are no infinities."""
+    table = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3F: 1.875,
+             0x40: 2.0, 0x7E: 448.0, 0x80: -0.0, 0x81: -(2.0 ** -9), 0xB8: -1.0, 0xFE: -448.0}
+    got = oracle.e4m3_decode(np.array(sorted(table), dtype=np.uint8))
+    for (c, want), g in zip(sorted(table.items()), got):
+        assert g == want, (hex(c), g, want)
+    assert np.signbit(oracle.e4m3_decode(np.array([0x80], dtype=np.uint8))[0])
+    nan = oracle.e4m3_decode(np.array([0x7F, 0xFF], dtype=np.uint8))
+    assert np.isnan(nan).all()
+    allv = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert np.isfinite(allv).sum() == 254 and not np.isinf(allv).any()
+
+
+def test_e4m3_decoder_is_monotone_symmetric_and_matches_torch():
+    """Codes 0x00..0x7E decode to strictly increasing values (each step one
+    unit in the last place of the lower code's binade: 2^-9 through the
+    subnormals and the first binade, 2^(e-10) in binade e), the sign bit
+    negates, and every code agrees with torch's independent float8_e4m3fn
+    decoding."""
+    pos = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    steps = np.diff(pos)
+    assert (steps > 0).all()
+    for c in range(1, 0x7F):
+        e = max((c - 1) >> 3, 1)
+        assert steps[c - 1] == 2.0 ** (e - 10), hex(c)
+    neg = oracle.e4m3_decode((np.arange(0x7F) | 0x80).astype(np.uint8))
+    np.testing.assert_array_equal(neg, -pos)
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = oracle.e4m3_decode(codes)
+    ok = np.isfinite(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+    assert np.isnan(got[~ok]).all()
+
+
+def _e4m3_pow2_workload(seed):
+    """A tree whose last level reads E4M3 pools with power-of-two scales
+    that differ per page, per KV head and between K and V, next to bf16
+    pools holding the same values (code value x scale is exact in bf16:
+    4 significant bits, exponents within range)."""
+    wl = W.build_cascade("q8", B=5, Hq=4, Hkv=2, d=16, page_size=4, shared=[[(0, 5, 7)], [(0, 2, 5), (2, 5, 3)]],
+                         suffix_range=(0, 9), seed=seed)
+    g = torch.Generator().manual_seed(seed + 11)
+    P = wl.num_pages
+    shape = (P, wl.Hkv, wl.page_size, wl.d)
+    # finite codes only (not S.1111.111)
+    k8 = torch.randint(0, 254, shape, generator=g, dtype=torch.int32)
+    v8 = torch.randint(0, 254, shape, generator=g, dtype=torch.int32)
+    k8 = torch.where(k8 >= 0x7F, k8 + 1, k8).to(torch.uint8)
+    v8 = torch.where(v8 >= 0x7F, v8 + 1, v8).to(torch.uint8)
+    ks = torch.pow(2.0, torch.randint(-3, 4, (P, wl.Hkv), generator=g).double()).float()
+    vs = torch.pow(2.0, torch.randint(-3, 4, (P, wl.Hkv), generator=g).double()).float()
+    w8 = W.with_e4m3_levels(wl, levels=(-1,))
+    w8.q8 = W.E4M3Pools(k8, v8, ks, vs)
+    kd = (k8.view(torch.float8_e4m3fn).double() * ks.double()[:, :, None, None]).to(torch.bfloat16)
+    vd = (v8.view(torch.float8_e4m3fn).double() * vs.double()[:, :, None, None]).to(torch.bfloat16)
+    assert torch.equal(kd.double(), k8.view(torch.float8_e4m3fn).double() * ks.double()[:, :, None, None])
+    # the bf16 twin: shared levels keep wl's pools, the last level the decoded values
+    twin = W.build_cascade("q8", B=5, Hq=4, Hkv=2, d=16, page_size=4,
+                           shared=[[(0, 5, 7)], [(0, 2, 5), (2, 5, 3)]], suffix_range=(0, 9), seed=seed)
+    last = set(twin.levels[-1].page_ids.tolist())
+    shared = set(p for lv in twin.levels[:-1] for p in lv.page_ids.tolist())
+    assert not (last & shared)
+    for p in last:
+        twin.k_pool[p] = kd[p]
+        twin.v_pool[p] = vd[p]
+    return w8, twin
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_e4m3_levels_equal_their_decoded_bf16_twin(seed):
+    """Cascade over a tree whose suffix level is stored as E4M3 codes and
+    per-(page, KV head) scales equals the cascade over bf16 pools holding the
+    decoded values (1e-12): pins which scale a key takes (its page, its KV
+    head, K's or V's) and that only the marked level is decoded."""
+    w8, twin = _e4m3_pow2_workload(seed)
+    O8, L8 = oracle.cascade(w8)
+    O, L = oracle.cascade(twin)
+    np.testing.assert_allclose(O8, O, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(L8, L, atol=1e-12, rtol=0)
+
+
+def test_e4m3_paged_decode_equals_decoded_bf16():
+    """The per-sequence paged decode over E4M3 pools equals the bf16 paged
+    decode over the decoded values (1e-12)."""
+    own = W.build_cascade("q8s", B=5, Hq=4, Hkv=2, d=16, page_size=4, shared=[], suffix_range=(0, 9), seed=9)
+    g = torch.Generator().manual_seed(5)
+    P = own.num_pages
+    k8 = torch.randint(0, 0x7F, (P, 2, 4, 16), generator=g, dtype=torch.int32).to(torch.uint8)
+    v8 = torch.randint(0x80, 0xFF, (P, 2, 4, 16), generator=g, dtype=torch.int32).to(torch.uint8)
+    ks = torch.pow(2.0, torch.randint(-2, 3, (P, 2), generator=g).double()).float()
+    vs = torch.pow(2.0, torch.randint(-2, 3, (P, 2), generator=g).double()).float()
+    kd = (k8.view(torch.float8_e4m3fn).double() * ks.double()[:, :, None, None]).to(torch.bfloat16)
+    vd = (v8.view(torch.float8_e4m3fn).double() * vs.double()[:, :, None, None]).to(torch.bfloat16)
+    pt, sl = W.full_page_tables(own)
+    O8, L8 = oracle.paged_decode_e4m3(own.q, k8, v8, ks, vs, pt, sl, own.scale)
+    O, L = oracle.paged_decode(own.q, kd, vd, pt, sl, own.scale)
+    np.testing.assert_allclose(O8, O, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(L8, L, atol=1e-12, rtol=0)
+
+
 # ------------------------------------------- planted mistakes must be caught
 _PINS = [
     test_single_key_returns_its_value,
@@ -336,6 +442,10 @@ _PINS = [
     test_paged_decode_and_prefix_agree_with_cascade,
     test_probe_output_is_the_code_row,
     test_gqa_mapping_consecutive_heads,
+    test_e4m3_decoder_special_values,
+    test_e4m3_decoder_is_monotone_symmetric_and_matches_torch,
+    lambda: test_e4m3_levels_equal_their_decoded_bf16_twin(0),
+    test_e4m3_paged_decode_equals_decoded_bf16,
 ]
 
 _MUTANTS = {
@@ -347,6 +457,12 @@ _MUTANTS = {
     "slot_reversed": ("long slot = t % L->page_size;",
                       "long slot = L->page_size - 1 - t % L->page_size;"),
     "reduce_wrong_factor": ("O[i] = x * o_c[i] + y * O[i];", "O[i] = y * o_c[i] + x * O[i];"),
+    "e4m3_bias": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3_subnormal": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
+    "e4m3_kv_scales_swapped": ("keys[n].k_scale = k_scales[l][page * Hkv + kvh];",
+                               "keys[n].k_scale = v_scales[l][page * Hkv + kvh];"),
+    "e4m3_scale_head_ignored": ("keys[n].v_scale = v_scales[l][page * Hkv + kvh];",
+                                "keys[n].v_scale = v_scales[l][page * Hkv];"),
 }
 
 
