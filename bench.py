@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--config", default="llama3_8b")
     ap.add_argument("--part", choices=["all", "prefix", "suffix"], default="all",
                     help="time the whole step, or its shared levels / private suffixes alone")
+    ap.add_argument("--e4m3", action="store_true",
+                    help="the levels of the per-sequence pass (private suffixes) read E4M3 copies of the pools")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: enough for 3x L2)")
     ap.add_argument("--graph-max", type=int, default=256, help="most steps captured in one CUDA graph")
     ap.add_argument("--min-timed-s", type=float, default=1.0,
@@ -268,6 +270,19 @@ def whole_job_tbs(world: int, bytes_per_step: float, us_step: float) -> float:
     return world * bytes_per_step / (us_step * 1e-6) / 1e12
 
 
+def plan_summary(hb, s) -> dict:
+    """Work items of a set's plan and how the persistent grid is split
+    between the two roles (host-side listing of the same plan)."""
+    info = s["plan"].info
+    wl = s["wl"]
+    items = hb.hp_cascade_plan_items(hb._levels_of(wl), wl.B, wl.Hq, wl.Hkv, wl.d, num_sms=info.grid)
+    tc_ctas = {it["cta"] for it in items if it["tc"]}
+    sm_ctas = {it["cta"] for it in items if not it["tc"]}
+    return {"tc_items": info.n_tc_items, "small_items": info.n_small_items, "grid": info.grid,
+            "part_rows": info.n_part_rows, "tc_ctas": len(tc_ctas), "paged_ctas": len(sm_ctas),
+            "ctas_with_both": len(tc_ctas & sm_ctas)}
+
+
 # ------------------------------------------------------------ graph timing
 class StepGraphs:
     """CUDA graphs of consecutive steps over `items` in rotation order (step i
@@ -433,7 +448,7 @@ def main():
             raise RuntimeError(f"device status {hb.status_str(st)}")
 
     # ---------------------------------------------------------- inputs
-    sets, ws_shared, l2_note = make_sets(args.config, args.part, 1000 * rank, args.sets)
+    sets, ws_shared, l2_note = make_sets(args.config, args.part, 1000 * rank, args.sets, e4m3=args.e4m3)
     R = len(sets)
     wl0 = sets[0]["wl"]
     info = sets[0]["plan"].info
@@ -783,8 +798,7 @@ def main():
             "decode_loop": loop,
             "extras": extras,
             "parity_spot": parity,
-            "plan": {"tc_items": info.n_tc_items, "small_items": info.n_small_items, "grid": info.grid,
-                     "part_rows": info.n_part_rows},
+            "plan": plan_summary(hb, sets[0]),
             "device": props.name,
         }
         print(json.dumps(line), flush=True)

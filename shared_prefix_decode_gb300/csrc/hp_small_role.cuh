@@ -32,17 +32,12 @@
 // pass is memory-bound and quantising its KV cache halves its bytes).  A
 // stage holds the 16-token chunk's codes (one box of 16 tokens x 128 bytes x
 // nh heads per K and per V) and the chunk's scales, which the producer copies
-// with cp.async tracked by the stage's barrier.  The consumers convert codes
-// to f16 in registers (exact) and use the f16 MMA: the queries are rounded
-// from bf16 to f16 once per item (exact for |q| in f16's normal range),
-// scores are scaled by the chunk's K scale, and P is multiplied by the V
-// scale before it is rounded to f16 for P V.  For S = Q K^T each thread reads
-// its 32-byte slice of a key row with two 16-byte loads and uses byte 4i..4i+3
-// at k-step i: the head dimension is visited in a permuted order, the same
-// for Q and K, so the dot product is unchanged.  For P V each thread reads
-// 16 consecutive columns of four key rows and pairs the bytes of two rows per
-// B register; the output columns come out in a matching permuted order that
-// the epilogue undoes (each thread ends with 32 consecutive columns).
+// with cp.async tracked by the stage's barrier.  The consumers decode codes
+// to f16 in registers with integer bit operations (exact, up to a power of
+// two) and use the f16 MMA: the queries are rounded from bf16 to f16 once per
+// item (exact for |q| in f16's normal range), scores are scaled by the
+// chunk's K scale, and P is weighted by the chunk's V scale before it is
+// rounded to f16 for P V.  The fragment layouts are in consumer_q8.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -460,12 +455,36 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
     }
 }
 
+// Four E4M3 codes (one 32-bit word, bytes b0..b3) -> two f16 pairs holding
+// the codes' values times 2^-8, exactly: lo = (b0, b2), hi = (b1, b3), the
+// first byte of each pair in the low half.  Each byte's sign stays on top of
+// its 16-bit half and its 7 other bits move to bits 7..13: the 4 exponent
+// bits land in f16's exponent field (f16's bias 15 against E4M3's 7: the
+// factor 2^-8) and the 3 mantissa bits on top of f16's mantissa; subnormal
+// codes (exponent 0) land on f16 subnormals with the same factor.  Integer
+// ALU operations only.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t &lo, uint32_t &hi)
+{
+    hi = (x & 0x80008000u) | ((x >> 1) & 0x3F803F80u);
+    lo = ((x << 8) & 0x80008000u) | ((x << 7) & 0x3F803F80u);
+}
+
 // E4M3 consumer warp w (0 <= w < nh), d = 128: as `consumer`, with codes
-// converted to f16 in registers.  The running output o' is kept in units of
-// the V scale of the latest chunk (vcur); when the next chunk's V scale
-// differs, o' is rescaled by vcur / vsc, folded into the softmax rescale, so
-// P stays in [0, 1] when it is rounded to f16.  A chunk whose V scale is 0
-// adds nothing to O (its weights still count in the denominator).
+// decoded to f16 in registers (values x 2^-8; the factor 2^8 is put back
+// into the K scale of the scores and into the final normalisation).
+//   - S = Q K^T: k-step i of thread (g, t) takes bytes 32t+4i .. 32t+4i+3 of
+//     its key rows; its two B registers pair bytes (0, 2) and (1, 3), and the
+//     query fragments pair the same columns, so the head dimension is summed
+//     in a permuted order (the same for Q and K).  Even and odd k-steps
+//     accumulate separately (two independent MMA chains per tile).
+//   - O' = P V: thread (g, t) reads columns 16g .. 16g+15 of key rows 2t,
+//     2t+1, 2t+8 and 2t+9; n8 tile j takes column 16g + j as its column g, so
+//     thread (g, t) ends with columns 32t .. 32t+31 of its rows.
+//   - The V scale of a chunk enters as P * (vsc / vref), vref being the first
+//     nonzero V scale of the item, so P stays near [0, 1] when it is rounded
+//     to f16 and O' needs no rescaling between chunks; O = O' vref 2^8 / l.
+//     A chunk whose V scale is 0 adds nothing to O (its weights still count
+//     in the denominator).
 template <int D, int NC, int S, int QR>
 __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, int lane)
 {
@@ -473,12 +492,13 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
     static_assert(D == 128, "E4M3 pools: d = 128");
     constexpr int kKs = D / 16;  // k-steps of the S MMA
     constexpr int kNt = D / 8;   // n8 tiles of O
+    constexpr float kDecode = 256.f;  // decoded code = value * 2^-8
     auto wait_warp = [&](uint32_t b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
     };
     uint32_t qa[kKs][4];
     float o[kNt][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, vcur = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, vref = 0.f;
     const int g = lane >> 2, t = lane & 3;
     const int r0 = g, r1 = g + 8;
     const uint32_t hoff = (uint32_t)w * L::kHeadBox;  // this warp's head within a box
@@ -493,8 +513,8 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
         const int kvh = m.kvh0 + w;
         const uint32_t stage = c.sbase + st * L::kStage;
         if (m.first) {
-            // query rows r0 / r1 of head w as f16: k-step i takes columns
-            // 32t + 4i .. 32t + 4i + 3 (a0/a1: the first pair, a2/a3: the second)
+            // query rows r0 / r1 of head w as f16: k-step i pairs columns
+            // (32t+4i, 32t+4i+2) in a0/a1 and (32t+4i+1, 32t+4i+3) in a2/a3
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 const int r = rr ? r1 : r0;
@@ -518,10 +538,10 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
                 }
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    qa[2 * cc][rr] = pack_f16x2(bf16lo_to_f32(x[cc].x), bf16hi_to_f32(x[cc].x));
-                    qa[2 * cc][2 + rr] = pack_f16x2(bf16lo_to_f32(x[cc].y), bf16hi_to_f32(x[cc].y));
-                    qa[2 * cc + 1][rr] = pack_f16x2(bf16lo_to_f32(x[cc].z), bf16hi_to_f32(x[cc].z));
-                    qa[2 * cc + 1][2 + rr] = pack_f16x2(bf16lo_to_f32(x[cc].w), bf16hi_to_f32(x[cc].w));
+                    qa[2 * cc][rr] = pack_f16x2(bf16lo_to_f32(x[cc].x), bf16lo_to_f32(x[cc].y));
+                    qa[2 * cc][2 + rr] = pack_f16x2(bf16hi_to_f32(x[cc].x), bf16hi_to_f32(x[cc].y));
+                    qa[2 * cc + 1][rr] = pack_f16x2(bf16lo_to_f32(x[cc].z), bf16lo_to_f32(x[cc].w));
+                    qa[2 * cc + 1][2 + rr] = pack_f16x2(bf16hi_to_f32(x[cc].z), bf16hi_to_f32(x[cc].w));
                 }
             }
 #pragma unroll
@@ -529,7 +549,7 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
                 o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
-            vcur = 0.f;
+            vref = 0.f;
         }
         const uint32_t kst = stage + hoff;
         const uint32_t vst = stage + L::kChunk + hoff;
@@ -547,10 +567,10 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
             __syncwarp();
         }
 
-        // S = Q K^T over 16 keys: n8 tile 0 = keys 0-7, tile 1 = keys 8-15;
-        // thread (g, t) reads bytes 32t .. 32t+31 of key rows g and g + 8
+        // S = Q K^T over 16 keys: n8 tile 0 = keys 0-7, tile 1 = keys 8-15
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
         {
+            float s0b[4] = {0.f, 0.f, 0.f, 0.f}, s1b[4] = {0.f, 0.f, 0.f, 0.f};
             const uint4 ka = ld_shared_v4(kst + r0 * 128 + (((2 * t) ^ (r0 & 7)) << 4));
             const uint4 kb = ld_shared_v4(kst + r0 * 128 + (((2 * t + 1) ^ (r0 & 7)) << 4));
             const uint4 kc = ld_shared_v4(kst + r1 * 128 + (((2 * t) ^ (r1 & 7)) << 4));
@@ -559,13 +579,21 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
             const uint32_t w1[8] = {kc.x, kc.y, kc.z, kc.w, kd.x, kd.y, kd.z, kd.w};
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
-                mma_f16_16816(s0, qa[ks], e4m3x2_to_f16x2(w0[ks]), e4m3x2_to_f16x2(w0[ks] >> 16));
-                mma_f16_16816(s1, qa[ks], e4m3x2_to_f16x2(w1[ks]), e4m3x2_to_f16x2(w1[ks] >> 16));
+                uint32_t b0, b1, c0, c1;
+                e4m3x4_to_f16(w0[ks], b0, b1);
+                e4m3x4_to_f16(w1[ks], c0, c1);
+                mma_f16_16816((ks & 1) ? s0b : s0, qa[ks], b0, b1);
+                mma_f16_16816((ks & 1) ? s1b : s1, qa[ks], c0, c1);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s0[e] += s0b[e];
+                s1[e] += s1b[e];
             }
         }
         // online softmax (rows r0: elements 0,1; rows r1: elements 2,3); the
-        // chunk's K scale multiplies the scores
-        const float cs = a.scale_log2 * ksc;
+        // chunk's K scale (and the decoding factor) multiplies the scores
+        const float cs = a.scale_log2 * ksc * kDecode;
         const int tq = 2 * t;
         float x[2][4];
 #pragma unroll
@@ -586,23 +614,20 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
         const float a0 = fast_exp2(m0 - ms0), a1 = fast_exp2(m1 - ms1);
         m0 = mn0;
         m1 = mn1;
-        // o' follows the V scale of this chunk (a chunk with scale 0 adds nothing)
-        const bool vuse = vsc != 0.f;
-        const float vr = (vuse && vcur != 0.f) ? vcur / vsc : 1.f;
-        if (vuse)
-            vcur = vsc;
-        const float f0 = a0 * vr, f1 = a1 * vr;
-        if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
+        if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
             for (int n = 0; n < kNt; ++n) {
-                o[n][0] *= f0;
-                o[n][1] *= f0;
-                o[n][2] *= f1;
-                o[n][3] *= f1;
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
             }
+            l0 *= a0;
+            l1 *= a1;
         }
-        l0 *= a0;
-        l1 *= a1;
+        if (vref == 0.f)
+            vref = vsc;
+        const float pv = vref != 0.f ? vsc / vref : 0.f;  // 0: the chunk adds nothing to O
         float p[2][4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -612,14 +637,12 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
         l0 += p[0][0] + p[0][1] + p[1][0] + p[1][1];
         l1 += p[0][2] + p[0][3] + p[1][2] + p[1][3];
         uint32_t pa[4];
-        const float pz = vuse ? 1.f : 0.f;
-        pa[0] = pack_f16x2(p[0][0] * pz, p[0][1] * pz);
-        pa[1] = pack_f16x2(p[0][2] * pz, p[0][3] * pz);
-        pa[2] = pack_f16x2(p[1][0] * pz, p[1][1] * pz);
-        pa[3] = pack_f16x2(p[1][2] * pz, p[1][3] * pz);
+        pa[0] = pack_f16x2(p[0][0] * pv, p[0][1] * pv);
+        pa[1] = pack_f16x2(p[0][2] * pv, p[0][3] * pv);
+        pa[2] = pack_f16x2(p[1][0] * pv, p[1][1] * pv);
+        pa[3] = pack_f16x2(p[1][2] * pv, p[1][3] * pv);
 
-        // O' += P V: thread (g, t) reads columns 16g .. 16g+15 of key rows 2t,
-        // 2t+1, 2t+8, 2t+9; n8 tile j takes column 16g + j as its column g
+        // O' += P V
         {
             const int ta = 2 * t, tb = 2 * t + 1;
             const uint4 va = ld_shared_v4(vst + ta * 128 + ((g ^ (ta & 7)) << 4));
@@ -630,13 +653,15 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
             const uint32_t C[4] = {vc.x, vc.y, vc.z, vc.w}, E[4] = {vd.x, vd.y, vd.z, vd.w};
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                // byte pairs (row 2t, row 2t+1) and (row 2t+8, row 2t+9) of columns 4q4 .. 4q4+3
-                const uint32_t lo01 = __byte_perm(A[q4], B[q4], 0x5140), hi01 = __byte_perm(A[q4], B[q4], 0x7362);
-                const uint32_t lo89 = __byte_perm(C[q4], E[q4], 0x5140), hi89 = __byte_perm(C[q4], E[q4], 0x7362);
-                mma_f16_16816(o[4 * q4 + 0], pa, e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo89));
-                mma_f16_16816(o[4 * q4 + 1], pa, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(lo89 >> 16));
-                mma_f16_16816(o[4 * q4 + 2], pa, e4m3x2_to_f16x2(hi01), e4m3x2_to_f16x2(hi89));
-                mma_f16_16816(o[4 * q4 + 3], pa, e4m3x2_to_f16x2(hi01 >> 16), e4m3x2_to_f16x2(hi89 >> 16));
+                // bytes (row 2t: c, c+1; row 2t+1: c, c+1) of columns c = 4q4, 4q4 + 2
+                uint32_t b0[4], b1[4];
+                e4m3x4_to_f16(__byte_perm(A[q4], B[q4], 0x5410), b0[0], b0[1]);
+                e4m3x4_to_f16(__byte_perm(A[q4], B[q4], 0x7632), b0[2], b0[3]);
+                e4m3x4_to_f16(__byte_perm(C[q4], E[q4], 0x5410), b1[0], b1[1]);
+                e4m3x4_to_f16(__byte_perm(C[q4], E[q4], 0x7632), b1[2], b1[3]);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    mma_f16_16816(o[4 * q4 + cc], pa, b0[cc], b1[cc]);
             }
         }
         // release the stage to the producer
@@ -649,8 +674,8 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
             L0 += __shfl_xor_sync(0xffffffffu, L0, 2);
             float L1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
             L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
-            const float inv0 = L0 > 0.f ? vcur / L0 : 0.f;
-            const float inv1 = L1 > 0.f ? vcur / L1 : 0.f;
+            const float inv0 = L0 > 0.f ? vref * kDecode / L0 : 0.f;
+            const float inv1 = L1 > 0.f ? vref * kDecode / L1 : 0.f;
             const int base = m.part_row + w * rows;  // this head's rows
             // o[j][0|2]: column 32t + j, o[j][1|3]: column 32t + 16 + j
 #pragma unroll
