@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--config", default="llama3_8b")
     ap.add_argument("--part", choices=["all", "prefix", "suffix"], default="all",
                     help="time the whole step, or its shared levels / private suffixes alone")
+    ap.add_argument("--B", type=int, default=0, help="batch override (a smaller variant of the workload)")
+    ap.add_argument("--prefix", type=int, default=-1, help="first-level prefix override")
     ap.add_argument("--e4m3", action="store_true",
                     help="the levels of the per-sequence pass (private suffixes) read E4M3 copies of the pools")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: enough for 3x L2)")
@@ -414,7 +416,12 @@ def main():
         shared by all.  e4m3: the levels of the per-sequence pass read E4M3
         copies of the pools."""
         def gen(seed):
-            wl = make_config(name, seed=seed, part=part, device=device)
+            kw = {}
+            if name == args.config and args.B > 0:
+                kw["B"] = args.B
+            if name == args.config and args.prefix >= 0:
+                kw["prefix"] = args.prefix
+            wl = make_config(name, seed=seed, part=part, device=device, **kw)
             return with_e4m3_levels(wl) if e4m3 else wl
 
         first = gen(seed0)

@@ -102,7 +102,11 @@ double schedule(HostPlan &P, int grid, int n_tc_ctas, bool mixed, int d, const C
         const int nh = P.hdr.small_nh;
         for (size_t j = 0; j < P.small.size(); ++j) {
             const WorkItem &w = P.small[j];
-            P.jobs_sm.push_back({cm.small(w, d, nh, P.level_kv[w.level] == HP_KV_E4M3 ? 2 : 4), (int32_t)j, false,
+            // an E4M3 chunk is half the bytes, but decoding its codes costs the
+            // consumers about as long as a bf16 chunk takes to stream (ncu:
+            // the E4M3 role executes twice the instructions per key):
+            // modelled at the bf16 rate per key
+            P.jobs_sm.push_back({cm.small(w, d, nh, 4), (int32_t)j, false,
                                  (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
         }
         P.jobs_all = P.jobs_tc;

@@ -471,15 +471,23 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t &lo, uint32_t
 
 // E4M3 consumer warp w (0 <= w < nh), d = 128: as `consumer`, with codes
 // decoded to f16 in registers (values x 2^-8; the factor 2^8 is put back
-// into the K scale of the scores and into the final normalisation).
-//   - S = Q K^T: k-step i of thread (g, t) takes bytes 32t+4i .. 32t+4i+3 of
-//     its key rows; its two B registers pair bytes (0, 2) and (1, 3), and the
-//     query fragments pair the same columns, so the head dimension is summed
-//     in a permuted order (the same for Q and K).  Even and odd k-steps
-//     accumulate separately (two independent MMA chains per tile).
-//   - O' = P V: thread (g, t) reads columns 16g .. 16g+15 of key rows 2t,
-//     2t+1, 2t+8 and 2t+9; n8 tile j takes column 16g + j as its column g, so
-//     thread (g, t) ends with columns 32t .. 32t+31 of its rows.
+// into the K scale of the scores and into the final normalisation) and the
+// operands of both products swapped so that the keys fill the MMA's 16 rows
+// and the head's query rows its 8 columns: with up to 8 query rows (G <= 8,
+// one sequence) a chunk costs 16 MMAs instead of 32; 9..16 rows take a
+// second column tile.
+//   - S^T = K Q^T: k-step i of thread (g, t) takes bytes 32t+4i .. 32t+4i+3
+//     of key rows g and g+8; its A registers pair bytes (0, 2) and (1, 3),
+//     and the query fragments (B) pair the same columns, so the head
+//     dimension is summed in a permuted order (the same for Q and K).  Even
+//     and odd k-steps accumulate separately (independent MMA chains).
+//   - The scores of a query are spread over the 8 lanes of one t (keys g and
+//     g + 8 each): maxima and sums are warp reductions over those lanes.
+//   - O'^T = V^T P^T: P^T's B fragments are the f16 score tiles transposed
+//     with movmatrix; V^T's A fragments pair the codes of keys (2t, 2t+1)
+//     and (2t+8, 2t+9) of thread (g, t)'s columns 16g .. 16g+15, m-tile j
+//     taking columns 16g + 2j and 16g + 2j + 1, so thread (g, t) ends with
+//     columns 16g .. 16g+15 of query rows 2t and 2t+1 (of each column tile).
 //   - The V scale of a chunk enters as P * (vsc / vref), vref being the first
 //     nonzero V scale of the item, so P stays near [0, 1] when it is rounded
 //     to f16 and O' needs no rescaling between chunks; O = O' vref 2^8 / l.
@@ -490,18 +498,22 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
 {
     using L = Layout<D, NC, S, QR, true>;
     static_assert(D == 128, "E4M3 pools: d = 128");
-    constexpr int kKs = D / 16;  // k-steps of the S MMA
-    constexpr int kNt = D / 8;   // n8 tiles of O
+    constexpr int kKs = D / 16;  // k-steps of S^T = K Q^T
+    constexpr int kMt = D / 16;  // m16 tiles of O^T
     constexpr float kDecode = 256.f;  // decoded code = value * 2^-8
     auto wait_warp = [&](uint32_t b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
     };
-    uint32_t qa[kKs][4];
-    float o[kNt][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, vref = 0.f;
+    // qb[ks][nt][0|1]: query rows nt*8 + g, column pairs (32t+4ks, +2) / (+1, +3)
+    uint32_t qb[kKs][2][2];
+    float o[kMt][2][4];
+    // per column tile: running max and sum of query rows nt*8 + 2t, + 1
+    float mq[2][2], lq[2][2];
+    float vref = 0.f;
     const int g = lane >> 2, t = lane & 3;
-    const int r0 = g, r1 = g + 8;
     const uint32_t hoff = (uint32_t)w * L::kHeadBox;  // this warp's head within a box
+    int rows = 0;
+    bool two = false;  // a second column tile (9..16 query rows)
     for (uint32_t k = 0;; ++k) {
         const uint32_t st = k % S;
         if (!wait_warp(c.full0 + 8 * st, (k / S) & 1u))
@@ -509,15 +521,14 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
         const StageMeta m = c.meta[st];
         if (m.n_seq < 0)
             break;  // sentinel: the producer's walk is over
-        const int rows = m.n_seq * a.G;
         const int kvh = m.kvh0 + w;
         const uint32_t stage = c.sbase + st * L::kStage;
         if (m.first) {
-            // query rows r0 / r1 of head w as f16: k-step i pairs columns
-            // (32t+4i, 32t+4i+2) in a0/a1 and (32t+4i+1, 32t+4i+3) in a2/a3
+            rows = m.n_seq * a.G;
+            two = rows > 8;
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int r = rr ? r1 : r0;
+            for (int nt = 0; nt < 2; ++nt) {
+                const int r = nt * 8 + g;
                 uint4 x[4];
                 if (r < rows && m.qslot) {
                     const int srow = w * a.G + r;
@@ -538,17 +549,20 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
                 }
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    qa[2 * cc][rr] = pack_f16x2(bf16lo_to_f32(x[cc].x), bf16lo_to_f32(x[cc].y));
-                    qa[2 * cc][2 + rr] = pack_f16x2(bf16hi_to_f32(x[cc].x), bf16hi_to_f32(x[cc].y));
-                    qa[2 * cc + 1][rr] = pack_f16x2(bf16lo_to_f32(x[cc].z), bf16lo_to_f32(x[cc].w));
-                    qa[2 * cc + 1][2 + rr] = pack_f16x2(bf16hi_to_f32(x[cc].z), bf16hi_to_f32(x[cc].w));
+                    qb[2 * cc][nt][0] = pack_f16x2(bf16lo_to_f32(x[cc].x), bf16lo_to_f32(x[cc].y));
+                    qb[2 * cc][nt][1] = pack_f16x2(bf16hi_to_f32(x[cc].x), bf16hi_to_f32(x[cc].y));
+                    qb[2 * cc + 1][nt][0] = pack_f16x2(bf16lo_to_f32(x[cc].z), bf16lo_to_f32(x[cc].w));
+                    qb[2 * cc + 1][nt][1] = pack_f16x2(bf16hi_to_f32(x[cc].z), bf16hi_to_f32(x[cc].w));
                 }
             }
 #pragma unroll
-            for (int n = 0; n < kNt; ++n)
-                o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
+            for (int j = 0; j < kMt; ++j)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+                    o[j][nt][0] = o[j][nt][1] = o[j][nt][2] = o[j][nt][3] = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+                mq[nt][0] = mq[nt][1] = -INFINITY, lq[nt][0] = lq[nt][1] = 0.f;
             vref = 0.f;
         }
         const uint32_t kst = stage + hoff;
@@ -567,82 +581,92 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
             __syncwarp();
         }
 
-        // S = Q K^T over 16 keys: n8 tile 0 = keys 0-7, tile 1 = keys 8-15
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T = K Q^T: rows = keys (g, g + 8), columns = query rows 2t, 2t+1
+        float sc[2][4];
         {
-            float s0b[4] = {0.f, 0.f, 0.f, 0.f}, s1b[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint4 ka = ld_shared_v4(kst + r0 * 128 + (((2 * t) ^ (r0 & 7)) << 4));
-            const uint4 kb = ld_shared_v4(kst + r0 * 128 + (((2 * t + 1) ^ (r0 & 7)) << 4));
-            const uint4 kc = ld_shared_v4(kst + r1 * 128 + (((2 * t) ^ (r1 & 7)) << 4));
-            const uint4 kd = ld_shared_v4(kst + r1 * 128 + (((2 * t + 1) ^ (r1 & 7)) << 4));
+            const int k0r = g, k1r = g + 8;
+            const uint4 ka = ld_shared_v4(kst + k0r * 128 + (((2 * t) ^ (k0r & 7)) << 4));
+            const uint4 kb = ld_shared_v4(kst + k0r * 128 + (((2 * t + 1) ^ (k0r & 7)) << 4));
+            const uint4 kc = ld_shared_v4(kst + k1r * 128 + (((2 * t) ^ (k1r & 7)) << 4));
+            const uint4 kd = ld_shared_v4(kst + k1r * 128 + (((2 * t + 1) ^ (k1r & 7)) << 4));
             const uint32_t w0[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
             const uint32_t w1[8] = {kc.x, kc.y, kc.z, kc.w, kd.x, kd.y, kd.z, kd.w};
+            float sb[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    sc[nt][e] = sb[nt][e] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
-                uint32_t b0, b1, c0, c1;
-                e4m3x4_to_f16(w0[ks], b0, b1);
-                e4m3x4_to_f16(w1[ks], c0, c1);
-                mma_f16_16816((ks & 1) ? s0b : s0, qa[ks], b0, b1);
-                mma_f16_16816((ks & 1) ? s1b : s1, qa[ks], c0, c1);
+                uint32_t ak[4];
+                e4m3x4_to_f16(w0[ks], ak[0], ak[2]);
+                e4m3x4_to_f16(w1[ks], ak[1], ak[3]);
+                mma_f16_16816((ks & 1) ? sb[0] : sc[0], ak, qb[ks][0][0], qb[ks][0][1]);
+                if (two)
+                    mma_f16_16816((ks & 1) ? sb[1] : sc[1], ak, qb[ks][1][0], qb[ks][1][1]);
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                s0[e] += s0b[e];
-                s1[e] += s1b[e];
-            }
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    sc[nt][e] += sb[nt][e];
         }
-        // online softmax (rows r0: elements 0,1; rows r1: elements 2,3); the
-        // chunk's K scale (and the decoding factor) multiplies the scores
+        // online softmax per query column: element e of tile nt is key
+        // (e < 2 ? g : g + 8), query row nt*8 + 2t + (e & 1); the chunk's K
+        // scale (and the decoding factor) multiplies the scores
         const float cs = a.scale_log2 * ksc * kDecode;
-        const int tq = 2 * t;
-        float x[2][4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int tk = tq + (e & 1);
-            x[0][e] = tk < nvalid ? s0[e] * cs : -INFINITY;
-            x[1][e] = tk + 8 < nvalid ? s1[e] * cs : -INFINITY;
-        }
-        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;  // all keys so far masked: nothing to scale
-        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float a0 = fast_exp2(m0 - ms0), a1 = fast_exp2(m1 - ms1);
-        m0 = mn0;
-        m1 = mn1;
-        if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
-#pragma unroll
-            for (int n = 0; n < kNt; ++n) {
-                o[n][0] *= a0;
-                o[n][1] *= a0;
-                o[n][2] *= a1;
-                o[n][3] *= a1;
-            }
-            l0 *= a0;
-            l1 *= a1;
-        }
         if (vref == 0.f)
             vref = vsc;
         const float pv = vref != 0.f ? vsc / vref : 0.f;  // 0: the chunk adds nothing to O
-        float p[2][4];
+        uint32_t pb[2][2];  // P^T fragments of each column tile (keys 0-7, 8-15)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            p[0][e] = fast_exp2(x[0][e] - ((e & 2) ? ms1 : ms0));
-            p[1][e] = fast_exp2(x[1][e] - ((e & 2) ? ms1 : ms0));
+        for (int nt = 0; nt < 2; ++nt) {
+            if (nt == 1 && !two)
+                break;
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = e < 2 ? g : g + 8;
+                x[e] = key < nvalid ? sc[nt][e] * cs : -INFINITY;
+            }
+            float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+            }
+            float al[2], ms[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float mn = fmaxf(mq[nt][i], mx[i]);
+                ms[i] = mn == -INFINITY ? 0.f : mn;  // all keys so far masked: nothing to scale
+                al[i] = fast_exp2(mq[nt][i] - ms[i]);
+                mq[nt][i] = mn;
+                lq[nt][i] *= al[i];
+            }
+            if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+#pragma unroll
+                for (int j = 0; j < kMt; ++j) {
+                    o[j][nt][0] *= al[0];
+                    o[j][nt][2] *= al[0];
+                    o[j][nt][1] *= al[1];
+                    o[j][nt][3] *= al[1];
+                }
+            }
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                p[e] = fast_exp2(x[e] - ms[e & 1]);
+            lq[nt][0] += p[0] + p[2];
+            lq[nt][1] += p[1] + p[3];
+            // [keys g][queries 2t, 2t+1] per 8x8 block, transposed to
+            // [query g][keys 2t, 2t+1]: the B fragments of P^T
+            pb[nt][0] = movmatrix_trans(pack_f16x2(p[0] * pv, p[1] * pv));
+            pb[nt][1] = movmatrix_trans(pack_f16x2(p[2] * pv, p[3] * pv));
         }
-        l0 += p[0][0] + p[0][1] + p[1][0] + p[1][1];
-        l1 += p[0][2] + p[0][3] + p[1][2] + p[1][3];
-        uint32_t pa[4];
-        pa[0] = pack_f16x2(p[0][0] * pv, p[0][1] * pv);
-        pa[1] = pack_f16x2(p[0][2] * pv, p[0][3] * pv);
-        pa[2] = pack_f16x2(p[1][0] * pv, p[1][1] * pv);
-        pa[3] = pack_f16x2(p[1][2] * pv, p[1][3] * pv);
 
-        // O' += P V
+        // O'^T += V^T P^T
         {
             const int ta = 2 * t, tb = 2 * t + 1;
             const uint4 va = ld_shared_v4(vst + ta * 128 + ((g ^ (ta & 7)) << 4));
@@ -653,15 +677,18 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
             const uint32_t C[4] = {vc.x, vc.y, vc.z, vc.w}, E[4] = {vd.x, vd.y, vd.z, vd.w};
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                // bytes (row 2t: c, c+1; row 2t+1: c, c+1) of columns c = 4q4, 4q4 + 2
-                uint32_t b0[4], b1[4];
-                e4m3x4_to_f16(__byte_perm(A[q4], B[q4], 0x5410), b0[0], b0[1]);
-                e4m3x4_to_f16(__byte_perm(A[q4], B[q4], 0x7632), b0[2], b0[3]);
-                e4m3x4_to_f16(__byte_perm(C[q4], E[q4], 0x5410), b1[0], b1[1]);
-                e4m3x4_to_f16(__byte_perm(C[q4], E[q4], 0x7632), b1[2], b1[3]);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    mma_f16_16816(o[4 * q4 + cc], pa, b0[cc], b1[cc]);
+                // m-tiles 2q4 and 2q4+1: columns 16g + 4q4 + (0, 1) and (2, 3)
+                uint32_t a0[4], a1[4];
+                e4m3x4_to_f16(__byte_perm(A[q4], B[q4], 0x5410), a0[0], a0[1]);
+                e4m3x4_to_f16(__byte_perm(C[q4], E[q4], 0x5410), a0[2], a0[3]);
+                e4m3x4_to_f16(__byte_perm(A[q4], B[q4], 0x7632), a1[0], a1[1]);
+                e4m3x4_to_f16(__byte_perm(C[q4], E[q4], 0x7632), a1[2], a1[3]);
+                mma_f16_16816(o[2 * q4][0], a0, pb[0][0], pb[0][1]);
+                mma_f16_16816(o[2 * q4 + 1][0], a1, pb[0][0], pb[0][1]);
+                if (two) {
+                    mma_f16_16816(o[2 * q4][1], a0, pb[1][0], pb[1][1]);
+                    mma_f16_16816(o[2 * q4 + 1][1], a1, pb[1][0], pb[1][1]);
+                }
             }
         }
         // release the stage to the producer
@@ -670,33 +697,33 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
             mbar_arrive(c.empty0 + 8 * st);
 
         if (m.last) {
-            float L0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
-            L0 += __shfl_xor_sync(0xffffffffu, L0, 2);
-            float L1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
-            L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
-            const float inv0 = L0 > 0.f ? vref * kDecode / L0 : 0.f;
-            const float inv1 = L1 > 0.f ? vref * kDecode / L1 : 0.f;
             const int base = m.part_row + w * rows;  // this head's rows
-            // o[j][0|2]: column 32t + j, o[j][1|3]: column 32t + 16 + j
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int r = rr ? r1 : r0;
-                if (r >= rows)
-                    continue;
-                const float inv = rr ? inv1 : inv0;
-                uint4 *dst = reinterpret_cast<uint4 *>(a.part_o + (size_t)(base + r) * D + 32 * t);
+            for (int nt = 0; nt < 2; ++nt) {
+                if (nt == 1 && !two)
+                    break;
+                float Lq[2] = {lq[nt][0], lq[nt][1]};
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {  // columns 32t + 16h .. + 15
+                for (int off = 4; off < 32; off <<= 1) {
+                    Lq[0] += __shfl_xor_sync(0xffffffffu, Lq[0], off);
+                    Lq[1] += __shfl_xor_sync(0xffffffffu, Lq[1], off);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = nt * 8 + 2 * t + i;
+                    if (r >= rows)
+                        continue;
+                    const float inv = Lq[i] > 0.f ? vref * kDecode / Lq[i] : 0.f;
+                    // columns 16g + 2j (element i) and 16g + 2j + 1 (element 2 + i) of m-tile j
                     uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        pk[i] = pack_bf16x2(o[2 * i][2 * rr + h] * inv, o[2 * i + 1][2 * rr + h] * inv);
-                    dst[2 * h] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[2 * h + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                }
-                if (t == 0) {
-                    const float Lr = rr ? L1 : L0;
-                    a.part_lse[base + r] = Lr > 0.f ? ((rr ? m1 : m0) + fast_log2(Lr)) * kLn2 : -INFINITY;
+                    for (int j = 0; j < kMt; ++j)
+                        pk[j] = pack_bf16x2(o[j][nt][i] * inv, o[j][nt][2 + i] * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.part_o + (size_t)(base + r) * D + 16 * g);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    if (g == 0)
+                        a.part_lse[base + r] = Lq[i] > 0.f ? (mq[nt][i] + fast_log2(Lq[i])) * kLn2 : -INFINITY;
                 }
             }
         }
