@@ -166,6 +166,43 @@ hp_status hp_suffix_decode_paged_e4m3(const void *q, int64_t q_sb, int64_t q_sh,
                                       size_t ws_bytes, hp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * hp_stream_decode -- a decode step of Parallel Prompting requests, each
+ * request's KV row read in place with the stream mask applied inside the
+ * kernel (Read Once, Answer Many, Section 3 "Parallel Prompting", Eq. 2, and
+ * Figure 2's in-kernel mask; Section 4 for the two index tensors).
+ *
+ * Request r (0 <= r < R) decodes P streams; its query for stream s is query
+ * sequence r*P + s: q rows (r*P + s, h) at q + (r*P + s)*q_sb + h*q_sh (bf16,
+ * as in the conventions above, 16-byte aligned, strides multiples of 8).
+ * Its KV row holds row_len[r] slots -- the document, then the streams'
+ * question and answer tokens in any order -- slot t at page
+ * row_pages[r*pt_stride + t/page_size], position t % page_size, of the bf16
+ * pools [num_pages][Hkv][page_size][d].  Slot t carries a stream id
+ * slot_sid[r*sid_stride + t] (-1 for the document) and a position
+ * slot_pos[r*sid_stride + t]; query r*P + s carries q_sid[r*P + s] and
+ * q_pos[r*P + s].  Slot t is visible to that query iff
+ *     slot_pos <= q_pos  and  (slot_sid == -1 or slot_sid == q_sid)
+ * (the causal condition on positions, which the streams share, and the
+ * stream condition of Eq. 2).  All device int32 arrays; sid_stride a multiple
+ * of 4 with sid_stride >= pt_stride*page_size, slot arrays 16-byte aligned.
+ * The streams of a request share the pass over its row (up to 8 groups of
+ * 16 / (Hq/Hkv) streams per pass; more streams take further passes).  Rows
+ * with no visible slot get out = 0, lse = -inf.  A page id outside
+ * [0, num_pages) or a row length above pt_stride*page_size sets HP_ERR_BOUNDS
+ * in the workspace status word.  ws: >= hp_stream_workspace_bytes.
+ * ------------------------------------------------------------------------- */
+size_t hp_stream_workspace_bytes(int32_t R, int32_t P, int32_t Hq, int32_t Hkv, int32_t d,
+                                 int32_t pt_stride, int32_t page_size);
+hp_status hp_stream_decode(const void *q, int64_t q_sb, int64_t q_sh, int32_t R, int32_t P,
+                           const void *k_pool, const void *v_pool, int32_t num_pages,
+                           int32_t page_size, const int32_t *row_pages, int32_t pt_stride,
+                           const int32_t *row_len, const int32_t *slot_sid, const int32_t *slot_pos,
+                           int32_t sid_stride, const int32_t *q_sid, const int32_t *q_pos, int32_t Hq,
+                           int32_t Hkv, int32_t d, float scale, void *out, hp_dtype out_dt,
+                           int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
+                           size_t ws_bytes, hp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * hp_prefix_attn -- inter-sequence batched attention against one contiguous
  * shared prefix (Hydragen, "Inter-Sequence Batched Prefix Attention": the
  * queries of sequences [row_begin, row_begin + rows) are stacked and attend

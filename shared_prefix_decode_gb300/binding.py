@@ -63,6 +63,10 @@ _SIGNATURES = {
     "hp_suffix_decode_paged_e4m3": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp,
                                             c_i32, c_vp, c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64, c_i64,
                                             c_vp, c_i64, c_vp, c_sz, c_vp]),
+    "hp_stream_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "hp_stream_decode": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp,
+                                 c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64, c_i64, c_vp,
+                                 c_i64, c_vp, c_sz, c_vp]),
     "hp_prefix_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "hp_prefix_attn": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_i32, c_vp, c_vp, c_i64, c_i64, c_i32,
                                c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_i64, c_i64, c_vp, c_i64,
@@ -241,6 +245,43 @@ def hp_suffix_decode_paged_e4m3(q: torch.Tensor, k8: torch.Tensor, v8: torch.Ten
         _ptr(page_table), page_table.stride(0), _ptr(seq_lens), Hq, Hkv, d, float(scale), _ptr(out), _dt(out.dtype),
         out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(), _stream(stream)),
         "hp_suffix_decode_paged_e4m3")
+    return out, lse
+
+
+# ------------------------------------------------- Parallel Prompting rows
+def stream_workspace_bytes(R: int, P: int, Hq: int, Hkv: int, d: int, pt_stride: int, page_size: int) -> int:
+    return int(library().hp_stream_workspace_bytes(R, P, Hq, Hkv, d, pt_stride, page_size))
+
+
+def hp_stream_decode(q: torch.Tensor, rows, P: int, scale: float, out: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """q [R*P, Hq, d] bf16; ``rows`` a ``workloads.StreamRows`` on the GPU
+    (pools, row page table and lengths, slot stream ids and positions, query
+    stream ids and positions)."""
+    RP, Hq, d = q.shape
+    _need(RP % P == 0, "q must hold R * P query rows")
+    R = RP // P
+    Pn, Hkv, ps, d2 = rows.k_pool.shape
+    _need(d2 == d and rows.v_pool.shape == rows.k_pool.shape, "pool shape mismatch")
+    for t, n in ((rows.row_pages, "row_pages"), (rows.row_len, "row_len"), (rows.slot_sid, "slot_sid"),
+                 (rows.slot_pos, "slot_pos"), (rows.q_sid, "q_sid"), (rows.q_pos, "q_pos")):
+        _need(t.dtype == torch.int32 and t.is_contiguous() and t.is_cuda, f"{n} must be contiguous int32 on the GPU")
+    _need(tuple(rows.row_len.shape) == (R,) and tuple(rows.q_sid.shape) == (RP,) and
+          tuple(rows.q_pos.shape) == (RP,) and rows.row_pages.shape[0] == R and rows.slot_sid.shape == rows.slot_pos.shape
+          and rows.slot_sid.shape[0] == R, "row arrays do not match R and P")
+    if out is None:
+        out = torch.empty(RP, Hq, d, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(RP, Hq, dtype=torch.float32, device=q.device)
+    pt = rows.row_pages.shape[1]
+    if ws is None:
+        ws = alloc_workspace(stream_workspace_bytes(R, P, Hq, Hkv, d, pt, ps), q.device)
+    _check(library().hp_stream_decode(
+        _ptr(q), q.stride(0), q.stride(1), R, P, _ptr(rows.k_pool), _ptr(rows.v_pool), Pn, ps, _ptr(rows.row_pages),
+        pt, _ptr(rows.row_len), _ptr(rows.slot_sid), _ptr(rows.slot_pos), rows.slot_sid.shape[1], _ptr(rows.q_sid),
+        _ptr(rows.q_pos), Hq, Hkv, d, float(scale), _ptr(out), _dt(out.dtype), out.stride(0), out.stride(1),
+        _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(), _stream(stream)), "hp_stream_decode")
     return out, lse
 
 

@@ -261,6 +261,44 @@ bool hp::encode_q_map(CUtensorMap *m, const void *q, int B, int Hq, int d, int64
 }
 
 
+// ----------------------------------------------- Parallel Prompting rows
+namespace {
+
+struct StreamGeo {
+    int ns_pg, n_sg, nh, spi, n_sblk, rows_item, split_len, n_split;
+    int64_t n_items, part_rows;
+};
+
+// Items of hp_stream_decode: consumer warps of an item serve (head, group of
+// ns_pg streams) pairs, at most 8; the streams of a request share one pass
+// over its row when their groups fit one item.
+StreamGeo stream_geo(int R, int P, int G, int Hkv, int max_len, int sms)
+{
+    StreamGeo g{};
+    g.ns_pg = std::max(1, std::min(kSmallRows / G, P));
+    const int n_sg_all = (int)ceil_div(P, g.ns_pg);
+    g.n_sg = std::min(n_sg_all, 8);
+    g.nh = 1;
+    for (int nh = 8; nh >= 1; nh /= 2)
+        if (nh * g.n_sg <= 8 && Hkv % nh == 0) {
+            g.nh = nh;
+            break;
+        }
+    g.spi = g.n_sg * g.ns_pg;
+    g.n_sblk = (int)ceil_div(P, g.spi);
+    g.rows_item = g.nh * g.n_sg * g.ns_pg * G;
+    const int64_t units = (int64_t)R * (Hkv / g.nh) * g.n_sblk;
+    const int64_t chunks = ceil_div(std::max(max_len, 1), kChunk);
+    const int64_t per = std::max<int64_t>(4, ceil_div(units * chunks, 2 * (int64_t)sms));
+    g.split_len = (int)(per * kChunk);
+    g.n_split = (int)ceil_div(std::max(max_len, 1), g.split_len);
+    g.n_items = units * g.n_split;
+    g.part_rows = g.n_items * g.rows_item;
+    return g;
+}
+
+}  // namespace
+
 // =================================================================== C ABI
 extern "C" {
 
@@ -421,6 +459,120 @@ hp_status hp_suffix_decode_paged_e4m3(const void *q, int64_t q_sb, int64_t q_sh,
     return suffix_decode_impl(q, q_sb, q_sh, B, k_pool, v_pool, k_scale, v_scale, true, num_pages, page_size,
                               page_table, pt_stride, seq_lens, Hq, Hkv, d, scale, out, out_dt, o_sb, o_sh, lse,
                               lse_sb, ws, ws_bytes, stream);
+}
+
+size_t hp_stream_workspace_bytes(int32_t R, int32_t P, int32_t Hq, int32_t Hkv, int32_t d, int32_t pt_stride,
+                                 int32_t page_size)
+{
+    if (R < 1 || P < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Hq / Hkv > kSmallRows || !supported_d(d) ||
+        pt_stride < 1 || page_size < 16 || page_size % 16)
+        return 0;
+    const StreamGeo g = stream_geo(R, P, Hq / Hkv, Hkv, pt_stride * page_size, device_sms());
+    return ws_layout(g.part_rows, d).total;
+}
+
+hp_status hp_stream_decode(const void *q, int64_t q_sb, int64_t q_sh, int32_t R, int32_t P, const void *k_pool,
+                           const void *v_pool, int32_t num_pages, int32_t page_size, const int32_t *row_pages,
+                           int32_t pt_stride, const int32_t *row_len, const int32_t *slot_sid,
+                           const int32_t *slot_pos, int32_t sid_stride, const int32_t *q_sid, const int32_t *q_pos,
+                           int32_t Hq, int32_t Hkv, int32_t d, float scale, void *out, hp_dtype out_dt,
+                           int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws, size_t ws_bytes,
+                           hp_stream_t stream)
+{
+    if (!q || !k_pool || !v_pool || !row_pages || !row_len || !slot_sid || !slot_pos || !q_sid || !q_pos || !out ||
+        !ws)
+        return HP_ERR_ARG;
+    if (R < 1 || P < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || num_pages < 1 || pt_stride < 1 || !std::isfinite(scale))
+        return HP_ERR_ARG;
+    if (!supported_d(d) || page_size < 16 || page_size > 256 || page_size % 16 || Hq / Hkv > kSmallRows)
+        return HP_ERR_UNSUPPORTED;
+    if ((int64_t)pt_stride * page_size > INT32_MAX || (int64_t)R * P > INT32_MAX / 2)
+        return HP_ERR_UNSUPPORTED;
+    // the slot arrays are read 16 slots at a time by bulk copies
+    if (sid_stride % 4 || (int64_t)sid_stride < (int64_t)pt_stride * page_size || !aligned(slot_sid, 16) ||
+        !aligned(slot_pos, 16))
+        return HP_ERR_UNSUPPORTED;
+    if (q_sb % 8 || q_sh % 8 || q_sb < 0 || q_sh < 0 || !aligned(q, 16) || !out_layout_ok(out, out_dt, o_sb, o_sh, d) ||
+        !aligned(k_pool, 16) || !aligned(v_pool, 16))
+        return HP_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    const int sms = device_sms();
+    const StreamGeo g = stream_geo(R, P, G, Hkv, pt_stride * page_size, sms);
+    const WsLayout wl = ws_layout(g.part_rows, d);
+    if (ws_bytes < wl.total || !aligned(ws, 256))
+        return HP_ERR_WORKSPACE;
+    if (g.n_items > INT32_MAX || g.part_rows > INT32_MAX)
+        return HP_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+
+    StreamParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    if (!encode_pool_map(&sp.map_k, k_pool, num_pages, Hkv, page_size, d, kChunk, g.nh) ||
+        !encode_pool_map(&sp.map_v, v_pool, num_pages, Hkv, page_size, d, kChunk, g.nh))
+        return HP_ERR_CUDA;
+    sp.G = G;
+    sp.Hkv = Hkv;
+    sp.scale_log2 = scale * kLog2e;
+    sp.n_items = (int32_t)g.n_items;
+    sp.R = R;
+    sp.P = P;
+    sp.row_pages = row_pages;
+    sp.pt_stride = pt_stride;
+    sp.row_len = row_len;
+    sp.slot_sid = slot_sid;
+    sp.slot_pos = slot_pos;
+    sp.sid_stride = sid_stride;
+    sp.q_sid = q_sid;
+    sp.q_pos = q_pos;
+    sp.num_pages = num_pages;
+    sp.page_size = page_size;
+    sp.split_len = g.split_len;
+    sp.n_split = g.n_split;
+    sp.nh = g.nh;
+    sp.n_sg = g.n_sg;
+    sp.ns_pg = g.ns_pg;
+    sp.spi = g.spi;
+    sp.n_sblk = g.n_sblk;
+    sp.rows_item = g.rows_item;
+    sp.q = static_cast<const uint16_t *>(q);
+    sp.q_sb = q_sb;
+    sp.q_sh = q_sh;
+    sp.part_o = reinterpret_cast<uint16_t *>(wsb + wl.off_o);
+    sp.part_lse = reinterpret_cast<float *>(wsb + wl.off_lse);
+    sp.status = status_ptr(ws);
+    const int grid = (int)std::min<int64_t>(g.n_items, (int64_t)sms);
+    if (launch_stream(sp, grid, d, s) != cudaSuccess)
+        return HP_ERR_CUDA;
+
+    MergeParams mp;
+    std::memset(&mp, 0, sizeof(mp));
+    mp.part_o = sp.part_o;
+    mp.part_lse = sp.part_lse;
+    mp.d = d;
+    mp.G = G;
+    mp.Hq = Hq;
+    mp.Hkv = Hkv;
+    mp.B = R * P;
+    mp.mode = 3;
+    mp.seq_lens = row_len;
+    mp.split_len = g.split_len;
+    mp.n_split = g.n_split;
+    mp.nh = g.nh;
+    mp.P = P;
+    mp.spi = g.spi;
+    mp.n_sblk = g.n_sblk;
+    mp.ns_pg = g.ns_pg;
+    mp.n_sg = g.n_sg;
+    mp.rows_item = g.rows_item;
+    mp.out = out;
+    mp.out_f32 = out_dt == HP_F32;
+    mp.o_sb = o_sb;
+    mp.o_sh = o_sh;
+    mp.lse = lse;
+    mp.lse_sb = lse_sb;
+    mp.status = status_ptr(ws);
+    return launch_merge(mp, (int64_t)R * P * Hq, s) == cudaSuccess ? HP_OK : HP_ERR_CUDA;
 }
 
 size_t hp_prefix_workspace_bytes(int32_t rows, int32_t Hq, int32_t Hkv, int32_t d, int32_t prefix_len)

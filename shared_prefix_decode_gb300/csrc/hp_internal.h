@@ -190,6 +190,36 @@ struct SmallParams {
     const float *v_scale;
 };
 
+// Parallel Prompting rows (hp_stream_decode): items (request, KV-head group,
+// stream block, key split) over each request's one KV row, with the stream
+// mask applied per key.
+struct StreamParams {
+    CUtensorMap map_k;  // head-group boxes: 64 columns x 16 tokens x nh heads
+    CUtensorMap map_v;
+    int32_t G, Hkv;
+    float scale_log2;
+    int32_t n_items;
+    int32_t R, P;          // requests, streams per request (query sequence r * P + s)
+    const int32_t *row_pages;  // [R][pt_stride] page ids of each request's row
+    int32_t pt_stride;
+    const int32_t *row_len;    // [R] slots of each row
+    const int32_t *slot_sid;   // [R][sid_stride] stream id per slot (-1: document)
+    const int32_t *slot_pos;   // [R][sid_stride] position per slot
+    int32_t sid_stride;
+    const int32_t *q_sid;      // [R * P] stream id of each query
+    const int32_t *q_pos;      // [R * P] position of each query
+    int32_t num_pages, page_size, split_len, n_split;
+    int32_t nh;                // KV heads per item
+    int32_t n_sg, ns_pg;       // stream groups per item (one consumer warp each per head), streams per group
+    int32_t spi, n_sblk;       // streams per item (n_sg * ns_pg), stream blocks per request
+    int32_t rows_item;         // partial rows per item: nh * n_sg * ns_pg * G
+    const uint16_t *q;
+    int64_t q_sb, q_sh;
+    uint16_t *part_o;
+    float *part_lse;
+    uint32_t *status;
+};
+
 // Fused cascade kernel (tensor-core and paged roles, one persistent launch).
 struct CascadeParams {
     CUtensorMap q_tc;      // box 64 columns x G heads x (128 / G) rows
@@ -253,10 +283,12 @@ struct MergeParams {
     const int32_t *tab;
     int32_t tab_stride;
     // implicit modes (plan == nullptr)
-    int32_t mode;            // 1: paged decode splits; 2: contiguous prefix splits
+    int32_t mode;            // 1: paged decode splits; 2: contiguous prefix splits; 3: stream rows
     const int32_t *seq_lens; // mode 1
     int32_t split_len, n_split, seqs_per_item, row_begin, rows, n_rc;
-    int32_t nh;  // mode 1: KV heads per small-kernel item
+    int32_t nh;  // mode 1, 3: KV heads per item
+    // mode 3 (Parallel Prompting rows; seq_lens = the rows' lengths [R])
+    int32_t P, spi, n_sblk, ns_pg, n_sg, rows_item;
     int32_t wait_prior;  // launched as a programmatic dependent: wait for the prior grid first
     void *out;
     int32_t out_f32;
@@ -279,6 +311,8 @@ __host__ __device__ inline const T *plan_array(const PlanHeader *h, int64_t off)
 // Launchers (return the cudaGetLastError() after the launch).
 cudaError_t launch_tc(const TcParams &p, int grid, int d, cudaStream_t s);
 cudaError_t launch_small(const SmallParams &p, int grid, int d, cudaStream_t s);
+cudaError_t launch_stream(const StreamParams &p, int grid, int d, cudaStream_t s);
+size_t stream_smem_bytes(int d);
 cudaError_t launch_merge(const MergeParams &p, int64_t out_rows, cudaStream_t s);
 // The merge as a programmatic dependent launch of the preceding kernel.
 cudaError_t launch_merge_dependent(const MergeParams &p, int64_t out_rows, cudaStream_t s);

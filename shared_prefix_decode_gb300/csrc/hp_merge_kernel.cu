@@ -42,6 +42,16 @@ __device__ __forceinline__ int part_row(const MergeParams &p, const PartList &L,
         const int item = ((L.b * groups + L.kvh / p.nh) * p.n_split + e);
         return (item * p.nh + L.kvh % p.nh) * p.G + L.g;
     }
+    if (p.mode == 3) {
+        // stream-row items (request, head group, stream block, split); rows
+        // [warp (head in group, stream group)][stream in group][g]
+        const int r = L.b / p.P, sidx = L.b % p.P;
+        const int sb = sidx / p.spi, si = sidx % p.spi;
+        const int groups = p.Hkv / p.nh;
+        const int item = ((r * groups + L.kvh / p.nh) * p.n_sblk + sb) * p.n_split + e;
+        const int w = (L.kvh % p.nh) * p.n_sg + si / p.ns_pg;
+        return item * p.rows_item + (w * p.ns_pg + si % p.ns_pg) * p.G + L.g;
+    }
     // mode 2: contiguous prefix items (rc, kvh, split) of two 128-row blocks
     const int rel = L.b - p.row_begin;
     const int rc = rel / p.seqs_per_item, sl = rel % p.seqs_per_item;
@@ -85,8 +95,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) hp_merge_kernel(const __grid
         pr_b = eb + L.g;
     } else {
         L.trow = nullptr;
-        if (p.mode == 1) {
-            int len = __ldg(p.seq_lens + L.b);
+        if (p.mode == 1 || p.mode == 3) {
+            int len = __ldg(p.seq_lens + (p.mode == 3 ? L.b / p.P : L.b));
             len = max(0, len);
             L.n = min(p.n_split, (len + p.split_len - 1) / p.split_len);
         } else {

@@ -402,6 +402,13 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ int ld_shared_s32(uint32_t addr)
+{
+    int v;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");

@@ -3,6 +3,8 @@
 // paged-decode role (hp_small_role.cuh) with one producer warp and four
 // consumer warps per CTA; CTA c walks items c, c + grid, ... of (sequence,
 // KV-head group, key split).  Q8: E4M3 pools with per-(page, KV head) scales.
+// Also the Parallel Prompting row kernel (hp_stream_decode): the same role in
+// its stream-mask mode, one producer and eight consumer warps per CTA.
 #include <cuda_runtime.h>
 
 #include "hp_internal.h"
@@ -113,6 +115,126 @@ __global__ void __launch_bounds__(kThreadsSmall) hp_small_kernel(const __grid_co
     __syncwarp();
 }
 
+// ------------------------------------------------ Parallel Prompting rows
+// Read Once, Answer Many, Section 3: one KV row per request holds the
+// document and every stream's question and answer tokens; the stream mask
+// (Eq. 2) keeps each stream's query on the document and its own tokens.  An
+// item is (request r, nh KV heads, a block of spi streams, a key range): the
+// row's chunks are loaded once for all the block's streams, and consumer warp
+// w computes head w / n_sg for streams (w % n_sg) * ns_pg .. of the block.
+constexpr int kStreamConsumers = 8;
+constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;
+constexpr int kStreamStages = 3;
+
+template <int D>
+struct StreamKernelLayout {
+    using R = smr::Layout<D, kStreamConsumers, kStreamStages, 0, false, true>;
+    static constexpr int kBar = R::kEnd;
+    static constexpr int kMeta = kBar + 2 * kStreamStages * 8;
+    static constexpr int kZero = kMeta + 128;  // 16 zero bytes, then the abort flag
+    static constexpr int kBytes = kZero + 32;
+    static_assert(kStreamStages * (int)sizeof(smr::StageMeta) <= 128, "stage metadata");
+};
+
+struct StreamItems {
+    const StreamParams *p;
+    int first, stride;
+    static constexpr bool kPrefetch = false, kTokens = false;
+    __device__ int prefetch(int) const { return 0; }
+    __device__ smr::Desc operator()(int k, int) const
+    {
+        const int idx = first + k * stride;
+        smr::Desc d;
+        const int split = idx % p->n_split;
+        int t = idx / p->n_split;
+        const int sb = t % p->n_sblk;
+        t /= p->n_sblk;
+        const int groups = p->Hkv / p->nh;
+        const int grp = t % groups;
+        const int r = t / groups;
+        int len = __ldg(p->row_len + r);
+        const int cap = p->pt_stride * p->page_size;
+        if (len < 0 || len > cap) {
+            atomicOr(p->status, kStBounds);
+            len = len < 0 ? 0 : cap;
+        }
+        d.seq_begin = r * p->P + sb * p->spi;
+        d.n_seq = min(p->spi, p->P - sb * p->spi);
+        d.kvh0 = grp * p->nh;
+        d.k0 = split * p->split_len;
+        d.k1 = min(d.k0 + p->split_len, len);
+        d.part_row = idx * p->rows_item;
+        d.pages = p->row_pages + (int64_t)r * p->pt_stride;
+        d.pbase = 0;
+        d.ps = p->page_size;
+        d.num_pages = p->num_pages;
+        d.map_k = &p->map_k;
+        d.map_v = &p->map_v;
+        d.slot_sid = p->slot_sid + (int64_t)r * p->sid_stride;
+        d.slot_pos = p->slot_pos + (int64_t)r * p->sid_stride;
+        d.valid = d.k0 < d.k1;
+        return d;
+    }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kStreamThreads) hp_stream_kernel(const __grid_constant__ StreamParams p)
+{
+    using KL = StreamKernelLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    smr::Ctx c;
+    c.smem = smem;
+    c.sbase = smem_u32(smem);
+    c.full0 = c.sbase + KL::kBar;
+    c.empty0 = c.full0 + kStreamStages * 8;
+    c.meta = reinterpret_cast<smr::StageMeta *>(smem + KL::kMeta);
+    c.zero16 = c.sbase + KL::kZero;
+    c.abort = reinterpret_cast<volatile int *>(smem + KL::kZero + 16);
+    c.status = p.status;
+    smr::Args a{p.q, p.q_sb, p.q_sh, nullptr, p.G, p.nh, p.scale_log2, p.part_o, p.part_lse};
+    a.n_sg = p.n_sg;
+    a.ns_pg = p.ns_pg;
+    a.q_sid = p.q_sid;
+    a.q_pos = p.q_pos;
+    const int n_warps = p.nh * p.n_sg;  // consumer warps of an item
+    if (threadIdx.x < 4)
+        reinterpret_cast<uint32_t *>(smem + KL::kZero)[threadIdx.x] = 0u;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStreamStages; ++s) {
+            mbar_init(c.full0 + 8 * s, 1);
+            mbar_init(c.empty0 + 8 * s, (uint32_t)n_warps);
+        }
+        *c.abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int n_items = p.n_items > (int)blockIdx.x ? (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    if (warp == kStreamConsumers)
+        smr::producer<D, kStreamConsumers, kStreamStages, 0, StreamItems, false, true>(
+            c, a, StreamItems{&p, (int)blockIdx.x, (int)gridDim.x}, n_items, lane);
+    else if (warp < n_warps)
+        smr::consumer<D, kStreamConsumers, kStreamStages, 0, true>(c, a, warp, lane);
+    __syncwarp();
+}
+
+template <int D>
+cudaError_t launch_stream_d(const StreamParams &p, int grid, cudaStream_t s)
+{
+    static DeviceOnce once;
+    const int bytes = StreamKernelLayout<D>::kBytes + 1024;
+    static_assert(StreamKernelLayout<D>::kBytes + 1024 <= 227 * 1024, "shared memory per CTA");
+    cudaError_t e = once.run([bytes] {
+        return cudaFuncSetAttribute(hp_stream_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
+    if (e != cudaSuccess)
+        return e;
+    hp_stream_kernel<D><<<grid, kStreamThreads, bytes, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <int D, bool Q8>
 cudaError_t launch_small_d(const SmallParams &p, int grid, cudaStream_t s)
 {
@@ -128,6 +250,18 @@ cudaError_t launch_small_d(const SmallParams &p, int grid, cudaStream_t s)
 }
 
 }  // namespace
+
+size_t stream_smem_bytes(int d)
+{
+    return d == 64 ? StreamKernelLayout<64>::kBytes + 1024 : StreamKernelLayout<128>::kBytes + 1024;
+}
+
+cudaError_t launch_stream(const StreamParams &p, int grid, int d, cudaStream_t s)
+{
+    if (grid <= 0)
+        return cudaSuccess;
+    return d == 64 ? launch_stream_d<64>(p, grid, s) : launch_stream_d<128>(p, grid, s);
+}
 
 size_t small_smem_bytes(int d, bool q8)
 {

@@ -51,8 +51,10 @@ namespace smr {
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // Shared memory of the role for NC consumer warps, S stages and a Q slot of
-// QR rows per stage; Q8: E4M3 pools (d = 128).
-template <int D, int NC, int S, int QR, bool Q8 = false>
+// QR rows per stage; Q8: E4M3 pools (d = 128); SM: the stream mask of a
+// Parallel Prompting row (each stage also holds its 16 keys' stream ids and
+// positions).
+template <int D, int NC, int S, int QR, bool Q8 = false, bool SM = false>
 struct Layout {
     static_assert(!Q8 || D == 128, "E4M3 pools: d = 128");
     static constexpr int kHalves = D / 64;
@@ -63,7 +65,8 @@ struct Layout {
     static constexpr int kQHalf = kQRows * 128;
     static constexpr int kQSlot = kHalves * kQHalf;
     static constexpr int kScales = Q8 ? 1024 : 0;  // Q8: K scales [NC], then V scales at +128 bytes (f32)
-    static constexpr int kStage = 2 * kChunk + kQSlot + kScales;  // K, V, Q slot, scales
+    static constexpr int kMask = SM ? 1024 : 0;    // SM: slot stream ids [16], then positions at +64 (int32)
+    static constexpr int kStage = 2 * kChunk + kQSlot + kScales + kMask;  // K, V, Q slot, scales, mask
     static constexpr int kEnd = S * kStage;
     static_assert(NC * 4 <= 128, "scale slots");
 };
@@ -85,6 +88,11 @@ struct Desc {
     int ps, num_pages;
     const void *map_k;
     const void *map_v;
+    // Parallel Prompting row (SM): stream id and position of key t of the
+    // row at slot_sid[t] / slot_pos[t] (16-byte aligned, readable to the end
+    // of the 16-key chunk holding the row's last key)
+    const int32_t *slot_sid = nullptr;
+    const int32_t *slot_pos = nullptr;
     // E4M3 pools: scale of (page, KV head h) at k_scale[page * Hkv + h]
     const float *k_scale = nullptr;
     const float *v_scale = nullptr;
@@ -121,6 +129,13 @@ struct Args {
     float scale_log2;
     uint16_t *part_o;  // bf16
     float *part_lse;
+    // SM: consumer warp w serves head w / n_sg of the item's group and its
+    // streams (query sequences) (w % n_sg) * ns_pg .. + ns_pg - 1 (ns_pg * G
+    // <= 16 rows), writing partial rows part_row + w * ns_pg * G ..; query
+    // sequence b carries stream id q_sid[b] and position q_pos[b]
+    int n_sg = 1, ns_pg = 0;
+    const int32_t *q_sid = nullptr;
+    const int32_t *q_pos = nullptr;
 };
 
 // Producer warp: walks items k = 0, 1, ... of `src` (src(k, pre) -> Desc,
@@ -129,10 +144,10 @@ struct Args {
 // dependent load at the item's start), then closes the ring with a sentinel
 // stage (n_seq = -1, completed by a plain arrival) that tells the consumers
 // to stop.  All 32 lanes call it.
-template <int D, int NC, int S, int QR, class Src, bool Q8 = false>
+template <int D, int NC, int S, int QR, class Src, bool Q8 = false, bool SM = false>
 __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src &src, int n_items, int lane)
 {
-    using L = Layout<D, NC, S, QR, Q8>;
+    using L = Layout<D, NC, S, QR, Q8, SM>;
     constexpr int kHalves = D / 64;
     auto wait_warp = [&](uint32_t b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
@@ -233,7 +248,7 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 m.qslot = ch == 0 && qslot;
                 c.meta[st] = m;
                 mbar_arrive_expect_tx(bar, (Q8 ? 2 : 2 * kHalves) * a.nh * L::kHeadBox +
-                                               (m.qslot ? kHalves * a.nh * a.G * 128 : 0));
+                                               (m.qslot ? kHalves * a.nh * a.G * 128 : 0) + (SM ? 128 : 0));
             }
             __syncwarp();
             constexpr int kBoxLanes = Q8 ? 2 : 2 * kHalves;  // K and V boxes (one per column half for bf16)
@@ -246,6 +261,11 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 const int h = lane - kBoxLanes;
                 tma_load_3d(c.sbase + st * L::kStage + 2 * L::kChunk + h * L::kQHalf, a.map_q, bar, h * 64,
                             d.kvh0 * a.G, d.seq_begin);
+            } else if (SM && lane >= 8 && lane < 10) {
+                // the chunk's 16 stream ids (lane 8) and positions (lane 9)
+                const uint32_t mk = c.sbase + st * L::kStage + 2 * L::kChunk + L::kQSlot + L::kScales;
+                bulk_load_h(mk + (lane - 8) * 64, (lane == 8 ? d.slot_sid : d.slot_pos) + t, 64, bar,
+                            l2_evict_first());
             }
         }
     }
@@ -271,10 +291,14 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
 
 // Consumer warp w (0 <= w < nh): processes the chunks in ring order until
 // the producer's sentinel stage.
-template <int D, int NC, int S, int QR>
+// SM (a Parallel Prompting row): warp w serves head w / n_sg and a group of
+// ns_pg streams; each key's visibility follows the row's stream mask
+// (Read Once, Answer Many, Section 3, Eq. 2): key k is visible to the query
+// of stream s at position p iff pos[k] <= p and (sid[k] = -1 or sid[k] = s).
+template <int D, int NC, int S, int QR, bool SM = false>
 __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int lane)
 {
-    using L = Layout<D, NC, S, QR>;
+    using L = Layout<D, NC, S, QR, false, SM>;
     constexpr int kHalves = D / 64;
     constexpr int kKs = D / 16;  // k-steps of the S MMA
     constexpr int kNt = D / 8;   // n8 tiles of O
@@ -286,7 +310,10 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     const int r0 = lane >> 2, r1 = r0 + 8;
     const int tq = 2 * (lane & 3);
-    const uint32_t hoff = (uint32_t)w * L::kHeadBox;  // this warp's head within a box
+    const int hw = SM ? w / a.n_sg : w;     // head of the item's group
+    const int sj = SM ? w % a.n_sg : 0;     // stream group (SM)
+    const uint32_t hoff = (uint32_t)hw * L::kHeadBox;  // this warp's head within a box
+    int qsid0 = 0, qsid1 = 0, qpos0 = 0, qpos1 = 0;     // SM: rows r0 / r1's stream and position
     for (uint32_t k = 0;; ++k) {
         const uint32_t st = k % S;
         if (!wait_warp(c.full0 + 8 * st, (k / S) & 1u))
@@ -294,8 +321,10 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
         const StageMeta m = c.meta[st];
         if (m.n_seq < 0)
             break;  // sentinel: the producer's walk is over
-        const int rows = m.n_seq * a.G;
-        const int kvh = m.kvh0 + w;
+        const int seq0 = SM ? m.seq_begin + sj * a.ns_pg : m.seq_begin;
+        const int n_seq = SM ? max(0, min(a.ns_pg, m.n_seq - sj * a.ns_pg)) : m.n_seq;
+        const int rows = n_seq * a.G;
+        const int kvh = m.kvh0 + hw;
         if (m.first && m.qslot) {
             // new item, Q rows in the stage: head w's rows are slot rows
             // w*G .. w*G+G-1; rows past G read a zero chunk
@@ -319,9 +348,15 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
             // new item: query fragments (A operand, rows r0 / r1) and state
             const uint16_t *q0 = nullptr, *q1 = nullptr;
             if (r0 < rows)
-                q0 = a.q + (int64_t)(m.seq_begin + r0 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r0 % a.G) * a.q_sh;
+                q0 = a.q + (int64_t)(seq0 + r0 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r0 % a.G) * a.q_sh;
             if (r1 < rows)
-                q1 = a.q + (int64_t)(m.seq_begin + r1 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r1 % a.G) * a.q_sh;
+                q1 = a.q + (int64_t)(seq0 + r1 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r1 % a.G) * a.q_sh;
+            if (SM) {
+                qsid0 = r0 < rows ? __ldg(a.q_sid + seq0 + r0 / a.G) : 0;
+                qpos0 = r0 < rows ? __ldg(a.q_pos + seq0 + r0 / a.G) : 0;
+                qsid1 = r1 < rows ? __ldg(a.q_sid + seq0 + r1 / a.G) : 0;
+                qpos1 = r1 < rows ? __ldg(a.q_pos + seq0 + r1 / a.G) : 0;
+            }
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
                 qa[ks][0] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + ks * 16 + tq)) : 0u;
@@ -376,6 +411,22 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
             const int tk = tq + (e & 1);
             x[0][e] = tk < nvalid ? s0[e] * cs : -INFINITY;
             x[1][e] = tk + 8 < nvalid ? s1[e] * cs : -INFINITY;
+        }
+        if (SM) {
+            // the stream mask: this chunk's stream ids and positions
+            const uint32_t mk = c.sbase + st * L::kStage + 2 * L::kChunk + L::kQSlot + L::kScales;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int qs = e < 2 ? qsid0 : qsid1, qp = e < 2 ? qpos0 : qpos1;
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    const int key = tile * 8 + tq + (e & 1);
+                    const int sid = ld_shared_s32(mk + 4 * key);
+                    const int pos = ld_shared_s32(mk + 64 + 4 * key);
+                    if (!(pos <= qp && (sid == -1 || sid == qs)))
+                        x[tile][e] = -INFINITY;
+                }
+            }
         }
         float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
         float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
@@ -434,7 +485,7 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
             L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
             const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f;
             const float inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
-            const int base = m.part_row + w * rows;  // this head's rows
+            const int base = m.part_row + w * (SM ? a.ns_pg * a.G : rows);  // this warp's rows
             if (r0 < rows) {
                 uint16_t *dst = a.part_o + (size_t)(base + r0) * D + tq;
 #pragma unroll

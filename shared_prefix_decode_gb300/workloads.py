@@ -45,6 +45,8 @@ __all__ = [
     "StreamRequests",
     "stream_requests",
     "streams_as_tree",
+    "StreamRows",
+    "stream_rows_paged",
     "E4M3Pools",
     "quantize_e4m3",
     "with_e4m3_levels",
@@ -517,6 +519,65 @@ def with_e4m3_levels(wl: CascadeWorkload, levels="paged") -> CascadeWorkload:
     lv = [TreeLevel(l.nodes.clone(), l.page_ids.clone(), i in marks or l.e4m3) for i, l in enumerate(wl.levels)]
     return CascadeWorkload(wl.name, wl.B, wl.Hq, wl.Hkv, wl.d, wl.page_size, wl.scale, wl.q, wl.k_pool, wl.v_pool,
                            lv, wl.seed, wl.part, quantize_e4m3(wl.k_pool, wl.v_pool))
+
+
+@dataclass
+class StreamRows:
+    """Parallel Prompting requests stored for hp_stream_decode: each
+    request's KV row in pages of a shared pool, with its slots' stream ids
+    and positions, and each query's stream id and position."""
+
+    k_pool: torch.Tensor     # bf16 [num_pages, Hkv, ps, d]
+    v_pool: torch.Tensor
+    row_pages: torch.Tensor  # int32 [R, pt_stride]
+    row_len: torch.Tensor    # int32 [R]
+    slot_sid: torch.Tensor   # int32 [R, sid_stride]; -2 past the row (never visible)
+    slot_pos: torch.Tensor   # int32 [R, sid_stride]
+    q_sid: torch.Tensor      # int32 [R * P]
+    q_pos: torch.Tensor      # int32 [R * P]
+    page_size: int
+
+    def to(self, device) -> "StreamRows":
+        return StreamRows(*(t.to(device) for t in (self.k_pool, self.v_pool, self.row_pages, self.row_len,
+                                                    self.slot_sid, self.slot_pos, self.q_sid, self.q_pos)),
+                          self.page_size)
+
+
+def stream_rows_paged(req: StreamRequests, page_size: int = 16, seed: int = 0, shuffle: bool = True) -> StreamRows:
+    """The rows of ``stream_requests`` in a paged pool: row r's slot t at
+    page row_pages[r, t // page_size], position t % page_size; the pages of
+    all rows in one seeded random physical order.  Unused page slots hold
+    N(0,1) bf16 (never visible: past the row's length)."""
+    ps = page_size
+    npg = [(row[0].numel() + ps - 1) // ps for row in req.rows]
+    total = max(1, sum(npg))
+    g = torch.Generator().manual_seed(seed + 5101)
+    perm = torch.randperm(total, generator=g) if shuffle else torch.arange(total)
+    k_pool = torch.randn(total, req.Hkv, ps, req.d, generator=g).to(torch.bfloat16)
+    v_pool = torch.randn(total, req.Hkv, ps, req.d, generator=g).to(torch.bfloat16)
+    pt_stride = max(1, max(npg))
+    sid_stride = (pt_stride * ps + 3) // 4 * 4
+    row_pages = torch.zeros(req.R, pt_stride, dtype=torch.int32)
+    slot_sid = torch.full((req.R, sid_stride), -2, dtype=torch.int32)
+    slot_pos = torch.full((req.R, sid_stride), 2 ** 30, dtype=torch.int32)
+    row_len = torch.zeros(req.R, dtype=torch.int32)
+    first = 0
+    for r, (sid, pos, k, v) in enumerate(req.rows):
+        nk = sid.numel()
+        pages = perm[first:first + npg[r]]
+        first += npg[r]
+        row_pages[r, :npg[r]] = pages.to(torch.int32)
+        for t0 in range(0, nk, ps):
+            m = min(ps, nk - t0)
+            p_ = int(pages[t0 // ps])
+            k_pool[p_, :, :m] = k[t0:t0 + m].transpose(0, 1)
+            v_pool[p_, :, :m] = v[t0:t0 + m].transpose(0, 1)
+        slot_sid[r, :nk] = sid
+        slot_pos[r, :nk] = pos
+        row_len[r] = nk
+    q_sid = torch.tensor([s for _ in range(req.R) for s in range(req.P)], dtype=torch.int32)
+    q_pos = torch.tensor(req.q_pos, dtype=torch.int32)
+    return StreamRows(k_pool, v_pool, row_pages, row_len, slot_sid, slot_pos, q_sid, q_pos, ps)
 
 
 def _probe_code(b: int, d: int) -> torch.Tensor:

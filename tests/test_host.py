@@ -497,3 +497,29 @@ def test_e4m3_unique_bytes_and_quantiser():
     # relative step of E4M3 is 2^-3 in the normal range: error <= 2^-4 of the value's binade
     err = (dec - x).abs()
     assert (err <= x.abs() * 2.0 ** -4 + q8.k_scale[:, :, None, None] * 2.0 ** -10).all()
+
+
+# ------------------------------------------------ Parallel Prompting rows
+def test_stream_rows_paged_layout():
+    """Each request's row sits in its pages slot by slot, with its stream
+    ids and positions; slots past the row are never visible (-2)."""
+    req = W.stream_requests(R=3, P=4, Hq=4, Hkv=2, d=64, doc_len=37, q_len_range=(1, 9), T=3, seed=2)
+    rows = W.stream_rows_paged(req, page_size=16, seed=1)
+    for r, (sid, pos, k, v) in enumerate(req.rows):
+        nk = sid.numel()
+        assert int(rows.row_len[r]) == nk
+        for t in range(nk):
+            page = int(rows.row_pages[r, t // 16])
+            assert torch.equal(rows.k_pool[page, :, t % 16], k[t]) and torch.equal(rows.v_pool[page, :, t % 16], v[t])
+        assert torch.equal(rows.slot_sid[r, :nk], sid) and torch.equal(rows.slot_pos[r, :nk], pos)
+        assert (rows.slot_sid[r, nk:] == -2).all()
+    assert rows.slot_sid.shape[1] % 4 == 0 and rows.slot_sid.shape[1] >= rows.row_pages.shape[1] * 16
+    assert rows.q_sid.tolist() == [s for _ in range(3) for s in range(4)]
+
+
+def test_stream_workspace_sizes_and_rejections():
+    assert hb.stream_workspace_bytes(2, 16, 32, 32, 128, 40, 16) > 0
+    assert hb.stream_workspace_bytes(2, 64, 32, 8, 128, 40, 16) > 0
+    assert hb.stream_workspace_bytes(0, 16, 32, 32, 128, 40, 16) == 0
+    assert hb.stream_workspace_bytes(2, 16, 32, 32, 96, 40, 16) == 0
+    assert hb.stream_workspace_bytes(2, 16, 64, 2, 128, 40, 16) == 0  # 32 query heads per KV head
