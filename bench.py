@@ -285,6 +285,54 @@ def plan_summary(hb, s) -> dict:
             "ctas_with_both": len(tc_ctas & sm_ctas)}
 
 
+def parallel_prompting_figure(hb, dev, stream, peaks, dist) -> dict:
+    """Parallel Prompting rows (Read Once, Answer Many, Section 3): R
+    requests of P streams over their own 8K-token documents, decode step 64,
+    questions U[32, 64]; each request's row read in place with the stream
+    mask (hp_stream_decode) against the same requests in the cascade form
+    (the document a node shared by the request's streams, each stream's
+    slots a private node).  Both read the same unique bytes."""
+    import torch
+    from shared_prefix_decode_gb300 import workloads as W
+    R, P, doc, T = 2, 64, 8192, 64
+    sets = []
+    for i in range(2):
+        req = W.stream_requests(R=R, P=P, Hq=32, Hkv=32, d=128, doc_len=doc, q_len_range=(32, 64), T=T, seed=900 + i)
+        rows = W.stream_rows_paged(req, seed=i).to(dev)
+        tree = W.streams_as_tree(req).to(dev)
+        plan = hb.CascadePlan.from_workload(tree)
+        q = req.q.to(dev)
+        ws = hb.alloc_workspace(hb.stream_workspace_bytes(R, P, 32, 32, 128, rows.row_pages.shape[1], 16), dev)
+        out = torch.empty(R * P, 32, 128, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(R * P, 32, dtype=torch.float32, device=dev)
+        sets.append({"req": req, "rows": rows, "tree": tree, "plan": plan, "q": q, "ws": ws, "out": out, "lse": lse})
+    nbytes = statistics.mean(int(s["rows"].row_len.sum()) * 32 * 128 * 4 for s in sets)
+
+    def in_place(s):
+        hb.hp_stream_decode(s["q"], s["rows"], P, s["req"].scale, out=s["out"], lse=s["lse"], ws=s["ws"],
+                            stream=stream)
+
+    def cascade(s):
+        hb.hp_cascade_decode(s["plan"], s["tree"].q, s["tree"].scale, out=s["out"], lse=s["lse"], stream=stream)
+
+    res = {"requests": R, "streams_per_request": P, "document_tokens": doc, "decode_step": T,
+           "unique_kv_bytes": nbytes}
+    for name, fn in (("in_place_masked_rows", in_place), ("cascade_form", cascade)):
+        with torch.cuda.stream(stream):
+            for s in sets:
+                fn(s)
+        torch.cuda.synchronize(dev)
+        g = StepGraphs(fn, sets, 8, 256, stream)
+        t, _, _ = timed_passes(g, 4, 0.2, stream, dev, dist)
+        st = pass_stats(t, 8)
+        res[name] = dict(st, tbs=nbytes / (st["median_us"] * 1e-6) / 1e12,
+                         roofline_frac=nbytes / (peaks["hbm_gbs"] * 1e9) / (st["median_us"] * 1e-6))
+    for s in sets:
+        if hb.hp_read_device_status(s["ws"]) != 0:
+            raise RuntimeError("parallel prompting rows: device status")
+    return res
+
+
 # ------------------------------------------------------------ graph timing
 class StepGraphs:
     """CUDA graphs of consecutive steps over `items` in rotation order (step i
@@ -738,21 +786,22 @@ def main():
                                               "unique bytes count codes and scales")
             del e_sets, e_ws
             torch.cuda.empty_cache()
-        # the other workloads at full size, cold L2
+        # the other workloads at full size, cold L2 (and, for the two that
+        # are mostly per-sequence bytes, with those levels in E4M3)
         per_cfg = {}
-        for name in ("codellama13b", "tree2", "doc_streams", "no_sharing"):
+        for name, e4 in (("codellama13b", False), ("codellama13b", True), ("tree2", False), ("doc_streams", False),
+                         ("no_sharing", False), ("no_sharing", True)):
             if name == args.config:
                 continue
-            c_sets, c_ws, c_note = make_sets(name, "all", 1000 * rank + 700, device=dev)
+            c_sets, c_ws, c_note = make_sets(name, "all", 1000 * rank + 700, device=dev, e4m3=e4)
             b = statistics.mean(s["wl"].unique_kv_bytes() for s in c_sets)
             f = statistics.mean(s["wl"].shared_flops() for s in c_sets)
-            per_cfg[name] = dict(measure(c_sets, c_ws, b, f, 8 * len(c_sets)), l2=c_note,
-                                 plan={"tc_items": c_sets[0]["plan"].info.n_tc_items,
-                                       "small_items": c_sets[0]["plan"].info.n_small_items,
-                                       "part_rows": c_sets[0]["plan"].info.n_part_rows})
+            per_cfg[name + ("_e4m3" if e4 else "")] = dict(
+                measure(c_sets, c_ws, b, f, 8 * len(c_sets)), l2=c_note, plan=plan_summary(hb, c_sets[0]))
             del c_sets, c_ws
             torch.cuda.empty_cache()
         extras["workloads"] = per_cfg
+        extras["parallel_prompting"] = parallel_prompting_figure(hb, dev, stream, peaks, dist)
 
     # ---------------------------------------------------- cpu baseline
     cpu = None
