@@ -316,8 +316,35 @@ hp_status validate_loop(const hp_tree_desc *d, int capacity)
 // end on a page boundary, and all of them to use the same pools and page
 // size.  The fused node takes the place of its first member; the sequence
 // then has one partial state, not one per node, for the same bytes.  Nodes
-// that grow in a decode loop stay on their own.  Concatenated page lists are
-// appended to P.page_ids.
+// that grow in a decode loop stay on their own.
+//
+// A narrow shared node -- 2 or 3 sequences, still on the paged path, page
+// aligned -- can join its sequences' chains too: each of them then reads the
+// node's keys itself, and each loses a partial state and a merge part
+// ("every merge has a cost", shared-prefix KV caching blog, "Prefix trees:
+// multi-level sharing"; ChunkAttention's realistic trees have many such
+// nodes).  It joins when the extra reads cost less than the merge parts they
+// save (narrow_pays), and only when every one of its sequences has an own
+// node to fuse it with.  Concatenated page lists are appended to P.page_ids.
+namespace {
+
+// Modelled cost of one more merge part per output row (ns): the merge
+// kernel's time grows by about this much per part of its rows.
+constexpr double kMergePartNs = 120.0;
+// HBM bytes per ns the re-reads are charged at.
+constexpr double kReadBytesPerNs = 6000.0;
+
+bool narrow_pays(const hp_tree_desc *d, const hp_tree_node &N, int page_size, int G)
+{
+    const int ns = N.seq_end - N.seq_begin;
+    if (ns < 2 || ns > 3 || ns * G > kSmallRows || N.kv_len <= 0 || N.kv_len % page_size)
+        return false;
+    const double extra = (double)(ns - 1) * N.kv_len * d->Hkv * d->d * 4.0 / kReadBytesPerNs;
+    return extra < kMergePartNs;
+}
+
+}  // namespace
+
 void plan_nodes(const hp_tree_desc *d, int G, int capacity, const std::vector<int32_t> &level_page_off, HostPlan &P)
 {
     const int last = d->num_levels - 1;
@@ -331,28 +358,33 @@ void plan_nodes(const hp_tree_desc *d, int G, int capacity, const std::vector<in
                A.page_size == Bl.page_size && A.kv_type == Bl.kv_type && A.k_scale == Bl.k_scale &&
                A.v_scale == Bl.v_scale;
     };
-    // members[l][n]: the (level, node) list a fused node starts with; skip[l][n]: fused into another
-    std::vector<std::vector<std::vector<std::pair<int, int>>>> members(d->num_levels);
-    std::vector<std::vector<char>> skip(d->num_levels);
-    for (int l = 0; l < d->num_levels; ++l) {
-        members[l].assign(d->levels[l].num_nodes, {});
-        skip[l].assign(d->levels[l].num_nodes, 0);
+    const int nl = d->num_levels;
+    // own[l][b]: the fusable node of level l that covers only sequence b, or -1;
+    // wide[l][b]: the narrow shared node of level l covering b, if it may join
+    std::vector<std::vector<int>> own(nl, std::vector<int>(d->B, -1)), wide(nl, std::vector<int>(d->B, -1));
+    std::vector<std::vector<char>> narrow(nl);
+    for (int l = 0; l < nl; ++l) {
+        narrow[l].assign(d->levels[l].num_nodes, 0);
+        for (int n = 0; n < d->levels[l].num_nodes; ++n) {
+            const hp_tree_node &N = d->levels[l].nodes[n];
+            if (fusable(l, N))
+                own[l][N.seq_begin] = n;
+            else if (!(capacity > 0 && l == last) && narrow_pays(d, N, d->levels[l].page_size, G))
+                narrow[l][n] = 1;
+        }
     }
-    // own[l][b]: the fusable node of level l that covers only sequence b, or -1
-    std::vector<std::vector<int>> own(d->num_levels, std::vector<int>(d->B, -1));
-    for (int l = 0; l < d->num_levels; ++l)
-        for (int n = 0; n < d->levels[l].num_nodes; ++n)
-            if (fusable(l, d->levels[l].nodes[n]))
-                own[l][d->levels[l].nodes[n].seq_begin] = n;
-    for (int b = 0; b < d->B; ++b) {
-        // this sequence's fusable nodes, level by level
+    // the chain of sequence b: its own nodes and the joining narrow nodes,
+    // same pools as the first, page-aligned ones first, at most one ragged
+    // node last
+    auto chain_of = [&](int b) {
         std::vector<std::pair<int, int>> cand;
-        for (int l = 0; l < d->num_levels; ++l)
-            if (own[l][b] >= 0 && (cand.empty() || same_pools(cand[0].first, l)))
-                cand.emplace_back(l, own[l][b]);
-        if (cand.size() < 2)
-            continue;
-        // page-aligned nodes first, then at most one that ends mid-page
+        for (int l = 0; l < nl; ++l) {
+            int n = own[l][b];
+            if (n < 0)
+                n = wide[l][b];
+            if (n >= 0 && (cand.empty() || same_pools(cand[0].first, l)))
+                cand.emplace_back(l, n);
+        }
         std::vector<std::pair<int, int>> chain;
         int ragged = -1;
         for (size_t i = 0; i < cand.size(); ++i) {
@@ -364,30 +396,105 @@ void plan_nodes(const hp_tree_desc *d, int G, int capacity, const std::vector<in
         }
         if (ragged >= 0)
             chain.push_back(cand[ragged]);
+        return chain;
+    };
+    auto has_own = [&](const std::vector<std::pair<int, int>> &ch) {
+        for (const auto &m : ch)
+            if (own[m.first][d->levels[m.first].nodes[m.second].seq_begin] == m.second &&
+                d->levels[m.first].nodes[m.second].seq_end - d->levels[m.first].nodes[m.second].seq_begin == 1)
+                return true;
+        return false;
+    };
+    // Narrow nodes join when every one of their sequences' chains takes them
+    // along with an own node; otherwise they stay whole (each round only
+    // withdraws nodes, so the rounds end).
+    for (;;) {
+        for (int l = 0; l < nl; ++l)
+            std::fill(wide[l].begin(), wide[l].end(), -1);
+        for (int l = 0; l < nl; ++l)
+            for (int n = 0; n < d->levels[l].num_nodes; ++n)
+                if (narrow[l][n]) {
+                    const hp_tree_node &N = d->levels[l].nodes[n];
+                    for (int b = N.seq_begin; b < N.seq_end; ++b)
+                        wide[l][b] = n;
+                }
+        bool changed = false;
+        for (int l = 0; l < nl; ++l)
+            for (int n = 0; n < d->levels[l].num_nodes; ++n) {
+                if (!narrow[l][n])
+                    continue;
+                const hp_tree_node &N = d->levels[l].nodes[n];
+                bool ok = true;
+                for (int b = N.seq_begin; b < N.seq_end && ok; ++b) {
+                    const auto ch = chain_of(b);
+                    ok = has_own(ch) && std::find(ch.begin(), ch.end(), std::make_pair(l, n)) != ch.end();
+                }
+                if (!ok) {
+                    narrow[l][n] = 0;
+                    changed = true;
+                }
+            }
+        if (!changed)
+            break;
+    }
+    for (int l = 0; l < nl; ++l)
+        std::fill(wide[l].begin(), wide[l].end(), -1);
+    for (int l = 0; l < nl; ++l)
+        for (int n = 0; n < d->levels[l].num_nodes; ++n)
+            if (narrow[l][n]) {
+                const hp_tree_node &N = d->levels[l].nodes[n];
+                for (int b = N.seq_begin; b < N.seq_end; ++b)
+                    wide[l][b] = n;
+            }
+    // heads[l][n]: the fused chains that take the place of node (l, n) (a
+    // narrow node heads one chain per sequence); skip[l][n]: fused away
+    std::vector<std::vector<std::vector<std::vector<std::pair<int, int>>>>> heads(nl);
+    std::vector<std::vector<char>> skip(nl);
+    for (int l = 0; l < nl; ++l) {
+        heads[l].assign(d->levels[l].num_nodes, {});
+        skip[l].assign(d->levels[l].num_nodes, 0);
+    }
+    for (int b = 0; b < d->B; ++b) {
+        const auto chain = chain_of(b);
         if (chain.size() < 2)
             continue;
         // the fused node sits where its first member (in tree order) was
         const auto head = *std::min_element(chain.begin(), chain.end());
-        members[head.first][head.second] = chain;
+        heads[head.first][head.second].push_back(chain);
         for (const auto &m : chain)
-            if (m != head)
-                skip[m.first][m.second] = 1;
+            skip[m.first][m.second] = 1;
     }
-    for (int l = 0; l < d->num_levels; ++l) {
+    for (int l = 0; l < nl; ++l) {
         const hp_tree_level &L = d->levels[l];
         for (int n = 0; n < L.num_nodes; ++n) {
-            if (skip[l][n])
+            const auto &chains = heads[l][n];
+            if (skip[l][n] && chains.empty())
                 continue;
             const hp_tree_node &N = L.nodes[n];
-            PNode pn;
-            pn.level = l;
-            pn.seq_begin = N.seq_begin;
-            pn.seq_end = N.seq_end;
-            pn.loop = capacity > 0 && l == last;
-            pn.kv_len = N.kv_len;
-            pn.page_base = level_page_off[l] + N.page_off;
-            const auto &ch = members[l][n];
-            if (!ch.empty()) {
+            if (chains.empty()) {
+                PNode pn;
+                pn.level = l;
+                pn.seq_begin = N.seq_begin;
+                pn.seq_end = N.seq_end;
+                pn.loop = capacity > 0 && l == last;
+                pn.kv_len = N.kv_len;
+                pn.page_base = level_page_off[l] + N.page_off;
+                P.nodes.push_back(pn);
+                continue;
+            }
+            for (const auto &ch : chains) {
+                // the sequence of the chain: its own node's (a narrow head covers several)
+                int b = -1;
+                for (const auto &m : ch) {
+                    const hp_tree_node &M = d->levels[m.first].nodes[m.second];
+                    if (M.seq_end - M.seq_begin == 1)
+                        b = M.seq_begin;
+                }
+                PNode pn;
+                pn.level = l;
+                pn.seq_begin = b;
+                pn.seq_end = b + 1;
+                pn.loop = false;
                 pn.kv_len = 0;
                 pn.page_base = (int32_t)P.page_ids.size();
                 for (const auto &m : ch) {
@@ -397,8 +504,8 @@ void plan_nodes(const hp_tree_desc *d, int G, int capacity, const std::vector<in
                     P.page_ids.insert(P.page_ids.end(), ML.page_ids + MN.page_off, ML.page_ids + MN.page_off + npg);
                     pn.kv_len += MN.kv_len;
                 }
+                P.nodes.push_back(pn);
             }
-            P.nodes.push_back(pn);
         }
     }
 }

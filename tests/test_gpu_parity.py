@@ -244,9 +244,22 @@ def _sample_rows(wl, n, seed):
 
 
 @pytest.mark.parametrize("name", ["codellama13b", "tree2", "doc_streams", "no_sharing"])
-def test_cascade_full_size_sampled(name):
+def test_cascade_full_size_all_rows(name):
+    """Every output row of the full-size workload, seed 0."""
     wl = W.make_config(name, seed=0)
-    rows = _sample_rows(wl, 96, 7)
+    O, L = oracle.cascade(wl)
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    out, lse = plan.decode(wg.q, wl.scale)
+    _status_ok(plan.ws)
+    _check(out, lse, O, L, f"{name} full, every row")
+
+
+@pytest.mark.parametrize("name", ["codellama13b", "tree2", "doc_streams", "no_sharing"])
+@pytest.mark.parametrize("seed", [1, 2, 3, 4])
+def test_cascade_full_size_sampled(name, seed):
+    wl = W.make_config(name, seed=seed)
+    rows = _sample_rows(wl, 96, 7 + seed)
     O, L = oracle.cascade(wl, rows)
     wg = wl.to(DEV)
     plan = hb.CascadePlan.from_workload(wg)
@@ -261,20 +274,54 @@ def test_cascade_full_size_sampled(name):
 
 
 # ------------------------------------------------- bit-exact index probes
+def _nodes_of(wl, b):
+    """(level, node index, seq_begin, kv_len, offset of the node in b's
+    context) of every node covering sequence b, in level order."""
+    out, off = [], 0
+    for li, lv in enumerate(wl.levels):
+        for i, (sb, se, kl, _) in enumerate(lv.nodes.tolist()):
+            if sb <= b < se:
+                out.append((li, i, sb, kl, off))
+                off += kl
+                break
+    return out
+
+
 def _probe_targets(wl, where):
-    n = wl.seq_kv_len()
+    """Collision-free probe targets, one per sequence, by rule (no fallback):
+    the i-th sequence of a node probes token i-derived slots of it, so two
+    sequences never probe the same stored token.
+      first:     each sequence its first non-empty node, token i (every node's
+                 first token is probed by the node's first sequence);
+      last:      its last non-empty node, token kv_len - 1 - i;
+      page_edge: the node at level b mod depth, token i*ps + (ps - 1 if b is
+                 odd else 0); when that passes the node's end, the same edge of
+                 its private node;
+      level<k>:  its node at level k, token i (every node of level k probed)."""
     ps = wl.page_size
     tg = []
     for b in range(wl.B):
+        nodes = [n for n in _nodes_of(wl, b) if n[3] > 0]
         if where == "first":
-            t = 0 if b == 0 else None
+            li, _, sb, kl, off = nodes[0]
+            t = b - sb
         elif where == "last":
-            t = n[b] - 1
+            li, _, sb, kl, off = nodes[-1]
+            t = kl - 1 - (b - sb)
         elif where == "page_edge":
-            t = min(n[b] - 1, (b % max(1, n[b] // ps)) * ps + (ps - 1 if b % 2 else 0))
+            li, _, sb, kl, off = nodes[b % len(nodes)]
+            t = (b - sb) * ps + (ps - 1 if b % 2 else 0)
+            if t >= kl:
+                li, _, sb, kl, off = next(n for n in nodes if n[2] == b and wl.levels[n[0]].nodes[n[1], 1] == b + 1)
+                t = min(kl - 1, ps - 1 if b % 2 else 0)
+        elif where.startswith("level"):
+            k = int(where[5:])
+            li, _, sb, kl, off = next(n for n in nodes if n[0] == k)
+            t = b - sb
         else:
             raise ValueError(where)
-        tg.append(t)
+        assert 0 <= t < kl, (where, b, t, kl)
+        tg.append(off + t)
     return tg
 
 
@@ -306,28 +353,8 @@ def _distinct_targets(wl, seed):
     return tg
 
 
-@pytest.mark.parametrize("name,kw", [
-    ("tiny", {}),
-    ("llama3_8b", dict(B=16, prefix=512)),
-    ("tree2", dict(B=32, prefix=256)),
-    ("codellama13b", dict(B=8, prefix=256)),
-])
-@pytest.mark.parametrize("mode", ["random", "last", "page_edge"])
-def test_probe_bit_exact(name, kw, mode):
-    wl = W.make_config(name, seed=11, **kw)
-    if mode == "random":
-        tg = _distinct_targets(wl, 3)
-    else:
-        tg = _probe_targets(wl, mode)
-        if mode == "last" or mode == "page_edge":
-            # make shared-node collisions impossible: fall back to distinct
-            # random targets for sequences whose pick lands in a shared node
-            # already used
-            try:
-                W.apply_probe(W.make_config(name, seed=11, **kw), tg)
-            except ValueError:
-                tg = _distinct_targets(wl, 5)
-    W.apply_probe(wl, tg)
+def _run_probe(wl, tg, what):
+    W.apply_probe(wl, tg)  # raises if two targets share a stored token
     wg = wl.to(DEV)
     plan = hb.CascadePlan.from_workload(wg)
     out, lse = plan.decode(wg.q, wl.scale)  # bf16 output
@@ -337,7 +364,42 @@ def test_probe_bit_exact(name, kw, mode):
         want = W.probe_expected(b, wl.d)
         got = out[b]
         bad = (got.view(torch.int16) != want.view(torch.int16)[None, :]).any(dim=1)
-        assert not bad.any(), f"{name} {mode}: sequence {b} (target {tg[b]}) heads {bad.nonzero().flatten().tolist()}"
+        assert not bad.any(), f"{what}: sequence {b} (target {tg[b]}) heads {bad.nonzero().flatten().tolist()}"
+
+
+PROBE_CASES = [
+    ("tiny", {}),
+    ("llama3_8b", dict(B=16, prefix=512)),
+    ("tree2", dict(B=32, prefix=256)),
+    ("codellama13b", dict(B=8, prefix=256)),
+    ("doc_streams", dict(B=24, prefix=320)),
+]
+
+
+@pytest.mark.parametrize("name,kw", PROBE_CASES)
+@pytest.mark.parametrize("mode", ["random", "first", "last", "page_edge"])
+def test_probe_bit_exact(name, kw, mode):
+    wl = W.make_config(name, seed=11, **kw)
+    tg = _distinct_targets(wl, 3) if mode == "random" else _probe_targets(wl, mode)
+    _run_probe(wl, tg, f"{name} {mode}")
+
+
+@pytest.mark.parametrize("level", [0, 1, 2])
+def test_probe_bit_exact_every_node_of_each_tree2_level(level):
+    """tree2 at B=32: level 0 (one node), level 1 (8 nodes of 4 sequences),
+    level 2 (the suffixes): every node's tokens probed by its sequences."""
+    wl = W.make_config("tree2", seed=12, B=32, prefix=256)
+    tg = _probe_targets(wl, f"level{level}")
+    _run_probe(wl, tg, f"tree2 level {level}")
+
+
+@pytest.mark.parametrize("mode", ["first", "last", "page_edge"])
+def test_probe_bit_exact_codellama13b_full_batch(mode):
+    """B = 256 sequences at G = 1: the shared node's 256 query rows run on
+    the tensor cores (two 128-row blocks), probed bit for bit."""
+    wl = W.make_config("codellama13b", seed=13, prefix=1024)
+    tg = _probe_targets(wl, mode)
+    _run_probe(wl, tg, f"codellama13b B=256 {mode}")
 
 
 def test_probe_bit_exact_paged_decode():
@@ -675,3 +737,74 @@ def test_decode_loop_full_size_sampled():
         _check(o, l, O, L, f"full-size decode loop step {s}")
     _status_ok(plan.ws)
     assert torch.equal(plan.suffix_len.cpu(), host.levels[-1].nodes[:, 2])
+
+
+# ------------------------------------------------ general forests (deep, many pools, narrow nodes)
+def _forest(seed, B=24, ps=16):
+    """Two system prompts, nested shared chunks down to pairs and triples of
+    sequences, private suffixes (ChunkAttention's realistic trees)."""
+    h = B // 2
+    lvl0 = [(0, h, 128), (h, B, 96)]
+    lvl1 = [(0, 6, 64), (6, 12, 48), (12, 18, 32), (18, 24, 64)]
+    lvl2 = [(b, min(b + 3, B), 16 * (1 + (b // 3) % 3)) for b in range(0, B, 3)]
+    lvl3 = [(b, b + 2, 32) for b in range(0, B, 4)]
+    return W.build_cascade(f"forest{seed}", B=B, Hq=8, Hkv=2, d=64, page_size=ps,
+                           shared=[lvl0, lvl1, lvl2, lvl3], suffix_range=(1, 40), seed=seed)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_cascade_forest_with_narrow_nodes(seed):
+    """Narrow shared nodes joined into their sequences' nodes (read per
+    sequence), wider ones on the tensor cores, every row against the oracle."""
+    wl = _forest(seed)
+    items = hb.hp_cascade_plan_items(hb._levels_of(wl), wl.B, wl.Hq, wl.Hkv, wl.d)
+    assert all(it["n_seq"] == 1 or it["n_seq"] > 3 for it in items)
+    O, L = oracle.cascade(wl)
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    out, lse = plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
+    _status_ok(plan.ws)
+    _check(out, lse, O, L, f"forest {seed}")
+
+
+def test_cascade_deep_chunk_tree_21_levels():
+    """A 64-token prompt shared by all sequences, then each sequence's keys
+    as a chain of 16-token chunk nodes, one level per chunk (21 levels)."""
+    B, ps = 5, 16
+    lens = [0, 3, 7, 12, 19]
+    levels = [[(0, B, 64)]] + [[(b, b + 1, ps) for b in range(B) if lens[b] > c] for c in range(max(lens))]
+    levels = [lv for lv in levels if lv]
+    wl = W.build_cascade("chunks", B=B, Hq=8, Hkv=2, d=64, page_size=ps, shared=levels, suffix_lens=[5] * B, seed=3)
+    assert len(wl.levels) == 21
+    O, L = oracle.cascade(wl)
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    out, lse = plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
+    _status_ok(plan.ws)
+    _check(out, lse, O, L, "21-level chunk tree")
+
+
+@pytest.mark.parametrize("n_pools", [2, 5, 8])
+def test_cascade_levels_over_several_pools(n_pools):
+    """A 12-level tree whose levels live in n_pools distinct pool pairs
+    (copies of one pool: the values, and so the oracle, are the same); the
+    plan keeps one tensor-map slot per pool set."""
+    B = 16
+    shared = [[(0, B, 64)], [(0, 8, 48), (8, 16, 32)]] + \
+             [[(b, b + 4, 16 * (1 + l % 2)) for b in range(0, B, 4)] for l in range(4)] + \
+             [[(b, b + 1, 16) for b in range(B)] for _ in range(5)]
+    wl = W.build_cascade("pools", B=B, Hq=16, Hkv=4, d=128, page_size=16, shared=shared, suffix_range=(0, 30), seed=4)
+    assert len(wl.levels) == 12
+    O, L = oracle.cascade(wl)
+    wg = wl.to(DEV)
+    pools = [(wg.k_pool.clone(), wg.v_pool.clone()) for _ in range(n_pools)]
+    levels = []
+    for i, lv in enumerate(wg.levels):
+        kp, vp = pools[i % n_pools]
+        levels.append((kp.data_ptr(), vp.data_ptr(), wg.num_pages, wg.page_size, lv.nodes.tolist(),
+                       lv.page_ids.cpu().tolist()))
+    plan = hb.CascadePlan(levels, wl.B, wl.Hq, wl.Hkv, wl.d, device=DEV)
+    assert plan.info.num_levels == n_pools
+    out, lse = plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
+    _status_ok(plan.ws)
+    _check(out, lse, O, L, f"{n_pools} pools")

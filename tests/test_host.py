@@ -400,26 +400,54 @@ def test_single_sequence_chains_are_fused():
     assert {it["level"] for it in _check_plan_items(loop, capacity=64)} == {0, 1, 2}
 
 
-def test_chunkattention_fig2_private_chunks_are_planned_as_one():
-    """In ChunkAttention's Figure 2 tree, sequence 1 owns chunks C4 then C6
-    and sequence 2 owns C5 then C7 (one page each).  The context list keeps
-    them apart, as the page lists it; the planner walks each pair as one
-    node of two pages at C4's / C5's level, and sequence 0's single C3
-    stays as it is."""
-    pool = _pool()
-    g, levels, names = _fig2_levels(pool)
-    ps = 16
-    items = hb.hp_cascade_plan_items(levels, 3, 4, 4, 128, num_sms=152)
-    lvl = {names[k]: k[0] for k in names}
+def _fused_by_seq(items):
     by_seq = {}
     for it in items:
         if it["n_seq"] == 1:
             by_seq.setdefault(it["seq_begin"], set()).add((it["level"], max(
                 x["k1"] for x in items if x["n_seq"] == 1 and x["seq_begin"] == it["seq_begin"]
                 and x["level"] == it["level"])))
+    return by_seq
+
+
+def test_chunkattention_fig2_private_chunks_are_planned_as_one():
+    """In ChunkAttention's Figure 2 tree, sequence 1 owns chunks C4 then C6
+    and sequence 2 owns C5 then C7 (one page each).  The context list keeps
+    them apart, as the page lists it; with 64-token chunks and 32 KV heads
+    (re-reading a shared chunk per sequence costs more than a merge part)
+    the planner walks each private pair as one node of two pages at C4's /
+    C5's level, and sequence 0's single C3 stays as it is."""
+    pool = _pool()
+    ps = 64
+    g, levels, names = _fig2_levels(pool, ps=ps)
+    items = hb.hp_cascade_plan_items(levels, 3, 32, 32, 128, num_sms=152)
+    lvl = {names[k]: k[0] for k in names}
+    by_seq = _fused_by_seq(items)
     assert by_seq[0] == {(lvl["C3"], ps)}
     assert by_seq[1] == {(lvl["C4"], 2 * ps)}
     assert by_seq[2] == {(lvl["C5"], 2 * ps)}
+
+
+def test_chunkattention_fig2_narrow_shared_chunks_join_the_chains():
+    """The same tree with 16-token chunks and 4 KV heads: re-reading the
+    shared chunks C0, C1, C2 (three sequences each) per sequence costs less
+    than their merge parts, so each sequence becomes one node at C0's level:
+    C0 C1 C2 C3 for sequence 0, C0 C1 C2 C4 C6 and C0 C1 C2 C5 C7 for
+    sequences 1 and 2."""
+    pool = _pool()
+    ps = 16
+    g, levels, names = _fig2_levels(pool, ps=ps)
+    items = hb.hp_cascade_plan_items(levels, 3, 4, 4, 128, num_sms=152)
+    lvl = {names[k]: k[0] for k in names}
+    assert all(it["n_seq"] == 1 for it in items)
+    by_seq = _fused_by_seq(items)
+    assert by_seq == {0: {(lvl["C0"], 4 * ps)}, 1: {(lvl["C0"], 5 * ps)}, 2: {(lvl["C0"], 5 * ps)}}
+    # the chunks are read per sequence: no item covers two sequences
+    tab = hb.hp_cascade_plan_merge_table(levels, 3, 4, 4, 128, num_sms=152)
+    for row, parts in enumerate(tab):
+        b, h = divmod(row, 4)
+        mine = [it for it in items if it["seq_begin"] == b and it["kvh"] <= h < it["kvh"] + it["n_kvh"]]
+        assert len(parts) == len(mine)  # one part per key range of the sequence's single node
 
 
 def test_deep_trees_and_pool_slot_limit():

@@ -742,3 +742,32 @@ def test_deep_chunk_tree_replayed():
     Or, Lr = _replay_plan(wl)
     np.testing.assert_allclose(Or, O, atol=1e-12)
     np.testing.assert_allclose(Lr, L, atol=1e-12)
+
+
+def _realistic_forest(seed, B=24, ps=16):
+    """A ChunkAttention-style forest: two system prompts, each shared by half
+    of the sequences, then nested shared chunks down to pairs and triples of
+    sequences (narrow nodes), then private suffixes."""
+    h = B // 2
+    lvl0 = [(0, h, 128), (h, B, 96)]
+    lvl1 = [(0, 6, 64), (6, 12, 48), (12, 18, 32), (18, 24, 64)]
+    lvl2 = [(b, min(b + 3, B), 16 * (1 + (b // 3) % 3)) for b in range(0, B, 3)]
+    lvl3 = [(b, b + 2, 32) for b in range(0, B, 4)]
+    return W.build_cascade(f"forest{seed}", B=B, Hq=8, Hkv=2, d=64, page_size=ps,
+                           shared=[lvl0, lvl1, lvl2, lvl3], suffix_range=(1, 40), seed=seed)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_narrow_nodes_fused_into_chains_replayed(seed):
+    """Narrow shared nodes (2-3 sequences, short) are read by each of their
+    sequences inside its own node (fewer partial states, a few more bytes);
+    the replayed plan still equals the definition."""
+    from shared_prefix_decode_gb300 import binding as hb
+    wl = _realistic_forest(seed)
+    items = hb.hp_cascade_plan_items(hb._levels_of(wl), wl.B, wl.Hq, wl.Hkv, wl.d)
+    # no item reads a node of 2-3 sequences as a shared item: they all joined
+    assert all(it["n_seq"] == 1 or it["n_seq"] > 3 for it in items)
+    O, L = oracle.cascade(wl)
+    Or, Lr = _replay_plan(wl)
+    np.testing.assert_allclose(Or, O, atol=1e-12)
+    np.testing.assert_allclose(Lr, L, atol=1e-12)
