@@ -291,7 +291,10 @@ def parallel_prompting_figure(hb, dev, stream, peaks, dist) -> dict:
     questions U[32, 64]; each request's row read in place with the stream
     mask (hp_stream_decode) against the same requests in the cascade form
     (the document a node shared by the request's streams, each stream's
-    slots a private node).  Both read the same unique bytes."""
+    slots a private node) -- both read the same unique bytes -- and against
+    one request per question (per-sequence paged decode over the document
+    and the question's own slots: the document read once per question, the
+    page's prefix-caching baseline)."""
     import torch
     from shared_prefix_decode_gb300 import workloads as W
     R, P, doc, T = 2, 64, 8192, 64
@@ -305,7 +308,11 @@ def parallel_prompting_figure(hb, dev, stream, peaks, dist) -> dict:
         ws = hb.alloc_workspace(hb.stream_workspace_bytes(R, P, 32, 32, 128, rows.row_pages.shape[1], 16), dev)
         out = torch.empty(R * P, 32, 128, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(R * P, 32, dtype=torch.float32, device=dev)
-        sets.append({"req": req, "rows": rows, "tree": tree, "plan": plan, "q": q, "ws": ws, "out": out, "lse": lse})
+        pt, sl = W.full_page_tables(tree)
+        pt, sl = pt.to(dev), sl.to(dev)
+        ws_n = hb.alloc_workspace(hb.suffix_workspace_bytes(R * P, 32, 128, pt.shape[1], 16), dev)
+        sets.append({"req": req, "rows": rows, "tree": tree, "plan": plan, "q": q, "ws": ws, "out": out, "lse": lse,
+                     "pt": pt, "sl": sl, "ws_n": ws_n})
     nbytes = statistics.mean(int(s["rows"].row_len.sum()) * 32 * 128 * 4 for s in sets)
 
     def in_place(s):
@@ -317,7 +324,12 @@ def parallel_prompting_figure(hb, dev, stream, peaks, dist) -> dict:
 
     res = {"requests": R, "streams_per_request": P, "document_tokens": doc, "decode_step": T,
            "unique_kv_bytes": nbytes}
-    for name, fn in (("in_place_masked_rows", in_place), ("cascade_form", cascade)):
+    def per_question(s):
+        hb.hp_suffix_decode_paged(s["tree"].q, s["tree"].k_pool, s["tree"].v_pool, s["pt"], s["sl"], s["tree"].scale,
+                                  out=s["out"], lse=s["lse"], ws=s["ws_n"], stream=stream)
+
+    for name, fn in (("in_place_masked_rows", in_place), ("cascade_form", cascade),
+                     ("one_request_per_question", per_question)):
         with torch.cuda.stream(stream):
             for s in sets:
                 fn(s)
