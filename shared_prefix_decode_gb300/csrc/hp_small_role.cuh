@@ -77,6 +77,17 @@ struct StageMeta {
     int nvalid;  // valid keys of the chunk (0 when its page id was out of range)
     int first, last;
     int qslot;   // first chunk only: the item's Q rows are in this stage's Q slot
+    int pairs;   // the item has at least kPairChunks chunks (E4M3 consumers take them two at a time)
+};
+
+// Items of at least this many chunks are consumed two chunks per pass by the
+// E4M3 consumers (more independent work per warp); shorter ones one by one,
+// where waiting for a second stage costs more than the overlap gains.
+constexpr int kPairChunks = 12;
+
+template <int N>
+struct Int {
+    static constexpr int value = N;
 };
 
 // The geometry of one item.
@@ -246,6 +257,7 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 m.first = ch == 0;
                 m.last = ch + 1 == nchunks;
                 m.qslot = ch == 0 && qslot;
+                m.pairs = nchunks >= kPairChunks;
                 c.meta[st] = m;
                 mbar_arrive_expect_tx(bar, (Q8 ? 2 : 2 * kHalves) * a.nh * L::kHeadBox +
                                                (m.qslot ? kHalves * a.nh * a.G * 128 : 0) + (SM ? 128 : 0));
@@ -549,6 +561,7 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
 {
     using L = Layout<D, NC, S, QR, true>;
     static_assert(D == 128, "E4M3 pools: d = 128");
+    static_assert(S >= 2, "two stages held at once");
     constexpr int kKs = D / 16;  // k-steps of S^T = K Q^T
     constexpr int kMt = D / 16;  // m16 tiles of O^T
     constexpr float kDecode = 256.f;  // decoded code = value * 2^-8
@@ -565,16 +578,198 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
     const uint32_t hoff = (uint32_t)w * L::kHeadBox;  // this warp's head within a box
     int rows = 0;
     bool two = false;  // a second column tile (9..16 query rows)
-    for (uint32_t k = 0;; ++k) {
-        const uint32_t st = k % S;
-        if (!wait_warp(c.full0 + 8 * st, (k / S) & 1u))
+    // One pass over NU (1 or 2) consecutive chunks of an item, in stages
+    // st[0..NU): with two, their scores share one softmax update and their
+    // decoding and MMAs interleave.
+    auto pass = [&](auto nu, const uint32_t(&st)[2]) {
+        constexpr int NU = decltype(nu)::value;
+        uint32_t kst[NU], vst[NU];
+        int nvalid[NU];
+        float ksc[NU], vsc[NU];
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const uint32_t stage = c.sbase + st[u] * L::kStage;
+            kst[u] = stage + hoff;
+            vst[u] = stage + L::kChunk + hoff;
+            nvalid[u] = c.meta[st[u]].nvalid;
+            ksc[u] = ld_shared_f32(stage + 2 * L::kChunk + L::kQSlot + 4 * w);
+            vsc[u] = ld_shared_f32(stage + 2 * L::kChunk + L::kQSlot + 128 + 4 * w);
+            if (nvalid[u] < kChunk) {
+                // rows past the valid keys: zero this head's V codes so that
+                // 0 * (whatever the pool holds there) stays 0
+                uint8_t *vp = c.smem + (vst[u] - c.sbase);
+                const int nz = (kChunk - nvalid[u]) * 8;
+                for (int i = lane; i < nz; i += 32)
+                    *reinterpret_cast<uint4 *>(vp + (nvalid[u] + i / 8) * 128 + (i % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+            }
+        }
+        __syncwarp();
+
+        // S^T = K Q^T: rows = keys (g, g + 8), columns = query rows 2t, 2t+1;
+        // the k-steps in two halves of four.  With one chunk, even and odd
+        // k-steps accumulate separately (independent MMA chains).
+        constexpr int NA = NU == 1 ? 2 : NU;  // accumulators
+        float sc[NA][2][4];
+#pragma unroll
+        for (int u = 0; u < NA; ++u)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    sc[u][nt][e] = 0.f;
+#pragma unroll
+        for (int hk = 0; hk < 2; ++hk) {
+            uint4 kw[NU][2];  // [chunk][key row g | g + 8]: bytes 32t + 16hk .. +15
+#pragma unroll
+            for (int u = 0; u < NU; ++u) {
+                const int k0r = g, k1r = g + 8;
+                kw[u][0] = ld_shared_v4(kst[u] + k0r * 128 + (((2 * t + hk) ^ (k0r & 7)) << 4));
+                kw[u][1] = ld_shared_v4(kst[u] + k1r * 128 + (((2 * t + hk) ^ (k1r & 7)) << 4));
+            }
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+                const int ks = 4 * hk + kq;
+#pragma unroll
+                for (int u = 0; u < NU; ++u) {
+                    auto word = [&](const uint4 &v) {
+                        return kq == 0 ? v.x : kq == 1 ? v.y : kq == 2 ? v.z : v.w;
+                    };
+                    uint32_t ak[4];
+                    e4m3x4_to_f16(word(kw[u][0]), ak[0], ak[2]);
+                    e4m3x4_to_f16(word(kw[u][1]), ak[1], ak[3]);
+                    const int acc = NU == 1 ? (ks & 1) : u;
+                    mma_f16_16816(sc[acc][0], ak, qb[ks][0][0], qb[ks][0][1]);
+                    if (two)
+                        mma_f16_16816(sc[acc][1], ak, qb[ks][1][0], qb[ks][1][1]);
+                }
+            }
+        }
+        if constexpr (NU == 1) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    sc[0][nt][e] += sc[1][nt][e];
+        }
+        // online softmax per query column over the pass's keys: element e of
+        // tile nt of chunk u is key (e < 2 ? g : g + 8) of the chunk, query
+        // row nt*8 + 2t + (e & 1); each chunk's K scale (and the decoding
+        // factor) multiplies its scores
+        float cs[NU], pv[NU];
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            cs[u] = a.scale_log2 * ksc[u] * kDecode;
+            if (vref == 0.f)
+                vref = vsc[u];
+        }
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+            pv[u] = vref != 0.f ? vsc[u] / vref : 0.f;  // 0: the chunk adds nothing to O
+        uint32_t pb[NU][2][2];  // [chunk][column tile]: P^T fragments (keys 0-7, 8-15)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            if (nt == 1 && !two)
+                break;
+            float x[NU][4];
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int u = 0; u < NU; ++u) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int key = e < 2 ? g : g + 8;
+                    x[u][e] = key < nvalid[u] ? sc[u][nt][e] * cs[u] : -INFINITY;
+                }
+                mx[0] = fmax3(mx[0], x[u][0], x[u][2]);
+                mx[1] = fmax3(mx[1], x[u][1], x[u][3]);
+            }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+            }
+            float al[2], ms[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float mn = fmaxf(mq[nt][i], mx[i]);
+                ms[i] = mn == -INFINITY ? 0.f : mn;  // all keys so far masked: nothing to scale
+                al[i] = fast_exp2(mq[nt][i] - ms[i]);
+                mq[nt][i] = mn;
+                lq[nt][i] *= al[i];
+            }
+            if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+#pragma unroll
+                for (int j = 0; j < kMt; ++j) {
+                    o[j][nt][0] *= al[0];
+                    o[j][nt][2] *= al[0];
+                    o[j][nt][1] *= al[1];
+                    o[j][nt][3] *= al[1];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < NU; ++u) {
+                float p[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    p[e] = fast_exp2(x[u][e] - ms[e & 1]);
+                lq[nt][0] += p[0] + p[2];
+                lq[nt][1] += p[1] + p[3];
+                // [keys g][queries 2t, 2t+1] per 8x8 block, transposed to
+                // [query g][keys 2t, 2t+1]: the B fragments of P^T
+                pb[u][nt][0] = movmatrix_trans(pack_f16x2(p[0] * pv[u], p[1] * pv[u]));
+                pb[u][nt][1] = movmatrix_trans(pack_f16x2(p[2] * pv[u], p[3] * pv[u]));
+            }
+        }
+
+        // O'^T += V^T P^T
+        const int ta = 2 * t, tb = 2 * t + 1;
+        uint4 vw[NU][4];
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            vw[u][0] = ld_shared_v4(vst[u] + ta * 128 + ((g ^ (ta & 7)) << 4));
+            vw[u][1] = ld_shared_v4(vst[u] + tb * 128 + ((g ^ (tb & 7)) << 4));
+            vw[u][2] = ld_shared_v4(vst[u] + (ta + 8) * 128 + ((g ^ (ta & 7)) << 4));
+            vw[u][3] = ld_shared_v4(vst[u] + (tb + 8) * 128 + ((g ^ (tb & 7)) << 4));
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+            for (int u = 0; u < NU; ++u) {
+                auto word = [&](const uint4 &v) { return q4 == 0 ? v.x : q4 == 1 ? v.y : q4 == 2 ? v.z : v.w; };
+                const uint32_t A = word(vw[u][0]), B = word(vw[u][1]), C = word(vw[u][2]), E = word(vw[u][3]);
+                // m-tiles 2q4 and 2q4+1: columns 16g + 4q4 + (0, 1) and (2, 3)
+                uint32_t a0[4], a1[4];
+                e4m3x4_to_f16(__byte_perm(A, B, 0x5410), a0[0], a0[1]);
+                e4m3x4_to_f16(__byte_perm(C, E, 0x5410), a0[2], a0[3]);
+                e4m3x4_to_f16(__byte_perm(A, B, 0x7632), a1[0], a1[1]);
+                e4m3x4_to_f16(__byte_perm(C, E, 0x7632), a1[2], a1[3]);
+                mma_f16_16816(o[2 * q4][0], a0, pb[u][0][0], pb[u][0][1]);
+                mma_f16_16816(o[2 * q4 + 1][0], a1, pb[u][0][0], pb[u][0][1]);
+                if (two) {
+                    mma_f16_16816(o[2 * q4][1], a0, pb[u][1][0], pb[u][1][1]);
+                    mma_f16_16816(o[2 * q4 + 1][1], a1, pb[u][1][0], pb[u][1][1]);
+                }
+            }
+        }
+        // release the stages to the producer
+        __syncwarp();
+        if (lane == 0)
+#pragma unroll
+            for (int u = 0; u < NU; ++u)
+                mbar_arrive(c.empty0 + 8 * st[u]);
+    };
+
+    for (uint32_t k = 0;;) {
+        const uint32_t st0 = k % S;
+        if (!wait_warp(c.full0 + 8 * st0, (k / S) & 1u))
             break;
-        const StageMeta m = c.meta[st];
+        const StageMeta m = c.meta[st0];
         if (m.n_seq < 0)
             break;  // sentinel: the producer's walk is over
         const int kvh = m.kvh0 + w;
-        const uint32_t stage = c.sbase + st * L::kStage;
         if (m.first) {
+            const uint32_t stage = c.sbase + st0 * L::kStage;
             rows = m.n_seq * a.G;
             two = rows > 8;
 #pragma unroll
@@ -616,138 +811,20 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
                 mq[nt][0] = mq[nt][1] = -INFINITY, lq[nt][0] = lq[nt][1] = 0.f;
             vref = 0.f;
         }
-        const uint32_t kst = stage + hoff;
-        const uint32_t vst = stage + L::kChunk + hoff;
-        const float ksc = ld_shared_f32(stage + 2 * L::kChunk + L::kQSlot + 4 * w);
-        const float vsc = ld_shared_f32(stage + 2 * L::kChunk + L::kQSlot + 128 + 4 * w);
-        const int nvalid = m.nvalid;
-        if (nvalid < kChunk) {
-            // rows past the valid keys: zero this head's V codes so that
-            // 0 * (whatever the pool holds there) stays 0
-            uint8_t *vp = c.smem + (vst - c.sbase);
-            const int nz = (kChunk - nvalid) * 8;
-            for (int i = lane; i < nz; i += 32)
-                *reinterpret_cast<uint4 *>(vp + (nvalid + i / 8) * 128 + (i % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
+        // a long item's chunk that is not its last: its successor is in the
+        // next stage
+        const bool pair = m.pairs && !m.last;
+        const uint32_t st[2] = {st0, (k + 1) % S};
+        if (pair && !wait_warp(c.full0 + 8 * st[1], ((k + 1) / S) & 1u))
+            break;
+        const bool last = pair ? c.meta[st[1]].last : m.last;
+        if (pair)
+            pass(Int<2>{}, st);
+        else
+            pass(Int<1>{}, st);
+        k += pair ? 2u : 1u;
 
-        // S^T = K Q^T: rows = keys (g, g + 8), columns = query rows 2t, 2t+1
-        float sc[2][4];
-        {
-            const int k0r = g, k1r = g + 8;
-            const uint4 ka = ld_shared_v4(kst + k0r * 128 + (((2 * t) ^ (k0r & 7)) << 4));
-            const uint4 kb = ld_shared_v4(kst + k0r * 128 + (((2 * t + 1) ^ (k0r & 7)) << 4));
-            const uint4 kc = ld_shared_v4(kst + k1r * 128 + (((2 * t) ^ (k1r & 7)) << 4));
-            const uint4 kd = ld_shared_v4(kst + k1r * 128 + (((2 * t + 1) ^ (k1r & 7)) << 4));
-            const uint32_t w0[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-            const uint32_t w1[8] = {kc.x, kc.y, kc.z, kc.w, kd.x, kd.y, kd.z, kd.w};
-            float sb[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    sc[nt][e] = sb[nt][e] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < kKs; ++ks) {
-                uint32_t ak[4];
-                e4m3x4_to_f16(w0[ks], ak[0], ak[2]);
-                e4m3x4_to_f16(w1[ks], ak[1], ak[3]);
-                mma_f16_16816((ks & 1) ? sb[0] : sc[0], ak, qb[ks][0][0], qb[ks][0][1]);
-                if (two)
-                    mma_f16_16816((ks & 1) ? sb[1] : sc[1], ak, qb[ks][1][0], qb[ks][1][1]);
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    sc[nt][e] += sb[nt][e];
-        }
-        // online softmax per query column: element e of tile nt is key
-        // (e < 2 ? g : g + 8), query row nt*8 + 2t + (e & 1); the chunk's K
-        // scale (and the decoding factor) multiplies the scores
-        const float cs = a.scale_log2 * ksc * kDecode;
-        if (vref == 0.f)
-            vref = vsc;
-        const float pv = vref != 0.f ? vsc / vref : 0.f;  // 0: the chunk adds nothing to O
-        uint32_t pb[2][2];  // P^T fragments of each column tile (keys 0-7, 8-15)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            if (nt == 1 && !two)
-                break;
-            float x[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int key = e < 2 ? g : g + 8;
-                x[e] = key < nvalid ? sc[nt][e] * cs : -INFINITY;
-            }
-            float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
-                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
-            }
-            float al[2], ms[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float mn = fmaxf(mq[nt][i], mx[i]);
-                ms[i] = mn == -INFINITY ? 0.f : mn;  // all keys so far masked: nothing to scale
-                al[i] = fast_exp2(mq[nt][i] - ms[i]);
-                mq[nt][i] = mn;
-                lq[nt][i] *= al[i];
-            }
-            if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
-#pragma unroll
-                for (int j = 0; j < kMt; ++j) {
-                    o[j][nt][0] *= al[0];
-                    o[j][nt][2] *= al[0];
-                    o[j][nt][1] *= al[1];
-                    o[j][nt][3] *= al[1];
-                }
-            }
-            float p[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                p[e] = fast_exp2(x[e] - ms[e & 1]);
-            lq[nt][0] += p[0] + p[2];
-            lq[nt][1] += p[1] + p[3];
-            // [keys g][queries 2t, 2t+1] per 8x8 block, transposed to
-            // [query g][keys 2t, 2t+1]: the B fragments of P^T
-            pb[nt][0] = movmatrix_trans(pack_f16x2(p[0] * pv, p[1] * pv));
-            pb[nt][1] = movmatrix_trans(pack_f16x2(p[2] * pv, p[3] * pv));
-        }
-
-        // O'^T += V^T P^T
-        {
-            const int ta = 2 * t, tb = 2 * t + 1;
-            const uint4 va = ld_shared_v4(vst + ta * 128 + ((g ^ (ta & 7)) << 4));
-            const uint4 vb = ld_shared_v4(vst + tb * 128 + ((g ^ (tb & 7)) << 4));
-            const uint4 vc = ld_shared_v4(vst + (ta + 8) * 128 + ((g ^ (ta & 7)) << 4));
-            const uint4 vd = ld_shared_v4(vst + (tb + 8) * 128 + ((g ^ (tb & 7)) << 4));
-            const uint32_t A[4] = {va.x, va.y, va.z, va.w}, B[4] = {vb.x, vb.y, vb.z, vb.w};
-            const uint32_t C[4] = {vc.x, vc.y, vc.z, vc.w}, E[4] = {vd.x, vd.y, vd.z, vd.w};
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                // m-tiles 2q4 and 2q4+1: columns 16g + 4q4 + (0, 1) and (2, 3)
-                uint32_t a0[4], a1[4];
-                e4m3x4_to_f16(__byte_perm(A[q4], B[q4], 0x5410), a0[0], a0[1]);
-                e4m3x4_to_f16(__byte_perm(C[q4], E[q4], 0x5410), a0[2], a0[3]);
-                e4m3x4_to_f16(__byte_perm(A[q4], B[q4], 0x7632), a1[0], a1[1]);
-                e4m3x4_to_f16(__byte_perm(C[q4], E[q4], 0x7632), a1[2], a1[3]);
-                mma_f16_16816(o[2 * q4][0], a0, pb[0][0], pb[0][1]);
-                mma_f16_16816(o[2 * q4 + 1][0], a1, pb[0][0], pb[0][1]);
-                if (two) {
-                    mma_f16_16816(o[2 * q4][1], a0, pb[1][0], pb[1][1]);
-                    mma_f16_16816(o[2 * q4 + 1][1], a1, pb[1][0], pb[1][1]);
-                }
-            }
-        }
-        // release the stage to the producer
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(c.empty0 + 8 * st);
-
-        if (m.last) {
+        if (last) {
             const int base = m.part_row + w * rows;  // this head's rows
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
