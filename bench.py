@@ -604,25 +604,40 @@ def main():
         roofline["traffic_note"] = tr.get("note", "")
 
     # --------------------------------------------------------------- e2e
+    # The step as a caller with host-resident queries runs it:
+    # hp_cascade_decode_host reads each step's q from pinned host memory
+    # (copy-in kernel) and the merge stores O and LSE into pinned host memory.
     h2d = sets[0]["wl"].q.numel() * 2
     d2h = sets[0]["res"].numel()
+    ws_host = hb.alloc_workspace(max(hb.host_workspace_bytes(s["plan"]) for s in sets), dev)
     for s in sets:
-        s["q_host"] = s["wl"].q.pin_memory()
+        wl = s["wl"]
+        s["q_host"] = wl.q.pin_memory()
         s["res_host"] = torch.empty(s["res"].shape, dtype=s["res"].dtype).pin_memory()
+        n_o = wl.B * wl.Hq * wl.d * 2
+        s["o_host"] = s["res_host"][:n_o].view(torch.bfloat16).view(wl.B, wl.Hq, wl.d)
+        s["lse_host"] = s["res_host"][n_o:].view(torch.float32).view(wl.B, wl.Hq)
 
     def e2e_step(s):
-        s["wg"].q.copy_(s["q_host"], non_blocking=True)
-        step(s, stream)
-        s["res_host"].copy_(s["res"], non_blocking=True)  # O and LSE
+        hb.hp_cascade_decode_host(s["plan"], s["q_host"], s["wl"].scale, s["o_host"], s["lse_host"], ws_host,
+                                  stream=stream)
 
     e2e_graphs = StepGraphs(e2e_step, sets, K, args.graph_max, stream)
     t_e2e, _, _ = timed_passes(e2e_graphs, min(args.warmup, 50), min(args.min_timed_s, 0.5), stream, dev, dist)
     st_e2e = pass_stats(t_e2e, K)
     us_e2e = st_e2e["median_us"]
+    # the host result equals the device-resident step's, bit for bit
+    step(sets[0], stream)
+    torch.cuda.synchronize()
+    same = bool(torch.equal(sets[0]["res_host"], sets[0]["res"].cpu()))
+    st = hb.hp_read_device_status(ws_host)
+    if st != hb.HP_OK:
+        raise RuntimeError(f"host-memory step: device status {hb.status_str(st)}")
     e2e = {"value": whole_job_tbs(world, bytes_per_step, us_e2e), "unit": "TB/s", "us_per_step": us_e2e,
            "min_us": st_e2e["min_us"], "p90_us": st_e2e["p90_us"],
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "path": "pinned host q -> device, hp_cascade_decode, device O and LSE (one buffer) -> pinned host"}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "equals_device_step": same,
+           "path": "hp_cascade_decode_host: q read from pinned host memory by a copy-in kernel, the step, "
+                   "O and LSE stored by the merge into pinned host memory"}
 
     # ------------------------------------------------ naive baseline
     naive = None

@@ -323,6 +323,28 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
                             int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
                             size_t ws_bytes, hp_stream_t stream);
 
+/* The same step for a caller whose queries arrive in, and whose outputs go
+ * to, page-locked host memory (a serving loop that receives the step's
+ * query vectors on the host and returns the attention output there): a
+ * copy-in kernel reads q from host memory over the host link into the
+ * workspace, the step runs on that copy, and the merge kernel stores O and
+ * LSE straight into the host buffers.  No copy engine is used, so the three
+ * kernels chain as programmatic dependents like the device-resident step;
+ * the copy-in kernel issues its host reads before it waits for the kernel
+ * ahead of it.  Not from the pages: their kernels take device tensors.
+ * q_host, out_host and lse_host (lse_host may be NULL) must be page-locked
+ * host memory (cudaHostAlloc / cudaHostRegister; HP_ERR_ARG otherwise, before
+ * any launch), laid out as in hp_cascade_decode.
+ * ws: >= hp_cascade_host_workspace_bytes(info) bytes (the step's workspace
+ * followed by a B x Hq x d bf16 copy of q).  The host buffers must not be
+ * written by the host while the step runs.  No host synchronisation, no
+ * allocation; graph-capturable. */
+size_t hp_cascade_host_workspace_bytes(const hp_plan_info *info);
+hp_status hp_cascade_decode_host(const void *plan_dev, const hp_plan_info *info, const void *q_host,
+                                 int64_t q_sb, int64_t q_sh, float scale, void *out_host, hp_dtype out_dt,
+                                 int64_t o_sb, int64_t o_sh, float *lse_host, int64_t lse_sb, void *ws,
+                                 size_t ws_bytes, hp_stream_t stream);
+
 /* The same step, recording caller-created CUDA events (cudaEvent_t handles;
  * any may be NULL) on `stream` -- as external event nodes when the stream is
  * being captured, so they time each replay: events[0] before the step's

@@ -75,6 +75,9 @@ _SIGNATURES = {
     "hp_cascade_plan": (c_i32, [ctypes.POINTER(HpTreeDesc), c_vp, c_sz, ctypes.POINTER(HpPlanInfo), c_vp]),
     "hp_cascade_decode": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_i64, c_i64, c_f32, c_vp,
                                   c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz, c_vp]),
+    "hp_cascade_host_workspace_bytes": (c_sz, [ctypes.POINTER(HpPlanInfo)]),
+    "hp_cascade_decode_host": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_i64, c_i64, c_f32, c_vp,
+                                       c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz, c_vp]),
     "hp_cascade_decode_profiled": (c_i32, [c_vp, ctypes.POINTER(HpPlanInfo), c_vp, c_i64, c_i64, c_f32, c_vp,
                                            c_i32, c_i64, c_i64, c_vp, c_i64, c_vp, c_sz, c_vp,
                                            ctypes.POINTER(c_vp)]),
@@ -489,6 +492,36 @@ def hp_cascade_decode(plan: CascadePlan, q: torch.Tensor, scale: float, out: Opt
         _dt(out.dtype), out.stride(0), out.stride(1), _ptr(lse), lse.stride(0), _ptr(ws), ws.numel(),
         _stream(stream)), "hp_cascade_decode")
     return out, lse
+
+
+def host_workspace_bytes(plan: CascadePlan) -> int:
+    n = int(library().hp_cascade_host_workspace_bytes(ctypes.byref(plan.info)))
+    if n == 0:
+        raise HpError(HP_ERR_ARG, "hp_cascade_host_workspace_bytes")
+    return n
+
+
+def hp_cascade_decode_host(plan: CascadePlan, q_host: torch.Tensor, scale: float, out_host: torch.Tensor,
+                           lse_host: Optional[torch.Tensor], ws: torch.Tensor, stream=None) -> None:
+    """One step with q read from, and O / LSE written to, page-locked host
+    tensors (``tensor.pin_memory()``); ws: a GPU byte tensor of at least
+    host_workspace_bytes(plan)."""
+    _need(q_host.dim() == 3 and tuple(q_host.shape) == (plan.B, plan.Hq, plan.d), "q shape does not match the plan")
+    _need(q_host.dtype == torch.bfloat16 and not q_host.is_cuda and q_host.is_pinned() and q_host.stride(2) == 1,
+          "q_host must be a pinned bf16 host tensor, d contiguous")
+    _need(tuple(out_host.shape) == tuple(q_host.shape) and out_host.dtype in (torch.bfloat16, torch.float32)
+          and not out_host.is_cuda and out_host.is_pinned() and out_host.stride(2) == 1,
+          "out_host must be a pinned [B][Hq][d] bf16 or f32 host tensor, d contiguous")
+    if lse_host is not None:
+        _need(tuple(lse_host.shape) == (plan.B, plan.Hq) and lse_host.dtype == torch.float32
+              and not lse_host.is_cuda and lse_host.is_pinned() and lse_host.stride(1) == 1,
+              "lse_host must be a pinned [B][Hq] f32 host tensor, heads contiguous")
+    _need(ws is not None and ws.dtype == torch.uint8 and ws.is_cuda, "workspace must be a uint8 GPU tensor")
+    _check(library().hp_cascade_decode_host(
+        _ptr(plan.plan), ctypes.byref(plan.info), _ptr(q_host), q_host.stride(0), q_host.stride(1), float(scale),
+        _ptr(out_host), _dt(out_host.dtype), out_host.stride(0), out_host.stride(1),
+        None if lse_host is None else _ptr(lse_host), 0 if lse_host is None else lse_host.stride(0), _ptr(ws),
+        ws.numel(), _stream(stream)), "hp_cascade_decode_host")
 
 
 def hp_cascade_decode_profiled(plan: CascadePlan, q: torch.Tensor, scale: float, out: torch.Tensor,

@@ -20,7 +20,7 @@ LIB = os.path.join(OUT_DIR, "libhp.so")
 OBJ_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["hp_api.cu", "hp_tc_kernel.cu", "hp_small_kernel.cu", "hp_merge_kernel.cu", "hp_noalloc.cu",
-           "hp_cascade_kernel.cu", "hp_append_kernel.cu", "hp_plan.cu"]
+           "hp_cascade_kernel.cu", "hp_append_kernel.cu", "hp_host_io_kernel.cu", "hp_plan.cu"]
 
 
 def nvcc() -> str:

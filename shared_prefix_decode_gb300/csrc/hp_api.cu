@@ -25,7 +25,7 @@ using namespace hp;
 
 namespace {
 
-constexpr int32_t kAbiVersion = 4;
+constexpr int32_t kAbiVersion = 5;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------- utilities
@@ -755,6 +755,36 @@ hp_status hp_cascade_loop_plan(const hp_tree_desc *desc, int32_t capacity, void 
     return cascade_plan_impl(desc, capacity, plan_dev, plan_bytes, info, stream);
 }
 
+// The arguments of a cascade step, checked before anything is launched;
+// fills *ext from the plan.
+static hp_status decode_args(const void *plan_dev, const hp_plan_info *info, const void *q, int64_t q_sb,
+                             int64_t q_sh, float scale, const void *out, hp_dtype out_dt, int64_t o_sb, int64_t o_sh,
+                             const void *ws, size_t ws_bytes, const int32_t *suffix_len, const void *k_new,
+                             const void *v_new, int64_t kv_sb, int64_t kv_sh, PlanExtent *ext)
+{
+    if (!plan_dev || !info || !q || !out || !ws || !std::isfinite(scale) || !(scale > 0.f))
+        return HP_ERR_ARG;
+    if (info->B < 1 || info->Hq < 1 || info->Hkv < 1 || info->Hq % info->Hkv || !supported_d(info->d))
+        return HP_ERR_ARG;
+    if (!q_layout_ok(q, q_sb, q_sh, info->B, info->Hq) || !out_layout_ok(out, out_dt, o_sb, o_sh, info->d))
+        return HP_ERR_UNSUPPORTED;
+    if (info->Hq / info->Hkv > kTcTile || info->grid < 1 || info->num_levels < 1 ||
+        info->num_levels > kMaxLevels || info->rec_stride < (int32_t)sizeof(RecHead) ||
+        info->rec_stride > kRecMaxBytes || info->rec_stride % 128)
+        return HP_ERR_ARG;
+    if (!plan_extent(plan_dev, info, ext))
+        return HP_ERR_ARG;
+    // a decode-loop plan runs with the current suffix lengths, a plain plan without
+    if ((ext->loop_capacity > 0) != (suffix_len != nullptr) || (suffix_len && !aligned(suffix_len, 4)))
+        return HP_ERR_ARG;
+    if (k_new && (!v_new || !aligned(k_new, 16) || !aligned(v_new, 16) || kv_sb <= 0 || kv_sh <= 0 || kv_sb % 8 ||
+                  kv_sh % 8))
+        return HP_ERR_UNSUPPORTED;
+    if (ws_bytes < (size_t)info->ws_bytes || !aligned(ws, 256))
+        return HP_ERR_WORKSPACE;
+    return HP_OK;
+}
+
 static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *info, const void *q,
                                      int64_t q_sb, int64_t q_sh, float scale, void *out, hp_dtype out_dt,
                                      int64_t o_sb, int64_t o_sh, float *lse, int64_t lse_sb, void *ws,
@@ -767,27 +797,11 @@ static hp_status cascade_decode_impl(const void *plan_dev, const hp_plan_info *i
             cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), reinterpret_cast<cudaStream_t>(stream),
                                      cudaEventRecordExternal);
     };
-    if (!plan_dev || !info || !q || !out || !ws || !std::isfinite(scale) || !(scale > 0.f))
-        return HP_ERR_ARG;
-    if (info->B < 1 || info->Hq < 1 || info->Hkv < 1 || info->Hq % info->Hkv || !supported_d(info->d))
-        return HP_ERR_ARG;
-    if (!q_layout_ok(q, q_sb, q_sh, info->B, info->Hq) || !out_layout_ok(out, out_dt, o_sb, o_sh, info->d))
-        return HP_ERR_UNSUPPORTED;
-    if (info->Hq / info->Hkv > kTcTile || info->grid < 1 || info->num_levels < 1 ||
-        info->num_levels > kMaxLevels || info->rec_stride < (int32_t)sizeof(RecHead) ||
-        info->rec_stride > kRecMaxBytes || info->rec_stride % 128)
-        return HP_ERR_ARG;
     PlanExtent ext;
-    if (!plan_extent(plan_dev, info, &ext))
-        return HP_ERR_ARG;
-    // a decode-loop plan runs with the current suffix lengths, a plain plan without
-    if ((ext.loop_capacity > 0) != (suffix_len != nullptr) || (suffix_len && !aligned(suffix_len, 4)))
-        return HP_ERR_ARG;
-    if (k_new && (!v_new || !aligned(k_new, 16) || !aligned(v_new, 16) || kv_sb <= 0 || kv_sh <= 0 || kv_sb % 8 ||
-                  kv_sh % 8))
-        return HP_ERR_UNSUPPORTED;
-    if (ws_bytes < (size_t)info->ws_bytes || !aligned(ws, 256))
-        return HP_ERR_WORKSPACE;
+    const hp_status st = decode_args(plan_dev, info, q, q_sb, q_sh, scale, out, out_dt, o_sb, o_sh, ws, ws_bytes,
+                                     suffix_len, k_new, v_new, kv_sb, kv_sh, &ext);
+    if (st != HP_OK)
+        return st;
     const WsLayout wl = ws_layout(info->n_part_rows, info->d);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *wsb = static_cast<uint8_t *>(ws);
@@ -881,6 +895,67 @@ hp_status hp_cascade_decode(const void *plan_dev, const hp_plan_info *info, cons
 {
     return cascade_decode_impl(plan_dev, info, q, q_sb, q_sh, scale, out, out_dt, o_sb, o_sh, lse, lse_sb, ws,
                                ws_bytes, stream, nullptr);
+}
+
+// The device-accessible address of page-locked host memory, or null when
+// p is not page-locked host memory (device memory, pageable memory, an
+// unknown pointer).
+static void *pinned_host_address(const void *p)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer leaves no sticky error behind
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+size_t hp_cascade_host_workspace_bytes(const hp_plan_info *info)
+{
+    if (!info || info->B < 1 || info->Hq < 1 || !supported_d(info->d) || info->ws_bytes < 1)
+        return 0;
+    return round_up((size_t)info->ws_bytes, 256) + (size_t)info->B * info->Hq * info->d * 2;
+}
+
+hp_status hp_cascade_decode_host(const void *plan_dev, const hp_plan_info *info, const void *q_host, int64_t q_sb,
+                                 int64_t q_sh, float scale, void *out_host, hp_dtype out_dt, int64_t o_sb,
+                                 int64_t o_sh, float *lse_host, int64_t lse_sb, void *ws, size_t ws_bytes,
+                                 hp_stream_t stream)
+{
+    if (!plan_dev || !info || !q_host || !out_host || !ws)
+        return HP_ERR_ARG;
+    const size_t need = hp_cascade_host_workspace_bytes(info);
+    if (need == 0)
+        return HP_ERR_ARG;
+    if (!q_layout_ok(q_host, q_sb, q_sh, info->B, info->Hq))
+        return HP_ERR_UNSUPPORTED;
+    if (ws_bytes < need || !aligned(ws, 256))
+        return HP_ERR_WORKSPACE;
+    void *q_dev = pinned_host_address(q_host);
+    void *out_dev = pinned_host_address(out_host);
+    void *lse_dev = lse_host ? pinned_host_address(lse_host) : nullptr;
+    if (!q_dev || !out_dev || (lse_host && !lse_dev) || !aligned(q_dev, 16))
+        return HP_ERR_ARG;
+    uint16_t *staged = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + round_up((size_t)info->ws_bytes, 256));
+    // the copy-in is launched only once the step's own arguments have been
+    // checked, so an argument error launches nothing
+    PlanExtent ext;
+    const hp_status st = decode_args(plan_dev, info, staged, (int64_t)info->Hq * info->d, info->d, scale, out_dev,
+                                     out_dt, o_sb, o_sh, ws, ws_bytes, nullptr, nullptr, nullptr, 0, 0, &ext);
+    if (st != HP_OK)
+        return st;
+    StageParams sp;
+    sp.src = static_cast<const uint16_t *>(q_dev);
+    sp.sb = q_sb;
+    sp.sh = q_sh;
+    sp.B = info->B;
+    sp.Hq = info->Hq;
+    sp.d = info->d;
+    sp.dst = staged;
+    if (launch_stage(sp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return HP_ERR_CUDA;
+    return cascade_decode_impl(plan_dev, info, staged, (int64_t)info->Hq * info->d, info->d, scale, out_dev, out_dt,
+                               o_sb, o_sh, static_cast<float *>(lse_dev), lse_sb, ws, ws_bytes, stream, nullptr);
 }
 
 hp_status hp_cascade_decode_loop(const void *plan_dev, const hp_plan_info *info, const int32_t *suffix_len,

@@ -259,6 +259,16 @@ struct CascadeParams {
 };
 
 // Decode-loop append: one token per sequence into its suffix pages.
+// Copy-in of host-resident queries (hp_host_io_kernel.cu): src rows
+// (b, h) at src + b * sb + h * sh (elements, device-accessible address of
+// page-locked host memory) to dst[(b * Hq + h) * d ..] in device memory.
+struct StageParams {
+    const uint16_t *src;
+    int64_t sb, sh;
+    int B, Hq, d;
+    uint16_t *dst;
+};
+
 struct AppendParams {
     const int32_t *leaf_tab;  // [B][leaf_stride] page ids (the plan's)
     int32_t leaf_stride, capacity, page_size, num_pages;
@@ -318,6 +328,7 @@ cudaError_t launch_merge(const MergeParams &p, int64_t out_rows, cudaStream_t s)
 cudaError_t launch_merge_dependent(const MergeParams &p, int64_t out_rows, cudaStream_t s);
 cudaError_t launch_cascade(const CascadeParams &p, int grid, int d, cudaStream_t s);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t s);
+cudaError_t launch_stage(const StageParams &p, cudaStream_t s);
 int cascade_heads_per_item(int Hkv);
 int cascade_q_rows();  // paged-role Q slot rows of the fused kernel
 int small_q_rows();    // Q slot rows of the standalone paged kernel

@@ -1,6 +1,7 @@
 """Host-side tests (no GPU): the C-ABI library loads and exports every symbol
 include/hp.h declares; the tree planner reproduces the pages' context list and
 rejects invalid trees before any launch."""
+import ctypes
 import json
 import os
 import re
@@ -30,7 +31,7 @@ def test_library_loads_and_exports_every_declared_symbol():
         assert hasattr(lib, name), f"{name} declared in hp.h but not exported"
     assert set(declared) == set(hb.exported_symbols())
     assert lib.hp_build_arch() == 103
-    assert lib.hp_abi_version() == 4
+    assert lib.hp_abi_version() == 5
 
 
 def test_status_strings():
@@ -551,3 +552,16 @@ def test_stream_workspace_sizes_and_rejections():
     assert hb.stream_workspace_bytes(0, 16, 32, 32, 128, 40, 16) == 0
     assert hb.stream_workspace_bytes(2, 16, 32, 32, 96, 40, 16) == 0
     assert hb.stream_workspace_bytes(2, 16, 64, 2, 128, 40, 16) == 0  # 32 query heads per KV head
+
+
+def test_host_workspace_bytes():
+    """hp_cascade_host_workspace_bytes: the step's workspace rounded up to
+    256 bytes, then a B x Hq x d bf16 copy of q; 0 for an invalid info."""
+    info = hb.HpPlanInfo()
+    info.B, info.Hq, info.Hkv, info.d, info.ws_bytes = 64, 32, 8, 128, 1000
+    assert hb.library().hp_cascade_host_workspace_bytes(ctypes.byref(info)) == 1024 + 64 * 32 * 128 * 2
+    info.ws_bytes = 4096
+    assert hb.library().hp_cascade_host_workspace_bytes(ctypes.byref(info)) == 4096 + 64 * 32 * 128 * 2
+    info.d = 96
+    assert hb.library().hp_cascade_host_workspace_bytes(ctypes.byref(info)) == 0
+    assert hb.library().hp_cascade_host_workspace_bytes(None) == 0
