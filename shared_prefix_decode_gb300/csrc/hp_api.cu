@@ -265,14 +265,14 @@ bool hp::encode_q_map(CUtensorMap *m, const void *q, int B, int Hq, int d, int64
 namespace {
 
 struct StreamGeo {
-    int ns_pg, n_sg, nh, spi, n_sblk, rows_item, split_len, n_split;
+    int ns_pg, n_sg, nh, sc, spi, n_sblk, rows_item, split_len, n_split;
     int64_t n_items, part_rows;
 };
 
 // Items of hp_stream_decode: consumer warps of an item serve (head, group of
 // ns_pg streams) pairs, at most 8; the streams of a request share one pass
 // over its row when their groups fit one item.
-StreamGeo stream_geo(int R, int P, int G, int Hkv, int max_len, int sms)
+StreamGeo stream_geo(int R, int P, int G, int Hkv, int d, int max_len, int sms)
 {
     StreamGeo g{};
     g.ns_pg = std::max(1, std::min(kSmallRows / G, P));
@@ -284,12 +284,29 @@ StreamGeo stream_geo(int R, int P, int G, int Hkv, int max_len, int sms)
             g.nh = nh;
             break;
         }
+    // an item of fewer than 8 heads takes several chunks per ring stage (at
+    // d = 128 two at most: four would not fit the consumers' registers)
+    g.sc = std::min(d == 128 ? 2 : 4, 8 / g.nh);
     g.spi = g.n_sg * g.ns_pg;
     g.n_sblk = (int)ceil_div(P, g.spi);
     g.rows_item = g.nh * g.n_sg * g.ns_pg * G;
     const int64_t units = (int64_t)R * (Hkv / g.nh) * g.n_sblk;
     const int64_t chunks = ceil_div(std::max(max_len, 1), kChunk);
-    const int64_t per = std::max<int64_t>(4, ceil_div(units * chunks, 2 * (int64_t)sms));
+    // The key splits: items go to the CTAs in turn, so the step lasts about
+    // ceil(items / SMs) items of ceil(chunks / splits) chunks each; take the
+    // split count with the shortest such makespan (ties: fewer splits, fewer
+    // partial states to merge), items of at least 4 chunks.
+    int64_t per = chunks, best = -1;
+    for (int64_t ns = 1; ns <= 256; ++ns) {
+        const int64_t p_ns = ceil_div(chunks, ns);
+        if (ns > 1 && p_ns < 4)
+            break;
+        const int64_t cost = ceil_div(units * ns, (int64_t)std::max(sms, 1)) * p_ns;
+        if (best < 0 || cost < best) {
+            best = cost;
+            per = p_ns;
+        }
+    }
     g.split_len = (int)(per * kChunk);
     g.n_split = (int)ceil_div(std::max(max_len, 1), g.split_len);
     g.n_items = units * g.n_split;
@@ -467,7 +484,7 @@ size_t hp_stream_workspace_bytes(int32_t R, int32_t P, int32_t Hq, int32_t Hkv, 
     if (R < 1 || P < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Hq / Hkv > kSmallRows || !supported_d(d) ||
         pt_stride < 1 || page_size < 16 || page_size % 16)
         return 0;
-    const StreamGeo g = stream_geo(R, P, Hq / Hkv, Hkv, pt_stride * page_size, device_sms());
+    const StreamGeo g = stream_geo(R, P, Hq / Hkv, Hkv, d, pt_stride * page_size, device_sms());
     return ws_layout(g.part_rows, d).total;
 }
 
@@ -497,7 +514,7 @@ hp_status hp_stream_decode(const void *q, int64_t q_sb, int64_t q_sh, int32_t R,
         return HP_ERR_UNSUPPORTED;
     const int G = Hq / Hkv;
     const int sms = device_sms();
-    const StreamGeo g = stream_geo(R, P, G, Hkv, pt_stride * page_size, sms);
+    const StreamGeo g = stream_geo(R, P, G, Hkv, d, pt_stride * page_size, sms);
     const WsLayout wl = ws_layout(g.part_rows, d);
     if (ws_bytes < wl.total || !aligned(ws, 256))
         return HP_ERR_WORKSPACE;
@@ -532,6 +549,7 @@ hp_status hp_stream_decode(const void *q, int64_t q_sb, int64_t q_sh, int32_t R,
     sp.nh = g.nh;
     sp.n_sg = g.n_sg;
     sp.ns_pg = g.ns_pg;
+    sp.sc = g.sc;
     sp.spi = g.spi;
     sp.n_sblk = g.n_sblk;
     sp.rows_item = g.rows_item;

@@ -213,6 +213,7 @@ struct StreamParams {
     int32_t n_sg, ns_pg;       // stream groups per item (one consumer warp each per head), streams per group
     int32_t spi, n_sblk;       // streams per item (n_sg * ns_pg), stream blocks per request
     int32_t rows_item;         // partial rows per item: nh * n_sg * ns_pg * G
+    int32_t sc;                // chunks of 16 keys per ring stage (1, 2 or 4; sc * nh <= 8)
     const uint16_t *q;
     int64_t q_sb, q_sh;
     uint16_t *part_o;
@@ -322,7 +323,6 @@ __host__ __device__ inline const T *plan_array(const PlanHeader *h, int64_t off)
 cudaError_t launch_tc(const TcParams &p, int grid, int d, cudaStream_t s);
 cudaError_t launch_small(const SmallParams &p, int grid, int d, cudaStream_t s);
 cudaError_t launch_stream(const StreamParams &p, int grid, int d, cudaStream_t s);
-size_t stream_smem_bytes(int d);
 cudaError_t launch_merge(const MergeParams &p, int64_t out_rows, cudaStream_t s);
 // The merge as a programmatic dependent launch of the preceding kernel.
 cudaError_t launch_merge_dependent(const MergeParams &p, int64_t out_rows, cudaStream_t s);

@@ -124,16 +124,20 @@ __global__ void __launch_bounds__(kThreadsSmall) hp_small_kernel(const __grid_co
 // w computes head w / n_sg for streams (w % n_sg) * ns_pg .. of the block.
 constexpr int kStreamConsumers = 8;
 constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;
-constexpr int kStreamStages = 3;
 
-template <int D>
+// A stage holds NC head-chunks (SC chunks of nh heads, SC * nh = NC): the
+// fewer the heads of an item, the smaller the stage and the more stages the
+// ring holds (up to 8), so the bytes in flight stay about the same.
+template <int D, int NC>
 struct StreamKernelLayout {
-    using R = smr::Layout<D, kStreamConsumers, kStreamStages, 0, false, true>;
+    static constexpr int kStageBytes = smr::Layout<D, NC, 1, 0, false, true>::kStage;
+    static constexpr int kStages = (200 * 1024 / kStageBytes) < 8 ? (200 * 1024 / kStageBytes) : 8;
+    using R = smr::Layout<D, NC, kStages, 0, false, true>;
     static constexpr int kBar = R::kEnd;
-    static constexpr int kMeta = kBar + 2 * kStreamStages * 8;
-    static constexpr int kZero = kMeta + 128;  // 16 zero bytes, then the abort flag
+    static constexpr int kMeta = kBar + 2 * kStages * 8;
+    static constexpr int kZero = kMeta + 512;  // 16 zero bytes, then the abort flag
     static constexpr int kBytes = kZero + 32;
-    static_assert(kStreamStages * (int)sizeof(smr::StageMeta) <= 128, "stage metadata");
+    static_assert(kStages >= 3 && kStages * (int)sizeof(smr::StageMeta) <= 512, "stage metadata");
 };
 
 struct StreamItems {
@@ -177,10 +181,11 @@ struct StreamItems {
     }
 };
 
-template <int D>
-__global__ void __launch_bounds__(kStreamThreads) hp_stream_kernel(const __grid_constant__ StreamParams p)
+template <int D, int SC, int NC>
+__global__ void __launch_bounds__(kStreamThreads, 1) hp_stream_kernel(const __grid_constant__ StreamParams p)
 {
-    using KL = StreamKernelLayout<D>;
+    using KL = StreamKernelLayout<D, NC>;
+    constexpr int kS = KL::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(kStreamThreads) hp_stream_kernel(const __grid_
     c.smem = smem;
     c.sbase = smem_u32(smem);
     c.full0 = c.sbase + KL::kBar;
-    c.empty0 = c.full0 + kStreamStages * 8;
+    c.empty0 = c.full0 + kS * 8;
     c.meta = reinterpret_cast<smr::StageMeta *>(smem + KL::kMeta);
     c.zero16 = c.sbase + KL::kZero;
     c.abort = reinterpret_cast<volatile int *>(smem + KL::kZero + 16);
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(kStreamThreads) hp_stream_kernel(const __grid_
     if (threadIdx.x < 4)
         reinterpret_cast<uint32_t *>(smem + KL::kZero)[threadIdx.x] = 0u;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStreamStages; ++s) {
+        for (int s = 0; s < kS; ++s) {
             mbar_init(c.full0 + 8 * s, 1);
             mbar_init(c.empty0 + 8 * s, (uint32_t)n_warps);
         }
@@ -213,26 +218,52 @@ __global__ void __launch_bounds__(kStreamThreads) hp_stream_kernel(const __grid_
     __syncthreads();
     const int n_items = p.n_items > (int)blockIdx.x ? (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     if (warp == kStreamConsumers)
-        smr::producer<D, kStreamConsumers, kStreamStages, 0, StreamItems, false, true>(
-            c, a, StreamItems{&p, (int)blockIdx.x, (int)gridDim.x}, n_items, lane);
+        smr::producer_rows<D, NC, kS, SC, StreamItems>(c, a, StreamItems{&p, (int)blockIdx.x, (int)gridDim.x},
+                                                       n_items, lane);
     else if (warp < n_warps)
-        smr::consumer<D, kStreamConsumers, kStreamStages, 0, true>(c, a, warp, lane);
+        smr::consumer_rows<D, NC, kS, SC>(c, a, warp, lane);
     __syncwarp();
 }
 
-template <int D>
+template <int D, int SC, int NC>
 cudaError_t launch_stream_d(const StreamParams &p, int grid, cudaStream_t s)
 {
-    static DeviceOnce once;
-    const int bytes = StreamKernelLayout<D>::kBytes + 1024;
-    static_assert(StreamKernelLayout<D>::kBytes + 1024 <= 227 * 1024, "shared memory per CTA");
+    static DeviceOnce once;  // per instantiation and device
+    const int bytes = StreamKernelLayout<D, NC>::kBytes + 1024;
+    static_assert(StreamKernelLayout<D, NC>::kBytes + 1024 <= 227 * 1024, "shared memory per CTA");
     cudaError_t e = once.run([bytes] {
-        return cudaFuncSetAttribute(hp_stream_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        return cudaFuncSetAttribute(hp_stream_kernel<D, SC, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    bytes);
     });
     if (e != cudaSuccess)
         return e;
-    hp_stream_kernel<D><<<grid, kStreamThreads, bytes, s>>>(p);
+    hp_stream_kernel<D, SC, NC><<<grid, kStreamThreads, bytes, s>>>(p);
     return cudaGetLastError();
+}
+
+// (chunks per stage, heads per item) as the planner chooses them: up to 8
+// head-chunks per stage, two chunks at most at d = 128 (four would not fit
+// the consumers' registers), four at d = 64.
+template <int D>
+cudaError_t launch_stream_sc(const StreamParams &p, int grid, cudaStream_t s)
+{
+    const int nc = p.sc * p.nh;
+    if (p.sc == 1 && nc == 8)
+        return launch_stream_d<D, 1, 8>(p, grid, s);
+    if (p.sc == 2 && nc == 8)
+        return launch_stream_d<D, 2, 8>(p, grid, s);
+    if (p.sc == 2 && nc == 4)
+        return launch_stream_d<D, 2, 4>(p, grid, s);
+    if constexpr (D == 128) {
+        if (p.sc == 2 && nc == 2)
+            return launch_stream_d<D, 2, 2>(p, grid, s);
+    } else {
+        if (p.sc == 4 && nc == 8)
+            return launch_stream_d<D, 4, 8>(p, grid, s);
+        if (p.sc == 4 && nc == 4)
+            return launch_stream_d<D, 4, 4>(p, grid, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <int D, bool Q8>
@@ -251,16 +282,13 @@ cudaError_t launch_small_d(const SmallParams &p, int grid, cudaStream_t s)
 
 }  // namespace
 
-size_t stream_smem_bytes(int d)
-{
-    return d == 64 ? StreamKernelLayout<64>::kBytes + 1024 : StreamKernelLayout<128>::kBytes + 1024;
-}
-
 cudaError_t launch_stream(const StreamParams &p, int grid, int d, cudaStream_t s)
 {
     if (grid <= 0)
         return cudaSuccess;
-    return d == 64 ? launch_stream_d<64>(p, grid, s) : launch_stream_d<128>(p, grid, s);
+    if (p.sc * p.nh > kStreamConsumers)
+        return cudaErrorInvalidValue;
+    return d == 64 ? launch_stream_sc<64>(p, grid, s) : launch_stream_sc<128>(p, grid, s);
 }
 
 size_t small_smem_bytes(int d, bool q8)

@@ -52,8 +52,8 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 // Shared memory of the role for NC consumer warps, S stages and a Q slot of
 // QR rows per stage; Q8: E4M3 pools (d = 128); SM: the stream mask of a
-// Parallel Prompting row (each stage also holds its 16 keys' stream ids and
-// positions).
+// Parallel Prompting row (each stage also holds its keys' stream ids and
+// positions: up to 8 chunks of 16 keys).
 template <int D, int NC, int S, int QR, bool Q8 = false, bool SM = false>
 struct Layout {
     static_assert(!Q8 || D == 128, "E4M3 pools: d = 128");
@@ -65,7 +65,7 @@ struct Layout {
     static constexpr int kQHalf = kQRows * 128;
     static constexpr int kQSlot = kHalves * kQHalf;
     static constexpr int kScales = Q8 ? 1024 : 0;  // Q8: K scales [NC], then V scales at +128 bytes (f32)
-    static constexpr int kMask = SM ? 1024 : 0;    // SM: slot stream ids [16], then positions at +64 (int32)
+    static constexpr int kMask = SM ? 1024 : 0;    // SM: stream ids of chunk c at 64c, positions at 512 + 64c (int32)
     static constexpr int kStage = 2 * kChunk + kQSlot + kScales + kMask;  // K, V, Q slot, scales, mask
     static constexpr int kEnd = S * kStage;
     static_assert(NC * 4 <= 128, "scale slots");
@@ -78,6 +78,7 @@ struct StageMeta {
     int first, last;
     int qslot;   // first chunk only: the item's Q rows are in this stage's Q slot
     int pairs;   // the item has at least kPairChunks chunks (E4M3 consumers take them two at a time)
+    int oob;     // rows stages: bit c set when chunk c's page id was out of range
 };
 
 // Items of at least this many chunks are consumed two chunks per pass by the
@@ -155,10 +156,10 @@ struct Args {
 // dependent load at the item's start), then closes the ring with a sentinel
 // stage (n_seq = -1, completed by a plain arrival) that tells the consumers
 // to stop.  All 32 lanes call it.
-template <int D, int NC, int S, int QR, class Src, bool Q8 = false, bool SM = false>
+template <int D, int NC, int S, int QR, class Src, bool Q8 = false>
 __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src &src, int n_items, int lane)
 {
-    using L = Layout<D, NC, S, QR, Q8, SM>;
+    using L = Layout<D, NC, S, QR, Q8>;
     constexpr int kHalves = D / 64;
     auto wait_warp = [&](uint32_t b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
@@ -260,7 +261,7 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 m.pairs = nchunks >= kPairChunks;
                 c.meta[st] = m;
                 mbar_arrive_expect_tx(bar, (Q8 ? 2 : 2 * kHalves) * a.nh * L::kHeadBox +
-                                               (m.qslot ? kHalves * a.nh * a.G * 128 : 0) + (SM ? 128 : 0));
+                                               (m.qslot ? kHalves * a.nh * a.G * 128 : 0));
             }
             __syncwarp();
             constexpr int kBoxLanes = Q8 ? 2 : 2 * kHalves;  // K and V boxes (one per column half for bf16)
@@ -273,11 +274,6 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
                 const int h = lane - kBoxLanes;
                 tma_load_3d(c.sbase + st * L::kStage + 2 * L::kChunk + h * L::kQHalf, a.map_q, bar, h * 64,
                             d.kvh0 * a.G, d.seq_begin);
-            } else if (SM && lane >= 8 && lane < 10) {
-                // the chunk's 16 stream ids (lane 8) and positions (lane 9)
-                const uint32_t mk = c.sbase + st * L::kStage + 2 * L::kChunk + L::kQSlot + L::kScales;
-                bulk_load_h(mk + (lane - 8) * 64, (lane == 8 ? d.slot_sid : d.slot_pos) + t, 64, bar,
-                            l2_evict_first());
             }
         }
     }
@@ -303,14 +299,10 @@ __device__ __forceinline__ void producer(const Ctx &c, const Args &a, const Src 
 
 // Consumer warp w (0 <= w < nh): processes the chunks in ring order until
 // the producer's sentinel stage.
-// SM (a Parallel Prompting row): warp w serves head w / n_sg and a group of
-// ns_pg streams; each key's visibility follows the row's stream mask
-// (Read Once, Answer Many, Section 3, Eq. 2): key k is visible to the query
-// of stream s at position p iff pos[k] <= p and (sid[k] = -1 or sid[k] = s).
-template <int D, int NC, int S, int QR, bool SM = false>
+template <int D, int NC, int S, int QR>
 __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int lane)
 {
-    using L = Layout<D, NC, S, QR, false, SM>;
+    using L = Layout<D, NC, S, QR>;
     constexpr int kHalves = D / 64;
     constexpr int kKs = D / 16;  // k-steps of the S MMA
     constexpr int kNt = D / 8;   // n8 tiles of O
@@ -322,10 +314,7 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     const int r0 = lane >> 2, r1 = r0 + 8;
     const int tq = 2 * (lane & 3);
-    const int hw = SM ? w / a.n_sg : w;     // head of the item's group
-    const int sj = SM ? w % a.n_sg : 0;     // stream group (SM)
-    const uint32_t hoff = (uint32_t)hw * L::kHeadBox;  // this warp's head within a box
-    int qsid0 = 0, qsid1 = 0, qpos0 = 0, qpos1 = 0;     // SM: rows r0 / r1's stream and position
+    const uint32_t hoff = (uint32_t)w * L::kHeadBox;  // this warp's head within a box
     for (uint32_t k = 0;; ++k) {
         const uint32_t st = k % S;
         if (!wait_warp(c.full0 + 8 * st, (k / S) & 1u))
@@ -333,10 +322,9 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
         const StageMeta m = c.meta[st];
         if (m.n_seq < 0)
             break;  // sentinel: the producer's walk is over
-        const int seq0 = SM ? m.seq_begin + sj * a.ns_pg : m.seq_begin;
-        const int n_seq = SM ? max(0, min(a.ns_pg, m.n_seq - sj * a.ns_pg)) : m.n_seq;
-        const int rows = n_seq * a.G;
-        const int kvh = m.kvh0 + hw;
+        const int seq0 = m.seq_begin;
+        const int rows = m.n_seq * a.G;
+        const int kvh = m.kvh0 + w;
         if (m.first && m.qslot) {
             // new item, Q rows in the stage: head w's rows are slot rows
             // w*G .. w*G+G-1; rows past G read a zero chunk
@@ -363,12 +351,6 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
                 q0 = a.q + (int64_t)(seq0 + r0 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r0 % a.G) * a.q_sh;
             if (r1 < rows)
                 q1 = a.q + (int64_t)(seq0 + r1 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r1 % a.G) * a.q_sh;
-            if (SM) {
-                qsid0 = r0 < rows ? __ldg(a.q_sid + seq0 + r0 / a.G) : 0;
-                qpos0 = r0 < rows ? __ldg(a.q_pos + seq0 + r0 / a.G) : 0;
-                qsid1 = r1 < rows ? __ldg(a.q_sid + seq0 + r1 / a.G) : 0;
-                qpos1 = r1 < rows ? __ldg(a.q_pos + seq0 + r1 / a.G) : 0;
-            }
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
                 qa[ks][0] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + ks * 16 + tq)) : 0u;
@@ -423,22 +405,6 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
             const int tk = tq + (e & 1);
             x[0][e] = tk < nvalid ? s0[e] * cs : -INFINITY;
             x[1][e] = tk + 8 < nvalid ? s1[e] * cs : -INFINITY;
-        }
-        if (SM) {
-            // the stream mask: this chunk's stream ids and positions
-            const uint32_t mk = c.sbase + st * L::kStage + 2 * L::kChunk + L::kQSlot + L::kScales;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int qs = e < 2 ? qsid0 : qsid1, qp = e < 2 ? qpos0 : qpos1;
-#pragma unroll
-                for (int tile = 0; tile < 2; ++tile) {
-                    const int key = tile * 8 + tq + (e & 1);
-                    const int sid = ld_shared_s32(mk + 4 * key);
-                    const int pos = ld_shared_s32(mk + 64 + 4 * key);
-                    if (!(pos <= qp && (sid == -1 || sid == qs)))
-                        x[tile][e] = -INFINITY;
-                }
-            }
         }
         float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
         float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
@@ -497,7 +463,7 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
             L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
             const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f;
             const float inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
-            const int base = m.part_row + w * (SM ? a.ns_pg * a.G : rows);  // this warp's rows
+            const int base = m.part_row + w * rows;  // this warp's rows
             if (r0 < rows) {
                 uint16_t *dst = a.part_o + (size_t)(base + r0) * D + tq;
 #pragma unroll
@@ -853,6 +819,379 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
                     if (g == 0)
                         a.part_lse[base + r] = Lq[i] > 0.f ? (mq[nt][i] + fast_log2(Lq[i])) * kLn2 : -INFINITY;
                 }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------ Parallel Prompting
+// The rows of hp_stream_decode (Read Once, Answer Many, Section 3): one KV
+// row per request holds the document, the questions and the interleaved
+// answers; each key carries a stream id (-1 for the document) and a
+// position, and a query of stream s at position p sees key k iff
+// pos[k] <= p and (sid[k] = -1 or sid[k] = s) (Eq. 2).  Consumer warp w of
+// an item serves KV head w / n_sg of the item's nh heads and the group of
+// ns_pg streams (w % n_sg); the group's 16 query rows see each chunk
+// through the mask.  A stage holds SC consecutive chunks of the row (SC *
+// nh <= NC head boxes), so that an item of few heads still keeps the ring's
+// bytes in flight and each warp has SC independent chunks per pass: chunk c
+// of a stage occupies head slots c * nh .. c * nh + nh - 1 of each column
+// half, its stream ids sit at mask + 64c and its positions at mask + 512 +
+// 64c.
+
+// Producer warp of the rows: as `producer`, a stage per SC chunks.  All 32
+// lanes call it.
+template <int D, int NC, int S, int SC, class Src>
+__device__ __forceinline__ void producer_rows(const Ctx &c, const Args &a, const Src &src, int n_items, int lane)
+{
+    using L = Layout<D, NC, S, 0, false, true>;
+    constexpr int kHalves = D / 64;
+    constexpr int kBoxes = 2 * kHalves;  // K and V boxes of one chunk
+    static_assert(SC >= 1 && 32 % SC == 0 && SC * kBoxes <= 16 && SC <= 8, "lanes and mask slots");
+    auto wait_warp = [&](uint32_t b, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
+    };
+    uint32_t k = 0;  // stages issued
+    bool ok = true;
+    bool prefetched = false;
+    for (int it = 0; ok && it < n_items; ++it) {
+        const Desc d = src(it, 0);
+        if (!d.valid)
+            continue;
+        if (!prefetched && lane == 0) {
+            prefetch_tensormap(d.map_k);
+            prefetch_tensormap(d.map_v);
+            prefetched = true;
+        }
+        const int nchunks = (d.k1 - d.k0 + kChunk - 1) / kChunk;
+        int pg = 0;
+        for (int ch0 = 0; ch0 < nchunks; ch0 += SC, ++k) {
+            if ((ch0 & 31) == 0) {  // page ids of the next 32 chunks, one per lane
+                const int cc = ch0 + lane;
+                pg = cc < nchunks ? d.pages[(d.k0 + cc * kChunk) / d.ps - d.pbase] : 0;
+            }
+            const uint32_t st = k % S;
+            if (k >= (uint32_t)S && !(ok = wait_warp(c.empty0 + 8 * st, ((k / S) - 1) & 1u)))
+                break;
+            const int n_sub = min(SC, nchunks - ch0);
+            // lane u < n_sub: the page of chunk u of the stage
+            const int cp = __shfl_sync(0xffffffffu, pg, (ch0 + lane) & 31);
+            const unsigned oob =
+                __ballot_sync(0xffffffffu, lane < n_sub && (unsigned)cp >= (unsigned)d.num_pages);
+            const int t0 = d.k0 + ch0 * kChunk;
+            const uint32_t bar = c.full0 + 8 * st;
+            const uint32_t stage = c.sbase + st * L::kStage;
+            if (lane == 0) {
+                if (oob)
+                    atomicOr(c.status, kStBounds);
+                StageMeta m{};
+                m.seq_begin = d.seq_begin;
+                m.n_seq = d.n_seq;
+                m.kvh0 = d.kvh0;
+                m.part_row = d.part_row;
+                m.nvalid = min(SC * kChunk, d.k1 - t0);
+                m.first = ch0 == 0;
+                m.last = ch0 + SC >= nchunks;
+                m.oob = (int)oob;
+                c.meta[st] = m;
+                mbar_arrive_expect_tx(bar, (uint32_t)n_sub * (kBoxes * a.nh * L::kHeadBox + 128));
+            }
+            __syncwarp();
+            // lanes 0 .. n_sub * kBoxes - 1: the K and V boxes of chunk
+            // lane / kBoxes; lanes 16 .. 16 + 2 n_sub - 1: its ids / positions
+            const int bu = lane < 16 ? lane / kBoxes : (lane - 16) >> 1;
+            int page = __shfl_sync(0xffffffffu, cp, bu < SC ? bu : 0);
+            if ((oob >> bu) & 1u)
+                page = d.num_pages;  // zero-filled boxes, chunk masked
+            if (lane < n_sub * kBoxes) {
+                const int b = lane % kBoxes, h = b % kHalves;
+                const bool is_v = b >= kHalves;
+                tma_load_4d_h(stage + (is_v ? L::kChunk : 0) + h * L::kHalf + bu * a.nh * L::kHeadBox,
+                              is_v ? d.map_v : d.map_k, bar, h * 64, (t0 + bu * kChunk) % d.ps, d.kvh0, page,
+                              l2_evict_first());
+            } else if (lane >= 16 && lane < 16 + 2 * n_sub) {
+                const bool is_pos = (lane - 16) & 1;
+                const uint32_t mk = stage + 2 * L::kChunk + L::kQSlot + L::kScales;
+                bulk_load_h(mk + (is_pos ? 512 : 0) + 64 * bu, (is_pos ? d.slot_pos : d.slot_sid) + t0 + bu * kChunk,
+                            64, bar, l2_evict_first());
+            }
+        }
+    }
+    // sentinel stage
+    {
+        const uint32_t st = k % S;
+        if (k >= (uint32_t)S)
+            wait_warp(c.empty0 + 8 * st, ((k / S) - 1) & 1u);
+        if (lane == 0) {
+            StageMeta m{};
+            m.n_seq = -1;
+            c.meta[st] = m;
+            mbar_arrive(c.full0 + 8 * st);
+        }
+        __syncwarp();
+        ++k;
+    }
+    // every copy issued has landed before the role ends
+    if (lane == 0)
+        for (uint32_t j = k > (uint32_t)S ? k - S : 0; j < k; ++j)
+            mbar_wait_drain(c.full0 + 8 * (j % S), (j / S) & 1u);
+}
+
+// Consumer warp w of the rows (w < nh * n_sg).  Per stage: S = Q K^T for
+// each of its SC chunks (independent MMA chains), the mask and the scale,
+// one online-softmax update over the stage's 16 SC keys, then P V per chunk.
+template <int D, int NC, int S, int SC>
+__device__ __forceinline__ void consumer_rows(const Ctx &c, const Args &a, int w, int lane)
+{
+    using L = Layout<D, NC, S, 0, false, true>;
+    constexpr int kHalves = D / 64;
+    constexpr int kKs = D / 16;  // k-steps of the S MMA
+    constexpr int kNt = D / 8;   // n8 tiles of O
+    auto wait_warp = [&](uint32_t b, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
+    };
+    uint32_t qa[kKs][4];
+    float o[kNt][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int r0 = lane >> 2, r1 = r0 + 8;
+    const int tq = 2 * (lane & 3);
+    const int hw = w / a.n_sg;  // head of the item's group
+    const int sj = w % a.n_sg;  // stream group
+    int qsid0 = 0, qsid1 = 0, qpos0 = 0, qpos1 = 0;  // rows r0 / r1's stream and position
+    int rows = 0;
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t st = k % S;
+        if (!wait_warp(c.full0 + 8 * st, (k / S) & 1u))
+            break;
+        const StageMeta m = c.meta[st];
+        if (m.n_seq < 0)
+            break;  // sentinel: the producer's walk is over
+        const int seq0 = m.seq_begin + sj * a.ns_pg;
+        rows = max(0, min(a.ns_pg, m.n_seq - sj * a.ns_pg)) * a.G;
+        if (m.first) {
+            // new item: query fragments (A operand, rows r0 / r1), their
+            // streams and positions, and the state
+            const int kvh = m.kvh0 + hw;
+            const uint16_t *q0 = nullptr, *q1 = nullptr;
+            if (r0 < rows)
+                q0 = a.q + (int64_t)(seq0 + r0 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r0 % a.G) * a.q_sh;
+            if (r1 < rows)
+                q1 = a.q + (int64_t)(seq0 + r1 / a.G) * a.q_sb + (int64_t)(kvh * a.G + r1 % a.G) * a.q_sh;
+            qsid0 = r0 < rows ? __ldg(a.q_sid + seq0 + r0 / a.G) : 0;
+            qpos0 = r0 < rows ? __ldg(a.q_pos + seq0 + r0 / a.G) : 0;
+            qsid1 = r1 < rows ? __ldg(a.q_sid + seq0 + r1 / a.G) : 0;
+            qpos1 = r1 < rows ? __ldg(a.q_pos + seq0 + r1 / a.G) : 0;
+#pragma unroll
+            for (int ks = 0; ks < kKs; ++ks) {
+                qa[ks][0] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + ks * 16 + tq)) : 0u;
+                qa[ks][1] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + ks * 16 + tq)) : 0u;
+                qa[ks][2] = q0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + ks * 16 + 8 + tq)) : 0u;
+                qa[ks][3] = q1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + ks * 16 + 8 + tq)) : 0u;
+            }
+#pragma unroll
+            for (int n = 0; n < kNt; ++n)
+                o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+        }
+        const uint32_t stage = c.sbase + st * L::kStage;
+        const uint32_t mk = stage + 2 * L::kChunk + L::kQSlot + L::kScales;
+        int valid[SC];  // valid keys of each chunk
+        bool zeroed = false;
+#pragma unroll
+        for (int u = 0; u < SC; ++u) {
+            valid[u] = ((m.oob >> u) & 1) ? 0 : max(0, min(kChunk, m.nvalid - u * kChunk));
+            if (valid[u] < kChunk) {
+                // rows past the valid keys (or a chunk the stage does not
+                // hold): zero this head's V so that 0 * (whatever the stage
+                // holds there) stays 0
+                uint8_t *vp = c.smem + (stage - c.sbase) + L::kChunk + (u * a.nh + hw) * L::kHeadBox;
+                const int nz = (kChunk - valid[u]) * 8 * kHalves;
+                for (int i = lane; i < nz; i += 32) {
+                    const int row = valid[u] + i / (8 * kHalves);
+                    const int rem = i % (8 * kHalves);
+                    const int h = rem >> 3, ch = rem & 7;
+                    *reinterpret_cast<uint4 *>(vp + h * L::kHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                zeroed = true;
+            }
+        }
+        if (zeroed) {
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // The stream mask first (rows r0: elements 0,1; rows r1: elements
+        // 2,3; key of tile t, element e: 8t + tq + (e & 1)): a chunk that no
+        // query row of this warp sees (another stream group's question or
+        // answer tokens) costs the warp no MMA.
+        bool see[SC][2][4];
+        bool vis_all = true;
+        unsigned vis = 0;
+#pragma unroll
+        for (int u = 0; u < SC; ++u) {
+            bool any = false;
+#pragma unroll
+            for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int key = tile * 8 + tq + j;
+                    const int sid = ld_shared_s32(mk + 64 * u + 4 * key);
+                    const int pos = ld_shared_s32(mk + 512 + 64 * u + 4 * key);
+                    const bool in = key < valid[u];
+                    see[u][tile][j] = in && pos <= qpos0 && (sid == -1 || sid == qsid0);
+                    see[u][tile][2 + j] = in && pos <= qpos1 && (sid == -1 || sid == qsid1);
+                    any = any || see[u][tile][j] || see[u][tile][2 + j];
+                }
+            const bool v = __any_sync(0xffffffffu, any);
+            vis |= (unsigned)v << u;
+            vis_all = vis_all && v;
+        }
+
+        // S = Q K^T per chunk: n8 tile 0 = keys 0-7, tile 1 = keys 8-15
+        float x[SC][2][4];
+        {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int tok = ri + ((mi >> 1) << 3);
+#pragma unroll
+            for (int u = 0; u < SC; ++u)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    x[u][0][e] = x[u][1][e] = 0.f;
+            auto s_chunk = [&](int u, int ks) {
+                const int dch = 2 * ks + (mi & 1);
+                const uint32_t kst = stage + (u * a.nh + hw) * L::kHeadBox;
+                const uint32_t addr = kst + (dch >> 3) * L::kHalf + tok * 128 + (((dch & 7) ^ (tok & 7)) << 4);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(addr, b0, b1, b2, b3);
+                mma_bf16_16816(x[u][0], qa[ks], b0, b1);
+                mma_bf16_16816(x[u][1], qa[ks], b2, b3);
+            };
+            if (vis_all) {  // every chunk: interleaved MMA chains
+#pragma unroll
+                for (int ks = 0; ks < kKs; ++ks)
+#pragma unroll
+                    for (int u = 0; u < SC; ++u)
+                        s_chunk(u, ks);
+            } else {
+#pragma unroll
+                for (int u = 0; u < SC; ++u)
+                    if ((vis >> u) & 1u)
+#pragma unroll
+                        for (int ks = 0; ks < kKs; ++ks)
+                            s_chunk(u, ks);
+            }
+        }
+        // scale and mask
+        const float cs = a.scale_log2;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < SC; ++u) {
+#pragma unroll
+            for (int tile = 0; tile < 2; ++tile) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    x[u][tile][e] = see[u][tile][e] ? x[u][tile][e] * cs : -INFINITY;
+                mx0 = fmax3(mx0, x[u][tile][0], x[u][tile][1]);
+                mx1 = fmax3(mx1, x[u][tile][2], x[u][tile][3]);
+            }
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;  // all keys so far masked: nothing to scale
+        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float a0 = fast_exp2(m0 - ms0), a1 = fast_exp2(m1 - ms1);
+        m0 = mn0;
+        m1 = mn1;
+        if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+            for (int n = 0; n < kNt; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
+            }
+            l0 *= a0;
+            l1 *= a1;
+        }
+        // the row sums take the weights before their rounding to bf16 for
+        // P V (the LSE keeps f32 accuracy)
+        uint32_t pa[SC][4];
+#pragma unroll
+        for (int u = 0; u < SC; ++u) {
+            float p[2][4];
+#pragma unroll
+            for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    p[tile][e] = fast_exp2(x[u][tile][e] - (e < 2 ? ms0 : ms1));
+            pa[u][0] = pack_bf16x2(p[0][0], p[0][1]);
+            pa[u][1] = pack_bf16x2(p[0][2], p[0][3]);
+            pa[u][2] = pack_bf16x2(p[1][0], p[1][1]);
+            pa[u][3] = pack_bf16x2(p[1][2], p[1][3]);
+            l0 += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+            l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+        }
+
+        // O += P V, chunk by chunk (the chunks this warp sees)
+        {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int tok = ri + ((mi & 1) << 3);
+            auto pv_chunk = [&](int u, int dp) {
+                const int dch = 2 * dp + (mi >> 1);
+                const uint32_t vst = stage + L::kChunk + (u * a.nh + hw) * L::kHeadBox;
+                const uint32_t addr = vst + (dch >> 3) * L::kHalf + tok * 128 + (((dch & 7) ^ (tok & 7)) << 4);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * dp], pa[u], b0, b1);
+                mma_bf16_16816(o[2 * dp + 1], pa[u], b2, b3);
+            };
+            if (vis_all) {
+#pragma unroll
+                for (int dp = 0; dp < D / 16; ++dp)
+#pragma unroll
+                    for (int u = 0; u < SC; ++u)
+                        pv_chunk(u, dp);
+            } else {
+#pragma unroll
+                for (int u = 0; u < SC; ++u)
+                    if ((vis >> u) & 1u)
+#pragma unroll
+                        for (int dp = 0; dp < D / 16; ++dp)
+                            pv_chunk(u, dp);
+            }
+        }
+        // release the stage to the producer
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(c.empty0 + 8 * st);
+
+        if (m.last) {
+            float L0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+            L0 += __shfl_xor_sync(0xffffffffu, L0, 2);
+            float L1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+            L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
+            const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f;
+            const float inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+            const int base = m.part_row + w * a.ns_pg * a.G;  // this warp's rows
+            if (r0 < rows) {
+                uint16_t *dst = a.part_o + (size_t)(base + r0) * D + tq;
+#pragma unroll
+                for (int n = 0; n < kNt; ++n)
+                    *reinterpret_cast<uint32_t *>(dst + n * 8) = pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
+                if ((lane & 3) == 0)
+                    a.part_lse[base + r0] = L0 > 0.f ? (m0 + fast_log2(L0)) * kLn2 : -INFINITY;
+            }
+            if (r1 < rows) {
+                uint16_t *dst = a.part_o + (size_t)(base + r1) * D + tq;
+#pragma unroll
+                for (int n = 0; n < kNt; ++n)
+                    *reinterpret_cast<uint32_t *>(dst + n * 8) = pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
+                if ((lane & 3) == 0)
+                    a.part_lse[base + r1] = L1 > 0.f ? (m1 + fast_log2(L1)) * kLn2 : -INFINITY;
             }
         }
     }
