@@ -272,7 +272,7 @@ struct StreamGeo {
 // Items of hp_stream_decode: consumer warps of an item serve (head, group of
 // ns_pg streams) pairs, at most 8; the streams of a request share one pass
 // over its row when their groups fit one item.
-StreamGeo stream_geo(int R, int P, int G, int Hkv, int d, int max_len, int sms)
+StreamGeo stream_geo(int R, int P, int G, int Hkv, int max_len, int sms)
 {
     StreamGeo g{};
     g.ns_pg = std::max(1, std::min(kSmallRows / G, P));
@@ -284,9 +284,8 @@ StreamGeo stream_geo(int R, int P, int G, int Hkv, int d, int max_len, int sms)
             g.nh = nh;
             break;
         }
-    // an item of fewer than 8 heads takes several chunks per ring stage (at
-    // d = 128 two at most: four would not fit the consumers' registers)
-    g.sc = std::min(d == 128 ? 2 : 4, 8 / g.nh);
+    // an item of fewer than 8 heads takes several chunks per ring stage
+    g.sc = std::min(4, 8 / g.nh);
     g.spi = g.n_sg * g.ns_pg;
     g.n_sblk = (int)ceil_div(P, g.spi);
     g.rows_item = g.nh * g.n_sg * g.ns_pg * G;
@@ -484,7 +483,7 @@ size_t hp_stream_workspace_bytes(int32_t R, int32_t P, int32_t Hq, int32_t Hkv, 
     if (R < 1 || P < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Hq / Hkv > kSmallRows || !supported_d(d) ||
         pt_stride < 1 || page_size < 16 || page_size % 16)
         return 0;
-    const StreamGeo g = stream_geo(R, P, Hq / Hkv, Hkv, d, pt_stride * page_size, device_sms());
+    const StreamGeo g = stream_geo(R, P, Hq / Hkv, Hkv, pt_stride * page_size, device_sms());
     return ws_layout(g.part_rows, d).total;
 }
 
@@ -514,7 +513,7 @@ hp_status hp_stream_decode(const void *q, int64_t q_sb, int64_t q_sh, int32_t R,
         return HP_ERR_UNSUPPORTED;
     const int G = Hq / Hkv;
     const int sms = device_sms();
-    const StreamGeo g = stream_geo(R, P, G, Hkv, d, pt_stride * page_size, sms);
+    const StreamGeo g = stream_geo(R, P, G, Hkv, pt_stride * page_size, sms);
     const WsLayout wl = ws_layout(g.part_rows, d);
     if (ws_bytes < wl.total || !aligned(ws, 256))
         return HP_ERR_WORKSPACE;

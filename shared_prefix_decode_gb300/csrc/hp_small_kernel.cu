@@ -122,8 +122,13 @@ __global__ void __launch_bounds__(kThreadsSmall) hp_small_kernel(const __grid_co
 // item is (request r, nh KV heads, a block of spi streams, a key range): the
 // row's chunks are loaded once for all the block's streams, and consumer warp
 // w computes head w / n_sg for streams (w % n_sg) * ns_pg .. of the block.
+// Warpgroup 0: the producer warp (warp 0) and three idle warps, which give
+// their registers to warpgroups 1 and 2: the eight consumer warps (4..11).
 constexpr int kStreamConsumers = 8;
-constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;
+constexpr int kStreamThreads = 384;
+constexpr uint32_t kStreamRegsLaunch = 168, kStreamRegsCtl = 56, kStreamRegsConsumer = 224;
+static_assert(128 * kStreamRegsCtl + 256 * kStreamRegsConsumer == kStreamThreads * kStreamRegsLaunch,
+              "register split");
 
 // A stage holds NC head-chunks (SC chunks of nh heads, SC * nh = NC): the
 // fewer the heads of an item, the smaller the stage and the more stages the
@@ -217,11 +222,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) hp_stream_kernel(const __gr
     }
     __syncthreads();
     const int n_items = p.n_items > (int)blockIdx.x ? (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-    if (warp == kStreamConsumers)
-        smr::producer_rows<D, NC, kS, SC, StreamItems>(c, a, StreamItems{&p, (int)blockIdx.x, (int)gridDim.x},
-                                                       n_items, lane);
-    else if (warp < n_warps)
-        smr::consumer_rows<D, NC, kS, SC>(c, a, warp, lane);
+    if (warp < 4) {
+        setmaxnreg_dec<kStreamRegsCtl>();
+        if (warp == 0)
+            smr::producer_rows<D, NC, kS, SC, StreamItems>(c, a, StreamItems{&p, (int)blockIdx.x, (int)gridDim.x},
+                                                           n_items, lane);
+    } else {
+        setmaxnreg_inc<kStreamRegsConsumer>();
+        if (warp - 4 < n_warps)
+            smr::consumer_rows<D, NC, kS, SC>(c, a, warp - 4, lane);
+    }
     __syncwarp();
 }
 
@@ -232,8 +242,15 @@ cudaError_t launch_stream_d(const StreamParams &p, int grid, cudaStream_t s)
     const int bytes = StreamKernelLayout<D, NC>::kBytes + 1024;
     static_assert(StreamKernelLayout<D, NC>::kBytes + 1024 <= 227 * 1024, "shared memory per CTA");
     cudaError_t e = once.run([bytes] {
-        return cudaFuncSetAttribute(hp_stream_kernel<D, SC, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    bytes);
+        cudaError_t r =
+            cudaFuncSetAttribute(hp_stream_kernel<D, SC, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (r != cudaSuccess)
+            return r;
+        cudaFuncAttributes fa;
+        if ((r = cudaFuncGetAttributes(&fa, hp_stream_kernel<D, SC, NC>)) != cudaSuccess)
+            return r;
+        // the register split assumes this allocation
+        return fa.numRegs == (int)kStreamRegsLaunch ? cudaSuccess : cudaErrorInvalidConfiguration;
     });
     if (e != cudaSuccess)
         return e;
@@ -242,8 +259,7 @@ cudaError_t launch_stream_d(const StreamParams &p, int grid, cudaStream_t s)
 }
 
 // (chunks per stage, heads per item) as the planner chooses them: up to 8
-// head-chunks per stage, two chunks at most at d = 128 (four would not fit
-// the consumers' registers), four at d = 64.
+// head-chunks per stage, at most four chunks.
 template <int D>
 cudaError_t launch_stream_sc(const StreamParams &p, int grid, cudaStream_t s)
 {
@@ -252,17 +268,10 @@ cudaError_t launch_stream_sc(const StreamParams &p, int grid, cudaStream_t s)
         return launch_stream_d<D, 1, 8>(p, grid, s);
     if (p.sc == 2 && nc == 8)
         return launch_stream_d<D, 2, 8>(p, grid, s);
-    if (p.sc == 2 && nc == 4)
-        return launch_stream_d<D, 2, 4>(p, grid, s);
-    if constexpr (D == 128) {
-        if (p.sc == 2 && nc == 2)
-            return launch_stream_d<D, 2, 2>(p, grid, s);
-    } else {
-        if (p.sc == 4 && nc == 8)
-            return launch_stream_d<D, 4, 8>(p, grid, s);
-        if (p.sc == 4 && nc == 4)
-            return launch_stream_d<D, 4, 4>(p, grid, s);
-    }
+    if (p.sc == 4 && nc == 8)
+        return launch_stream_d<D, 4, 8>(p, grid, s);
+    if (p.sc == 4 && nc == 4)
+        return launch_stream_d<D, 4, 4>(p, grid, s);
     return cudaErrorInvalidValue;
 }
 
