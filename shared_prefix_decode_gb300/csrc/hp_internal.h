@@ -55,6 +55,11 @@ constexpr uint32_t kPlanMagic = 0x31504C48u;  // "HLP1"
 constexpr int kTcTile = 128;                  // keys per tensor-core tile
 constexpr int kTcMaxRows = 256;               // query rows per tensor-core item (2 x M=128)
 constexpr int kSmallRows = 16;                // query rows per small item (one m16 tile)
+// E4M3 paged items of at least this many 16-key chunks are consumed two
+// chunks per pass (more independent work per consumer warp); shorter ones
+// chunk by chunk, where waiting for a second stage costs more than the
+// overlap gains.
+constexpr int kPairChunks = 12;
 constexpr int kChunk = 16;                    // keys per small-kernel chunk
 constexpr size_t kWsHeader = 256;             // status word + reserved
 // Partial attention states in the workspace: LSE as f32, O / l as bf16 (raw

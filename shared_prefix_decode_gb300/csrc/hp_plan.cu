@@ -105,8 +105,11 @@ double schedule(HostPlan &P, int grid, int n_tc_ctas, bool mixed, int d, const C
             // an E4M3 chunk is half the bytes, but decoding its codes costs the
             // consumers about as long as a bf16 chunk takes to stream (ncu:
             // the E4M3 role executes twice the instructions per key):
-            // modelled at the bf16 rate per key
-            P.jobs_sm.push_back({cm.small(w, d, nh, 4), (int32_t)j, false,
+            // modelled at the bf16 rate per key when the item is consumed two
+            // chunks per pass, at 1.5 times that rate chunk by chunk (timed
+            // on the benchmarked shape with E4M3 suffixes and on CodeLlama-13b)
+            const bool paired = ceil_div(w.k1_model - w.k0, (int64_t)kChunk) >= kPairChunks;
+            P.jobs_sm.push_back({cm.small(w, d, nh, P.q8 && !paired ? 6 : 4), (int32_t)j, false,
                                  (int64_t)sizeof(RecItem) + 4 * item_pages(w, P.level_ps[w.level])});
         }
         P.jobs_all = P.jobs_tc;

@@ -81,10 +81,6 @@ struct StageMeta {
     int oob;     // rows stages: bit c set when chunk c's page id was out of range
 };
 
-// Items of at least this many chunks are consumed two chunks per pass by the
-// E4M3 consumers (more independent work per warp); shorter ones one by one,
-// where waiting for a second stage costs more than the overlap gains.
-constexpr int kPairChunks = 12;
 
 template <int N>
 struct Int {
