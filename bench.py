@@ -71,6 +71,8 @@ def parse_args():
     ap.add_argument("--loop-steps", type=int, default=64,
                     help="decode-loop measurement: steps per input set in one graph (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--parallel-prompting-only", action="store_true",
+                    help="print only the Parallel Prompting figure (extras.parallel_prompting) as one JSON line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
@@ -469,6 +471,11 @@ def main():
     K = args.steps
     stream = torch.cuda.Stream(device=dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
+    if args.parallel_prompting_only:
+        pp = parallel_prompting_figure(hb, dev, stream, peaks, dist)
+        if rank == 0:
+            print(json.dumps({"parallel_prompting": pp, "device": props.name}))
+        return
 
     def make_sets(name, part, seed0, n_sets=0, device=None, e4m3=False):
         """Input sets of one workload (R of them: R x working set >= 3x L2,

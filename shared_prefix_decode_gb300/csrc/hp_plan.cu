@@ -693,7 +693,15 @@ hp_status build_plan(const hp_tree_desc *d, HostPlan &P, bool encode, int capaci
         const int64_t per = std::max<int64_t>(1, ceil_div(tc_tiles, std::max(1, n_tc_ctas)));
         tc_split = kTcTile * std::min(kMaxTcTiles, per);
         const int n_sm = std::max(1, sms - (n_tc_ctas < sms ? n_tc_ctas : 0));
-        small_split = kChunk * std::max<int64_t>(2, ceil_div(small_chunks, (int64_t)n_sm));
+        // E4M3 paged items are bound by their consumers, not by HBM: with
+        // long per-CTA work, four items per CTA spread it evenly (an item
+        // per CTA leaves some CTAs two and others one when the nodes do not
+        // divide by the CTAs; per-sequence-only workload 224.0 against
+        // 254.5 us); with short work the extra items cost more than they
+        // balance (benchmarked step with E4M3 suffixes: 21.6 against 19.8)
+        const int64_t per_cta = ceil_div(small_chunks, (int64_t)n_sm);
+        const int64_t parts = P.q8 && per_cta >= 64 ? 4 : 1;
+        small_split = kChunk * std::max<int64_t>(2, ceil_div(small_chunks, (int64_t)n_sm * parts));
     };
     int best_k = sms;
     bool best_mixed = false;
