@@ -1,14 +1,13 @@
 // hp_ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers with bounded
 // waits, TMA tensor copies, tcgen05 (TMEM allocation, MMA, commit, TMEM
 // loads/stores), ldmatrix, the m16n8k16 bf16 and f16 MMAs, cp.async with
-// mbarrier tracking.  Written from the public PTX ISA description of each
-// instruction; E4M3 -> f16 conversion through cuda_fp8.h.
+// mbarrier tracking, movmatrix.  Written from the public PTX ISA description
+// of each instruction.
 #pragma once
 
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include "hp_internal.h"
 
@@ -378,14 +377,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
                  "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
                  : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Two E4M3 codes (bits 0-7 and 8-15) -> two f16 values (low half from the
-// low byte).  Every E4M3 value is exact in f16.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
-{
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
