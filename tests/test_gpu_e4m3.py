@@ -152,3 +152,21 @@ def test_e4m3_cascade_equals_e4m3_paged_decode():
     torch.cuda.synchronize()
     assert (oc - on).abs().max().item() <= O_MAX
     assert (lc - ln).abs().max().item() <= LSE_ABS
+
+
+def test_e4m3_per_sequence_workload_full_size_sampled_rows():
+    """The per-sequence-only workload at full size (B=64, 32 heads, 2048
+    tokens each) in E4M3, where the planner splits the consumer-bound paged
+    work into about four items per CTA: 96 sampled rows against the oracle."""
+    wl = W.with_e4m3_levels(W.make_config("no_sharing", seed=2))
+    wg = wl.to(DEV)
+    plan = hb.CascadePlan.from_workload(wg)
+    assert plan.info.n_small_items >= 4 * 152 * 0.9
+    out, lse = plan.decode(wg.q, wl.scale, out_dtype=torch.float32)
+    _status_ok(plan.ws)
+    g = torch.Generator().manual_seed(4)
+    flat = torch.randperm(wl.B * wl.Hq, generator=g)[:96].tolist()
+    O, L = oracle.cascade(wl, rows=[(f // wl.Hq, f % wl.Hq) for f in flat])
+    o = out.double().cpu().numpy().reshape(wl.B * wl.Hq, wl.d)[flat]
+    l = lse.double().cpu().numpy().reshape(wl.B * wl.Hq)[flat]
+    _check(torch.from_numpy(o), torch.from_numpy(l), O, L, "e4m3 no_sharing full size")

@@ -89,6 +89,21 @@ def test_stream_decode_d64_pages_and_early_steps(T, page_size):
     _check(out, lse, O, L, f"d64 T {T} page {page_size}")
 
 
+@pytest.mark.parametrize("P,Hkv", [(64, 1), (64, 2), (32, 4), (16, 8)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_stream_decode_every_stage_shape(P, Hkv, d):
+    """Every (chunks per stage, heads per item) form the planner picks (MHA,
+    16 streams per consumer warp): 64 streams over 1 or 2 KV heads give
+    items of 1 or 2 heads and four chunks per stage, 32 streams over 4 heads
+    items of 4 heads and two chunks, 16 streams over 8 heads items of 8
+    heads and one chunk; at d = 64 and d = 128."""
+    req = W.stream_requests(R=2, P=P, Hq=Hkv, Hkv=Hkv, d=d, doc_len=300, q_len_range=(5, 40), T=3,
+                            seed=20 + Hkv + d)
+    rows, out, lse = _run(req, seed=Hkv)
+    O, L = _oracle_rows(req, rows)
+    _check(out, lse, O, L, f"Hkv {Hkv} d {d}")
+
+
 def test_stream_decode_prefill_positions():
     """Queries that are not the newest token of their stream (earlier
     positions): the causal half of the mask hides the stream's later tokens."""

@@ -565,3 +565,18 @@ def test_host_workspace_bytes():
     info.d = 96
     assert hb.library().hp_cascade_host_workspace_bytes(ctypes.byref(info)) == 0
     assert hb.library().hp_cascade_host_workspace_bytes(None) == 0
+
+
+def test_e4m3_paged_work_split_into_about_four_items_per_cta():
+    """The per-sequence-only workload (B=64, 32 heads, 2048 tokens each):
+    bf16 paged items are about one per CTA (HBM-bound, fewer partial states),
+    E4M3 ones about four per CTA (consumer-bound, spread evenly); a short
+    E4M3 workload keeps one per CTA."""
+    bf = W.make_config("no_sharing", seed=2)
+    q8 = W.with_e4m3_levels(bf)
+    _, n_bf, _, _ = hb.hp_cascade_plan_stats(hb._levels_of(bf), bf.B, bf.Hq, bf.Hkv, bf.d)
+    _, n_q8, _, _ = hb.hp_cascade_plan_stats(hb._levels_of(q8), q8.B, q8.Hq, q8.Hkv, q8.d)
+    assert n_bf == 256 and 4 * 152 * 0.9 <= n_q8 <= 4 * 152 * 1.4
+    short = W.with_e4m3_levels(W.make_config("no_sharing", seed=2, B=16, prefix=400))
+    _, n_short, _, _ = hb.hp_cascade_plan_stats(hb._levels_of(short), short.B, short.Hq, short.Hkv, short.d)
+    assert n_short <= 2 * 152
