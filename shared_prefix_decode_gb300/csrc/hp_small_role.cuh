@@ -33,11 +33,13 @@
 // stage holds the 16-token chunk's codes (one box of 16 tokens x 128 bytes x
 // nh heads per K and per V) and the chunk's scales, which the producer copies
 // with cp.async tracked by the stage's barrier.  The consumers decode codes
-// to f16 in registers with integer bit operations (exact, up to a power of
-// two) and use the f16 MMA: the queries are rounded from bf16 to f16 once per
-// item (exact for |q| in f16's normal range), scores are scaled by the
-// chunk's K scale, and P is weighted by the chunk's V scale before it is
-// rounded to f16 for P V.  The fragment layouts are in consumer_q8.
+// to f16 in registers, exactly: K codes with integer bit operations (up to a
+// power of two), V codes with the hardware conversion (the two spread the
+// work over two pipes), and use the f16 MMA: the queries are rounded from
+// bf16 to f16 once per item (exact for |q| in f16's normal range), scores
+// are scaled by the chunk's K scale, and P is weighted by the chunk's V
+// scale before it is rounded to f16 for P V.  The fragment layouts are in
+// consumer_q8.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -488,6 +490,14 @@ __device__ __forceinline__ void consumer(const Ctx &c, const Args &a, int w, int
 // factor 2^-8) and the 3 mantissa bits on top of f16's mantissa; subnormal
 // codes (exponent 0) land on f16 subnormals with the same factor.  Integer
 // ALU operations only.
+// Two E4M3 codes (bits 0-7 and 8-15) -> two f16 values, exact (low half
+// from the low byte), by the hardware conversion.
+__device__ __forceinline__ uint32_t e4m3x2_cvt(uint32_t two_codes)
+{
+    uint32_t r;
+    asm("{.reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t;}" : "=r"(r) : "r"(two_codes));
+    return r;
+}
 __device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t &lo, uint32_t &hi)
 {
     hi = (x & 0x80008000u) | ((x >> 1) & 0x3F803F80u);
@@ -495,8 +505,9 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t &lo, uint32_t
 }
 
 // E4M3 consumer warp w (0 <= w < nh), d = 128: as `consumer`, with codes
-// decoded to f16 in registers (values x 2^-8; the factor 2^8 is put back
-// into the K scale of the scores and into the final normalisation) and the
+// decoded to f16 in registers (K codes as values x 2^-8 by integer
+// operations, the factor 2^8 put back into the K scale of the scores; V
+// codes as their values by the hardware conversion) and the
 // operands of both products swapped so that the keys fill the MMA's 16 rows
 // and the head's query rows its 8 columns: with up to 8 query rows (G <= 8,
 // one sequence) a chunk costs 16 MMAs instead of 32; 9..16 rows take a
@@ -510,12 +521,14 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t &lo, uint32_t
 //     g + 8 each): maxima and sums are warp reductions over those lanes.
 //   - O'^T = V^T P^T: P^T's B fragments are the f16 score tiles transposed
 //     with movmatrix; V^T's A fragments pair the codes of keys (2t, 2t+1)
-//     and (2t+8, 2t+9) of thread (g, t)'s columns 16g .. 16g+15, m-tile j
+//     and (2t+8, 2t+9) (byte permutes put the two keys' codes of a column
+//     side by side for the conversion) of thread (g, t)'s columns
+//     16g .. 16g+15, m-tile j
 //     taking columns 16g + 2j and 16g + 2j + 1, so thread (g, t) ends with
 //     columns 16g .. 16g+15 of query rows 2t and 2t+1 (of each column tile).
 //   - The V scale of a chunk enters as P * (vsc / vref), vref being the first
 //     nonzero V scale of the item, so P stays near [0, 1] when it is rounded
-//     to f16 and O' needs no rescaling between chunks; O = O' vref 2^8 / l.
+//     to f16 and O' needs no rescaling between chunks; O = O' vref / l.
 //     A chunk whose V scale is 0 adds nothing to O (its weights still count
 //     in the denominator).
 template <int D, int NC, int S, int QR>
@@ -526,7 +539,7 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
     static_assert(S >= 2, "two stages held at once");
     constexpr int kKs = D / 16;  // k-steps of S^T = K Q^T
     constexpr int kMt = D / 16;  // m16 tiles of O^T
-    constexpr float kDecode = 256.f;  // decoded code = value * 2^-8
+    constexpr float kDecode = 256.f;  // a K code decoded by integer operations = value * 2^-8
     auto wait_warp = [&](uint32_t b, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, c.status, c.abort)) != 0;
     };
@@ -702,10 +715,16 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
                 const uint32_t A = word(vw[u][0]), B = word(vw[u][1]), C = word(vw[u][2]), E = word(vw[u][3]);
                 // m-tiles 2q4 and 2q4+1: columns 16g + 4q4 + (0, 1) and (2, 3)
                 uint32_t a0[4], a1[4];
-                e4m3x4_to_f16(__byte_perm(A, B, 0x5410), a0[0], a0[1]);
-                e4m3x4_to_f16(__byte_perm(C, E, 0x5410), a0[2], a0[3]);
-                e4m3x4_to_f16(__byte_perm(A, B, 0x7632), a1[0], a1[1]);
-                e4m3x4_to_f16(__byte_perm(C, E, 0x7632), a1[2], a1[3]);
+                const uint32_t ab0 = __byte_perm(A, B, 0x5140), ce0 = __byte_perm(C, E, 0x5140);
+                const uint32_t ab1 = __byte_perm(A, B, 0x7362), ce1 = __byte_perm(C, E, 0x7362);
+                a0[0] = e4m3x2_cvt(ab0);
+                a0[1] = e4m3x2_cvt(ab0 >> 16);
+                a0[2] = e4m3x2_cvt(ce0);
+                a0[3] = e4m3x2_cvt(ce0 >> 16);
+                a1[0] = e4m3x2_cvt(ab1);
+                a1[1] = e4m3x2_cvt(ab1 >> 16);
+                a1[2] = e4m3x2_cvt(ce1);
+                a1[3] = e4m3x2_cvt(ce1 >> 16);
                 mma_f16_16816(o[2 * q4][0], a0, pb[u][0][0], pb[u][0][1]);
                 mma_f16_16816(o[2 * q4 + 1][0], a1, pb[u][0][0], pb[u][0][1]);
                 if (two) {
@@ -803,7 +822,7 @@ __device__ __forceinline__ void consumer_q8(const Ctx &c, const Args &a, int w, 
                     const int r = nt * 8 + 2 * t + i;
                     if (r >= rows)
                         continue;
-                    const float inv = Lq[i] > 0.f ? vref * kDecode / Lq[i] : 0.f;
+                    const float inv = Lq[i] > 0.f ? vref / Lq[i] : 0.f;
                     // columns 16g + 2j (element i) and 16g + 2j + 1 (element 2 + i) of m-tile j
                     uint32_t pk[8];
 #pragma unroll
