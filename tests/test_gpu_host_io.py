@@ -28,7 +28,8 @@ def _host_bufs(wl, out_dtype=torch.bfloat16):
 
 
 @pytest.mark.parametrize("name,kw", [("llama3_8b", dict(B=16, prefix=512)), ("tree2", dict(B=32, prefix=256)),
-                                     ("codellama13b", dict(B=32, prefix=384)), ("no_sharing", dict(B=4, prefix=100))])
+                                     ("codellama13b", dict(B=32, prefix=384)), ("no_sharing", dict(B=4, prefix=100)),
+                                     ("tiny", {}), ("doc_streams", dict(B=24, prefix=640))])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_host_step_equals_device_step_and_oracle(name, kw, out_dtype):
     wl = W.make_config(name, seed=2, **kw)
@@ -97,7 +98,7 @@ def test_host_steps_in_one_graph():
 
 
 def _raw_call(plan, q_ptr, out_ptr, lse_ptr, ws, ws_bytes=None, q_sb=None):
-    wl_b, hq, d = plan.B, plan.Hq, plan.d
+    hq, d = plan.Hq, plan.d
     return hb.library().hp_cascade_decode_host(
         plan.plan.data_ptr(), ctypes.byref(plan.info), q_ptr, hq * d if q_sb is None else q_sb, d,
         ctypes.c_float(0.088), out_ptr, hb.HP_BF16, hq * d, d, lse_ptr, hq, ws.data_ptr(),
