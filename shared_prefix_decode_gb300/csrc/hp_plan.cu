@@ -23,8 +23,11 @@ namespace {
 // first chunks, then each item streams its KV.
 struct CostModel {
     // ns; a tensor-core tile costs tc_tile with two 128-row blocks, tc_tile1
-    // with one (timelines: about 2.1-2.5 us and 1.85 us at d = 128)
-    double cta = 1500, tc_item = 6000, tc_tile = 2300, tc_tile1 = 1850, sm_start = 1000, sm_item = 200,
+    // with one (timelines: about 2.1-2.5 us and 1.85 us at d = 128; 2.6 us
+    // gave the shortest steps over 2.0-3.3 us on the workloads with many
+    // tiles per CTA: document + streams 165.4 against 167.9 us at 2.3,
+    // CodeLlama-13b with E4M3 suffixes 227.6 against 236.1)
+    double cta = 1500, tc_item = 6000, tc_tile = 2600, tc_tile1 = 1850, sm_start = 1000, sm_item = 200,
            sm_bytes_per_ns = 60;
     double tc(const WorkItem &w, int G, int d) const
     {
